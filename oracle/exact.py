@@ -1,0 +1,136 @@
+"""Exact (rational-arithmetic) laws of speculative sampling on tiny vocabularies.
+
+TEST INFRASTRUCTURE ONLY (same rule as the rest of ``oracle/``).
+
+This module states the stochastic acceptance rule of zero-to-sglang ch.10
+"Speculative decoding (code walk-through)", section 5.1 -- a draft y drawn
+from q is accepted with probability min(1, p[y]/q[y]); on rejection the token
+is drawn from the normalised positive residual (p - q)+; after full acceptance
+the bonus is drawn from p -- with ``fractions.Fraction`` so that laws come out
+exactly.  It is used to pin the C oracle: the pages' worked example (p = [0.4,
+0.6], q = [0.8, 0.2] gives exactly 0.4 / 0.6, and resampling from p instead
+gives 0.56 / 0.44), and the losslessness claim of the same section (the law of
+the committed tokens equals the target's own autoregressive law) for chains
+and for trees whose children are i.i.d. draws from q, tried sibling by sibling
+against the updated residual.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+from typing import Callable, Dict, Sequence, Tuple
+
+Dist = Tuple[Fraction, ...]
+Law = Dict[Tuple[int, ...], Fraction]
+
+
+def normalise(w: Sequence[Fraction]) -> Dist:
+    s = sum(w)
+    return tuple(x / s for x in w)
+
+
+def positive_residual(p: Dist, q: Dist) -> Dist:
+    """(p - q)+ normalised (section 5.1).  Only called after a rejection,
+    where the residual has positive mass."""
+    r = [max(Fraction(0), a - b) for a, b in zip(p, q)]
+    return normalise(r)
+
+
+def one_draft_law(p: Dist, q: Dist, on_reject: str = "residual") -> Dist:
+    """Law of the token output by one draft y ~ q verified against p.
+    on_reject='residual' is the rule of section 5.1; 'p' resamples from p,
+    the mistake the same section warns about."""
+    out = [Fraction(0)] * len(p)
+    reject_mass = Fraction(0)
+    for y, qy in enumerate(q):
+        if qy == 0:
+            continue
+        a = min(Fraction(1), p[y] / qy)
+        out[y] += qy * a
+        reject_mass += qy * (1 - a)
+    if reject_mass > 0:
+        r = positive_residual(p, q) if on_reject == "residual" else p
+        for v in range(len(p)):
+            out[v] += reject_mass * r[v]
+    return tuple(out)
+
+
+def acceptance_masses(p: Dist, q: Dist) -> Tuple[Fraction, Fraction]:
+    """(sum_v min(p, q), sum_v (p - q)+): the mass the acceptance branch
+    contributes and the mass the rejection branch must supply."""
+    acc = sum(min(a, b) for a, b in zip(p, q))
+    rej = sum(max(Fraction(0), a - b) for a, b in zip(p, q))
+    return acc, rej
+
+
+class ToyModels:
+    """A target p(.|context) and a draft q(.|context) over a tiny vocabulary,
+    given as exact distributions by two callables on token tuples."""
+
+    def __init__(self, V: int, target: Callable[[Tuple[int, ...]], Dist],
+                 draft: Callable[[Tuple[int, ...]], Dist]):
+        self.V, self.p, self.q = V, target, draft
+
+
+def _add(law: Law, seq: Tuple[int, ...], pr: Fraction) -> None:
+    if pr:
+        law[seq] = law.get(seq, Fraction(0)) + pr
+
+
+def round_law(m: ToyModels, ctx: Tuple[int, ...], width: int, depth: int) -> Law:
+    """Law of the tokens committed in one verification round when every tree
+    node has ``width`` children drawn i.i.d. from q(.|node context) down to
+    ``depth`` levels (width 1 = a chain of ``depth`` drafts).  Children are
+    tried in sibling order against p_cur, which each rejection replaces with
+    the positive residual; with no child accepted the token is drawn from
+    p_cur; at a leaf the bonus is drawn from p."""
+
+    def node(c: Tuple[int, ...], d: int) -> Law:
+        return siblings(c, m.p(c), width if d > 0 else 0, d)
+
+    def siblings(c: Tuple[int, ...], pc: Dist, left: int, d: int) -> Law:
+        law: Law = {}
+        if left == 0:
+            for t, pt in enumerate(pc):
+                _add(law, (t,), pt)
+            return law
+        qd = m.q(c)
+        for y, qy in enumerate(qd):
+            if qy == 0:
+                continue
+            a = min(Fraction(1), pc[y] / qy)
+            if a > 0:
+                for seq, pr in node(c + (y,), d - 1).items():
+                    _add(law, (y,) + seq, qy * a * pr)
+            if a < 1:
+                r = positive_residual(pc, qd)
+                for seq, pr in siblings(c, r, left - 1, d).items():
+                    _add(law, seq, qy * (1 - a) * pr)
+        return law
+
+    return node(ctx, depth)
+
+
+def spec_law(m: ToyModels, ctx: Tuple[int, ...], M: int, width: int, depth: int) -> Law:
+    """Law of the first M committed tokens over as many rounds as needed."""
+    if M <= 0:
+        return {(): Fraction(1)}
+    law: Law = {}
+    for seq, pr in round_law(m, ctx, width, depth).items():
+        if len(seq) >= M:
+            _add(law, seq[:M], pr)
+        else:
+            for rest, pr2 in spec_law(m, ctx + seq, M - len(seq), width, depth).items():
+                _add(law, seq + rest, pr * pr2)
+    return law
+
+
+def target_law(m: ToyModels, ctx: Tuple[int, ...], M: int) -> Law:
+    """Autoregressive law of M tokens sampled from the target alone."""
+    law: Law = {(): Fraction(1)}
+    for _ in range(M):
+        nxt: Law = {}
+        for seq, pr in law.items():
+            for t, pt in enumerate(m.p(ctx + seq)):
+                _add(nxt, seq + (t,), pr * pt)
+        law = nxt
+    return law
