@@ -1,0 +1,416 @@
+"""Benchmark: one whole speculative step (draft steps, tree build, batched
+verify, KV compaction) over a batch of synthetic logits, on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c3] [--mode sample]
+                  [--impl ours|reference]
+
+Prints one JSON line (rank 0).  The default workload is the EAGLE tree with
+stochastic verification: B=128 requests, topk 8, 6 draft steps, 64 tree
+nodes, vocabulary 128256, bf16 logits, temperature 0.7, KV compaction over a
+page-16 slot pool with 4096-byte slots.  Inputs (draft logits 1.35 GB,
+target logits 2.1 GB) are larger than L2, so no flush is needed between
+steps.  ``--impl reference`` times the CPU oracle on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, assemble_target, generate  # noqa: E402
+
+METRIC = "verified tokens/s (whole draft + tree + verify + compaction step)"
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT = "softmax_topk_kernel"
+
+
+def describe(cfg, mode):
+    w = (f"{cfg.name}: {cfg.kind} B={cfg.B} topk={cfg.topk} steps={cfg.steps} N={cfg.N} V={cfg.V}"
+         + (f" V_t={cfg.V_t} K={cfg.K}" if cfg.kind == "tli" else "")
+         + f" {str(cfg.dtype).replace('torch.', '')} logits, {mode} verify T={cfg.T}"
+         + (f", KV compaction page {cfg.page_size} x {cfg.bytes_per_slot} B slots" if cfg.page_size else ""))
+    return w
+
+
+def default_mode(cfg):
+    return cfg.modes[-1]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_draft_select_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args, cfg, mode, rank, world):
+    import speculative_decoding_draft_select_gb300 as sd
+    from speculative_decoding_draft_select_gb300 import pipeline as pl
+    from speculative_decoding_draft_select_gb300.build import build
+
+    build()
+    sd.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if world > 1:  # weak scaling: every rank verifies its own batch
+        cfg = cfg.scaled(seed=cfg.seed + 7919 * rank)
+    work = generate(cfg, dev)
+    compact = bool(cfg.page_size)
+    sampled = cfg.kind == "chain" and mode == "sample"
+    buf = pl.StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, dev, want_q=(mode == "sample"),
+                         sampled=sampled, V_t=cfg.V_t or None, page_size=cfg.page_size)
+    eos = int(work["eos_id"])
+    kv = work.get("kv_pool")
+    # the target model's output for this tree (deterministic draft -> same tree every step)
+    pl.run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], draft_u=work["draft_u"],
+                 d2t=work.get("d2t"), t2d=work.get("t2d"))
+    target = assemble_target(work, buf.tree["q_row"]).contiguous()
+    Vq = cfg.V_t if cfg.kind == "tli" else cfg.V
+    row_bytes = cfg.V * (2 if cfg.dtype == torch.bfloat16 else 4)
+
+    stream = torch.cuda.current_stream()
+    dom_events = []
+
+    def step(record):
+        # draft side, with events around each big draft-step kernel
+        k = cfg.topk
+        for s in range(cfg.steps):
+            r = cfg.B * (1 if s == 0 else k)
+            a = buf.offs[s]
+            rows = work["draft_table"][a:a + r]
+            qs = buf.q[a:a + r] if buf.q is not None else None
+            ev = None
+            if record and s >= 1 and cfg.kind != "tli":
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(stream)
+            if cfg.kind == "tli":
+                if record and s >= 1:
+                    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    ev[0].record(stream)
+                sd.tli_constrain_map(rows, work["d2t"], cfg.T, t2d=work["t2d"], top1_draft=buf.top1_draft[a:a + r],
+                                     top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
+                                     stats=buf.stats)
+                if ev:
+                    ev[1].record(stream)
+                sd.spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
+            elif sampled:
+                sd.spec_softmax_topk(rows, cfg.T, 1, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
+                                     stats=buf.stats)
+                if ev:
+                    ev[1].record(stream)
+                sd.spec_sample(work["draft_u"][a:a + r], probs=qs, out_token=buf.tok[a:a + r],
+                               out_prob=buf.prob[a:a + r], stats=buf.stats)
+                sd.spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
+            else:
+                sd.spec_softmax_topk(rows, cfg.T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
+                                     stats=buf.stats)
+                if ev:
+                    ev[1].record(stream)
+                sd.spec_tree_expand(buf.pool, s, buf.topk_p[s], buf.topk_idx[s])
+            if ev:
+                dom_events.append((ev, r))
+        sd.spec_build_tree(buf.pool, cfg.N, work["root_token"], work["seq_lens"], out=buf.tree)
+        pl.run_verify(buf, target, mode, cfg.T, work["coins"], work["u_final"], work.get("budget"), eos)
+        if compact:
+            pl.run_compact(buf, work["seq_lens"], work["req_to_token"], cfg.page_size, kv_pool=kv)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    committed = 0
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(True)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    committed = int(buf.verify_out["num_committed"].sum().item())
+    accept = float(buf.verify_out["accept_length"].float().mean().item())
+    dom_ms = [ev[0].elapsed_time(ev[1]) for ev, _ in dom_events]
+    dom_rows = [r for _, r in dom_events]
+
+    # max over ranks
+    t_total = torch.tensor([total_ms, committed * args.steps], dtype=torch.float64, device=dev)
+    if world > 1:
+        mx = t_total.clone()
+        torch.distributed.all_reduce(mx[:1], op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(t_total[1:], op=torch.distributed.ReduceOp.SUM)
+        t_total[0] = mx[0]
+    total_ms_max = float(t_total[0].item())
+    tokens_all = float(t_total[1].item())
+    value = tokens_all / (total_ms_max / 1e3)
+
+    # dominant kernel: the draft-step softmax/top-k (or TLI constrain) launches
+    if cfg.kind == "tli":
+        per_row = cfg.V * 2 + (cfg.V_t * 4 if mode == "sample" else 0)
+        kname = "tli_constrain_kernel"
+    else:
+        per_row = row_bytes + (cfg.V * 4 if buf.q is not None else 0)
+        kname = DOMINANT
+    dom_avg_ms = statistics.mean(dom_ms) if dom_ms else None
+    dom_bytes = per_row * statistics.mean(dom_rows) if dom_rows else None
+    peak, peak_kind = hbm_peak()
+    achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9 if dom_ms else None
+    roofline = None
+    if achieved:
+        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                    "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "bytes_per_launch": int(dom_bytes), "avg_launch_us": round(dom_avg_ms * 1e3, 2),
+                    "traffic": ncu_traffic(kname, cfg.name)}
+
+    # e2e: host buffers through the same API, copies inside the timed region
+    e2e = run_e2e(args, cfg, mode, work, buf, target, step, compact) if not args.no_e2e else None
+
+    launches = pl.kernels_per_step(buf, mode, compact, kv is not None) * args.steps
+    clocks = clk.summary()
+    ms_per_step = total_ms_max / args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "input_dtype": str(cfg.dtype).replace("torch.", ""),
+        "data": "synthetic (seeded; shapes and value distributions of the workload, no model weights)",
+        "config": {"workload": describe(cfg, mode), "B": cfg.B, "topk": cfg.topk, "num_steps": cfg.steps,
+                   "N": cfg.N, "V": cfg.V, "mode": mode, "T": cfg.T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (draft + target logits), no flush"},
+        "us_per_step_median": round(statistics.median(step_ms) * 1e3, 2),
+        "verified_tokens_per_step": committed, "mean_accept_length": round(accept, 3),
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "stats": buf.stats.cpu().tolist(),
+    }
+    return line, work
+
+
+def run_e2e(args, cfg, mode, work, buf, target, step_fn, compact):
+    """Per step: pinned-host -> device copies of the step's inputs, the step,
+    device -> host copy of its results."""
+    inputs = {"draft_table": work["draft_table"], "target": target, "coins": work["coins"],
+              "u_final": work["u_final"], "root_token": work["root_token"], "seq_lens": work["seq_lens"]}
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inputs.items()}
+    for k, v in inputs.items():
+        host[k].copy_(v)
+    outs = {"committed": buf.verify_out["committed"], "num_committed": buf.verify_out["num_committed"],
+            "accept_length": buf.verify_out["accept_length"], "next_root": buf.verify_out["next_root"]}
+    if compact:
+        outs.update({"new_kv_len": buf.compact_out["new_kv_len"], "num_freed": buf.compact_out["num_freed"],
+                     "freed": buf.compact_out["freed"]})
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    n = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    tokens = 0
+    for _ in range(n):
+        for k, v in inputs.items():
+            v.copy_(host[k], non_blocking=True)
+        step_fn(False)
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+        torch.cuda.synchronize()
+        tokens += int(host_out["num_committed"].sum())
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(dt / n * 1e3, 3)}
+
+
+# ---------------------------------------------------------------- reference
+
+
+def oracle_sample(cfg, mode, work, budget_s):
+    """The CPU oracle, single-threaded, on as many requests as fit in
+    ``budget_s`` seconds of oracle time (at least one)."""
+    from oracle.pipeline import fetch_request, run_request
+
+    tokens, secs, reqs = 0, 0.0, 0
+    for b in range(cfg.B):
+        d = fetch_request(cfg, work, b)
+        t0 = time.perf_counter()
+        _, _, _, v, _ = run_request(cfg, d, mode, compact=bool(cfg.page_size))
+        secs += time.perf_counter() - t0
+        tokens += int(v["num_committed"][0])
+        reqs += 1
+        if secs >= budget_s:
+            break
+    return tokens, secs, reqs
+
+
+def cpu_baseline(cfg, mode, work, budget_s=15.0):
+    tokens, secs, reqs = oracle_sample(cfg, mode, work, budget_s)
+    return {"value": round(tokens / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reqs} of {cfg.B} requests of {cfg.name}, one at a time (full draft, tree, verify"
+                      f"{', compaction index work' if cfg.page_size else ''}); {tokens} tokens in {secs:.2f} s"}
+
+
+def run_reference(args, cfg, mode, rank):
+    if rank != 0:
+        return None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    work = generate(cfg.scaled(bytes_per_slot=0), dev)
+    per_step_budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(cfg, mode, work, per_step_budget / 4)
+    tok, sec = 0, 0.0
+    reqs = 0
+    for _ in range(args.steps):
+        t, s, r = oracle_sample(cfg, mode, work, per_step_budget)
+        tok, sec, reqs = tok + t, sec + s, reqs + r
+    value = tok / sec
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; same generator as the GPU arm)",
+        "config": {"workload": describe(cfg, mode), "B": cfg.B, "mode": mode},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{reqs} requests over {args.steps} steps, one at a time, fp64 C oracle"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="c3", choices=sorted(CONFIGS))
+    ap.add_argument("--mode", default=None, choices=[None, "greedy", "sample"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = CONFIGS[args.config]
+    mode = args.mode or default_mode(cfg)
+
+    if args.impl == "reference":
+        line = run_reference(args, cfg, mode, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line, work = run_ours(args, cfg, mode, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(cfg, mode, work)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

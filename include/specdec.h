@@ -1,0 +1,301 @@
+/*
+ * specdec.h -- C ABI of the GB300 (sm_103a) speculative-decoding draft/verify
+ * library (libspecdec.so).
+ *
+ * The path: per-step draft softmax and top-k, expansion of the top-k into a
+ * candidate tree, tree build (mask, positions, retrieve links), one batched
+ * verification pass over the target logits of every tree node (greedy
+ * first-rejection commit with bonus token, or stochastic acceptance with the
+ * positive residual), accepted-path KV-slot compaction, and the TLI
+ * heterogeneous-vocabulary constraint and id remapping.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [HB]  ai-infra-handbooks, "EAGLE speculative decoding in four parts: why
+ *         it became a worker" -- "Drafting, verification and slots".
+ *   [ML]  secrett2633 blog, "[SGLang] Multi-Layer EAGLE" -- section 2
+ *         (select_top_k_tokens, tree_info) and section 3 (softmax, fast_topk).
+ *   [ZS]  zero-to-sglang ch.10 "Speculative decoding (code walk-through)" --
+ *         3.2 drafting and EOS, 3.3 row alignment, 4.1 greedy commitment,
+ *         5.1 stochastic acceptance and residual, 5.2 verify input and KV.
+ *   [TLI] SGLang PR #22883 "TLI (Token-Level Intersection)" -- Modifications.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer is a DEVICE pointer owned by the caller, unless a comment
+ *     says otherwise.  The library allocates nothing.  Calls that need
+ *     scratch take (ws, ws_bytes), sized by the matching *_ws_size call.
+ *   - Work is enqueued asynchronously on the caller's stream (0 = legacy
+ *     default stream).  No call synchronises the device.
+ *   - Requests b in [0,B); tree nodes n in [0,N); node 0 is the root (the
+ *     last committed token).  Logit rows are row-major and contiguous:
+ *     target logits [B, N, V], row (b, n) = the target's next-token logits
+ *     after the path root..n, which verifies n's children and, at a leaf,
+ *     gives the bonus ([ZS] 3.3: row L-1+i verifies draft i).
+ *   - dtype: SPEC_F32 or SPEC_BF16 for logit buffers.  Ids are int32;
+ *     probabilities are fp32.  NaN logits are treated as -inf; ties in
+ *     argmax / top-k go to the lowest index.
+ *   - Random numbers are inputs (uniforms in [0,1)), so results are
+ *     deterministic: no float atomics, fixed reduction orders.
+ *   - Return value: SPEC_OK, or a negative SPEC_ERR_* code.  Arguments are
+ *     checked on the host before anything is enqueued; a failed check
+ *     enqueues nothing.  Data-dependent anomalies are not errors: they are
+ *     counted in the optional stats array (int32[SPEC_NUM_STATS], device,
+ *     incremented with integer atomics; the caller zeroes it).
+ */
+#ifndef SPECDEC_H
+#define SPECDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* spec_stream_t; /* same object as cudaStream_t */
+
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG (-1)  /* null pointer, bad size or shape, bad option */
+#define SPEC_ERR_UNSUPPORTED (-2)  /* dtype, alignment or size beyond a stated limit */
+#define SPEC_ERR_CUDA (-3)         /* a launch failed (cudaGetLastError) */
+#define SPEC_ERR_WORKSPACE (-4)    /* ws_bytes below the *_ws_size value */
+
+#define SPEC_F32 0
+#define SPEC_BF16 1
+
+/* stats[] slots */
+#define SPEC_STAT_NONFINITE_ROW 0     /* a row whose maximum is not finite */
+#define SPEC_STAT_Q_ZERO 1            /* accept test met q[y] == 0 */
+#define SPEC_STAT_RESIDUAL_FALLBACK 2 /* residual had no positive mass; p_cur kept */
+#define SPEC_STAT_CDF_FALLBACK 3      /* inverse CDF found no crossing; last positive taken */
+#define SPEC_STAT_EMPTY_INTERSECTION 4/* TLI row with no finite intersection logit */
+#define SPEC_STAT_BAD_REQUEST 5       /* compaction input out of range; request skipped */
+#define SPEC_NUM_STATS 8
+
+/* Limits (checked on the host; SPEC_ERR_UNSUPPORTED beyond them). */
+#define SPEC_MAX_TOPK 32          /* k of spec_softmax_topk / spec_tree_expand */
+#define SPEC_MAX_POOL 16384       /* candidate-pool size P of spec_build_tree */
+#define SPEC_MAX_NODES 2048       /* tree nodes N per request */
+#define SPEC_MAX_VOCAB (1 << 22)  /* V of every logit row */
+
+/* walk_info[b*3 + 2] values */
+#define SPEC_FINAL_ACCEPTED 0    /* the last committed token is an accepted draft */
+#define SPEC_FINAL_CORRECTION 1  /* drawn after a rejection at the final node */
+#define SPEC_FINAL_BONUS 2       /* drawn at a leaf after full acceptance */
+
+/* ------------------------------------------------------------------ draft */
+
+/* Draft-step softmax and top-k.  [ML] section 3: probs = softmax(logits),
+ * then top-k; [ZS] 5.1: with a temperature, the stored probabilities are the
+ * processed ones.
+ *   logits     [R, V] (dtype), row-major.
+ *   T          temperature > 0; p_v = exp((l_v - max l)/T) / sum_u exp(...).
+ *   k          1 <= k <= min(V, SPEC_MAX_TOPK).
+ *   topk_p     [R, k] fp32 out: probabilities of the top-k tokens.
+ *   topk_idx   [R, k] int32 out: indices by (logit desc, index asc).
+ *   probs_or_null [R, V] fp32 out (optional): the full distribution (the
+ *              draft distribution q that stochastic verify reads).
+ * A row whose maximum is not finite gets zero probabilities and counts in
+ * SPEC_STAT_NONFINITE_ROW. */
+int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
+                      float* topk_p, int32_t* topk_idx, float* probs_or_null,
+                      int32_t* stats_or_null, spec_stream_t stream);
+
+/* Draft sampling with caller uniforms (chain drafts drawn from q; [ZS] 5.1
+ * "a candidate y drawn from the draft distribution q").  One token per row
+ * by inverse CDF over vocabulary order: the smallest v whose inclusive prefix
+ * sum of the row's weights exceeds u[r] times their total.
+ *   probs_or_null  [R, V] fp32 weights; if NULL, weights are
+ *                  exp((l - max l)/T) of logits_or_null [R, V] (dtype).
+ *   u              [R] fp32 uniforms in [0,1).
+ *   out_token      [R] int32 out.
+ *   out_prob_or_null [R] fp32 out: the drawn token's normalised weight.
+ * If rounding leaves no crossing, the last index with positive weight is
+ * taken (SPEC_STAT_CDF_FALLBACK). */
+int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_null, int64_t R,
+                int64_t V, float T, const float* u, int32_t* out_token, float* out_prob_or_null,
+                int32_t* stats_or_null, spec_stream_t stream);
+
+/* Candidate-pool size P = 1 + k + (num_steps - 1) * k * k. */
+int64_t spec_tree_pool_size(int k, int num_steps);
+
+/* One draft step of the tree expansion ([ML] section 2, select_top_k_tokens
+ * with tree_info = (scores, tokens, parents)).
+ *   step 0: topk_p / topk_idx are [B, 1, k] (the root rows).  Initialises
+ *     the pool: id 0 = root (score 1), ids 1..k = the root's children,
+ *     score = topk_p.
+ *   step s >= 1: topk_p / topk_idx are [B, k, k]: row (b, f) belongs to
+ *     frontier slot f.  Child j of frontier node f gets score
+ *     frontier_score[f] * topk_p[f][j] (one fp32 multiply, round to nearest)
+ *     and pool id 1 + k + (s-1)k^2 + f*k + j.
+ *   Every expansion enters the pool; the new frontier is the best k of this
+ *   step's candidates by (score desc, pool id asc), written to
+ *   frontier_score / frontier_id [B, k] (in/out).
+ *   pool_qrow marks each new frontier node with the row of the step-major
+ *   draft-row table that will hold its draft distribution: step 0's rows are
+ *   [0, B) (the roots, row b), step t >= 1's rows are B + (t-1)*B*k +
+ *   b*k + slot.  Not set on the last step.  Candidates never expanded keep -1.
+ *   pool_* are [B, P] (P = spec_tree_pool_size(k, num_steps)).
+ * 1 <= k <= SPEC_MAX_TOPK, 0 <= step < num_steps. */
+int spec_tree_expand(int step, int num_steps, int B, int k, const float* topk_p,
+                     const int32_t* topk_idx, float* pool_score, int32_t* pool_token,
+                     int32_t* pool_parent, int32_t* pool_qrow, float* frontier_score,
+                     int32_t* frontier_id, spec_stream_t stream);
+
+/* Tree build ([HB] "Drafting, verification and slots": build_eagle_tree
+ * produces the attention mask and positions; [ZS] 5.2 lists the verify input
+ * draft_token, positions, custom_mask and retrieve_*).  The N-1 best pool
+ * candidates by (score desc, pool id asc) become nodes 1..N-1 in ascending
+ * pool-id order (parents precede children; siblings in draft-rank order).
+ * Inputs: pool [B, P] from spec_tree_expand, root_token [B], seq_lens [B]
+ * (tokens already in the KV cache; the root sits at position seq_len).
+ * Outputs, all [B, N] int32 unless noted:
+ *   draft_token           token of node n (root_token at n = 0)
+ *   parent                parent node (-1 at the root)
+ *   positions             seq_len + depth(n)
+ *   tree_mask [B, N, N] u8  1 iff column m is n or an ancestor of n
+ *   retrieve_index        b*N + n
+ *   retrieve_next_token   first child of n, -1 if none
+ *   retrieve_next_sibling next node with the same parent, -1 if none
+ *   q_row                 draft-row table row of n's draft distribution, -1
+ * 1 <= N <= min(P, SPEC_MAX_NODES), P <= SPEC_MAX_POOL. */
+int spec_build_tree(int B, int k, int num_steps, int N, const float* pool_score,
+                    const int32_t* pool_token, const int32_t* pool_parent,
+                    const int32_t* pool_qrow, const int32_t* root_token, const int32_t* seq_lens,
+                    int32_t* draft_token, int32_t* parent, int32_t* positions, uint8_t* tree_mask,
+                    int32_t* retrieve_index, int32_t* retrieve_next_token,
+                    int32_t* retrieve_next_sibling, int32_t* q_row, spec_stream_t stream);
+
+/* ----------------------------------------------------------------- verify */
+
+/* Scratch bytes for spec_verify_greedy / spec_verify_sample (per-row
+ * max, normaliser and argmax of the target logits). */
+size_t spec_verify_ws_size(int B, int N);
+
+/* Greedy verify ([ZS] 4.1 greedy_commit, generalised to trees).  One pass
+ * over every target row computes its argmax (lowest index on ties); then per
+ * request, from the root: t = argmax(row n) is committed; a child carrying t
+ * is accepted (its KV is valid); the walk stops when t == eos_id, when the
+ * budget is used, or when no child carries t (t is then the correction, or
+ * the bonus at a leaf); otherwise it descends into the child.
+ *   target_logits [B, N, V] (dtype)
+ *   draft_token, retrieve_next_token, retrieve_next_sibling [B, N] int32
+ *     (as written by spec_build_tree; any tree whose children have larger
+ *     node indices than their parent works)
+ *   budget_or_null [B] remaining output tokens (<= 0: commit nothing);
+ *     NULL = no limit.  eos_id < 0: none.
+ * Outputs: committed [B, N] (-1 padded), num_committed [B], accept_length [B]
+ * (accepted drafts), accept_path [B, N] (node ids from 0, -1 padded),
+ * next_root [B] (last committed token, -1 if none), walk_info_or_null [B, 3]
+ * = (final node, children rejected over the walk, SPEC_FINAL_*).
+ * ws: spec_verify_ws_size(B, N) bytes, 256-byte aligned. */
+int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void* target_logits,
+                       const int32_t* draft_token, const int32_t* retrieve_next_token,
+                       const int32_t* retrieve_next_sibling, const int32_t* budget_or_null,
+                       int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                       int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                       int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                       size_t ws_bytes, spec_stream_t stream);
+
+/* Stochastic verify ([ZS] 5.1).  p_n = softmax(target row n / T).  At node
+ * n the children are tried in sibling order: child c with draft token y is
+ * accepted iff coins[b, c] < p_cur[y] / q_n[y] (acceptance probability
+ * min(1, p/q)); each rejection replaces p_cur by the normalised positive
+ * residual (p_cur - q_n)+ and the next sibling is tried; if no child is
+ * accepted (or n is a leaf) one token is drawn from p_cur by inverse CDF with
+ * u_final[b] (the correction after a rejection, or the bonus from p after
+ * full acceptance).  EOS and budget end the walk after any committed token.
+ * q[y] == 0 accepts iff p_cur[y] > 0.  A residual without positive mass
+ * leaves p_cur unchanged (SPEC_STAT_RESIDUAL_FALLBACK).
+ *   q             draft distributions, fp32 rows of length V.  With
+ *                 q_row_or_null, node n's row is q + q_row[b*N+n]*V (the
+ *                 step-major draft-row table, q_row from spec_build_tree);
+ *                 with NULL, q is [B, N, V] in node order.  Only rows of
+ *                 nodes with children are read.
+ *   coins [B, N]  uniform per child node (index 0 unused); u_final [B].
+ * Other arguments and outputs as spec_verify_greedy. */
+int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                       const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                       const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                       const float* coins, const float* u_final, const int32_t* budget_or_null,
+                       int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                       int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                       int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                       size_t ws_bytes, spec_stream_t stream);
+
+/* ------------------------------------------------------------- compaction */
+
+/* Capacity (entries) the freed list of spec_compact_slots needs. */
+int64_t spec_compact_freed_capacity(int B, int N, int page_size);
+
+/* Accepted-path KV-slot compaction ([HB] "Drafting, verification and
+ * slots": slots for every candidate are allocated before drafting, only the
+ * accepted path's are kept, and with a page size above 1 data must be
+ * copied; [ZS] 5.2: the cache returns to the committed path and the
+ * correction/bonus token has no KV yet).
+ * Layout: tree node n occupies logical position seq_len + n, physical slot
+ * req_to_token[b*max_ctx + seq_len + n]; with page_size P, slot = page*P +
+ * position % P.  Root + accepted nodes stay: new_kv_len = seq_len + 1 +
+ * accept_length.
+ *   page_size == 1: req_to_token[seq_len + i] = old slot of node path[i]
+ *     (i = 1..accept_length); the slots of nodes off the path are freed in
+ *     node order; no moves.
+ *   page_size > 1: for i = 1..accept_length with path[i] != i a move
+ *     (src = slot(seq_len + path[i]), dst = slot(seq_len + i)) is emitted in
+ *     move_src/move_dst [B, N] (num_moves [B]); with kv_pool_or_null
+ *     ([num_slots, bytes_per_slot] bytes) the payload is copied in place
+ *     with the semantics of copying in increasing i (sources are read before
+ *     any overlapping destination is written).  Pages this step first
+ *     touched (first position in [seq_len, seq_len + N)) whose first position
+ *     is >= new_kv_len are freed (page id = slot / page_size).
+ *   freed [capacity] is compacted across requests in (b, node/page) order;
+ *   num_freed [1] receives the count.
+ * A request with seq_len < 0, seq_len + N > max_ctx, accept_length outside
+ * [0, N), or a slot outside [0, num_slots) when copying, is skipped
+ * (new_kv_len = -1, SPEC_STAT_BAD_REQUEST). */
+int spec_compact_slots(int B, int N, int page_size, const int32_t* seq_lens,
+                       const int32_t* accept_path, const int32_t* accept_length,
+                       int32_t* req_to_token, int64_t max_ctx, int32_t* move_src,
+                       int32_t* move_dst, int32_t* num_moves, int32_t* freed,
+                       int64_t freed_capacity, int32_t* num_freed, int32_t* new_kv_len,
+                       void* kv_pool_or_null, int64_t num_slots, int64_t bytes_per_slot,
+                       int32_t* stats_or_null, spec_stream_t stream);
+
+/* -------------------------------------------------------------------- TLI */
+
+/* TLI constrain + top-1 + map ([TLI] Modifications: constrain_draft_logits
+ * sets non-intersection draft logits to -inf before the top-k;
+ * map_draft_to_target_ids maps the chosen id; TLI requires topk == 1).
+ *   draft_logits [R, V_d] (dtype).
+ *   d2t [V_d] target id of each draft id, -1 outside the intersection.
+ *   t2d_or_null [V_t] its inverse on the intersection (-1 elsewhere);
+ *     required when q_target_or_null is given.
+ *   top1_draft / top1_target [R]: argmax over the intersection by
+ *     (logit desc, index asc) and its target id; top1_p [R]: its probability
+ *     under the constrained softmax at temperature T.
+ *   q_target_or_null [R, V_t] fp32: the constrained draft distribution in
+ *     target-vocabulary order (0 off the intersection) -- the q that
+ *     stochastic verify reads.
+ * A row with no finite intersection logit gets -1 / -1 / 0, a zero q row and
+ * counts in SPEC_STAT_EMPTY_INTERSECTION. */
+int tli_constrain_map(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                      const int32_t* d2t, const int32_t* t2d_or_null, float T,
+                      int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                      float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream);
+
+/* Id remapping in either direction ([TLI] Modifications:
+ * map_target_to_draft_ids / map_draft_to_target_ids): out[i] = table[in[i]]
+ * when 0 <= in[i] < table_len and that entry is >= 0, else fallback_id (the
+ * unk id, or eos for models without one). */
+int tli_map_ids(const int32_t* in, int32_t* out, int64_t n, const int32_t* table,
+                int64_t table_len, int32_t fallback_id, spec_stream_t stream);
+
+/* TLI configuration check ([TLI] Modifications, server_args validation):
+ * SPEC_OK iff topk == 1, num_steps >= 1 and num_draft_tokens ==
+ * num_steps + 1.  Host only. */
+int tli_check_config(int topk, int num_steps, int num_draft_tokens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_H */

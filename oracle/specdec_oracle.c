@@ -588,8 +588,9 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
  *                (first position in [seq_len, seq_len + N)) whose first
  *                position is >= new_kv_len, page id = slot / P.
  * freed is compacted across requests in (b, node or page) order.
- * Requests with seq_len + N > max_ctx are skipped (new_kv_len = -1) and
- * counted in *bad. */
+ * Requests with seq_len < 0, seq_len + N > max_ctx, accept_length outside
+ * [0, N) or a path that does not start at 0 and increase are skipped
+ * (new_kv_len = -1) and counted in *bad. */
 int oracle_compact_slots(int B, int N, int page_size, const int32_t* seq_lens,
                          const int32_t* accept_path, const int32_t* accept_length,
                          int32_t* req_to_token, int64_t max_ctx,
@@ -610,7 +611,10 @@ int oracle_compact_slots(int B, int N, int page_size, const int32_t* seq_lens,
         int a = accept_length[b];
         for (int i = 0; i < N; ++i) { move_src[o + i] = -1; move_dst[o + i] = -1; }
         num_moves[b] = 0;
-        if (sl < 0 || sl + N > max_ctx || a < 0 || a >= N) { new_kv_len[b] = -1; ++*bad; continue; }
+        int ok = sl >= 0 && sl + N <= max_ctx && a >= 0 && a < N && accept_path[o] == 0;
+        for (int i = 1; ok && i <= a; ++i)
+            ok = accept_path[o + i] > accept_path[o + i - 1] && accept_path[o + i] < N;
+        if (!ok) { new_kv_len[b] = -1; ++*bad; continue; }
         new_kv_len[b] = (int32_t)(sl + 1 + a);
         memset(on_path, 0, (size_t)N);
         for (int i = 0; i <= a; ++i) on_path[accept_path[o + i]] = 1;

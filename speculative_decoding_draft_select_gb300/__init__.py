@@ -1,0 +1,352 @@
+"""Python binding of libspecdec.so (include/specdec.h).
+
+Argument marshalling only: every function checks that its tensors live on
+the GPU, are contiguous and have the expected dtype, allocates outputs the
+caller did not pass (torch.empty on the same device), and calls the C entry
+point of the same name on torch's current CUDA stream.  All computation runs
+in the library's CUDA kernels; there is no CPU path.  If the library is not
+built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "SpecError", "F32", "BF16", "STATS", "lib", "library_path",
+    "spec_softmax_topk", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
+    "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_sample", "spec_compact_freed_capacity",
+    "spec_compact_slots", "tli_constrain_map", "tli_map_ids", "tli_check_config",
+    "new_stats", "new_pool",
+]
+
+F32 = 0
+BF16 = 1
+STATS = {"nonfinite_row": 0, "q_zero": 1, "residual_fallback": 2, "cdf_fallback": 3,
+         "empty_intersection": 4, "bad_request": 5}
+NUM_STATS = 8
+_ERRORS = {-1: "invalid argument", -2: "unsupported", -3: "CUDA launch failed", -4: "workspace too small"}
+
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecdec.so")
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P]),
+    "spec_sample": (_I, [_P, _I, _P, _I64, _I64, _F, _P, _P, _P, _P, _P]),
+    "spec_tree_pool_size": (_I64, [_I, _I]),
+    "spec_tree_expand": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "spec_build_tree": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "spec_verify_ws_size": (_SZ, [_I, _I]),
+    "spec_verify_greedy": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                _SZ, _P]),
+    "spec_verify_sample": (_I, [_I, _I, _I64, _I, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P,
+                                _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_compact_freed_capacity": (_I64, [_I, _I, _I]),
+    "spec_compact_slots": (_I, [_I, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, _I64,
+                                _I64, _P, _P]),
+    "tli_constrain_map": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _F, _P, _P, _P, _P, _P, _P]),
+    "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
+    "tli_check_config": (_I, [_I, _I, _I]),
+}
+
+
+class SpecError(RuntimeError):
+    def __init__(self, name: str, rc: int):
+        super().__init__(f"{name}: {_ERRORS.get(rc, 'error')} (rc={rc})")
+        self.rc = rc
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it with "
+                               "speculative_decoding_draft_select_gb300.build.build()")
+        l = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _call(name, *args):
+    rc = getattr(lib(), name)(*args)
+    if rc != 0:
+        raise SpecError(name, rc)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _logit_code(t):
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise ValueError("logits must be float32 or bfloat16")
+
+
+def _out(t, shape, dtype, like, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return _dev(t, dtype, name)
+
+
+def new_stats(device="cuda"):
+    """A zeroed int32[8] stats array."""
+    return torch.zeros(NUM_STATS, dtype=torch.int32, device=device)
+
+
+# ------------------------------------------------------------------- draft
+
+def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want_probs=False, stats=None):
+    """logits [R, V] -> (topk_p [R, k] f32, topk_idx [R, k] i32, probs [R, V] f32 or None)."""
+    _dev(logits, name="logits")
+    V = logits.shape[-1]
+    R = logits.numel() // V
+    topk_p = _out(topk_p, (R, k), torch.float32, logits, "topk_p")
+    topk_idx = _out(topk_idx, (R, k), torch.int32, logits, "topk_idx")
+    if want_probs and probs is None:
+        probs = torch.empty((R, V), dtype=torch.float32, device=logits.device)
+    _dev(probs, torch.float32, "probs")
+    _dev(stats, torch.int32, "stats")
+    _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
+          _ptr(topk_idx), _ptr(probs), _ptr(stats), _stream())
+    return topk_p, topk_idx, probs
+
+
+def spec_sample(u, logits=None, probs=None, T=1.0, out_token=None, out_prob=None, stats=None):
+    """One token per row by inverse CDF with uniforms u [R]."""
+    src = probs if probs is not None else logits
+    _dev(src, name="probs/logits")
+    _dev(u, torch.float32, "u")
+    V = src.shape[-1]
+    R = src.numel() // V
+    out_token = _out(out_token, (R,), torch.int32, src, "out_token")
+    out_prob = _out(out_prob, (R,), torch.float32, src, "out_prob")
+    _dev(stats, torch.int32, "stats")
+    if probs is not None:
+        _dev(probs, torch.float32, "probs")
+        code = F32
+    else:
+        code = _logit_code(logits)
+    _call("spec_sample", _ptr(logits if probs is None else None), code, _ptr(probs), R, V, float(T), _ptr(u),
+          _ptr(out_token), _ptr(out_prob), _ptr(stats), _stream())
+    return out_token, out_prob
+
+
+def spec_tree_pool_size(k, num_steps):
+    return int(lib().spec_tree_pool_size(int(k), int(num_steps)))
+
+
+def new_pool(B, k, num_steps, device="cuda"):
+    """Pool [B, P] (score, token, parent, qrow) and frontier [B, k] tensors."""
+    P = spec_tree_pool_size(k, num_steps)
+    return {
+        "score": torch.empty((B, P), dtype=torch.float32, device=device),
+        "token": torch.empty((B, P), dtype=torch.int32, device=device),
+        "parent": torch.empty((B, P), dtype=torch.int32, device=device),
+        "qrow": torch.empty((B, P), dtype=torch.int32, device=device),
+        "frontier_score": torch.empty((B, k), dtype=torch.float32, device=device),
+        "frontier_id": torch.empty((B, k), dtype=torch.int32, device=device),
+        "B": B, "k": k, "num_steps": num_steps, "P": P,
+    }
+
+
+def spec_tree_expand(pool, step, topk_p, topk_idx):
+    _dev(topk_p, torch.float32, "topk_p")
+    _dev(topk_idx, torch.int32, "topk_idx")
+    _call("spec_tree_expand", int(step), pool["num_steps"], pool["B"], pool["k"], _ptr(topk_p), _ptr(topk_idx),
+          _ptr(pool["score"]), _ptr(pool["token"]), _ptr(pool["parent"]), _ptr(pool["qrow"]),
+          _ptr(pool["frontier_score"]), _ptr(pool["frontier_id"]), _stream())
+    return pool
+
+
+def spec_build_tree(pool, N, root_token, seq_lens, out=None):
+    """Returns a dict of [B, N] tensors (tree_mask [B, N, N] uint8)."""
+    B = pool["B"]
+    dev = pool["score"].device
+    _dev(root_token, torch.int32, "root_token")
+    _dev(seq_lens, torch.int32, "seq_lens")
+    if out is None:
+        out = {name: torch.empty((B, N), dtype=torch.int32, device=dev)
+               for name in ("draft_token", "parent", "positions", "retrieve_index", "retrieve_next_token",
+                            "retrieve_next_sibling", "q_row")}
+        out["tree_mask"] = torch.empty((B, N, N), dtype=torch.uint8, device=dev)
+    _call("spec_build_tree", B, pool["k"], pool["num_steps"], int(N), _ptr(pool["score"]), _ptr(pool["token"]),
+          _ptr(pool["parent"]), _ptr(pool["qrow"]), _ptr(root_token), _ptr(seq_lens), _ptr(out["draft_token"]),
+          _ptr(out["parent"]), _ptr(out["positions"]), _ptr(out["tree_mask"]), _ptr(out["retrieve_index"]),
+          _ptr(out["retrieve_next_token"]), _ptr(out["retrieve_next_sibling"]), _ptr(out["q_row"]), _stream())
+    return out
+
+
+# ------------------------------------------------------------------ verify
+
+def spec_verify_ws_size(B, N):
+    return int(lib().spec_verify_ws_size(int(B), int(N)))
+
+
+def _verify_outputs(B, N, dev, out):
+    if out is not None:
+        return out
+    return {
+        "committed": torch.empty((B, N), dtype=torch.int32, device=dev),
+        "num_committed": torch.empty((B,), dtype=torch.int32, device=dev),
+        "accept_length": torch.empty((B,), dtype=torch.int32, device=dev),
+        "accept_path": torch.empty((B, N), dtype=torch.int32, device=dev),
+        "next_root": torch.empty((B,), dtype=torch.int32, device=dev),
+        "walk_info": torch.empty((B, 3), dtype=torch.int32, device=dev),
+    }
+
+
+def _workspace(B, N, dev, ws):
+    need = spec_verify_ws_size(B, N)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _dev(ws, torch.uint8, "ws")
+    return ws
+
+
+def spec_verify_greedy(target, draft_token, next_token, next_sibling, budget=None, eos_id=-1, out=None, ws=None,
+                       stats=None):
+    """target [B, N, V] (f32 or bf16)."""
+    _dev(target, name="target")
+    B, N, V = target.shape
+    for name, t in (("draft_token", draft_token), ("next_token", next_token), ("next_sibling", next_sibling)):
+        _dev(t, torch.int32, name)
+    _dev(budget, torch.int32, "budget")
+    _dev(stats, torch.int32, "stats")
+    out = _verify_outputs(B, N, target.device, out)
+    ws = _workspace(B, N, target.device, ws)
+    _call("spec_verify_greedy", B, N, V, _logit_code(target), _ptr(target), _ptr(draft_token), _ptr(next_token),
+          _ptr(next_sibling), _ptr(budget), int(eos_id), _ptr(out["committed"]), _ptr(out["num_committed"]),
+          _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]), _ptr(out.get("walk_info")),
+          _ptr(stats), _ptr(ws), ws.numel(), _stream())
+    return out
+
+
+def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coins, u_final, q_row=None,
+                       budget=None, eos_id=-1, out=None, ws=None, stats=None):
+    """target [B, N, V]; q fp32 rows of length V (a [rows, V] table with q_row [B, N], or [B, N, V])."""
+    _dev(target, name="target")
+    B, N, V = target.shape
+    _dev(q, torch.float32, "q")
+    if q.shape[-1] != V:
+        raise ValueError("q rows must have length V")
+    for name, t in (("draft_token", draft_token), ("next_token", next_token), ("next_sibling", next_sibling)):
+        _dev(t, torch.int32, name)
+    _dev(q_row, torch.int32, "q_row")
+    _dev(coins, torch.float32, "coins")
+    _dev(u_final, torch.float32, "u_final")
+    _dev(budget, torch.int32, "budget")
+    _dev(stats, torch.int32, "stats")
+    out = _verify_outputs(B, N, target.device, out)
+    ws = _workspace(B, N, target.device, ws)
+    _call("spec_verify_sample", B, N, V, _logit_code(target), _ptr(target), float(T), _ptr(q), _ptr(q_row),
+          _ptr(draft_token), _ptr(next_token), _ptr(next_sibling), _ptr(coins), _ptr(u_final), _ptr(budget),
+          int(eos_id), _ptr(out["committed"]), _ptr(out["num_committed"]), _ptr(out["accept_length"]),
+          _ptr(out["accept_path"]), _ptr(out["next_root"]), _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws),
+          ws.numel(), _stream())
+    return out
+
+
+# -------------------------------------------------------------- compaction
+
+def spec_compact_freed_capacity(B, N, page_size):
+    return int(lib().spec_compact_freed_capacity(int(B), int(N), int(page_size)))
+
+
+def spec_compact_slots(seq_lens, accept_path, accept_length, req_to_token, page_size, kv_pool=None, out=None,
+                       stats=None):
+    """req_to_token [B, max_ctx] int32 and kv_pool [slots, bytes] uint8 are updated in place."""
+    _dev(seq_lens, torch.int32, "seq_lens")
+    _dev(accept_path, torch.int32, "accept_path")
+    _dev(accept_length, torch.int32, "accept_length")
+    _dev(req_to_token, torch.int32, "req_to_token")
+    _dev(kv_pool, torch.uint8, "kv_pool")
+    _dev(stats, torch.int32, "stats")
+    B, N = accept_path.shape
+    max_ctx = req_to_token.shape[1]
+    cap = spec_compact_freed_capacity(B, N, page_size)
+    dev = accept_path.device
+    if out is None:
+        out = {
+            "move_src": torch.empty((B, N), dtype=torch.int32, device=dev),
+            "move_dst": torch.empty((B, N), dtype=torch.int32, device=dev),
+            "num_moves": torch.empty((B,), dtype=torch.int32, device=dev),
+            "freed": torch.empty((max(cap, 1),), dtype=torch.int32, device=dev),
+            "num_freed": torch.empty((1,), dtype=torch.int32, device=dev),
+            "new_kv_len": torch.empty((B,), dtype=torch.int32, device=dev),
+        }
+    slots = kv_pool.shape[0] if kv_pool is not None else 0
+    bps = kv_pool.shape[1] if kv_pool is not None else 0
+    _call("spec_compact_slots", B, N, int(page_size), _ptr(seq_lens), _ptr(accept_path), _ptr(accept_length),
+          _ptr(req_to_token), max_ctx, _ptr(out["move_src"]), _ptr(out["move_dst"]), _ptr(out["num_moves"]),
+          _ptr(out["freed"]), out["freed"].numel(), _ptr(out["num_freed"]), _ptr(out["new_kv_len"]), _ptr(kv_pool),
+          slots, bps, _ptr(stats), _stream())
+    return out
+
+
+# --------------------------------------------------------------------- TLI
+
+def tli_constrain_map(draft_logits, d2t, T, t2d=None, want_q=False, top1_draft=None, top1_target=None,
+                      top1_p=None, q_target=None, stats=None):
+    _dev(draft_logits, name="draft_logits")
+    _dev(d2t, torch.int32, "d2t")
+    _dev(t2d, torch.int32, "t2d")
+    Vd = draft_logits.shape[-1]
+    R = draft_logits.numel() // Vd
+    if d2t.numel() != Vd:
+        raise ValueError("d2t must have V_d entries")
+    Vt = t2d.numel() if t2d is not None else 1
+    top1_draft = _out(top1_draft, (R,), torch.int32, draft_logits, "top1_draft")
+    top1_target = _out(top1_target, (R,), torch.int32, draft_logits, "top1_target")
+    top1_p = _out(top1_p, (R,), torch.float32, draft_logits, "top1_p")
+    if want_q and q_target is None:
+        q_target = torch.empty((R, Vt), dtype=torch.float32, device=draft_logits.device)
+    _dev(q_target, torch.float32, "q_target")
+    _dev(stats, torch.int32, "stats")
+    _call("tli_constrain_map", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t), _ptr(t2d),
+          float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target), _ptr(stats), _stream())
+    return top1_draft, top1_target, top1_p, q_target
+
+
+def tli_map_ids(ids, table, fallback_id, out=None):
+    _dev(ids, torch.int32, "ids")
+    _dev(table, torch.int32, "table")
+    out = _out(out, ids.shape, torch.int32, ids, "out")
+    _call("tli_map_ids", _ptr(ids), _ptr(out), ids.numel(), _ptr(table), table.numel(), int(fallback_id), _stream())
+    return out
+
+
+def tli_check_config(topk, num_steps, num_draft_tokens) -> bool:
+    return lib().tli_check_config(int(topk), int(num_steps), int(num_draft_tokens)) == 0

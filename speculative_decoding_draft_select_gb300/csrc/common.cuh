@@ -1,0 +1,249 @@
+// Shared device helpers of the sm_103a kernels: logit decoding, streaming
+// vector loads, the (value desc, index asc) order, warp/block reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "specdec.h"
+
+namespace specdec {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ inline float neg_inf() { return -__builtin_huge_valf(); }
+
+// Ordering key of a logit: NaN becomes -inf (max.f32 returns the non-NaN
+// operand), every other value is kept.
+__device__ __forceinline__ float order_key(float x) { return fmaxf(x, neg_inf()); }
+
+// 2^x with the hardware approximation (relative error about 2^-22; inputs
+// below -126 flush to 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int DT>
+struct Logit;
+
+// fp32 logits: a 16-byte vector holds 4 elements.
+template <>
+struct Logit<SPEC_F32> {
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return __ldg(static_cast<const float*>(p) + i);
+  }
+};
+
+// bf16 logits: a 16-byte vector holds 8 elements.
+template <>
+struct Logit<SPEC_BF16> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const uint16_t*>(p) + i)) << 16);
+  }
+};
+
+// Read-only 16-byte load that does not allocate in L1 (streamed data).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Streaming 16-byte store (evict-first).
+__device__ __forceinline__ void st_stream(void* p, float4 v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
+// Unpack one 16-byte vector into kVec floats.
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4& v, float* x);
+
+template <>
+__device__ __forceinline__ void unpack<SPEC_F32>(const uint4& v, float* x) {
+  x[0] = __uint_as_float(v.x);
+  x[1] = __uint_as_float(v.y);
+  x[2] = __uint_as_float(v.z);
+  x[3] = __uint_as_float(v.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack<SPEC_BF16>(const uint4& v, float* x) {
+  x[0] = bf16_lo(v.x);
+  x[1] = bf16_hi(v.x);
+  x[2] = bf16_lo(v.y);
+  x[3] = bf16_hi(v.y);
+  x[4] = bf16_lo(v.z);
+  x[5] = bf16_hi(v.z);
+  x[6] = bf16_lo(v.w);
+  x[7] = bf16_hi(v.w);
+}
+
+// (value desc, index asc): true if (va, ia) comes before (vb, ib).
+__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Warp-wide best (value desc, index asc).
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (before(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Merge two online-softmax partials (m, s), s = sum 2^((x - m) * c).
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c) {
+  if (m2 > m) {
+    s = (m == neg_inf() ? 0.0f : s * fast_exp2((m - m2) * c)) + s2;
+    m = m2;
+  } else if (m2 != neg_inf()) {
+    s += s2 * fast_exp2((m2 - m) * c);
+  }
+}
+
+__device__ __forceinline__ void warp_merge_ms(float& m, float& s, float c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    merge_ms(m, s, m2, s2, c);
+  }
+}
+
+// Inclusive scan of one float per thread across a block, in thread order;
+// also returns the block total.  `sh` holds at least 32 floats.  All threads
+// of the block must call it.
+__device__ __forceinline__ float block_inclusive_scan(float v, float* sh, float& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < nw ? sh[lane] : 0.0f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      float y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) sh[lane] = w;
+  }
+  __syncthreads();
+  total = sh[nw - 1];
+  return x + (warp > 0 ? sh[warp - 1] : 0.0f);
+}
+
+__device__ __forceinline__ void bump(int32_t* stats, int slot, int n = 1) {
+  if (stats != nullptr && n != 0) atomicAdd(stats + slot, n);
+}
+
+// Aligned vector span of a row: elements [head, head + nvec*kVec) start on a
+// 16-byte boundary; [0, head) and the rest are handled one by one.
+struct RowSpan {
+  int64_t head, nvec;
+};
+
+// Visit every element of a row once.  Each thread sees its elements in
+// increasing index order: a few leading scalars up to the first 16-byte
+// boundary, then 16-byte vectors (UNROLL loads in flight per thread), then
+// the trailing scalars.  F provides
+//   template <int N> void visit(const float* x, int64_t first_index).
+template <int DT, int UNROLL, class F>
+__device__ __forceinline__ void for_row(const void* row, int64_t V, F& f);
+
+template <int DT>
+__device__ __forceinline__ RowSpan row_span(const void* row, int64_t V) {
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  constexpr int kv = Logit<DT>::kVec;
+  uintptr_t a = reinterpret_cast<uintptr_t>(row);
+  int64_t head = static_cast<int64_t>(((16 - (a & 15)) & 15) / esz);
+  if (head > V) head = V;
+  int64_t nvec = (V - head) / kv;
+  return {head, nvec};
+}
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace specdec
+
+namespace specdec {
+
+template <int DT, int UNROLL, class F>
+__device__ __forceinline__ void for_row(const void* row, int64_t V, F& f) {
+  constexpr int kv = Logit<DT>::kVec;
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  const RowSpan sp = row_span<DT>(row, V);
+  const int64_t nt = blockDim.x;
+  for (int64_t i = threadIdx.x; i < sp.head; i += nt) {
+    float x = Logit<DT>::load1(row, i);
+    f.template visit<1>(&x, i);
+  }
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+  int64_t i = threadIdx.x;
+  for (; i + (UNROLL - 1) * nt < sp.nvec; i += UNROLL * nt) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) v[u] = ld_stream(vp + i + u * nt);
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      float x[kv];
+      unpack<DT>(v[u], x);
+      f.template visit<kv>(x, sp.head + (i + u * nt) * kv);
+    }
+  }
+  for (; i < sp.nvec; i += nt) {
+    float x[kv];
+    unpack<DT>(ld_stream(vp + i), x);
+    f.template visit<kv>(x, sp.head + i * kv);
+  }
+  for (int64_t t = sp.head + sp.nvec * kv + threadIdx.x; t < V; t += nt) {
+    float x = Logit<DT>::load1(row, t);
+    f.template visit<1>(&x, t);
+  }
+}
+
+}  // namespace specdec

@@ -1,0 +1,176 @@
+// TLI (Token-Level Intersection): heterogeneous-vocabulary drafting.
+//
+// SGLang PR #22883 "TLI (Token-Level Intersection)", section Modifications:
+// vocab_mapping.py exposes constrain_draft_logits (non-intersection draft
+// logits set to -inf before the top-k), map_target_to_draft_ids and
+// map_draft_to_target_ids, and intersection_draft_ids; the TLIWorker hook
+// capture_for_decode constrains the draft logits before top-k sampling; the
+// server arguments require topk == 1 and num_draft_tokens == num_steps + 1.
+// The rejection sampler of the target is unchanged, so verification reads
+// the constrained draft distribution written in target-vocabulary order.
+//
+// tli_constrain_kernel: one CTA per draft row.  Pass 1 streams the row with
+// 16-byte loads, skipping ids outside the intersection (d2t[v] < 0, read
+// through the read-only cache: the table is shared by every row and stays in
+// L2), and keeps the masked top-1 and online-softmax partials.  Pass 2
+// (optional) writes q in target order: q_t[t] = p(t2d[t]) or 0, with
+// coalesced 16-byte stores and gathers from the draft row (L2-resident).
+#include <climits>
+
+#include "common.cuh"
+
+namespace specdec {
+namespace {
+
+constexpr int kTliThreads = 512;
+
+struct MaskedVisitor {
+  const int32_t* d2t;
+  float c, m, s;
+  int bi;
+  template <int N>
+  __device__ __forceinline__ void visit(const float* xin, int64_t first) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      if (__ldg(d2t + first + j) < 0) continue;
+      const float x = order_key(xin[j]);
+      const int idx = static_cast<int>(first) + j;
+      if (before(x, idx, m, bi)) {
+        if (x > m) s = (m == neg_inf()) ? 0.0f : s * fast_exp2((m - x) * c);
+        m = x;
+        bi = idx;
+      }
+      if (m != neg_inf()) s += fast_exp2(fmaf(x, c, -m * c));
+    }
+  }
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kTliThreads)
+    tli_constrain_kernel(int64_t Vd, int64_t Vt, const void* __restrict__ draft, const int32_t* __restrict__ d2t,
+                         const int32_t* __restrict__ t2d, float c, int32_t* __restrict__ top1_draft,
+                         int32_t* __restrict__ top1_target, float* __restrict__ top1_p, float* __restrict__ q,
+                         int32_t* __restrict__ stats) {
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  constexpr int kWarps = kTliThreads / 32;
+  __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
+  __shared__ int wi[kWarps];
+  __shared__ float s_m, s_invz;
+  __shared__ int s_best;
+  const int64_t r = blockIdx.x;
+  const void* row = static_cast<const char*>(draft) + r * Vd * esz;
+  MaskedVisitor st{d2t, c, neg_inf(), 0.0f, INT_MAX};
+  for_row<DT, 4>(row, Vd, st);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float bv = st.m;
+  int bi = st.bi;
+  warp_best(bv, bi);
+  float m = st.m, s = st.s;
+  warp_merge_ms(m, s, c);
+  if (lane == 0) {
+    wv[warp] = bv;
+    wi[warp] = bi;
+    wm[warp] = m;
+    ws[warp] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < kWarps ? wv[lane] : neg_inf();
+    bi = lane < kWarps ? wi[lane] : INT_MAX;
+    warp_best(bv, bi);
+    m = lane < kWarps ? wm[lane] : neg_inf();
+    s = lane < kWarps ? ws[lane] : 0.0f;
+    warp_merge_ms(m, s, c);
+    if (lane == 0) {
+      const bool ok = bi != INT_MAX && isfinite(bv);
+      s_best = ok ? bi : -1;
+      s_m = m;
+      s_invz = 1.0f / s;
+      top1_draft[r] = ok ? bi : -1;
+      top1_target[r] = ok ? __ldg(d2t + bi) : -1;
+      top1_p[r] = ok ? fminf(fast_exp2(fmaf(bv, c, -m * c)) * (1.0f / s), 1.0f) : 0.0f;
+      if (!ok) bump(stats, SPEC_STAT_EMPTY_INTERSECTION);
+    }
+  }
+  __syncthreads();
+  if (q == nullptr) return;
+  float* out = q + r * Vt;
+  const bool ok = s_best >= 0;
+  const float mc = s_m * c, invz = s_invz;
+  const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (reinterpret_cast<uintptr_t>(t2d) & 15) == 0;
+  const int64_t nv = vec ? Vt / 4 : 0;
+  for (int64_t i = threadIdx.x; i < nv; i += kTliThreads) {
+    const int4 d = __ldg(reinterpret_cast<const int4*>(t2d) + i);
+    float4 p;
+    p.x = (ok && d.x >= 0 && d.x < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.x)), c, -mc)) * invz, 1.0f) : 0.0f;
+    p.y = (ok && d.y >= 0 && d.y < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.y)), c, -mc)) * invz, 1.0f) : 0.0f;
+    p.z = (ok && d.z >= 0 && d.z < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.z)), c, -mc)) * invz, 1.0f) : 0.0f;
+    p.w = (ok && d.w >= 0 && d.w < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.w)), c, -mc)) * invz, 1.0f) : 0.0f;
+    st_stream(out + 4 * i, p);
+  }
+  for (int64_t t = nv * 4 + threadIdx.x; t < Vt; t += kTliThreads) {
+    const int32_t d = __ldg(t2d + t);
+    out[t] = (ok && d >= 0 && d < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d)), c, -mc)) * invz, 1.0f)
+                            : 0.0f;
+  }
+}
+
+__global__ void map_ids_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out, int64_t n,
+                               const int32_t* __restrict__ table, int64_t table_len, int32_t fallback) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t x = __ldg(in + i);
+    int32_t y = fallback;
+    if (x >= 0 && x < table_len) {
+      const int32_t t = __ldg(table + x);
+      if (t >= 0) y = t;
+    }
+    out[i] = y;
+  }
+}
+
+}  // namespace
+}  // namespace specdec
+
+using namespace specdec;
+
+extern "C" int tli_constrain_map(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                                 const int32_t* d2t, const int32_t* t2d_or_null, float T, int32_t* top1_draft,
+                                 int32_t* top1_target, float* top1_p, float* q_target_or_null,
+                                 int32_t* stats_or_null, spec_stream_t stream) {
+  if (R < 0 || V_d < 1 || V_t < 1 || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (V_d > SPEC_MAX_VOCAB || V_t > SPEC_MAX_VOCAB || R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  if (R == 0) return SPEC_OK;
+  if (!draft_logits || !d2t || !top1_draft || !top1_target || !top1_p) return SPEC_ERR_INVALID_ARG;
+  if (q_target_or_null && !t2d_or_null) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float c = kLog2e / T;
+  const unsigned grid = static_cast<unsigned>(R);
+  if (dtype == SPEC_BF16)
+    tli_constrain_kernel<SPEC_BF16><<<grid, kTliThreads, 0, s>>>(V_d, V_t, draft_logits, d2t, t2d_or_null, c,
+                                                                 top1_draft, top1_target, top1_p,
+                                                                 q_target_or_null, stats_or_null);
+  else
+    tli_constrain_kernel<SPEC_F32><<<grid, kTliThreads, 0, s>>>(V_d, V_t, draft_logits, d2t, t2d_or_null, c,
+                                                                top1_draft, top1_target, top1_p,
+                                                                q_target_or_null, stats_or_null);
+  return launch_status();
+}
+
+extern "C" int tli_map_ids(const int32_t* in, int32_t* out, int64_t n, const int32_t* table, int64_t table_len,
+                           int32_t fallback_id, spec_stream_t stream) {
+  if (n < 0 || table_len < 0) return SPEC_ERR_INVALID_ARG;
+  if (n == 0) return SPEC_OK;
+  if (!in || !out || (!table && table_len > 0)) return SPEC_ERR_INVALID_ARG;
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  map_ids_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), threads, 0,
+                   reinterpret_cast<cudaStream_t>(stream)>>>(in, out, n, table, table_len, fallback_id);
+  return launch_status();
+}
+
+extern "C" int tli_check_config(int topk, int num_steps, int num_draft_tokens) {
+  return (topk == 1 && num_steps >= 1 && num_draft_tokens == num_steps + 1) ? SPEC_OK : SPEC_ERR_INVALID_ARG;
+}

@@ -1,0 +1,488 @@
+// Batched verification over the target logits of every tree node.
+//
+// zero-to-sglang ch.10 "Speculative decoding (code walk-through)":
+//   3.3  row L-1+i of the target output verifies draft i, row L+k-1 gives the
+//        bonus -- here row (b, n) verifies node n's children;
+//   4.1  greedy_commit: commit the target's choice, stop at the first
+//        mismatch, at EOS or when the budget is used; bonus on full accept;
+//   5.1  stochastic acceptance: accept y ~ q with min(1, p[y]/q[y]); after a
+//        rejection draw from the normalised positive residual (p - q)+; after
+//        full acceptance draw the bonus from p.
+// "EAGLE speculative decoding in four parts" (ai-infra-handbooks),
+// "Drafting, verification and slots": one target pass verifies every tree
+// candidate; the verify kernels walk the tree to each request's longest
+// accepted path.
+//
+// Pass 1 (row_stats_kernel) is the bandwidth kernel: one CTA streams one
+// target row once with 16-byte loads and produces its argmax and, for
+// sampling, the online-softmax max and normaliser.  Pass 2 walks each
+// request's tree.  The greedy walk needs only the argmax per row (one warp
+// per request).  The stochastic walk (one CTA per request) gathers p[y] and
+// q[y] of every child of the current node at once, and after each
+// rejection streams the node's target and q rows to get the residual's mass.
+// The residual after j rejections is kept in closed form,
+//   p_j(v) = max(0, p(v) - A_j q(v)) / c_j,  A_{j+1} = A_j + c_j,
+//   c_{j+1} = sum_v max(0, p(v) - A_{j+1} q(v)),  A_0 = 0, c_0 = 1,
+// which equals the repeated normalised update (p_j - q)+ / sum (p_j - q)+.
+// The last residual pass also leaves the per-tile sums the inverse-CDF draw
+// needs, so a correction token costs one row sweep plus one tile rescan.
+#include <climits>
+
+#include "cdf.cuh"
+#include "common.cuh"
+
+namespace specdec {
+namespace {
+
+constexpr int kStatThreads = 512;
+constexpr int kWalkThreads = 512;
+
+__device__ __forceinline__ float prob_of(float key, float c, float mc, float invz) {
+  return fminf(fast_exp2(fmaf(key, c, -mc)) * invz, 1.0f);
+}
+
+template <bool STOCH>
+struct RowStatVisitor {
+  float c, m, s;
+  int bi;
+  template <int N>
+  __device__ __forceinline__ void visit(const float* xin, int64_t first) {
+    float x[N];
+    float vmax = neg_inf();
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      x[j] = order_key(xin[j]);
+      vmax = fmaxf(vmax, x[j]);
+    }
+    if (vmax > m) {
+      int j0 = 0;
+#pragma unroll
+      for (int j = N - 1; j >= 0; --j)
+        if (x[j] == vmax) j0 = j;
+      bi = static_cast<int>(first) + j0;
+      if (STOCH) s = (m == neg_inf()) ? 0.0f : s * fast_exp2((m - vmax) * c);
+      m = vmax;
+    }
+    if (STOCH && m != neg_inf()) {
+      const float mc = m * c;
+#pragma unroll
+      for (int j = 0; j < N; ++j) s += fast_exp2(fmaf(x[j], c, -mc));
+    }
+  }
+};
+
+template <int DT, bool STOCH>
+__global__ void __launch_bounds__(kStatThreads)
+    row_stats_kernel(const void* __restrict__ logits, int64_t V, float c, int32_t* __restrict__ amax,
+                     float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  constexpr int kWarps = kStatThreads / 32;
+  __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
+  __shared__ int wi[kWarps];
+  const int64_t r = blockIdx.x;
+  const void* row = static_cast<const char*>(logits) + r * V * esz;
+  RowStatVisitor<STOCH> st{c, neg_inf(), 0.0f, INT_MAX};
+  for_row<DT, 4>(row, V, st);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float bv = st.m;
+  int bi = st.bi;
+  warp_best(bv, bi);
+  float m = st.m, s = st.s;
+  if (STOCH) warp_merge_ms(m, s, c);
+  if (lane == 0) {
+    wv[warp] = bv;
+    wi[warp] = bi;
+    wm[warp] = m;
+    ws[warp] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < kWarps ? wv[lane] : neg_inf();
+    bi = lane < kWarps ? wi[lane] : INT_MAX;
+    warp_best(bv, bi);
+    if (STOCH) {
+      m = lane < kWarps ? wm[lane] : neg_inf();
+      s = lane < kWarps ? ws[lane] : 0.0f;
+      warp_merge_ms(m, s, c);
+    }
+    if (lane == 0) {
+      amax[r] = bi == INT_MAX ? 0 : bi;
+      if (STOCH) {
+        m_out[r] = m;
+        z_out[r] = s;
+      }
+      if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
+    }
+  }
+}
+
+// ------------------------------------------------------------ greedy walk
+
+__global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, const int32_t* __restrict__ dtok,
+                                   const int32_t* __restrict__ ntok, const int32_t* __restrict__ nsib,
+                                   const int32_t* __restrict__ budget, int32_t eos, int32_t* committed,
+                                   int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
+                                   int32_t* next_root, int32_t* walk_info) {
+  extern __shared__ int32_t sh[];
+  int32_t *s_am = sh, *s_dt = sh + N, *s_nt = sh + 2 * N, *s_ns = sh + 3 * N, *s_com = sh + 4 * N,
+          *s_path = sh + 5 * N;
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const int64_t o = static_cast<int64_t>(b) * N;
+  for (int i = lane; i < N; i += 32) {
+    s_am[i] = __ldg(amax + o + i);
+    s_dt[i] = __ldg(dtok + o + i);
+    s_nt[i] = __ldg(ntok + o + i);
+    s_ns[i] = __ldg(nsib + o + i);
+    s_com[i] = -1;
+    s_path[i] = -1;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    const int rem = budget ? __ldg(budget + b) : INT_MAX;
+    int len = 0, acc = 0, rej = 0, kind = SPEC_FINAL_ACCEPTED, n = 0;
+    s_path[0] = 0;
+    while (rem > 0 && len < N) {
+      const int32_t t = s_am[n];
+      s_com[len++] = t;
+      int found = -1, hops = 0;
+      for (int c = s_nt[n]; c > 0 && c < N && hops < N; c = s_ns[c], ++hops) {
+        if (s_dt[c] == t) {
+          found = c;
+          break;
+        }
+        ++rej;
+      }
+      if (found >= 0) s_path[++acc] = found;
+      if (t == eos || len == rem || found < 0) {
+        if (found >= 0) {
+          kind = SPEC_FINAL_ACCEPTED;
+          n = found;
+        } else {
+          kind = s_nt[n] > 0 ? SPEC_FINAL_CORRECTION : SPEC_FINAL_BONUS;
+        }
+        break;
+      }
+      n = found;
+    }
+    num_committed[b] = len;
+    accept_length[b] = acc;
+    next_root[b] = len > 0 ? s_com[len - 1] : -1;
+    if (walk_info) {
+      walk_info[3 * b] = n;
+      walk_info[3 * b + 1] = rej;
+      walk_info[3 * b + 2] = kind;
+    }
+  }
+  __syncwarp();
+  for (int i = lane; i < N; i += 32) {
+    committed[o + i] = s_com[i];
+    accept_path[o + i] = s_path[i];
+  }
+}
+
+// -------------------------------------------------------- stochastic walk
+
+// Weights of the current distribution at a node: p (A == 0) or the
+// unnormalised residual max(0, p - A q).
+template <int DT>
+struct ResidualWeights {
+  const void* lrow;
+  const float* qrow;
+  int64_t V;
+  float c, mc, invz, A;
+  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
+    load8_logits<DT>(lrow, V, v0, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = prob_of(x[j], c, mc, invz);
+    if (A != 0.0f && qrow != nullptr) {
+      float q[8];
+      load8_f32(qrow, V, v0, q);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = fmaxf(0.0f, fmaf(-A, q[j], x[j]));
+    }
+  }
+  __device__ __forceinline__ float at(int64_t v) const {
+    const float p = prob_of(order_key(Logit<DT>::load1(lrow, v)), c, mc, invz);
+    return (A != 0.0f && qrow != nullptr) ? fmaxf(0.0f, fmaf(-A, __ldg(qrow + v), p)) : p;
+  }
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kWalkThreads)
+    sample_walk_kernel(int N, int64_t V, float c, const void* __restrict__ target,
+                       const float* __restrict__ m_row, const float* __restrict__ z_row,
+                       const float* __restrict__ q, const int32_t* __restrict__ q_row,
+                       const int32_t* __restrict__ dtok, const int32_t* __restrict__ ntok,
+                       const int32_t* __restrict__ nsib, const float* __restrict__ coins,
+                       const float* __restrict__ u_final, const int32_t* __restrict__ budget, int32_t eos,
+                       int32_t* committed, int32_t* num_committed, int32_t* accept_length,
+                       int32_t* accept_path, int32_t* next_root, int32_t* walk_info, int32_t* stats) {
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  extern __shared__ float dyn[];
+  const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
+  float* tile_sum = dyn;
+  float* red = tile_sum + ntiles;
+  float* g_l = red + ntiles * (kWalkThreads / 32);
+  float* g_q = g_l + N;
+  float* g_u = g_q + N;
+  int32_t* s_dt = reinterpret_cast<int32_t*>(g_u + N);
+  int32_t* s_nt = s_dt + N;
+  int32_t* s_ns = s_nt + N;
+  int32_t* s_com = s_ns + N;
+  int32_t* s_path = s_com + N;
+  int32_t* s_ch = s_path + N;
+  __shared__ float scan_sh[33];
+  __shared__ int s_n, s_len, s_acc, s_rej, s_kind, s_done, s_nch, s_accept, s_tiles_ok, s_rem;
+  __shared__ int64_t s_qrow;
+  __shared__ float s_m, s_invz, s_A, s_cj, s_total;
+
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int64_t o = static_cast<int64_t>(b) * N;
+  for (int i = tid; i < N; i += kWalkThreads) {
+    s_dt[i] = __ldg(dtok + o + i);
+    s_nt[i] = __ldg(ntok + o + i);
+    s_ns[i] = __ldg(nsib + o + i);
+    s_com[i] = -1;
+    s_path[i] = -1;
+  }
+  if (tid == 0) {
+    s_rem = budget ? __ldg(budget + b) : INT_MAX;
+    s_n = 0;
+    s_len = 0;
+    s_acc = 0;
+    s_rej = 0;
+    s_kind = SPEC_FINAL_ACCEPTED;
+    s_done = s_rem <= 0;
+    s_path[0] = 0;
+  }
+  __syncthreads();
+  const float cT = c;
+  while (!s_done) {
+    // enter node n: children in sibling order, row statistics, q row
+    if (tid == 0) {
+      const int n = s_n;
+      int nch = 0;
+      for (int ch = s_nt[n]; ch > 0 && ch < N && nch < N; ch = s_ns[ch]) s_ch[nch++] = ch;
+      s_nch = nch;
+      s_m = __ldg(m_row + o + n);
+      s_invz = 1.0f / __ldg(z_row + o + n);
+      s_qrow = q_row ? static_cast<int64_t>(__ldg(q_row + o + n)) : o + n;
+      s_A = 0.0f;
+      s_cj = 1.0f;
+      s_tiles_ok = 0;
+    }
+    __syncthreads();
+    const int n = s_n, nch = s_nch;
+    const void* lrow = static_cast<const char*>(target) + (o + n) * V * esz;
+    const float* qrow = (nch > 0 && s_qrow >= 0) ? q + s_qrow * V : nullptr;
+    const float mc = s_m * cT, invz = s_invz;
+    for (int t = tid; t < nch; t += kWalkThreads) {
+      const int ch = s_ch[t];
+      const int32_t y = s_dt[ch];
+      const bool ok = y >= 0 && y < V;
+      g_l[t] = ok ? order_key(Logit<DT>::load1(lrow, y)) : neg_inf();
+      g_q[t] = (ok && qrow) ? __ldg(qrow + y) : 0.0f;
+      g_u[t] = __ldg(coins + o + ch);
+    }
+    __syncthreads();
+    int accepted = -1;
+    for (int i = 0; i < nch; ++i) {
+      if (tid == 0) {
+        const float p = prob_of(g_l[i], cT, mc, invz);
+        const float pc = s_A == 0.0f ? p : fmaxf(0.0f, fmaf(-s_A, g_q[i], p)) / s_cj;
+        const float ratio = pc / g_q[i];
+        if (g_q[i] == 0.0f) bump(stats, SPEC_STAT_Q_ZERO);
+        s_accept = g_u[i] < ratio;
+      }
+      __syncthreads();
+      if (s_accept) {
+        accepted = s_ch[i];
+        break;
+      }
+      // rejected: mass of the next residual
+      ResidualWeights<DT> w{lrow, qrow, V, cT, mc, invz, s_A + s_cj};
+      const float total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
+      if (tid == 0) {
+        if (total > 0.0f && isfinite(total)) {
+          s_A = s_A + s_cj;
+          s_cj = total;
+          s_tiles_ok = 1;
+          s_total = total;
+        } else {
+          bump(stats, SPEC_STAT_RESIDUAL_FALLBACK);
+          s_tiles_ok = 0;
+        }
+        ++s_rej;
+      }
+      __syncthreads();
+    }
+    if (accepted >= 0) {
+      if (tid == 0) {
+        const int32_t y = s_dt[accepted];
+        s_com[s_len++] = y;
+        s_path[++s_acc] = accepted;
+        s_n = accepted;
+        if (y == eos || s_len == s_rem || s_len >= N) {
+          s_kind = SPEC_FINAL_ACCEPTED;
+          s_done = 1;
+        }
+      }
+      __syncthreads();
+      continue;
+    }
+    // no child accepted (or a leaf): draw from the current distribution
+    ResidualWeights<DT> w{lrow, qrow, V, cT, mc, invz, s_A};
+    float total;
+    if (s_tiles_ok) {
+      total = s_total;
+    } else {
+      total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
+    }
+    const int32_t tok = cdf_search<kWalkThreads>(w, V, __ldg(u_final + b), tile_sum, total, scan_sh, stats);
+    if (tid == 0) {
+      s_com[s_len++] = tok;
+      s_kind = nch > 0 ? SPEC_FINAL_CORRECTION : SPEC_FINAL_BONUS;
+      s_done = 1;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    num_committed[b] = s_len;
+    accept_length[b] = s_acc;
+    next_root[b] = s_len > 0 ? s_com[s_len - 1] : -1;
+    if (walk_info) {
+      walk_info[3 * b] = s_n;
+      walk_info[3 * b + 1] = s_rej;
+      walk_info[3 * b + 2] = s_kind;
+    }
+  }
+  for (int i = tid; i < N; i += kWalkThreads) {
+    committed[o + i] = s_com[i];
+    accept_path[o + i] = s_path[i];
+  }
+}
+
+struct VerifyWs {
+  int32_t* amax;
+  float* m;
+  float* z;
+};
+
+VerifyWs carve(void* ws, int B, int N) {
+  const size_t rows = static_cast<size_t>(B) * N;
+  char* p = static_cast<char*>(ws);
+  VerifyWs w;
+  w.amax = reinterpret_cast<int32_t*>(p);
+  p += align256(rows * sizeof(int32_t));
+  w.m = reinterpret_cast<float*>(p);
+  p += align256(rows * sizeof(float));
+  w.z = reinterpret_cast<float*>(p);
+  return w;
+}
+
+int check_common(int B, int N, int64_t V, int dtype, const void* target, const int32_t* dtok,
+                 const int32_t* ntok, const int32_t* nsib, int32_t* committed, int32_t* num_committed,
+                 int32_t* accept_length, int32_t* accept_path, int32_t* next_root, void* ws, size_t ws_bytes) {
+  if (B < 0 || N < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (N > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB || static_cast<int64_t>(B) * N > INT_MAX)
+    return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  if (!target || !dtok || !ntok || !nsib || !committed || !num_committed || !accept_length || !accept_path ||
+      !next_root || !ws)
+    return SPEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return SPEC_ERR_INVALID_ARG;
+  if (ws_bytes < spec_verify_ws_size(B, N)) return SPEC_ERR_WORKSPACE;
+  return 1;
+}
+
+}  // namespace
+}  // namespace specdec
+
+using namespace specdec;
+
+extern "C" size_t spec_verify_ws_size(int B, int N) {
+  if (B < 0 || N < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * N;
+  return align256(rows * sizeof(int32_t)) + 2 * align256(rows * sizeof(float));
+}
+
+extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void* target_logits,
+                                  const int32_t* draft_token, const int32_t* retrieve_next_token,
+                                  const int32_t* retrieve_next_sibling, const int32_t* budget_or_null,
+                                  int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                  int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                  int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                  size_t ws_bytes, spec_stream_t stream) {
+  const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
+                              retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
+                              next_root, ws, ws_bytes);
+  if (rc <= 0) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  VerifyWs w = carve(ws, B, N);
+  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
+  if (dtype == SPEC_BF16)
+    row_stats_kernel<SPEC_BF16, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, w.amax, nullptr,
+                                                                     nullptr, stats_or_null);
+  else
+    row_stats_kernel<SPEC_F32, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, w.amax, nullptr,
+                                                                    nullptr, stats_or_null);
+  int e = launch_status();
+  if (e != SPEC_OK) return e;
+  greedy_walk_kernel<<<B, 32, sizeof(int32_t) * 6 * N, s>>>(
+      N, w.amax, draft_token, retrieve_next_token, retrieve_next_sibling, budget_or_null, eos_id, committed,
+      num_committed, accept_length, accept_path, next_root, walk_info_or_null);
+  return launch_status();
+}
+
+extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                  const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                                  const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                  const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                  int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                  int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                  int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                  size_t ws_bytes, spec_stream_t stream) {
+  if (!(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
+  const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
+                              retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
+                              next_root, ws, ws_bytes);
+  if (rc <= 0) return rc;
+  if (!q || !coins || !u_final) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  VerifyWs w = carve(ws, B, N);
+  const float c = kLog2e / T;
+  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
+  const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
+  const size_t smem = sizeof(float) * (ntiles * (1 + kWalkThreads / 32) + 3 * static_cast<int64_t>(N)) +
+                      sizeof(int32_t) * 6 * static_cast<int64_t>(N);
+  if (dtype == SPEC_BF16) {
+    row_stats_kernel<SPEC_BF16, true><<<rows, kStatThreads, 0, s>>>(target_logits, V, c, w.amax, w.m, w.z,
+                                                                    stats_or_null);
+    int e = launch_status();
+    if (e != SPEC_OK) return e;
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<SPEC_BF16>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem)) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    sample_walk_kernel<SPEC_BF16><<<B, kWalkThreads, smem, s>>>(
+        N, V, c, target_logits, w.m, w.z, q, q_row_or_null, draft_token, retrieve_next_token,
+        retrieve_next_sibling, coins, u_final, budget_or_null, eos_id, committed, num_committed, accept_length,
+        accept_path, next_root, walk_info_or_null, stats_or_null);
+  } else {
+    row_stats_kernel<SPEC_F32, true><<<rows, kStatThreads, 0, s>>>(target_logits, V, c, w.amax, w.m, w.z,
+                                                                   stats_or_null);
+    int e = launch_status();
+    if (e != SPEC_OK) return e;
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<SPEC_F32>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem)) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    sample_walk_kernel<SPEC_F32><<<B, kWalkThreads, smem, s>>>(
+        N, V, c, target_logits, w.m, w.z, q, q_row_or_null, draft_token, retrieve_next_token,
+        retrieve_next_sibling, coins, u_final, budget_or_null, eos_id, committed, num_committed, accept_length,
+        accept_path, next_root, walk_info_or_null, stats_or_null);
+  }
+  return launch_status();
+}

@@ -1,0 +1,141 @@
+"""One speculative-decoding step over a batch, composed from the C ABI.
+
+Draft side (one launch pair per draft step), as in "[SGLang] Multi-Layer
+EAGLE" sections 2-3 and "EAGLE speculative decoding in four parts",
+"Drafting, verification and slots":
+  - EAGLE tree:  spec_softmax_topk on the step's draft rows (writing the
+                 draft distribution q into the step-major table when the
+                 verify samples), then spec_tree_expand;
+  - sampled chain: spec_softmax_topk (q) then spec_sample with the step's
+                 uniforms, then spec_tree_expand with k = 1;
+  - TLI chain:   tli_constrain_map (q in target order), then
+                 spec_tree_expand with the mapped top-1 (SGLang PR #22883).
+then spec_build_tree.  Verify: spec_verify_greedy or spec_verify_sample over
+the target logits in node order.  Compaction: spec_compact_slots.
+
+All buffers are allocated once in ``StepBuffers``; a step only enqueues
+kernels on the current stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity, spec_compact_slots,
+               spec_sample, spec_softmax_topk, spec_tree_expand, spec_verify_greedy, spec_verify_sample,
+               spec_verify_ws_size, tli_constrain_map)
+
+
+def step_offsets(B, topk, steps):
+    offs = [0] + [B + (s - 1) * B * topk for s in range(1, steps)]
+    return offs, B + (steps - 1) * B * topk
+
+
+class StepBuffers:
+    """Preallocated device buffers of one step.
+
+    kind: "tree" (EAGLE top-k tree), "chain" (topk 1; drafts by argmax, or
+    sampled when ``sampled``), "tli" (chain with the TLI constraint).
+    """
+
+    def __init__(self, kind, B, topk, steps, N, V, device, want_q, sampled=False, V_t=None, page_size=0,
+                 max_ctx=0):
+        self.kind, self.B, self.topk, self.steps, self.N, self.V = kind, B, topk, steps, N, V
+        self.sampled, self.want_q = sampled, want_q
+        self.Vq = V_t if kind == "tli" else V
+        self.offs, self.rows = step_offsets(B, topk, steps)
+        dev = torch.device(device)
+        self.device = dev
+        self.pool = new_pool(B, topk, steps, dev)
+        kk = topk
+        self.topk_p = [torch.empty((B * (1 if s == 0 else kk), kk), dtype=torch.float32, device=dev)
+                       for s in range(steps)]
+        self.topk_idx = [torch.empty((B * (1 if s == 0 else kk), kk), dtype=torch.int32, device=dev)
+                         for s in range(steps)]
+        self.q = torch.empty((self.rows, self.Vq), dtype=torch.float32, device=dev) if want_q else None
+        self.tok = torch.empty((self.rows,), dtype=torch.int32, device=dev)
+        self.prob = torch.empty((self.rows,), dtype=torch.float32, device=dev)
+        self.top1_draft = torch.empty((self.rows,), dtype=torch.int32, device=dev)
+        self.tree = None
+        self.ws = torch.empty(max(spec_verify_ws_size(B, N), 256), dtype=torch.uint8, device=dev)
+        self.verify_out = None
+        self.stats = new_stats(dev)
+        self.compact_out = None
+        if page_size:
+            cap = spec_compact_freed_capacity(B, N, page_size)
+            self.compact_out = {
+                "move_src": torch.empty((B, N), dtype=torch.int32, device=dev),
+                "move_dst": torch.empty((B, N), dtype=torch.int32, device=dev),
+                "num_moves": torch.empty((B,), dtype=torch.int32, device=dev),
+                "freed": torch.empty((max(cap, 1),), dtype=torch.int32, device=dev),
+                "num_freed": torch.empty((1,), dtype=torch.int32, device=dev),
+                "new_kv_len": torch.empty((B,), dtype=torch.int32, device=dev),
+            }
+        self._alloc_tree()
+
+    def _alloc_tree(self):
+        B, N, dev = self.B, self.N, self.device
+        self.tree = {name: torch.empty((B, N), dtype=torch.int32, device=dev)
+                     for name in ("draft_token", "parent", "positions", "retrieve_index", "retrieve_next_token",
+                                  "retrieve_next_sibling", "q_row")}
+        self.tree["tree_mask"] = torch.empty((B, N, N), dtype=torch.uint8, device=dev)
+        self.verify_out = {
+            "committed": torch.empty((B, N), dtype=torch.int32, device=dev),
+            "num_committed": torch.empty((B,), dtype=torch.int32, device=dev),
+            "accept_length": torch.empty((B,), dtype=torch.int32, device=dev),
+            "accept_path": torch.empty((B, N), dtype=torch.int32, device=dev),
+            "next_root": torch.empty((B,), dtype=torch.int32, device=dev),
+            "walk_info": torch.empty((B, 3), dtype=torch.int32, device=dev),
+        }
+
+
+def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=None, d2t=None, t2d=None):
+    """Draft steps + tree build.  Returns buf.tree."""
+    B, k = buf.B, buf.topk
+    for s in range(buf.steps):
+        r = B * (1 if s == 0 else k)
+        a = buf.offs[s]
+        rows = draft_table[a:a + r]
+        qs = buf.q[a:a + r] if buf.q is not None else None
+        if buf.kind == "tli":
+            tli_constrain_map(rows, d2t, T, t2d=t2d, top1_draft=buf.top1_draft[a:a + r],
+                              top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
+                              stats=buf.stats)
+            spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
+        elif buf.kind == "chain" and buf.sampled:
+            spec_softmax_topk(rows, T, 1, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
+                              stats=buf.stats)
+            spec_sample(draft_u[a:a + r], probs=qs, out_token=buf.tok[a:a + r], out_prob=buf.prob[a:a + r],
+                        stats=buf.stats)
+            spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
+        else:
+            spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
+                              stats=buf.stats)
+            spec_tree_expand(buf.pool, s, buf.topk_p[s], buf.topk_idx[s])
+    spec_build_tree(buf.pool, buf.N, root_token, seq_lens, out=buf.tree)
+    return buf.tree
+
+
+def run_verify(buf: StepBuffers, target, mode, T=1.0, coins=None, u_final=None, budget=None, eos_id=-1):
+    t = buf.tree
+    if mode == "greedy":
+        return spec_verify_greedy(target, t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"],
+                                  budget=budget, eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)
+    return spec_verify_sample(target, T, buf.q, t["draft_token"], t["retrieve_next_token"],
+                              t["retrieve_next_sibling"], coins, u_final, q_row=t["q_row"], budget=budget,
+                              eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)
+
+
+def run_compact(buf: StepBuffers, seq_lens, req_to_token, page_size, kv_pool=None):
+    v = buf.verify_out
+    return spec_compact_slots(seq_lens, v["accept_path"], v["accept_length"], req_to_token, page_size,
+                              kv_pool=kv_pool, out=buf.compact_out, stats=buf.stats)
+
+
+def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> int:
+    """Number of kernel launches one step enqueues."""
+    per_step = 3 if (buf.kind == "chain" and buf.sampled) else 2
+    n = buf.steps * per_step + 1  # + build_tree
+    n += 2  # verify: row pass + walk
+    if compact:
+        n += 1 + (1 if (kv_pool and buf.compact_out is not None) else 0)
+    return n

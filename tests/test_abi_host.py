@@ -1,0 +1,67 @@
+"""The C-ABI library loads and exports every entry point include/specdec.h
+declares; argument checks that run on the host return their error codes
+without enqueuing anything.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_draft_select_gb300 as sd
+from speculative_decoding_draft_select_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "specdec.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|int64_t|size_t)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return sd.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(sd._SIGS) >= set(names)
+
+
+def test_host_side_argument_checks(lib):
+    null = None
+    # k > V, T <= 0, bad dtype, null pointers
+    assert lib.spec_softmax_topk(null, 1, 4, 3, 1.0, 4, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 0.0, 2, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 1.0, 2, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(ctypes.c_void_p(16), 7, 4, 8, 1.0, 2, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                 null, null, null) == -2
+    assert lib.spec_softmax_topk(ctypes.c_void_p(16), 1, 4, 100, 1.0, 33, ctypes.c_void_p(16),
+                                 ctypes.c_void_p(16), null, null, null) == -2  # k above the limit
+    # empty batches are no-ops
+    assert lib.spec_softmax_topk(null, 1, 0, 8, 1.0, 2, null, null, null, null, null) == 0
+    assert lib.spec_tree_expand(0, 2, 4, 0, null, null, null, null, null, null, null, null, null) == -1
+    assert lib.spec_tree_expand(2, 2, 4, 2, null, null, null, null, null, null, null, null, null) == -1
+    assert lib.spec_build_tree(1, 2, 2, 8, *([null] * 15)) == -1  # N > P = 7
+    assert lib.spec_verify_greedy(2, 4, 10, 1, *([null] * 5), -1, *([null] * 8), 0, null) == -1
+    assert lib.spec_verify_sample(2, 4, 10, 1, null, 0.0, *([null] * 8), -1, *([null] * 8), 0, null) == -1
+    assert lib.spec_compact_slots(2, 4, 0, *([null] * 4), 16, *([null] * 4), 0, *([null] * 3), 0, 0, null,
+                                  null) == -1
+    assert lib.tli_constrain_map(4, 10, 10, null, 1, null, null, 1.0, null, null, null, null, null, null) == -1
+    assert lib.tli_map_ids(null, null, -1, null, 0, 0, null) == -1
+
+
+def test_sizes_and_config_check(lib):
+    assert sd.spec_tree_pool_size(8, 6) == 1 + 8 + 5 * 64
+    assert sd.spec_tree_pool_size(4, 3) == 37
+    assert sd.spec_verify_ws_size(128, 64) >= 128 * 64 * 12
+    assert sd.spec_compact_freed_capacity(128, 64, 16) == 128 * 5
+    assert sd.spec_compact_freed_capacity(4, 16, 1) == 60
+    assert sd.tli_check_config(1, 4, 5)
+    assert not sd.tli_check_config(2, 4, 5)
+    assert not sd.tli_check_config(1, 4, 4)

@@ -1,0 +1,423 @@
+"""CUDA path vs the CPU oracle on the same seeded inputs, through the C ABI.
+
+Bars: integer outputs (indices, tokens, tree fields, accept lengths and
+paths, compacted slots) bit-exact; probabilities within 1e-5 absolute; a
+sampled token or acceptance decision may differ only where the oracle's
+uniform lies within 1e-5 of the decision boundary (counted)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_draft_select_gb300 as sd
+from speculative_decoding_draft_select_gb300.pipeline import StepBuffers, run_draft, run_verify
+from workloads import CONFIGS, assemble_target, generate
+
+from oracle.pipeline import fetch_request, np_logits, run_request
+
+pytestmark = pytest.mark.gpu
+
+PROB_TOL = 1e-5
+BOUNDARY = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_draft_select_gb300.build import build
+    build()
+    sd.lib()
+
+
+def dev(x, dtype=None):
+    t = torch.as_tensor(x)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda().contiguous()
+
+
+def make_logits(rng, R, V, dtype, std=3.0):
+    x = rng.normal(0, std, (R, V)).astype(np.float32)
+    t = torch.from_numpy(x).to(dtype)
+    return t
+
+
+# ------------------------------------------------------------ softmax/top-k
+
+CASES = [(7, 1, 1), (5, 7, 3), (9, 33, 4), (4, 4095, 8), (3, 4097, 8), (6, 32000, 4), (2, 128256, 8),
+         (3, 1000, 16), (2, 3000, 32), (300, 200, 2)]
+
+
+@pytest.mark.parametrize("R,V,k", CASES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_softmax_topk_parity(R, V, k, dtype, T):
+    rng = np.random.default_rng(R * 1000 + V + k)
+    x = make_logits(rng, R, V, dtype)
+    if V >= 8:
+        x[0, 3] = x[0, 5] = x[0].max() + 1  # tie at the max: lower index first
+        x[min(1, R - 1), 2] = float("-inf")
+    if R > 2 and V >= 4:
+        x[2, 1] = float("nan")
+    topk_p, topk_idx, probs = sd.spec_softmax_topk(dev(x), T, k, want_probs=True)
+    torch.cuda.synchronize()
+    op, oi, oprobs, oflag = oracle.softmax_topk(np_logits(x), T, k, want_probs=True)
+    np.testing.assert_array_equal(topk_idx.cpu().numpy(), oi)
+    np.testing.assert_allclose(topk_p.cpu().numpy(), op, rtol=0, atol=PROB_TOL)
+    np.testing.assert_allclose(probs.cpu().numpy(), oprobs, rtol=0, atol=PROB_TOL)
+
+
+def test_softmax_topk_nonfinite_rows_flagged():
+    x = torch.full((3, 50), float("-inf"))
+    x[1, 7] = float("inf")
+    x[2] = torch.randn(50)
+    stats = sd.new_stats()
+    tp, ti, pr = sd.spec_softmax_topk(dev(x), 1.0, 2, want_probs=True, stats=stats)
+    torch.cuda.synchronize()
+    assert int(stats[sd.STATS["nonfinite_row"]]) == 2
+    assert torch.all(pr[:2] == 0) and torch.all(tp[:2] == 0)
+    _, oi, _, _ = oracle.softmax_topk(np_logits(x), 1.0, 2)
+    np.testing.assert_array_equal(ti.cpu().numpy(), oi)
+
+
+# ---------------------------------------------------------------- sampling
+
+@pytest.mark.parametrize("V", [1, 7, 33, 4097, 32000])
+@pytest.mark.parametrize("use_probs", [True, False])
+def test_sample_parity(V, use_probs):
+    rng = np.random.default_rng(V)
+    R = 64
+    x = make_logits(rng, R, V, torch.bfloat16)
+    u = rng.random(R).astype(np.float32)
+    u[:3] = [0.0, 0.5, np.nextafter(np.float32(1), np.float32(0))]
+    if use_probs:
+        _, _, probs, _ = oracle.softmax_topk(np_logits(x), 0.8, 1, want_probs=True)
+        probs = probs.astype(np.float32)
+        tok, prob = sd.spec_sample(dev(u), probs=dev(probs))
+        otok, oprob, margin, _ = oracle.sample(u, probs=probs)
+    else:
+        tok, prob = sd.spec_sample(dev(u), logits=dev(x), T=0.8)
+        otok, oprob, margin, _ = oracle.sample(u, logits=np_logits(x), T=0.8)
+    torch.cuda.synchronize()
+    tok, prob = tok.cpu().numpy(), prob.cpu().numpy()
+    clear = margin >= BOUNDARY
+    np.testing.assert_array_equal(tok[clear], otok[clear])
+    np.testing.assert_allclose(prob[clear], oprob[clear], atol=PROB_TOL)
+    assert clear.sum() >= R - 2
+
+
+# -------------------------------------------------------------------- tree
+
+def oracle_topk_inputs(rng, B, k, steps, ties=False):
+    out = []
+    for s in range(steps):
+        rows = B * (1 if s == 0 else k)
+        p = np.sort(rng.uniform(0.001, 1.0, (rows, k)).astype(np.float32), axis=1)[:, ::-1].copy()
+        p /= np.float32(k)
+        if ties:
+            p[::3, 1:] = p[::3, :1]  # equal probabilities inside a row
+            p = np.round(p * 64) / 64  # many equal products across rows
+        idx = np.stack([rng.choice(50000, k, replace=False) for _ in range(rows)]).astype(np.int32)
+        out.append((np.ascontiguousarray(p, np.float32), idx))
+    return out
+
+
+@pytest.mark.parametrize("B,k,steps,N,ties", [(4, 1, 6, 7, False), (64, 4, 5, 16, False), (16, 8, 6, 64, False),
+                                              (8, 3, 4, 2, True), (8, 4, 5, 16, True), (3, 2, 3, 11, True),
+                                              (2, 16, 3, 200, False)])
+def test_tree_parity(B, k, steps, N, ties):
+    rng = np.random.default_rng(B * 7 + k + N)
+    inputs = oracle_topk_inputs(rng, B, k, steps, ties)
+    opool = oracle.Pool(B, k, steps)
+    gpool = sd.new_pool(B, k, steps)
+    for s, (p, idx) in enumerate(inputs):
+        oracle.tree_expand(opool, s, p, idx)
+        sd.spec_tree_expand(gpool, s, dev(p), dev(idx))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(gpool["frontier_id"].cpu().numpy(), opool.frontier_id)
+        np.testing.assert_array_equal(gpool["frontier_score"].cpu().numpy(), opool.frontier_score)
+    for name, arr in (("score", opool.score), ("token", opool.token), ("parent", opool.parent),
+                      ("qrow", opool.qrow)):
+        np.testing.assert_array_equal(gpool[name].cpu().numpy(), arr, err_msg=name)
+    root = rng.integers(0, 1000, B).astype(np.int32)
+    seq = rng.integers(16, 2048, B).astype(np.int32)
+    gt = sd.spec_build_tree(gpool, N, dev(root), dev(seq))
+    ot = oracle.build_tree(opool, N, root, seq)
+    torch.cuda.synchronize()
+    for name in ot:
+        np.testing.assert_array_equal(gt[name].cpu().numpy(), ot[name], err_msg=name)
+
+
+# ------------------------------------------------------------------ verify
+
+def verify_compare(g, o, b_g, b_o=0, mode="greedy"):
+    """Returns True when compared exactly, False when skipped as a boundary case."""
+    if mode == "sample" and o["margin"][b_o] < BOUNDARY:
+        return False
+    for name in ("committed", "num_committed", "accept_length", "accept_path", "next_root", "walk_info"):
+        gv = g[name][b_g].cpu().numpy()
+        np.testing.assert_array_equal(gv, o[name][b_o], err_msg=f"{name} request {b_g}")
+    return True
+
+
+def chain_meta(B, N):
+    nt = np.tile(np.array([n + 1 if n + 1 < N else -1 for n in range(N)], np.int32), (B, 1))
+    return nt, np.full((B, N), -1, np.int32)
+
+
+@pytest.mark.parametrize("V,dtype", [(1000, torch.bfloat16), (4097, torch.bfloat16), (33, torch.float32)])
+def test_verify_greedy_chain_eos_budget(V, dtype):
+    rng = np.random.default_rng(V)
+    B, N = 96, 16
+    target = make_logits(rng, B * N, V, dtype).view(B, N, V)
+    eos = 5
+    # make drafts agree with the target argmax often, plant EOS rows
+    am = target.float().argmax(-1).numpy()
+    draft = np.where(rng.random((B, N)) < 0.8, np.roll(am, 1, axis=1), rng.integers(0, V, (B, N))).astype(np.int32)
+    plant = torch.from_numpy(rng.random((B, N)) < 1 / 8)
+    tf = target.float()
+    tf[plant, eos] = 50.0
+    target = tf.to(dtype)
+    budget = rng.integers(0, 20, B).astype(np.int32)
+    budget[0] = 0
+    nt, ns = chain_meta(B, N)
+    g = sd.spec_verify_greedy(dev(target), dev(draft), dev(nt), dev(ns), budget=dev(budget), eos_id=eos)
+    o = oracle.verify_greedy(np_logits(target), draft, nt, ns, budget=budget, eos=eos)
+    torch.cuda.synchronize()
+    for b in range(B):
+        for name in ("committed", "num_committed", "accept_length", "accept_path", "next_root", "walk_info"):
+            np.testing.assert_array_equal(g[name][b].cpu().numpy(), o[name][b], err_msg=f"{name} {b}")
+    assert (o["accept_length"] > 2).any()
+
+
+def small(cfg_name, **kw):
+    return CONFIGS[cfg_name].scaled(**kw)
+
+
+def run_gpu_pipeline(cfg, work, mode):
+    buf = StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, "cuda", want_q=(mode == "sample"),
+                      sampled=(cfg.kind == "chain" and mode == "sample"), V_t=cfg.V_t or None)
+    tree = run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"],
+                     draft_u=work["draft_u"], d2t=work.get("d2t"), t2d=work.get("t2d"))
+    target = assemble_target(work, tree["q_row"])
+    out = run_verify(buf, target, mode, cfg.T, work["coins"], work["u_final"], work.get("budget"),
+                     int(work["eos_id"]))
+    torch.cuda.synchronize()
+    return buf, tree, out
+
+
+def compare_pipeline(cfg, work, mode, reqs):
+    buf, tree, out = run_gpu_pipeline(cfg, work, mode)
+    exact = boundary = 0
+    for b in reqs:
+        ot, q, target, o, _ = run_request(cfg, fetch_request(cfg, work, b), mode)
+        for name in ("draft_token", "parent", "positions", "tree_mask", "retrieve_index", "retrieve_next_token",
+                     "retrieve_next_sibling", "q_row"):
+            gv = tree[name][b].cpu().numpy()
+            ov = ot[name][0]
+            if name == "retrieve_index":
+                ov = ov + b * cfg.N
+            np.testing.assert_array_equal(gv, ov, err_msg=f"{cfg.name} {name} request {b}")
+        if verify_compare(out, o, b, 0, mode):
+            exact += 1
+        else:
+            boundary += 1
+    return exact, boundary, out
+
+
+SMALL = {
+    "c1": dict(),
+    "c2": dict(B=12, V=4097),
+    "c3": dict(B=6, V=4097, page_size=0, bytes_per_slot=0),
+    "c4": dict(B=16, V=6001, V_t=5003, K=2500),
+    "c5": dict(B=48, V=3001),
+}
+
+
+@pytest.mark.parametrize("name,mode", [("c1", "greedy"), ("c1", "sample"), ("c2", "greedy"), ("c3", "sample"),
+                                       ("c4", "sample"), ("c5", "greedy"), ("c5", "sample")])
+def test_pipeline_small(name, mode):
+    cfg = small(name, **SMALL[name])
+    work = generate(cfg, "cuda")
+    exact, boundary, _ = compare_pipeline(cfg, work, mode, range(cfg.B))
+    assert exact >= cfg.B - 1, (exact, boundary)
+
+
+@pytest.mark.parametrize("name,mode", [("c2", "greedy"), ("c3", "sample"), ("c4", "sample"), ("c5", "greedy"),
+                                       ("c5", "sample")])
+def test_pipeline_full_size_sampled_requests(name, mode):
+    """Full-size workloads in the bench's launch configuration; the oracle
+    recomputes a few requests one by one."""
+    cfg = CONFIGS[name].scaled(page_size=0, bytes_per_slot=0)
+    work = generate(cfg, "cuda")
+    reqs = [0, cfg.B // 2, cfg.B - 1]
+    exact, boundary, out = compare_pipeline(cfg, work, mode, reqs)
+    assert exact >= len(reqs) - 1, (exact, boundary)
+    al = out["accept_length"].float().mean().item()
+    assert 0.0 <= al < cfg.N
+
+
+def test_verify_sample_tree_given_q_node_order():
+    """Stochastic tree verify with q in node order (q_row = NULL) on oracle
+    trees, including q[y] == 0 children and zero-mass target entries."""
+    rng = np.random.default_rng(77)
+    B, k, steps, N, V = 24, 3, 4, 12, 257
+    opool = oracle.Pool(B, k, steps)
+    for s, (p, idx) in enumerate(oracle_topk_inputs(rng, B, k, steps)):
+        oracle.tree_expand(opool, s, p, np.ascontiguousarray(idx % V, np.int32))
+    t = oracle.build_tree(opool, N, rng.integers(0, V, B).astype(np.int32), np.zeros(B, np.int32))
+    target = make_logits(rng, B * N, V, torch.float32, std=2.0).view(B, N, V)
+    target[:, :, :5] = float("-inf")
+    _, _, q, _ = oracle.softmax_topk(np_logits(target + torch.randn(B, N, V) * 0.7), 1.0, 1, want_probs=True)
+    q = q.astype(np.float32).reshape(B, N, V)
+    dt = t["draft_token"]
+    q[np.arange(B)[:, None], t["parent"].clip(0), dt] *= (rng.random((B, N)) > 0.1)  # some q[y] = 0
+    coins = rng.random((B, N)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    stats = sd.new_stats()
+    g = sd.spec_verify_sample(dev(target), 1.0, dev(q), dev(dt), dev(t["retrieve_next_token"]),
+                              dev(t["retrieve_next_sibling"]), dev(coins), dev(uf), stats=stats)
+    o = oracle.verify_sample(np_logits(target), 1.0, q, dt, t["retrieve_next_token"], t["retrieve_next_sibling"],
+                             coins, uf)
+    torch.cuda.synchronize()
+    exact = sum(verify_compare(g, o, b, b, "sample") for b in range(B))
+    assert exact >= B - 1
+    assert int(stats[sd.STATS["q_zero"]]) == o["q_zero"]
+
+
+def test_worked_example_monte_carlo_gpu(golden):
+    """p=[0.4,0.6], q=[0.8,0.2]: the committed token is 0 with probability
+    exactly 0.4 (zero-to-sglang ch.10, section 5.1)."""
+    g = golden("stochastic_worked_example.json")
+    n = g["monte_carlo"]["trials"]
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    B, N, V = n, 2, 2
+    target = torch.log(torch.tensor([0.4, 0.6], device="cuda")).expand(B, N, V).contiguous()
+    q = torch.tensor([0.8, 0.2], device="cuda").expand(B, N, V).contiguous()
+    y = (torch.rand(B, generator=gen, device="cuda") >= 0.8).int()
+    draft = torch.stack([torch.zeros_like(y), y], 1).contiguous()
+    nt = torch.tensor([1, -1], dtype=torch.int32, device="cuda").expand(B, 2).contiguous()
+    ns = torch.full((B, 2), -1, dtype=torch.int32, device="cuda")
+    coins = torch.rand((B, N), generator=gen, device="cuda")
+    uf = torch.rand((B,), generator=gen, device="cuda")
+    out = sd.spec_verify_sample(target, 1.0, q, draft, nt, ns, coins, uf)
+    f0 = (out["committed"][:, 0] == 0).float().mean().item()
+    sigma = math.sqrt(0.4 * 0.6 / n)
+    assert abs(f0 - 0.4) < g["monte_carlo"]["sigma_bound"] * sigma
+    assert abs(f0 - 0.56) > 100 * sigma
+
+
+# -------------------------------------------------------------- compaction
+
+@pytest.mark.parametrize("ps,with_kv", [(1, False), (16, True), (16, False), (4, True)])
+def test_compact_parity(ps, with_kv):
+    cfg = CONFIGS["c3"].scaled(page_size=ps, bytes_per_slot=4096 if with_kv else 0)
+    if ps != 16:
+        cfg = cfg.scaled(B=40)
+    work = generate(cfg, "cuda")
+    rng = np.random.default_rng(ps)
+    B, N = cfg.B, cfg.N
+    acc = rng.integers(0, N, B).astype(np.int32)
+    acc[:3] = [0, N - 1, 2]
+    path = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        path[b, :acc[b] + 1] = [0] + sorted(rng.choice(np.arange(1, N), acc[b], replace=False))
+    path[2, :3] = [0, 2, 3]  # the race case
+    path[1] = np.arange(N)
+    seq = work["seq_lens"].cpu().numpy()
+    rt_o = work["req_to_token"].cpu().numpy().copy()
+    kv_o = work["kv_pool"].cpu().numpy().copy() if with_kv else None
+    o = oracle.compact_slots(seq, path, acc, rt_o, ps, kv_pool=kv_o)
+    rt_g = work["req_to_token"].clone()
+    kv_g = work["kv_pool"] if with_kv else None
+    stats = sd.new_stats()
+    g = sd.spec_compact_slots(work["seq_lens"], dev(path), dev(acc), rt_g, ps, kv_pool=kv_g, stats=stats)
+    torch.cuda.synchronize()
+    for name in ("move_src", "move_dst", "num_moves", "new_kv_len"):
+        np.testing.assert_array_equal(g[name].cpu().numpy(), o[name], err_msg=name)
+    nf = int(g["num_freed"].item())
+    assert nf == len(o["freed"])
+    np.testing.assert_array_equal(g["freed"][:nf].cpu().numpy(), o["freed"])
+    np.testing.assert_array_equal(rt_g.cpu().numpy(), rt_o)
+    if with_kv:
+        assert np.array_equal(kv_g.cpu().numpy(), kv_o)
+    assert int(stats[sd.STATS["bad_request"]]) == int(o["bad"][0])
+
+
+# --------------------------------------------------------------------- TLI
+
+@pytest.mark.parametrize("Vd,Vt,K,dtype", [(4097, 3001, 1500, torch.bfloat16), (151936, 128256, 60000, torch.bfloat16),
+                                           (37, 29, 11, torch.float32)])
+def test_tli_parity(Vd, Vt, K, dtype):
+    rng = np.random.default_rng(Vd)
+    dids = np.sort(rng.choice(Vd, K, replace=False))
+    tids = rng.choice(Vt, K, replace=False)
+    d2t = np.full(Vd, -1, np.int32)
+    d2t[dids] = tids
+    t2d = np.full(Vt, -1, np.int32)
+    t2d[tids] = dids
+    R = 24
+    x = make_logits(rng, R, Vd, dtype)
+    x[3, torch.from_numpy(dids)] = float("-inf")  # empty after masking
+    x[4, int(dids[2])] = x[4, int(dids[5])] = 40.0  # tie inside the intersection
+    stats = sd.new_stats()
+    td, tt, tp, qt = sd.tli_constrain_map(dev(x), dev(d2t), 0.9, t2d=dev(t2d), want_q=True, stats=stats)
+    torch.cuda.synchronize()
+    o = oracle.tli_constrain_map(np_logits(x), d2t, t2d, 0.9, want_q=True)
+    np.testing.assert_array_equal(td.cpu().numpy(), o["top1_draft"])
+    np.testing.assert_array_equal(tt.cpu().numpy(), o["top1_target"])
+    np.testing.assert_allclose(tp.cpu().numpy(), o["top1_p"], atol=PROB_TOL)
+    np.testing.assert_allclose(qt.cpu().numpy(), o["q_target"], atol=PROB_TOL)
+    assert int(stats[sd.STATS["empty_intersection"]]) == int(o["row_flag"].sum()) == 1
+    ids = np.concatenate([dids[:100], np.setdiff1d(np.arange(Vd), dids)[:50], [-3, Vd, Vd + 9]]).astype(np.int32)
+    g = sd.tli_map_ids(dev(ids), dev(d2t), 7)
+    np.testing.assert_array_equal(g.cpu().numpy(), oracle.map_ids(ids, d2t, 7))
+    back = sd.tli_map_ids(sd.tli_map_ids(dev(dids.astype(np.int32)), dev(d2t), -1), dev(t2d), -1)
+    np.testing.assert_array_equal(back.cpu().numpy(), dids)
+
+
+# ------------------------------------------------------- toy LM end to end
+
+def test_greedy_spec_decoding_on_gpu_equals_argmax_decoding():
+    """Rounds of draft tree -> verify on the GPU reproduce plain argmax
+    decoding of the target (zero-to-sglang ch.10, 4.2: every committed token
+    is the target's choice on the committed prefix)."""
+    rng = np.random.default_rng(12)
+    V, k, S, N = 40, 3, 3, 8
+    tab = torch.from_numpy(rng.normal(0, 2, (V * V, V)).astype(np.float32))
+    dtab = tab + torch.from_numpy(rng.normal(0, 0.8, tab.shape).astype(np.float32))
+    tab_g, dtab_g = tab.cuda(), dtab.cuda()
+    ctx = [3, 17]
+    ref = list(ctx)
+    for _ in range(50):
+        ref.append(int(torch.argmax(tab[ref[-2] * V + ref[-1]])))
+    out = list(ctx)
+    while len(out) < len(ref):
+        pool = sd.new_pool(1, k, S)
+        pctx = {0: tuple(out)}
+        rows = dtab_g[[pctx[0][-2] * V + pctx[0][-1]]]
+        for s in range(S):
+            tp, ti, _ = sd.spec_softmax_topk(rows.contiguous(), 1.0, k)
+            sd.spec_tree_expand(pool, s, tp, ti)
+            tok = pool["token"][0].cpu().numpy()
+            par = pool["parent"][0].cpu().numpy()
+            lo = 1 if s == 0 else 1 + k + (s - 1) * k * k
+            hi = 1 + k if s == 0 else lo + k * k
+            for pid in range(lo, hi):
+                pctx[pid] = pctx[int(par[pid])] + (int(tok[pid]),)
+            fr = pool["frontier_id"][0].cpu().numpy()
+            rows = dtab_g[[pctx[int(f)][-2] * V + pctx[int(f)][-1] for f in fr]]
+        t = sd.spec_build_tree(pool, N, dev(np.array([out[-1]], np.int32)), dev(np.array([len(out)], np.int32)))
+        par = t["parent"][0].cpu().numpy()
+        dtk = t["draft_token"][0].cpu().numpy()
+        nctx = [tuple(out)]
+        for n in range(1, N):
+            nctx.append(nctx[par[n]] + (int(dtk[n]),))
+        target = torch.stack([tab_g[c[-2] * V + c[-1]] for c in nctx])[None].contiguous()
+        v = sd.spec_verify_greedy(target, t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"])
+        nc = int(v["num_committed"][0])
+        out += v["committed"][0, :nc].cpu().tolist()
+    assert out[:len(ref)] == ref
