@@ -103,10 +103,13 @@ def test_sample_parity(V, use_probs):
         otok, oprob, margin, _ = oracle.sample(u, logits=np_logits(x), T=0.8)
     torch.cuda.synchronize()
     tok, prob = tok.cpu().numpy(), prob.cpu().numpy()
-    clear = margin >= BOUNDARY
-    np.testing.assert_array_equal(tok[clear], otok[clear])
-    np.testing.assert_allclose(prob[clear], oprob[clear], atol=PROB_TOL)
-    assert clear.sum() >= R - 2
+    # a token may differ only where u is within 1e-5 of a CDF boundary, and
+    # such differences are rare (fp32 vs fp64 rounding of the prefix sums)
+    diff = tok != otok
+    assert not (diff & (margin >= BOUNDARY)).any()
+    assert diff.sum() <= 1
+    same = ~diff
+    np.testing.assert_allclose(prob[same], oprob[same], atol=PROB_TOL)
 
 
 # -------------------------------------------------------------------- tree
@@ -154,12 +157,16 @@ def test_tree_parity(B, k, steps, N, ties):
 # ------------------------------------------------------------------ verify
 
 def verify_compare(g, o, b_g, b_o=0, mode="greedy"):
-    """Returns True when compared exactly, False when skipped as a boundary case."""
+    """True when every output matches the oracle; False for a difference the
+    tolerance allows (stochastic mode, the oracle's uniform within 1e-5 of a
+    decision boundary); raises otherwise."""
+    names = ("committed", "num_committed", "accept_length", "accept_path", "next_root", "walk_info")
+    if all(np.array_equal(g[n][b_g].cpu().numpy(), o[n][b_o]) for n in names):
+        return True
     if mode == "sample" and o["margin"][b_o] < BOUNDARY:
         return False
-    for name in ("committed", "num_committed", "accept_length", "accept_path", "next_root", "walk_info"):
-        gv = g[name][b_g].cpu().numpy()
-        np.testing.assert_array_equal(gv, o[name][b_o], err_msg=f"{name} request {b_g}")
+    for n in names:
+        np.testing.assert_array_equal(g[n][b_g].cpu().numpy(), o[n][b_o], err_msg=f"{n} request {b_g}")
     return True
 
 
