@@ -222,6 +222,31 @@ int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_lo
                        int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
                        size_t ws_bytes, spec_stream_t stream);
 
+/* Greedy verify without caller scratch.  No passage of the pages has a
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory at all -- a plugin that receives only its input and output
+ * buffers from a host framework that owns every byte of device memory, or a
+ * real-time path that must not call cudaMalloc (which can block and
+ * synchronise the device).  It behaves exactly like spec_verify_greedy
+ * (same arguments, minus ws / ws_bytes), but keeps the per-row argmax in a
+ * fixed array of device memory inside the library.  That array holds
+ * SPEC_NOALLOC_MAX_ROWS rows (1 MiB), every GPU that loads the library keeps
+ * it until the process exits, and calls with B*N above it return
+ * SPEC_ERR_UNSUPPORTED.  The array is shared: calls whose work overlaps on
+ * the GPU (different streams, no ordering between them) race on it and give
+ * undefined results; calls ordered on one stream are safe.  The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress),
+ * so make that first call before any stream capture.  Nothing is allocated,
+ * by this call or by the library. */
+#define SPEC_NOALLOC_MAX_ROWS (1 << 18)
+int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, const void* target_logits,
+                               const int32_t* draft_token, const int32_t* retrieve_next_token,
+                               const int32_t* retrieve_next_sibling, const int32_t* budget_or_null,
+                               int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                               int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                               int32_t* walk_info_or_null, int32_t* stats_or_null,
+                               spec_stream_t stream);
+
 /* ------------------------------------------------------------- compaction */
 
 /* Capacity (entries) the freed list of spec_compact_slots needs. */

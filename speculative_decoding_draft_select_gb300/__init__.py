@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "SpecError", "F32", "BF16", "STATS", "lib", "library_path",
     "spec_softmax_topk", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
-    "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_sample", "spec_compact_freed_capacity",
+    "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_map_ids", "tli_check_config",
     "new_stats", "new_pool",
 ]
@@ -54,6 +54,8 @@ _SIGS = {
     "spec_compact_slots": (_I, [_I, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, _I64,
                                 _I64, _P, _P]),
     "tli_constrain_map": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _F, _P, _P, _P, _P, _P, _P]),
+    "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                        _P]),
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
     "tli_check_config": (_I, [_I, _I, _I]),
 }
@@ -251,6 +253,27 @@ def spec_verify_greedy(target, draft_token, next_token, next_sibling, budget=Non
           _ptr(next_sibling), _ptr(budget), int(eos_id), _ptr(out["committed"]), _ptr(out["num_committed"]),
           _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]), _ptr(out.get("walk_info")),
           _ptr(stats), _ptr(ws), ws.numel(), _stream())
+    return out
+
+
+def spec_verify_greedy_noalloc(target, draft_token, next_token, next_sibling, budget=None, eos_id=-1, out=None,
+                               stats=None):
+    """Greedy verify for callers that cannot allocate device scratch: the
+    library keeps the per-row argmax in its own fixed 1 MiB device array
+    (B*N <= 262144 rows).  Outputs are still the caller's tensors (allocated
+    here only when not passed).  Calls that overlap on the GPU race on the
+    shared array."""
+    _dev(target, name="target")
+    B, N, V = target.shape
+    for name, t in (("draft_token", draft_token), ("next_token", next_token), ("next_sibling", next_sibling)):
+        _dev(t, torch.int32, name)
+    _dev(budget, torch.int32, "budget")
+    _dev(stats, torch.int32, "stats")
+    out = _verify_outputs(B, N, target.device, out)
+    _call("spec_verify_greedy_noalloc", B, N, V, _logit_code(target), _ptr(target), _ptr(draft_token),
+          _ptr(next_token), _ptr(next_sibling), _ptr(budget), int(eos_id), _ptr(out["committed"]),
+          _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]),
+          _ptr(out.get("walk_info")), _ptr(stats), _stream())
     return out
 
 

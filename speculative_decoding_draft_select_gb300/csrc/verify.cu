@@ -486,3 +486,74 @@ extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void
   }
   return launch_status();
 }
+
+// ------------------------------------------------- greedy verify, no scratch
+//
+// For callers that cannot allocate: the per-row argmax lives in this fixed
+// array (SPEC_NOALLOC_MAX_ROWS entries) instead of caller scratch.  Host code
+// may not use the array's name as a device pointer; its device address is
+// looked up once per device with cudaGetSymbolAddress and cached.
+#include <atomic>
+#include <mutex>
+
+namespace specdec {
+namespace {
+
+__device__ __align__(256) int32_t g_noalloc_argmax[SPEC_NOALLOC_MAX_ROWS];
+
+constexpr int kMaxDevices = 64;
+std::atomic<int32_t*> g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_argmax on the current device (nullptr on error).
+int32_t* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int32_t* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_argmax) != cudaSuccess || addr == nullptr) return nullptr;
+    p = static_cast<int32_t*>(addr);
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, const void* target_logits,
+                                          const int32_t* draft_token, const int32_t* retrieve_next_token,
+                                          const int32_t* retrieve_next_sibling, const int32_t* budget_or_null,
+                                          int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                          int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                          int32_t* walk_info_or_null, int32_t* stats_or_null,
+                                          spec_stream_t stream) {
+  if (B < 0 || N < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (N > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB || static_cast<int64_t>(B) * N > SPEC_NOALLOC_MAX_ROWS)
+    return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !draft_token || !retrieve_next_token || !retrieve_next_sibling || !committed ||
+      !num_committed || !accept_length || !accept_path || !next_root)
+    return SPEC_ERR_INVALID_ARG;
+  int32_t* amax = noalloc_scratch();
+  if (amax == nullptr) return SPEC_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
+  if (dtype == SPEC_BF16)
+    row_stats_kernel<SPEC_BF16, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, amax, nullptr,
+                                                                     nullptr, stats_or_null);
+  else
+    row_stats_kernel<SPEC_F32, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, amax, nullptr,
+                                                                    nullptr, stats_or_null);
+  int e = launch_status();
+  if (e != SPEC_OK) return e;
+  greedy_walk_kernel<<<B, 32, sizeof(int32_t) * 6 * N, s>>>(
+      N, amax, draft_token, retrieve_next_token, retrieve_next_sibling, budget_or_null, eos_id, committed,
+      num_committed, accept_length, accept_path, next_root, walk_info_or_null);
+  return launch_status();
+}
