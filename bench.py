@@ -152,59 +152,42 @@ def run_ours(args, cfg, mode, rank, world):
     work = generate(cfg, dev)
     compact = bool(cfg.page_size)
     sampled = cfg.kind == "chain" and mode == "sample"
+    q_mode = args.q or ("probs" if cfg.kind == "tli" else "logits")
     buf = pl.StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, dev, want_q=(mode == "sample"),
-                         sampled=sampled, V_t=cfg.V_t or None, page_size=cfg.page_size)
+                         sampled=sampled, V_t=cfg.V_t or None, page_size=cfg.page_size, q_mode=q_mode)
     eos = int(work["eos_id"])
     kv = work.get("kv_pool")
     # the target model's output for this tree (deterministic draft -> same tree every step)
     pl.run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], draft_u=work["draft_u"],
                  d2t=work.get("d2t"), t2d=work.get("t2d"))
     target = assemble_target(work, buf.tree["q_row"]).contiguous()
-    Vq = cfg.V_t if cfg.kind == "tli" else cfg.V
     row_bytes = cfg.V * (2 if cfg.dtype == torch.bfloat16 else 4)
 
     stream = torch.cuda.current_stream()
     dom_events = []
 
+    class Timer:
+        """CUDA events around the draft steps' softmax/top-k (or TLI) launches
+        with R = B*topk rows (steps >= 1), on the launching stream."""
+        record = False
+
+        def begin(self, s):
+            self.ev = None
+            if self.record and s >= 1:
+                self.ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                self.ev[0].record(stream)
+
+        def end(self, s):
+            if self.ev is not None:
+                self.ev[1].record(stream)
+                dom_events.append((self.ev, cfg.B * cfg.topk))
+
+    timer = Timer()
+
     def step(record):
-        # draft side, with events around each big draft-step kernel
-        k = cfg.topk
-        for s in range(cfg.steps):
-            r = cfg.B * (1 if s == 0 else k)
-            a = buf.offs[s]
-            rows = work["draft_table"][a:a + r]
-            qs = buf.q[a:a + r] if buf.q is not None else None
-            ev = None
-            if record and s >= 1 and cfg.kind != "tli":
-                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                ev[0].record(stream)
-            if cfg.kind == "tli":
-                if record and s >= 1:
-                    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    ev[0].record(stream)
-                sd.tli_constrain_map(rows, work["d2t"], cfg.T, t2d=work["t2d"], top1_draft=buf.top1_draft[a:a + r],
-                                     top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
-                                     stats=buf.stats)
-                if ev:
-                    ev[1].record(stream)
-                sd.spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
-            elif sampled:
-                sd.spec_softmax_topk(rows, cfg.T, 1, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
-                                     stats=buf.stats)
-                if ev:
-                    ev[1].record(stream)
-                sd.spec_sample(work["draft_u"][a:a + r], probs=qs, out_token=buf.tok[a:a + r],
-                               out_prob=buf.prob[a:a + r], stats=buf.stats)
-                sd.spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
-            else:
-                sd.spec_softmax_topk(rows, cfg.T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
-                                     stats=buf.stats)
-                if ev:
-                    ev[1].record(stream)
-                sd.spec_tree_expand(buf.pool, s, buf.topk_p[s], buf.topk_idx[s])
-            if ev:
-                dom_events.append((ev, r))
-        sd.spec_build_tree(buf.pool, cfg.N, work["root_token"], work["seq_lens"], out=buf.tree)
+        timer.record = record
+        pl.run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], draft_u=work["draft_u"],
+                     d2t=work.get("d2t"), t2d=work.get("t2d"), timer=timer)
         pl.run_verify(buf, target, mode, cfg.T, work["coins"], work["u_final"], work.get("budget"), eos)
         if compact:
             pl.run_compact(buf, work["seq_lens"], work["req_to_token"], cfg.page_size, kv_pool=kv)
@@ -252,7 +235,7 @@ def run_ours(args, cfg, mode, rank, world):
         per_row = cfg.V * 2 + (cfg.V_t * 4 if mode == "sample" else 0)
         kname = "tli_constrain_kernel"
     else:
-        per_row = row_bytes + (cfg.V * 4 if buf.q is not None else 0)
+        per_row = row_bytes + (cfg.V * 4 if buf.q is not None else 0)  # read + written q
         kname = DOMINANT
     dom_avg_ms = statistics.mean(dom_ms) if dom_ms else None
     dom_bytes = per_row * statistics.mean(dom_rows) if dom_rows else None
@@ -277,7 +260,8 @@ def run_ours(args, cfg, mode, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "input_dtype": str(cfg.dtype).replace("torch.", ""),
         "data": "synthetic (seeded; shapes and value distributions of the workload, no model weights)",
         "config": {"workload": describe(cfg, mode), "B": cfg.B, "topk": cfg.topk, "num_steps": cfg.steps,
-                   "N": cfg.N, "V": cfg.V, "mode": mode, "T": cfg.T, "parallelism": f"replicas x{world}",
+                   "N": cfg.N, "V": cfg.V, "mode": mode, "T": cfg.T, "q": q_mode if mode == "sample" else None,
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (draft + target logits), no flush"},
         "us_per_step_median": round(statistics.median(step_ms) * 1e3, 2),
         "verified_tokens_per_step": committed, "mean_accept_length": round(accept, 3),
@@ -383,6 +367,8 @@ def main():
     ap.add_argument("--mode", default=None, choices=[None, "greedy", "sample"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--q", default=None, choices=[None, "logits", "probs"],
+                    help="draft distribution for stochastic verify: logit rows + row stats, or written fp32 rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     args = ap.parse_args()

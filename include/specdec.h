@@ -94,11 +94,15 @@ typedef struct CUstream_st* spec_stream_t; /* same object as cudaStream_t */
  *   topk_idx   [R, k] int32 out: indices by (logit desc, index asc).
  *   probs_or_null [R, V] fp32 out (optional): the full distribution (the
  *              draft distribution q that stochastic verify reads).
+ *   row_stats_or_null [R, 2] fp32 out (optional): the row's maximum m and
+ *              normaliser Z = sum 2^((l - m) log2(e)/T), from which
+ *              spec_verify_sample_qlogits recomputes exactly the values
+ *              probs_or_null would hold.
  * A row whose maximum is not finite gets zero probabilities and counts in
  * SPEC_STAT_NONFINITE_ROW. */
 int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
                       float* topk_p, int32_t* topk_idx, float* probs_or_null,
-                      int32_t* stats_or_null, spec_stream_t stream);
+                      float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream);
 
 /* Draft sampling with caller uniforms (chain drafts drawn from q; [ZS] 5.1
  * "a candidate y drawn from the draft distribution q").  One token per row
@@ -221,6 +225,28 @@ int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_lo
                        int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                        int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
                        size_t ws_bytes, spec_stream_t stream);
+
+/* Stochastic verify with the draft distribution given in logit form: node
+ * n's q row is q[v] = 2^((l_v - m) log2(e)/T_q) / Z of draft-logit row
+ * r = q_row[b*N+n] (NULL: r = b*N+n), with (m, Z) = q_stats[r] as written by
+ * spec_softmax_topk's row_stats.  These are bit-for-bit the probabilities
+ * spec_softmax_topk would have written (rows whose maximum is not finite
+ * give q = 0), so the result equals spec_verify_sample on the materialised
+ * q, while the draft side writes no q and verify reads a rejected node's
+ * draft row in the logits' dtype instead of fp32.  The rule is [ZS] 5.1's,
+ * as in spec_verify_sample ([ZS] 5.2: the verify input carries the draft
+ * distributions; their storage form is free).
+ *   q_logits [rows, V] (q_dtype), q_stats [rows, 2] fp32, T_q > 0.
+ * Other arguments and outputs as spec_verify_sample. */
+int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                               const void* q_logits, int q_dtype, const float* q_stats, float T_q,
+                               const int32_t* q_row_or_null, const int32_t* draft_token,
+                               const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                               const float* coins, const float* u_final, const int32_t* budget_or_null,
+                               int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                               int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                               int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                               size_t ws_bytes, spec_stream_t stream);
 
 /* Greedy verify without caller scratch.  No passage of the pages has a
  * counterpart: this entry point exists for callers that cannot allocate

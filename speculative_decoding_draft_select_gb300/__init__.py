@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "SpecError", "F32", "BF16", "STATS", "lib", "library_path",
     "spec_softmax_topk", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
-    "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample", "spec_compact_freed_capacity",
+    "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
+    "spec_verify_sample_qlogits", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_map_ids", "tli_check_config",
     "new_stats", "new_pool",
 ]
@@ -40,7 +41,7 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 
 _SIGS = {
-    "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P]),
+    "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P]),
     "spec_sample": (_I, [_P, _I, _P, _I64, _I64, _F, _P, _P, _P, _P, _P]),
     "spec_tree_pool_size": (_I64, [_I, _I]),
     "spec_tree_expand": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -50,6 +51,8 @@ _SIGS = {
                                 _SZ, _P]),
     "spec_verify_sample": (_I, [_I, _I, _I64, _I, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P,
                                 _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_sample_qlogits": (_I, [_I, _I, _I64, _I, _P, _F, _P, _I, _P, _F, _P, _P, _P, _P, _P, _P, _P,
+                                        _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_compact_freed_capacity": (_I64, [_I, _I, _I]),
     "spec_compact_slots": (_I, [_I, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, _I64,
                                 _I64, _P, _P]),
@@ -130,8 +133,10 @@ def new_stats(device="cuda"):
 
 # ------------------------------------------------------------------- draft
 
-def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want_probs=False, stats=None):
-    """logits [R, V] -> (topk_p [R, k] f32, topk_idx [R, k] i32, probs [R, V] f32 or None)."""
+def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want_probs=False, row_stats=None,
+                      stats=None):
+    """logits [R, V] -> (topk_p [R, k] f32, topk_idx [R, k] i32, probs [R, V] f32 or None).
+    row_stats [R, 2] f32 (optional) receives each row's (max, normaliser)."""
     _dev(logits, name="logits")
     V = logits.shape[-1]
     R = logits.numel() // V
@@ -140,9 +145,10 @@ def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want
     if want_probs and probs is None:
         probs = torch.empty((R, V), dtype=torch.float32, device=logits.device)
     _dev(probs, torch.float32, "probs")
+    _dev(row_stats, torch.float32, "row_stats")
     _dev(stats, torch.int32, "stats")
     _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
-          _ptr(topk_idx), _ptr(probs), _ptr(stats), _stream())
+          _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _stream())
     return topk_p, topk_idx, probs
 
 
@@ -299,6 +305,33 @@ def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coin
           int(eos_id), _ptr(out["committed"]), _ptr(out["num_committed"]), _ptr(out["accept_length"]),
           _ptr(out["accept_path"]), _ptr(out["next_root"]), _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws),
           ws.numel(), _stream())
+    return out
+
+
+def spec_verify_sample_qlogits(target, T, q_logits, q_stats, T_q, draft_token, next_token, next_sibling, coins,
+                               u_final, q_row=None, budget=None, eos_id=-1, out=None, ws=None, stats=None):
+    """Stochastic verify with q given as draft-logit rows [rows, V] plus their
+    (max, normaliser) [rows, 2] from spec_softmax_topk(row_stats=...)."""
+    _dev(target, name="target")
+    B, N, V = target.shape
+    _dev(q_logits, name="q_logits")
+    if q_logits.shape[-1] != V:
+        raise ValueError("q_logits rows must have length V")
+    _dev(q_stats, torch.float32, "q_stats")
+    for name, t in (("draft_token", draft_token), ("next_token", next_token), ("next_sibling", next_sibling)):
+        _dev(t, torch.int32, name)
+    _dev(q_row, torch.int32, "q_row")
+    _dev(coins, torch.float32, "coins")
+    _dev(u_final, torch.float32, "u_final")
+    _dev(budget, torch.int32, "budget")
+    _dev(stats, torch.int32, "stats")
+    out = _verify_outputs(B, N, target.device, out)
+    ws = _workspace(B, N, target.device, ws)
+    _call("spec_verify_sample_qlogits", B, N, V, _logit_code(target), _ptr(target), float(T), _ptr(q_logits),
+          _logit_code(q_logits), _ptr(q_stats), float(T_q), _ptr(q_row), _ptr(draft_token), _ptr(next_token),
+          _ptr(next_sibling), _ptr(coins), _ptr(u_final), _ptr(budget), int(eos_id), _ptr(out["committed"]),
+          _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]),
+          _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws), ws.numel(), _stream())
     return out
 
 

@@ -247,3 +247,53 @@ __device__ __forceinline__ void for_row(const void* row, int64_t V, F& f) {
 }
 
 }  // namespace specdec
+
+namespace specdec {
+
+// Like for_row, but every thread of the block runs the same number of visits,
+// so a visitor may use warp votes and shuffles: a thread with no element for
+// a slot gets visit(x = -inf..., first, valid = false).
+template <int DT, int UNROLL, class F>
+__device__ __forceinline__ void for_row_uniform(const void* row, int64_t V, F& f) {
+  constexpr int kv = Logit<DT>::kVec;
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  const RowSpan sp = row_span<DT>(row, V);
+  const int64_t nt = blockDim.x;
+  for (int64_t i0 = 0; i0 < sp.head; i0 += nt) {
+    const int64_t i = i0 + threadIdx.x;
+    const bool ok = i < sp.head;
+    float x = ok ? Logit<DT>::load1(row, i) : neg_inf();
+    f.template visit<1>(&x, i, ok);
+  }
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+  for (int64_t i0 = 0; i0 < sp.nvec; i0 += UNROLL * nt) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t i = i0 + threadIdx.x + u * nt;
+      if (i < sp.nvec) v[u] = ld_stream(vp + i);
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t i = i0 + threadIdx.x + u * nt;
+      const bool ok = i < sp.nvec;
+      float x[kv];
+      if (ok) {
+        unpack<DT>(v[u], x);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kv; ++j) x[j] = neg_inf();
+      }
+      f.template visit<kv>(x, sp.head + i * kv, ok);
+    }
+  }
+  const int64_t t_begin = sp.head + sp.nvec * kv;
+  for (int64_t t0 = t_begin; t0 < V; t0 += nt) {
+    const int64_t t = t0 + threadIdx.x;
+    const bool ok = t < V;
+    float x = ok ? Logit<DT>::load1(row, t) : neg_inf();
+    f.template visit<1>(&x, t, ok);
+  }
+}
+
+}  // namespace specdec

@@ -6,11 +6,12 @@
 // stored draft distribution is the processed one (temperature applied), and
 // drafts are drawn from it.
 //
-// One CTA streams one logit row with 16-byte loads (UNROLL in flight per
-// thread).  A single pass gives the online softmax partials (max, sum of
-// 2^((x - max) * log2e / T)) and each thread's top-K list; block merges are
-// fixed-order.  The optional probability row is written by a second sweep
-// of the row (served from L2) with streaming stores.
+// One CTA streams one logit row with 16-byte loads (4 in flight per thread).
+// A single pass gives each thread's online softmax partials (max, sum of
+// 2^((x - max) * log2e / T)) and each warp's top-K by warp select (a shared
+// threshold and candidate buffer, so the common element costs one compare);
+// block merges are fixed-order.  The optional probability row is written by
+// a second sweep of the row (served from L2) with streaming stores.
 #include <climits>
 
 #include "cdf.cuh"
@@ -20,64 +21,17 @@ namespace specdec {
 namespace {
 
 constexpr int kDraftThreads = 512;
+constexpr int kCandCap = 512;  // candidate slots per warp
 
-template <int K>
-struct TopK {
-  float v[K];
-  int i[K];
-  __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int j = 0; j < K; ++j) {
-      v[j] = neg_inf();
-      i[j] = INT_MAX;
-    }
-  }
-  // Insert (x, idx) if it beats the K-th entry; keeps (value desc, index asc).
-  __device__ __forceinline__ void push(float x, int idx) {
-    if (!before(x, idx, v[K - 1], i[K - 1])) return;
-    v[K - 1] = x;
-    i[K - 1] = idx;
-#pragma unroll
-    for (int j = K - 1; j > 0; --j) {
-      if (before(v[j], i[j], v[j - 1], i[j - 1])) {
-        float tv = v[j];
-        v[j] = v[j - 1];
-        v[j - 1] = tv;
-        int ti = i[j];
-        i[j] = i[j - 1];
-        i[j - 1] = ti;
-      }
-    }
-  }
-  // Remove the head (the caller has consumed it).
-  __device__ __forceinline__ void pop() {
-#pragma unroll
-    for (int j = 0; j < K - 1; ++j) {
-      v[j] = v[j + 1];
-      i[j] = i[j + 1];
-    }
-    v[K - 1] = neg_inf();
-    i[K - 1] = INT_MAX;
-  }
-};
-
-// Per-thread state of the softmax + top-k sweep.
-template <int K, bool WANT_TOPK>
-struct SoftmaxTopKVisitor {
-  float c;  // log2(e) / T
-  float m;  // running max (ordering keys)
-  float s;  // sum of 2^((x - m) c)
-  TopK<K> top;
-
+// Running online-softmax partials of one thread: m = max key seen,
+// s = sum 2^((x - m) c).
+struct SoftmaxPartial {
+  float c, m, s;
   template <int N>
-  __device__ __forceinline__ void visit(const float* xin, int64_t first) {
-    float x[N];
+  __device__ __forceinline__ float update(const float* x) {
     float vmax = neg_inf();
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-      x[j] = order_key(xin[j]);
-      vmax = fmaxf(vmax, x[j]);
-    }
+    for (int j = 0; j < N; ++j) vmax = fmaxf(vmax, x[j]);
     if (vmax > m) {
       s = (m == neg_inf()) ? 0.0f : s * fast_exp2((m - vmax) * c);
       m = vmax;
@@ -87,47 +41,110 @@ struct SoftmaxTopKVisitor {
 #pragma unroll
       for (int j = 0; j < N; ++j) s += fast_exp2(fmaf(x[j], c, -mc));
     }
-    if (WANT_TOPK && vmax >= top.v[K - 1]) {
-#pragma unroll
-      for (int j = 0; j < N; ++j) top.push(x[j], static_cast<int>(first + j));
-    }
+    return vmax;
   }
 };
 
-// Block merge of per-thread top-K lists: each warp pops its best K into
-// shared memory, then warp 0 merges the warps' lists the same way.
-// Result in out_v / out_i [K] (shared).  All threads call it.
+// Warp-select top-K: each warp keeps its current top-K (sorted) and a
+// candidate buffer in shared memory.  An element is a candidate only if its
+// key is >= the warp's current K-th best value (a key below it can never
+// enter the top-K), so after the first few vectors candidates are rare.
+// When the buffer runs full the warp merges buffer and list back into a
+// sorted top-K (K rounds of a warp-wide (value desc, index asc) argmax).
 template <int K>
-__device__ void block_topk(TopK<K>& t, float* wv, int* wi, float* out_v, int* out_i) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+struct WarpSel {
+  float bv[kCandCap];
+  int bi[kCandCap];
+  float lv[K];
+  int li[K];
+};
+
+// Merge `n` entries (e < K from the list, the rest from the buffer) into the
+// sorted list.  Warp-synchronous; all lanes call it.
+template <int K>
+__device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, int n, float& thr, int lane) {
+  __syncwarp();
+  float nv = neg_inf();
+  int ni = INT_MAX;
   for (int r = 0; r < K; ++r) {
-    float bv = t.v[0];
-    int bi = t.i[0];
-    warp_best(bv, bi);
-    if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
-    if (lane == 0) {
-      wv[warp * K + r] = bv;
-      wi[warp * K + r] = bi;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    TopK<K> u;
-    u.init();
-    for (int e = lane; e < nw * K; e += 32) u.push(wv[e], wi[e]);
-    for (int r = 0; r < K; ++r) {
-      float bv = u.v[0];
-      int bi = u.i[0];
-      warp_best(bv, bi);
-      if (u.v[0] == bv && u.i[0] == bi && bi != INT_MAX) u.pop();
-      if (lane == 0) {
-        out_v[r] = bv;
-        out_i[r] = bi;
+    float bv = neg_inf();
+    int bi = INT_MAX, bpos = -1;
+    for (int e = lane; e < n; e += 32) {
+      const float v = e < K ? w.lv[e] : w.bv[e - K];
+      const int i = e < K ? w.li[e] : w.bi[e - K];
+      if (before(v, i, bv, bi)) {
+        bv = v;
+        bi = i;
+        bpos = e;
       }
     }
+    float wv = bv;
+    int wi = bi;
+    warp_best(wv, wi);
+    if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
+      if (bpos < K) {
+        w.lv[bpos] = neg_inf();
+        w.li[bpos] = INT_MAX;
+      } else {
+        w.bv[bpos - K] = neg_inf();
+        w.bi[bpos - K] = INT_MAX;
+      }
+    }
+    __syncwarp();
+    if (lane == r) {
+      nv = wv;
+      ni = wi;
+    }
   }
-  __syncthreads();
+  if (lane < K) {
+    w.lv[lane] = nv;
+    w.li[lane] = ni;
+  }
+  thr = __shfl_sync(0xffffffffu, nv, K - 1);
+  __syncwarp();
 }
+
+template <int K>
+struct DraftVisitor {
+  SoftmaxPartial sp;
+  WarpSel<K>* w;
+  int cnt;    // warp-uniform candidate count
+  float thr;  // warp-uniform K-th best value so far
+  int lane;
+
+  template <int N>
+  __device__ __forceinline__ void visit(const float* xin, int64_t first, bool ok) {
+    float x[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) x[j] = order_key(xin[j]);
+    const float vmax = sp.template update<N>(x);
+    if (!__any_sync(0xffffffffu, ok && vmax >= thr)) return;
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) c += (ok && x[j] >= thr);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = cnt + incl - c;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      if (ok && x[j] >= thr) {
+        w->bv[pos] = x[j];
+        w->bi[pos] = static_cast<int>(first) + j;
+        ++pos;
+      }
+    }
+    cnt += total;
+    if (cnt > kCandCap - 32 * N) {
+      warp_select_merge<K>(*w, cnt + K, thr, lane);
+      cnt = 0;
+    }
+  }
+};
 
 // Block merge of (m, s) partials; every thread receives the row's (m, s).
 __device__ __forceinline__ void block_ms(float& m, float& s, float c, float* sm, float* ss) {
@@ -151,6 +168,18 @@ __device__ __forceinline__ void block_ms(float& m, float& s, float c, float* sm,
   m = sm[32];
   s = ss[32];
 }
+
+// Per-thread stats-only visitor (draft sampling from logits).
+struct StatsVisitor {
+  SoftmaxPartial sp;
+  template <int N>
+  __device__ __forceinline__ void visit(const float* xin, int64_t) {
+    float x[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) x[j] = order_key(xin[j]);
+    sp.template update<N>(x);
+  }
+};
 
 // Writes p = 2^((x - m) c) / Z for every element of a row.
 template <int DT>
@@ -183,31 +212,69 @@ struct ZeroWriter {
   }
 };
 
+template <int K>
+constexpr size_t draft_smem_bytes() {
+  return sizeof(WarpSel<K>) * (kDraftThreads / 32);
+}
+
 template <int DT, int K>
 __global__ void __launch_bounds__(kDraftThreads)
     softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
-                        float* __restrict__ probs, int32_t* __restrict__ stats) {
+                        float* __restrict__ probs, float* __restrict__ row_stats,
+                        int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  __shared__ float wv[(kDraftThreads / 32) * K];
-  __shared__ int wi[(kDraftThreads / 32) * K];
+  constexpr int kWarps = kDraftThreads / 32;
+  extern __shared__ __align__(16) unsigned char dsm[];
+  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm);
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
 
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
+  WarpSel<K>& w = sel[warp];
+  if (lane < K) {
+    w.lv[lane] = neg_inf();
+    w.li[lane] = INT_MAX;
+  }
+  __syncwarp();
+  DraftVisitor<K> st{{c, neg_inf(), 0.0f}, &w, 0, neg_inf(), lane};
+  for_row_uniform<DT, 4>(row, V, st);
+  if (st.cnt > 0) warp_select_merge<K>(w, st.cnt + K, st.thr, lane);
 
-  SoftmaxTopKVisitor<K, true> st;
-  st.c = c;
-  st.m = neg_inf();
-  st.s = 0.0f;
-  st.top.init();
-  for_row<DT, 4>(row, V, st);
-
-  float m = st.m, s = st.s;
-  block_ms(m, s, c, sm, ss);
-  block_topk<K>(st.top, wv, wi, fv, fi);
+  float m = st.sp.m, s = st.sp.s;
+  block_ms(m, s, c, sm, ss);  // its barriers also publish every warp's list
+  if (warp == 0) {
+    // merge the warps' sorted lists: K rounds over kWarps * K entries
+    for (int rr = 0; rr < K; ++rr) {
+      float bv = neg_inf();
+      int bi = INT_MAX, bpos = -1;
+      for (int e = lane; e < kWarps * K; e += 32) {
+        const float v = sel[e / K].lv[e % K];
+        const int i = sel[e / K].li[e % K];
+        if (before(v, i, bv, bi)) {
+          bv = v;
+          bi = i;
+          bpos = e;
+        }
+      }
+      float wv = bv;
+      int wi = bi;
+      warp_best(wv, wi);
+      if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
+        sel[bpos / K].lv[bpos % K] = neg_inf();
+        sel[bpos / K].li[bpos % K] = INT_MAX;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        fv[rr] = wv;
+        fi[rr] = wi;
+      }
+    }
+  }
+  __syncthreads();
 
   const bool finite = isfinite(m);
   const float mc = m * c;
@@ -217,14 +284,19 @@ __global__ void __launch_bounds__(kDraftThreads)
     topk_idx[r * k + j] = fi[j];
     topk_p[r * k + j] = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
   }
-  if (threadIdx.x == 0 && !finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
+  if (threadIdx.x == 0) {
+    if (!finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
+    if (row_stats != nullptr) {
+      row_stats[2 * r] = m;
+      row_stats[2 * r + 1] = s;
+    }
+  }
   if (probs != nullptr) {
     float* out = probs + r * V;
     if (finite) {
       const RowSpan sp = row_span<DT>(row, V);
-      ProbWriter<DT> w{c, mc, invz, out,
-                       (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
-      for_row<DT, 2>(row, V, w);
+      ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
+      for_row<DT, 2>(row, V, pw);
     } else {
       ZeroWriter z{out};
       for_row<DT, 2>(row, V, z);
@@ -292,13 +364,9 @@ __global__ void __launch_bounds__(kSampleThreads)
     return;
   }
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  SoftmaxTopKVisitor<1, false> st;
-  st.c = c;
-  st.m = neg_inf();
-  st.s = 0.0f;
-  st.top.init();
+  StatsVisitor st{{c, neg_inf(), 0.0f}};
   for_row<DT, 4>(row, V, st);
-  float m = st.m, s = st.s;
+  float m = st.sp.m, s = st.sp.s;
   block_ms(m, s, c, sm, ss);
   if (!isfinite(m)) {
     if (threadIdx.x == 0) {
@@ -314,21 +382,26 @@ __global__ void __launch_bounds__(kSampleThreads)
 
 template <int DT, int K>
 int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                        int32_t* topk_idx, float* probs, int32_t* stats, cudaStream_t s) {
-  softmax_topk_kernel<DT, K><<<static_cast<unsigned>(R), kDraftThreads, 0, s>>>(
-      logits, V, c, k, topk_p, topk_idx, probs, stats);
+                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
+  constexpr size_t smem = draft_smem_bytes<K>();
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  softmax_topk_kernel<DT, K><<<static_cast<unsigned>(R), kDraftThreads, smem, s>>>(
+      logits, V, c, k, topk_p, topk_idx, probs, row_stats, stats);
   return launch_status();
 }
 
 template <int DT>
 int dispatch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                          int32_t* topk_idx, float* probs, int32_t* stats, cudaStream_t s) {
-  if (k <= 1) return launch_softmax_topk<DT, 1>(logits, R, V, c, k, topk_p, topk_idx, probs, stats, s);
-  if (k <= 2) return launch_softmax_topk<DT, 2>(logits, R, V, c, k, topk_p, topk_idx, probs, stats, s);
-  if (k <= 4) return launch_softmax_topk<DT, 4>(logits, R, V, c, k, topk_p, topk_idx, probs, stats, s);
-  if (k <= 8) return launch_softmax_topk<DT, 8>(logits, R, V, c, k, topk_p, topk_idx, probs, stats, s);
-  if (k <= 16) return launch_softmax_topk<DT, 16>(logits, R, V, c, k, topk_p, topk_idx, probs, stats, s);
-  return launch_softmax_topk<DT, 32>(logits, R, V, c, k, topk_p, topk_idx, probs, stats, s);
+                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
+  if (k <= 1) return launch_softmax_topk<DT, 1>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+  if (k <= 2) return launch_softmax_topk<DT, 2>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+  if (k <= 4) return launch_softmax_topk<DT, 4>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+  if (k <= 8) return launch_softmax_topk<DT, 8>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+  if (k <= 16) return launch_softmax_topk<DT, 16>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+  return launch_softmax_topk<DT, 32>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
 }
 
 }  // namespace
@@ -338,7 +411,7 @@ using namespace specdec;
 
 extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
                                  float* topk_p, int32_t* topk_idx, float* probs_or_null,
-                                 int32_t* stats_or_null, spec_stream_t stream) {
+                                 float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream) {
   if (R < 0 || V < 1 || k < 1 || k > V || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
   if (R > 0 && (logits == nullptr || topk_p == nullptr || topk_idx == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
@@ -347,8 +420,10 @@ extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64
   const float c = kLog2e / T;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return dtype == SPEC_BF16
-             ? dispatch_softmax_topk<SPEC_BF16>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null, stats_or_null, s)
-             : dispatch_softmax_topk<SPEC_F32>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null, stats_or_null, s);
+             ? dispatch_softmax_topk<SPEC_BF16>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
+                                                row_stats_or_null, stats_or_null, s)
+             : dispatch_softmax_topk<SPEC_F32>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
+                                               row_stats_or_null, stats_or_null, s);
 }
 
 extern "C" int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_null, int64_t R,

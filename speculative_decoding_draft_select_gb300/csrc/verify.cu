@@ -183,41 +183,102 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
 
 // -------------------------------------------------------- stochastic walk
 
+// Where a node's draft distribution q comes from.
+//   QProbs:     materialised fp32 rows (q[v] read directly).
+//   QLogits<D>: the draft logits row and that row's (max, normaliser) as the
+//               draft softmax wrote them; q[v] = 2^((l_v - max) c) / Z with
+//               the same fp32 operations as the written probabilities, so
+//               both forms give bit-identical q values.
+struct QRowProbs {
+  const float* row;  // nullptr: no row (q = 0)
+  int64_t V;
+  __device__ __forceinline__ float at(int64_t v) const { return row ? __ldg(row + v) : 0.0f; }
+  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
+    if (row) {
+      load8_f32(row, V, v0, x);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+  }
+};
+
+struct QProbs {
+  const float* q;
+  int64_t V;
+  __device__ __forceinline__ QRowProbs row(int64_t r) const { return {r >= 0 ? q + r * V : nullptr, V}; }
+};
+
+template <int QDT>
+struct QRowLogits {
+  const void* row;  // nullptr: no row, or a row whose max is not finite (q = 0)
+  int64_t V;
+  float c, mc, invz;
+  __device__ __forceinline__ float at(int64_t v) const {
+    return row ? prob_of(order_key(Logit<QDT>::load1(row, v)), c, mc, invz) : 0.0f;
+  }
+  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
+    if (row) {
+      load8_logits<QDT>(row, V, v0, x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = prob_of(x[j], c, mc, invz);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+  }
+};
+
+template <int QDT>
+struct QLogits {
+  const void* q;
+  const float* stats;  // [rows, 2]: max, normaliser
+  int64_t V;
+  float c;
+  __device__ __forceinline__ QRowLogits<QDT> row(int64_t r) const {
+    constexpr int esz = QDT == SPEC_BF16 ? 2 : 4;
+    if (r < 0) return {nullptr, V, c, 0.0f, 0.0f};
+    const float m = __ldg(stats + 2 * r), z = __ldg(stats + 2 * r + 1);
+    if (!isfinite(m)) return {nullptr, V, c, 0.0f, 0.0f};
+    return {static_cast<const char*>(q) + r * V * esz, V, c, m * c, 1.0f / z};
+  }
+};
+
 // Weights of the current distribution at a node: p (A == 0) or the
 // unnormalised residual max(0, p - A q).
-template <int DT>
+template <int DT, class QRow>
 struct ResidualWeights {
   const void* lrow;
-  const float* qrow;
+  QRow qrow;
   int64_t V;
   float c, mc, invz, A;
   __device__ __forceinline__ void load8(int64_t v0, float* x) const {
     load8_logits<DT>(lrow, V, v0, x);
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = prob_of(x[j], c, mc, invz);
-    if (A != 0.0f && qrow != nullptr) {
+    if (A != 0.0f) {
       float q[8];
-      load8_f32(qrow, V, v0, q);
+      qrow.load8(v0, q);
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = fmaxf(0.0f, fmaf(-A, q[j], x[j]));
     }
   }
   __device__ __forceinline__ float at(int64_t v) const {
     const float p = prob_of(order_key(Logit<DT>::load1(lrow, v)), c, mc, invz);
-    return (A != 0.0f && qrow != nullptr) ? fmaxf(0.0f, fmaf(-A, __ldg(qrow + v), p)) : p;
+    return A != 0.0f ? fmaxf(0.0f, fmaf(-A, qrow.at(v), p)) : p;
   }
 };
 
-template <int DT>
+template <int DT, class QSrc>
 __global__ void __launch_bounds__(kWalkThreads)
     sample_walk_kernel(int N, int64_t V, float c, const void* __restrict__ target,
-                       const float* __restrict__ m_row, const float* __restrict__ z_row,
-                       const float* __restrict__ q, const int32_t* __restrict__ q_row,
-                       const int32_t* __restrict__ dtok, const int32_t* __restrict__ ntok,
-                       const int32_t* __restrict__ nsib, const float* __restrict__ coins,
-                       const float* __restrict__ u_final, const int32_t* __restrict__ budget, int32_t eos,
-                       int32_t* committed, int32_t* num_committed, int32_t* accept_length,
-                       int32_t* accept_path, int32_t* next_root, int32_t* walk_info, int32_t* stats) {
+                       const float* __restrict__ m_row, const float* __restrict__ z_row, QSrc qsrc,
+                       const int32_t* __restrict__ q_row, const int32_t* __restrict__ dtok,
+                       const int32_t* __restrict__ ntok, const int32_t* __restrict__ nsib,
+                       const float* __restrict__ coins, const float* __restrict__ u_final,
+                       const int32_t* __restrict__ budget, int32_t eos, int32_t* committed,
+                       int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
+                       int32_t* next_root, int32_t* walk_info, int32_t* stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   extern __shared__ float dyn[];
   const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
@@ -275,14 +336,14 @@ __global__ void __launch_bounds__(kWalkThreads)
     __syncthreads();
     const int n = s_n, nch = s_nch;
     const void* lrow = static_cast<const char*>(target) + (o + n) * V * esz;
-    const float* qrow = (nch > 0 && s_qrow >= 0) ? q + s_qrow * V : nullptr;
+    const auto qrow = qsrc.row(nch > 0 ? s_qrow : -1);
     const float mc = s_m * cT, invz = s_invz;
     for (int t = tid; t < nch; t += kWalkThreads) {
       const int ch = s_ch[t];
       const int32_t y = s_dt[ch];
       const bool ok = y >= 0 && y < V;
       g_l[t] = ok ? order_key(Logit<DT>::load1(lrow, y)) : neg_inf();
-      g_q[t] = (ok && qrow) ? __ldg(qrow + y) : 0.0f;
+      g_q[t] = ok ? qrow.at(y) : 0.0f;
       g_u[t] = __ldg(coins + o + ch);
     }
     __syncthreads();
@@ -301,7 +362,7 @@ __global__ void __launch_bounds__(kWalkThreads)
         break;
       }
       // rejected: mass of the next residual
-      ResidualWeights<DT> w{lrow, qrow, V, cT, mc, invz, s_A + s_cj};
+      ResidualWeights<DT, decltype(qrow)> w{lrow, qrow, V, cT, mc, invz, s_A + s_cj};
       const float total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
       if (tid == 0) {
         if (total > 0.0f && isfinite(total)) {
@@ -332,7 +393,7 @@ __global__ void __launch_bounds__(kWalkThreads)
       continue;
     }
     // no child accepted (or a leaf): draw from the current distribution
-    ResidualWeights<DT> w{lrow, qrow, V, cT, mc, invz, s_A};
+    ResidualWeights<DT, decltype(qrow)> w{lrow, qrow, V, cT, mc, invz, s_A};
     float total;
     if (s_tiles_ok) {
       total = s_total;
@@ -436,6 +497,36 @@ extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void
   return launch_status();
 }
 
+namespace specdec {
+namespace {
+
+template <int DT, class QSrc>
+int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, QSrc qsrc, const int32_t* q_row,
+                         const int32_t* dtok, const int32_t* ntok, const int32_t* nsib, const float* coins,
+                         const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
+                         int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                         int32_t* walk_info, int32_t* stats, VerifyWs w, cudaStream_t s) {
+  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
+  const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
+  const size_t smem = sizeof(float) * (ntiles * (1 + kWalkThreads / 32) + 3 * static_cast<int64_t>(N)) +
+                      sizeof(int32_t) * 6 * static_cast<int64_t>(N);
+  row_stats_kernel<DT, true><<<rows, kStatThreads, 0, s>>>(target, V, c, w.amax, w.m, w.z, stats);
+  int e = launch_status();
+  if (e != SPEC_OK) return e;
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<DT, QSrc>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  sample_walk_kernel<DT, QSrc><<<B, kWalkThreads, smem, s>>>(N, V, c, target, w.m, w.z, qsrc, q_row, dtok, ntok,
+                                                             nsib, coins, u_final, budget, eos, committed,
+                                                             num_committed, accept_length, accept_path, next_root,
+                                                             walk_info, stats);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace specdec
+
 extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
                                   const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
                                   const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
@@ -451,40 +542,70 @@ extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void
   if (rc <= 0) return rc;
   if (!q || !coins || !u_final) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  VerifyWs w = carve(ws, B, N);
   const float c = kLog2e / T;
-  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
-  const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
-  const size_t smem = sizeof(float) * (ntiles * (1 + kWalkThreads / 32) + 3 * static_cast<int64_t>(N)) +
-                      sizeof(int32_t) * 6 * static_cast<int64_t>(N);
+  const QProbs qs{q, V};
+  if (dtype == SPEC_BF16)
+    return launch_sample_verify<SPEC_BF16>(B, N, V, target_logits, c, qs, q_row_or_null, draft_token,
+                                           retrieve_next_token, retrieve_next_sibling, coins, u_final,
+                                           budget_or_null, eos_id, committed, num_committed, accept_length,
+                                           accept_path, next_root, walk_info_or_null, stats_or_null,
+                                           carve(ws, B, N), s);
+  return launch_sample_verify<SPEC_F32>(B, N, V, target_logits, c, qs, q_row_or_null, draft_token,
+                                        retrieve_next_token, retrieve_next_sibling, coins, u_final, budget_or_null,
+                                        eos_id, committed, num_committed, accept_length, accept_path, next_root,
+                                        walk_info_or_null, stats_or_null, carve(ws, B, N), s);
+}
+
+namespace specdec {
+namespace {
+
+template <int DT, int QDT>
+int sample_verify_qlogits(int B, int N, int64_t V, const void* target, float c, const void* q_logits,
+                          const float* q_stats, float cq, const int32_t* q_row, const int32_t* dtok,
+                          const int32_t* ntok, const int32_t* nsib, const float* coins, const float* u_final,
+                          const int32_t* budget, int32_t eos, int32_t* committed, int32_t* num_committed,
+                          int32_t* accept_length, int32_t* accept_path, int32_t* next_root, int32_t* walk_info,
+                          int32_t* stats, VerifyWs w, cudaStream_t s) {
+  const QLogits<QDT> qs{q_logits, q_stats, V, cq};
+  return launch_sample_verify<DT>(B, N, V, target, c, qs, q_row, dtok, ntok, nsib, coins, u_final, budget, eos,
+                                  committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
+                                  w, s);
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                          const void* q_logits, int q_dtype, const float* q_stats, float T_q,
+                                          const int32_t* q_row_or_null, const int32_t* draft_token,
+                                          const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                          const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                          int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                          int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                          int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                          size_t ws_bytes, spec_stream_t stream) {
+  if (!(T > 0.0f) || !isfinite(T) || !(T_q > 0.0f) || !isfinite(T_q)) return SPEC_ERR_INVALID_ARG;
+  const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
+                              retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
+                              next_root, ws, ws_bytes);
+  if (rc <= 0) return rc;
+  if (!q_logits || !q_stats || !coins || !u_final) return SPEC_ERR_INVALID_ARG;
+  if (q_dtype != SPEC_F32 && q_dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float c = kLog2e / T, cq = kLog2e / T_q;
+  const VerifyWs w = carve(ws, B, N);
+#define SPEC_QL(DT, QDT)                                                                                         \
+  return sample_verify_qlogits<DT, QDT>(B, N, V, target_logits, c, q_logits, q_stats, cq, q_row_or_null,        \
+                                        draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final, \
+                                        budget_or_null, eos_id, committed, num_committed, accept_length,         \
+                                        accept_path, next_root, walk_info_or_null, stats_or_null, w, s)
   if (dtype == SPEC_BF16) {
-    row_stats_kernel<SPEC_BF16, true><<<rows, kStatThreads, 0, s>>>(target_logits, V, c, w.amax, w.m, w.z,
-                                                                    stats_or_null);
-    int e = launch_status();
-    if (e != SPEC_OK) return e;
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<SPEC_BF16>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem)) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    sample_walk_kernel<SPEC_BF16><<<B, kWalkThreads, smem, s>>>(
-        N, V, c, target_logits, w.m, w.z, q, q_row_or_null, draft_token, retrieve_next_token,
-        retrieve_next_sibling, coins, u_final, budget_or_null, eos_id, committed, num_committed, accept_length,
-        accept_path, next_root, walk_info_or_null, stats_or_null);
-  } else {
-    row_stats_kernel<SPEC_F32, true><<<rows, kStatThreads, 0, s>>>(target_logits, V, c, w.amax, w.m, w.z,
-                                                                   stats_or_null);
-    int e = launch_status();
-    if (e != SPEC_OK) return e;
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<SPEC_F32>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem)) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    sample_walk_kernel<SPEC_F32><<<B, kWalkThreads, smem, s>>>(
-        N, V, c, target_logits, w.m, w.z, q, q_row_or_null, draft_token, retrieve_next_token,
-        retrieve_next_sibling, coins, u_final, budget_or_null, eos_id, committed, num_committed, accept_length,
-        accept_path, next_root, walk_info_or_null, stats_or_null);
+    if (q_dtype == SPEC_BF16) SPEC_QL(SPEC_BF16, SPEC_BF16);
+    SPEC_QL(SPEC_BF16, SPEC_F32);
   }
-  return launch_status();
+  if (q_dtype == SPEC_BF16) SPEC_QL(SPEC_F32, SPEC_BF16);
+  SPEC_QL(SPEC_F32, SPEC_F32);
+#undef SPEC_QL
 }
 
 // ------------------------------------------------- greedy verify, no scratch

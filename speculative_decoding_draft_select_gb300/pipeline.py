@@ -10,8 +10,11 @@ EAGLE" sections 2-3 and "EAGLE speculative decoding in four parts",
                  uniforms, then spec_tree_expand with k = 1;
   - TLI chain:   tli_constrain_map (q in target order), then
                  spec_tree_expand with the mapped top-1 (SGLang PR #22883).
-then spec_build_tree.  Verify: spec_verify_greedy or spec_verify_sample over
-the target logits in node order.  Compaction: spec_compact_slots.
+then spec_build_tree.  Verify: spec_verify_greedy, or for sampling either
+spec_verify_sample on the written q table (q_mode "probs") or
+spec_verify_sample_qlogits on the draft logits plus the per-row (max,
+normaliser) the draft kernel records (q_mode "logits": no q is written; the
+q values are bit-identical).  Compaction: spec_compact_slots.
 
 All buffers are allocated once in ``StepBuffers``; a step only enqueues
 kernels on the current stream.
@@ -22,7 +25,7 @@ import torch
 
 from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity, spec_compact_slots,
                spec_sample, spec_softmax_topk, spec_tree_expand, spec_verify_greedy, spec_verify_sample,
-               spec_verify_ws_size, tli_constrain_map)
+               spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map)
 
 
 def step_offsets(B, topk, steps):
@@ -38,9 +41,11 @@ class StepBuffers:
     """
 
     def __init__(self, kind, B, topk, steps, N, V, device, want_q, sampled=False, V_t=None, page_size=0,
-                 max_ctx=0):
+                 max_ctx=0, q_mode="probs"):
+        if kind == "tli" and q_mode != "probs":
+            raise ValueError("TLI verification reads q in target order: q_mode must be 'probs'")
         self.kind, self.B, self.topk, self.steps, self.N, self.V = kind, B, topk, steps, N, V
-        self.sampled, self.want_q = sampled, want_q
+        self.sampled, self.want_q, self.q_mode = sampled, want_q, q_mode
         self.Vq = V_t if kind == "tli" else V
         self.offs, self.rows = step_offsets(B, topk, steps)
         dev = torch.device(device)
@@ -51,7 +56,12 @@ class StepBuffers:
                        for s in range(steps)]
         self.topk_idx = [torch.empty((B * (1 if s == 0 else kk), kk), dtype=torch.int32, device=dev)
                          for s in range(steps)]
-        self.q = torch.empty((self.rows, self.Vq), dtype=torch.float32, device=dev) if want_q else None
+        self.q = (torch.empty((self.rows, self.Vq), dtype=torch.float32, device=dev)
+                  if want_q and q_mode == "probs" else None)
+        self.q_stats = (torch.empty((self.rows, 2), dtype=torch.float32, device=dev)
+                        if want_q and q_mode == "logits" else None)
+        self.draft_table = None
+        self.T_draft = None
         self.tok = torch.empty((self.rows,), dtype=torch.int32, device=dev)
         self.prob = torch.empty((self.rows,), dtype=torch.float32, device=dev)
         self.top1_draft = torch.empty((self.rows,), dtype=torch.int32, device=dev)
@@ -88,28 +98,44 @@ class StepBuffers:
         }
 
 
-def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=None, d2t=None, t2d=None):
-    """Draft steps + tree build.  Returns buf.tree."""
+def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=None, d2t=None, t2d=None, timer=None):
+    """Draft steps + tree build.  Returns buf.tree.  ``timer`` (optional) has
+    begin(step) / end(step), called around each step's softmax/top-k or TLI
+    launch."""
     B, k = buf.B, buf.topk
+    buf.draft_table, buf.T_draft = draft_table, T
     for s in range(buf.steps):
         r = B * (1 if s == 0 else k)
         a = buf.offs[s]
         rows = draft_table[a:a + r]
         qs = buf.q[a:a + r] if buf.q is not None else None
+        st = buf.q_stats[a:a + r] if buf.q_stats is not None else None
+        if timer is not None:
+            timer.begin(s)
         if buf.kind == "tli":
             tli_constrain_map(rows, d2t, T, t2d=t2d, top1_draft=buf.top1_draft[a:a + r],
                               top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
                               stats=buf.stats)
+            if timer is not None:
+                timer.end(s)
             spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
         elif buf.kind == "chain" and buf.sampled:
-            spec_softmax_topk(rows, T, 1, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
+            spec_softmax_topk(rows, T, 1, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,
                               stats=buf.stats)
-            spec_sample(draft_u[a:a + r], probs=qs, out_token=buf.tok[a:a + r], out_prob=buf.prob[a:a + r],
-                        stats=buf.stats)
+            if timer is not None:
+                timer.end(s)
+            if qs is not None:
+                spec_sample(draft_u[a:a + r], probs=qs, out_token=buf.tok[a:a + r], out_prob=buf.prob[a:a + r],
+                            stats=buf.stats)
+            else:
+                spec_sample(draft_u[a:a + r], logits=rows, T=T, out_token=buf.tok[a:a + r],
+                            out_prob=buf.prob[a:a + r], stats=buf.stats)
             spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
         else:
-            spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs,
+            spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,
                               stats=buf.stats)
+            if timer is not None:
+                timer.end(s)
             spec_tree_expand(buf.pool, s, buf.topk_p[s], buf.topk_idx[s])
     spec_build_tree(buf.pool, buf.N, root_token, seq_lens, out=buf.tree)
     return buf.tree
@@ -120,6 +146,11 @@ def run_verify(buf: StepBuffers, target, mode, T=1.0, coins=None, u_final=None, 
     if mode == "greedy":
         return spec_verify_greedy(target, t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"],
                                   budget=budget, eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)
+    if buf.q_mode == "logits":
+        return spec_verify_sample_qlogits(target, T, buf.draft_table, buf.q_stats, buf.T_draft, t["draft_token"],
+                                          t["retrieve_next_token"], t["retrieve_next_sibling"], coins, u_final,
+                                          q_row=t["q_row"], budget=budget, eos_id=eos_id, out=buf.verify_out,
+                                          ws=buf.ws, stats=buf.stats)
     return spec_verify_sample(target, T, buf.q, t["draft_token"], t["retrieve_next_token"],
                               t["retrieve_next_sibling"], coins, u_final, q_row=t["q_row"], budget=budget,
                               eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)

@@ -36,20 +36,22 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_side_argument_checks(lib):
     null = None
     # k > V, T <= 0, bad dtype, null pointers
-    assert lib.spec_softmax_topk(null, 1, 4, 3, 1.0, 4, null, null, null, null, null) == -1
-    assert lib.spec_softmax_topk(null, 1, 4, 8, 0.0, 2, null, null, null, null, null) == -1
-    assert lib.spec_softmax_topk(null, 1, 4, 8, 1.0, 2, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 3, 1.0, 4, null, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 0.0, 2, null, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 1.0, 2, null, null, null, null, null, null) == -1
     assert lib.spec_softmax_topk(ctypes.c_void_p(16), 7, 4, 8, 1.0, 2, ctypes.c_void_p(16), ctypes.c_void_p(16),
-                                 null, null, null) == -2
+                                 null, null, null, null) == -2
     assert lib.spec_softmax_topk(ctypes.c_void_p(16), 1, 4, 100, 1.0, 33, ctypes.c_void_p(16),
-                                 ctypes.c_void_p(16), null, null, null) == -2  # k above the limit
+                                 ctypes.c_void_p(16), null, null, null, null) == -2  # k above the limit
     # empty batches are no-ops
-    assert lib.spec_softmax_topk(null, 1, 0, 8, 1.0, 2, null, null, null, null, null) == 0
+    assert lib.spec_softmax_topk(null, 1, 0, 8, 1.0, 2, null, null, null, null, null, null) == 0
     assert lib.spec_tree_expand(0, 2, 4, 0, null, null, null, null, null, null, null, null, null) == -1
     assert lib.spec_tree_expand(2, 2, 4, 2, null, null, null, null, null, null, null, null, null) == -1
     assert lib.spec_build_tree(1, 2, 2, 8, *([null] * 15)) == -1  # N > P = 7
     assert lib.spec_verify_greedy(2, 4, 10, 1, *([null] * 5), -1, *([null] * 8), 0, null) == -1
     assert lib.spec_verify_sample(2, 4, 10, 1, null, 0.0, *([null] * 8), -1, *([null] * 8), 0, null) == -1
+    assert lib.spec_verify_sample_qlogits(2, 4, 10, 1, null, 1.0, null, 1, null, 0.0, *([null] * 7), -1,
+                                          *([null] * 8), 0, null) == -1
     assert lib.spec_compact_slots(2, 4, 0, *([null] * 4), 16, *([null] * 4), 0, *([null] * 3), 0, 0, null,
                                   null) == -1
     assert lib.tli_constrain_map(4, 10, 10, null, 1, null, null, 1.0, null, null, null, null, null, null) == -1

@@ -204,9 +204,9 @@ def small(cfg_name, **kw):
     return CONFIGS[cfg_name].scaled(**kw)
 
 
-def run_gpu_pipeline(cfg, work, mode):
+def run_gpu_pipeline(cfg, work, mode, q_mode="probs"):
     buf = StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, "cuda", want_q=(mode == "sample"),
-                      sampled=(cfg.kind == "chain" and mode == "sample"), V_t=cfg.V_t or None)
+                      sampled=(cfg.kind == "chain" and mode == "sample"), V_t=cfg.V_t or None, q_mode=q_mode)
     tree = run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"],
                      draft_u=work["draft_u"], d2t=work.get("d2t"), t2d=work.get("t2d"))
     target = assemble_target(work, tree["q_row"])
@@ -216,8 +216,8 @@ def run_gpu_pipeline(cfg, work, mode):
     return buf, tree, out
 
 
-def compare_pipeline(cfg, work, mode, reqs):
-    buf, tree, out = run_gpu_pipeline(cfg, work, mode)
+def compare_pipeline(cfg, work, mode, reqs, q_mode="probs"):
+    buf, tree, out = run_gpu_pipeline(cfg, work, mode, q_mode)
     exact = boundary = 0
     for b in reqs:
         ot, q, target, o, _ = run_request(cfg, fetch_request(cfg, work, b), mode)
@@ -244,24 +244,28 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("name,mode", [("c1", "greedy"), ("c1", "sample"), ("c2", "greedy"), ("c3", "sample"),
-                                       ("c4", "sample"), ("c5", "greedy"), ("c5", "sample")])
-def test_pipeline_small(name, mode):
+@pytest.mark.parametrize("name,mode,q_mode", [("c1", "greedy", "probs"), ("c1", "sample", "probs"),
+                                              ("c1", "sample", "logits"), ("c2", "greedy", "probs"),
+                                              ("c3", "sample", "probs"), ("c3", "sample", "logits"),
+                                              ("c4", "sample", "probs"), ("c5", "greedy", "probs"),
+                                              ("c5", "sample", "probs"), ("c5", "sample", "logits")])
+def test_pipeline_small(name, mode, q_mode):
     cfg = small(name, **SMALL[name])
     work = generate(cfg, "cuda")
-    exact, boundary, _ = compare_pipeline(cfg, work, mode, range(cfg.B))
+    exact, boundary, _ = compare_pipeline(cfg, work, mode, range(cfg.B), q_mode)
     assert exact >= cfg.B - 1, (exact, boundary)
 
 
-@pytest.mark.parametrize("name,mode", [("c2", "greedy"), ("c3", "sample"), ("c4", "sample"), ("c5", "greedy"),
-                                       ("c5", "sample")])
-def test_pipeline_full_size_sampled_requests(name, mode):
+@pytest.mark.parametrize("name,mode,q_mode", [("c2", "greedy", "probs"), ("c3", "sample", "logits"),
+                                              ("c4", "sample", "probs"), ("c5", "greedy", "probs"),
+                                              ("c5", "sample", "logits")])
+def test_pipeline_full_size_sampled_requests(name, mode, q_mode):
     """Full-size workloads in the bench's launch configuration; the oracle
     recomputes a few requests one by one."""
     cfg = CONFIGS[name].scaled(page_size=0, bytes_per_slot=0)
     work = generate(cfg, "cuda")
     reqs = [0, cfg.B // 2, cfg.B - 1]
-    exact, boundary, out = compare_pipeline(cfg, work, mode, reqs)
+    exact, boundary, out = compare_pipeline(cfg, work, mode, reqs, q_mode)
     assert exact >= len(reqs) - 1, (exact, boundary)
     al = out["accept_length"].float().mean().item()
     assert 0.0 <= al < cfg.N
@@ -293,6 +297,24 @@ def test_verify_sample_tree_given_q_node_order():
     exact = sum(verify_compare(g, o, b, b, "sample") for b in range(B))
     assert exact >= B - 1
     assert int(stats[sd.STATS["q_zero"]]) == o["q_zero"]
+
+
+@pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
+def test_q_in_logit_form_equals_written_q(qdtype):
+    """spec_verify_sample_qlogits on (draft logits, row max/normaliser) gives
+    exactly spec_verify_sample's result on the probabilities the draft kernel
+    writes for the same rows."""
+    rng = np.random.default_rng(5)
+    B, k, steps, N, V = 16, 4, 4, 14, 3001
+    cfg = CONFIGS["c3"].scaled(B=B, topk=k, steps=steps, N=N, V=V, dtype=qdtype, page_size=0, bytes_per_slot=0)
+    work = generate(cfg, "cuda")
+    outs = []
+    for q_mode in ("probs", "logits"):
+        buf, tree, out = run_gpu_pipeline(cfg, work, "sample", q_mode)
+        outs.append({n: v.clone() for n, v in out.items()})
+    for n in outs[0]:
+        assert torch.equal(outs[0][n], outs[1][n]), n
+    assert int(outs[0]["accept_length"].sum()) > 0
 
 
 def test_worked_example_monte_carlo_gpu(golden):
