@@ -208,6 +208,29 @@ inline int launch_status() {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Grid of a persistent kernel: as many CTAs as fit on the device at once
+// (SM count x resident CTAs per SM), but no more than there are work items.
+// Sets the dynamic shared-memory limit first when it exceeds the default.
+template <class Kernel>
+inline int persistent_grid(Kernel kernel, int threads, size_t smem, int64_t items, int* err) {
+  *err = SPEC_OK;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess) {
+    *err = SPEC_ERR_CUDA;
+    return 0;
+  }
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1) {
+    *err = SPEC_ERR_CUDA;
+    return 0;
+  }
+  const int64_t g = static_cast<int64_t>(sms) * per_sm;
+  return static_cast<int>(items < g ? items : g);
+}
+
 }  // namespace specdec
 
 namespace specdec {

@@ -16,12 +16,14 @@
 
 #include "cdf.cuh"
 #include "common.cuh"
+#include "stream.cuh"
 
 namespace specdec {
 namespace {
 
 constexpr int kDraftThreads = 512;
-constexpr int kCandCap = 512;  // candidate slots per warp
+constexpr int kCandCap = 320;  // candidate slots per warp
+constexpr int kFlushAt = 64;   // merge once more candidates than this wait
 
 // Running online-softmax partials of one thread: m = max key seen,
 // s = sum 2^((x - m) c).
@@ -48,22 +50,27 @@ struct SoftmaxPartial {
 // Warp-select top-K: each warp keeps its current top-K (sorted) and a
 // candidate buffer in shared memory.  An element is a candidate only if its
 // key is >= the warp's current K-th best value (a key below it can never
-// enter the top-K), so after the first few vectors candidates are rare.
-// When the buffer runs full the warp merges buffer and list back into a
-// sorted top-K (K rounds of a warp-wide (value desc, index asc) argmax).
+// enter the top-K), so after the first few vectors candidates are rare and
+// the common element costs one compare.  Candidates are appended with a
+// shared-memory atomic; the buffer order does not matter because the merge
+// selects by (value desc, index asc).  Once more than kFlushAt candidates
+// wait, the warp merges buffer and list back into a sorted top-K (K rounds
+// of a warp-wide argmax) and raises its threshold.
 template <int K>
 struct WarpSel {
   float bv[kCandCap];
   int bi[kCandCap];
   float lv[K];
   int li[K];
+  int cnt;
 };
 
-// Merge `n` entries (e < K from the list, the rest from the buffer) into the
-// sorted list.  Warp-synchronous; all lanes call it.
+// Merge the list and the cnt buffered candidates into the sorted list.
+// Warp-synchronous; all lanes call it.
 template <int K>
-__device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, int n, float& thr, int lane) {
+__device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, float& thr, int lane) {
   __syncwarp();
+  const int n = w.cnt + K;
   float nv = neg_inf();
   int ni = INT_MAX;
   for (int r = 0; r < K; ++r) {
@@ -100,6 +107,7 @@ __device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, int n, float& t
     w.lv[lane] = nv;
     w.li[lane] = ni;
   }
+  if (lane == 0) w.cnt = 0;
   thr = __shfl_sync(0xffffffffu, nv, K - 1);
   __syncwarp();
 }
@@ -108,9 +116,20 @@ template <int K>
 struct DraftVisitor {
   SoftmaxPartial sp;
   WarpSel<K>* w;
-  int cnt;    // warp-uniform candidate count
   float thr;  // warp-uniform K-th best value so far
   int lane;
+
+  __device__ __forceinline__ void reset() {
+    sp.m = neg_inf();
+    sp.s = 0.0f;
+    thr = neg_inf();
+    if (lane < K) {
+      w->lv[lane] = neg_inf();
+      w->li[lane] = INT_MAX;
+    }
+    if (lane == 0) w->cnt = 0;
+    __syncwarp();
+  }
 
   template <int N>
   __device__ __forceinline__ void visit(const float* xin, int64_t first, bool ok) {
@@ -118,31 +137,23 @@ struct DraftVisitor {
 #pragma unroll
     for (int j = 0; j < N; ++j) x[j] = order_key(xin[j]);
     const float vmax = sp.template update<N>(x);
-    if (!__any_sync(0xffffffffu, ok && vmax >= thr)) return;
-    int c = 0;
+    if (ok && vmax >= thr) {
 #pragma unroll
-    for (int j = 0; j < N; ++j) c += (ok && x[j] >= thr);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int pos = cnt + incl - c;
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      if (ok && x[j] >= thr) {
-        w->bv[pos] = x[j];
-        w->bi[pos] = static_cast<int>(first) + j;
-        ++pos;
+      for (int j = 0; j < N; ++j) {
+        if (x[j] >= thr) {
+          const int pos = atomicAdd(&w->cnt, 1);
+          w->bv[pos] = x[j];
+          w->bi[pos] = static_cast<int>(first) + j;
+        }
       }
     }
-    cnt += total;
-    if (cnt > kCandCap - 32 * N) {
-      warp_select_merge<K>(*w, cnt + K, thr, lane);
-      cnt = 0;
-    }
+    __syncwarp();
+    if (w->cnt > kFlushAt) warp_select_merge<K>(*w, thr, lane);
+  }
+
+  __device__ __forceinline__ void finish() {
+    __syncwarp();
+    if (w->cnt > 0) warp_select_merge<K>(*w, thr, lane);
   }
 };
 
@@ -212,95 +223,104 @@ struct ZeroWriter {
   }
 };
 
+constexpr int kDraftChunk = 16384;
+constexpr int kDraftStages = 4;
+
 template <int K>
 constexpr size_t draft_smem_bytes() {
-  return sizeof(WarpSel<K>) * (kDraftThreads / 32);
+  return sizeof(StreamSmem<kDraftChunk, kDraftStages>) + sizeof(WarpSel<K>) * (kDraftThreads / 32);
 }
 
+// Persistent: each CTA streams its rows through the shared-memory ring
+// (bulk copies) and keeps the online softmax per thread and the top-K per
+// warp; block merges are fixed-order.
 template <int DT, int K>
 __global__ void __launch_bounds__(kDraftThreads)
-    softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
+    softmax_topk_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kDraftThreads / 32;
-  extern __shared__ __align__(16) unsigned char dsm[];
-  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm);
+  extern __shared__ __align__(128) unsigned char dsm[];
+  auto* ring = reinterpret_cast<StreamSmem<kDraftChunk, kDraftStages>*>(dsm);
+  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm + sizeof(StreamSmem<kDraftChunk, kDraftStages>));
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t r = blockIdx.x;
-  const void* row = static_cast<const char*>(logits) + r * V * esz;
-  WarpSel<K>& w = sel[warp];
-  if (lane < K) {
-    w.lv[lane] = neg_inf();
-    w.li[lane] = INT_MAX;
-  }
-  __syncwarp();
-  DraftVisitor<K> st{{c, neg_inf(), 0.0f}, &w, 0, neg_inf(), lane};
-  for_row_uniform<DT, 4>(row, V, st);
-  if (st.cnt > 0) warp_select_merge<K>(w, st.cnt + K, st.thr, lane);
+  RowStreamer<esz, kDraftChunk, kDraftStages> streamer;
+  streamer.init(ring, logits, V, R);
+  DraftVisitor<K> st{{c, neg_inf(), 0.0f}, &sel[warp], neg_inf(), lane};
 
-  float m = st.sp.m, s = st.sp.s;
-  block_ms(m, s, c, sm, ss);  // its barriers also publish every warp's list
-  if (warp == 0) {
-    // merge the warps' sorted lists: K rounds over kWarps * K entries
-    for (int rr = 0; rr < K; ++rr) {
-      float bv = neg_inf();
-      int bi = INT_MAX, bpos = -1;
-      for (int e = lane; e < kWarps * K; e += 32) {
-        const float v = sel[e / K].lv[e % K];
-        const int i = sel[e / K].li[e % K];
-        if (before(v, i, bv, bi)) {
-          bv = v;
-          bi = i;
-          bpos = e;
+  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+    st.reset();
+    if (!stream_row<DT, kDraftChunk, kDraftStages>(streamer, r, st, stats)) {
+      streamer.drain();
+      return;
+    }
+    st.finish();
+    float m = st.sp.m, s = st.sp.s;
+    block_ms(m, s, c, sm, ss);  // its barriers also publish every warp's list
+    if (warp == 0) {
+      // merge the warps' sorted lists: K rounds over kWarps * K entries
+      for (int rr = 0; rr < K; ++rr) {
+        float bv = neg_inf();
+        int bi = INT_MAX, bpos = -1;
+        for (int e = lane; e < kWarps * K; e += 32) {
+          const float v = sel[e / K].lv[e % K];
+          const int i = sel[e / K].li[e % K];
+          if (before(v, i, bv, bi)) {
+            bv = v;
+            bi = i;
+            bpos = e;
+          }
+        }
+        float wv = bv;
+        int wi = bi;
+        warp_best(wv, wi);
+        if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
+          sel[bpos / K].lv[bpos % K] = neg_inf();
+          sel[bpos / K].li[bpos % K] = INT_MAX;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          fv[rr] = wv;
+          fi[rr] = wi;
         }
       }
-      float wv = bv;
-      int wi = bi;
-      warp_best(wv, wi);
-      if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
-        sel[bpos / K].lv[bpos % K] = neg_inf();
-        sel[bpos / K].li[bpos % K] = INT_MAX;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        fv[rr] = wv;
-        fi[rr] = wi;
-      }
     }
-  }
-  __syncthreads();
+    __syncthreads();
 
-  const bool finite = isfinite(m);
-  const float mc = m * c;
-  const float invz = 1.0f / s;
-  if (threadIdx.x < k) {
-    const int j = threadIdx.x;
-    topk_idx[r * k + j] = fi[j];
-    topk_p[r * k + j] = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
-  }
-  if (threadIdx.x == 0) {
-    if (!finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
-    if (row_stats != nullptr) {
-      row_stats[2 * r] = m;
-      row_stats[2 * r + 1] = s;
+    const bool finite = isfinite(m);
+    const float mc = m * c;
+    const float invz = 1.0f / s;
+    if (threadIdx.x < k) {
+      const int j = threadIdx.x;
+      topk_idx[r * k + j] = fi[j];
+      topk_p[r * k + j] = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
     }
-  }
-  if (probs != nullptr) {
-    float* out = probs + r * V;
-    if (finite) {
-      const RowSpan sp = row_span<DT>(row, V);
-      ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
-      for_row<DT, 2>(row, V, pw);
-    } else {
-      ZeroWriter z{out};
-      for_row<DT, 2>(row, V, z);
+    if (threadIdx.x == 0) {
+      if (!finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
+      if (row_stats != nullptr) {
+        row_stats[2 * r] = m;
+        row_stats[2 * r + 1] = s;
+      }
     }
+    if (probs != nullptr) {
+      const void* row = static_cast<const char*>(logits) + r * V * esz;
+      float* out = probs + r * V;
+      if (finite) {
+        const RowSpan sp = row_span<DT>(row, V);
+        ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
+        for_row<DT, 2>(row, V, pw);
+      } else {
+        ZeroWriter z{out};
+        for_row<DT, 2>(row, V, z);
+      }
+    }
+    __syncthreads();  // fv / fi / sm / ss and the warp lists are reused by the next row
   }
 }
 
@@ -384,12 +404,11 @@ template <int DT, int K>
 int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
                         int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
   constexpr size_t smem = draft_smem_bytes<K>();
-  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem)) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  softmax_topk_kernel<DT, K><<<static_cast<unsigned>(R), kDraftThreads, smem, s>>>(
-      logits, V, c, k, topk_p, topk_idx, probs, row_stats, stats);
+  int err;
+  const int grid = persistent_grid(softmax_topk_kernel<DT, K>, kDraftThreads, smem, R, &err);
+  if (err != SPEC_OK) return err;
+  softmax_topk_kernel<DT, K><<<grid, kDraftThreads, smem, s>>>(logits, V, R, c, k, topk_p, topk_idx, probs,
+                                                                row_stats, stats);
   return launch_status();
 }
 

@@ -30,6 +30,7 @@
 
 #include "cdf.cuh"
 #include "common.cuh"
+#include "stream.cuh"
 
 namespace specdec {
 namespace {
@@ -46,7 +47,7 @@ struct RowStatVisitor {
   float c, m, s;
   int bi;
   template <int N>
-  __device__ __forceinline__ void visit(const float* xin, int64_t first) {
+  __device__ __forceinline__ void visit(const float* xin, int64_t first, bool) {
     float x[N];
     float vmax = neg_inf();
 #pragma unroll
@@ -71,50 +72,74 @@ struct RowStatVisitor {
   }
 };
 
+constexpr int kStreamChunk = 16384;
+constexpr int kStreamStages = 4;
+
+// Pass 1: one persistent CTA streams its rows through the shared-memory
+// ring (bulk copies, 4 x 16 KB in flight) and reduces each row to its
+// argmax and, for sampling, online-softmax max and normaliser.
 template <int DT, bool STOCH>
 __global__ void __launch_bounds__(kStatThreads)
-    row_stats_kernel(const void* __restrict__ logits, int64_t V, float c, int32_t* __restrict__ amax,
+    row_stats_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int32_t* __restrict__ amax,
                      float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kStatThreads / 32;
+  extern __shared__ __align__(128) unsigned char dsm[];
+  auto* ring = reinterpret_cast<StreamSmem<kStreamChunk, kStreamStages>*>(dsm);
   __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
   __shared__ int wi[kWarps];
-  const int64_t r = blockIdx.x;
-  const void* row = static_cast<const char*>(logits) + r * V * esz;
-  RowStatVisitor<STOCH> st{c, neg_inf(), 0.0f, INT_MAX};
-  for_row<DT, 4>(row, V, st);
-
+  RowStreamer<esz, kStreamChunk, kStreamStages> st;
+  st.init(ring, logits, V, R);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float bv = st.m;
-  int bi = st.bi;
-  warp_best(bv, bi);
-  float m = st.m, s = st.s;
-  if (STOCH) warp_merge_ms(m, s, c);
-  if (lane == 0) {
-    wv[warp] = bv;
-    wi[warp] = bi;
-    wm[warp] = m;
-    ws[warp] = s;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    bv = lane < kWarps ? wv[lane] : neg_inf();
-    bi = lane < kWarps ? wi[lane] : INT_MAX;
+  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+    RowStatVisitor<STOCH> v{c, neg_inf(), 0.0f, INT_MAX};
+    if (!stream_row<DT, kStreamChunk, kStreamStages>(st, r, v, stats)) {
+      st.drain();
+      return;
+    }
+    float bv = v.m;
+    int bi = v.bi;
     warp_best(bv, bi);
-    if (STOCH) {
-      m = lane < kWarps ? wm[lane] : neg_inf();
-      s = lane < kWarps ? ws[lane] : 0.0f;
-      warp_merge_ms(m, s, c);
-    }
+    float m = v.m, s = v.s;
+    if (STOCH) warp_merge_ms(m, s, c);
     if (lane == 0) {
-      amax[r] = bi == INT_MAX ? 0 : bi;
-      if (STOCH) {
-        m_out[r] = m;
-        z_out[r] = s;
-      }
-      if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
+      wv[warp] = bv;
+      wi[warp] = bi;
+      wm[warp] = m;
+      ws[warp] = s;
     }
+    __syncthreads();
+    if (warp == 0) {
+      bv = lane < kWarps ? wv[lane] : neg_inf();
+      bi = lane < kWarps ? wi[lane] : INT_MAX;
+      warp_best(bv, bi);
+      if (STOCH) {
+        m = lane < kWarps ? wm[lane] : neg_inf();
+        s = lane < kWarps ? ws[lane] : 0.0f;
+        warp_merge_ms(m, s, c);
+      }
+      if (lane == 0) {
+        amax[r] = bi == INT_MAX ? 0 : bi;
+        if (STOCH) {
+          m_out[r] = m;
+          z_out[r] = s;
+        }
+        if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
+      }
+    }
+    __syncthreads();
   }
+}
+
+template <int DT, bool STOCH>
+int launch_row_stats(const void* logits, int64_t V, int64_t R, float c, int32_t* amax, float* m, float* z,
+                     int32_t* stats, cudaStream_t s) {
+  constexpr size_t smem = sizeof(StreamSmem<kStreamChunk, kStreamStages>);
+  int err;
+  const int grid = persistent_grid(row_stats_kernel<DT, STOCH>, kStatThreads, smem, R, &err);
+  if (err != SPEC_OK) return err;
+  row_stats_kernel<DT, STOCH><<<grid, kStatThreads, smem, s>>>(logits, V, R, c, amax, m, z, stats);
+  return launch_status();
 }
 
 // ------------------------------------------------------------ greedy walk
@@ -482,14 +507,12 @@ extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void
   if (rc <= 0) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   VerifyWs w = carve(ws, B, N);
-  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
-  if (dtype == SPEC_BF16)
-    row_stats_kernel<SPEC_BF16, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, w.amax, nullptr,
-                                                                     nullptr, stats_or_null);
-  else
-    row_stats_kernel<SPEC_F32, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, w.amax, nullptr,
-                                                                    nullptr, stats_or_null);
-  int e = launch_status();
+  const int64_t rows = static_cast<int64_t>(B) * N;
+  int e = dtype == SPEC_BF16
+              ? launch_row_stats<SPEC_BF16, false>(target_logits, V, rows, 0.0f, w.amax, nullptr, nullptr,
+                                                   stats_or_null, s)
+              : launch_row_stats<SPEC_F32, false>(target_logits, V, rows, 0.0f, w.amax, nullptr, nullptr,
+                                                  stats_or_null, s);
   if (e != SPEC_OK) return e;
   greedy_walk_kernel<<<B, 32, sizeof(int32_t) * 6 * N, s>>>(
       N, w.amax, draft_token, retrieve_next_token, retrieve_next_sibling, budget_or_null, eos_id, committed,
@@ -506,12 +529,11 @@ int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, Q
                          const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
                          int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                          int32_t* walk_info, int32_t* stats, VerifyWs w, cudaStream_t s) {
-  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
+  const int64_t rows = static_cast<int64_t>(B) * N;
   const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
   const size_t smem = sizeof(float) * (ntiles * (1 + kWalkThreads / 32) + 3 * static_cast<int64_t>(N)) +
                       sizeof(int32_t) * 6 * static_cast<int64_t>(N);
-  row_stats_kernel<DT, true><<<rows, kStatThreads, 0, s>>>(target, V, c, w.amax, w.m, w.z, stats);
-  int e = launch_status();
+  int e = launch_row_stats<DT, true>(target, V, rows, c, w.amax, w.m, w.z, stats, s);
   if (e != SPEC_OK) return e;
   if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<DT, QSrc>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -664,14 +686,12 @@ extern "C" int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, co
   int32_t* amax = noalloc_scratch();
   if (amax == nullptr) return SPEC_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(B) * N);
-  if (dtype == SPEC_BF16)
-    row_stats_kernel<SPEC_BF16, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, amax, nullptr,
-                                                                     nullptr, stats_or_null);
-  else
-    row_stats_kernel<SPEC_F32, false><<<rows, kStatThreads, 0, s>>>(target_logits, V, 0.0f, amax, nullptr,
-                                                                    nullptr, stats_or_null);
-  int e = launch_status();
+  const int64_t rows = static_cast<int64_t>(B) * N;
+  int e = dtype == SPEC_BF16
+              ? launch_row_stats<SPEC_BF16, false>(target_logits, V, rows, 0.0f, amax, nullptr, nullptr,
+                                                   stats_or_null, s)
+              : launch_row_stats<SPEC_F32, false>(target_logits, V, rows, 0.0f, amax, nullptr, nullptr,
+                                                  stats_or_null, s);
   if (e != SPEC_OK) return e;
   greedy_walk_kernel<<<B, 32, sizeof(int32_t) * 6 * N, s>>>(
       N, amax, draft_token, retrieve_next_token, retrieve_next_sibling, budget_or_null, eos_id, committed,
