@@ -25,35 +25,29 @@ namespace specdec {
 //              float at(int64_t v) const
 template <int THREADS, class W>
 __device__ float cdf_tile_pass(const W& w, int64_t V, float* red, float* tile_sum) {
-  constexpr int kTile = THREADS * 8, kWarps = THREADS / 32;
+  constexpr int kTile = THREADS * 8, kWarps = THREADS / 32, kUnroll = 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ntiles = (V + kTile - 1) / kTile;
-  int64_t t = 0;
-  for (; t + 1 < ntiles; t += 2) {
-    float x0[8], x1[8];
-    w.load8(t * kTile + threadIdx.x * 8, x0);
-    w.load8((t + 1) * kTile + threadIdx.x * 8, x1);
-    float s0 = 0.0f, s1 = 0.0f;
+  // kUnroll tiles per iteration: all their loads are issued before the sums
+  for (int64_t t = 0; t < ntiles; t += kUnroll) {
+    float x[kUnroll][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      s0 += x0[j];
-      s1 += x1[j];
-    }
-    s0 = warp_sum(s0);
-    s1 = warp_sum(s1);
-    if (lane == 0) {
-      red[t * kWarps + warp] = s0;
-      red[(t + 1) * kWarps + warp] = s1;
-    }
-  }
-  for (; t < ntiles; ++t) {
-    float x0[8];
-    w.load8(t * kTile + threadIdx.x * 8, x0);
-    float s0 = 0.0f;
+    for (int u = 0; u < kUnroll; ++u) {
+      if (t + u < ntiles) {
+        w.load8((t + u) * kTile + threadIdx.x * 8, x[u]);
+      } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s0 += x0[j];
-    s0 = warp_sum(s0);
-    if (lane == 0) red[t * kWarps + warp] = s0;
+        for (int j = 0; j < 8; ++j) x[u][j] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      float s0 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s0 += x[u][j];
+      s0 = warp_sum(s0);
+      if (lane == 0 && t + u < ntiles) red[(t + u) * kWarps + warp] = s0;
+    }
   }
   __syncthreads();
   for (int64_t i = threadIdx.x; i < ntiles; i += THREADS) {

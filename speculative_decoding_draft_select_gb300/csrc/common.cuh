@@ -189,6 +189,8 @@ struct RowSpan {
 //   template <int N> void visit(const float* x, int64_t first_index).
 template <int DT, int UNROLL, class F>
 __device__ __forceinline__ void for_row(const void* row, int64_t V, F& f);
+template <int DT, int UNROLL, class F>
+__device__ __forceinline__ void for_row(const void* row, int64_t V, F& f, int tid, int nthreads);
 
 template <int DT>
 __device__ __forceinline__ RowSpan row_span(const void* row, int64_t V) {
@@ -236,17 +238,17 @@ inline int persistent_grid(Kernel kernel, int threads, size_t smem, int64_t item
 namespace specdec {
 
 template <int DT, int UNROLL, class F>
-__device__ __forceinline__ void for_row(const void* row, int64_t V, F& f) {
+__device__ __forceinline__ void for_row(const void* row, int64_t V, F& f, int tid, int nthreads) {
   constexpr int kv = Logit<DT>::kVec;
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   const RowSpan sp = row_span<DT>(row, V);
-  const int64_t nt = blockDim.x;
-  for (int64_t i = threadIdx.x; i < sp.head; i += nt) {
+  const int64_t nt = nthreads;
+  for (int64_t i = tid; i < sp.head; i += nt) {
     float x = Logit<DT>::load1(row, i);
     f.template visit<1>(&x, i);
   }
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
-  int64_t i = threadIdx.x;
+  int64_t i = tid;
   for (; i + (UNROLL - 1) * nt < sp.nvec; i += UNROLL * nt) {
     uint4 v[UNROLL];
 #pragma unroll
@@ -263,10 +265,15 @@ __device__ __forceinline__ void for_row(const void* row, int64_t V, F& f) {
     unpack<DT>(ld_stream(vp + i), x);
     f.template visit<kv>(x, sp.head + i * kv);
   }
-  for (int64_t t = sp.head + sp.nvec * kv + threadIdx.x; t < V; t += nt) {
+  for (int64_t t = sp.head + sp.nvec * kv + tid; t < V; t += nt) {
     float x = Logit<DT>::load1(row, t);
     f.template visit<1>(&x, t);
   }
+}
+
+template <int DT, int UNROLL, class F>
+__device__ __forceinline__ void for_row(const void* row, int64_t V, F& f) {
+  for_row<DT, UNROLL>(row, V, f, static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x));
 }
 
 }  // namespace specdec

@@ -157,15 +157,28 @@ struct DraftVisitor {
   }
 };
 
-// Block merge of (m, s) partials; every thread receives the row's (m, s).
+// Merge of (m, s) partials over the first NT threads (whole warps); every
+// one of them receives the row's (m, s).  NT == blockDim.x uses
+// __syncthreads, otherwise the consumer-warp named barrier.
+template <int NT>
+__device__ __forceinline__ void group_sync() {
+  if (NT == 0) {
+    __syncthreads();
+  } else {
+    consumer_sync(NT);
+  }
+}
+
+template <int NT>
 __device__ __forceinline__ void block_ms(float& m, float& s, float c, float* sm, float* ss) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (NT == 0 ? static_cast<int>(blockDim.x) : NT) >> 5;
   warp_merge_ms(m, s, c);
   if (lane == 0) {
     sm[warp] = m;
     ss[warp] = s;
   }
-  __syncthreads();
+  group_sync<NT>();
   if (warp == 0) {
     float mm = lane < nw ? sm[lane] : neg_inf();
     float s2 = lane < nw ? ss[lane] : 0.0f;
@@ -175,7 +188,7 @@ __device__ __forceinline__ void block_ms(float& m, float& s, float c, float* sm,
       ss[32] = s2;
     }
   }
-  __syncthreads();
+  group_sync<NT>();
   m = sm[32];
   s = ss[32];
 }
@@ -223,52 +236,55 @@ struct ZeroWriter {
   }
 };
 
-constexpr int kDraftChunk = 16384;
+constexpr int kDraftChunk = 32768;
 constexpr int kDraftStages = 4;
+constexpr int kDraftWarps = kDraftThreads / 32;     // consumer warps
+constexpr int kDraftBlock = kDraftThreads + 32;     // + the producer warp
+using DraftPipeSmem = PipeSmem<kDraftChunk, kDraftStages>;
 
 template <int K>
 constexpr size_t draft_smem_bytes() {
-  return sizeof(StreamSmem<kDraftChunk, kDraftStages>) + sizeof(WarpSel<K>) * (kDraftThreads / 32);
+  return sizeof(DraftPipeSmem) + sizeof(WarpSel<K>) * kDraftWarps;
 }
 
-// Persistent: each CTA streams its rows through the shared-memory ring
-// (bulk copies) and keeps the online softmax per thread and the top-K per
-// warp; block merges are fixed-order.
+// Persistent (one CTA per SM): the producer warp streams the CTA's rows
+// through the shared-memory ring (bulk copies, 4 x 32 KB in flight); 16
+// consumer warps keep the online softmax per thread and the top-K per warp;
+// merges are fixed-order.
 template <int DT, int K>
-__global__ void __launch_bounds__(kDraftThreads)
+__global__ void __launch_bounds__(kDraftBlock, 1)
     softmax_topk_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  constexpr int kWarps = kDraftThreads / 32;
   extern __shared__ __align__(128) unsigned char dsm[];
-  auto* ring = reinterpret_cast<StreamSmem<kDraftChunk, kDraftStages>*>(dsm);
-  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm + sizeof(StreamSmem<kDraftChunk, kDraftStages>));
+  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm + sizeof(DraftPipeSmem));
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  RowStreamer<esz, kDraftChunk, kDraftStages> streamer;
-  streamer.init(ring, logits, V, R);
+  RowPipe<esz, kDraftChunk, kDraftStages, kDraftWarps> pipe;
+  pipe.init(reinterpret_cast<DraftPipeSmem*>(dsm), logits, V, R);
+  if (warp == kDraftWarps) {
+    if (lane == 0) pipe.produce(stats);
+    return;
+  }
   DraftVisitor<K> st{{c, neg_inf(), 0.0f}, &sel[warp], neg_inf(), lane};
-
+  bool aborted = false;
   for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
     st.reset();
-    if (!stream_row<DT, kDraftChunk, kDraftStages>(streamer, r, st, stats)) {
-      streamer.drain();
-      return;
-    }
+    pipe_row<DT, kDraftChunk, kDraftStages, kDraftWarps>(pipe, r, st, stats, aborted);
     st.finish();
     float m = st.sp.m, s = st.sp.s;
-    block_ms(m, s, c, sm, ss);  // its barriers also publish every warp's list
+    block_ms<kDraftThreads>(m, s, c, sm, ss);  // its barriers also publish every warp's list
     if (warp == 0) {
-      // merge the warps' sorted lists: K rounds over kWarps * K entries
+      // merge the warps' sorted lists: K rounds over kDraftWarps * K entries
       for (int rr = 0; rr < K; ++rr) {
         float bv = neg_inf();
         int bi = INT_MAX, bpos = -1;
-        for (int e = lane; e < kWarps * K; e += 32) {
+        for (int e = lane; e < kDraftWarps * K; e += 32) {
           const float v = sel[e / K].lv[e % K];
           const int i = sel[e / K].li[e % K];
           if (before(v, i, bv, bi)) {
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(kDraftThreads)
         }
       }
     }
-    __syncthreads();
+    consumer_sync(kDraftThreads);
 
     const bool finite = isfinite(m);
     const float mc = m * c;
@@ -314,14 +330,15 @@ __global__ void __launch_bounds__(kDraftThreads)
       if (finite) {
         const RowSpan sp = row_span<DT>(row, V);
         ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
-        for_row<DT, 2>(row, V, pw);
+        for_row<DT, 2>(row, V, pw, threadIdx.x, kDraftThreads);
       } else {
         ZeroWriter z{out};
-        for_row<DT, 2>(row, V, z);
+        for_row<DT, 2>(row, V, z, threadIdx.x, kDraftThreads);
       }
     }
-    __syncthreads();  // fv / fi / sm / ss and the warp lists are reused by the next row
+    consumer_sync(kDraftThreads);  // fv / fi / sm / ss and the warp lists are reused by the next row
   }
+  pipe.finish();
 }
 
 // ---------------------------------------------------------------- sampling
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   StatsVisitor st{{c, neg_inf(), 0.0f}};
   for_row<DT, 4>(row, V, st);
   float m = st.sp.m, s = st.sp.s;
-  block_ms(m, s, c, sm, ss);
+  block_ms<0>(m, s, c, sm, ss);
   if (!isfinite(m)) {
     if (threadIdx.x == 0) {
       bump(stats, SPEC_STAT_NONFINITE_ROW);
@@ -405,10 +422,10 @@ int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k
                         int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
   constexpr size_t smem = draft_smem_bytes<K>();
   int err;
-  const int grid = persistent_grid(softmax_topk_kernel<DT, K>, kDraftThreads, smem, R, &err);
+  const int grid = persistent_grid(softmax_topk_kernel<DT, K>, kDraftBlock, smem, R, &err);
   if (err != SPEC_OK) return err;
-  softmax_topk_kernel<DT, K><<<grid, kDraftThreads, smem, s>>>(logits, V, R, c, k, topk_p, topk_idx, probs,
-                                                                row_stats, stats);
+  softmax_topk_kernel<DT, K><<<grid, kDraftBlock, smem, s>>>(logits, V, R, c, k, topk_p, topk_idx, probs,
+                                                              row_stats, stats);
   return launch_status();
 }
 

@@ -72,31 +72,36 @@ struct RowStatVisitor {
   }
 };
 
-constexpr int kStreamChunk = 16384;
-constexpr int kStreamStages = 4;
+constexpr int kPipeChunk = 32768;
+constexpr int kPipeStages = 4;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kPipeThreads = kConsumers + 32;  // + the producer warp
+using StatPipeSmem = PipeSmem<kPipeChunk, kPipeStages>;
 
-// Pass 1: one persistent CTA streams its rows through the shared-memory
-// ring (bulk copies, 4 x 16 KB in flight) and reduces each row to its
-// argmax and, for sampling, online-softmax max and normaliser.
+// Pass 1: persistent CTAs (one per SM); the producer warp streams the CTA's
+// rows through the shared-memory ring (4 x 32 KB bulk copies in flight) and
+// 16 consumer warps reduce each row to its argmax and, for sampling,
+// online-softmax max and normaliser.
 template <int DT, bool STOCH>
-__global__ void __launch_bounds__(kStatThreads)
+__global__ void __launch_bounds__(kPipeThreads, 1)
     row_stats_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int32_t* __restrict__ amax,
                      float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  constexpr int kWarps = kStatThreads / 32;
   extern __shared__ __align__(128) unsigned char dsm[];
-  auto* ring = reinterpret_cast<StreamSmem<kStreamChunk, kStreamStages>*>(dsm);
-  __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
-  __shared__ int wi[kWarps];
-  RowStreamer<esz, kStreamChunk, kStreamStages> st;
-  st.init(ring, logits, V, R);
+  __shared__ float wm[kConsumerWarps], ws[kConsumerWarps], wv[kConsumerWarps];
+  __shared__ int wi[kConsumerWarps];
+  RowPipe<esz, kPipeChunk, kPipeStages, kConsumerWarps> pipe;
+  pipe.init(reinterpret_cast<StatPipeSmem*>(dsm), logits, V, R);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) pipe.produce(stats);
+    return;
+  }
+  bool aborted = false;
   for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
     RowStatVisitor<STOCH> v{c, neg_inf(), 0.0f, INT_MAX};
-    if (!stream_row<DT, kStreamChunk, kStreamStages>(st, r, v, stats)) {
-      st.drain();
-      return;
-    }
+    pipe_row<DT, kPipeChunk, kPipeStages, kConsumerWarps>(pipe, r, v, stats, aborted);
     float bv = v.m;
     int bi = v.bi;
     warp_best(bv, bi);
@@ -108,14 +113,14 @@ __global__ void __launch_bounds__(kStatThreads)
       wm[warp] = m;
       ws[warp] = s;
     }
-    __syncthreads();
+    consumer_sync(kConsumers);
     if (warp == 0) {
-      bv = lane < kWarps ? wv[lane] : neg_inf();
-      bi = lane < kWarps ? wi[lane] : INT_MAX;
+      bv = lane < kConsumerWarps ? wv[lane] : neg_inf();
+      bi = lane < kConsumerWarps ? wi[lane] : INT_MAX;
       warp_best(bv, bi);
       if (STOCH) {
-        m = lane < kWarps ? wm[lane] : neg_inf();
-        s = lane < kWarps ? ws[lane] : 0.0f;
+        m = lane < kConsumerWarps ? wm[lane] : neg_inf();
+        s = lane < kConsumerWarps ? ws[lane] : 0.0f;
         warp_merge_ms(m, s, c);
       }
       if (lane == 0) {
@@ -127,18 +132,19 @@ __global__ void __launch_bounds__(kStatThreads)
         if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
       }
     }
-    __syncthreads();
+    consumer_sync(kConsumers);
   }
+  pipe.finish();
 }
 
 template <int DT, bool STOCH>
 int launch_row_stats(const void* logits, int64_t V, int64_t R, float c, int32_t* amax, float* m, float* z,
                      int32_t* stats, cudaStream_t s) {
-  constexpr size_t smem = sizeof(StreamSmem<kStreamChunk, kStreamStages>);
+  constexpr size_t smem = sizeof(StatPipeSmem);
   int err;
-  const int grid = persistent_grid(row_stats_kernel<DT, STOCH>, kStatThreads, smem, R, &err);
+  const int grid = persistent_grid(row_stats_kernel<DT, STOCH>, kPipeThreads, smem, R, &err);
   if (err != SPEC_OK) return err;
-  row_stats_kernel<DT, STOCH><<<grid, kStatThreads, smem, s>>>(logits, V, R, c, amax, m, z, stats);
+  row_stats_kernel<DT, STOCH><<<grid, kPipeThreads, smem, s>>>(logits, V, R, c, amax, m, z, stats);
   return launch_status();
 }
 
