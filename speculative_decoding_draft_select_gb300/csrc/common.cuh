@@ -89,6 +89,24 @@ __device__ __forceinline__ void unpack<SPEC_BF16>(const uint4& v, float* x) {
   x[7] = bf16_hi(v.w);
 }
 
+// A 16-byte vector of -inf logits.
+template <int DT>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+  const uint32_t w = DT == SPEC_BF16 ? 0xff80ff80u : 0xff800000u;
+  return make_uint4(w, w, w, w);
+}
+
+// Maximum of the 8 bf16 logits of a 16-byte vector, as a float: three packed
+// bf16x2 max operations and one scalar.  NaN elements are ignored (the max
+// of a NaN and a number is the number); eight NaNs give NaN.
+__device__ __forceinline__ float max8_bf16(const uint4& w) {
+  uint32_t a, b;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(w.x), "r"(w.y));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(w.z), "r"(w.w));
+  asm("max.bf16x2 %0, %0, %1;" : "+r"(a) : "r"(b));
+  return fmaxf(bf16_lo(a), bf16_hi(a));
+}
+
 // (value desc, index asc): true if (va, ia) comes before (vb, ib).
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);

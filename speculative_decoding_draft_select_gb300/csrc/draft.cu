@@ -112,16 +112,16 @@ __device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, float& thr, int
   __syncwarp();
 }
 
-template <int K>
+template <int DT, int K>
 struct DraftVisitor {
-  SoftmaxPartial sp;
+  float c, m, s0, s1;  // online softmax (two accumulators)
   WarpSel<K>* w;
-  float thr;  // warp-uniform K-th best value so far
+  float thr;           // warp-uniform K-th best value so far
   int lane;
 
   __device__ __forceinline__ void reset() {
-    sp.m = neg_inf();
-    sp.s = 0.0f;
+    m = neg_inf();
+    s0 = s1 = 0.0f;
     thr = neg_inf();
     if (lane < K) {
       w->lv[lane] = neg_inf();
@@ -130,16 +130,59 @@ struct DraftVisitor {
     if (lane == 0) w->cnt = 0;
     __syncwarp();
   }
-
-  template <int N>
-  __device__ __forceinline__ void visit(const float* xin, int64_t first, bool ok) {
-    float x[N];
+  __device__ __forceinline__ void rescale(float nm) {
+    if (m == neg_inf()) {
+      s0 = s1 = 0.0f;
+    } else {
+      const float f = fast_exp2((m - nm) * c);
+      s0 *= f;
+      s1 *= f;
+    }
+    m = nm;
+  }
+  __device__ __forceinline__ void flush_check() {
+    __syncwarp();
+    if (w->cnt > kFlushAt) warp_select_merge<K>(*w, thr, lane);
+  }
+  // Scalar ends of a row (NaN as -inf).
+  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
+    const float xk = order_key(x);
+    if (ok) {
+      if (xk > m) rescale(xk);
+      if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
+      if (xk >= thr) {
+        const int pos = atomicAdd(&w->cnt, 1);
+        w->bv[pos] = xk;
+        w->bi[pos] = static_cast<int>(idx);
+      }
+    }
+    flush_check();
+  }
+  // A 16-byte vector.  NaN elements are skipped by the max and never become
+  // candidates (NaN >= thr is false); they turn the sum into NaN, which the
+  // kernel repairs for that row.
+  __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool ok) {
+    constexpr int kv = Logit<DT>::kVec;
+    float x[kv];
+    unpack<DT>(raw, x);
+    float vmax;
+    if (DT == SPEC_BF16) {
+      vmax = max8_bf16(raw);
+    } else {
+      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
+    }
+    if (vmax > m) rescale(vmax);
+    if (m != neg_inf()) {
+      const float mc = m * c;
 #pragma unroll
-    for (int j = 0; j < N; ++j) x[j] = order_key(xin[j]);
-    const float vmax = sp.template update<N>(x);
+      for (int j = 0; j < kv; j += 2) {
+        s0 += fast_exp2(fmaf(x[j], c, -mc));
+        s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
+      }
+    }
     if (ok && vmax >= thr) {
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
+      for (int j = 0; j < kv; ++j) {
         if (x[j] >= thr) {
           const int pos = atomicAdd(&w->cnt, 1);
           w->bv[pos] = x[j];
@@ -147,13 +190,22 @@ struct DraftVisitor {
         }
       }
     }
-    __syncwarp();
-    if (w->cnt > kFlushAt) warp_select_merge<K>(*w, thr, lane);
+    flush_check();
   }
 
   __device__ __forceinline__ void finish() {
     __syncwarp();
     if (w->cnt > 0) warp_select_merge<K>(*w, thr, lane);
+  }
+};
+
+// Sum of 2^((key(x) - m) c) over a row with NaN as -inf.
+struct KeyedSum {
+  float c, mc, s;
+  template <int N>
+  __device__ __forceinline__ void visit(const float* x, int64_t) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) s += fast_exp2(fmaf(order_key(x[j]), c, -mc));
   }
 };
 
@@ -236,7 +288,7 @@ struct ZeroWriter {
   }
 };
 
-constexpr int kDraftChunk = 32768;
+constexpr int kDraftChunk = 16384;
 constexpr int kDraftStages = 4;
 constexpr int kDraftWarps = kDraftThreads / 32;     // consumer warps
 constexpr int kDraftBlock = kDraftThreads + 32;     // + the producer warp
@@ -247,12 +299,12 @@ constexpr size_t draft_smem_bytes() {
   return sizeof(DraftPipeSmem) + sizeof(WarpSel<K>) * kDraftWarps;
 }
 
-// Persistent (one CTA per SM): the producer warp streams the CTA's rows
-// through the shared-memory ring (bulk copies, 4 x 32 KB in flight); 16
+// Persistent (two CTAs per SM): the producer warp streams the CTA's rows
+// through the shared-memory ring (bulk copies, 4 x 16 KB in flight); 16
 // consumer warps keep the online softmax per thread and the top-K per warp;
 // merges are fixed-order.
 template <int DT, int K>
-__global__ void __launch_bounds__(kDraftBlock, 1)
+__global__ void __launch_bounds__(kDraftBlock, 2)
     softmax_topk_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
@@ -271,14 +323,27 @@ __global__ void __launch_bounds__(kDraftBlock, 1)
     if (lane == 0) pipe.produce(stats);
     return;
   }
-  DraftVisitor<K> st{{c, neg_inf(), 0.0f}, &sel[warp], neg_inf(), lane};
+  DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), lane};
   bool aborted = false;
   for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+    const void* row = static_cast<const char*>(logits) + r * V * esz;
     st.reset();
     pipe_row<DT, kDraftChunk, kDraftStages, kDraftWarps>(pipe, r, st, stats, aborted);
     st.finish();
-    float m = st.sp.m, s = st.sp.s;
+    float m = st.m, s = st.s0 + st.s1;
     block_ms<kDraftThreads>(m, s, c, sm, ss);  // its barriers also publish every warp's list
+    if (isfinite(m) && !isfinite(s)) {
+      // the row holds a NaN: recompute the normaliser with NaN as -inf
+      KeyedSum ks{c, m * c, 0.0f};
+      for_row<DT, 2>(row, V, ks, threadIdx.x, kDraftThreads);
+      float part = warp_sum(ks.s);
+      consumer_sync(kDraftThreads);
+      if (lane == 0) ss[warp] = part;
+      consumer_sync(kDraftThreads);
+      float tot = 0.0f;
+      for (int w2 = 0; w2 < kDraftWarps; ++w2) tot += ss[w2];
+      s = tot;
+    }
     if (warp == 0) {
       // merge the warps' sorted lists: K rounds over kDraftWarps * K entries
       for (int rr = 0; rr < K; ++rr) {
@@ -306,6 +371,31 @@ __global__ void __launch_bounds__(kDraftBlock, 1)
           fi[rr] = wi;
         }
       }
+      if (fi[k - 1] == INT_MAX && k <= V) {
+        // fewer than k non-NaN logits: rank the row again with NaN as -inf,
+        // each pick the best element after the previous one in the order
+        float pv = neg_inf();
+        int pi = -1;
+        for (int rr = 0; rr < k; ++rr) {
+          float bv = neg_inf();
+          int bi = INT_MAX;
+          for (int64_t v = lane; v < V; v += 32) {
+            const float x = order_key(Logit<DT>::load1(row, v));
+            if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
+              bv = x;
+              bi = static_cast<int>(v);
+            }
+          }
+          warp_best(bv, bi);
+          if (lane == 0) {
+            fv[rr] = bv;
+            fi[rr] = bi;
+          }
+          pv = bv;
+          pi = bi;
+          __syncwarp();
+        }
+      }
     }
     consumer_sync(kDraftThreads);
 
@@ -325,7 +415,6 @@ __global__ void __launch_bounds__(kDraftBlock, 1)
       }
     }
     if (probs != nullptr) {
-      const void* row = static_cast<const char*>(logits) + r * V * esz;
       float* out = probs + r * V;
       if (finite) {
         const RowSpan sp = row_span<DT>(row, V);

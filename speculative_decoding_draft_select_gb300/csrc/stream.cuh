@@ -196,7 +196,10 @@ struct RowPipe {
 // Consumer threads: visit every element of row r once (the body through the
 // pipe, the ends with direct loads).  Within a warp every lane runs the same
 // number of visits (warp-uniform): consumer thread t sees the 16-byte vectors
-// t, t + NCW*32, ... of each chunk.  After an abort (`aborted` set, here or
+// t, t + NCW*32, ... of each chunk.  F provides
+//   void visit_vec(const uint4& raw, int64_t first_index, bool ok)
+//   void visit1(float x, int64_t index, bool ok)
+// (an invalid slot passes -inf values with ok = false).  After an abort (`aborted` set, here or
 // earlier) the row is skipped, but the caller still runs its per-row
 // barriers, so every consumer warp reaches the same barriers.
 template <int DT, int CHUNK, int NSTAGE, int NCW, class F>
@@ -211,8 +214,7 @@ __device__ __forceinline__ void pipe_row(RowPipe<DT == SPEC_BF16 ? 2 : 4, CHUNK,
   for (int64_t i0 = 0; i0 < rb.head; i0 += nt) {
     const int64_t i = i0 + threadIdx.x;
     const bool ok = i < rb.head;
-    float x = ok ? Logit<DT>::load1(row, i) : neg_inf();
-    f.template visit<1>(&x, i, ok);
+    f.visit1(ok ? Logit<DT>::load1(row, i) : neg_inf(), i, ok);
   }
   for (int64_t off = 0; off < rb.bytes; off += CHUNK) {
     const unsigned char* st = p.acquire(stats);
@@ -226,22 +228,15 @@ __device__ __forceinline__ void pipe_row(RowPipe<DT == SPEC_BF16 ? 2 : 4, CHUNK,
     for (int v0 = 0; v0 < nvec; v0 += nt) {
       const int v = v0 + static_cast<int>(threadIdx.x);
       const bool ok = v < nvec;
-      float x[kv];
-      if (ok) {
-        unpack<DT>(*reinterpret_cast<const uint4*>(st + v * 16), x);
-      } else {
-#pragma unroll
-        for (int j = 0; j < kv; ++j) x[j] = neg_inf();
-      }
-      f.template visit<kv>(x, first + static_cast<int64_t>(v) * kv, ok);
+      const uint4 raw = ok ? *reinterpret_cast<const uint4*>(st + v * 16) : neg_inf_vec<DT>();
+      f.visit_vec(raw, first + static_cast<int64_t>(v) * kv, ok);
     }
     p.release();
   }
   for (int64_t t0 = rb.tail0; t0 < p.V; t0 += nt) {
     const int64_t t = t0 + threadIdx.x;
     const bool ok = t < p.V;
-    float x = ok ? Logit<DT>::load1(row, t) : neg_inf();
-    f.template visit<1>(&x, t, ok);
+    f.visit1(ok ? Logit<DT>::load1(row, t) : neg_inf(), t, ok);
   }
 }
 

@@ -35,62 +35,101 @@
 namespace specdec {
 namespace {
 
-constexpr int kStatThreads = 512;
 constexpr int kWalkThreads = 512;
 
 __device__ __forceinline__ float prob_of(float key, float c, float mc, float invz) {
   return fminf(fast_exp2(fmaf(key, c, -mc)) * invz, 1.0f);
 }
 
-template <bool STOCH>
+// Per-thread row statistics: running max m (NaN ignored), the first index
+// holding it, and for sampling s = sum 2^((x - m) c) in two accumulators
+// (shorter dependency chains).  A NaN element turns s into NaN; the kernel
+// then recomputes s for that row with NaN as -inf.
+template <int DT, bool STOCH>
 struct RowStatVisitor {
-  float c, m, s;
+  float c, m, s0, s1;
   int bi;
-  template <int N>
-  __device__ __forceinline__ void visit(const float* xin, int64_t first, bool) {
-    float x[N];
-    float vmax = neg_inf();
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      x[j] = order_key(xin[j]);
-      vmax = fmaxf(vmax, x[j]);
+  __device__ __forceinline__ void rescale(float nm) {
+    if (STOCH) {
+      if (m == neg_inf()) {
+        s0 = s1 = 0.0f;
+      } else {
+        const float f = fast_exp2((m - nm) * c);
+        s0 *= f;
+        s1 *= f;
+      }
+    }
+    m = nm;
+  }
+  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
+    if (!ok) return;
+    const float xk = order_key(x);
+    if (xk > m) {
+      rescale(xk);
+      bi = static_cast<int>(idx);
+    }
+    if (STOCH && m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
+  }
+  __device__ __forceinline__ void visit_vec(const uint4& w, int64_t first, bool) {
+    constexpr int kv = Logit<DT>::kVec;
+    float x[kv];
+    unpack<DT>(w, x);
+    float vmax;
+    if (DT == SPEC_BF16) {
+      vmax = max8_bf16(w);
+    } else {
+      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
     }
     if (vmax > m) {
       int j0 = 0;
 #pragma unroll
-      for (int j = N - 1; j >= 0; --j)
+      for (int j = kv - 1; j >= 0; --j)
         if (x[j] == vmax) j0 = j;
+      rescale(vmax);
       bi = static_cast<int>(first) + j0;
-      if (STOCH) s = (m == neg_inf()) ? 0.0f : s * fast_exp2((m - vmax) * c);
-      m = vmax;
     }
     if (STOCH && m != neg_inf()) {
       const float mc = m * c;
 #pragma unroll
-      for (int j = 0; j < N; ++j) s += fast_exp2(fmaf(x[j], c, -mc));
+      for (int j = 0; j < kv; j += 2) {
+        s0 += fast_exp2(fmaf(x[j], c, -mc));
+        s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
+      }
     }
   }
 };
 
-constexpr int kPipeChunk = 32768;
+// Sum of 2^((key(x) - m) c) over a row with NaN as -inf (the slow path for
+// rows that contain NaN).
+struct KeyedSum {
+  float c, mc, s;
+  template <int N>
+  __device__ __forceinline__ void visit(const float* x, int64_t) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) s += fast_exp2(fmaf(order_key(x[j]), c, -mc));
+  }
+};
+
+constexpr int kPipeChunk = 16384;
 constexpr int kPipeStages = 4;
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kPipeThreads = kConsumers + 32;  // + the producer warp
 using StatPipeSmem = PipeSmem<kPipeChunk, kPipeStages>;
 
-// Pass 1: persistent CTAs (one per SM); the producer warp streams the CTA's
-// rows through the shared-memory ring (4 x 32 KB bulk copies in flight) and
+// Pass 1: persistent CTAs (two per SM); the producer warp streams the CTA's
+// rows through the shared-memory ring (4 x 16 KB bulk copies in flight) and
 // 16 consumer warps reduce each row to its argmax and, for sampling,
 // online-softmax max and normaliser.
 template <int DT, bool STOCH>
-__global__ void __launch_bounds__(kPipeThreads, 1)
+__global__ void __launch_bounds__(kPipeThreads, 2)
     row_stats_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int32_t* __restrict__ amax,
                      float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ float wm[kConsumerWarps], ws[kConsumerWarps], wv[kConsumerWarps];
   __shared__ int wi[kConsumerWarps];
+  __shared__ float s_m, s_s, s_bv;
   RowPipe<esz, kPipeChunk, kPipeStages, kConsumerWarps> pipe;
   pipe.init(reinterpret_cast<StatPipeSmem*>(dsm), logits, V, R);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -100,12 +139,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   }
   bool aborted = false;
   for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-    RowStatVisitor<STOCH> v{c, neg_inf(), 0.0f, INT_MAX};
+    RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX};
     pipe_row<DT, kPipeChunk, kPipeStages, kConsumerWarps>(pipe, r, v, stats, aborted);
     float bv = v.m;
     int bi = v.bi;
     warp_best(bv, bi);
-    float m = v.m, s = v.s;
+    float m = v.m, s = v.s0 + v.s1;
     if (STOCH) warp_merge_ms(m, s, c);
     if (lane == 0) {
       wv[warp] = bv;
@@ -125,14 +164,38 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       }
       if (lane == 0) {
         amax[r] = bi == INT_MAX ? 0 : bi;
-        if (STOCH) {
-          m_out[r] = m;
-          z_out[r] = s;
-        }
+        s_m = m;
+        s_s = s;
+        s_bv = bv;
         if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
       }
     }
     consumer_sync(kConsumers);
+    if (STOCH) {
+      m = s_m;
+      s = s_s;
+      if (isfinite(m) && !isfinite(s)) {
+        // the row holds a NaN: recompute the normaliser with NaN as -inf
+        const void* row = static_cast<const char*>(logits) + r * V * esz;
+        KeyedSum ks{c, m * c, 0.0f};
+        for_row<DT, 2>(row, V, ks, threadIdx.x, kConsumers);
+        float t = warp_sum(ks.s);
+        if (lane == 0) ws[warp] = t;
+        consumer_sync(kConsumers);
+        if (threadIdx.x == 0) {
+          float tot = 0.0f;
+          for (int w = 0; w < kConsumerWarps; ++w) tot += ws[w];
+          s_s = tot;
+        }
+        consumer_sync(kConsumers);
+        s = s_s;
+      }
+      if (threadIdx.x == 0) {
+        m_out[r] = m;
+        z_out[r] = s;
+      }
+      consumer_sync(kConsumers);
+    }
   }
   pipe.finish();
 }
