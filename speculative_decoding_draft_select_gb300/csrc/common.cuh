@@ -228,29 +228,6 @@ inline int launch_status() {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Grid of a persistent kernel: as many CTAs as fit on the device at once
-// (SM count x resident CTAs per SM), but no more than there are work items.
-// Sets the dynamic shared-memory limit first when it exceeds the default.
-template <class Kernel>
-inline int persistent_grid(Kernel kernel, int threads, size_t smem, int64_t items, int* err) {
-  *err = SPEC_OK;
-  int dev = 0, sms = 0, per_sm = 0;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-          cudaSuccess) {
-    *err = SPEC_ERR_CUDA;
-    return 0;
-  }
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1) {
-    *err = SPEC_ERR_CUDA;
-    return 0;
-  }
-  const int64_t g = static_cast<int64_t>(sms) * per_sm;
-  return static_cast<int>(items < g ? items : g);
-}
-
 }  // namespace specdec
 
 namespace specdec {
@@ -298,49 +275,42 @@ __device__ __forceinline__ void for_row(const void* row, int64_t V, F& f) {
 
 namespace specdec {
 
-// Like for_row, but every thread of the block runs the same number of visits,
-// so a visitor may use warp votes and shuffles: a thread with no element for
-// a slot gets visit(x = -inf..., first, valid = false).
+// Visit every element of a row once with 16-byte loads (UNROLL in flight per
+// thread), handing the visitor raw vectors.  Every thread runs the same
+// number of visits, so visitors may use warp votes and shuffles.  F provides
+//   void visit_vec(const uint4& raw, int64_t first_index, bool ok)
+//   void visit1(float x, int64_t index, bool ok)
+// and an invalid slot passes -inf values with ok = false.  Thread t sees the
+// vectors t, t + nthreads, ... (and the same for the scalar ends).
 template <int DT, int UNROLL, class F>
-__device__ __forceinline__ void for_row_uniform(const void* row, int64_t V, F& f) {
+__device__ __forceinline__ void for_row_raw(const void* row, int64_t V, F& f, int tid, int nthreads) {
   constexpr int kv = Logit<DT>::kVec;
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   const RowSpan sp = row_span<DT>(row, V);
-  const int64_t nt = blockDim.x;
+  const int64_t nt = nthreads;
   for (int64_t i0 = 0; i0 < sp.head; i0 += nt) {
-    const int64_t i = i0 + threadIdx.x;
+    const int64_t i = i0 + tid;
     const bool ok = i < sp.head;
-    float x = ok ? Logit<DT>::load1(row, i) : neg_inf();
-    f.template visit<1>(&x, i, ok);
+    f.visit1(ok ? Logit<DT>::load1(row, i) : neg_inf(), i, ok);
   }
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
   for (int64_t i0 = 0; i0 < sp.nvec; i0 += UNROLL * nt) {
     uint4 v[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      const int64_t i = i0 + threadIdx.x + u * nt;
-      if (i < sp.nvec) v[u] = ld_stream(vp + i);
+      const int64_t i = i0 + tid + u * nt;
+      v[u] = i < sp.nvec ? ld_stream(vp + i) : neg_inf_vec<DT>();
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      const int64_t i = i0 + threadIdx.x + u * nt;
-      const bool ok = i < sp.nvec;
-      float x[kv];
-      if (ok) {
-        unpack<DT>(v[u], x);
-      } else {
-#pragma unroll
-        for (int j = 0; j < kv; ++j) x[j] = neg_inf();
-      }
-      f.template visit<kv>(x, sp.head + i * kv, ok);
+      const int64_t i = i0 + tid + u * nt;
+      f.visit_vec(v[u], sp.head + i * kv, i < sp.nvec);
     }
   }
-  const int64_t t_begin = sp.head + sp.nvec * kv;
-  for (int64_t t0 = t_begin; t0 < V; t0 += nt) {
-    const int64_t t = t0 + threadIdx.x;
+  for (int64_t t0 = sp.head + sp.nvec * kv; t0 < V; t0 += nt) {
+    const int64_t t = t0 + tid;
     const bool ok = t < V;
-    float x = ok ? Logit<DT>::load1(row, t) : neg_inf();
-    f.template visit<1>(&x, t, ok);
+    f.visit1(ok ? Logit<DT>::load1(row, t) : neg_inf(), t, ok);
   }
 }
 

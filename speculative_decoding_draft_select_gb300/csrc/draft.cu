@@ -16,7 +16,6 @@
 
 #include "cdf.cuh"
 #include "common.cuh"
-#include "stream.cuh"
 
 namespace specdec {
 namespace {
@@ -209,28 +208,16 @@ struct KeyedSum {
   }
 };
 
-// Merge of (m, s) partials over the first NT threads (whole warps); every
-// one of them receives the row's (m, s).  NT == blockDim.x uses
-// __syncthreads, otherwise the consumer-warp named barrier.
-template <int NT>
-__device__ __forceinline__ void group_sync() {
-  if (NT == 0) {
-    __syncthreads();
-  } else {
-    consumer_sync(NT);
-  }
-}
-
-template <int NT>
+// Block merge of (m, s) partials; every thread receives the row's (m, s).
+template <int UNUSED>
 __device__ __forceinline__ void block_ms(float& m, float& s, float c, float* sm, float* ss) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = (NT == 0 ? static_cast<int>(blockDim.x) : NT) >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   warp_merge_ms(m, s, c);
   if (lane == 0) {
     sm[warp] = m;
     ss[warp] = s;
   }
-  group_sync<NT>();
+  __syncthreads();
   if (warp == 0) {
     float mm = lane < nw ? sm[lane] : neg_inf();
     float s2 = lane < nw ? ss[lane] : 0.0f;
@@ -240,7 +227,7 @@ __device__ __forceinline__ void block_ms(float& m, float& s, float c, float* sm,
       ss[32] = s2;
     }
   }
-  group_sync<NT>();
+  __syncthreads();
   m = sm[32];
   s = ss[32];
 }
@@ -288,146 +275,130 @@ struct ZeroWriter {
   }
 };
 
-constexpr int kDraftChunk = 16384;
-constexpr int kDraftStages = 4;
-constexpr int kDraftWarps = kDraftThreads / 32;     // consumer warps
-constexpr int kDraftBlock = kDraftThreads + 32;     // + the producer warp
-using DraftPipeSmem = PipeSmem<kDraftChunk, kDraftStages>;
-
 template <int K>
 constexpr size_t draft_smem_bytes() {
-  return sizeof(DraftPipeSmem) + sizeof(WarpSel<K>) * kDraftWarps;
+  return sizeof(WarpSel<K>) * (kDraftThreads / 32);
 }
 
-// Persistent (two CTAs per SM): the producer warp streams the CTA's rows
-// through the shared-memory ring (bulk copies, 4 x 16 KB in flight); 16
-// consumer warps keep the online softmax per thread and the top-K per warp;
-// merges are fixed-order.
+// One CTA per row: 16-byte loads (4 in flight per thread), the online
+// softmax per thread, the top-K per warp by warp select; merges are
+// fixed-order.
 template <int DT, int K>
-__global__ void __launch_bounds__(kDraftBlock, 2)
-    softmax_topk_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int k,
+__global__ void __launch_bounds__(kDraftThreads)
+    softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  extern __shared__ __align__(128) unsigned char dsm[];
-  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm + sizeof(DraftPipeSmem));
+  constexpr int kWarps = kDraftThreads / 32;
+  extern __shared__ __align__(16) unsigned char dsm[];
+  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm);
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  RowPipe<esz, kDraftChunk, kDraftStages, kDraftWarps> pipe;
-  pipe.init(reinterpret_cast<DraftPipeSmem*>(dsm), logits, V, R);
-  if (warp == kDraftWarps) {
-    if (lane == 0) pipe.produce(stats);
-    return;
-  }
+  const int64_t r = blockIdx.x;
+  const void* row = static_cast<const char*>(logits) + r * V * esz;
   DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), lane};
-  bool aborted = false;
-  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-    const void* row = static_cast<const char*>(logits) + r * V * esz;
-    st.reset();
-    pipe_row<DT, kDraftChunk, kDraftStages, kDraftWarps>(pipe, r, st, stats, aborted);
-    st.finish();
-    float m = st.m, s = st.s0 + st.s1;
-    block_ms<kDraftThreads>(m, s, c, sm, ss);  // its barriers also publish every warp's list
-    if (isfinite(m) && !isfinite(s)) {
-      // the row holds a NaN: recompute the normaliser with NaN as -inf
-      KeyedSum ks{c, m * c, 0.0f};
-      for_row<DT, 2>(row, V, ks, threadIdx.x, kDraftThreads);
-      float part = warp_sum(ks.s);
-      consumer_sync(kDraftThreads);
-      if (lane == 0) ss[warp] = part;
-      consumer_sync(kDraftThreads);
-      float tot = 0.0f;
-      for (int w2 = 0; w2 < kDraftWarps; ++w2) tot += ss[w2];
-      s = tot;
-    }
-    if (warp == 0) {
-      // merge the warps' sorted lists: K rounds over kDraftWarps * K entries
-      for (int rr = 0; rr < K; ++rr) {
-        float bv = neg_inf();
-        int bi = INT_MAX, bpos = -1;
-        for (int e = lane; e < kDraftWarps * K; e += 32) {
-          const float v = sel[e / K].lv[e % K];
-          const int i = sel[e / K].li[e % K];
-          if (before(v, i, bv, bi)) {
-            bv = v;
-            bi = i;
-            bpos = e;
-          }
-        }
-        float wv = bv;
-        int wi = bi;
-        warp_best(wv, wi);
-        if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
-          sel[bpos / K].lv[bpos % K] = neg_inf();
-          sel[bpos / K].li[bpos % K] = INT_MAX;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          fv[rr] = wv;
-          fi[rr] = wi;
-        }
-      }
-      if (fi[k - 1] == INT_MAX && k <= V) {
-        // fewer than k non-NaN logits: rank the row again with NaN as -inf,
-        // each pick the best element after the previous one in the order
-        float pv = neg_inf();
-        int pi = -1;
-        for (int rr = 0; rr < k; ++rr) {
-          float bv = neg_inf();
-          int bi = INT_MAX;
-          for (int64_t v = lane; v < V; v += 32) {
-            const float x = order_key(Logit<DT>::load1(row, v));
-            if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
-              bv = x;
-              bi = static_cast<int>(v);
-            }
-          }
-          warp_best(bv, bi);
-          if (lane == 0) {
-            fv[rr] = bv;
-            fi[rr] = bi;
-          }
-          pv = bv;
-          pi = bi;
-          __syncwarp();
-        }
-      }
-    }
-    consumer_sync(kDraftThreads);
-
-    const bool finite = isfinite(m);
-    const float mc = m * c;
-    const float invz = 1.0f / s;
-    if (threadIdx.x < k) {
-      const int j = threadIdx.x;
-      topk_idx[r * k + j] = fi[j];
-      topk_p[r * k + j] = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
-    }
-    if (threadIdx.x == 0) {
-      if (!finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
-      if (row_stats != nullptr) {
-        row_stats[2 * r] = m;
-        row_stats[2 * r + 1] = s;
-      }
-    }
-    if (probs != nullptr) {
-      float* out = probs + r * V;
-      if (finite) {
-        const RowSpan sp = row_span<DT>(row, V);
-        ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
-        for_row<DT, 2>(row, V, pw, threadIdx.x, kDraftThreads);
-      } else {
-        ZeroWriter z{out};
-        for_row<DT, 2>(row, V, z, threadIdx.x, kDraftThreads);
-      }
-    }
-    consumer_sync(kDraftThreads);  // fv / fi / sm / ss and the warp lists are reused by the next row
+  st.reset();
+  for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
+  st.finish();
+  float m = st.m, s = st.s0 + st.s1;
+  block_ms<0>(m, s, c, sm, ss);  // its barriers also publish every warp's list
+  if (isfinite(m) && !isfinite(s)) {
+    // the row holds a NaN: recompute the normaliser with NaN as -inf
+    KeyedSum ks{c, m * c, 0.0f};
+    for_row<DT, 2>(row, V, ks);
+    const float part = warp_sum(ks.s);
+    __syncthreads();
+    if (lane == 0) ss[warp] = part;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w2 = 0; w2 < kWarps; ++w2) tot += ss[w2];
+    s = tot;
   }
-  pipe.finish();
+  if (warp == 0) {
+    // merge the warps' sorted lists: K rounds over kWarps * K entries
+    for (int rr = 0; rr < K; ++rr) {
+      float bv = neg_inf();
+      int bi = INT_MAX, bpos = -1;
+      for (int e = lane; e < kWarps * K; e += 32) {
+        const float v = sel[e / K].lv[e % K];
+        const int i = sel[e / K].li[e % K];
+        if (before(v, i, bv, bi)) {
+          bv = v;
+          bi = i;
+          bpos = e;
+        }
+      }
+      float wv = bv;
+      int wi = bi;
+      warp_best(wv, wi);
+      if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
+        sel[bpos / K].lv[bpos % K] = neg_inf();
+        sel[bpos / K].li[bpos % K] = INT_MAX;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        fv[rr] = wv;
+        fi[rr] = wi;
+      }
+    }
+    if (fi[k - 1] == INT_MAX && k <= V) {
+      // fewer than k non-NaN logits: rank the row again with NaN as -inf,
+      // each pick the best element after the previous one in the order
+      float pv = neg_inf();
+      int pi = -1;
+      for (int rr = 0; rr < k; ++rr) {
+        float bv = neg_inf();
+        int bi = INT_MAX;
+        for (int64_t v = lane; v < V; v += 32) {
+          const float x = order_key(Logit<DT>::load1(row, v));
+          if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
+            bv = x;
+            bi = static_cast<int>(v);
+          }
+        }
+        warp_best(bv, bi);
+        if (lane == 0) {
+          fv[rr] = bv;
+          fi[rr] = bi;
+        }
+        pv = bv;
+        pi = bi;
+        __syncwarp();
+      }
+    }
+  }
+  __syncthreads();
+
+  const bool finite = isfinite(m);
+  const float mc = m * c;
+  const float invz = 1.0f / s;
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    topk_idx[r * k + j] = fi[j];
+    topk_p[r * k + j] = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
+  }
+  if (threadIdx.x == 0) {
+    if (!finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
+    if (row_stats != nullptr) {
+      row_stats[2 * r] = m;
+      row_stats[2 * r + 1] = s;
+    }
+  }
+  if (probs != nullptr) {
+    float* out = probs + r * V;
+    if (finite) {
+      const RowSpan sp = row_span<DT>(row, V);
+      ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
+      for_row<DT, 2>(row, V, pw);
+    } else {
+      ZeroWriter z{out};
+      for_row<DT, 2>(row, V, z);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- sampling
@@ -510,11 +481,12 @@ template <int DT, int K>
 int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
                         int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
   constexpr size_t smem = draft_smem_bytes<K>();
-  int err;
-  const int grid = persistent_grid(softmax_topk_kernel<DT, K>, kDraftBlock, smem, R, &err);
-  if (err != SPEC_OK) return err;
-  softmax_topk_kernel<DT, K><<<grid, kDraftBlock, smem, s>>>(logits, V, R, c, k, topk_p, topk_idx, probs,
-                                                              row_stats, stats);
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  softmax_topk_kernel<DT, K><<<static_cast<unsigned>(R), kDraftThreads, smem, s>>>(logits, V, c, k, topk_p,
+                                                                                   topk_idx, probs, row_stats, stats);
   return launch_status();
 }
 

@@ -30,7 +30,6 @@
 
 #include "cdf.cuh"
 #include "common.cuh"
-#include "stream.cuh"
 
 namespace specdec {
 namespace {
@@ -110,104 +109,80 @@ struct KeyedSum {
   }
 };
 
-constexpr int kPipeChunk = 16384;
-constexpr int kPipeStages = 4;
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kPipeThreads = kConsumers + 32;  // + the producer warp
-using StatPipeSmem = PipeSmem<kPipeChunk, kPipeStages>;
+constexpr int kStatThreads = 512;
 
-// Pass 1: persistent CTAs (two per SM); the producer warp streams the CTA's
-// rows through the shared-memory ring (4 x 16 KB bulk copies in flight) and
-// 16 consumer warps reduce each row to its argmax and, for sampling,
-// online-softmax max and normaliser.
+// Pass 1: one CTA per target row streams it with 16-byte loads (4 in
+// flight per thread) and reduces it to its argmax and, for sampling, the
+// online-softmax max and normaliser.  Measured on GB300 this plain load loop
+// keeps HBM at the copy rate; staging through shared memory with bulk
+// copies was slower for this access pattern.
 template <int DT, bool STOCH>
-__global__ void __launch_bounds__(kPipeThreads, 2)
-    row_stats_kernel(const void* __restrict__ logits, int64_t V, int64_t R, float c, int32_t* __restrict__ amax,
+__global__ void __launch_bounds__(kStatThreads)
+    row_stats_kernel(const void* __restrict__ logits, int64_t V, float c, int32_t* __restrict__ amax,
                      float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ float wm[kConsumerWarps], ws[kConsumerWarps], wv[kConsumerWarps];
-  __shared__ int wi[kConsumerWarps];
-  __shared__ float s_m, s_s, s_bv;
-  RowPipe<esz, kPipeChunk, kPipeStages, kConsumerWarps> pipe;
-  pipe.init(reinterpret_cast<StatPipeSmem*>(dsm), logits, V, R);
+  constexpr int kWarps = kStatThreads / 32;
+  __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
+  __shared__ int wi[kWarps];
+  __shared__ float s_m, s_s;
+  const int64_t r = blockIdx.x;
+  const void* row = static_cast<const char*>(logits) + r * V * esz;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == kConsumerWarps) {
-    if (lane == 0) pipe.produce(stats);
-    return;
+  RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX};
+  for_row_raw<DT, 4>(row, V, v, threadIdx.x, kStatThreads);
+  float bv = v.m;
+  int bi = v.bi;
+  warp_best(bv, bi);
+  float m = v.m, s = v.s0 + v.s1;
+  if (STOCH) warp_merge_ms(m, s, c);
+  if (lane == 0) {
+    wv[warp] = bv;
+    wi[warp] = bi;
+    wm[warp] = m;
+    ws[warp] = s;
   }
-  bool aborted = false;
-  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-    RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX};
-    pipe_row<DT, kPipeChunk, kPipeStages, kConsumerWarps>(pipe, r, v, stats, aborted);
-    float bv = v.m;
-    int bi = v.bi;
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < kWarps ? wv[lane] : neg_inf();
+    bi = lane < kWarps ? wi[lane] : INT_MAX;
     warp_best(bv, bi);
-    float m = v.m, s = v.s0 + v.s1;
-    if (STOCH) warp_merge_ms(m, s, c);
-    if (lane == 0) {
-      wv[warp] = bv;
-      wi[warp] = bi;
-      wm[warp] = m;
-      ws[warp] = s;
-    }
-    consumer_sync(kConsumers);
-    if (warp == 0) {
-      bv = lane < kConsumerWarps ? wv[lane] : neg_inf();
-      bi = lane < kConsumerWarps ? wi[lane] : INT_MAX;
-      warp_best(bv, bi);
-      if (STOCH) {
-        m = lane < kConsumerWarps ? wm[lane] : neg_inf();
-        s = lane < kConsumerWarps ? ws[lane] : 0.0f;
-        warp_merge_ms(m, s, c);
-      }
-      if (lane == 0) {
-        amax[r] = bi == INT_MAX ? 0 : bi;
-        s_m = m;
-        s_s = s;
-        s_bv = bv;
-        if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
-      }
-    }
-    consumer_sync(kConsumers);
     if (STOCH) {
-      m = s_m;
-      s = s_s;
-      if (isfinite(m) && !isfinite(s)) {
-        // the row holds a NaN: recompute the normaliser with NaN as -inf
-        const void* row = static_cast<const char*>(logits) + r * V * esz;
-        KeyedSum ks{c, m * c, 0.0f};
-        for_row<DT, 2>(row, V, ks, threadIdx.x, kConsumers);
-        float t = warp_sum(ks.s);
-        if (lane == 0) ws[warp] = t;
-        consumer_sync(kConsumers);
-        if (threadIdx.x == 0) {
-          float tot = 0.0f;
-          for (int w = 0; w < kConsumerWarps; ++w) tot += ws[w];
-          s_s = tot;
-        }
-        consumer_sync(kConsumers);
-        s = s_s;
-      }
-      if (threadIdx.x == 0) {
-        m_out[r] = m;
-        z_out[r] = s;
-      }
-      consumer_sync(kConsumers);
+      m = lane < kWarps ? wm[lane] : neg_inf();
+      s = lane < kWarps ? ws[lane] : 0.0f;
+      warp_merge_ms(m, s, c);
+    }
+    if (lane == 0) {
+      amax[r] = bi == INT_MAX ? 0 : bi;
+      s_m = m;
+      s_s = s;
+      if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
     }
   }
-  pipe.finish();
+  if (!STOCH) return;
+  __syncthreads();
+  m = s_m;
+  s = s_s;
+  if (isfinite(m) && !isfinite(s)) {
+    // the row holds a NaN: recompute the normaliser with NaN as -inf
+    KeyedSum ks{c, m * c, 0.0f};
+    for_row<DT, 2>(row, V, ks);
+    const float part = warp_sum(ks.s);
+    __syncthreads();
+    if (lane == 0) ws[warp] = part;
+    __syncthreads();
+    s = 0.0f;
+    for (int w = 0; w < kWarps; ++w) s += ws[w];
+  }
+  if (threadIdx.x == 0) {
+    m_out[r] = m;
+    z_out[r] = s;
+  }
 }
 
 template <int DT, bool STOCH>
 int launch_row_stats(const void* logits, int64_t V, int64_t R, float c, int32_t* amax, float* m, float* z,
                      int32_t* stats, cudaStream_t s) {
-  constexpr size_t smem = sizeof(StatPipeSmem);
-  int err;
-  const int grid = persistent_grid(row_stats_kernel<DT, STOCH>, kPipeThreads, smem, R, &err);
-  if (err != SPEC_OK) return err;
-  row_stats_kernel<DT, STOCH><<<grid, kPipeThreads, smem, s>>>(logits, V, R, c, amax, m, z, stats);
+  row_stats_kernel<DT, STOCH><<<static_cast<unsigned>(R), kStatThreads, 0, s>>>(logits, V, c, amax, m, z, stats);
   return launch_status();
 }
 
