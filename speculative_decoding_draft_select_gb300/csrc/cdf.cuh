@@ -23,9 +23,9 @@ namespace specdec {
 
 // W provides:  void load8(int64_t v0, float* x) const   (0 beyond V)
 //              float at(int64_t v) const
-template <int THREADS, class W>
+template <int THREADS, class W, int kUnroll = 4>
 __device__ float cdf_tile_pass(const W& w, int64_t V, float* red, float* tile_sum) {
-  constexpr int kTile = THREADS * 8, kWarps = THREADS / 32, kUnroll = 4;
+  constexpr int kTile = THREADS * 8, kWarps = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ntiles = (V + kTile - 1) / kTile;
   // kUnroll tiles per iteration: all their loads are issued before the sums

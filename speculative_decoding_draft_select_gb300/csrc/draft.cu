@@ -107,7 +107,9 @@ __device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, float& thr, int
     w.li[lane] = ni;
   }
   if (lane == 0) w.cnt = 0;
-  thr = __shfl_sync(0xffffffffu, nv, K - 1);
+  // the list's K-th value only counts once K real entries exist; a seeded
+  // threshold is never lowered
+  thr = fmaxf(thr, __shfl_sync(0xffffffffu, nv, K - 1));
   __syncwarp();
 }
 
@@ -115,13 +117,15 @@ template <int DT, int K>
 struct DraftVisitor {
   float c, m, s0, s1;  // online softmax (two accumulators)
   WarpSel<K>* w;
-  float thr;           // warp-uniform K-th best value so far
+  float thr;           // warp-uniform lower bound of the row's K-th best key
   int lane;
+  bool seeded;
 
   __device__ __forceinline__ void reset() {
     m = neg_inf();
     s0 = s1 = 0.0f;
     thr = neg_inf();
+    seeded = false;
     if (lane < K) {
       w->lv[lane] = neg_inf();
       w->li[lane] = INT_MAX;
@@ -178,6 +182,22 @@ struct DraftVisitor {
         s0 += fast_exp2(fmaf(x[j], c, -mc));
         s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
       }
+    }
+    if (!seeded) {
+      // Seed the threshold with the K-th largest of the 32 lanes' maxima of
+      // this first vector: K distinct elements reach it, so no element below
+      // it can be in the row's top-K.  Saves the flood of candidates a -inf
+      // threshold would let in.
+      float mine = ok ? vmax : neg_inf();
+      float kth = neg_inf();
+#pragma unroll 1
+      for (int r = 0; r < K; ++r) {
+        kth = warp_max(mine);
+        const unsigned hit = __ballot_sync(0xffffffffu, mine == kth);
+        if (lane == __ffs(hit) - 1) mine = neg_inf();
+      }
+      thr = kth == kth ? kth : neg_inf();
+      seeded = true;
     }
     if (ok && vmax >= thr) {
 #pragma unroll
@@ -300,7 +320,7 @@ __global__ void __launch_bounds__(kDraftThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), lane};
+  DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), lane, false};
   st.reset();
   for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
   st.finish();
