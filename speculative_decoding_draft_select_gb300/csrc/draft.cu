@@ -22,7 +22,6 @@ namespace {
 
 constexpr int kDraftThreads = 512;
 constexpr int kCandCap = 320;  // candidate slots per warp
-constexpr int kFlushAt = 64;   // merge once more candidates than this wait
 
 // Running online-softmax partials of one thread: m = max key seen,
 // s = sum 2^((x - m) c).
@@ -50,26 +49,24 @@ struct SoftmaxPartial {
 // candidate buffer in shared memory.  An element is a candidate only if its
 // key is >= the warp's current K-th best value (a key below it can never
 // enter the top-K), so after the first few vectors candidates are rare and
-// the common element costs one compare.  Candidates are appended with a
-// shared-memory atomic; the buffer order does not matter because the merge
-// selects by (value desc, index asc).  Once more than kFlushAt candidates
-// wait, the warp merges buffer and list back into a sorted top-K (K rounds
-// of a warp-wide argmax) and raises its threshold.
+// the common element costs one compare and one warp vote.  Candidates are
+// appended at warp-scanned positions; once the buffer may not hold another
+// full vector of them, the warp merges buffer and list back into a sorted
+// top-K (K rounds of a warp-wide argmax) and raises its threshold.
 template <int K>
 struct WarpSel {
   float bv[kCandCap];
   int bi[kCandCap];
   float lv[K];
   int li[K];
-  int cnt;
 };
 
-// Merge the list and the cnt buffered candidates into the sorted list.
+// Merge the list and the n buffered candidates into the sorted list.
 // Warp-synchronous; all lanes call it.
 template <int K>
-__device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, float& thr, int lane) {
+__device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, int cnt, float& thr, int lane) {
   __syncwarp();
-  const int n = w.cnt + K;
+  const int n = cnt + K;
   float nv = neg_inf();
   int ni = INT_MAX;
   for (int r = 0; r < K; ++r) {
@@ -106,7 +103,6 @@ __device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, float& thr, int
     w.lv[lane] = nv;
     w.li[lane] = ni;
   }
-  if (lane == 0) w.cnt = 0;
   // the list's K-th value only counts once K real entries exist; a seeded
   // threshold is never lowered
   thr = fmaxf(thr, __shfl_sync(0xffffffffu, nv, K - 1));
@@ -118,6 +114,7 @@ struct DraftVisitor {
   float c, m, s0, s1;  // online softmax (two accumulators)
   WarpSel<K>* w;
   float thr;           // warp-uniform lower bound of the row's K-th best key
+  int cnt;             // warp-uniform number of buffered candidates
   int lane;
   bool seeded;
 
@@ -125,12 +122,12 @@ struct DraftVisitor {
     m = neg_inf();
     s0 = s1 = 0.0f;
     thr = neg_inf();
+    cnt = 0;
     seeded = false;
     if (lane < K) {
       w->lv[lane] = neg_inf();
       w->li[lane] = INT_MAX;
     }
-    if (lane == 0) w->cnt = 0;
     __syncwarp();
   }
   __device__ __forceinline__ void rescale(float nm) {
@@ -143,9 +140,33 @@ struct DraftVisitor {
     }
     m = nm;
   }
-  __device__ __forceinline__ void flush_check() {
-    __syncwarp();
-    if (w->cnt > kFlushAt) warp_select_merge<K>(*w, thr, lane);
+  // Append this lane's n candidates (keys x[j] >= thr) at warp-scanned
+  // positions; merge when the buffer may not hold another full vector.
+  template <int N>
+  __device__ __forceinline__ void append(const float* x, int64_t first, bool ok) {
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) n += (ok && x[j] >= thr);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int pos = cnt + incl - n;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      if (ok && x[j] >= thr) {
+        w->bv[pos] = x[j];
+        w->bi[pos] = static_cast<int>(first) + j;
+        ++pos;
+      }
+    }
+    cnt += __shfl_sync(0xffffffffu, incl, 31);
+    if (cnt > kCandCap - 32 * 8) {
+      warp_select_merge<K>(*w, cnt, thr, lane);
+      cnt = 0;
+    }
   }
   // Scalar ends of a row (NaN as -inf).
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
@@ -153,13 +174,8 @@ struct DraftVisitor {
     if (ok) {
       if (xk > m) rescale(xk);
       if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
-      if (xk >= thr) {
-        const int pos = atomicAdd(&w->cnt, 1);
-        w->bv[pos] = xk;
-        w->bi[pos] = static_cast<int>(idx);
-      }
     }
-    flush_check();
+    if (__any_sync(0xffffffffu, ok && xk >= thr)) append<1>(&xk, idx, ok);
   }
   // A 16-byte vector.  NaN elements are skipped by the max and never become
   // candidates (NaN >= thr is false); they turn the sum into NaN, which the
@@ -199,22 +215,12 @@ struct DraftVisitor {
       thr = kth == kth ? kth : neg_inf();
       seeded = true;
     }
-    if (ok && vmax >= thr) {
-#pragma unroll
-      for (int j = 0; j < kv; ++j) {
-        if (x[j] >= thr) {
-          const int pos = atomicAdd(&w->cnt, 1);
-          w->bv[pos] = x[j];
-          w->bi[pos] = static_cast<int>(first) + j;
-        }
-      }
-    }
-    flush_check();
+    if (__any_sync(0xffffffffu, ok && vmax >= thr)) append<kv>(x, first, ok);
   }
 
   __device__ __forceinline__ void finish() {
-    __syncwarp();
-    if (w->cnt > 0) warp_select_merge<K>(*w, thr, lane);
+    if (cnt > 0) warp_select_merge<K>(*w, cnt, thr, lane);
+    cnt = 0;
   }
 };
 
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kDraftThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), lane, false};
+  DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), 0, lane, false};
   st.reset();
   for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
   st.finish();

@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kWalkThreads)
       }
       // rejected: mass of the next residual
       ResidualWeights<DT, decltype(qrow)> w{lrow, qrow, V, cT, mc, invz, s_A + s_cj};
-      const float total = cdf_tile_pass<kWalkThreads, decltype(w), 8>(w, V, red, tile_sum);
+      const float total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
       if (tid == 0) {
         if (total > 0.0f && isfinite(total)) {
           s_A = s_A + s_cj;
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kWalkThreads)
     if (s_tiles_ok) {
       total = s_total;
     } else {
-      total = cdf_tile_pass<kWalkThreads, decltype(w), 8>(w, V, red, tile_sum);
+      total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
     }
     const int32_t tok = cdf_search<kWalkThreads>(w, V, __ldg(u_final + b), tile_sum, total, scan_sh, stats);
     if (tid == 0) {
