@@ -21,7 +21,6 @@ namespace specdec {
 namespace {
 
 constexpr int kDraftThreads = 512;
-constexpr int kCandCap = 320;  // candidate slots per warp
 
 // Running online-softmax partials of one thread: m = max key seen,
 // s = sum 2^((x - m) c).
@@ -45,76 +44,30 @@ struct SoftmaxPartial {
   }
 };
 
-// Warp-select top-K: each warp keeps its current top-K (sorted) and a
-// candidate buffer in shared memory.  An element is a candidate only if its
-// key is >= the warp's current K-th best value (a key below it can never
-// enter the top-K), so after the first few vectors candidates are rare and
-// the common element costs one compare and one warp vote.  Candidates are
-// appended at warp-scanned positions; once the buffer may not hold another
-// full vector of them, the warp merges buffer and list back into a sorted
-// top-K (K rounds of a warp-wide argmax) and raises its threshold.
+// Warp-select top-K: each warp keeps its current top-K (sorted) and every
+// lane a few private candidate slots in shared memory.  An element is a
+// candidate only if its key is >= the warp's threshold, a lower bound of the
+// row's K-th best key (a key below it can never enter the top-K), so after
+// the first vectors candidates are rare and the common element costs one
+// compare.  When some lane's slots could overflow on the next vector, the
+// warp merges list and slots back into a sorted top-K (K rounds of a
+// warp-wide (value desc, index asc) argmax) and raises its threshold.
+constexpr int kSlots = 16;  // candidate slots per lane
+
 template <int K>
 struct WarpSel {
-  float bv[kCandCap];
-  int bi[kCandCap];
+  float bv[kSlots][32];
+  int bi[kSlots][32];
   float lv[K];
   int li[K];
 };
-
-// Merge the list and the n buffered candidates into the sorted list.
-// Warp-synchronous; all lanes call it.
-template <int K>
-__device__ __forceinline__ void warp_select_merge(WarpSel<K>& w, int cnt, float& thr, int lane) {
-  __syncwarp();
-  const int n = cnt + K;
-  float nv = neg_inf();
-  int ni = INT_MAX;
-  for (int r = 0; r < K; ++r) {
-    float bv = neg_inf();
-    int bi = INT_MAX, bpos = -1;
-    for (int e = lane; e < n; e += 32) {
-      const float v = e < K ? w.lv[e] : w.bv[e - K];
-      const int i = e < K ? w.li[e] : w.bi[e - K];
-      if (before(v, i, bv, bi)) {
-        bv = v;
-        bi = i;
-        bpos = e;
-      }
-    }
-    float wv = bv;
-    int wi = bi;
-    warp_best(wv, wi);
-    if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
-      if (bpos < K) {
-        w.lv[bpos] = neg_inf();
-        w.li[bpos] = INT_MAX;
-      } else {
-        w.bv[bpos - K] = neg_inf();
-        w.bi[bpos - K] = INT_MAX;
-      }
-    }
-    __syncwarp();
-    if (lane == r) {
-      nv = wv;
-      ni = wi;
-    }
-  }
-  if (lane < K) {
-    w.lv[lane] = nv;
-    w.li[lane] = ni;
-  }
-  // the list's K-th value only counts once K real entries exist; a seeded
-  // threshold is never lowered
-  thr = fmaxf(thr, __shfl_sync(0xffffffffu, nv, K - 1));
-  __syncwarp();
-}
 
 template <int DT, int K>
 struct DraftVisitor {
   float c, m, s0, s1;  // online softmax (two accumulators)
   WarpSel<K>* w;
   float thr;           // warp-uniform lower bound of the row's K-th best key
-  int cnt;             // warp-uniform number of buffered candidates
+  int n;               // this lane's used candidate slots
   int lane;
   bool seeded;
 
@@ -122,7 +75,7 @@ struct DraftVisitor {
     m = neg_inf();
     s0 = s1 = 0.0f;
     thr = neg_inf();
-    cnt = 0;
+    n = 0;
     seeded = false;
     if (lane < K) {
       w->lv[lane] = neg_inf();
@@ -140,33 +93,62 @@ struct DraftVisitor {
     }
     m = nm;
   }
-  // Append this lane's n candidates (keys x[j] >= thr) at warp-scanned
-  // positions; merge when the buffer may not hold another full vector.
-  template <int N>
-  __device__ __forceinline__ void append(const float* x, int64_t first, bool ok) {
-    int n = 0;
-#pragma unroll
-    for (int j = 0; j < N; ++j) n += (ok && x[j] >= thr);
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int pos = cnt + incl - n;
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      if (ok && x[j] >= thr) {
-        w->bv[pos] = x[j];
-        w->bi[pos] = static_cast<int>(first) + j;
-        ++pos;
+  __device__ __forceinline__ void push(float x, int idx) {
+    w->bv[n][lane] = x;
+    w->bi[n][lane] = idx;
+    ++n;
+  }
+  // Merge the list and every lane's slots into the sorted list.
+  // Warp-synchronous; all lanes call it.
+  __device__ __forceinline__ void merge() {
+    __syncwarp();
+    float nv = neg_inf();
+    int ni = INT_MAX;
+    for (int r = 0; r < K; ++r) {
+      float bv = neg_inf();
+      int bi = INT_MAX, bpos = -2;
+      if (lane < K && before(w->lv[lane], w->li[lane], bv, bi)) {
+        bv = w->lv[lane];
+        bi = w->li[lane];
+        bpos = -1;
+      }
+      for (int e = 0; e < n; ++e) {
+        const float v = w->bv[e][lane];
+        const int i = w->bi[e][lane];
+        if (before(v, i, bv, bi)) {
+          bv = v;
+          bi = i;
+          bpos = e;
+        }
+      }
+      float wv = bv;
+      int wi = bi;
+      warp_best(wv, wi);
+      if (bpos != -2 && wi != INT_MAX && bv == wv && bi == wi) {
+        if (bpos == -1) {
+          w->lv[lane] = neg_inf();
+          w->li[lane] = INT_MAX;
+        } else {
+          w->bv[bpos][lane] = neg_inf();
+          w->bi[bpos][lane] = INT_MAX;
+        }
+      }
+      __syncwarp();
+      if (lane == r) {
+        nv = wv;
+        ni = wi;
       }
     }
-    cnt += __shfl_sync(0xffffffffu, incl, 31);
-    if (cnt > kCandCap - 32 * 8) {
-      warp_select_merge<K>(*w, cnt, thr, lane);
-      cnt = 0;
+    __syncwarp();
+    if (lane < K) {
+      w->lv[lane] = nv;
+      w->li[lane] = ni;
     }
+    n = 0;
+    // the list's K-th value only counts once K real entries exist; a seeded
+    // threshold is never lowered
+    thr = fmaxf(thr, __shfl_sync(0xffffffffu, nv, K - 1));
+    __syncwarp();
   }
   // Scalar ends of a row (NaN as -inf).
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
@@ -174,8 +156,9 @@ struct DraftVisitor {
     if (ok) {
       if (xk > m) rescale(xk);
       if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
+      if (xk >= thr) push(xk, static_cast<int>(idx));
     }
-    if (__any_sync(0xffffffffu, ok && xk >= thr)) append<1>(&xk, idx, ok);
+    if (__any_sync(0xffffffffu, n > kSlots - 8)) merge();
   }
   // A 16-byte vector.  NaN elements are skipped by the max and never become
   // candidates (NaN >= thr is false); they turn the sum into NaN, which the
@@ -215,12 +198,16 @@ struct DraftVisitor {
       thr = kth == kth ? kth : neg_inf();
       seeded = true;
     }
-    if (__any_sync(0xffffffffu, ok && vmax >= thr)) append<kv>(x, first, ok);
+    if (ok && vmax >= thr) {
+#pragma unroll
+      for (int j = 0; j < kv; ++j)
+        if (x[j] >= thr) push(x[j], static_cast<int>(first) + j);
+    }
+    if (__any_sync(0xffffffffu, n > kSlots - kv)) merge();
   }
 
   __device__ __forceinline__ void finish() {
-    if (cnt > 0) warp_select_merge<K>(*w, cnt, thr, lane);
-    cnt = 0;
+    if (__any_sync(0xffffffffu, n > 0)) merge();
   }
 };
 
