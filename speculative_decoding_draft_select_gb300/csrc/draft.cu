@@ -20,7 +20,10 @@
 namespace specdec {
 namespace {
 
-constexpr int kDraftThreads = 512;
+#ifndef SPEC_DRAFT_THREADS
+#define SPEC_DRAFT_THREADS 256
+#endif
+constexpr int kDraftThreads = SPEC_DRAFT_THREADS;
 
 // Running online-softmax partials of one thread: m = max key seen,
 // s = sum 2^((x - m) c).
@@ -44,30 +47,70 @@ struct SoftmaxPartial {
   }
 };
 
-// Warp-select top-K: each warp keeps its current top-K (sorted) and every
-// lane a few private candidate slots in shared memory.  An element is a
-// candidate only if its key is >= the warp's threshold, a lower bound of the
-// row's K-th best key (a key below it can never enter the top-K), so after
-// the first vectors candidates are rare and the common element costs one
-// compare.  When some lane's slots could overflow on the next vector, the
-// warp merges list and slots back into a sorted top-K (K rounds of a
-// warp-wide (value desc, index asc) argmax) and raises its threshold.
-constexpr int kSlots = 16;  // candidate slots per lane
-
+// Register top-K of one thread, sorted by (value desc, index asc).
 template <int K>
-struct WarpSel {
-  float bv[kSlots][32];
-  int bi[kSlots][32];
-  float lv[K];
-  int li[K];
+struct TopK {
+  float v[K];
+  int i[K];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      v[j] = neg_inf();
+      i[j] = INT_MAX;
+    }
+  }
+  __device__ __forceinline__ void push(float x, int idx) {
+    if (!before(x, idx, v[K - 1], i[K - 1])) return;
+    v[K - 1] = x;
+    i[K - 1] = idx;
+#pragma unroll
+    for (int j = K - 1; j > 0; --j) {
+      if (before(v[j], i[j], v[j - 1], i[j - 1])) {
+        const float tv = v[j];
+        v[j] = v[j - 1];
+        v[j - 1] = tv;
+        const int ti = i[j];
+        i[j] = i[j - 1];
+        i[j - 1] = ti;
+      }
+    }
+  }
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) {
+      v[j] = v[j + 1];
+      i[j] = i[j + 1];
+    }
+    v[K - 1] = neg_inf();
+    i[K - 1] = INT_MAX;
+  }
+};
+
+// Warp-select top-K.  Each warp keeps a threshold, a lower bound of the
+// row's K-th best key: a key below it can never enter the top-K.  In the
+// streaming loop a lane whose 16-byte vector reaches the threshold stores
+// the whole raw vector in one of its private shared-memory slots (one
+// store, so the rare divergent branch stays cheap).  At a merge (some lane's
+// slots are full, or the row ends) every lane expands its slot vectors into
+// a register top-K, the warp combines the 32 lists (K rounds of a warp-wide
+// (value desc, index asc) argmax), and the threshold rises to the warp's
+// K-th value.  The threshold starts at the K-th largest of the 32 lanes'
+// maxima of their first vector (K distinct elements reach it).
+constexpr int kSlots = 8;  // candidate vectors per lane
+
+struct WarpSlots {
+  uint4 raw[kSlots][32];
+  int first[kSlots][32];
 };
 
 template <int DT, int K>
 struct DraftVisitor {
   float c, m, s0, s1;  // online softmax (two accumulators)
-  WarpSel<K>* w;
+  WarpSlots* w;
   float thr;           // warp-uniform lower bound of the row's K-th best key
-  int n;               // this lane's used candidate slots
+  float hv;            // lane j < K holds the warp's j-th best so far
+  int hi;
+  int n;               // this lane's used slots
   int lane;
   bool seeded;
 
@@ -75,13 +118,10 @@ struct DraftVisitor {
     m = neg_inf();
     s0 = s1 = 0.0f;
     thr = neg_inf();
+    hv = neg_inf();
+    hi = INT_MAX;
     n = 0;
     seeded = false;
-    if (lane < K) {
-      w->lv[lane] = neg_inf();
-      w->li[lane] = INT_MAX;
-    }
-    __syncwarp();
   }
   __device__ __forceinline__ void rescale(float nm) {
     if (m == neg_inf()) {
@@ -93,72 +133,61 @@ struct DraftVisitor {
     }
     m = nm;
   }
-  __device__ __forceinline__ void push(float x, int idx) {
-    w->bv[n][lane] = x;
-    w->bi[n][lane] = idx;
-    ++n;
-  }
-  // Merge the list and every lane's slots into the sorted list.
   // Warp-synchronous; all lanes call it.
   __device__ __forceinline__ void merge() {
-    __syncwarp();
-    float nv = neg_inf();
-    int ni = INT_MAX;
-    for (int r = 0; r < K; ++r) {
-      float bv = neg_inf();
-      int bi = INT_MAX, bpos = -2;
-      if (lane < K && before(w->lv[lane], w->li[lane], bv, bi)) {
-        bv = w->lv[lane];
-        bi = w->li[lane];
-        bpos = -1;
+    constexpr int kv = Logit<DT>::kVec;
+    TopK<K> t;
+    t.init();
+    if (lane < K) t.push(hv, hi);
+    for (int e = 0; e < n; ++e) {
+      float x[kv];
+      unpack<DT>(w->raw[e][lane], x);
+      const int f = w->first[e][lane];
+      if (f < 0) {  // a single element (row end), in position 0
+        if (x[0] >= thr) t.push(x[0], -f - 1);
+        continue;
       }
-      for (int e = 0; e < n; ++e) {
-        const float v = w->bv[e][lane];
-        const int i = w->bi[e][lane];
-        if (before(v, i, bv, bi)) {
-          bv = v;
-          bi = i;
-          bpos = e;
-        }
-      }
-      float wv = bv;
-      int wi = bi;
-      warp_best(wv, wi);
-      if (bpos != -2 && wi != INT_MAX && bv == wv && bi == wi) {
-        if (bpos == -1) {
-          w->lv[lane] = neg_inf();
-          w->li[lane] = INT_MAX;
-        } else {
-          w->bv[bpos][lane] = neg_inf();
-          w->bi[bpos][lane] = INT_MAX;
-        }
-      }
-      __syncwarp();
-      if (lane == r) {
-        nv = wv;
-        ni = wi;
-      }
-    }
-    __syncwarp();
-    if (lane < K) {
-      w->lv[lane] = nv;
-      w->li[lane] = ni;
+#pragma unroll
+      for (int j = 0; j < kv; ++j)
+        if (x[j] >= thr) t.push(x[j], f + j);
     }
     n = 0;
-    // the list's K-th value only counts once K real entries exist; a seeded
-    // threshold is never lowered
-    thr = fmaxf(thr, __shfl_sync(0xffffffffu, nv, K - 1));
+#pragma unroll 1
+    for (int r = 0; r < K; ++r) {
+      float bv = t.v[0];
+      int bi = t.i[0];
+      warp_best(bv, bi);
+      if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
+      if (lane == r) {
+        hv = bv;
+        hi = bi;
+      }
+    }
+    // the K-th value only counts once K real entries exist; the threshold
+    // never falls
+    thr = fmaxf(thr, __shfl_sync(0xffffffffu, hv, K - 1));
     __syncwarp();
   }
-  // Scalar ends of a row (NaN as -inf).
+  // Scalar ends of a row (NaN as -inf): a slot holding one element in
+  // position 0, marked by the negative index -(idx + 1).
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
     const float xk = order_key(x);
     if (ok) {
       if (xk > m) rescale(xk);
       if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
-      if (xk >= thr) push(xk, static_cast<int>(idx));
     }
-    if (__any_sync(0xffffffffu, n > kSlots - 8)) merge();
+    if (__any_sync(0xffffffffu, n == kSlots)) merge();
+    if (ok && xk >= thr) {
+      uint4 raw = neg_inf_vec<DT>();
+      if (DT == SPEC_BF16) {
+        raw.x = (__float_as_uint(xk) >> 16) | 0xff800000u;
+      } else {
+        raw.x = __float_as_uint(xk);
+      }
+      w->raw[n][lane] = raw;
+      w->first[n][lane] = -static_cast<int>(idx) - 1;
+      ++n;
+    }
   }
   // A 16-byte vector.  NaN elements are skipped by the max and never become
   // candidates (NaN >= thr is false); they turn the sum into NaN, which the
@@ -183,10 +212,6 @@ struct DraftVisitor {
       }
     }
     if (!seeded) {
-      // Seed the threshold with the K-th largest of the 32 lanes' maxima of
-      // this first vector: K distinct elements reach it, so no element below
-      // it can be in the row's top-K.  Saves the flood of candidates a -inf
-      // threshold would let in.
       float mine = ok ? vmax : neg_inf();
       float kth = neg_inf();
 #pragma unroll 1
@@ -199,16 +224,75 @@ struct DraftVisitor {
       seeded = true;
     }
     if (ok && vmax >= thr) {
-#pragma unroll
-      for (int j = 0; j < kv; ++j)
-        if (x[j] >= thr) push(x[j], static_cast<int>(first) + j);
+      w->raw[n][lane] = raw;
+      w->first[n][lane] = static_cast<int>(first);
+      ++n;
     }
-    if (__any_sync(0xffffffffu, n > kSlots - kv)) merge();
+    if (__any_sync(0xffffffffu, n == kSlots)) merge();
   }
 
   __device__ __forceinline__ void finish() {
     if (__any_sync(0xffffffffu, n > 0)) merge();
   }
+};
+
+// K == 1: the top-1 is the argmax; no candidates needed.
+template <int DT>
+struct ArgmaxVisitor {
+  float c, m, s0, s1;
+  int bi;
+  __device__ __forceinline__ void reset() {
+    m = neg_inf();
+    s0 = s1 = 0.0f;
+    bi = INT_MAX;
+  }
+  __device__ __forceinline__ void rescale(float nm) {
+    if (m == neg_inf()) {
+      s0 = s1 = 0.0f;
+    } else {
+      const float f = fast_exp2((m - nm) * c);
+      s0 *= f;
+      s1 *= f;
+    }
+    m = nm;
+  }
+  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
+    if (!ok) return;
+    const float xk = order_key(x);
+    if (before(xk, static_cast<int>(idx), m, bi)) {
+      if (xk > m) rescale(xk);
+      bi = static_cast<int>(idx);
+    }
+    if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
+  }
+  __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool ok) {
+    constexpr int kv = Logit<DT>::kVec;
+    float x[kv];
+    unpack<DT>(raw, x);
+    float vmax;
+    if (DT == SPEC_BF16) {
+      vmax = max8_bf16(raw);
+    } else {
+      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
+    }
+    if (ok && before(vmax, static_cast<int>(first), m, bi)) {
+      int j0 = 0;
+#pragma unroll
+      for (int j = kv - 1; j >= 0; --j)
+        if (x[j] == vmax) j0 = j;
+      if (vmax > m) rescale(vmax);
+      bi = static_cast<int>(first) + j0;
+    }
+    if (m != neg_inf()) {
+      const float mc = m * c;
+#pragma unroll
+      for (int j = 0; j < kv; j += 2) {
+        s0 += fast_exp2(fmaf(x[j], c, -mc));
+        s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
+      }
+    }
+  }
+  __device__ __forceinline__ void finish() {}
 };
 
 // Sum of 2^((key(x) - m) c) over a row with NaN as -inf.
@@ -290,7 +374,7 @@ struct ZeroWriter {
 
 template <int K>
 constexpr size_t draft_smem_bytes() {
-  return sizeof(WarpSel<K>) * (kDraftThreads / 32);
+  return K == 1 ? 16 : sizeof(WarpSlots) * (kDraftThreads / 32);
 }
 
 // One CTA per row: 16-byte loads (4 in flight per thread), the online
@@ -305,7 +389,8 @@ __global__ void __launch_bounds__(kDraftThreads)
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kDraftThreads / 32;
   extern __shared__ __align__(16) unsigned char dsm[];
-  WarpSel<K>* sel = reinterpret_cast<WarpSel<K>*>(dsm);
+  __shared__ float lv[kWarps * K];
+  __shared__ int li[kWarps * K];
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
@@ -313,11 +398,34 @@ __global__ void __launch_bounds__(kDraftThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  DraftVisitor<DT, K> st{c, neg_inf(), 0.0f, 0.0f, &sel[warp], neg_inf(), 0, lane, false};
-  st.reset();
-  for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
-  st.finish();
-  float m = st.m, s = st.s0 + st.s1;
+  float m, s;
+  if constexpr (K == 1) {
+    ArgmaxVisitor<DT> st{c};
+    st.reset();
+    for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
+    float bv = st.m;
+    int bi = st.bi;
+    warp_best(bv, bi);
+    if (lane == 0) {
+      lv[warp] = bv;
+      li[warp] = bi;
+    }
+    m = st.m;
+    s = st.s0 + st.s1;
+  } else {
+    DraftVisitor<DT, K> st{c};
+    st.w = reinterpret_cast<WarpSlots*>(dsm) + warp;
+    st.lane = lane;
+    st.reset();
+    for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
+    st.finish();
+    if (lane < K) {
+      lv[warp * K + lane] = st.hv;
+      li[warp * K + lane] = st.hi;
+    }
+    m = st.m;
+    s = st.s0 + st.s1;
+  }
   block_ms<0>(m, s, c, sm, ss);  // its barriers also publish every warp's list
   if (isfinite(m) && !isfinite(s)) {
     // the row holds a NaN: recompute the normaliser with NaN as -inf
@@ -333,31 +441,20 @@ __global__ void __launch_bounds__(kDraftThreads)
   }
   if (warp == 0) {
     // merge the warps' sorted lists: K rounds over kWarps * K entries
+    TopK<K> t;
+    t.init();
+    for (int e = lane; e < kWarps * K; e += 32) t.push(lv[e], li[e]);
     for (int rr = 0; rr < K; ++rr) {
-      float bv = neg_inf();
-      int bi = INT_MAX, bpos = -1;
-      for (int e = lane; e < kWarps * K; e += 32) {
-        const float v = sel[e / K].lv[e % K];
-        const int i = sel[e / K].li[e % K];
-        if (before(v, i, bv, bi)) {
-          bv = v;
-          bi = i;
-          bpos = e;
-        }
-      }
-      float wv = bv;
-      int wi = bi;
-      warp_best(wv, wi);
-      if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
-        sel[bpos / K].lv[bpos % K] = neg_inf();
-        sel[bpos / K].li[bpos % K] = INT_MAX;
-      }
-      __syncwarp();
+      float bv = t.v[0];
+      int bi = t.i[0];
+      warp_best(bv, bi);
+      if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
       if (lane == 0) {
-        fv[rr] = wv;
-        fi[rr] = wi;
+        fv[rr] = bv;
+        fi[rr] = bi;
       }
     }
+    __syncwarp();
     if (fi[k - 1] == INT_MAX && k <= V) {
       // fewer than k non-NaN logits: rank the row again with NaN as -inf,
       // each pick the best element after the previous one in the order

@@ -109,7 +109,10 @@ struct KeyedSum {
   }
 };
 
-constexpr int kStatThreads = 512;
+#ifndef SPEC_STAT_THREADS
+#define SPEC_STAT_THREADS 256
+#endif
+constexpr int kStatThreads = SPEC_STAT_THREADS;
 
 // Pass 1: one CTA per target row streams it with 16-byte loads (4 in
 // flight per thread) and reduces it to its argmax and, for sampling, the
