@@ -86,42 +86,33 @@ struct TopK {
   }
 };
 
-// Warp-select top-K.  Each warp keeps a threshold, a lower bound of the
-// row's K-th best key: a key below it can never enter the top-K.  In the
-// streaming loop a lane whose 16-byte vector reaches the threshold stores
-// the whole raw vector in one of its private shared-memory slots (one
-// store, so the rare divergent branch stays cheap).  At a merge (some lane's
-// slots are full, or the row ends) every lane expands its slot vectors into
-// a register top-K, the warp combines the 32 lists (K rounds of a warp-wide
-// (value desc, index asc) argmax), and the threshold rises to the warp's
-// K-th value.  The threshold starts at the K-th largest of the 32 lanes'
-// maxima of their first vector (K distinct elements reach it).
-constexpr int kSlots = 8;  // candidate vectors per lane
-
-struct WarpSlots {
-  uint4 raw[kSlots][32];
-  int first[kSlots][32];
-};
-
+// Top-K with a warp-shared threshold.  Each lane keeps its own register
+// top-K; the warp keeps a threshold, a lower bound of the row's K-th best
+// key (a key below it can never enter the top-K), so an element is looked at
+// only if it reaches the threshold, and once the threshold is tight that is
+// rare.  The threshold is the K-th largest of the 32 lanes' best keys (K
+// distinct elements reach it): taken after the first vector, and again every
+// 8 vectors while some lane has inserted since.  At the row end the warp
+// combines its 32 lists (K rounds of a warp-wide (value desc, index asc)
+// argmax); lane j then holds the warp's j-th best.
 template <int DT, int K>
 struct DraftVisitor {
   float c, m, s0, s1;  // online softmax (two accumulators)
-  WarpSlots* w;
-  float thr;           // warp-uniform lower bound of the row's K-th best key
-  float hv;            // lane j < K holds the warp's j-th best so far
-  int hi;
-  int n;               // this lane's used slots
+  TopK<K> t;
+  float thr;           // warp-uniform
   int lane;
-  bool seeded;
+  int since;           // vectors since the last threshold refresh
+  bool dirty;          // this lane inserted since the last refresh
+  float hv;            // after finish(): lane j < K holds the warp's j-th best
+  int hi;
 
   __device__ __forceinline__ void reset() {
     m = neg_inf();
     s0 = s1 = 0.0f;
+    t.init();
     thr = neg_inf();
-    hv = neg_inf();
-    hi = INT_MAX;
-    n = 0;
-    seeded = false;
+    since = 8;  // refresh after the first vector
+    dirty = false;
   }
   __device__ __forceinline__ void rescale(float nm) {
     if (m == neg_inf()) {
@@ -133,60 +124,29 @@ struct DraftVisitor {
     }
     m = nm;
   }
-  // Warp-synchronous; all lanes call it.
-  __device__ __forceinline__ void merge() {
-    constexpr int kv = Logit<DT>::kVec;
-    TopK<K> t;
-    t.init();
-    if (lane < K) t.push(hv, hi);
-    for (int e = 0; e < n; ++e) {
-      float x[kv];
-      unpack<DT>(w->raw[e][lane], x);
-      const int f = w->first[e][lane];
-      if (f < 0) {  // a single element (row end), in position 0
-        if (x[0] >= thr) t.push(x[0], -f - 1);
-        continue;
-      }
-#pragma unroll
-      for (int j = 0; j < kv; ++j)
-        if (x[j] >= thr) t.push(x[j], f + j);
-    }
-    n = 0;
+  // K-th largest of the lanes' best keys (warp-synchronous).
+  __device__ __forceinline__ void refresh() {
+    float mine = t.v[0];
+    float kth = neg_inf();
 #pragma unroll 1
     for (int r = 0; r < K; ++r) {
-      float bv = t.v[0];
-      int bi = t.i[0];
-      warp_best(bv, bi);
-      if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
-      if (lane == r) {
-        hv = bv;
-        hi = bi;
-      }
+      kth = warp_max(mine);
+      const unsigned hit = __ballot_sync(0xffffffffu, mine == kth);
+      if (lane == __ffs(hit) - 1) mine = neg_inf();
     }
-    // the K-th value only counts once K real entries exist; the threshold
-    // never falls
-    thr = fmaxf(thr, __shfl_sync(0xffffffffu, hv, K - 1));
-    __syncwarp();
+    if (kth == kth) thr = fmaxf(thr, kth);
+    dirty = false;
+    since = 0;
   }
-  // Scalar ends of a row (NaN as -inf): a slot holding one element in
-  // position 0, marked by the negative index -(idx + 1).
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
     const float xk = order_key(x);
     if (ok) {
       if (xk > m) rescale(xk);
       if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
-    }
-    if (__any_sync(0xffffffffu, n == kSlots)) merge();
-    if (ok && xk >= thr) {
-      uint4 raw = neg_inf_vec<DT>();
-      if (DT == SPEC_BF16) {
-        raw.x = (__float_as_uint(xk) >> 16) | 0xff800000u;
-      } else {
-        raw.x = __float_as_uint(xk);
+      if (xk >= thr) {
+        t.push(xk, static_cast<int>(idx));
+        dirty = true;
       }
-      w->raw[n][lane] = raw;
-      w->first[n][lane] = -static_cast<int>(idx) - 1;
-      ++n;
     }
   }
   // A 16-byte vector.  NaN elements are skipped by the max and never become
@@ -211,28 +171,27 @@ struct DraftVisitor {
         s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
       }
     }
-    if (!seeded) {
-      float mine = ok ? vmax : neg_inf();
-      float kth = neg_inf();
-#pragma unroll 1
-      for (int r = 0; r < K; ++r) {
-        kth = warp_max(mine);
-        const unsigned hit = __ballot_sync(0xffffffffu, mine == kth);
-        if (lane == __ffs(hit) - 1) mine = neg_inf();
-      }
-      thr = kth == kth ? kth : neg_inf();
-      seeded = true;
+    if (ok && vmax >= thr && vmax >= t.v[K - 1]) {
+#pragma unroll
+      for (int j = 0; j < kv; ++j)
+        if (x[j] >= thr) t.push(x[j], static_cast<int>(first) + j);
+      dirty = true;
     }
-    if (ok && vmax >= thr) {
-      w->raw[n][lane] = raw;
-      w->first[n][lane] = static_cast<int>(first);
-      ++n;
-    }
-    if (__any_sync(0xffffffffu, n == kSlots)) merge();
+    if (++since >= 8 && __any_sync(0xffffffffu, dirty)) refresh();
   }
 
   __device__ __forceinline__ void finish() {
-    if (__any_sync(0xffffffffu, n > 0)) merge();
+#pragma unroll 1
+    for (int r = 0; r < K; ++r) {
+      float bv = t.v[0];
+      int bi = t.i[0];
+      warp_best(bv, bi);
+      if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
+      if (lane == r) {
+        hv = bv;
+        hi = bi;
+      }
+    }
   }
 };
 
@@ -374,7 +333,7 @@ struct ZeroWriter {
 
 template <int K>
 constexpr size_t draft_smem_bytes() {
-  return K == 1 ? 16 : sizeof(WarpSlots) * (kDraftThreads / 32);
+  return 16;
 }
 
 // One CTA per row: 16-byte loads (4 in flight per thread), the online
@@ -414,7 +373,6 @@ __global__ void __launch_bounds__(kDraftThreads)
     s = st.s0 + st.s1;
   } else {
     DraftVisitor<DT, K> st{c};
-    st.w = reinterpret_cast<WarpSlots*>(dsm) + warp;
     st.lane = lane;
     st.reset();
     for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
