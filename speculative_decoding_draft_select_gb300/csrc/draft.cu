@@ -86,116 +86,9 @@ struct TopK {
   }
 };
 
-// Top-K with a warp-shared threshold.  Each lane keeps its own register
-// top-K; the warp keeps a threshold, a lower bound of the row's K-th best
-// key (a key below it can never enter the top-K), so an element is looked at
-// only if it reaches the threshold, and once the threshold is tight that is
-// rare.  The threshold is the K-th largest of the 32 lanes' best keys (K
-// distinct elements reach it): taken after the first vector, and again every
-// 8 vectors while some lane has inserted since.  At the row end the warp
-// combines its 32 lists (K rounds of a warp-wide (value desc, index asc)
-// argmax); lane j then holds the warp's j-th best.
-template <int DT, int K>
-struct DraftVisitor {
-  float c, m, s0, s1;  // online softmax (two accumulators)
-  TopK<K> t;
-  float thr;           // warp-uniform
-  int lane;
-  int since;           // vectors since the last threshold refresh
-  bool dirty;          // this lane inserted since the last refresh
-  float hv;            // after finish(): lane j < K holds the warp's j-th best
-  int hi;
-
-  __device__ __forceinline__ void reset() {
-    m = neg_inf();
-    s0 = s1 = 0.0f;
-    t.init();
-    thr = neg_inf();
-    since = 8;  // refresh after the first vector
-    dirty = false;
-  }
-  __device__ __forceinline__ void rescale(float nm) {
-    if (m == neg_inf()) {
-      s0 = s1 = 0.0f;
-    } else {
-      const float f = fast_exp2((m - nm) * c);
-      s0 *= f;
-      s1 *= f;
-    }
-    m = nm;
-  }
-  // K-th largest of the lanes' best keys (warp-synchronous).
-  __device__ __forceinline__ void refresh() {
-    float mine = t.v[0];
-    float kth = neg_inf();
-#pragma unroll 1
-    for (int r = 0; r < K; ++r) {
-      kth = warp_max(mine);
-      const unsigned hit = __ballot_sync(0xffffffffu, mine == kth);
-      if (lane == __ffs(hit) - 1) mine = neg_inf();
-    }
-    if (kth == kth) thr = fmaxf(thr, kth);
-    dirty = false;
-    since = 0;
-  }
-  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
-    const float xk = order_key(x);
-    if (ok) {
-      if (xk > m) rescale(xk);
-      if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
-      if (xk >= thr) {
-        t.push(xk, static_cast<int>(idx));
-        dirty = true;
-      }
-    }
-  }
-  // A 16-byte vector.  NaN elements are skipped by the max and never become
-  // candidates (NaN >= thr is false); they turn the sum into NaN, which the
-  // kernel repairs for that row.
-  __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool ok) {
-    constexpr int kv = Logit<DT>::kVec;
-    float x[kv];
-    unpack<DT>(raw, x);
-    float vmax;
-    if (DT == SPEC_BF16) {
-      vmax = max8_bf16(raw);
-    } else {
-      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
-    }
-    if (vmax > m) rescale(vmax);
-    if (m != neg_inf()) {
-      const float mc = m * c;
-#pragma unroll
-      for (int j = 0; j < kv; j += 2) {
-        s0 += fast_exp2(fmaf(x[j], c, -mc));
-        s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
-      }
-    }
-    if (ok && vmax >= thr && vmax >= t.v[K - 1]) {
-#pragma unroll
-      for (int j = 0; j < kv; ++j)
-        if (x[j] >= thr) t.push(x[j], static_cast<int>(first) + j);
-      dirty = true;
-    }
-    if (++since >= 8 && __any_sync(0xffffffffu, dirty)) refresh();
-  }
-
-  __device__ __forceinline__ void finish() {
-#pragma unroll 1
-    for (int r = 0; r < K; ++r) {
-      float bv = t.v[0];
-      int bi = t.i[0];
-      warp_best(bv, bi);
-      if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
-      if (lane == r) {
-        hv = bv;
-        hi = bi;
-      }
-    }
-  }
-};
-
-// K == 1: the top-1 is the argmax; no candidates needed.
+// Pass A of a draft row: each thread's online softmax and its best element
+// (value desc, index asc; NaN skipped).  For K == 1 the block's best is the
+// top-1; for K > 1 the thread bests give the pass-B threshold.
 template <int DT>
 struct ArgmaxVisitor {
   float c, m, s0, s1;
@@ -253,6 +146,86 @@ struct ArgmaxVisitor {
   }
   __device__ __forceinline__ void finish() {}
 };
+
+// Pass B of a draft row (K > 1): collect every element that comes before or
+// at the threshold pair (tv, ti) in the (value desc, index asc) order.  The
+// threshold is the K-th best of the thread bests of pass A, so at least K
+// elements qualify and no element after it can be in the top-K.  Appends use
+// a shared counter; their order does not matter (the final selection is by
+// the total order).
+constexpr int kCandCap = 1024;
+
+template <int DT>
+struct CandVisitor {
+  float tv;
+  int ti;
+  float* bv;
+  int* bi;
+  int* cnt;
+  __device__ __forceinline__ bool qualifies(float x, int idx) const {
+    return x > tv || (x == tv && idx <= ti);
+  }
+  __device__ __forceinline__ void add(float x, int idx) {
+    const int pos = atomicAdd(cnt, 1);
+    if (pos < kCandCap) {
+      bv[pos] = x;
+      bi[pos] = idx;
+    }
+  }
+  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
+    const float xk = order_key(x);
+    if (ok && qualifies(xk, static_cast<int>(idx))) add(xk, static_cast<int>(idx));
+  }
+  __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool ok) {
+    constexpr int kv = Logit<DT>::kVec;
+    float vmax;
+    float x[kv];
+    unpack<DT>(raw, x);
+    if (DT == SPEC_BF16) {
+      vmax = max8_bf16(raw);
+    } else {
+      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
+    }
+    // a -inf threshold (fewer than K finite keys) must still see -inf keys
+    if (!ok || !(vmax > tv || (vmax == tv && first <= ti) || tv == neg_inf())) return;
+#pragma unroll
+    for (int j = 0; j < kv; ++j) {
+      const float xk = order_key(x[j]);
+      if (qualifies(xk, static_cast<int>(first) + j)) add(xk, static_cast<int>(first) + j);
+    }
+  }
+};
+
+// The K best (value desc, index asc) of n pairs in shared memory, by warp 0:
+// K rounds of a warp-wide argmax, the winner's owner removing it.  Results
+// in out_v / out_i [K].
+template <int K>
+__device__ __forceinline__ void warp_select_k(float* v, int* idx, int n, float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  for (int r = 0; r < K; ++r) {
+    float bv = neg_inf();
+    int bi = INT_MAX, bpos = -1;
+    for (int e = lane; e < n; e += 32)
+      if (before(v[e], idx[e], bv, bi)) {
+        bv = v[e];
+        bi = idx[e];
+        bpos = e;
+      }
+    float wv = bv;
+    int wi = bi;
+    warp_best(wv, wi);
+    if (bpos >= 0 && wi != INT_MAX && bv == wv && bi == wi) {
+      v[bpos] = neg_inf();
+      idx[bpos] = INT_MAX;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      out_v[r] = wv;
+      out_i[r] = wi;
+    }
+  }
+  __syncwarp();
+}
 
 // Sum of 2^((key(x) - m) c) over a row with NaN as -inf.
 struct KeyedSum {
@@ -333,58 +306,43 @@ struct ZeroWriter {
 
 template <int K>
 constexpr size_t draft_smem_bytes() {
-  return 16;
+  return K == 1 ? 16 : kCandCap * (sizeof(float) + sizeof(int));
 }
 
-// One CTA per row: 16-byte loads (4 in flight per thread), the online
-// softmax per thread, the top-K per warp by warp select; merges are
-// fixed-order.
+// One CTA per row, 16-byte loads (4 in flight per thread).  Pass A: the
+// online softmax and every thread's best element; the K-th best of those
+// bests is a threshold with at least K elements before or at it.  Pass B
+// (K > 1): the row again, mostly from L2, collecting the few elements before
+// or at the threshold; the exact top-K is selected among them.  All
+// reductions are fixed-order.
 template <int DT, int K>
-__global__ void __launch_bounds__(kDraftThreads)
+__global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
     softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kDraftThreads / 32;
-  extern __shared__ __align__(16) unsigned char dsm[];
-  __shared__ float lv[kWarps * K];
-  __shared__ int li[kWarps * K];
+  extern __shared__ __align__(16) unsigned char dsm[];  // K > 1: candidate buffer
+  __shared__ float lv[kDraftThreads];
+  __shared__ int li[kDraftThreads];
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
+  __shared__ int s_cnt;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  float m, s;
-  if constexpr (K == 1) {
-    ArgmaxVisitor<DT> st{c};
-    st.reset();
-    for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
-    float bv = st.m;
-    int bi = st.bi;
-    warp_best(bv, bi);
-    if (lane == 0) {
-      lv[warp] = bv;
-      li[warp] = bi;
-    }
-    m = st.m;
-    s = st.s0 + st.s1;
-  } else {
-    DraftVisitor<DT, K> st{c};
-    st.lane = lane;
-    st.reset();
-    for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
-    st.finish();
-    if (lane < K) {
-      lv[warp * K + lane] = st.hv;
-      li[warp * K + lane] = st.hi;
-    }
-    m = st.m;
-    s = st.s0 + st.s1;
-  }
-  block_ms<0>(m, s, c, sm, ss);  // its barriers also publish every warp's list
+  // pass A: online softmax and every thread's best element
+  ArgmaxVisitor<DT> st{c};
+  st.reset();
+  for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
+  lv[threadIdx.x] = st.m;
+  li[threadIdx.x] = st.bi;
+  if (threadIdx.x == 0) s_cnt = 0;
+  float m = st.m, s = st.s0 + st.s1;
+  block_ms<0>(m, s, c, sm, ss);  // its barriers also publish lv / li
   if (isfinite(m) && !isfinite(s)) {
     // the row holds a NaN: recompute the normaliser with NaN as -inf
     KeyedSum ks{c, m * c, 0.0f};
@@ -397,25 +355,57 @@ __global__ void __launch_bounds__(kDraftThreads)
     for (int w2 = 0; w2 < kWarps; ++w2) tot += ss[w2];
     s = tot;
   }
-  if (warp == 0) {
-    // merge the warps' sorted lists: K rounds over kWarps * K entries
-    TopK<K> t;
-    t.init();
-    for (int e = lane; e < kWarps * K; e += 32) t.push(lv[e], li[e]);
-    for (int rr = 0; rr < K; ++rr) {
-      float bv = t.v[0];
-      int bi = t.i[0];
-      warp_best(bv, bi);
-      if (t.v[0] == bv && t.i[0] == bi && bi != INT_MAX) t.pop();
-      if (lane == 0) {
-        fv[rr] = bv;
-        fi[rr] = bi;
+  if constexpr (K == 1) {
+    if (warp == 0) warp_select_k<1>(lv, li, kDraftThreads, fv, fi);
+  } else {
+    // threshold: the K-th best of the thread bests (K distinct elements
+    // come before or at it)
+    if (warp == 0) warp_select_k<K>(lv, li, kDraftThreads, fv, fi);
+    __syncthreads();
+    const float tv = fv[K - 1];
+    const int ti = fi[K - 1];
+    // pass B: the row again (just read, so mostly from L2)
+    float* cv = reinterpret_cast<float*>(dsm);
+    int* ci = reinterpret_cast<int*>(cv + kCandCap);
+    CandVisitor<DT> cand{tv, ti, cv, ci, &s_cnt};
+    for_row_raw<DT, 4>(row, V, cand, threadIdx.x, kDraftThreads);
+    __syncthreads();
+    if (warp == 0) {
+      const int n = s_cnt;
+      if (n <= kCandCap) {
+        warp_select_k<K>(cv, ci, n, fv, fi);
+      } else {
+        // more candidates than the buffer holds (a long run of equal
+        // keys): rank the whole row, each pick the best element after the
+        // previous pick in the order
+        float pv = neg_inf();
+        int pi = -1;
+        for (int rr = 0; rr < K; ++rr) {
+          float bv = neg_inf();
+          int bi = INT_MAX;
+          for (int64_t v = lane; v < V; v += 32) {
+            const float x = order_key(Logit<DT>::load1(row, v));
+            if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
+              bv = x;
+              bi = static_cast<int>(v);
+            }
+          }
+          warp_best(bv, bi);
+          if (lane == 0) {
+            fv[rr] = bv;
+            fi[rr] = bi;
+          }
+          pv = bv;
+          pi = bi;
+          __syncwarp();
+        }
       }
     }
+  }
+  if (warp == 0) {
     __syncwarp();
     if (fi[k - 1] == INT_MAX && k <= V) {
-      // fewer than k non-NaN logits: rank the row again with NaN as -inf,
-      // each pick the best element after the previous one in the order
+      // fewer than k non-NaN logits: rank the row again with NaN as -inf
       float pv = neg_inf();
       int pi = -1;
       for (int rr = 0; rr < k; ++rr) {

@@ -120,7 +120,7 @@ constexpr int kStatThreads = SPEC_STAT_THREADS;
 // keeps HBM at the copy rate; staging through shared memory with bulk
 // copies was slower for this access pattern.
 template <int DT, bool STOCH>
-__global__ void __launch_bounds__(kStatThreads)
+__global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
     row_stats_kernel(const void* __restrict__ logits, int64_t V, float c, int32_t* __restrict__ amax,
                      float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
