@@ -7,11 +7,13 @@
 // drafts are drawn from it.
 //
 // One CTA streams one logit row with 16-byte loads (4 in flight per thread).
-// A single pass gives each thread's online softmax partials (max, sum of
-// 2^((x - max) * log2e / T)) and each warp's top-K by warp select (a shared
-// threshold and candidate buffer, so the common element costs one compare);
-// block merges are fixed-order.  The optional probability row is written by
-// a second sweep of the row (served from L2) with streaming stores.
+// That pass gives each thread's online softmax partials (max, sum of
+// 2^((x - max) * log2e / T)) and its best element.  The K-th best of the
+// thread bests bounds the top-K from below, so only the few threads whose
+// best reaches it can own a top-K element: the block reads their elements
+// again (from L2) and ranks the few that reach the bound.  Block merges are
+// fixed-order.  The optional probability row is written by a second sweep
+// of the row (served from L2) with streaming stores.
 #include <climits>
 
 #include "cdf.cuh"
@@ -21,7 +23,7 @@ namespace specdec {
 namespace {
 
 #ifndef SPEC_DRAFT_THREADS
-#define SPEC_DRAFT_THREADS 256
+#define SPEC_DRAFT_THREADS 128
 #endif
 constexpr int kDraftThreads = SPEC_DRAFT_THREADS;
 
@@ -154,6 +156,9 @@ struct ArgmaxVisitor {
 // a shared counter; their order does not matter (the final selection is by
 // the total order).
 constexpr int kCandCap = 1024;
+// Up to this many candidates are placed by ranking (n^2 / threads compares
+// per thread); more (long runs of equal keys) go to the warp select.
+constexpr int kRankCands = 256;
 
 template <int DT>
 struct CandVisitor {
@@ -195,6 +200,50 @@ struct CandVisitor {
     }
   }
 };
+
+// The elements owned by the threads listed in owner[0..n_owner) (owner t
+// holds, in the layout of for_row_raw, the scalars t, t + nthreads, ... of
+// the head and tail and the 16-byte vectors t, t + nthreads, ...), visited
+// by the whole block: each block thread takes every nthreads-th (owner,
+// vector) pair, 4 loads in flight.
+template <int DT, class F>
+__device__ __forceinline__ void rescan_owners(const void* row, int64_t V, F& f, const int* owner, int n_owner,
+                                              int nthreads) {
+  constexpr int kv = Logit<DT>::kVec;
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  const RowSpan sp = row_span<DT>(row, V);
+  const int tid = threadIdx.x;
+  const int64_t tail0 = sp.head + sp.nvec * kv;
+  for (int e = tid; e < n_owner; e += nthreads) {
+    const int t = owner[e];
+    for (int64_t i = t; i < sp.head; i += nthreads) f.visit1(Logit<DT>::load1(row, i), i, true);
+    for (int64_t i = tail0 + t; i < V; i += nthreads) f.visit1(Logit<DT>::load1(row, i), i, true);
+  }
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+  const int64_t per = (sp.nvec + nthreads - 1) / nthreads;  // vectors of owner 0
+  const int64_t total = per * n_owner;
+  for (int64_t e0 = 0; e0 < total; e0 += 4 * static_cast<int64_t>(nthreads)) {
+    uint4 v[4];
+    int64_t vi[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t e = e0 + tid + u * static_cast<int64_t>(nthreads);
+      vi[u] = e < total ? owner[e / per] + (e % per) * nthreads : sp.nvec;
+      if (vi[u] < sp.nvec) v[u] = __ldg(vp + vi[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (vi[u] < sp.nvec) f.visit_vec(v[u], sp.head + vi[u] * kv, true);
+  }
+}
+
+// Number of the n pairs (v, idx) in shared memory that come before (x, i)
+// in the (value desc, index asc) order.
+__device__ __forceinline__ int rank_among(float x, int i, const float* v, const int* idx, int n) {
+  int r = 0;
+  for (int e = 0; e < n; ++e) r += before(v[e], idx[e], x, i) ? 1 : 0;
+  return r;
+}
 
 // The K best (value desc, index asc) of n pairs in shared memory, by warp 0:
 // K rounds of a warp-wide argmax, the winner's owner removing it.  Results
@@ -312,8 +361,9 @@ constexpr size_t draft_smem_bytes() {
 // One CTA per row, 16-byte loads (4 in flight per thread).  Pass A: the
 // online softmax and every thread's best element; the K-th best of those
 // bests is a threshold with at least K elements before or at it.  Pass B
-// (K > 1): the row again, mostly from L2, collecting the few elements before
-// or at the threshold; the exact top-K is selected among them.  All
+// (K > 1): the block reads again (from L2) the elements of the threads
+// whose best reaches the threshold (about K of them), collecting the
+// elements before or at it; the exact top-K is ranked among them.  All
 // reductions are fixed-order.
 template <int DT, int K>
 __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
@@ -329,7 +379,9 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
-  __shared__ int s_cnt;
+  __shared__ int s_owner[K > 1 ? kDraftThreads : 1];
+  __shared__ int s_cnt, s_nown, s_ti;
+  __shared__ float s_tv;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
@@ -340,7 +392,16 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
   for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
   lv[threadIdx.x] = st.m;
   li[threadIdx.x] = st.bi;
-  if (threadIdx.x == 0) s_cnt = 0;
+  if (threadIdx.x == 0) {
+    s_cnt = 0;
+    s_nown = 0;
+    s_tv = neg_inf();  // no thread best ranked K-1 (equal empty pairs): all qualify
+    s_ti = INT_MAX;
+  }
+  if (threadIdx.x < K) {
+    fv[threadIdx.x] = neg_inf();
+    fi[threadIdx.x] = INT_MAX;
+  }
   float m = st.m, s = st.s0 + st.s1;
   block_ms<0>(m, s, c, sm, ss);  // its barriers also publish lv / li
   if (isfinite(m) && !isfinite(s)) {
@@ -359,19 +420,35 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
     if (warp == 0) warp_select_k<1>(lv, li, kDraftThreads, fv, fi);
   } else {
     // threshold: the K-th best of the thread bests (K distinct elements
-    // come before or at it)
-    if (warp == 0) warp_select_k<K>(lv, li, kDraftThreads, fv, fi);
+    // come before or at it), found by ranking every thread best
+    const int rank = rank_among(st.m, st.bi, lv, li, kDraftThreads);
+    if (rank == K - 1) {
+      s_tv = st.m;
+      s_ti = st.bi;
+    }
     __syncthreads();
-    const float tv = fv[K - 1];
-    const int ti = fi[K - 1];
-    // pass B: the row again (just read, so mostly from L2)
+    const float tv = s_tv;
+    const int ti = s_ti;
+    // pass B: an element can only qualify if its thread's best does; the
+    // block reads the few qualifying threads' elements again (from L2)
     float* cv = reinterpret_cast<float*>(dsm);
     int* ci = reinterpret_cast<int*>(cv + kCandCap);
     CandVisitor<DT> cand{tv, ti, cv, ci, &s_cnt};
-    for_row_raw<DT, 4>(row, V, cand, threadIdx.x, kDraftThreads);
+    if (cand.qualifies(st.m, st.bi)) s_owner[atomicAdd(&s_nown, 1)] = threadIdx.x;
     __syncthreads();
-    if (warp == 0) {
-      const int n = s_cnt;
+    rescan_owners<DT>(row, V, cand, s_owner, s_nown, kDraftThreads);
+    __syncthreads();
+    const int n = s_cnt;
+    if (n <= kRankCands) {
+      // the candidates' pairs are distinct: their ranks place them
+      for (int e = threadIdx.x; e < n; e += kDraftThreads) {
+        const int rk = rank_among(cv[e], ci[e], cv, ci, n);
+        if (rk < K) {
+          fv[rk] = cv[e];
+          fi[rk] = ci[e];
+        }
+      }
+    } else if (warp == 0) {
       if (n <= kCandCap) {
         warp_select_k<K>(cv, ci, n, fv, fi);
       } else {
@@ -401,6 +478,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
         }
       }
     }
+    __syncthreads();
   }
   if (warp == 0) {
     __syncwarp();
