@@ -6,9 +6,10 @@
 // u the draw is the smallest v whose inclusive prefix sum of the weights
 // exceeds u * W, W the total.
 //
-// The row is cut into tiles of THREADS * 8 elements; thread j of a tile owns
-// its 8 consecutive elements.  cdf_tile_pass streams the row once and
-// records every tile's sum (warp sums in a fixed order, no atomics).
+// The row is cut into tiles of THREADS * E elements; thread j of a tile
+// owns its E consecutive elements (E = 8 for the one-CTA-per-row draft
+// sampler, larger for the walk).  cdf_tile_pass / cdf_tile_pass_split stream
+// the row once and record every tile's sum in a fixed order, no atomics.
 // cdf_search walks the tile sums in order to the first tile whose running
 // prefix exceeds u * W and rescans only that tile with a block scan; if
 // rounding leaves no crossing inside it, the following tiles are scanned;
@@ -62,10 +63,113 @@ __device__ float cdf_tile_pass(const W& w, int64_t V, float* red, float* tile_su
   return total;
 }
 
-template <int THREADS, class W>
+// cdf_tile_pass split over the C CTAs of a thread-block cluster that walk
+// one row together (a latency-bound walk; C = 1 is a lone CTA).  Tiles are
+// THREADS * E elements.  CTA `rank` sums the tiles rank, rank + C, ... (its
+// local tiles i = 0, 1, ...): every thread stores the sum of its E elements
+// of local tile i in part[i % P][thread], and every P local tiles (and at
+// the end) each warp reduces whole tiles (lanes over the partials in thread
+// order, then a butterfly), so the stream itself carries no reduction.
+// Each tile sum is stored into tile_sum of every CTA of the cluster; after
+// the cluster barrier all of them hold the same tile sums and the same total
+// (tile order).
+//
+// Loads: where w.ring_ok(), each thread keeps its next D tiles in flight
+// with asynchronous copies into its own slots of a shared-memory ring, so
+// loading overlaps the arithmetic without block barriers (a thread reads
+// only what it copied); otherwise direct 16-byte loads.  W provides
+//   template <int E> static constexpr int chunks()   16-byte chunks per thread and tile
+//   bool ring_ok() const                             rows 16-byte aligned
+//   template <int E> void issue(uint4* slot, int stride, int64_t v0) const
+//   template <int E> float ring_sum(const uint4* slot, int stride, int64_t v0) const
+//   template <int E> float load_sum(int64_t v0) const
+// where ring_sum and load_sum add the same values in the same order.  ring:
+// D * chunks<E>() * THREADS 16-byte slots, chunk c of slot s of thread t at
+// ring[(s * chunks + c) * THREADS + t].  part: cdf_part_tiles * THREADS
+// floats.  V + THREADS * E < 2^31.
+constexpr int kPartTiles = 64;  // P
+
+template <int THREADS, int E, int C>
+__host__ __device__ inline int cdf_part_tiles(int64_t V) {
+  const int64_t ntiles = (V + THREADS * E - 1) / (THREADS * E);
+  const int64_t nloc = (ntiles + C - 1) / C;
+  return static_cast<int>(nloc < kPartTiles ? nloc : kPartTiles);
+}
+
+template <int THREADS, int E, int D, int C, class W>
+__device__ float cdf_tile_pass_split(const W& w, int64_t V64, float* part, float* tile_sum, uint4* ring,
+                                     unsigned rank) {
+  constexpr int kTile = THREADS * E, kWarps = THREADS / 32, K = W::template chunks<E>(), P = kPartTiles;
+  const int V = static_cast<int>(V64);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+  const int ntiles = (V + kTile - 1) / kTile;
+  const int r = static_cast<int>(rank);
+  const int nloc = ntiles > r ? (ntiles - r + C - 1) / C : 0;
+  const int off = tid * E;
+  auto first = [&](int i) { return (r + C * i) * kTile + off; };  // thread's first element of local tile i
+  // reduce local tiles [i0, i1) (at most P) and store their sums everywhere
+  auto flush = [&](int i0, int i1) {
+    __syncthreads();
+    for (int i = i0 + warp; i < i1; i += kWarps) {
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kWarps; ++j) s += part[(i % P) * THREADS + j * 32 + lane];
+      s = warp_sum(s);
+      if (lane == 0) {
+        const int t = r + C * i;
+        if (C == 1) {
+          tile_sum[t] = s;
+        } else {
+#pragma unroll
+          for (int q = 0; q < C; ++q) st_cluster_f32(tile_sum + t, q, s);
+        }
+      }
+    }
+    __syncthreads();
+  };
+  int done = 0;  // local tiles reduced so far
+  if (w.ring_ok()) {
+    uint4* mine = ring + tid;
+#pragma unroll
+    for (int s = 0; s < D; ++s) {
+      if (s < nloc) w.template issue<E>(mine + s * K * THREADS, THREADS, first(s));
+      cp_async_commit();  // one group per local tile (empty ones keep the count)
+    }
+    int s = 0;
+    for (int i = 0; i < nloc; ++i) {
+      cp_async_wait<D - 1>();  // tile i has landed
+      const float ps = w.template ring_sum<E>(mine + s * K * THREADS, THREADS, first(i));
+      part[(i % P) * THREADS + tid] = ps;  // the slot has been read
+      if (i + D < nloc) w.template issue<E>(mine + s * K * THREADS, THREADS, first(i + D));
+      cp_async_commit();
+      s = s + 1 == D ? 0 : s + 1;
+      if (i + 1 - done == P && i + 1 < nloc) {
+        flush(done, i + 1);
+        done = i + 1;
+      }
+    }
+    cp_async_wait<0>();
+  } else {
+    for (int i = 0; i < nloc; ++i) {
+      part[(i % P) * THREADS + tid] = w.template load_sum<E>(first(i));
+      if (i + 1 - done == P && i + 1 < nloc) {
+        flush(done, i + 1);
+        done = i + 1;
+      }
+    }
+  }
+  flush(done, nloc);
+  if (C > 1) cluster_barrier();
+  float total = 0.0f;
+  for (int t = 0; t < ntiles; ++t) total += tile_sum[t];
+  return total;
+}
+
+template <int THREADS, class W, int E = 8>
 __device__ int32_t cdf_search(const W& w, int64_t V, float u, const float* tile_sum, float total,
                               float* scan_sh, int32_t* stats) {
-  constexpr int kTile = THREADS * 8;
+  static_assert(E % 8 == 0, "elements per thread come in groups of 8");
+  constexpr int kTile = THREADS * E;
   __shared__ int32_t s_tok;
   const int64_t ntiles = (V + kTile - 1) / kTile;
   if (threadIdx.x == 0) s_tok = INT_MAX;
@@ -76,18 +180,19 @@ __device__ int32_t cdf_search(const W& w, int64_t V, float u, const float* tile_
     for (int64_t t = 0; t < ntiles; ++t) {
       const float after = prefix + tile_sum[t];
       if (after > target) {
-        const int64_t v0 = t * kTile + threadIdx.x * 8;
-        float x[8];
-        w.load8(v0, x);
+        const int64_t v0 = t * kTile + threadIdx.x * E;
+        float x[E];
+#pragma unroll
+        for (int g = 0; g < E / 8; ++g) w.load8(v0 + 8 * g, x + 8 * g);
         float sum = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sum += x[j];
+        for (int j = 0; j < E; ++j) sum += x[j];
         float tot;
         const float incl = block_inclusive_scan(sum, scan_sh, tot);
         float C = prefix + (incl - sum);
         int found = -1;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < E; ++j) {
           C += x[j];
           if (found < 0 && C > target && v0 + j < V) found = j;
         }

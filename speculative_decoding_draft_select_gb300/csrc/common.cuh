@@ -65,6 +65,61 @@ __device__ __forceinline__ void st_stream(void* p, float4 v) {
                : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, cached in L2
+// only); bytes past src_bytes (0..16) are zero-filled.  The source must be
+// 16-byte aligned.  Completion is awaited with cp_async_wait by the issuing
+// thread, which alone may then read the destination.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Thread-block clusters: this CTA's rank, a barrier over every thread of
+// every CTA of the cluster (release / acquire: shared-memory writes before
+// it, local or remote, are visible after it), and a store into the shared
+// memory of another CTA of the cluster at the address that corresponds to
+// a local one.
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(float* local, unsigned rank, float v) {
+  const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(local));
+  unsigned ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
+// Asynchronous copy of the E elements [v0, v0 + E) of a row (element size
+// ESZ, 16-byte aligned base, v0 * ESZ a multiple of 16) into E * ESZ / 16
+// chunks slot[0], slot[stride], ...; elements at or past V are zero-filled.
+template <int E, int ESZ>
+__device__ __forceinline__ void issue_row(uint4* slot, int stride, const void* row, int64_t V, int64_t v0) {
+  constexpr int per = 16 / ESZ, nch = E / per;
+  const char* src = static_cast<const char*>(row) + v0 * ESZ;
+  if (v0 + E <= V) {
+#pragma unroll
+    for (int c = 0; c < nch; ++c) cp_async16(slot + c * stride, src + 16 * c, 16);
+    return;
+  }
+#pragma unroll
+  for (int c = 0; c < nch; ++c) {
+    const int64_t left = V - (v0 + c * per);
+    const int n = left <= 0 ? 0 : (left >= per ? per : static_cast<int>(left));
+    cp_async16(slot + c * stride, n > 0 ? src + 16 * c : row, n * ESZ);
+  }
+}
+
 // Unpack one 16-byte vector into kVec floats.
 template <int DT>
 __device__ __forceinline__ void unpack(const uint4& v, float* x);

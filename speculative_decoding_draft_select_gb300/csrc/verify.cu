@@ -34,7 +34,28 @@
 namespace specdec {
 namespace {
 
-constexpr int kWalkThreads = 512;
+#ifndef SPEC_WALK_THREADS
+#define SPEC_WALK_THREADS 128
+#endif
+#ifndef SPEC_WALK_CLUSTER
+#define SPEC_WALK_CLUSTER 4
+#endif
+#ifndef SPEC_WALK_ELEMS
+#define SPEC_WALK_ELEMS 16
+#endif
+// The stochastic walk: kWalkCluster CTAs of kWalkThreads threads per request.
+constexpr int kWalkThreads = SPEC_WALK_THREADS;
+constexpr int kWalkCluster = SPEC_WALK_CLUSTER;
+constexpr int kWalkElems = SPEC_WALK_ELEMS;  // consecutive elements per thread in a tile
+constexpr size_t kMaxDynSmem = 227 * 1024;  // opt-in shared memory of one CTA
+
+// Tiles each walk thread keeps in flight: 2 to 8, the ring at most 32 KB per
+// CTA (four CTAs share an SM).
+__host__ __device__ constexpr int walk_ring_depth(int chunks) {
+  return 32768 / (chunks * kWalkThreads * 16) > 8   ? 8
+         : 32768 / (chunks * kWalkThreads * 16) < 2 ? 2
+                                                     : 32768 / (chunks * kWalkThreads * 16);
+}
 
 __device__ __forceinline__ float prob_of(float key, float c, float mc, float invz) {
   return fminf(fast_exp2(fmaf(key, c, -mc)) * invz, 1.0f);
@@ -258,13 +279,73 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
 // Where a node's draft distribution q comes from.
 //   QProbs:     materialised fp32 rows (q[v] read directly).
 //   QLogits<D>: the draft logits row and that row's (max, normaliser) as the
-//               draft softmax wrote them; q[v] = 2^((l_v - max) c) / Z with
-//               the same fp32 operations as the written probabilities, so
-//               both forms give bit-identical q values.
+//               draft softmax wrote them.  q_at(y), used by the acceptance
+//               test, takes the same fp32 operations as the written
+//               probabilities, so both forms give bit-identical q[y].
+// The residual sweeps need q for a whole row; there (load8, ring_q8,
+// sweep_at) the normaliser is folded into the exponent,
+// q[v] = 2^(l_v c + nb), nb = -(max c + log2 Z), one operation fewer per
+// element.  Rows whose 16-byte chunks start aligned are streamed through the
+// walk's shared-memory ring (issue / ring_q8), others with direct loads.
+
+__device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Exponent offset nb of a row's softmax: p(x) = 2^(x c + nb); -inf when the
+// row has no finite max, which makes every probability 0 (a NaN logit gives
+// NaN, which the residual's max(0, .) turns into 0).
+__device__ __forceinline__ float folded_offset(float m, float c, float z) {
+  return (isfinite(m) && z > 0.0f && isfinite(z)) ? -fmaf(m, c, log2f(z)) : neg_inf();
+}
+
+// 8 logits [v0, v0 + 8) of a row as floats (NaN kept); past V: -inf.
+template <int DT>
+__device__ __forceinline__ void raw8_global(const void* row, int64_t V, int64_t v0, float* x) {
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  const char* p = static_cast<const char*>(row) + v0 * esz;
+  if (v0 + 8 <= V && aligned16(p)) {
+    if (DT == SPEC_BF16) {
+      unpack<SPEC_BF16>(__ldg(reinterpret_cast<const uint4*>(p)), x);
+    } else {
+      unpack<SPEC_F32>(__ldg(reinterpret_cast<const uint4*>(p)), x);
+      unpack<SPEC_F32>(__ldg(reinterpret_cast<const uint4*>(p) + 1), x + 4);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = v0 + j < V ? Logit<DT>::load1(row, v0 + j) : neg_inf();
+  }
+}
+
+// Group g (elements [8g, 8g + 8)) of a thread's ring chunks of one row, as
+// floats.  DT: logits (bf16 or fp32).
+template <int DT>
+__device__ __forceinline__ void ring8(const uint4* slot, int stride, int g, float* x) {
+  if (DT == SPEC_BF16) {
+    unpack<SPEC_BF16>(slot[g * stride], x);
+  } else {
+    unpack<SPEC_F32>(slot[(2 * g) * stride], x);
+    unpack<SPEC_F32>(slot[(2 * g + 1) * stride], x + 4);
+  }
+}
+
+__device__ __forceinline__ void mask_past(float* x, int64_t v0, int64_t V, float fill) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (v0 + j >= V) x[j] = fill;
+}
+
+// Pairs of fp32 lanes (the packed fp32 instructions of sm_100 and later:
+// each lane rounds exactly as the scalar operation).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 splat(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 exp2_2(float2 a) { return make_float2(fast_exp2(a.x), fast_exp2(a.y)); }
+
 struct QRowProbs {
+  static constexpr int kEsz = 4;
   const float* row;  // nullptr: no row (q = 0)
   int64_t V;
-  __device__ __forceinline__ float at(int64_t v) const { return row ? __ldg(row + v) : 0.0f; }
+  __device__ __forceinline__ float q_at(int64_t v) const { return row ? __ldg(row + v) : 0.0f; }
+  __device__ __forceinline__ float sweep_at(int64_t v) const { return q_at(v); }
   __device__ __forceinline__ void load8(int64_t v0, float* x) const {
     if (row) {
       load8_f32(row, V, v0, x);
@@ -273,9 +354,24 @@ struct QRowProbs {
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
     }
   }
+  __device__ __forceinline__ bool ring_ok() const { return row == nullptr || aligned16(row); }
+  template <int E>
+  __device__ __forceinline__ void issue(uint4* slot, int stride, int64_t v0) const {
+    if (row) issue_row<E, 4>(slot, stride, row, V, v0);
+  }
+  // q of group g from the ring (zero-filled past V)
+  __device__ __forceinline__ void ring_q8(const uint4* slot, int stride, int g, int64_t, bool, float* x) const {
+    if (row) {
+      ring8<SPEC_F32>(slot, stride, g, x);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+  }
 };
 
 struct QProbs {
+  using Row = QRowProbs;
   const float* q;
   int64_t V;
   __device__ __forceinline__ QRowProbs row(int64_t r) const { return {r >= 0 ? q + r * V : nullptr, V}; }
@@ -283,17 +379,46 @@ struct QProbs {
 
 template <int QDT>
 struct QRowLogits {
+  static constexpr int kEsz = QDT == SPEC_BF16 ? 2 : 4;
   const void* row;  // nullptr: no row, or a row whose max is not finite (q = 0)
   int64_t V;
-  float c, mc, invz;
-  __device__ __forceinline__ float at(int64_t v) const {
+  float c, mc, invz, nb;
+  __device__ __forceinline__ float q_at(int64_t v) const {
     return row ? prob_of(order_key(Logit<QDT>::load1(row, v)), c, mc, invz) : 0.0f;
+  }
+  __device__ __forceinline__ float sweep_at(int64_t v) const {
+    return row ? fast_exp2(fmaf(order_key(Logit<QDT>::load1(row, v)), c, nb)) : 0.0f;
+  }
+  // 8 q values from 8 logits (NaN as -inf), in the packed form of the sweeps
+  __device__ __forceinline__ void probs8(float* x) const {
+    const float2 c2 = splat(c), nb2 = splat(nb);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 e = exp2_2(fma2(make_float2(order_key(x[j]), order_key(x[j + 1])), c2, nb2));
+      x[j] = e.x;
+      x[j + 1] = e.y;
+    }
   }
   __device__ __forceinline__ void load8(int64_t v0, float* x) const {
     if (row) {
-      load8_logits<QDT>(row, V, v0, x);
+      raw8_global<QDT>(row, V, v0, x);
+      probs8(x);
+    } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = prob_of(x[j], c, mc, invz);
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+  }
+  __device__ __forceinline__ bool ring_ok() const { return row == nullptr || aligned16(row); }
+  template <int E>
+  __device__ __forceinline__ void issue(uint4* slot, int stride, int64_t v0) const {
+    if (row) issue_row<E, kEsz>(slot, stride, row, V, v0);
+  }
+  __device__ __forceinline__ void ring_q8(const uint4* slot, int stride, int g, int64_t v0, bool full,
+                                          float* x) const {
+    if (row) {
+      ring8<QDT>(slot, stride, g, x);
+      if (!full) mask_past(x, v0, V, neg_inf());
+      probs8(x);
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
@@ -303,46 +428,118 @@ struct QRowLogits {
 
 template <int QDT>
 struct QLogits {
+  using Row = QRowLogits<QDT>;
   const void* q;
   const float* stats;  // [rows, 2]: max, normaliser
   int64_t V;
   float c;
   __device__ __forceinline__ QRowLogits<QDT> row(int64_t r) const {
     constexpr int esz = QDT == SPEC_BF16 ? 2 : 4;
-    if (r < 0) return {nullptr, V, c, 0.0f, 0.0f};
+    if (r < 0) return {nullptr, V, c, 0.0f, 0.0f, 0.0f};
     const float m = __ldg(stats + 2 * r), z = __ldg(stats + 2 * r + 1);
-    if (!isfinite(m)) return {nullptr, V, c, 0.0f, 0.0f};
-    return {static_cast<const char*>(q) + r * V * esz, V, c, m * c, 1.0f / z};
+    if (!isfinite(m)) return {nullptr, V, c, 0.0f, 0.0f, 0.0f};
+    return {static_cast<const char*>(q) + r * V * esz, V, c, m * c, 1.0f / z, folded_offset(m, c, z)};
   }
 };
 
-// Weights of the current distribution at a node: p (A == 0) or the
-// unnormalised residual max(0, p - A q).
+// Weights of the current distribution at a node for the sweeps: p (A == 0)
+// or the unnormalised residual max(0, p - A q), with p(v) = 2^(l_v c + nb).
+// Element values are computed two at a time with the packed fp32
+// instructions; load8 (per element, for the draw), ring_sum and load_sum
+// (sums for the tile pass) give the same values.
 template <int DT, class QRow>
 struct ResidualWeights {
+  static constexpr int kTargetEsz = DT == SPEC_BF16 ? 2 : 4;
+  template <int E>
+  __host__ __device__ static constexpr int target_chunks() {
+    return E * kTargetEsz / 16;
+  }
+  template <int E>
+  __host__ __device__ static constexpr int chunks() {
+    return E * (kTargetEsz + QRow::kEsz) / 16;
+  }
   const void* lrow;
   QRow qrow;
   int64_t V;
-  float c, mc, invz, A;
-  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
-    load8_logits<DT>(lrow, V, v0, x);
+  float c, nb, A;
+  // x <- weights of 8 elements from logits l (and q values when A != 0)
+  __device__ __forceinline__ void values8(float* l, const float* q) const {
+    const float2 c2 = splat(c), nb2 = splat(nb), na2 = splat(-A);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = prob_of(x[j], c, mc, invz);
+    for (int j = 0; j < 8; j += 2) {
+      float2 r = exp2_2(fma2(make_float2(l[j], l[j + 1]), c2, nb2));
+      if (q != nullptr) r = fma2(na2, make_float2(q[j], q[j + 1]), r);
+      l[j] = fmaxf(0.0f, r.x);
+      l[j + 1] = fmaxf(0.0f, r.y);
+    }
+  }
+  __device__ __forceinline__ static float2 acc8(float2 acc, const float* x) {
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) acc = add2(acc, make_float2(x[j], x[j + 1]));
+    return acc;
+  }
+  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
+    raw8_global<DT>(lrow, V, v0, x);
     if (A != 0.0f) {
       float q[8];
       qrow.load8(v0, q);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = fmaxf(0.0f, fmaf(-A, q[j], x[j]));
+      values8(x, q);
+    } else {
+      values8(x, nullptr);
     }
   }
   __device__ __forceinline__ float at(int64_t v) const {
-    const float p = prob_of(order_key(Logit<DT>::load1(lrow, v)), c, mc, invz);
-    return A != 0.0f ? fmaxf(0.0f, fmaf(-A, qrow.at(v), p)) : p;
+    const float p = fast_exp2(fmaf(Logit<DT>::load1(lrow, v), c, nb));
+    return fmaxf(0.0f, A != 0.0f ? fmaf(-A, qrow.sweep_at(v), p) : p);
+  }
+  template <int E>
+  __device__ __forceinline__ float load_sum(int64_t v0) const {
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int g = 0; g < E / 8; ++g) {
+      float x[8];
+      load8(v0 + 8 * g, x);
+      acc = acc8(acc, x);
+    }
+    return acc.x + acc.y;
+  }
+  __device__ __forceinline__ bool ring_ok() const { return aligned16(lrow) && (A == 0.0f || qrow.ring_ok()); }
+  template <int E>
+  __device__ __forceinline__ void issue(uint4* slot, int stride, int64_t v0) const {
+    issue_row<E, kTargetEsz>(slot, stride, lrow, V, v0);
+    if (A != 0.0f) qrow.template issue<E>(slot + target_chunks<E>() * stride, stride, v0);
+  }
+  template <int E>
+  __device__ __forceinline__ float ring_sum(const uint4* slot, int stride, int64_t v0) const {
+    const bool full = v0 + E <= V;
+    const uint4* qslot = slot + target_chunks<E>() * stride;
+    float2 acc = make_float2(0.0f, 0.0f);
+    if (A != 0.0f) {
+#pragma unroll
+      for (int g = 0; g < E / 8; ++g) {
+        float x[8], q[8];
+        ring8<DT>(slot, stride, g, x);
+        if (!full) mask_past(x, v0 + 8 * g, V, neg_inf());
+        qrow.ring_q8(qslot, stride, g, v0 + 8 * g, full, q);
+        values8(x, q);
+        acc = acc8(acc, x);
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < E / 8; ++g) {
+        float x[8];
+        ring8<DT>(slot, stride, g, x);
+        if (!full) mask_past(x, v0 + 8 * g, V, neg_inf());
+        values8(x, nullptr);
+        acc = acc8(acc, x);
+      }
+    }
+    return acc.x + acc.y;
   }
 };
 
 template <int DT, class QSrc>
-__global__ void __launch_bounds__(kWalkThreads)
+__global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     sample_walk_kernel(int N, int64_t V, float c, const void* __restrict__ target,
                        const float* __restrict__ m_row, const float* __restrict__ z_row, QSrc qsrc,
                        const int32_t* __restrict__ q_row, const int32_t* __restrict__ dtok,
@@ -352,11 +549,16 @@ __global__ void __launch_bounds__(kWalkThreads)
                        int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
                        int32_t* next_root, int32_t* walk_info, int32_t* stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  extern __shared__ float dyn[];
-  const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
-  float* tile_sum = dyn;
-  float* red = tile_sum + ntiles;
-  float* g_l = red + ntiles * (kWalkThreads / 32);
+  using Weights = ResidualWeights<DT, typename QSrc::Row>;
+  constexpr int kChunks = Weights::template chunks<kWalkElems>();
+  constexpr int kRing = walk_ring_depth(kChunks);
+  extern __shared__ uint4 dyn_ring[];
+  uint4* ring = dyn_ring;
+  float* dyn = reinterpret_cast<float*>(ring + kRing * kChunks * kWalkThreads);
+  const int64_t ntiles = (V + kWalkThreads * kWalkElems - 1) / (kWalkThreads * kWalkElems);
+  float* tile_sums = dyn;  // two buffers of ntiles, used by alternate passes
+  float* part = tile_sums + 2 * ntiles;
+  float* g_l = part + static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, kWalkCluster>(V)) * kWalkThreads;
   float* g_q = g_l + N;
   float* g_u = g_q + N;
   int32_t* s_dt = reinterpret_cast<int32_t*>(g_u + N);
@@ -368,10 +570,22 @@ __global__ void __launch_bounds__(kWalkThreads)
   __shared__ float scan_sh[33];
   __shared__ int s_n, s_len, s_acc, s_rej, s_kind, s_done, s_nch, s_accept, s_tiles_ok, s_rem;
   __shared__ int64_t s_qrow;
-  __shared__ float s_m, s_invz, s_A, s_cj, s_total;
+  __shared__ float s_m, s_invz, s_nb, s_A, s_cj, s_total;
 
-  const int b = blockIdx.x, tid = threadIdx.x;
+  // the kWalkCluster CTAs of a cluster walk request b together: each pass
+  // over a row is split between them, everything else is done by each CTA
+  // on the same data, so all of them take the same decisions; rank 0 alone
+  // counts anomalies and writes the outputs
+  const unsigned rank = kWalkCluster > 1 ? cluster_rank() : 0u;
+  const int b = blockIdx.x / kWalkCluster, tid = threadIdx.x;
+  int32_t* const cstats = rank == 0 ? stats : nullptr;
   const int64_t o = static_cast<int64_t>(b) * N;
+  int par = 0;  // tile-sum buffer of the next pass
+  auto pass = [&](const Weights& w) -> float {
+    float* ts = tile_sums + par * ntiles;
+    par ^= 1;
+    return cdf_tile_pass_split<kWalkThreads, kWalkElems, kRing, kWalkCluster>(w, V, part, ts, ring, rank);
+  };
   for (int i = tid; i < N; i += kWalkThreads) {
     s_dt[i] = __ldg(dtok + o + i);
     s_nt[i] = __ldg(ntok + o + i);
@@ -390,6 +604,7 @@ __global__ void __launch_bounds__(kWalkThreads)
     s_path[0] = 0;
   }
   __syncthreads();
+  if (kWalkCluster > 1) cluster_barrier();  // every CTA of the cluster is running
   const float cT = c;
   while (!s_done) {
     // enter node n: children in sibling order, row statistics, q row
@@ -398,8 +613,10 @@ __global__ void __launch_bounds__(kWalkThreads)
       int nch = 0;
       for (int ch = s_nt[n]; ch > 0 && ch < N && nch < N; ch = s_ns[ch]) s_ch[nch++] = ch;
       s_nch = nch;
+      const float z = __ldg(z_row + o + n);
       s_m = __ldg(m_row + o + n);
-      s_invz = 1.0f / __ldg(z_row + o + n);
+      s_invz = 1.0f / z;
+      s_nb = folded_offset(s_m, c, z);
       s_qrow = q_row ? static_cast<int64_t>(__ldg(q_row + o + n)) : o + n;
       s_A = 0.0f;
       s_cj = 1.0f;
@@ -409,23 +626,24 @@ __global__ void __launch_bounds__(kWalkThreads)
     const int n = s_n, nch = s_nch;
     const void* lrow = static_cast<const char*>(target) + (o + n) * V * esz;
     const auto qrow = qsrc.row(nch > 0 ? s_qrow : -1);
-    const float mc = s_m * cT, invz = s_invz;
+    const float mc = s_m * cT, invz = s_invz, nb = s_nb;
+    const bool p_finite = isfinite(s_m);  // else p = 0 on the whole row
     for (int t = tid; t < nch; t += kWalkThreads) {
       const int ch = s_ch[t];
       const int32_t y = s_dt[ch];
       const bool ok = y >= 0 && y < V;
       g_l[t] = ok ? order_key(Logit<DT>::load1(lrow, y)) : neg_inf();
-      g_q[t] = ok ? qrow.at(y) : 0.0f;
+      g_q[t] = ok ? qrow.q_at(y) : 0.0f;
       g_u[t] = __ldg(coins + o + ch);
     }
     __syncthreads();
     int accepted = -1;
     for (int i = 0; i < nch; ++i) {
       if (tid == 0) {
-        const float p = prob_of(g_l[i], cT, mc, invz);
+        const float p = p_finite ? prob_of(g_l[i], cT, mc, invz) : 0.0f;
         const float pc = s_A == 0.0f ? p : fmaxf(0.0f, fmaf(-s_A, g_q[i], p)) / s_cj;
         const float ratio = pc / g_q[i];
-        if (g_q[i] == 0.0f) bump(stats, SPEC_STAT_Q_ZERO);
+        if (g_q[i] == 0.0f) bump(cstats, SPEC_STAT_Q_ZERO);
         s_accept = g_u[i] < ratio;
       }
       __syncthreads();
@@ -434,8 +652,8 @@ __global__ void __launch_bounds__(kWalkThreads)
         break;
       }
       // rejected: mass of the next residual
-      ResidualWeights<DT, decltype(qrow)> w{lrow, qrow, V, cT, mc, invz, s_A + s_cj};
-      const float total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
+      const Weights w{lrow, qrow, V, cT, nb, s_A + s_cj};
+      const float total = pass(w);
       if (tid == 0) {
         if (total > 0.0f && isfinite(total)) {
           s_A = s_A + s_cj;
@@ -443,7 +661,7 @@ __global__ void __launch_bounds__(kWalkThreads)
           s_tiles_ok = 1;
           s_total = total;
         } else {
-          bump(stats, SPEC_STAT_RESIDUAL_FALLBACK);
+          bump(cstats, SPEC_STAT_RESIDUAL_FALLBACK);
           s_tiles_ok = 0;
         }
         ++s_rej;
@@ -465,14 +683,16 @@ __global__ void __launch_bounds__(kWalkThreads)
       continue;
     }
     // no child accepted (or a leaf): draw from the current distribution
-    ResidualWeights<DT, decltype(qrow)> w{lrow, qrow, V, cT, mc, invz, s_A};
+    const Weights w{lrow, qrow, V, cT, nb, s_A};
     float total;
     if (s_tiles_ok) {
-      total = s_total;
+      total = s_total;  // the last pass's tile sums are in buffer par ^ 1
     } else {
-      total = cdf_tile_pass<kWalkThreads>(w, V, red, tile_sum);
+      total = pass(w);
     }
-    const int32_t tok = cdf_search<kWalkThreads>(w, V, __ldg(u_final + b), tile_sum, total, scan_sh, stats);
+    const int32_t tok =
+        cdf_search<kWalkThreads, Weights, kWalkElems>(w, V, __ldg(u_final + b), tile_sums + (par ^ 1) * ntiles, total,
+                                                      scan_sh, cstats);
     if (tid == 0) {
       s_com[s_len++] = tok;
       s_kind = nch > 0 ? SPEC_FINAL_CORRECTION : SPEC_FINAL_BONUS;
@@ -480,6 +700,8 @@ __global__ void __launch_bounds__(kWalkThreads)
     }
     __syncthreads();
   }
+  if (kWalkCluster > 1) cluster_barrier();  // no CTA leaves while another may store into it
+  if (rank != 0) return;
   if (tid == 0) {
     num_committed[b] = s_len;
     accept_length[b] = s_acc;
@@ -576,17 +798,23 @@ int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, Q
                          const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
                          int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                          int32_t* walk_info, int32_t* stats, VerifyWs w, cudaStream_t s) {
+  using Weights = ResidualWeights<DT, typename QSrc::Row>;
   const int64_t rows = static_cast<int64_t>(B) * N;
-  const int64_t ntiles = (V + kWalkThreads * 8 - 1) / (kWalkThreads * 8);
-  const size_t smem = sizeof(float) * (ntiles * (1 + kWalkThreads / 32) + 3 * static_cast<int64_t>(N)) +
+  constexpr int kChunks = Weights::template chunks<kWalkElems>();
+  const int64_t ntiles = (V + kWalkThreads * kWalkElems - 1) / (kWalkThreads * kWalkElems);
+  const size_t ring = sizeof(uint4) * walk_ring_depth(kChunks) * kChunks * kWalkThreads;
+  const int64_t parts =
+      static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, kWalkCluster>(V)) * kWalkThreads;
+  const size_t smem = ring + sizeof(float) * (2 * ntiles + parts + 3 * static_cast<int64_t>(N)) +
                       sizeof(int32_t) * 6 * static_cast<int64_t>(N);
+  if (smem > kMaxDynSmem) return SPEC_ERR_UNSUPPORTED;  // V in the millions
   int e = launch_row_stats<DT, true>(target, V, rows, c, w.amax, w.m, w.z, stats, s);
   if (e != SPEC_OK) return e;
   if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<DT, QSrc>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  sample_walk_kernel<DT, QSrc><<<B, kWalkThreads, smem, s>>>(N, V, c, target, w.m, w.z, qsrc, q_row, dtok, ntok,
+  sample_walk_kernel<DT, QSrc><<<B * kWalkCluster, kWalkThreads, smem, s>>>(N, V, c, target, w.m, w.z, qsrc, q_row, dtok, ntok,
                                                              nsib, coins, u_final, budget, eos, committed,
                                                              num_committed, accept_length, accept_path, next_root,
                                                              walk_info, stats);
