@@ -80,6 +80,23 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Pairs of fp32 lanes (the packed fp32 instructions of sm_100 and later:
+// each lane rounds exactly as the scalar operation).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 splat(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 exp2_2(float2 a) { return make_float2(fast_exp2(a.x), fast_exp2(a.y)); }
+
+// s + (sum over even j of 2^(x_j c - mc), sum over odd j of the same): the
+// two running sums of an online softmax, one per lane (N even).
+template <int N>
+__device__ __forceinline__ float2 exp2_sum_pairs(float2 s, const float* x, float c, float mc) {
+  const float2 c2 = splat(c), nmc2 = splat(-mc);
+#pragma unroll
+  for (int j = 0; j < N; j += 2) s = add2(s, exp2_2(fma2(make_float2(x[j], x[j + 1]), c2, nmc2)));
+  return s;
+}
+
 // Thread-block clusters: this CTA's rank, a barrier over every thread of
 // every CTA of the cluster (release / acquire: shared-memory writes before
 // it, local or remote, are visible after it), and a store into the shared

@@ -26,6 +26,10 @@ namespace {
 #define SPEC_DRAFT_THREADS 128
 #endif
 constexpr int kDraftThreads = SPEC_DRAFT_THREADS;
+#ifndef SPEC_DRAFT_UNROLL
+#define SPEC_DRAFT_UNROLL 4
+#endif
+constexpr int kDraftUnroll = SPEC_DRAFT_UNROLL;  // 16-byte loads in flight per thread
 
 // Running online-softmax partials of one thread: m = max key seen,
 // s = sum 2^((x - m) c).
@@ -138,12 +142,9 @@ struct ArgmaxVisitor {
       bi = static_cast<int>(first) + j0;
     }
     if (m != neg_inf()) {
-      const float mc = m * c;
-#pragma unroll
-      for (int j = 0; j < kv; j += 2) {
-        s0 += fast_exp2(fmaf(x[j], c, -mc));
-        s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
-      }
+      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, m * c);
+      s0 = a.x;
+      s1 = a.y;
     }
   }
   __device__ __forceinline__ void finish() {}
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
   // pass A: online softmax and every thread's best element
   ArgmaxVisitor<DT> st{c};
   st.reset();
-  for_row_raw<DT, 4>(row, V, st, threadIdx.x, kDraftThreads);
+  for_row_raw<DT, kDraftUnroll>(row, V, st, threadIdx.x, kDraftThreads);
   lv[threadIdx.x] = st.m;
   li[threadIdx.x] = st.bi;
   if (threadIdx.x == 0) {

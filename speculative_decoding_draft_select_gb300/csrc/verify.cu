@@ -109,12 +109,9 @@ struct RowStatVisitor {
       bi = static_cast<int>(first) + j0;
     }
     if (STOCH && m != neg_inf()) {
-      const float mc = m * c;
-#pragma unroll
-      for (int j = 0; j < kv; j += 2) {
-        s0 += fast_exp2(fmaf(x[j], c, -mc));
-        s1 += fast_exp2(fmaf(x[j + 1], c, -mc));
-      }
+      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, m * c);
+      s0 = a.x;
+      s1 = a.y;
     }
   }
 };
@@ -134,6 +131,10 @@ struct KeyedSum {
 #define SPEC_STAT_THREADS 256
 #endif
 constexpr int kStatThreads = SPEC_STAT_THREADS;
+#ifndef SPEC_STAT_UNROLL
+#define SPEC_STAT_UNROLL 8
+#endif
+constexpr int kStatUnroll = SPEC_STAT_UNROLL;  // 16-byte loads in flight per thread
 
 // Pass 1: one CTA per target row streams it with 16-byte loads (4 in
 // flight per thread) and reduces it to its argmax and, for sampling, the
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
   const void* row = static_cast<const char*>(logits) + r * V * esz;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX};
-  for_row_raw<DT, 4>(row, V, v, threadIdx.x, kStatThreads);
+  for_row_raw<DT, kStatUnroll>(row, V, v, threadIdx.x, kStatThreads);
   float bv = v.m;
   int bi = v.bi;
   warp_best(bv, bi);
@@ -332,13 +333,6 @@ __device__ __forceinline__ void mask_past(float* x, int64_t v0, int64_t V, float
   for (int j = 0; j < 8; ++j)
     if (v0 + j >= V) x[j] = fill;
 }
-
-// Pairs of fp32 lanes (the packed fp32 instructions of sm_100 and later:
-// each lane rounds exactly as the scalar operation).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 splat(float a) { return make_float2(a, a); }
-__device__ __forceinline__ float2 exp2_2(float2 a) { return make_float2(fast_exp2(a.x), fast_exp2(a.y)); }
 
 struct QRowProbs {
   static constexpr int kEsz = 4;
