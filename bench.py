@@ -165,6 +165,19 @@ def run_ours(args, cfg, mode, rank, world):
 
     stream = torch.cuda.current_stream()
     dom_events = []
+    # timing events inside a captured graph must be event-record nodes
+    # ("external" events); without that, steps run eagerly
+    use_graph = not args.no_graph
+    if use_graph:
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            use_graph = False
+
+    def timing_event():
+        if use_graph:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        return torch.cuda.Event(enable_timing=True)
 
     class Timer:
         """CUDA events around the draft steps' softmax/top-k (or TLI) launches
@@ -174,21 +187,28 @@ def run_ours(args, cfg, mode, rank, world):
         def begin(self, s):
             self.ev = None
             if self.record and s >= 1:
-                self.ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                self.ev[0].record(stream)
+                self.ev = (timing_event(), timing_event())
+                self.ev[0].record(torch.cuda.current_stream())
 
         def end(self, s):
             if self.ev is not None:
-                self.ev[1].record(stream)
+                self.ev[1].record(torch.cuda.current_stream())
                 dom_events.append((self.ev, cfg.B * cfg.topk))
 
     timer = Timer()
+    verify_events = []
 
     def step(record):
         timer.record = record
         pl.run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], draft_u=work["draft_u"],
                      d2t=work.get("d2t"), t2d=work.get("t2d"), timer=timer)
+        if record:
+            ev = (timing_event(), timing_event())
+            ev[0].record(torch.cuda.current_stream())
         pl.run_verify(buf, target, mode, cfg.T, work["coins"], work["u_final"], work.get("budget"), eos)
+        if record:
+            ev[1].record(torch.cuda.current_stream())
+            verify_events.append(ev)
         if compact:
             pl.run_compact(buf, work["seq_lens"], work["req_to_token"], cfg.page_size, kv_pool=kv)
 
@@ -198,6 +218,15 @@ def run_ours(args, cfg, mode, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # one CUDA graph per timed step (each holds its own timing events, so
+    # every step's launch times can be read after the loop); each is
+    # replayed once untimed first
+    graphs = None
+    if use_graph:
+        graphs = [pl.capture_step(lambda: step(True), warm=False) for _ in range(args.steps)]
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     committed = 0
@@ -205,7 +234,10 @@ def run_ours(args, cfg, mode, rank, world):
         t0 = time.perf_counter()
         for i in range(args.steps):
             starts[i].record(stream)
-            step(True)
+            if graphs is not None:
+                graphs[i].replay()
+            else:
+                step(True)
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
@@ -248,6 +280,16 @@ def run_ours(args, cfg, mode, rank, world):
                     "bytes_per_launch": int(dom_bytes), "avg_launch_us": round(dom_avg_ms * 1e3, 2),
                     "traffic": ncu_traffic(kname, cfg.name)}
 
+    # the batched verify (row statistics of every target row + tree walk):
+    # target-logit bytes read / its time
+    verify = None
+    if verify_events:
+        v_ms = statistics.mean(a.elapsed_time(b) for a, b in verify_events)
+        v_bytes = cfg.B * cfg.N * row_bytes
+        v_gbs = v_bytes / (v_ms * 1e-3) / 1e9
+        verify = {"us_per_step": round(v_ms * 1e3, 2), "logit_bytes": int(v_bytes), "achieved": round(v_gbs, 1),
+                  "peak": peak, "unit": "GB/s", "frac": round(v_gbs / peak, 4)}
+
     # e2e: host buffers through the same API, copies inside the timed region
     e2e = run_e2e(args, cfg, mode, work, buf, target, step, compact) if not args.no_e2e else None
 
@@ -261,11 +303,11 @@ def run_ours(args, cfg, mode, rank, world):
         "data": "synthetic (seeded; shapes and value distributions of the workload, no model weights)",
         "config": {"workload": describe(cfg, mode), "B": cfg.B, "topk": cfg.topk, "num_steps": cfg.steps,
                    "N": cfg.N, "V": cfg.V, "mode": mode, "T": cfg.T, "q": q_mode if mode == "sample" else None,
-                   "parallelism": f"replicas x{world}",
+                   "parallelism": f"replicas x{world}", "cuda_graph": graphs is not None,
                    "l2": "inputs larger than L2 (draft + target logits), no flush"},
         "us_per_step_median": round(statistics.median(step_ms) * 1e3, 2),
         "verified_tokens_per_step": committed, "mean_accept_length": round(accept, 3),
-        "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "roofline": roofline, "verify": verify, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "stats": buf.stats.cpu().tolist(),
     }
     return line, work
@@ -371,6 +413,7 @@ def main():
                     help="draft distribution for stochastic verify: logit rows + row stats, or written fp32 rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
+    ap.add_argument("--no-graph", action="store_true", help="launch every kernel eagerly (no CUDA graph)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

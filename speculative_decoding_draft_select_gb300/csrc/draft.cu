@@ -202,11 +202,13 @@ struct CandVisitor {
   }
 };
 
+constexpr int kRescanUnroll = 4;  // loads in flight per thread (8 measured slower)
+
 // The elements owned by the threads listed in owner[0..n_owner) (owner t
 // holds, in the layout of for_row_raw, the scalars t, t + nthreads, ... of
 // the head and tail and the 16-byte vectors t, t + nthreads, ...), visited
 // by the whole block: each block thread takes every nthreads-th (owner,
-// vector) pair, 4 loads in flight.
+// vector) pair, kRescanUnroll loads in flight.
 template <int DT, class F>
 __device__ __forceinline__ void rescan_owners(const void* row, int64_t V, F& f, const int* owner, int n_owner,
                                               int nthreads) {
@@ -221,20 +223,21 @@ __device__ __forceinline__ void rescan_owners(const void* row, int64_t V, F& f, 
     for (int64_t i = tail0 + t; i < V; i += nthreads) f.visit1(Logit<DT>::load1(row, i), i, true);
   }
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
-  const int64_t per = (sp.nvec + nthreads - 1) / nthreads;  // vectors of owner 0
-  const int64_t total = per * n_owner;
-  for (int64_t e0 = 0; e0 < total; e0 += 4 * static_cast<int64_t>(nthreads)) {
-    uint4 v[4];
-    int64_t vi[4];
+  const int nvec = static_cast<int>(sp.nvec);                // V < 2^31
+  const int per = (nvec + nthreads - 1) / nthreads;         // vectors of owner 0
+  const int total = per * n_owner;
+  for (int e0 = 0; e0 < total; e0 += kRescanUnroll * nthreads) {
+    uint4 v[kRescanUnroll];
+    int vi[kRescanUnroll];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t e = e0 + tid + u * static_cast<int64_t>(nthreads);
-      vi[u] = e < total ? owner[e / per] + (e % per) * nthreads : sp.nvec;
-      if (vi[u] < sp.nvec) v[u] = __ldg(vp + vi[u]);
+    for (int u = 0; u < kRescanUnroll; ++u) {
+      const int e = e0 + tid + u * nthreads;
+      vi[u] = e < total ? owner[e / per] + (e % per) * nthreads : nvec;
+      if (vi[u] < nvec) v[u] = __ldg(vp + vi[u]);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (vi[u] < sp.nvec) f.visit_vec(v[u], sp.head + vi[u] * kv, true);
+    for (int u = 0; u < kRescanUnroll; ++u)
+      if (vi[u] < nvec) f.visit_vec(v[u], sp.head + static_cast<int64_t>(vi[u]) * kv, true);
   }
 }
 
@@ -354,6 +357,36 @@ struct ZeroWriter {
   }
 };
 
+// The n best of a row by (key desc, index asc; NaN as -inf), by one warp:
+// each pick is the best element after the previous pick in that order,
+// starting after (+inf, -1), which every element follows (rows with long
+// runs of equal keys, and the fewer-than-k fallback).
+template <int DT>
+__device__ void warp_rank_row(const void* row, int64_t V, int n, float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  float pv = __int_as_float(0x7f800000);
+  int pi = -1;
+  for (int rr = 0; rr < n; ++rr) {
+    float bv = neg_inf();
+    int bi = INT_MAX;
+    for (int64_t v = lane; v < V; v += 32) {
+      const float x = order_key(Logit<DT>::load1(row, v));
+      if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
+        bv = x;
+        bi = static_cast<int>(v);
+      }
+    }
+    warp_best(bv, bi);
+    if (lane == 0) {
+      out_v[rr] = bv;
+      out_i[rr] = bi;
+    }
+    pv = bv;
+    pi = bi;
+    __syncwarp();
+  }
+}
+
 template <int K>
 constexpr size_t draft_smem_bytes() {
   return K == 1 ? 16 : kCandCap * (sizeof(float) + sizeof(int));
@@ -366,21 +399,21 @@ constexpr size_t draft_smem_bytes() {
 // whose best reaches the threshold (about K of them), collecting the
 // elements before or at it; the exact top-K is ranked among them.  All
 // reductions are fixed-order.
-template <int DT, int K>
-__global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
+template <int DT, int K, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  constexpr int kWarps = kDraftThreads / 32;
+  constexpr int kWarps = THREADS / 32;
   extern __shared__ __align__(16) unsigned char dsm[];  // K > 1: candidate buffer
-  __shared__ float lv[kDraftThreads];
-  __shared__ int li[kDraftThreads];
+  __shared__ float lv[THREADS];
+  __shared__ int li[THREADS];
   __shared__ float fv[K];
   __shared__ int fi[K];
   __shared__ float sm[33], ss[33];
-  __shared__ int s_owner[K > 1 ? kDraftThreads : 1];
+  __shared__ int s_owner[K > 1 ? THREADS : 1];
   __shared__ int s_cnt, s_nown, s_ti;
   __shared__ float s_tv;
 
@@ -390,7 +423,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
   // pass A: online softmax and every thread's best element
   ArgmaxVisitor<DT> st{c};
   st.reset();
-  for_row_raw<DT, kDraftUnroll>(row, V, st, threadIdx.x, kDraftThreads);
+  for_row_raw<DT, kDraftUnroll>(row, V, st, threadIdx.x, THREADS);
   lv[threadIdx.x] = st.m;
   li[threadIdx.x] = st.bi;
   if (threadIdx.x == 0) {
@@ -418,11 +451,11 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
     s = tot;
   }
   if constexpr (K == 1) {
-    if (warp == 0) warp_select_k<1>(lv, li, kDraftThreads, fv, fi);
+    if (warp == 0) warp_select_k<1>(lv, li, THREADS, fv, fi);
   } else {
     // threshold: the K-th best of the thread bests (K distinct elements
     // come before or at it), found by ranking every thread best
-    const int rank = rank_among(st.m, st.bi, lv, li, kDraftThreads);
+    const int rank = rank_among(st.m, st.bi, lv, li, THREADS);
     if (rank == K - 1) {
       s_tv = st.m;
       s_ti = st.bi;
@@ -437,12 +470,12 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
     CandVisitor<DT> cand{tv, ti, cv, ci, &s_cnt};
     if (cand.qualifies(st.m, st.bi)) s_owner[atomicAdd(&s_nown, 1)] = threadIdx.x;
     __syncthreads();
-    rescan_owners<DT>(row, V, cand, s_owner, s_nown, kDraftThreads);
+    rescan_owners<DT>(row, V, cand, s_owner, s_nown, THREADS);
     __syncthreads();
     const int n = s_cnt;
     if (n <= kRankCands) {
       // the candidates' pairs are distinct: their ranks place them
-      for (int e = threadIdx.x; e < n; e += kDraftThreads) {
+      for (int e = threadIdx.x; e < n; e += THREADS) {
         const int rk = rank_among(cv[e], ci[e], cv, ci, n);
         if (rk < K) {
           fv[rk] = cv[e];
@@ -454,59 +487,16 @@ __global__ void __launch_bounds__(kDraftThreads, 1024 / kDraftThreads)
         warp_select_k<K>(cv, ci, n, fv, fi);
       } else {
         // more candidates than the buffer holds (a long run of equal
-        // keys): rank the whole row, each pick the best element after the
-        // previous pick in the order
-        float pv = neg_inf();
-        int pi = -1;
-        for (int rr = 0; rr < K; ++rr) {
-          float bv = neg_inf();
-          int bi = INT_MAX;
-          for (int64_t v = lane; v < V; v += 32) {
-            const float x = order_key(Logit<DT>::load1(row, v));
-            if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
-              bv = x;
-              bi = static_cast<int>(v);
-            }
-          }
-          warp_best(bv, bi);
-          if (lane == 0) {
-            fv[rr] = bv;
-            fi[rr] = bi;
-          }
-          pv = bv;
-          pi = bi;
-          __syncwarp();
-        }
+        // keys): rank the whole row
+        warp_rank_row<DT>(row, V, K, fv, fi);
       }
     }
     __syncthreads();
   }
   if (warp == 0) {
     __syncwarp();
-    if (fi[k - 1] == INT_MAX && k <= V) {
-      // fewer than k non-NaN logits: rank the row again with NaN as -inf
-      float pv = neg_inf();
-      int pi = -1;
-      for (int rr = 0; rr < k; ++rr) {
-        float bv = neg_inf();
-        int bi = INT_MAX;
-        for (int64_t v = lane; v < V; v += 32) {
-          const float x = order_key(Logit<DT>::load1(row, v));
-          if (before(pv, pi, x, static_cast<int>(v)) && before(x, static_cast<int>(v), bv, bi)) {
-            bv = x;
-            bi = static_cast<int>(v);
-          }
-        }
-        warp_best(bv, bi);
-        if (lane == 0) {
-          fv[rr] = bv;
-          fi[rr] = bi;
-        }
-        pv = bv;
-        pi = bi;
-        __syncwarp();
-      }
-    }
+    // fewer than k non-NaN logits: rank the row again with NaN as -inf
+    if (fi[k - 1] == INT_MAX && k <= V) warp_rank_row<DT>(row, V, k, fv, fi);
   }
   __syncthreads();
 
@@ -614,17 +604,31 @@ __global__ void __launch_bounds__(kSampleThreads)
   sample_row(w, V, __ldg(u + r), red, tile_sum, scan_sh, stats, out_token + r, op);
 }
 
-template <int DT, int K>
-int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
+template <int DT, int K, int THREADS>
+int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
+                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
   constexpr size_t smem = draft_smem_bytes<K>();
-  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K>,
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K, THREADS>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  softmax_topk_kernel<DT, K><<<static_cast<unsigned>(R), kDraftThreads, smem, s>>>(logits, V, c, k, topk_p,
-                                                                                   topk_idx, probs, row_stats, stats);
+  softmax_topk_kernel<DT, K, THREADS><<<static_cast<unsigned>(R), THREADS, smem, s>>>(
+      logits, V, c, k, topk_p, topk_idx, probs, row_stats, stats);
   return launch_status();
+}
+
+// One CTA per row.  With few rows (at most two per SM of a 152-SM GB300)
+// a row gets 512 threads, so that each SM still keeps enough loads in
+// flight; otherwise kDraftThreads.
+constexpr int64_t kFewRows = 2 * 152;
+
+template <int DT, int K>
+int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
+                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
+  if (R <= kFewRows)
+    return launch_softmax_topk_t<DT, K, 512>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+  return launch_softmax_topk_t<DT, K, kDraftThreads>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats,
+                                                     s);
 }
 
 template <int DT>

@@ -17,7 +17,9 @@ normaliser) the draft kernel records (q_mode "logits": no q is written; the
 q values are bit-identical).  Compaction: spec_compact_slots.
 
 All buffers are allocated once in ``StepBuffers``; a step only enqueues
-kernels on the current stream.
+kernels on the current stream, so a whole step can be captured once in a
+CUDA graph (``capture_step``) and replayed: the same kernels, without the
+per-launch host cost and the gaps between launches.
 """
 from __future__ import annotations
 
@@ -160,6 +162,24 @@ def run_compact(buf: StepBuffers, seq_lens, req_to_token, page_size, kv_pool=Non
     v = buf.verify_out
     return spec_compact_slots(seq_lens, v["accept_path"], v["accept_length"], req_to_token, page_size,
                               kv_pool=kv_pool, out=buf.compact_out, stats=buf.stats)
+
+
+def capture_step(fn, warm=True):
+    """Capture the launches ``fn()`` enqueues (one step on preallocated
+    buffers) in a CUDA graph; ``graph.replay()`` re-runs them on the same
+    buffers.  With ``warm``, ``fn`` first runs once eagerly on a side stream
+    so that every kernel's attributes are set before the capture (a caller
+    that has already run the step may skip it)."""
+    if warm:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    return graph
 
 
 def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> int:

@@ -70,6 +70,56 @@ def test_softmax_topk_parity(R, V, k, dtype, T):
     np.testing.assert_allclose(probs.cpu().numpy(), oprobs, rtol=0, atol=PROB_TOL)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_softmax_topk_row_edges(dtype):
+    """Rows with equal maxima far apart (lower index first), a long NaN run,
+    fewer than k finite keys, a +inf element, and ties at the end of the
+    row, against the oracle; topk_p does not depend on whether the
+    probabilities are written."""
+    rng = np.random.default_rng(17)
+    R, V, k, run = 6, 40000, 8, 10048
+    x = make_logits(rng, R, V, torch.float32).numpy()
+    top = x.max() + 2
+    x[0, [25000, 10, 31000, 9]] = [top, top, top - 1, top - 1]
+    x[1, run:2 * run] = np.nan
+    x[1, 5] = np.nan
+    x[2, :] = -np.inf
+    x[2, [3, 20000, 39999]] = [1.0, 2.0, 1.0]
+    x[3, 12345] = np.inf
+    x[4, [run - 1, run, 2 * run - 1, 2 * run]] = [top, top, top - 0.5, top - 0.5]
+    x[5, V - 8:] = top
+    xt = torch.from_numpy(x).to(dtype)
+    stats = sd.new_stats()
+    tp, ti, pr = sd.spec_softmax_topk(dev(xt), 0.7, k, want_probs=True, stats=stats)
+    rs = torch.empty((R, 2), device="cuda")
+    tp2, ti2, _ = sd.spec_softmax_topk(dev(xt), 0.7, k, row_stats=rs)
+    torch.cuda.synchronize()
+    op, oi, oprobs, _ = oracle.softmax_topk(np_logits(xt), 0.7, k, want_probs=True)
+    np.testing.assert_array_equal(ti.cpu().numpy(), oi)
+    np.testing.assert_array_equal(ti2.cpu().numpy(), oi)
+    np.testing.assert_allclose(tp.cpu().numpy(), op, rtol=0, atol=PROB_TOL)
+    assert torch.equal(tp, tp2)
+    np.testing.assert_allclose(pr.cpu().numpy(), oprobs, rtol=0, atol=PROB_TOL)
+    assert int(stats[sd.STATS["nonfinite_row"]]) == 1
+    assert not torch.isfinite(rs[3, 0])
+
+
+@pytest.mark.parametrize("k", [8, 32])
+def test_softmax_topk_long_equal_runs(k):
+    """More equal keys than the candidate buffer holds (the whole-row rank
+    fallback) and rows with fewer than k non-NaN keys."""
+    R, V = 3, 5000
+    x = torch.zeros((R, V))
+    x[1, ::3] = float("nan")
+    x[2, :] = float("nan")
+    x[2, [7, 4000]] = 1.0
+    tp, ti, _ = sd.spec_softmax_topk(dev(x), 1.0, k)
+    torch.cuda.synchronize()
+    op, oi, _, _ = oracle.softmax_topk(np_logits(x), 1.0, k)
+    np.testing.assert_array_equal(ti.cpu().numpy(), oi)
+    np.testing.assert_allclose(tp.cpu().numpy(), op, rtol=0, atol=PROB_TOL)
+
+
 def test_softmax_topk_nonfinite_rows_flagged():
     x = torch.full((3, 50), float("-inf"))
     x[1, 7] = float("inf")
@@ -450,3 +500,61 @@ def test_greedy_spec_decoding_on_gpu_equals_argmax_decoding():
         nc = int(v["num_committed"][0])
         out += v["committed"][0, :nc].cpu().tolist()
     assert out[:len(ref)] == ref
+
+
+@pytest.mark.parametrize("name,mode,q_mode", [("c3", "sample", "logits"), ("c5", "greedy", "probs"),
+                                              ("c4", "sample", "probs")])
+def test_captured_step_replays_the_eager_step(name, mode, q_mode):
+    """A whole step (draft steps, tree build, verify, compaction) captured in
+    a CUDA graph and replayed writes exactly what the eager step wrote."""
+    from speculative_decoding_draft_select_gb300.pipeline import capture_step, run_compact
+    cfg = small(name, **SMALL[name])
+    if name == "c3":
+        cfg = cfg.scaled(page_size=16, bytes_per_slot=64)
+    work = generate(cfg, "cuda")
+    buf = StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, "cuda", want_q=(mode == "sample"),
+                      sampled=(cfg.kind == "chain" and mode == "sample"), V_t=cfg.V_t or None,
+                      page_size=cfg.page_size, q_mode=q_mode)
+    tree = run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"],
+                     draft_u=work["draft_u"], d2t=work.get("d2t"), t2d=work.get("t2d"))
+    target = assemble_target(work, tree["q_row"]).contiguous()
+    r2t0 = work["req_to_token"].clone() if cfg.page_size else None
+    kv0 = work["kv_pool"].clone() if cfg.page_size else None
+
+    def step():
+        run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], draft_u=work["draft_u"],
+                  d2t=work.get("d2t"), t2d=work.get("t2d"))
+        run_verify(buf, target, mode, cfg.T, work["coins"], work["u_final"], work.get("budget"),
+                   int(work["eos_id"]))
+        if cfg.page_size:
+            run_compact(buf, work["seq_lens"], work["req_to_token"], cfg.page_size, kv_pool=work["kv_pool"])
+
+    def outputs():
+        o = {f"tree.{k}": v.clone() for k, v in buf.tree.items()}
+        o.update({f"verify.{k}": v.clone() for k, v in buf.verify_out.items()})
+        if cfg.page_size:
+            o.update({f"compact.{k}": v.clone() for k, v in buf.compact_out.items()})
+            o["req_to_token"] = work["req_to_token"].clone()
+            o["kv_pool"] = work["kv_pool"].clone()
+        return o
+
+    def reset():
+        for d in (buf.tree, buf.verify_out, buf.compact_out or {}):
+            for v in d.values():
+                v.fill_(-7)
+        if cfg.page_size:  # compaction edits the slot table and pool in place
+            work["req_to_token"].copy_(r2t0)
+            work["kv_pool"].copy_(kv0)
+
+    reset()
+    step()
+    torch.cuda.synchronize()
+    eager = outputs()
+    reset()
+    graph = capture_step(step)
+    reset()
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = outputs()
+    for k in eager:
+        assert torch.equal(eager[k], replayed[k]), k
