@@ -386,4 +386,30 @@ __device__ __forceinline__ void for_row_raw(const void* row, int64_t V, F& f, in
   }
 }
 
+// for_row_raw for rows of fewer than 2^31 elements, without per-vector
+// bounds tests: full rounds of UNROLL 16-byte vectors, then the thread's
+// remaining vectors one by one.  Each thread still sees its elements (the
+// same ones as in for_row_raw) in increasing index order; ok is always
+// true.  Not warp-uniform (visitors must not use warp collectives).
+template <int DT, int UNROLL, class F>
+__device__ __forceinline__ void for_row_fast(const void* row, int64_t V64, F& f, int tid, int nthreads) {
+  constexpr int kv = Logit<DT>::kVec;
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  const RowSpan sp = row_span<DT>(row, V64);
+  const int V = static_cast<int>(V64), head = static_cast<int>(sp.head), nvec = static_cast<int>(sp.nvec);
+  if (tid < head) f.visit1(Logit<DT>::load1(row, tid), tid, true);  // head < kv <= nthreads
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+  int i = tid;
+  for (; i + (UNROLL - 1) * nthreads < nvec; i += UNROLL * nthreads) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) v[u] = ld_stream(vp + i + u * nthreads);
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) f.visit_vec(v[u], head + (i + u * nthreads) * kv, true);
+  }
+  for (; i < nvec; i += nthreads) f.visit_vec(ld_stream(vp + i), head + i * kv, true);
+  const int t = head + nvec * kv + tid;
+  if (t < V) f.visit1(Logit<DT>::load1(row, t), t, true);  // tail < kv <= nthreads
+}
+
 }  // namespace specdec

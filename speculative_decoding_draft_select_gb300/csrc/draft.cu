@@ -93,14 +93,18 @@ struct TopK {
 };
 
 // Pass A of a draft row: each thread's online softmax and its best element
-// (value desc, index asc; NaN skipped).  For K == 1 the block's best is the
+// (key desc, index asc; NaN as -inf).  A thread visits its elements in
+// increasing index order, so only a strictly larger key replaces its best;
+// a thread whose keys are all -inf ends with bi = INT_MAX and takes its
+// first element afterwards (own_first).  For K == 1 the block's best is the
 // top-1; for K > 1 the thread bests give the pass-B threshold.
 template <int DT>
 struct ArgmaxVisitor {
-  float c, m, s0, s1;
+  float c, m, mc, s0, s1;  // mc = m c
   int bi;
   __device__ __forceinline__ void reset() {
     m = neg_inf();
+    mc = 0.0f;
     s0 = s1 = 0.0f;
     bi = INT_MAX;
   }
@@ -113,15 +117,16 @@ struct ArgmaxVisitor {
       s1 *= f;
     }
     m = nm;
+    mc = nm * c;
   }
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
     if (!ok) return;
     const float xk = order_key(x);
-    if (before(xk, static_cast<int>(idx), m, bi)) {
-      if (xk > m) rescale(xk);
+    if (xk > m) {
+      rescale(xk);
       bi = static_cast<int>(idx);
     }
-    if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
+    if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
   }
   __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool ok) {
     constexpr int kv = Logit<DT>::kVec;
@@ -133,21 +138,33 @@ struct ArgmaxVisitor {
     } else {
       vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
     }
-    if (ok && before(vmax, static_cast<int>(first), m, bi)) {
+    if (ok && vmax > m) {
       int j0 = 0;
 #pragma unroll
       for (int j = kv - 1; j >= 0; --j)
         if (x[j] == vmax) j0 = j;
-      if (vmax > m) rescale(vmax);
+      rescale(vmax);
       bi = static_cast<int>(first) + j0;
     }
     if (m != neg_inf()) {
-      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, m * c);
+      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
       s0 = a.x;
       s1 = a.y;
     }
   }
-  __device__ __forceinline__ void finish() {}
+  // the thread's first element in the visiting order, if its best is unset
+  __device__ __forceinline__ void own_first(const void* row, int64_t V, int tid) {
+    if (bi != INT_MAX) return;
+    constexpr int kv = Logit<DT>::kVec;
+    const RowSpan sp = row_span<DT>(row, V);
+    if (tid < sp.head) {
+      bi = tid;
+    } else if (tid < sp.nvec) {
+      bi = static_cast<int>(sp.head + static_cast<int64_t>(tid) * kv);
+    } else if (sp.head + sp.nvec * kv + tid < V) {
+      bi = static_cast<int>(sp.head + sp.nvec * kv + tid);
+    }
+  }
 };
 
 // Pass B of a draft row (K > 1): collect every element that comes before or
@@ -223,21 +240,22 @@ __device__ __forceinline__ void rescan_owners(const void* row, int64_t V, F& f, 
     for (int64_t i = tail0 + t; i < V; i += nthreads) f.visit1(Logit<DT>::load1(row, i), i, true);
   }
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
-  const int nvec = static_cast<int>(sp.nvec);                // V < 2^31
-  const int per = (nvec + nthreads - 1) / nthreads;         // vectors of owner 0
-  const int total = per * n_owner;
-  for (int e0 = 0; e0 < total; e0 += kRescanUnroll * nthreads) {
-    uint4 v[kRescanUnroll];
-    int vi[kRescanUnroll];
+  const int nvec = static_cast<int>(sp.nvec);  // V < 2^31
+  // kRescanUnroll owners at a time; thread tid takes vector j of each, j =
+  // tid, tid + nthreads, ... (owner t's j-th vector is t + j nthreads)
+  for (int o0 = 0; o0 < n_owner; o0 += kRescanUnroll) {
+    for (int j = tid; j * nthreads < nvec; j += nthreads) {
+      uint4 v[kRescanUnroll];
+      int vi[kRescanUnroll];
 #pragma unroll
-    for (int u = 0; u < kRescanUnroll; ++u) {
-      const int e = e0 + tid + u * nthreads;
-      vi[u] = e < total ? owner[e / per] + (e % per) * nthreads : nvec;
-      if (vi[u] < nvec) v[u] = __ldg(vp + vi[u]);
+      for (int u = 0; u < kRescanUnroll; ++u) {
+        vi[u] = o0 + u < n_owner ? owner[o0 + u] + j * nthreads : nvec;
+        if (vi[u] < nvec) v[u] = __ldg(vp + vi[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kRescanUnroll; ++u)
+        if (vi[u] < nvec) f.visit_vec(v[u], sp.head + static_cast<int64_t>(vi[u]) * kv, true);
     }
-#pragma unroll
-    for (int u = 0; u < kRescanUnroll; ++u)
-      if (vi[u] < nvec) f.visit_vec(v[u], sp.head + static_cast<int64_t>(vi[u]) * kv, true);
   }
 }
 
@@ -423,7 +441,8 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   // pass A: online softmax and every thread's best element
   ArgmaxVisitor<DT> st{c};
   st.reset();
-  for_row_raw<DT, kDraftUnroll>(row, V, st, threadIdx.x, THREADS);
+  for_row_fast<DT, kDraftUnroll>(row, V, st, threadIdx.x, THREADS);
+  st.own_first(row, V, threadIdx.x);
   lv[threadIdx.x] = st.m;
   li[threadIdx.x] = st.bi;
   if (threadIdx.x == 0) {
@@ -454,11 +473,13 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     if (warp == 0) warp_select_k<1>(lv, li, THREADS, fv, fi);
   } else {
     // threshold: the K-th best of the thread bests (K distinct elements
-    // come before or at it), found by ranking every thread best
-    const int rank = rank_among(st.m, st.bi, lv, li, THREADS);
-    if (rank == K - 1) {
-      s_tv = st.m;
-      s_ti = st.bi;
+    // come before or at it), by K rounds of a warp argmax in warp 0
+    if (warp == 0) {
+      warp_select_k<K>(lv, li, THREADS, fv, fi);
+      if (lane == 0) {
+        s_tv = fv[K - 1];
+        s_ti = fi[K - 1];
+      }
     }
     __syncthreads();
     const float tv = s_tv;
