@@ -387,10 +387,11 @@ __device__ __forceinline__ void for_row_raw(const void* row, int64_t V, F& f, in
 }
 
 // for_row_raw for rows of fewer than 2^31 elements, without per-vector
-// bounds tests: full rounds of UNROLL 16-byte vectors, then the thread's
-// remaining vectors one by one.  Each thread still sees its elements (the
-// same ones as in for_row_raw) in increasing index order; ok is always
-// true.  Not warp-uniform (visitors must not use warp collectives).
+// bounds tests in the full rounds of UNROLL 16-byte vectors; the thread's
+// remaining vectors (fewer than UNROLL) are loaded together in one last
+// round.  Each thread still sees its elements (the same ones as in
+// for_row_raw) in increasing index order; ok is always true.  Not
+// warp-uniform (visitors must not use warp collectives).
 template <int DT, int UNROLL, class F>
 __device__ __forceinline__ void for_row_fast(const void* row, int64_t V64, F& f, int tid, int nthreads) {
   constexpr int kv = Logit<DT>::kVec;
@@ -407,7 +408,15 @@ __device__ __forceinline__ void for_row_fast(const void* row, int64_t V64, F& f,
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) f.visit_vec(v[u], head + (i + u * nthreads) * kv, true);
   }
-  for (; i < nvec; i += nthreads) f.visit_vec(ld_stream(vp + i), head + i * kv, true);
+  if (i < nvec) {
+    uint4 v[UNROLL - 1 > 0 ? UNROLL - 1 : 1];
+#pragma unroll
+    for (int u = 0; u < UNROLL - 1; ++u)
+      if (i + u * nthreads < nvec) v[u] = ld_stream(vp + i + u * nthreads);
+#pragma unroll
+    for (int u = 0; u < UNROLL - 1; ++u)
+      if (i + u * nthreads < nvec) f.visit_vec(v[u], head + (i + u * nthreads) * kv, true);
+  }
   const int t = head + nvec * kv + tid;
   if (t < V) f.visit1(Logit<DT>::load1(row, t), t, true);  // tail < kv <= nthreads
 }

@@ -69,6 +69,7 @@ template <int DT, bool STOCH>
 struct RowStatVisitor {
   float c, m, s0, s1;
   int bi;
+  float mc;  // m c
   __device__ __forceinline__ void rescale(float nm) {
     if (STOCH) {
       if (m == neg_inf()) {
@@ -78,6 +79,7 @@ struct RowStatVisitor {
         s0 *= f;
         s1 *= f;
       }
+      mc = nm * c;
     }
     m = nm;
   }
@@ -88,7 +90,7 @@ struct RowStatVisitor {
       rescale(xk);
       bi = static_cast<int>(idx);
     }
-    if (STOCH && m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -m * c));
+    if (STOCH && m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
   }
   __device__ __forceinline__ void visit_vec(const uint4& w, int64_t first, bool) {
     constexpr int kv = Logit<DT>::kVec;
@@ -109,7 +111,7 @@ struct RowStatVisitor {
       bi = static_cast<int>(first) + j0;
     }
     if (STOCH && m != neg_inf()) {
-      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, m * c);
+      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
       s0 = a.x;
       s1 = a.y;
     }
@@ -153,8 +155,8 @@ __global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX};
-  for_row_raw<DT, kStatUnroll>(row, V, v, threadIdx.x, kStatThreads);
+  RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX, 0.0f};
+  for_row_fast<DT, kStatUnroll>(row, V, v, threadIdx.x, kStatThreads);
   float bv = v.m;
   int bi = v.bi;
   warp_best(bv, bi);
