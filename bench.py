@@ -139,6 +139,23 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 
+def rank_config(cfg, rank, world):
+    """Weak scaling: with several ranks every rank verifies its own batch of
+    the same shape (its own seed)."""
+    return cfg.scaled(seed=cfg.seed + 7919 * rank) if world > 1 else cfg
+
+
+def reduce_over_ranks(total_ms, tokens, world, device):
+    """(the longest rank's timed span, the verified tokens of all ranks)."""
+    if world == 1:
+        return float(total_ms), float(tokens)
+    span = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    tok = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(span, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(tok, op=torch.distributed.ReduceOp.SUM)
+    return float(span.item()), float(tok.item())
+
+
 def run_ours(args, cfg, mode, rank, world):
     import speculative_decoding_draft_select_gb300 as sd
     from speculative_decoding_draft_select_gb300 import pipeline as pl
@@ -147,8 +164,7 @@ def run_ours(args, cfg, mode, rank, world):
     build()
     sd.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
-    if world > 1:  # weak scaling: every rank verifies its own batch
-        cfg = cfg.scaled(seed=cfg.seed + 7919 * rank)
+    cfg = rank_config(cfg, rank, world)
     work = generate(cfg, dev)
     compact = bool(cfg.page_size)
     sampled = cfg.kind == "chain" and mode == "sample"
@@ -251,15 +267,7 @@ def run_ours(args, cfg, mode, rank, world):
     dom_ms = [ev[0].elapsed_time(ev[1]) for ev, _ in dom_events]
     dom_rows = [r for _, r in dom_events]
 
-    # max over ranks
-    t_total = torch.tensor([total_ms, committed * args.steps], dtype=torch.float64, device=dev)
-    if world > 1:
-        mx = t_total.clone()
-        torch.distributed.all_reduce(mx[:1], op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(t_total[1:], op=torch.distributed.ReduceOp.SUM)
-        t_total[0] = mx[0]
-    total_ms_max = float(t_total[0].item())
-    tokens_all = float(t_total[1].item())
+    total_ms_max, tokens_all = reduce_over_ranks(total_ms, committed * args.steps, world, dev)
     value = tokens_all / (total_ms_max / 1e3)
 
     # dominant kernel: the draft-step softmax/top-k (or TLI constrain) launches
