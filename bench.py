@@ -293,7 +293,7 @@ def run_ours(args, cfg, mode, rank, world):
     verify = None
     if verify_events:
         v_ms = statistics.mean(a.elapsed_time(b) for a, b in verify_events)
-        v_bytes = cfg.B * cfg.N * row_bytes
+        v_bytes = cfg.B * cfg.N * (cfg.V_t or cfg.V) * (2 if cfg.dtype == torch.bfloat16 else 4)  # target rows
         v_gbs = v_bytes / (v_ms * 1e-3) / 1e9
         verify = {"us_per_step": round(v_ms * 1e3, 2), "logit_bytes": int(v_bytes), "achieved": round(v_gbs, 1),
                   "peak": peak, "unit": "GB/s", "frac": round(v_gbs / peak, 4)}
