@@ -113,11 +113,14 @@ int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float
  *   u              [R] fp32 uniforms in [0,1).
  *   out_token      [R] int32 out.
  *   out_prob_or_null [R] fp32 out: the drawn token's normalised weight.
+ *   row_stats_or_null [R, 2] fp32 in (logits only, optional): each row's
+ *                  maximum as spec_softmax_topk recorded it; the row is
+ *                  then read once instead of twice.  The result is the same.
  * If rounding leaves no crossing, the last index with positive weight is
  * taken (SPEC_STAT_CDF_FALLBACK). */
 int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_null, int64_t R,
                 int64_t V, float T, const float* u, int32_t* out_token, float* out_prob_or_null,
-                int32_t* stats_or_null, spec_stream_t stream);
+                const float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream);
 
 /* Candidate-pool size P = 1 + k + (num_steps - 1) * k * k. */
 int64_t spec_tree_pool_size(int k, int num_steps);

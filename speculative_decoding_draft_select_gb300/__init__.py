@@ -42,7 +42,7 @@ _SZ = ctypes.c_size_t
 
 _SIGS = {
     "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P]),
-    "spec_sample": (_I, [_P, _I, _P, _I64, _I64, _F, _P, _P, _P, _P, _P]),
+    "spec_sample": (_I, [_P, _I, _P, _I64, _I64, _F, _P, _P, _P, _P, _P, _P]),
     "spec_tree_pool_size": (_I64, [_I, _I]),
     "spec_tree_expand": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_build_tree": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -152,8 +152,10 @@ def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want
     return topk_p, topk_idx, probs
 
 
-def spec_sample(u, logits=None, probs=None, T=1.0, out_token=None, out_prob=None, stats=None):
-    """One token per row by inverse CDF with uniforms u [R]."""
+def spec_sample(u, logits=None, probs=None, T=1.0, out_token=None, out_prob=None, stats=None, row_stats=None):
+    """One token per row by inverse CDF with uniforms u [R].  row_stats
+    [R, 2] (logits only, optional): the rows' (max, normaliser) from
+    spec_softmax_topk, so that each row is read once."""
     src = probs if probs is not None else logits
     _dev(src, name="probs/logits")
     _dev(u, torch.float32, "u")
@@ -162,13 +164,14 @@ def spec_sample(u, logits=None, probs=None, T=1.0, out_token=None, out_prob=None
     out_token = _out(out_token, (R,), torch.int32, src, "out_token")
     out_prob = _out(out_prob, (R,), torch.float32, src, "out_prob")
     _dev(stats, torch.int32, "stats")
+    _dev(row_stats, torch.float32, "row_stats")
     if probs is not None:
         _dev(probs, torch.float32, "probs")
         code = F32
     else:
         code = _logit_code(logits)
     _call("spec_sample", _ptr(logits if probs is None else None), code, _ptr(probs), R, V, float(T), _ptr(u),
-          _ptr(out_token), _ptr(out_prob), _ptr(stats), _stream())
+          _ptr(out_token), _ptr(out_prob), _ptr(row_stats if probs is None else None), _ptr(stats), _stream())
     return out_token, out_prob
 
 

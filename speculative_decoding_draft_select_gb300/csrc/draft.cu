@@ -593,7 +593,7 @@ template <int DT, bool FROM_PROBS>
 __global__ void __launch_bounds__(kSampleThreads)
     sample_kernel(const void* __restrict__ logits, const float* __restrict__ probs, int64_t V,
                   float c, const float* __restrict__ u, int32_t* __restrict__ out_token,
-                  float* __restrict__ out_prob, int32_t* __restrict__ stats) {
+                  float* __restrict__ out_prob, const float* __restrict__ row_stats, int32_t* __restrict__ stats) {
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   extern __shared__ float dyn[];
   __shared__ float scan_sh[33];
@@ -609,10 +609,16 @@ __global__ void __launch_bounds__(kSampleThreads)
     return;
   }
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  StatsVisitor st{{c, neg_inf(), 0.0f}};
-  for_row<DT, 4>(row, V, st);
-  float m = st.sp.m, s = st.sp.s;
-  block_ms<0>(m, s, c, sm, ss);
+  float m;
+  if (row_stats != nullptr) {
+    m = __ldg(row_stats + 2 * r);  // the row's max from the caller's softmax pass
+  } else {
+    StatsVisitor st{{c, neg_inf(), 0.0f}};
+    for_row<DT, 4>(row, V, st);
+    float s = st.sp.s;
+    m = st.sp.m;
+    block_ms<0>(m, s, c, sm, ss);
+  }
   if (!isfinite(m)) {
     if (threadIdx.x == 0) {
       bump(stats, SPEC_STAT_NONFINITE_ROW);
@@ -687,7 +693,7 @@ extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64
 
 extern "C" int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_null, int64_t R,
                            int64_t V, float T, const float* u, int32_t* out_token, float* out_prob_or_null,
-                           int32_t* stats_or_null, spec_stream_t stream) {
+                           const float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream) {
   if (R < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (R > 0 && (u == nullptr || out_token == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (R > 0 && logits_or_null == nullptr && probs_or_null == nullptr) return SPEC_ERR_INVALID_ARG;
@@ -706,12 +712,14 @@ extern "C" int spec_sample(const void* logits_or_null, int dtype, const float* p
   }
   if (probs_or_null)
     sample_kernel<SPEC_F32, true><<<grid, kSampleThreads, smem, s>>>(nullptr, probs_or_null, V, c, u, out_token,
-                                                                     out_prob_or_null, stats_or_null);
+                                                                     out_prob_or_null, nullptr, stats_or_null);
   else if (dtype == SPEC_BF16)
     sample_kernel<SPEC_BF16, false><<<grid, kSampleThreads, smem, s>>>(logits_or_null, nullptr, V, c, u, out_token,
-                                                                       out_prob_or_null, stats_or_null);
+                                                                       out_prob_or_null, row_stats_or_null,
+                                                                       stats_or_null);
   else
     sample_kernel<SPEC_F32, false><<<grid, kSampleThreads, smem, s>>>(logits_or_null, nullptr, V, c, u, out_token,
-                                                                      out_prob_or_null, stats_or_null);
+                                                                      out_prob_or_null, row_stats_or_null,
+                                                                      stats_or_null);
   return launch_status();
 }

@@ -10,11 +10,12 @@
 // the constrained draft distribution written in target-vocabulary order.
 //
 // tli_constrain_kernel: one CTA per draft row.  Pass 1 streams the row with
-// 16-byte loads, skipping ids outside the intersection (d2t[v] < 0, read
-// through the read-only cache: the table is shared by every row and stays in
-// L2), and keeps the masked top-1 and online-softmax partials.  Pass 2
-// (optional) writes q in target order: q_t[t] = p(t2d[t]) or 0, with
-// coalesced 16-byte stores and gathers from the draft row (L2-resident).
+// 16-byte loads together with the matching 16-byte loads of d2t (the table
+// is shared by every row and stays in L2), masks ids outside the
+// intersection (d2t[v] < 0) to -inf and keeps the masked top-1 and
+// online-softmax partials.  Pass 2 (optional) writes q in target order:
+// q_t[t] = p(t2d[t]) or 0, with coalesced 16-byte stores and gathers from
+// the draft row (L2-resident), 8 in flight per thread.
 #include <climits>
 
 #include "common.cuh"
@@ -24,26 +25,84 @@ namespace {
 
 constexpr int kTliThreads = 512;
 
+// Pass 1 of a draft row: the online softmax and the best element over the
+// intersection only (ids with d2t < 0 count as -inf, as do NaN logits).
+// Each thread visits its elements in increasing index order, so only a
+// strictly larger key replaces its best.  The mask comes with the logits:
+// two 16-byte loads of d2t per 8 bf16 logits (one per 4 fp32 ones).
+template <int DT>
 struct MaskedVisitor {
   const int32_t* d2t;
-  float c, m, s;
+  float c, m, mc, s0, s1;
   int bi;
-  template <int N>
-  __device__ __forceinline__ void visit(const float* xin, int64_t first) {
+  __device__ __forceinline__ void rescale(float nm) {
+    if (m == neg_inf()) {
+      s0 = s1 = 0.0f;
+    } else {
+      const float f = fast_exp2((m - nm) * c);
+      s0 *= f;
+      s1 *= f;
+    }
+    m = nm;
+    mc = nm * c;
+  }
+  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
+    if (!ok || __ldg(d2t + idx) < 0) return;
+    const float xk = order_key(x);
+    if (xk > m) {
+      rescale(xk);
+      bi = static_cast<int>(idx);
+    }
+    if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
+  }
+  __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool) {
+    constexpr int kv = Logit<DT>::kVec;
+    float x[kv];
+    unpack<DT>(raw, x);
+    int d[kv];
+    if ((reinterpret_cast<uintptr_t>(d2t + first) & 15) == 0) {
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-      if (__ldg(d2t + first + j) < 0) continue;
-      const float x = order_key(xin[j]);
-      const int idx = static_cast<int>(first) + j;
-      if (before(x, idx, m, bi)) {
-        if (x > m) s = (m == neg_inf()) ? 0.0f : s * fast_exp2((m - x) * c);
-        m = x;
-        bi = idx;
+      for (int h = 0; h < kv / 4; ++h) {
+        const int4 t = __ldg(reinterpret_cast<const int4*>(d2t + first) + h);
+        d[4 * h] = t.x;
+        d[4 * h + 1] = t.y;
+        d[4 * h + 2] = t.z;
+        d[4 * h + 3] = t.w;
       }
-      if (m != neg_inf()) s += fast_exp2(fmaf(x, c, -m * c));
+    } else {
+#pragma unroll
+      for (int j = 0; j < kv; ++j) d[j] = __ldg(d2t + first + j);
+    }
+    float vmax = neg_inf();
+#pragma unroll
+    for (int j = 0; j < kv; ++j) {
+      x[j] = d[j] >= 0 ? order_key(x[j]) : neg_inf();
+      vmax = fmaxf(vmax, x[j]);
+    }
+    if (vmax > m) {
+      int j0 = 0;
+#pragma unroll
+      for (int j = kv - 1; j >= 0; --j)
+        if (x[j] == vmax) j0 = j;
+      rescale(vmax);
+      bi = static_cast<int>(first) + j0;
+    }
+    if (m != neg_inf()) {
+      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
+      s0 = a.x;
+      s1 = a.y;
     }
   }
 };
+
+// q_t = min(2^((key - m) c) / Z, 1) of draft logit d of the row, or 0 off
+// the intersection (d < 0) or when the row has no intersection logit.
+template <int DT>
+__device__ __forceinline__ float q_of(const void* row, int32_t d, int64_t Vd, bool ok, float c, float mc,
+                                      float invz) {
+  return (ok && d >= 0 && d < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d)), c, -mc)) * invz, 1.0f)
+                                  : 0.0f;
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kTliThreads)
@@ -59,14 +118,14 @@ __global__ void __launch_bounds__(kTliThreads)
   __shared__ int s_best;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(draft) + r * Vd * esz;
-  MaskedVisitor st{d2t, c, neg_inf(), 0.0f, INT_MAX};
-  for_row<DT, 4>(row, Vd, st);
+  MaskedVisitor<DT> st{d2t, c, neg_inf(), 0.0f, 0.0f, 0.0f, INT_MAX};
+  for_row_fast<DT, 4>(row, Vd, st, threadIdx.x, kTliThreads);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float bv = st.m;
   int bi = st.bi;
   warp_best(bv, bi);
-  float m = st.m, s = st.s;
+  float m = st.m, s = st.s0 + st.s1;
   warp_merge_ms(m, s, c);
   if (lane == 0) {
     wv[warp] = bv;
@@ -99,21 +158,32 @@ __global__ void __launch_bounds__(kTliThreads)
   const bool ok = s_best >= 0;
   const float mc = s_m * c, invz = s_invz;
   const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (reinterpret_cast<uintptr_t>(t2d) & 15) == 0;
-  const int64_t nv = vec ? Vt / 4 : 0;
-  for (int64_t i = threadIdx.x; i < nv; i += kTliThreads) {
+  const int nv = vec ? static_cast<int>(Vt / 4) : 0;
+  // two groups of 4 targets per thread and step: 8 gathers from the draft
+  // row (just read, in L2) in flight
+  int i = threadIdx.x;
+  for (; i + kTliThreads < nv; i += 2 * kTliThreads) {
+    const int4 d0 = __ldg(reinterpret_cast<const int4*>(t2d) + i);
+    const int4 d1 = __ldg(reinterpret_cast<const int4*>(t2d) + i + kTliThreads);
+    float4 p0, p1;
+    p0.x = q_of<DT>(row, d0.x, Vd, ok, c, mc, invz);
+    p0.y = q_of<DT>(row, d0.y, Vd, ok, c, mc, invz);
+    p0.z = q_of<DT>(row, d0.z, Vd, ok, c, mc, invz);
+    p0.w = q_of<DT>(row, d0.w, Vd, ok, c, mc, invz);
+    p1.x = q_of<DT>(row, d1.x, Vd, ok, c, mc, invz);
+    p1.y = q_of<DT>(row, d1.y, Vd, ok, c, mc, invz);
+    p1.z = q_of<DT>(row, d1.z, Vd, ok, c, mc, invz);
+    p1.w = q_of<DT>(row, d1.w, Vd, ok, c, mc, invz);
+    st_stream(out + 4 * i, p0);
+    st_stream(out + 4 * (i + kTliThreads), p1);
+  }
+  for (; i < nv; i += kTliThreads) {
     const int4 d = __ldg(reinterpret_cast<const int4*>(t2d) + i);
-    float4 p;
-    p.x = (ok && d.x >= 0 && d.x < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.x)), c, -mc)) * invz, 1.0f) : 0.0f;
-    p.y = (ok && d.y >= 0 && d.y < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.y)), c, -mc)) * invz, 1.0f) : 0.0f;
-    p.z = (ok && d.z >= 0 && d.z < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.z)), c, -mc)) * invz, 1.0f) : 0.0f;
-    p.w = (ok && d.w >= 0 && d.w < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d.w)), c, -mc)) * invz, 1.0f) : 0.0f;
-    st_stream(out + 4 * i, p);
+    st_stream(out + 4 * i, make_float4(q_of<DT>(row, d.x, Vd, ok, c, mc, invz), q_of<DT>(row, d.y, Vd, ok, c, mc, invz),
+                                       q_of<DT>(row, d.z, Vd, ok, c, mc, invz), q_of<DT>(row, d.w, Vd, ok, c, mc, invz)));
   }
-  for (int64_t t = nv * 4 + threadIdx.x; t < Vt; t += kTliThreads) {
-    const int32_t d = __ldg(t2d + t);
-    out[t] = (ok && d >= 0 && d < Vd) ? fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, d)), c, -mc)) * invz, 1.0f)
-                            : 0.0f;
-  }
+  for (int64_t t = static_cast<int64_t>(nv) * 4 + threadIdx.x; t < Vt; t += kTliThreads)
+    out[t] = q_of<DT>(row, __ldg(t2d + t), Vd, ok, c, mc, invz);
 }
 
 __global__ void map_ids_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out, int64_t n,

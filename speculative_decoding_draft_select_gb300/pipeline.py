@@ -131,7 +131,7 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
                             stats=buf.stats)
             else:
                 spec_sample(draft_u[a:a + r], logits=rows, T=T, out_token=buf.tok[a:a + r],
-                            out_prob=buf.prob[a:a + r], stats=buf.stats)
+                            out_prob=buf.prob[a:a + r], stats=buf.stats, row_stats=st)
             spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
         else:
             spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,

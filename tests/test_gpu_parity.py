@@ -162,6 +162,25 @@ def test_sample_parity(V, use_probs):
     np.testing.assert_allclose(prob[same], oprob[same], atol=PROB_TOL)
 
 
+@pytest.mark.parametrize("V", [7, 4097, 129280])
+def test_sample_with_row_stats_equals_sample_alone(V):
+    """Given the row statistics of spec_softmax_topk, spec_sample reads each
+    row once and draws exactly what it draws on its own."""
+    rng = np.random.default_rng(V + 3)
+    R = 48
+    x = dev(make_logits(rng, R, V, torch.bfloat16))
+    x[5] = float("-inf")  # a row without a finite max
+    u = dev(rng.random(R).astype(np.float32))
+    rs = torch.empty((R, 2), device="cuda")
+    sd.spec_softmax_topk(x, 0.8, 1, row_stats=rs)
+    s1, s2 = sd.new_stats(), sd.new_stats()
+    a = sd.spec_sample(u, logits=x, T=0.8, stats=s1)
+    b = sd.spec_sample(u, logits=x, T=0.8, row_stats=rs, stats=s2)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(s1, s2) and int(s1[sd.STATS["nonfinite_row"]]) == 1
+
+
 # -------------------------------------------------------------------- tree
 
 def oracle_topk_inputs(rng, B, k, steps, ties=False):
