@@ -196,7 +196,7 @@ def run_ours(args, cfg, mode, rank, world):
         return torch.cuda.Event(enable_timing=True)
 
     class Timer:
-        """CUDA events around the draft steps' softmax/top-k (or TLI) launches
+        """CUDA events around the draft steps' softmax/top-k (softmax/draw, TLI) launches
         with R = B*topk rows (steps >= 1), on the launching stream."""
         record = False
 
@@ -276,7 +276,7 @@ def run_ours(args, cfg, mode, rank, world):
         kname = "tli_constrain_kernel"
     else:
         per_row = row_bytes + (cfg.V * 4 if buf.q is not None else 0)  # read + written q
-        kname = DOMINANT
+        kname = "softmax_sample_kernel" if (cfg.kind == "chain" and mode == "sample") else DOMINANT
     dom_avg_ms = statistics.mean(dom_ms) if dom_ms else None
     dom_bytes = per_row * statistics.mean(dom_rows) if dom_rows else None
     peak, peak_kind = hbm_peak()

@@ -122,6 +122,25 @@ int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_nul
                 int64_t V, float T, const float* u, int32_t* out_token, float* out_prob_or_null,
                 const float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream);
 
+/* Draft softmax and sampling in one pass, for sampled chains (drafts drawn
+ * from q, [ZS] 5.1).  Per row: m, Z as spec_softmax_topk defines them and
+ * one token by inverse CDF over vocabulary order with the uniform u[r] (the
+ * smallest v whose inclusive prefix sum of 2^((l - m) log2(e)/T) exceeds
+ * u[r] times the total), reading the row once.
+ *   logits     [R, V] (dtype), V <= 524288 for bf16, 262144 for fp32
+ *              (SPEC_ERR_UNSUPPORTED above).
+ *   u          [R] fp32 uniforms in [0,1).
+ *   out_token  [R] int32 out; out_prob_or_null [R] fp32 out: its weight
+ *              divided by the total.
+ *   row_stats_or_null [R, 2] fp32 out: (m, Z) for spec_verify_sample_qlogits.
+ *   probs_or_null [R, V] fp32 out: the distribution, with the same m and Z.
+ * A row with no finite max gets token 0, probability 0, zero probabilities
+ * and counts in SPEC_STAT_NONFINITE_ROW; no crossing after rounding takes
+ * the last index of positive weight (SPEC_STAT_CDF_FALLBACK). */
+int spec_softmax_sample(const void* logits, int dtype, int64_t R, int64_t V, float T, const float* u,
+                        int32_t* out_token, float* out_prob_or_null, float* row_stats_or_null,
+                        float* probs_or_null, int32_t* stats_or_null, spec_stream_t stream);
+
 /* Candidate-pool size P = 1 + k + (num_steps - 1) * k * k. */
 int64_t spec_tree_pool_size(int k, int num_steps);
 

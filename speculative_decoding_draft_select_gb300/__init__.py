@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "SpecError", "F32", "BF16", "STATS", "lib", "library_path",
-    "spec_softmax_topk", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
+    "spec_softmax_topk", "spec_softmax_sample", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
     "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
     "spec_verify_sample_qlogits", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_map_ids", "tli_check_config",
@@ -43,6 +43,7 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P]),
     "spec_sample": (_I, [_P, _I, _P, _I64, _I64, _F, _P, _P, _P, _P, _P, _P]),
+    "spec_softmax_sample": (_I, [_P, _I, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P]),
     "spec_tree_pool_size": (_I64, [_I, _I]),
     "spec_tree_expand": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_build_tree": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -150,6 +151,27 @@ def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want
     _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
           _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _stream())
     return topk_p, topk_idx, probs
+
+
+def spec_softmax_sample(logits, T, u, out_token=None, out_prob=None, row_stats=None, probs=None, want_probs=False,
+                        stats=None):
+    """Draft softmax and one inverse-CDF token per row in one pass:
+    logits [R, V], u [R] -> (out_token [R] i32, out_prob [R] f32, probs or
+    None); row_stats [R, 2] (optional) receives (max, normaliser)."""
+    _dev(logits, name="logits")
+    _dev(u, torch.float32, "u")
+    V = logits.shape[-1]
+    R = logits.numel() // V
+    out_token = _out(out_token, (R,), torch.int32, logits, "out_token")
+    out_prob = _out(out_prob, (R,), torch.float32, logits, "out_prob")
+    if want_probs and probs is None:
+        probs = torch.empty((R, V), dtype=torch.float32, device=logits.device)
+    _dev(probs, torch.float32, "probs")
+    _dev(row_stats, torch.float32, "row_stats")
+    _dev(stats, torch.int32, "stats")
+    _call("spec_softmax_sample", _ptr(logits), _logit_code(logits), R, V, float(T), _ptr(u), _ptr(out_token),
+          _ptr(out_prob), _ptr(row_stats), _ptr(probs), _ptr(stats), _stream())
+    return out_token, out_prob, probs
 
 
 def spec_sample(u, logits=None, probs=None, T=1.0, out_token=None, out_prob=None, stats=None, row_stats=None):

@@ -405,6 +405,21 @@ __device__ void warp_rank_row(const void* row, int64_t V, int n, float* out_v, i
   }
 }
 
+// p = min(2^((key(x) - m) c) / Z, 1) for the V elements of a row, written
+// to out (zeros when the row has no finite max), streaming stores.
+template <int DT>
+__device__ __forceinline__ void write_probs(const void* row, int64_t V, bool finite, float mc, float c, float invz,
+                                            float* out) {
+  if (finite) {
+    const RowSpan sp = row_span<DT>(row, V);
+    ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
+    for_row<DT, 2>(row, V, pw);
+  } else {
+    ZeroWriter z{out};
+    for_row<DT, 2>(row, V, z);
+  }
+}
+
 template <int K>
 constexpr size_t draft_smem_bytes() {
   return K == 1 ? 16 : kCandCap * (sizeof(float) + sizeof(int));
@@ -536,17 +551,7 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
       row_stats[2 * r + 1] = s;
     }
   }
-  if (probs != nullptr) {
-    float* out = probs + r * V;
-    if (finite) {
-      const RowSpan sp = row_span<DT>(row, V);
-      ProbWriter<DT> pw{c, mc, invz, out, (reinterpret_cast<uintptr_t>(out + sp.head) & 15) == 0};
-      for_row<DT, 2>(row, V, pw);
-    } else {
-      ZeroWriter z{out};
-      for_row<DT, 2>(row, V, z);
-    }
-  }
+  if (probs != nullptr) write_probs<DT>(row, V, finite, mc, c, invz, probs + r * V);
 }
 
 // ---------------------------------------------------------------- sampling
@@ -631,6 +636,296 @@ __global__ void __launch_bounds__(kSampleThreads)
   sample_row(w, V, __ldg(u + r), red, tile_sum, scan_sh, stats, out_token + r, op);
 }
 
+// ------------------------------------------------ fused softmax + sampling
+//
+// Sampled chains (one token per draft row, [ZS] 5.1: "a candidate y drawn
+// from the draft distribution q") need the row's softmax statistics, which
+// verification reads, and an inverse-CDF draw from the same distribution.
+// One CTA per row streams the row once with the lean loop's layout.  Tile i
+// is kFusedRounds rounds of 16-byte vectors (round u: vectors i U T + u T +
+// [0, T), contiguous in the vocabulary).  Each thread keeps its running max
+// key and its sums relative to it: its partial of every finished tile in
+// shared memory, as log2(partial) + max c, and its total.  After the pass one
+// block max, 2^(stored - M c) and fixed-order reductions give Z and the tile
+// sums; the draw walks
+// the tile sums and rescans only the crossing tile, round by round with a
+// block scan.  Head and tail scalars (rows not 16-byte aligned) form a tile
+// of their own before and after the vectors.
+constexpr int kFusedThreads = 128;  // all rows of a 1024-row step resident at once
+constexpr int kFusedRounds = 4;
+constexpr int kFusedMaxTiles = 128;  // partials: tiles x threads floats of shared memory
+
+template <int DT>
+__host__ __device__ constexpr int64_t fused_max_vocab() {
+  return static_cast<int64_t>(kFusedMaxTiles) * kFusedRounds * kFusedThreads * Logit<DT>::kVec;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
+    softmax_sample_kernel(const void* __restrict__ logits, int64_t V64, float c, const float* __restrict__ u,
+                          int32_t* __restrict__ out_token, float* __restrict__ out_prob,
+                          float* __restrict__ row_stats, float* __restrict__ probs, int32_t* __restrict__ stats) {
+  constexpr int T = kFusedThreads, U = kFusedRounds, kv = Logit<DT>::kVec, kWarps = T / 32;
+  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  extern __shared__ float part[];  // [ntiles][T]: log2 of the partials plus the max they are relative to
+  __shared__ float tsum[kFusedMaxTiles + 2];
+  __shared__ float red[33], scan_sh[33], rtot[U * kWarps];
+  __shared__ int s_tok;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t r = blockIdx.x;
+  const void* row = static_cast<const char*>(logits) + r * V64 * esz;
+  const RowSpan sp = row_span<DT>(row, V64);
+  const int V = static_cast<int>(V64), head = static_cast<int>(sp.head), nvec = static_cast<int>(sp.nvec);
+  const int tail0 = head + nvec * kv, ntiles = (nvec + U * T - 1) / (U * T);
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+
+  float m = neg_inf(), mc = 0.0f, s = 0.0f, hs = 0.0f, tl = 0.0f;
+  if (tid < head) {  // head < kv <= T
+    const float x = order_key(Logit<DT>::load1(row, tid));
+    if (x != neg_inf()) {
+      m = x;
+      mc = x * c;
+      hs = s = 1.0f;
+    }
+  }
+  // tile i's partial is stored as log2(partial) + m c, m the thread's max at
+  // the tile's end; 2^(stored - M c) brings it to the row max after the pass
+  auto vec_step = [&](const uint4& raw, float2& acc) {
+    float x[kv];
+    unpack<DT>(raw, x);
+    // NaN-ignoring max; a NaN element makes the sums NaN (repaired below)
+    const float vmax = DT == SPEC_BF16 ? max8_bf16(raw) : fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
+    if (vmax > m) {
+      const float f = m == neg_inf() ? 0.0f : fast_exp2((m - vmax) * c);
+      s *= f;
+      hs *= f;
+      acc.x *= f;
+      acc.y *= f;
+      m = vmax;
+      mc = vmax * c;
+    }
+    if (m != neg_inf()) acc = exp2_sum_pairs<kv>(acc, x, c, mc);
+  };
+  const int nfull = nvec / (U * T);
+  for (int i = 0; i < nfull; ++i) {  // full tiles: no bounds tests
+    const int base = i * U * T + tid;
+    uint4 v[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q) v[q] = ld_stream(vp + base + q * T);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < U; ++q) vec_step(v[q], acc);
+    const float pt = acc.x + acc.y;
+    part[i * T + tid] = fast_log2(pt) + mc;
+    s += pt;
+  }
+  if (nfull < ntiles) {  // the last, partial tile
+    const int base = nfull * U * T + tid;
+    uint4 v[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q)
+      if (base + q * T < nvec) v[q] = ld_stream(vp + base + q * T);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < U; ++q)
+      if (base + q * T < nvec) vec_step(v[q], acc);
+    const float pt = acc.x + acc.y;
+    part[nfull * T + tid] = fast_log2(pt) + mc;
+    s += pt;
+  }
+  if (tail0 + tid < V) {  // fewer than kv tail elements
+    const float x = order_key(Logit<DT>::load1(row, tail0 + tid));
+    if (x > m) {
+      const float f = m == neg_inf() ? 0.0f : fast_exp2((m - x) * c);
+      s *= f;
+      hs *= f;
+      m = x;
+      mc = x * c;
+    }
+    if (m != neg_inf()) {
+      tl = fast_exp2(fmaf(x, c, -mc));
+      s += tl;
+    }
+  }
+  // a NaN in this thread's elements: recompute its partials with NaN as -inf
+  // (the max is already NaN-free)
+  if (!isfinite(s) && m != neg_inf() && isfinite(m)) {
+    s = 0.0f;
+    for (int i = 0; i < ntiles; ++i) {
+      const int base = i * U * T + tid;
+      float pt = 0.0f;
+      for (int q = 0; q < U; ++q) {
+        if (base + q * T >= nvec) continue;
+        float x[kv];
+        unpack<DT>(__ldg(vp + base + q * T), x);
+#pragma unroll
+        for (int j = 0; j < kv; ++j) pt += fast_exp2(fmaf(order_key(x[j]), c, -mc));
+      }
+      part[i * T + tid] = fast_log2(pt) + mc;
+      s += pt;
+    }
+    s += hs + tl;
+  }
+  // row max, per-thread scale, normaliser (fixed order)
+  float mb = warp_max(m);
+  if (lane == 0) red[warp] = mb;
+  __syncthreads();
+  if (warp == 0) {
+    float x = lane < kWarps ? red[lane] : neg_inf();
+    x = warp_max(x);
+    if (lane == 0) red[32] = x;
+  }
+  __syncthreads();
+  const float M = red[32];
+  const bool finite = isfinite(M);
+  const float f = (finite && m != neg_inf()) ? fast_exp2((m - M) * c) : 0.0f;
+  const float zw = warp_sum(s * f);
+  __syncthreads();
+  if (lane == 0) red[warp] = zw;
+  const float Mc_ = M * c;
+  for (int j = 0; j < ntiles; ++j) part[j * T + tid] = finite ? fast_exp2(part[j * T + tid] - Mc_) : 0.0f;
+  hs *= f;
+  tl *= f;
+  __syncthreads();
+  float Z = 0.0f;
+  for (int w2 = 0; w2 < kWarps; ++w2) Z += red[w2];
+  for (int j = warp; j < ntiles; j += kWarps) {
+    float a = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) a += part[j * T + q * 32 + lane];
+    a = warp_sum(a);
+    if (lane == 0) tsum[1 + j] = a;
+  }
+  if (warp == 0) {  // head and tail threads are all in warp 0
+    const float h = warp_sum(hs), t = warp_sum(tl);
+    if (lane == 0) {
+      tsum[0] = h;
+      tsum[ntiles + 1] = t;
+      s_tok = INT_MAX;
+    }
+  }
+  __syncthreads();
+  if (!finite) {
+    if (tid == 0) {
+      bump(stats, SPEC_STAT_NONFINITE_ROW);
+      out_token[r] = 0;
+      if (out_prob) out_prob[r] = 0.0f;
+      if (row_stats) {
+        row_stats[2 * r] = M;
+        row_stats[2 * r + 1] = Z;
+      }
+    }
+    if (probs) write_probs<DT>(row, V64, false, 0.0f, c, 0.0f, probs + r * V64);
+    return;
+  }
+  float W = 0.0f;
+  for (int j = 0; j < ntiles + 2; ++j) W += tsum[j];
+  const float Mc = M * c;
+  const float target = __ldg(u + r) * W;
+  float prefix = 0.0f;
+  if (W > 0.0f && isfinite(W)) {
+    for (int j = 0; j < ntiles + 2; ++j) {
+      const float after = prefix + tsum[j];
+      if (after > target) {
+        if (j == 0 || j == ntiles + 1) {  // a scalar tile, scanned by thread 0
+          if (tid == 0) {
+            const int lo = j == 0 ? 0 : tail0, hi = j == 0 ? head : V;
+            float C = prefix;
+            for (int e = lo; e < hi; ++e) {
+              C += fast_exp2(fmaf(order_key(Logit<DT>::load1(row, e)), c, -Mc));
+              if (C > target) {
+                s_tok = e;
+                break;
+              }
+            }
+          }
+        } else {
+          // the tile's rounds: all loads at once, the rounds' totals, then
+          // a block scan of the crossing round only (later rounds if
+          // rounding moves the crossing)
+          float w[U][kv], ws[U];
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
+            const int vi = (j - 1) * U * T + q * T + tid;
+            ws[q] = 0.0f;
+            if (vi < nvec) {
+              unpack<DT>(__ldg(vp + vi), w[q]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < kv; ++k) w[q][k] = neg_inf();
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
+#pragma unroll
+            for (int k = 0; k < kv; ++k) {
+              w[q][k] = fast_exp2(fmaf(order_key(w[q][k]), c, -Mc));
+              ws[q] += w[q][k];
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
+            const float t = warp_sum(ws[q]);
+            if (lane == 0) rtot[q * kWarps + warp] = t;
+          }
+          __syncthreads();
+          float C0 = prefix;
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
+            float rt = 0.0f;
+            for (int w2 = 0; w2 < kWarps; ++w2) rt += rtot[q * kWarps + w2];
+            if (C0 + rt > target || q == U - 1) {
+              const int vi = (j - 1) * U * T + q * T + tid;
+              float tot;
+              const float incl = block_inclusive_scan(ws[q], scan_sh, tot);
+              float C = C0 + (incl - ws[q]);
+              int fnd = -1;
+#pragma unroll
+              for (int k = 0; k < kv; ++k) {
+                C += w[q][k];
+                if (fnd < 0 && C > target && vi < nvec) fnd = k;
+              }
+              if (fnd >= 0) atomicMin(&s_tok, head + vi * kv + fnd);
+              __syncthreads();
+              if (s_tok != INT_MAX) break;
+            }
+            C0 += rt;
+          }
+        }
+        __syncthreads();
+        if (s_tok != INT_MAX) break;
+      }
+      prefix = after;
+    }
+  }
+  __syncthreads();
+  if (s_tok == INT_MAX) {
+    // rounding left no crossing: the last index of positive weight
+    __syncthreads();
+    if (tid == 0) s_tok = -1;
+    __syncthreads();
+    for (int v = tid; v < V; v += T)
+      if (fast_exp2(fmaf(order_key(Logit<DT>::load1(row, v)), c, -Mc)) > 0.0f) atomicMax(&s_tok, v);
+    __syncthreads();
+    if (tid == 0) {
+      if (s_tok < 0) s_tok = 0;
+      bump(stats, SPEC_STAT_CDF_FALLBACK);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int tok = s_tok;
+    out_token[r] = tok;
+    if (out_prob)
+      out_prob[r] = W > 0.0f ? fast_exp2(fmaf(order_key(Logit<DT>::load1(row, tok)), c, -Mc)) / W : 0.0f;
+    if (row_stats) {
+      row_stats[2 * r] = M;
+      row_stats[2 * r + 1] = Z;
+    }
+  }
+  if (probs) write_probs<DT>(row, V64, true, Mc, c, 1.0f / Z, probs + r * V64);
+}
+
 template <int DT, int K, int THREADS>
 int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
                           int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
@@ -689,6 +984,41 @@ extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64
                                                 row_stats_or_null, stats_or_null, s)
              : dispatch_softmax_topk<SPEC_F32>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
                                                row_stats_or_null, stats_or_null, s);
+}
+
+extern "C" int spec_softmax_sample(const void* logits, int dtype, int64_t R, int64_t V, float T, const float* u,
+                                   int32_t* out_token, float* out_prob_or_null, float* row_stats_or_null,
+                                   float* probs_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+  if (R < 0 || V < 1 || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
+  if (R > 0 && (logits == nullptr || u == nullptr || out_token == nullptr)) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  if (V > (dtype == SPEC_BF16 ? fused_max_vocab<SPEC_BF16>() : fused_max_vocab<SPEC_F32>()))
+    return SPEC_ERR_UNSUPPORTED;
+  if (R == 0) return SPEC_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float c = kLog2e / T;
+  const int kv = dtype == SPEC_BF16 ? 8 : 4;
+  const int64_t ntiles = (V / kv + kFusedRounds * kFusedThreads - 1) / (kFusedRounds * kFusedThreads);
+  const size_t smem = sizeof(float) * static_cast<size_t>(ntiles > 0 ? ntiles : 1) * kFusedThreads;
+  const unsigned grid = static_cast<unsigned>(R);
+  if (dtype == SPEC_BF16) {
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_sample_kernel<SPEC_BF16>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem)) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    softmax_sample_kernel<SPEC_BF16><<<grid, kFusedThreads, smem, s>>>(logits, V, c, u, out_token, out_prob_or_null,
+                                                                      row_stats_or_null, probs_or_null,
+                                                                      stats_or_null);
+  } else {
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_sample_kernel<SPEC_F32>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem)) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    softmax_sample_kernel<SPEC_F32><<<grid, kFusedThreads, smem, s>>>(logits, V, c, u, out_token, out_prob_or_null,
+                                                                     row_stats_or_null, probs_or_null, stats_or_null);
+  }
+  return launch_status();
 }
 
 extern "C" int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_null, int64_t R,

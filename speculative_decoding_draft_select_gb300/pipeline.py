@@ -6,8 +6,9 @@ EAGLE" sections 2-3 and "EAGLE speculative decoding in four parts",
   - EAGLE tree:  spec_softmax_topk on the step's draft rows (writing the
                  draft distribution q into the step-major table when the
                  verify samples), then spec_tree_expand;
-  - sampled chain: spec_softmax_topk (q) then spec_sample with the step's
-                 uniforms, then spec_tree_expand with k = 1;
+  - sampled chain: spec_softmax_sample (q or its row statistics, and the
+                 draw with the step's uniforms, in one pass), then
+                 spec_tree_expand with k = 1;
   - TLI chain:   tli_constrain_map (q in target order), then
                  spec_tree_expand with the mapped top-1 (SGLang PR #22883).
 then spec_build_tree.  Verify: spec_verify_greedy, or for sampling either
@@ -26,7 +27,7 @@ from __future__ import annotations
 import torch
 
 from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity, spec_compact_slots,
-               spec_sample, spec_softmax_topk, spec_tree_expand, spec_verify_greedy, spec_verify_sample,
+               spec_softmax_sample, spec_softmax_topk, spec_tree_expand, spec_verify_greedy, spec_verify_sample,
                spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map)
 
 
@@ -122,16 +123,11 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
                 timer.end(s)
             spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
         elif buf.kind == "chain" and buf.sampled:
-            spec_softmax_topk(rows, T, 1, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,
-                              stats=buf.stats)
+            # softmax (q or its row statistics) and the draw in one pass
+            spec_softmax_sample(rows, T, draft_u[a:a + r], out_token=buf.tok[a:a + r], out_prob=buf.prob[a:a + r],
+                                row_stats=st, probs=qs, stats=buf.stats)
             if timer is not None:
                 timer.end(s)
-            if qs is not None:
-                spec_sample(draft_u[a:a + r], probs=qs, out_token=buf.tok[a:a + r], out_prob=buf.prob[a:a + r],
-                            stats=buf.stats)
-            else:
-                spec_sample(draft_u[a:a + r], logits=rows, T=T, out_token=buf.tok[a:a + r],
-                            out_prob=buf.prob[a:a + r], stats=buf.stats, row_stats=st)
             spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
         else:
             spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,
@@ -184,7 +180,7 @@ def capture_step(fn, warm=True):
 
 def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> int:
     """Number of kernel launches one step enqueues."""
-    per_step = 3 if (buf.kind == "chain" and buf.sampled) else 2
+    per_step = 2  # softmax/top-k (or softmax and draw, or TLI constrain) + tree expand
     n = buf.steps * per_step + 1  # + build_tree
     n += 2  # verify: row pass + walk
     if compact:

@@ -43,6 +43,13 @@ def test_host_side_argument_checks(lib):
                                  null, null, null, null) == -2
     assert lib.spec_softmax_topk(ctypes.c_void_p(16), 1, 4, 100, 1.0, 33, ctypes.c_void_p(16),
                                  ctypes.c_void_p(16), null, null, null, null) == -2  # k above the limit
+    # fused softmax + draw: T <= 0, bad dtype, a vocabulary beyond its shared-memory tiles
+    p16 = ctypes.c_void_p(16)
+    assert lib.spec_softmax_sample(p16, 1, 4, 8, 0.0, p16, p16, null, null, null, null, null) == -1
+    assert lib.spec_softmax_sample(p16, 5, 4, 8, 1.0, p16, p16, null, null, null, null, null) == -2
+    assert lib.spec_softmax_sample(p16, 1, 4, 524289, 1.0, p16, p16, null, null, null, null, null) == -2
+    assert lib.spec_softmax_sample(p16, 0, 4, 262145, 1.0, p16, p16, null, null, null, null, null) == -2
+    assert lib.spec_softmax_sample(null, 1, 0, 8, 1.0, null, null, null, null, null, null, null) == 0
     # empty batches are no-ops
     assert lib.spec_softmax_topk(null, 1, 0, 8, 1.0, 2, null, null, null, null, null, null) == 0
     assert lib.spec_tree_expand(0, 2, 4, 0, null, null, null, null, null, null, null, null, null) == -1

@@ -181,6 +181,44 @@ def test_sample_with_row_stats_equals_sample_alone(V):
     assert torch.equal(s1, s2) and int(s1[sd.STATS["nonfinite_row"]]) == 1
 
 
+@pytest.mark.parametrize("V", [7, 33, 4097, 32000, 129280])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_softmax_sample_parity(V, dtype):
+    """One pass gives the draw of spec_sample, the probabilities of
+    spec_softmax_topk and the row maximum; against the oracle (a token may
+    differ only within 1e-5 of a CDF boundary)."""
+    rng = np.random.default_rng(V + 11)
+    R = 40
+    x = make_logits(rng, R, V, dtype)
+    x[3] = float("-inf")
+    x[4, 1] = float("inf")
+    if V >= 8:
+        x[5, 2] = float("nan")
+    u = rng.random(R).astype(np.float32)
+    u[:3] = [0.0, 0.5, np.nextafter(np.float32(1), np.float32(0))]
+    rs = torch.empty((R, 2), device="cuda")
+    stats = sd.new_stats()
+    tok, prob, probs = sd.spec_softmax_sample(dev(x), 0.8, dev(u), row_stats=rs, want_probs=True, stats=stats)
+    torch.cuda.synchronize()
+    xl = np_logits(x)
+    otok, oprob, margin, _ = oracle.sample(u, logits=xl, T=0.8)
+    _, _, oprobs, _ = oracle.softmax_topk(xl, 0.8, 1, want_probs=True)
+    tok, prob = tok.cpu().numpy(), prob.cpu().numpy()
+    keys = x.float().numpy()
+    keys = np.where(np.isnan(keys), -np.inf, keys)  # NaN counts as -inf
+    finite = np.isfinite(keys.max(axis=1))
+    diff = (tok != otok) & finite
+    assert not (diff & (margin >= BOUNDARY)).any()
+    assert diff.sum() <= 1
+    same = ~diff & finite
+    np.testing.assert_allclose(prob[same], oprob[same], atol=PROB_TOL)
+    assert (tok[~finite] == 0).all() and (prob[~finite] == 0).all()
+    assert int(stats[sd.STATS["nonfinite_row"]]) == int((~finite).sum()) == 2
+    np.testing.assert_allclose(probs.cpu().numpy(), oprobs, rtol=0, atol=PROB_TOL)
+    np.testing.assert_array_equal(rs[torch.from_numpy(finite).cuda(), 0].cpu().numpy(),
+                                  keys[finite].max(axis=1).astype(np.float32))
+
+
 # -------------------------------------------------------------------- tree
 
 def oracle_topk_inputs(rng, B, k, steps, ties=False):
