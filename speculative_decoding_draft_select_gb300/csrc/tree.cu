@@ -113,6 +113,8 @@ __device__ __forceinline__ int block_exclusive_scan_int(int v, int* sh, int& tot
 }
 
 constexpr int kBuildThreads = 512;
+constexpr int64_t kRankPool = 1024;  // selection by rank counting up to this many candidates
+constexpr int kParallelLinks = 256;  // first child / next sibling one thread per node up to N
 
 __global__ void __launch_bounds__(kBuildThreads)
     build_tree_kernel(int N, int64_t P, int64_t L, const float* __restrict__ pool_score,
@@ -135,31 +137,41 @@ __global__ void __launch_bounds__(kBuildThreads)
   const int32_t* pa = pool_parent + b * P;
   const int32_t* qr = pool_qrow + b * P;
 
-  // 1. rank the non-root candidates by (score desc, pool id asc): bitonic sort
+  // 1. the N-1 best non-root candidates by (score desc, pool id asc): keys
+  // are distinct, so a candidate's rank is the number of smaller keys
+  // (small pools); larger pools are sorted (bitonic)
   for (int64_t i = threadIdx.x; i < L; i += nt)
     keys[i] = i < P - 1 ? rank_key(__ldg(sc + i + 1), static_cast<int32_t>(i + 1)) : ~0ull;
-  __syncthreads();
-  for (int64_t size = 2; size <= L; size <<= 1) {
-    for (int64_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int64_t i = threadIdx.x; i < L; i += nt) {
-        const int64_t j = i ^ stride;
-        if (j > i) {
-          const bool asc = (i & size) == 0;
-          const uint64_t a = keys[i], c = keys[j];
-          if ((a > c) == asc) {
-            keys[i] = c;
-            keys[j] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  // 2. the root and the N-1 best candidates, numbered in pool-id order
   for (int64_t i = threadIdx.x; i < P; i += nt) node_of[i] = i == 0 ? 1 : 0;
   __syncthreads();
-  for (int64_t r = threadIdx.x; r < N - 1; r += nt) node_of[static_cast<uint32_t>(keys[r])] = 1;
+  if (P - 1 <= kRankPool) {
+    for (int64_t i = threadIdx.x; i < P - 1; i += nt) {
+      const uint64_t ki = keys[i];
+      int rank = 0;
+      for (int64_t j = 0; j < P - 1; ++j) rank += keys[j] < ki ? 1 : 0;
+      if (rank < N - 1) node_of[i + 1] = 1;
+    }
+  } else {
+    for (int64_t size = 2; size <= L; size <<= 1) {
+      for (int64_t stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int64_t i = threadIdx.x; i < L; i += nt) {
+          const int64_t j = i ^ stride;
+          if (j > i) {
+            const bool asc = (i & size) == 0;
+            const uint64_t a = keys[i], c = keys[j];
+            if ((a > c) == asc) {
+              keys[i] = c;
+              keys[j] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int64_t r = threadIdx.x; r < N - 1; r += nt) node_of[static_cast<uint32_t>(keys[r])] = 1;
+  }
   __syncthreads();
+  // 2. the root and the selected candidates, numbered in pool-id order
   const int64_t chunk = (P + nt - 1) / nt;
   const int64_t lo = threadIdx.x * chunk, hi = min(P, lo + chunk);
   int cnt = 0;
@@ -206,18 +218,33 @@ __global__ void __launch_bounds__(kBuildThreads)
     while (a > m) a = npar[a];
     mask[e] = a == m ? 1 : 0;
   }
-  // 4. first child and next sibling, in node order
-  if (threadIdx.x == 0) {
-    for (int n = 0; n < N; ++n) nxt[n] = -1;
-    for (int n = N - 1; n >= 1; --n) {
-      const int p = npar[n];
-      next_sibling[o + n] = p >= 0 ? nxt[p] : -1;
-      if (p >= 0) nxt[p] = n;
+  // 4. first child and next sibling, in node order (the smallest later node
+  // with parent n, or with n's parent)
+  if (N <= kParallelLinks) {
+    for (int n = threadIdx.x; n < N; n += nt) {
+      const int p = n > 0 ? npar[n] : -1;
+      int fc = -1, ns = -1;
+      for (int m2 = n + 1; m2 < N && (fc < 0 || (p >= 0 && ns < 0)); ++m2) {
+        const int q = npar[m2];
+        if (fc < 0 && q == n) fc = m2;
+        if (p >= 0 && ns < 0 && q == p) ns = m2;
+      }
+      next_token[o + n] = fc;
+      next_sibling[o + n] = ns;
     }
-    next_sibling[o] = -1;
+  } else {
+    if (threadIdx.x == 0) {
+      for (int n = 0; n < N; ++n) nxt[n] = -1;
+      for (int n = N - 1; n >= 1; --n) {
+        const int p = npar[n];
+        next_sibling[o + n] = p >= 0 ? nxt[p] : -1;
+        if (p >= 0) nxt[p] = n;
+      }
+      next_sibling[o] = -1;
+    }
+    __syncthreads();
+    for (int n = threadIdx.x; n < N; n += nt) next_token[o + n] = nxt[n];
   }
-  __syncthreads();
-  for (int n = threadIdx.x; n < N; n += nt) next_token[o + n] = nxt[n];
 }
 
 }  // namespace

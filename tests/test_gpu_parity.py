@@ -237,7 +237,8 @@ def oracle_topk_inputs(rng, B, k, steps, ties=False):
 
 @pytest.mark.parametrize("B,k,steps,N,ties", [(4, 1, 6, 7, False), (64, 4, 5, 16, False), (16, 8, 6, 64, False),
                                               (8, 3, 4, 2, True), (8, 4, 5, 16, True), (3, 2, 3, 11, True),
-                                              (2, 16, 3, 200, False)])
+                                              (2, 16, 3, 200, False), (2, 16, 3, 300, True),
+                                              (2, 32, 3, 100, True)])
 def test_tree_parity(B, k, steps, N, ties):
     rng = np.random.default_rng(B * 7 + k + N)
     inputs = oracle_topk_inputs(rng, B, k, steps, ties)
