@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "specdec.h"
 
 namespace specdec {
@@ -102,6 +104,40 @@ __device__ __forceinline__ float2 exp2_sum_pairs(float2 s, const float* x, float
 #pragma unroll
   for (int j = 0; j < N; j += 2) s = add2(s, exp2_2(fma2(make_float2(x[j], x[j + 1]), c2, nmc2)));
   return s;
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// (launch_k) so that it may be scheduled before the previous kernel on the
+// stream has finished; pdl_enter, its first statement, waits until that
+// kernel has completed and its writes are visible, then lets the next kernel
+// be scheduled.  A kernel must touch no global memory before pdl_enter.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The last launch_k failure of this thread since launch_status last ran.
+inline cudaError_t& launch_error() {
+  static thread_local cudaError_t e = cudaSuccess;
+  return e;
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) launch_error() = e;
+  return e;
 }
 
 // Thread-block clusters: this CTA's rank, a barrier over every thread of
@@ -301,8 +337,10 @@ __device__ __forceinline__ RowSpan row_span(const void* row, int64_t V) {
 }
 
 inline int launch_status() {
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
+  const cudaError_t k = launch_error();
+  launch_error() = cudaSuccess;
+  return (e == cudaSuccess && k == cudaSuccess) ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

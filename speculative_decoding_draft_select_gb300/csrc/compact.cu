@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kIndexThreads)
                          int32_t* req_to_token, int64_t max_ctx, int32_t* move_src, int32_t* move_dst,
                          int32_t* num_moves, int32_t* freed, int32_t* num_freed, int32_t* new_kv_len,
                          int32_t* stats) {
+  pdl_enter();
   __shared__ int scan_sh[33];
   __shared__ int running;
   if (threadIdx.x == 0) running = 0;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     compact_payload_kernel(int N, const int32_t* __restrict__ move_src, const int32_t* __restrict__ move_dst,
                            const int32_t* __restrict__ num_moves, uint8_t* kv, int64_t num_slots,
                            int64_t bps, int32_t* stats) {
+  pdl_enter();
   const int b = blockIdx.x;
   const int nm = num_moves[b];
   const bool vec = (bps & 15) == 0 && (reinterpret_cast<uintptr_t>(kv) & 15) == 0;
@@ -186,13 +188,11 @@ extern "C" int spec_compact_slots(int B, int N, int page_size, const int32_t* se
     return SPEC_ERR_INVALID_ARG;
   if (kv_pool_or_null && (num_slots < 1 || bytes_per_slot < 1)) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  compact_index_kernel<<<1, kIndexThreads, 0, s>>>(B, N, page_size, seq_lens, accept_path, accept_length,
-                                                   req_to_token, max_ctx, move_src, move_dst, num_moves, freed,
-                                                   num_freed, new_kv_len, stats_or_null);
+  launch_k(compact_index_kernel, 1, kIndexThreads, 0, s, B, N, page_size, seq_lens, accept_path, accept_length,
+           req_to_token, max_ctx, move_src, move_dst, num_moves, freed, num_freed, new_kv_len, stats_or_null);
   int e = launch_status();
   if (e != SPEC_OK || B == 0 || !kv_pool_or_null || page_size == 1) return e;
-  compact_payload_kernel<<<B, kCopyThreads, 0, s>>>(N, move_src, move_dst, num_moves,
-                                                    static_cast<uint8_t*>(kv_pool_or_null), num_slots,
-                                                    bytes_per_slot, stats_or_null);
+  launch_k(compact_payload_kernel, B, kCopyThreads, 0, s, N, move_src, move_dst, num_moves,
+           static_cast<uint8_t*>(kv_pool_or_null), num_slots, bytes_per_slot, stats_or_null);
   return launch_status();
 }

@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats) {
+  pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = THREADS / 32;
   extern __shared__ __align__(16) unsigned char dsm[];  // K > 1: candidate buffer
@@ -599,6 +600,7 @@ __global__ void __launch_bounds__(kSampleThreads)
     sample_kernel(const void* __restrict__ logits, const float* __restrict__ probs, int64_t V,
                   float c, const float* __restrict__ u, int32_t* __restrict__ out_token,
                   float* __restrict__ out_prob, const float* __restrict__ row_stats, int32_t* __restrict__ stats) {
+  pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   extern __shared__ float dyn[];
   __shared__ float scan_sh[33];
@@ -665,6 +667,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
     softmax_sample_kernel(const void* __restrict__ logits, int64_t V64, float c, const float* __restrict__ u,
                           int32_t* __restrict__ out_token, float* __restrict__ out_prob,
                           float* __restrict__ row_stats, float* __restrict__ probs, int32_t* __restrict__ stats) {
+  pdl_enter();
   constexpr int T = kFusedThreads, U = kFusedRounds, kv = Logit<DT>::kVec, kWarps = T / 32;
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   extern __shared__ float part[];  // [ntiles][T]: log2 of the partials plus the max they are relative to
@@ -934,8 +937,8 @@ int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, int
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  softmax_topk_kernel<DT, K, THREADS><<<static_cast<unsigned>(R), THREADS, smem, s>>>(
-      logits, V, c, k, topk_p, topk_idx, probs, row_stats, stats);
+  launch_k(softmax_topk_kernel<DT, K, THREADS>, static_cast<unsigned>(R), THREADS, smem, s, logits, V, c, k, topk_p,
+           topk_idx, probs, row_stats, stats);
   return launch_status();
 }
 
@@ -1007,16 +1010,15 @@ extern "C" int spec_softmax_sample(const void* logits, int dtype, int64_t R, int
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem)) != cudaSuccess)
       return SPEC_ERR_CUDA;
-    softmax_sample_kernel<SPEC_BF16><<<grid, kFusedThreads, smem, s>>>(logits, V, c, u, out_token, out_prob_or_null,
-                                                                      row_stats_or_null, probs_or_null,
-                                                                      stats_or_null);
+    launch_k(softmax_sample_kernel<SPEC_BF16>, grid, kFusedThreads, smem, s, logits, V, c, u, out_token,
+             out_prob_or_null, row_stats_or_null, probs_or_null, stats_or_null);
   } else {
     if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_sample_kernel<SPEC_F32>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem)) != cudaSuccess)
       return SPEC_ERR_CUDA;
-    softmax_sample_kernel<SPEC_F32><<<grid, kFusedThreads, smem, s>>>(logits, V, c, u, out_token, out_prob_or_null,
-                                                                     row_stats_or_null, probs_or_null, stats_or_null);
+    launch_k(softmax_sample_kernel<SPEC_F32>, grid, kFusedThreads, smem, s, logits, V, c, u, out_token,
+             out_prob_or_null, row_stats_or_null, probs_or_null, stats_or_null);
   }
   return launch_status();
 }
@@ -1041,15 +1043,13 @@ extern "C" int spec_sample(const void* logits_or_null, int dtype, const float* p
     cudaFuncSetAttribute(sample_kernel<SPEC_BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   }
   if (probs_or_null)
-    sample_kernel<SPEC_F32, true><<<grid, kSampleThreads, smem, s>>>(nullptr, probs_or_null, V, c, u, out_token,
-                                                                     out_prob_or_null, nullptr, stats_or_null);
+    launch_k(sample_kernel<SPEC_F32, true>, grid, kSampleThreads, smem, s, nullptr, probs_or_null, V, c, u, out_token,
+             out_prob_or_null, nullptr, stats_or_null);
   else if (dtype == SPEC_BF16)
-    sample_kernel<SPEC_BF16, false><<<grid, kSampleThreads, smem, s>>>(logits_or_null, nullptr, V, c, u, out_token,
-                                                                       out_prob_or_null, row_stats_or_null,
-                                                                       stats_or_null);
+    launch_k(sample_kernel<SPEC_BF16, false>, grid, kSampleThreads, smem, s, logits_or_null, nullptr, V, c, u,
+             out_token, out_prob_or_null, row_stats_or_null, stats_or_null);
   else
-    sample_kernel<SPEC_F32, false><<<grid, kSampleThreads, smem, s>>>(logits_or_null, nullptr, V, c, u, out_token,
-                                                                      out_prob_or_null, row_stats_or_null,
-                                                                      stats_or_null);
+    launch_k(sample_kernel<SPEC_F32, false>, grid, kSampleThreads, smem, s, logits_or_null, nullptr, V, c, u,
+             out_token, out_prob_or_null, row_stats_or_null, stats_or_null);
   return launch_status();
 }

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kTliThreads)
                          const int32_t* __restrict__ t2d, float c, int32_t* __restrict__ top1_draft,
                          int32_t* __restrict__ top1_target, float* __restrict__ top1_p, float* __restrict__ q,
                          int32_t* __restrict__ stats) {
+  pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kTliThreads / 32;
   __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
@@ -179,8 +180,9 @@ __global__ void __launch_bounds__(kTliThreads)
   }
   for (; i < nv; i += kTliThreads) {
     const int4 d = __ldg(reinterpret_cast<const int4*>(t2d) + i);
-    st_stream(out + 4 * i, make_float4(q_of<DT>(row, d.x, Vd, ok, c, mc, invz), q_of<DT>(row, d.y, Vd, ok, c, mc, invz),
-                                       q_of<DT>(row, d.z, Vd, ok, c, mc, invz), q_of<DT>(row, d.w, Vd, ok, c, mc, invz)));
+    st_stream(out + 4 * i,
+              make_float4(q_of<DT>(row, d.x, Vd, ok, c, mc, invz), q_of<DT>(row, d.y, Vd, ok, c, mc, invz),
+                          q_of<DT>(row, d.z, Vd, ok, c, mc, invz), q_of<DT>(row, d.w, Vd, ok, c, mc, invz)));
   }
   for (int64_t t = static_cast<int64_t>(nv) * 4 + threadIdx.x; t < Vt; t += kTliThreads)
     out[t] = q_of<DT>(row, __ldg(t2d + t), Vd, ok, c, mc, invz);
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kTliThreads)
 
 __global__ void map_ids_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out, int64_t n,
                                const int32_t* __restrict__ table, int64_t table_len, int32_t fallback) {
+  pdl_enter();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t x = __ldg(in + i);
@@ -219,13 +222,11 @@ extern "C" int tli_constrain_map(int64_t R, int64_t V_d, int64_t V_t, const void
   const float c = kLog2e / T;
   const unsigned grid = static_cast<unsigned>(R);
   if (dtype == SPEC_BF16)
-    tli_constrain_kernel<SPEC_BF16><<<grid, kTliThreads, 0, s>>>(V_d, V_t, draft_logits, d2t, t2d_or_null, c,
-                                                                 top1_draft, top1_target, top1_p,
-                                                                 q_target_or_null, stats_or_null);
+    launch_k(tli_constrain_kernel<SPEC_BF16>, grid, kTliThreads, 0, s, V_d, V_t, draft_logits, d2t, t2d_or_null, c,
+             top1_draft, top1_target, top1_p, q_target_or_null, stats_or_null);
   else
-    tli_constrain_kernel<SPEC_F32><<<grid, kTliThreads, 0, s>>>(V_d, V_t, draft_logits, d2t, t2d_or_null, c,
-                                                                top1_draft, top1_target, top1_p,
-                                                                q_target_or_null, stats_or_null);
+    launch_k(tli_constrain_kernel<SPEC_F32>, grid, kTliThreads, 0, s, V_d, V_t, draft_logits, d2t, t2d_or_null, c,
+             top1_draft, top1_target, top1_p, q_target_or_null, stats_or_null);
   return launch_status();
 }
 
@@ -236,8 +237,9 @@ extern "C" int tli_map_ids(const int32_t* in, int32_t* out, int64_t n, const int
   if (!in || !out || (!table && table_len > 0)) return SPEC_ERR_INVALID_ARG;
   const int threads = 256;
   const int64_t blocks = (n + threads - 1) / threads;
-  map_ids_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), threads, 0,
-                   reinterpret_cast<cudaStream_t>(stream)>>>(in, out, n, table, table_len, fallback_id);
+  const unsigned grid = static_cast<unsigned>(blocks < 4096 ? blocks : 4096);
+  launch_k(map_ids_kernel, grid, threads, 0, reinterpret_cast<cudaStream_t>(stream), in, out, n, table, table_len,
+           fallback_id);
   return launch_status();
 }
 

@@ -34,6 +34,7 @@ __global__ void tree_expand_kernel(int step, int num_steps, int B, int k, int64_
                                    const int32_t* __restrict__ topk_idx, float* pool_score,
                                    int32_t* pool_token, int32_t* pool_parent, int32_t* pool_qrow,
                                    float* frontier_score, int32_t* frontier_id) {
+  pdl_enter();
   extern __shared__ uint64_t keys[];
   const int b = blockIdx.x;
   const int nc = step == 0 ? k : k * k;
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(kBuildThreads)
                       const int32_t* __restrict__ seq_lens, int32_t* draft_token, int32_t* parent,
                       int32_t* positions, uint8_t* tree_mask, int32_t* retrieve_index,
                       int32_t* next_token, int32_t* next_sibling, int32_t* q_row) {
+  pdl_enter();
   extern __shared__ uint64_t dyn[];
   uint64_t* keys = dyn;                                       // [L]
   int32_t* node_of = reinterpret_cast<int32_t*>(keys + L);    // [P]
@@ -271,9 +273,9 @@ extern "C" int spec_tree_expand(int step, int num_steps, int B, int k, const flo
   if (static_cast<int64_t>(B) * k * num_steps > INT_MAX) return SPEC_ERR_UNSUPPORTED;
   const int nc = step == 0 ? k : k * k;
   const int threads = ((nc + 31) / 32) * 32;
-  tree_expand_kernel<<<B, threads, sizeof(uint64_t) * nc, reinterpret_cast<cudaStream_t>(stream)>>>(
-      step, num_steps, B, k, P, topk_p, topk_idx, pool_score, pool_token, pool_parent, pool_qrow,
-      frontier_score, frontier_id);
+  launch_k(tree_expand_kernel, B, threads, sizeof(uint64_t) * nc, reinterpret_cast<cudaStream_t>(stream), step,
+           num_steps, B, k, P, topk_p, topk_idx, pool_score, pool_token, pool_parent, pool_qrow, frontier_score,
+           frontier_id);
   return launch_status();
 }
 
@@ -300,8 +302,8 @@ extern "C" int spec_build_tree(int B, int k, int num_steps, int N, const float* 
                              static_cast<int>(smem)) != cudaSuccess)
       return SPEC_ERR_CUDA;
   }
-  build_tree_kernel<<<B, kBuildThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      N, P, L, pool_score, pool_token, pool_parent, pool_qrow, root_token, seq_lens, draft_token, parent,
-      positions, tree_mask, retrieve_index, retrieve_next_token, retrieve_next_sibling, q_row);
+  launch_k(build_tree_kernel, B, kBuildThreads, smem, reinterpret_cast<cudaStream_t>(stream), N, P, L, pool_score,
+           pool_token, pool_parent, pool_qrow, root_token, seq_lens, draft_token, parent, positions, tree_mask,
+           retrieve_index, retrieve_next_token, retrieve_next_sibling, q_row);
   return launch_status();
 }

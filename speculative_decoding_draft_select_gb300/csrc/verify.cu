@@ -147,6 +147,7 @@ template <int DT, bool STOCH>
 __global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
     row_stats_kernel(const void* __restrict__ logits, int64_t V, float c, int32_t* __restrict__ amax,
                      float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
+  pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kStatThreads / 32;
   __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
@@ -209,7 +210,8 @@ __global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
 template <int DT, bool STOCH>
 int launch_row_stats(const void* logits, int64_t V, int64_t R, float c, int32_t* amax, float* m, float* z,
                      int32_t* stats, cudaStream_t s) {
-  row_stats_kernel<DT, STOCH><<<static_cast<unsigned>(R), kStatThreads, 0, s>>>(logits, V, c, amax, m, z, stats);
+  launch_k(row_stats_kernel<DT, STOCH>, static_cast<unsigned>(R), kStatThreads, 0, s, logits, V, c, amax, m, z,
+           stats);
   return launch_status();
 }
 
@@ -220,6 +222,7 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
                                    const int32_t* __restrict__ budget, int32_t eos, int32_t* committed,
                                    int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
                                    int32_t* next_root, int32_t* walk_info) {
+  pdl_enter();
   extern __shared__ int32_t sh[];
   int32_t *s_am = sh, *s_dt = sh + N, *s_nt = sh + 2 * N, *s_ns = sh + 3 * N, *s_com = sh + 4 * N,
           *s_path = sh + 5 * N;
@@ -544,6 +547,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
                        const int32_t* __restrict__ budget, int32_t eos, int32_t* committed,
                        int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
                        int32_t* next_root, int32_t* walk_info, int32_t* stats) {
+  pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   using Weights = ResidualWeights<DT, typename QSrc::Row>;
   constexpr int kChunks = Weights::template chunks<kWalkElems>();
@@ -779,9 +783,9 @@ extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void
               : launch_row_stats<SPEC_F32, false>(target_logits, V, rows, 0.0f, w.amax, nullptr, nullptr,
                                                   stats_or_null, s);
   if (e != SPEC_OK) return e;
-  greedy_walk_kernel<<<B, 32, sizeof(int32_t) * 6 * N, s>>>(
-      N, w.amax, draft_token, retrieve_next_token, retrieve_next_sibling, budget_or_null, eos_id, committed,
-      num_committed, accept_length, accept_path, next_root, walk_info_or_null);
+  launch_k(greedy_walk_kernel, B, 32, sizeof(int32_t) * 6 * N, s, N, w.amax, draft_token, retrieve_next_token,
+           retrieve_next_sibling, budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
+           next_root, walk_info_or_null);
   return launch_status();
 }
 
@@ -810,10 +814,9 @@ int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, Q
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  sample_walk_kernel<DT, QSrc><<<B * kWalkCluster, kWalkThreads, smem, s>>>(N, V, c, target, w.m, w.z, qsrc, q_row, dtok, ntok,
-                                                             nsib, coins, u_final, budget, eos, committed,
-                                                             num_committed, accept_length, accept_path, next_root,
-                                                             walk_info, stats);
+  launch_k(sample_walk_kernel<DT, QSrc>, B * kWalkCluster, kWalkThreads, smem, s, N, V, c, target, w.m, w.z, qsrc,
+           q_row, dtok, ntok, nsib, coins, u_final, budget, eos, committed, num_committed, accept_length, accept_path,
+           next_root, walk_info, stats);
   return launch_status();
 }
 
@@ -964,8 +967,8 @@ extern "C" int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, co
               : launch_row_stats<SPEC_F32, false>(target_logits, V, rows, 0.0f, amax, nullptr, nullptr,
                                                   stats_or_null, s);
   if (e != SPEC_OK) return e;
-  greedy_walk_kernel<<<B, 32, sizeof(int32_t) * 6 * N, s>>>(
-      N, amax, draft_token, retrieve_next_token, retrieve_next_sibling, budget_or_null, eos_id, committed,
-      num_committed, accept_length, accept_path, next_root, walk_info_or_null);
+  launch_k(greedy_walk_kernel, B, 32, sizeof(int32_t) * 6 * N, s, N, amax, draft_token, retrieve_next_token,
+           retrieve_next_sibling, budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
+           next_root, walk_info_or_null);
   return launch_status();
 }
