@@ -273,7 +273,7 @@ def run_ours(args, cfg, mode, rank, world):
     # dominant kernel: the draft-step softmax/top-k (or TLI constrain) launches
     if cfg.kind == "tli":
         per_row = cfg.V * 2 + (cfg.V_t * 4 if mode == "sample" else 0)
-        kname = "tli_constrain_kernel"
+        kname = "tli_planned_kernel"
     else:
         per_row = row_bytes + (cfg.V * 4 if buf.q is not None else 0)  # read + written q
         kname = "softmax_sample_kernel" if (cfg.kind == "chain" and mode == "sample") else DOMINANT

@@ -355,6 +355,36 @@ int tli_constrain_map(int64_t R, int64_t V_d, int64_t V_t, const void* draft_log
                       int32_t* top1_draft, int32_t* top1_target, float* top1_p,
                       float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream);
 
+/* Map plan of a vocabulary pair ([TLI] Modifications: vocab_mapping.py
+ * builds the id maps once per model pair).  The plan is derived from d2t and
+ * t2d alone and lets tli_constrain_map_planned keep the intersection in
+ * shared memory:
+ *   int32 K (the number of ids with d2t >= 0) and 3 pad words;
+ *   uint2 mw[Wp], Wp = ceil(V_d / 32) rounded up to even: .x bit j set when
+ *     d2t[32 w + j] >= 0, .y the number of set bits in words before w;
+ *   int32 t2r[V_t rounded up to 4]: for target id t with d = t2d[t],
+ *     0 <= d < V_d and d in the intersection: the rank of d among the
+ *     intersection ids in increasing id order; -1 when t2d[t] < 0 or
+ *     d >= V_d (and for the pad entries); -2 - d when d is outside the
+ *     intersection.
+ * tli_plan_bytes: its size in bytes (-1 for sizes out of range).
+ * tli_plan_build: fills `plan` (device, 16-byte aligned, caller-owned,
+ * tli_plan_bytes(V_d, V_t) bytes) from d2t [V_d] and t2d [V_t], in stream
+ * order (three launches). */
+int64_t tli_plan_bytes(int64_t V_d, int64_t V_t);
+int tli_plan_build(int64_t V_d, int64_t V_t, const int32_t* d2t, const int32_t* t2d, void* plan,
+                   spec_stream_t stream);
+
+/* tli_constrain_map with a plan built by tli_plan_build from the same d2t
+ * and t2d (the outputs are the same).  Persistent CTAs keep the plan's
+ * bitmap and, when they fit, the row's intersection logits in shared
+ * memory; a draft vocabulary whose bitmap does not fit falls back to
+ * tli_constrain_map. */
+int tli_constrain_map_planned(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                              const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
+                              int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                              float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream);
+
 /* Id remapping in either direction ([TLI] Modifications:
  * map_target_to_draft_ids / map_draft_to_target_ids): out[i] = table[in[i]]
  * when 0 <= in[i] < table_len and that entry is >= 0, else fallback_id (the

@@ -268,6 +268,24 @@ def tli_constrain_map(draft_logits, d2t, t2d, T: float, want_q: bool = False):
     return o
 
 
+def tli_plan(d2t, t2d):
+    """The TLI map plan of (d2t, t2d): K, bitmap words, intersection ids
+    before each word, each target's partner rank (layout of tli_plan_build;
+    words = ceil(V_d / 32) rounded up to even, t2r padded to a multiple of 4)."""
+    d2 = _c(d2t, np.int32)
+    t2 = _c(t2d, np.int32)
+    Vd, Vt = d2.size, t2.size
+    words = (Vd + 31) // 32
+    words += words & 1
+    Vt4 = (Vt + 3) // 4 * 4
+    o = {"K": np.zeros(1, np.int32), "bits": np.zeros(words, np.uint32), "before": np.zeros(words, np.uint32),
+         "t2r": np.zeros(Vt4, np.int32)}
+    rc = lib().oracle_tli_plan(ctypes.c_int64(Vd), ctypes.c_int64(Vt), _p(d2), _p(t2), _p(o["K"]), _p(o["bits"]),
+                               _p(o["before"]), ctypes.c_int64(words), _p(o["t2r"]), ctypes.c_int64(Vt4))
+    _check(rc, "tli_plan")
+    return o
+
+
 def map_ids(ids, table, fallback: int):
     a = _c(ids, np.int32)
     t = _c(table, np.int32)

@@ -703,6 +703,49 @@ int oracle_tli_constrain_map(int64_t R, int64_t Vd, int64_t Vt, const void* draf
     return OR_OK;
 }
 
+/* The map plan of a vocabulary pair, written out from its definition (the
+ * layout that tli_plan_build fills; [TLI] "Modifications": vocab_mapping.py
+ * builds the id maps once per model pair, and the plan restates them):
+ * K = number of draft ids with d2t >= 0; for word w of 32 draft ids, bits[w]
+ * (bit j set when 32 w + j < Vd and d2t[32 w + j] >= 0) and before[w] (the
+ * intersection ids in earlier words); for target id t < Vt4 (Vt rounded up
+ * to 4) with d = t2d[t] (-1 past Vt): t2r[t] = the number of intersection
+ * ids below d when d is one, -2 - d when 0 <= d < Vd is not one, else -1. */
+int oracle_tli_plan(int64_t Vd, int64_t Vt, const int32_t* d2t, const int32_t* t2d,
+                    int32_t* K, uint32_t* bits, uint32_t* before, int64_t words,
+                    int32_t* t2r, int64_t Vt4)
+{
+    if (Vd < 1 || Vt < 1 || words * 32 < Vd || Vt4 < Vt) return OR_ERR;
+    int32_t* below = (int32_t*)malloc(sizeof(int32_t) * (size_t)Vd);
+    if (!below) return OR_ERR;
+    int32_t k = 0;
+    for (int64_t v = 0; v < Vd; ++v) {
+        below[v] = k;
+        if (d2t[v] >= 0) ++k;
+    }
+    *K = k;
+    int32_t seen = 0;
+    for (int64_t w = 0; w < words; ++w) {
+        bits[w] = 0u;
+        before[w] = (uint32_t)seen;
+        for (int j = 0; j < 32; ++j) {
+            int64_t v = 32 * w + j;
+            if (v < Vd && d2t[v] >= 0) {
+                bits[w] |= 1u << j;
+                ++seen;
+            }
+        }
+    }
+    for (int64_t t = 0; t < Vt4; ++t) {
+        int32_t d = t < Vt ? t2d[t] : -1;
+        if (d < 0 || d >= Vd) t2r[t] = -1;
+        else if (d2t[d] >= 0) t2r[t] = below[d];
+        else t2r[t] = -2 - d;
+    }
+    free(below);
+    return OR_OK;
+}
+
 /* [TLI] "Modifications": map_target_to_draft_ids / map_draft_to_target_ids;
  * ids outside the table or without a partner map to the fallback id (the
  * unk id, or eos where a model has no unk). */

@@ -19,7 +19,8 @@ __all__ = [
     "spec_softmax_topk", "spec_softmax_sample", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
     "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
     "spec_verify_sample_qlogits", "spec_compact_freed_capacity",
-    "spec_compact_slots", "tli_constrain_map", "tli_map_ids", "tli_check_config",
+    "spec_compact_slots", "tli_constrain_map", "tli_plan_bytes", "tli_plan_build", "tli_map_ids",
+    "tli_check_config",
     "new_stats", "new_pool",
 ]
 
@@ -58,6 +59,9 @@ _SIGS = {
     "spec_compact_slots": (_I, [_I, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, _I64,
                                 _I64, _P, _P]),
     "tli_constrain_map": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _F, _P, _P, _P, _P, _P, _P]),
+    "tli_plan_bytes": (_I64, [_I64, _I64]),
+    "tli_plan_build": (_I, [_I64, _I64, _P, _P, _P, _P]),
+    "tli_constrain_map_planned": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P]),
     "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P]),
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
@@ -399,8 +403,29 @@ def spec_compact_slots(seq_lens, accept_path, accept_length, req_to_token, page_
 
 # --------------------------------------------------------------------- TLI
 
+def tli_plan_bytes(Vd, Vt) -> int:
+    n = lib().tli_plan_bytes(int(Vd), int(Vt))
+    if n < 0:
+        raise SpecError("tli_plan_bytes", -2)
+    return n
+
+
+def tli_plan_build(d2t, t2d, plan=None):
+    """The map plan of (d2t, t2d) as a uint8 device tensor (see
+    tli_plan_build in include/specdec.h)."""
+    _dev(d2t, torch.int32, "d2t")
+    _dev(t2d, torch.int32, "t2d")
+    n = tli_plan_bytes(d2t.numel(), t2d.numel())
+    if plan is None:
+        plan = torch.empty(n, dtype=torch.uint8, device=d2t.device)
+    elif plan.numel() < n or plan.dtype != torch.uint8 or not plan.is_cuda or plan.data_ptr() % 16:
+        raise ValueError(f"plan must be a 16-byte aligned uint8 device tensor of >= {n} bytes")
+    _call("tli_plan_build", d2t.numel(), t2d.numel(), _ptr(d2t), _ptr(t2d), _ptr(plan), _stream())
+    return plan
+
+
 def tli_constrain_map(draft_logits, d2t, T, t2d=None, want_q=False, top1_draft=None, top1_target=None,
-                      top1_p=None, q_target=None, stats=None):
+                      top1_p=None, q_target=None, stats=None, plan=None):
     _dev(draft_logits, name="draft_logits")
     _dev(d2t, torch.int32, "d2t")
     _dev(t2d, torch.int32, "t2d")
@@ -416,8 +441,16 @@ def tli_constrain_map(draft_logits, d2t, T, t2d=None, want_q=False, top1_draft=N
         q_target = torch.empty((R, Vt), dtype=torch.float32, device=draft_logits.device)
     _dev(q_target, torch.float32, "q_target")
     _dev(stats, torch.int32, "stats")
-    _call("tli_constrain_map", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t), _ptr(t2d),
-          float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target), _ptr(stats), _stream())
+    if plan is not None:
+        if plan.dtype != torch.uint8 or not plan.is_cuda or plan.numel() < tli_plan_bytes(Vd, Vt):
+            raise ValueError("plan must come from tli_plan_build for these vocabulary sizes")
+        _call("tli_constrain_map_planned", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t),
+              _ptr(t2d), _ptr(plan), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target),
+              _ptr(stats), _stream())
+    else:
+        _call("tli_constrain_map", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t),
+              _ptr(t2d), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target),
+              _ptr(stats), _stream())
     return top1_draft, top1_target, top1_p, q_target
 
 

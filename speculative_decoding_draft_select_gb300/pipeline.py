@@ -9,8 +9,10 @@ EAGLE" sections 2-3 and "EAGLE speculative decoding in four parts",
   - sampled chain: spec_softmax_sample (q or its row statistics, and the
                  draw with the step's uniforms, in one pass), then
                  spec_tree_expand with k = 1;
-  - TLI chain:   tli_constrain_map (q in target order), then
-                 spec_tree_expand with the mapped top-1 (SGLang PR #22883).
+  - TLI chain:   tli_plan_build once per step (the vocabulary maps'
+                 plan), then per draft step tli_constrain_map with it (q in
+                 target order) and spec_tree_expand with the mapped top-1
+                 (SGLang PR #22883).
 then spec_build_tree.  Verify: spec_verify_greedy, or for sampling either
 spec_verify_sample on the written q table (q_mode "probs") or
 spec_verify_sample_qlogits on the draft logits plus the per-row (max,
@@ -28,7 +30,7 @@ import torch
 
 from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity, spec_compact_slots,
                spec_softmax_sample, spec_softmax_topk, spec_tree_expand, spec_verify_greedy, spec_verify_sample,
-               spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map)
+               spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map, tli_plan_build, tli_plan_bytes)
 
 
 def step_offsets(B, topk, steps):
@@ -68,6 +70,8 @@ class StepBuffers:
         self.tok = torch.empty((self.rows,), dtype=torch.int32, device=dev)
         self.prob = torch.empty((self.rows,), dtype=torch.float32, device=dev)
         self.top1_draft = torch.empty((self.rows,), dtype=torch.int32, device=dev)
+        self.tli_plan = (torch.empty(tli_plan_bytes(V, V_t), dtype=torch.uint8, device=dev)
+                         if kind == "tli" else None)
         self.tree = None
         self.ws = torch.empty(max(spec_verify_ws_size(B, N), 256), dtype=torch.uint8, device=dev)
         self.verify_out = None
@@ -107,6 +111,8 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
     launch."""
     B, k = buf.B, buf.topk
     buf.draft_table, buf.T_draft = draft_table, T
+    if buf.kind == "tli":
+        tli_plan_build(d2t, t2d, plan=buf.tli_plan)
     for s in range(buf.steps):
         r = B * (1 if s == 0 else k)
         a = buf.offs[s]
@@ -118,7 +124,7 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
         if buf.kind == "tli":
             tli_constrain_map(rows, d2t, T, t2d=t2d, top1_draft=buf.top1_draft[a:a + r],
                               top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
-                              stats=buf.stats)
+                              stats=buf.stats, plan=buf.tli_plan)
             if timer is not None:
                 timer.end(s)
             spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
@@ -182,6 +188,8 @@ def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> in
     """Number of kernel launches one step enqueues."""
     per_step = 2  # softmax/top-k (or softmax and draw, or TLI constrain) + tree expand
     n = buf.steps * per_step + 1  # + build_tree
+    if buf.kind == "tli":
+        n += 3  # the map plan
     n += 2  # verify: row pass + walk
     if compact:
         n += 1 + (1 if (kv_pool and buf.compact_out is not None) else 0)

@@ -63,6 +63,14 @@ def test_host_side_argument_checks(lib):
                                   null) == -1
     assert lib.tli_constrain_map(4, 10, 10, null, 1, null, null, 1.0, null, null, null, null, null, null) == -1
     assert lib.tli_map_ids(null, null, -1, null, 0, 0, null) == -1
+    # plan: missing or misaligned buffers, planned constrain without a plan
+    assert lib.tli_plan_build(10, 10, null, null, null, null) == -1
+    assert lib.tli_plan_build(10, 10, p16, p16, ctypes.c_void_p(24), null) == -1
+    assert lib.tli_plan_build(1 << 23, 10, p16, p16, p16, null) == -2
+    assert lib.tli_constrain_map_planned(4, 10, 10, p16, 1, p16, p16, null, 1.0, p16, p16, p16, null, null,
+                                         null) == -1
+    assert lib.tli_constrain_map_planned(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
+                                         null) == 0
 
 
 def test_sizes_and_config_check(lib):
@@ -71,6 +79,9 @@ def test_sizes_and_config_check(lib):
     assert sd.spec_verify_ws_size(128, 64) >= 128 * 64 * 12
     assert sd.spec_compact_freed_capacity(128, 64, 16) == 128 * 5
     assert sd.spec_compact_freed_capacity(4, 16, 1) == 60
+    # plan: 16-byte header, 8 bytes per bitmap word (count rounded up to even), 4 per target (to 4)
+    assert sd.tli_plan_bytes(151936, 128256) == 16 + 8 * 4748 + 4 * 128256
+    assert sd.tli_plan_bytes(33, 5) == 16 + 8 * 2 + 4 * 8
     assert sd.tli_check_config(1, 4, 5)
     assert not sd.tli_check_config(2, 4, 5)
     assert not sd.tli_check_config(1, 4, 4)

@@ -486,9 +486,17 @@ def test_compact_parity(ps, with_kv):
 
 # --------------------------------------------------------------------- TLI
 
-@pytest.mark.parametrize("Vd,Vt,K,dtype", [(4097, 3001, 1500, torch.bfloat16), (151936, 128256, 60000, torch.bfloat16),
-                                           (37, 29, 11, torch.float32)])
-def test_tli_parity(Vd, Vt, K, dtype):
+# Cases: the resident-bitmap kernel with the intersection logits in shared
+# memory (bf16), with more rows than CTAs (each CTA walks several rows), with
+# fp32 logits too many to hold (gathers from the row), and a draft
+# vocabulary too large for the bitmap (one CTA per row, mask from d2t).
+@pytest.mark.parametrize("Vd,Vt,K,dtype,R", [(4097, 3001, 1500, torch.bfloat16, 24),
+                                             (151936, 128256, 60000, torch.bfloat16, 200),
+                                             (37, 29, 11, torch.float32, 24),
+                                             (4101, 999, 700, torch.bfloat16, 700),
+                                             (151936, 128256, 60000, torch.float32, 24),
+                                             (1000003, 50000, 30000, torch.bfloat16, 6)])
+def test_tli_parity(Vd, Vt, K, dtype, R):
     rng = np.random.default_rng(Vd)
     dids = np.sort(rng.choice(Vd, K, replace=False))
     tids = rng.choice(Vt, K, replace=False)
@@ -496,24 +504,82 @@ def test_tli_parity(Vd, Vt, K, dtype):
     d2t[dids] = tids
     t2d = np.full(Vt, -1, np.int32)
     t2d[tids] = dids
-    R = 24
     x = make_logits(rng, R, Vd, dtype)
     x[3, torch.from_numpy(dids)] = float("-inf")  # empty after masking
     x[4, int(dids[2])] = x[4, int(dids[5])] = 40.0  # tie inside the intersection
-    stats = sd.new_stats()
-    td, tt, tp, qt = sd.tli_constrain_map(dev(x), dev(d2t), 0.9, t2d=dev(t2d), want_q=True, stats=stats)
-    torch.cuda.synchronize()
     o = oracle.tli_constrain_map(np_logits(x), d2t, t2d, 0.9, want_q=True)
-    np.testing.assert_array_equal(td.cpu().numpy(), o["top1_draft"])
-    np.testing.assert_array_equal(tt.cpu().numpy(), o["top1_target"])
-    np.testing.assert_allclose(tp.cpu().numpy(), o["top1_p"], atol=PROB_TOL)
-    np.testing.assert_allclose(qt.cpu().numpy(), o["q_target"], atol=PROB_TOL)
-    assert int(stats[sd.STATS["empty_intersection"]]) == int(o["row_flag"].sum()) == 1
+    plan = sd.tli_plan_build(dev(d2t), dev(t2d))
+    for p in (None, plan):
+        stats = sd.new_stats()
+        td, tt, tp, qt = sd.tli_constrain_map(dev(x), dev(d2t), 0.9, t2d=dev(t2d), want_q=True, stats=stats, plan=p)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(td.cpu().numpy(), o["top1_draft"])
+        np.testing.assert_array_equal(tt.cpu().numpy(), o["top1_target"])
+        np.testing.assert_allclose(tp.cpu().numpy(), o["top1_p"], atol=PROB_TOL)
+        np.testing.assert_allclose(qt.cpu().numpy(), o["q_target"], atol=PROB_TOL)
+        assert int(stats[sd.STATS["empty_intersection"]]) == int(o["row_flag"].sum()) == 1
+        # without q the top-1 outputs are the same
+        td2, tt2, tp2, _ = sd.tli_constrain_map(dev(x), dev(d2t), 0.9, t2d=dev(t2d), plan=p)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(td2.cpu().numpy(), o["top1_draft"])
+        np.testing.assert_allclose(tp2.cpu().numpy(), o["top1_p"], atol=PROB_TOL)
     ids = np.concatenate([dids[:100], np.setdiff1d(np.arange(Vd), dids)[:50], [-3, Vd, Vd + 9]]).astype(np.int32)
     g = sd.tli_map_ids(dev(ids), dev(d2t), 7)
     np.testing.assert_array_equal(g.cpu().numpy(), oracle.map_ids(ids, d2t, 7))
     back = sd.tli_map_ids(sd.tli_map_ids(dev(dids.astype(np.int32)), dev(d2t), -1), dev(t2d), -1)
     np.testing.assert_array_equal(back.cpu().numpy(), dids)
+
+
+def test_tli_t2d_outside_intersection():
+    """A target id whose t2d entry names a draft id outside the intersection
+    reads that id's logit from the row (the map is taken as given); ids past
+    the draft vocabulary give 0."""
+    Vd, Vt, K, R = 5000, 3000, 1200, 8
+    rng = np.random.default_rng(5)
+    dids = np.sort(rng.choice(Vd, K, replace=False))
+    tids = rng.choice(Vt, K, replace=False)
+    d2t = np.full(Vd, -1, np.int32)
+    d2t[dids] = tids
+    t2d = np.full(Vt, -1, np.int32)
+    t2d[tids] = dids
+    outside = np.setdiff1d(np.arange(Vd), dids)[:5]
+    free_t = np.setdiff1d(np.arange(Vt), tids)[:6]
+    t2d[free_t[:5]] = outside
+    x = make_logits(rng, R, Vd, torch.bfloat16)
+    x[:, torch.from_numpy(outside)] = -2.0  # below the row's masked max: q stays below 1
+    o = oracle.tli_constrain_map(np_logits(x), d2t, t2d, 0.8, want_q=True)
+    t2d[free_t[5]] = Vd + 3  # past the vocabulary: 0 (the oracle row keeps 0 there)
+    for p in (None, sd.tli_plan_build(dev(d2t), dev(t2d))):
+        td, tt, tp, qt = sd.tli_constrain_map(dev(x), dev(d2t), 0.8, t2d=dev(t2d), want_q=True, plan=p)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(td.cpu().numpy(), o["top1_draft"])
+        np.testing.assert_allclose(qt.cpu().numpy(), o["q_target"], atol=PROB_TOL)
+    assert (o["q_target"][:, free_t[:5]] > 0).all()
+
+
+@pytest.mark.parametrize("Vd,Vt,K", [(151936, 128256, 60000), (33, 5, 3), (64, 64, 0), (100003, 7, 7)])
+def test_tli_plan_parity(Vd, Vt, K):
+    """The plan tli_plan_build writes equals the oracle's, word for word."""
+    rng = np.random.default_rng(K + Vd)
+    dids = np.sort(rng.choice(Vd, K, replace=False))
+    tids = rng.choice(Vt, K, replace=False)
+    d2t = np.full(Vd, -1, np.int32)
+    d2t[dids] = tids
+    t2d = np.full(Vt, -1, np.int32)
+    t2d[tids] = dids
+    free = np.setdiff1d(np.arange(Vt), tids)
+    if len(free) >= 2:
+        t2d[free[0]] = np.setdiff1d(np.arange(Vd), dids)[0]  # a partner outside the intersection
+        t2d[free[1]] = Vd  # past the vocabulary
+    o = oracle.tli_plan(d2t, t2d)
+    g = sd.tli_plan_build(dev(d2t), dev(t2d)).cpu().numpy()
+    words = len(o["bits"])
+    assert g.size == sd.tli_plan_bytes(Vd, Vt) == 16 + 8 * words + 4 * len(o["t2r"])
+    assert int(g[:4].view(np.int32)[0]) == int(o["K"][0])
+    mw = g[16:16 + 8 * words].view(np.uint32).reshape(words, 2)
+    np.testing.assert_array_equal(mw[:, 0], o["bits"])
+    np.testing.assert_array_equal(mw[:, 1], o["before"])
+    np.testing.assert_array_equal(g[16 + 8 * words:].view(np.int32), o["t2r"])
 
 
 # ------------------------------------------------------- toy LM end to end

@@ -637,6 +637,52 @@ def test_tli_random_maps_and_empty_intersection():
     assert (oracle.map_ids(np.array([-1, Vd, Vd + 5]), d2t, 42) == 42).all()
 
 
+def test_tli_plan_against_sorted_intersection():
+    """The plan's ranks are positions in the sorted intersection_draft_ids
+    (searchsorted), its bitmap reproduces the mask id by id, K is the
+    intersection size; partners outside the intersection or the vocabulary
+    and the padding take their codes."""
+    rng = np.random.default_rng(11)
+    for Vd, Vt, K in ((300, 203, 120), (64, 6, 5), (1000, 999, 0), (77, 77, 77)):
+        dids = np.sort(rng.choice(Vd, K, replace=False))
+        tids = rng.choice(Vt, K, replace=False) if K <= Vt else None
+        if tids is None:
+            continue
+        d2t = np.full(Vd, -1, np.int32)
+        d2t[dids] = tids
+        t2d = np.full(Vt, -1, np.int32)
+        t2d[tids] = dids
+        free = np.setdiff1d(np.arange(Vt), tids)
+        outside = np.setdiff1d(np.arange(Vd), dids)
+        planted = {}
+        if len(free) >= 2 and len(outside) >= 1:
+            t2d[free[0]] = outside[0]
+            t2d[free[1]] = Vd + 4
+            planted = {int(free[0]): -2 - int(outside[0]), int(free[1]): -1}
+        o = oracle.tli_plan(d2t, t2d)
+        assert int(o["K"][0]) == K
+        words = len(o["bits"])
+        assert words % 2 == 0 and words * 32 >= Vd > (words - 2) * 32
+        for v in range(words * 32):
+            bit = (int(o["bits"][v >> 5]) >> (v & 31)) & 1
+            assert bit == (1 if v < Vd and d2t[v] >= 0 else 0)
+        assert int(o["before"][0]) == 0
+        for w in range(1, words):
+            assert int(o["before"][w]) == int(o["before"][w - 1]) + bin(int(o["bits"][w - 1])).count("1")
+        assert len(o["t2r"]) == (Vt + 3) // 4 * 4
+        for t in range(len(o["t2r"])):
+            if t >= Vt:
+                expect = -1
+            elif t in planted:
+                expect = planted[t]
+            elif t2d[t] < 0:
+                expect = -1
+            else:
+                expect = int(np.searchsorted(dids, t2d[t]))
+                assert dids[expect] == t2d[t]
+            assert int(o["t2r"][t]) == expect
+
+
 def test_tli_config_constraints(golden):
     g = golden("tli_constraints.json")
     for c in g["valid"]:
