@@ -122,22 +122,44 @@ inline cudaError_t& launch_error() {
   return e;
 }
 
+// Launch configuration with programmatic stream serialization and, for
+// cluster > 1, a thread-block cluster of that many CTAs along x.
+struct LaunchCfg {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster = 1) {
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (cluster > 1) {
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
+  }
+  LaunchCfg(const LaunchCfg&) = delete;
+};
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             int cluster, Args&&... args) {
+  LaunchCfg lc(grid, block, smem, s, cluster);
+  const cudaError_t e = cudaLaunchKernelEx(&lc.cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) launch_error() = e;
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                             Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-  if (e != cudaSuccess) launch_error() = e;
-  return e;
+  return launch_kc(kernel, grid, block, smem, s, 1, std::forward<Args>(args)...);
 }
 
 // Thread-block clusters: this CTA's rank, a barrier over every thread of

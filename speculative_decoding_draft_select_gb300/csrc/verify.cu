@@ -37,15 +37,12 @@ namespace {
 #ifndef SPEC_WALK_THREADS
 #define SPEC_WALK_THREADS 128
 #endif
-#ifndef SPEC_WALK_CLUSTER
-#define SPEC_WALK_CLUSTER 4
-#endif
 #ifndef SPEC_WALK_ELEMS
 #define SPEC_WALK_ELEMS 16
 #endif
-// The stochastic walk: kWalkCluster CTAs of kWalkThreads threads per request.
+// The stochastic walk: a cluster of 1, 2 or 4 CTAs of kWalkThreads threads
+// per request.
 constexpr int kWalkThreads = SPEC_WALK_THREADS;
-constexpr int kWalkCluster = SPEC_WALK_CLUSTER;
 constexpr int kWalkElems = SPEC_WALK_ELEMS;  // consecutive elements per thread in a tile
 constexpr size_t kMaxDynSmem = 227 * 1024;  // opt-in shared memory of one CTA
 
@@ -537,8 +534,8 @@ struct ResidualWeights {
   }
 };
 
-template <int DT, class QSrc>
-__global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
+template <int DT, class QSrc, int C>
+__global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     sample_walk_kernel(int N, int64_t V, float c, const void* __restrict__ target,
                        const float* __restrict__ m_row, const float* __restrict__ z_row, QSrc qsrc,
                        const int32_t* __restrict__ q_row, const int32_t* __restrict__ dtok,
@@ -558,7 +555,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
   const int64_t ntiles = (V + kWalkThreads * kWalkElems - 1) / (kWalkThreads * kWalkElems);
   float* tile_sums = dyn;  // two buffers of ntiles, used by alternate passes
   float* part = tile_sums + 2 * ntiles;
-  float* g_l = part + static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, kWalkCluster>(V)) * kWalkThreads;
+  float* g_l = part + static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, C>(V)) * kWalkThreads;
   float* g_q = g_l + N;
   float* g_u = g_q + N;
   int32_t* s_dt = reinterpret_cast<int32_t*>(g_u + N);
@@ -572,19 +569,19 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
   __shared__ int64_t s_qrow;
   __shared__ float s_m, s_invz, s_nb, s_A, s_cj, s_total;
 
-  // the kWalkCluster CTAs of a cluster walk request b together: each pass
+  // the C CTAs of a cluster walk request b together: each pass
   // over a row is split between them, everything else is done by each CTA
   // on the same data, so all of them take the same decisions; rank 0 alone
   // counts anomalies and writes the outputs
-  const unsigned rank = kWalkCluster > 1 ? cluster_rank() : 0u;
-  const int b = blockIdx.x / kWalkCluster, tid = threadIdx.x;
+  const unsigned rank = C > 1 ? cluster_rank() : 0u;
+  const int b = blockIdx.x / C, tid = threadIdx.x;
   int32_t* const cstats = rank == 0 ? stats : nullptr;
   const int64_t o = static_cast<int64_t>(b) * N;
   int par = 0;  // tile-sum buffer of the next pass
   auto pass = [&](const Weights& w) -> float {
     float* ts = tile_sums + par * ntiles;
     par ^= 1;
-    return cdf_tile_pass_split<kWalkThreads, kWalkElems, kRing, kWalkCluster>(w, V, part, ts, ring, rank);
+    return cdf_tile_pass_split<kWalkThreads, kWalkElems, kRing, C>(w, V, part, ts, ring, rank);
   };
   for (int i = tid; i < N; i += kWalkThreads) {
     s_dt[i] = __ldg(dtok + o + i);
@@ -604,7 +601,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     s_path[0] = 0;
   }
   __syncthreads();
-  if (kWalkCluster > 1) cluster_barrier();  // every CTA of the cluster is running
+  if (C > 1) cluster_barrier();  // every CTA of the cluster is running
   const float cT = c;
   while (!s_done) {
     // enter node n: children in sibling order, row statistics, q row
@@ -700,7 +697,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     }
     __syncthreads();
   }
-  if (kWalkCluster > 1) cluster_barrier();  // no CTA leaves while another may store into it
+  if (C > 1) cluster_barrier();  // no CTA leaves while another may store into it
   if (rank != 0) return;
   if (tid == 0) {
     num_committed[b] = s_len;
@@ -792,31 +789,97 @@ extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void
 namespace specdec {
 namespace {
 
+// Shared memory of the walk kernel with C CTAs per request.
+template <int DT, class QSrc, int C>
+size_t walk_smem(int N, int64_t V) {
+  using Weights = ResidualWeights<DT, typename QSrc::Row>;
+  constexpr int kChunks = Weights::template chunks<kWalkElems>();
+  const int64_t ntiles = (V + kWalkThreads * kWalkElems - 1) / (kWalkThreads * kWalkElems);
+  const size_t ring = sizeof(uint4) * walk_ring_depth(kChunks) * kChunks * kWalkThreads;
+  const int64_t parts = static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, C>(V)) * kWalkThreads;
+  return ring + sizeof(float) * (2 * ntiles + parts + 3 * static_cast<int64_t>(N)) +
+         sizeof(int32_t) * 6 * static_cast<int64_t>(N);
+}
+
+// Requests (clusters of C CTAs) the GPU holds at once with this shared
+// memory, or 0 when the kernel cannot be configured.
+template <int DT, class QSrc, int C>
+int64_t walk_capacity(size_t smem) {
+  auto kernel = sample_walk_kernel<DT, QSrc, C>;
+  if (smem > kMaxDynSmem) return 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (C == 1) {
+    int dev = 0, sms = 0, per = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kWalkThreads, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return static_cast<int64_t>(sms) * per;
+  }
+  LaunchCfg lc(dim3(C), dim3(kWalkThreads), smem, nullptr, C);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &lc.cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int DT, class QSrc, int C>
+void launch_walk(int B, size_t smem, cudaStream_t s, int N, int64_t V, const void* target, float c, QSrc qsrc,
+                 const int32_t* q_row, const int32_t* dtok, const int32_t* ntok, const int32_t* nsib,
+                 const float* coins, const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
+                 int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                 int32_t* walk_info, int32_t* stats, const VerifyWs& w) {
+  launch_kc(sample_walk_kernel<DT, QSrc, C>, B * C, kWalkThreads, smem, s, C, N, V, c, target, w.m, w.z, qsrc,
+            q_row, dtok, ntok, nsib, coins, u_final, budget, eos, committed, num_committed, accept_length,
+            accept_path, next_root, walk_info, stats);
+}
+
+// Row statistics of every target row, then the walk.  Each request's walk
+// is split across a cluster of C CTAs: the largest C of 4, 2, 1 whose B
+// clusters the GPU holds at once (a request's passes run one after
+// another, so a second wave of clusters would wait for the first), or 1
+// when none does.
 template <int DT, class QSrc>
 int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, QSrc qsrc, const int32_t* q_row,
                          const int32_t* dtok, const int32_t* ntok, const int32_t* nsib, const float* coins,
                          const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
                          int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                          int32_t* walk_info, int32_t* stats, VerifyWs w, cudaStream_t s) {
-  using Weights = ResidualWeights<DT, typename QSrc::Row>;
   const int64_t rows = static_cast<int64_t>(B) * N;
-  constexpr int kChunks = Weights::template chunks<kWalkElems>();
-  const int64_t ntiles = (V + kWalkThreads * kWalkElems - 1) / (kWalkThreads * kWalkElems);
-  const size_t ring = sizeof(uint4) * walk_ring_depth(kChunks) * kChunks * kWalkThreads;
-  const int64_t parts =
-      static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, kWalkCluster>(V)) * kWalkThreads;
-  const size_t smem = ring + sizeof(float) * (2 * ntiles + parts + 3 * static_cast<int64_t>(N)) +
-                      sizeof(int32_t) * 6 * static_cast<int64_t>(N);
-  if (smem > kMaxDynSmem) return SPEC_ERR_UNSUPPORTED;  // V in the millions
+  const size_t smem4 = walk_smem<DT, QSrc, 4>(N, V), smem2 = walk_smem<DT, QSrc, 2>(N, V),
+               smem1 = walk_smem<DT, QSrc, 1>(N, V);
+  if (smem1 > kMaxDynSmem) return SPEC_ERR_UNSUPPORTED;  // V in the millions
+  int C = 1;
+  if (walk_capacity<DT, QSrc, 4>(smem4) >= B) {
+    C = 4;
+  } else if (walk_capacity<DT, QSrc, 2>(smem2) >= B) {
+    C = 2;
+  } else if (walk_capacity<DT, QSrc, 1>(smem1) < 1) {
+    return SPEC_ERR_CUDA;
+  }
   int e = launch_row_stats<DT, true>(target, V, rows, c, w.amax, w.m, w.z, stats, s);
   if (e != SPEC_OK) return e;
-  if (smem > 48 * 1024 && cudaFuncSetAttribute(sample_walk_kernel<DT, QSrc>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem)) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  launch_k(sample_walk_kernel<DT, QSrc>, B * kWalkCluster, kWalkThreads, smem, s, N, V, c, target, w.m, w.z, qsrc,
-           q_row, dtok, ntok, nsib, coins, u_final, budget, eos, committed, num_committed, accept_length, accept_path,
-           next_root, walk_info, stats);
+  if (C == 4)
+    launch_walk<DT, QSrc, 4>(B, smem4, s, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
+                             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
+                             w);
+  else if (C == 2)
+    launch_walk<DT, QSrc, 2>(B, smem2, s, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
+                             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
+                             w);
+  else
+    launch_walk<DT, QSrc, 1>(B, smem1, s, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
+                             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
+                             w);
   return launch_status();
 }
 

@@ -379,11 +379,14 @@ def test_pipeline_full_size_sampled_requests(name, mode, q_mode):
     assert 0.0 <= al < cfg.N
 
 
-def test_verify_sample_tree_given_q_node_order():
+@pytest.mark.parametrize("B", [24, 200, 400])
+def test_verify_sample_tree_given_q_node_order(B):
     """Stochastic tree verify with q in node order (q_row = NULL) on oracle
-    trees, including q[y] == 0 children and zero-mass target entries."""
-    rng = np.random.default_rng(77)
-    B, k, steps, N, V = 24, 3, 4, 12, 257
+    trees, including q[y] == 0 children and zero-mass target entries.  The
+    batch sizes take each walk layout: 4 CTAs per request while the GPU
+    holds all the clusters at once, then 2, then 1."""
+    rng = np.random.default_rng(77 + B)
+    k, steps, N, V = 3, 4, 12, 257
     opool = oracle.Pool(B, k, steps)
     for s, (p, idx) in enumerate(oracle_topk_inputs(rng, B, k, steps)):
         oracle.tree_expand(opool, s, p, np.ascontiguousarray(idx % V, np.int32))
