@@ -69,6 +69,7 @@ typedef struct CUstream_st* spec_stream_t; /* same object as cudaStream_t */
 #define SPEC_STAT_CDF_FALLBACK 3      /* inverse CDF found no crossing; last positive taken */
 #define SPEC_STAT_EMPTY_INTERSECTION 4/* TLI row with no finite intersection logit */
 #define SPEC_STAT_BAD_REQUEST 5       /* compaction input out of range; request skipped */
+#define SPEC_STAT_WAIT_TIMEOUT 6      /* a CTA gave up waiting on another's row (results void) */
 #define SPEC_NUM_STATS 8
 
 /* Limits (checked on the host; SPEC_ERR_UNSUPPORTED beyond them). */

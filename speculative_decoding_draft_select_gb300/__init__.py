@@ -27,7 +27,7 @@ __all__ = [
 F32 = 0
 BF16 = 1
 STATS = {"nonfinite_row": 0, "q_zero": 1, "residual_fallback": 2, "cdf_fallback": 3,
-         "empty_intersection": 4, "bad_request": 5}
+         "empty_intersection": 4, "bad_request": 5, "wait_timeout": 6}
 NUM_STATS = 8
 _ERRORS = {-1: "invalid argument", -2: "unsupported", -3: "CUDA launch failed", -4: "workspace too small"}
 

@@ -87,7 +87,7 @@ __device__ float cdf_tile_pass(const W& w, int64_t V, float* red, float* tile_su
 // D * chunks<E>() * THREADS 16-byte slots, chunk c of slot s of thread t at
 // ring[(s * chunks + c) * THREADS + t].  part: cdf_part_tiles * THREADS
 // floats.  V + THREADS * E < 2^31.
-constexpr int kPartTiles = 64;  // P
+constexpr int kPartTiles = 16;  // P
 
 template <int THREADS, int E, int C>
 __host__ __device__ inline int cdf_part_tiles(int64_t V) {

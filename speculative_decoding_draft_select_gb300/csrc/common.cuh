@@ -89,6 +89,33 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Streams the 16-byte items src[i], i = tid, tid + THREADS, ... < n, through
+// this thread's D slots of a cp.async ring (slot s at ring[s * THREADS +
+// tid]), D items in flight; calls f(item, i) in increasing i.  Only the
+// issuing thread reads its slots, so no barrier is needed.
+template <int THREADS, int D, class F>
+__device__ __forceinline__ void ring_stream(const uint4* src, int n, uint4* ring, F&& f) {
+  const int tid = threadIdx.x;
+  uint4* mine = ring + tid;
+#pragma unroll
+  for (int s = 0; s < D; ++s) {
+    const int i = tid + s * THREADS;
+    if (i < n) cp_async16(mine + s * THREADS, src + i, 16);
+    cp_async_commit();  // one group per item (empty ones keep the count)
+  }
+  int s = 0;
+  for (int i = tid; i < n; i += THREADS) {
+    cp_async_wait<D - 1>();  // item i has landed
+    const uint4 v = mine[s * THREADS];
+    f(v, i);
+    const int nx = i + D * THREADS;
+    if (nx < n) cp_async16(mine + s * THREADS, src + nx, 16);
+    cp_async_commit();
+    s = s + 1 == D ? 0 : s + 1;
+  }
+  cp_async_wait<0>();
+}
+
 // Pairs of fp32 lanes (the packed fp32 instructions of sm_100 and later:
 // each lane rounds exactly as the scalar operation).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
@@ -180,6 +207,24 @@ __device__ __forceinline__ void st_cluster_f32(float* local, unsigned rank, floa
   unsigned ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_i32(int* local, unsigned rank, int v) {
+  const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(local));
+  unsigned ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
+// Flags between CTAs of one launch: a release store (the writer's earlier
+// global stores are visible to whoever acquires the flag) and an acquire
+// load, both at GPU scope.
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Asynchronous copy of the E elements [v0, v0 + E) of a row (element size

@@ -352,33 +352,6 @@ struct Elem<SPEC_F32> {
   __device__ __forceinline__ static float value(T e) { return e; }
 };
 
-// Streams the 16-byte items src[i], i = tid, tid + THREADS, ... < n, through
-// this thread's D slots of a cp.async ring (slot s at ring[s * THREADS +
-// tid]), D items in flight; calls f(item, i) in increasing i.  Only the
-// issuing thread reads its slots, so no barrier is needed.
-template <int THREADS, int D, class F>
-__device__ __forceinline__ void ring_stream(const uint4* src, int n, uint4* ring, F&& f) {
-  const int tid = threadIdx.x;
-  uint4* mine = ring + tid;
-#pragma unroll
-  for (int s = 0; s < D; ++s) {
-    const int i = tid + s * THREADS;
-    if (i < n) cp_async16(mine + s * THREADS, src + i, 16);
-    cp_async_commit();  // one group per item (empty ones keep the count)
-  }
-  int s = 0;
-  for (int i = tid; i < n; i += THREADS) {
-    cp_async_wait<D - 1>();  // item i has landed
-    const uint4 v = mine[s * THREADS];
-    f(v, i);
-    const int nx = i + D * THREADS;
-    if (nx < n) cp_async16(mine + s * THREADS, src + nx, 16);
-    cp_async_commit();
-    s = s + 1 == D ? 0 : s + 1;
-  }
-  cp_async_wait<0>();
-}
-
 // Bits of ids [first, first + N) from the bitmap (N <= 8).
 template <int N>
 __device__ __forceinline__ uint32_t bits_at(const uint2* mw, int first) {

@@ -13,13 +13,15 @@
 // candidate; the verify kernels walk the tree to each request's longest
 // accepted path.
 //
-// Pass 1 (row_stats_kernel) is the bandwidth kernel: one CTA streams one
-// target row once with 16-byte loads and produces its argmax and, for
-// sampling, the online-softmax max and normaliser.  Pass 2 walks each
-// request's tree.  The greedy walk needs only the argmax per row (one warp
-// per request).  The stochastic walk (one CTA per request) gathers p[y] and
-// q[y] of every child of the current node at once, and after each
-// rejection streams the node's target and q rows to get the residual's mass.
+// Greedy: row_argmax_kernel streams every target row once with 16-byte
+// loads (one CTA per row) for its argmax; greedy_walk_kernel then walks
+// each request's tree (one warp per request).  Stochastic:
+// sample_verify_kernel, one persistent launch, computes the online-softmax
+// max and normaliser of every target row (the batched pass, each row read
+// once) and walks each request's tree as soon as the rows on its path are
+// done (a cluster of CTAs per request).  The walk gathers p[y] and q[y] of
+// every child of the current node at once, and after each rejection streams
+// the node's target and q rows to get the residual's mass.
 // The residual after j rejections is kept in closed form,
 //   p_j(v) = max(0, p(v) - A_j q(v)) / c_j,  A_{j+1} = A_j + c_j,
 //   c_{j+1} = sum_v max(0, p(v) - A_{j+1} q(v)),  A_0 = 0, c_0 = 1,
@@ -53,6 +55,10 @@ __host__ __device__ constexpr int walk_ring_depth(int chunks) {
          : 32768 / (chunks * kWalkThreads * 16) < 2 ? 2
                                                      : 32768 / (chunks * kWalkThreads * 16);
 }
+
+// Bound on a wait for another CTA's row (about 50 ms at 2 GHz); past it the
+// launch counts SPEC_STAT_WAIT_TIMEOUT and goes on.
+constexpr long long kWaitLimitCycles = 100000000LL;
 
 __device__ __forceinline__ float prob_of(float key, float c, float mc, float invz) {
   return fminf(fast_exp2(fmaf(key, c, -mc)) * invz, 1.0f);
@@ -126,89 +132,51 @@ struct KeyedSum {
   }
 };
 
-#ifndef SPEC_STAT_THREADS
-#define SPEC_STAT_THREADS 256
-#endif
-constexpr int kStatThreads = SPEC_STAT_THREADS;
-#ifndef SPEC_STAT_UNROLL
-#define SPEC_STAT_UNROLL 8
-#endif
-constexpr int kStatUnroll = SPEC_STAT_UNROLL;  // 16-byte loads in flight per thread
+constexpr int kStatThreads = 256;
+constexpr int kStatUnroll = 8;  // 16-byte loads in flight per thread
 
-// Pass 1: one CTA per target row streams it with 16-byte loads (4 in
-// flight per thread) and reduces it to its argmax and, for sampling, the
-// online-softmax max and normaliser.  Measured on GB300 this plain load loop
-// keeps HBM at the copy rate; staging through shared memory with bulk
-// copies was slower for this access pattern.
-template <int DT, bool STOCH>
+// Greedy pass 1: one CTA per target row streams it with 16-byte loads (8 in
+// flight per thread) and reduces it to its argmax (value desc, index asc,
+// NaN skipped).  Measured on GB300 this plain load loop keeps HBM at the
+// copy rate; staging through shared memory with bulk copies was slower for
+// this access pattern.  (The stochastic verify computes its row statistics
+// inside sample_verify_kernel.)
+template <int DT>
 __global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
-    row_stats_kernel(const void* __restrict__ logits, int64_t V, float c, int32_t* __restrict__ amax,
-                     float* __restrict__ m_out, float* __restrict__ z_out, int32_t* __restrict__ stats) {
+    row_argmax_kernel(const void* __restrict__ logits, int64_t V, int32_t* __restrict__ amax,
+                      int32_t* __restrict__ stats) {
   pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = kStatThreads / 32;
-  __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
+  __shared__ float wv[kWarps];
   __shared__ int wi[kWarps];
-  __shared__ float s_m, s_s;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  RowStatVisitor<DT, STOCH> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX, 0.0f};
+  RowStatVisitor<DT, false> v{0.0f, neg_inf(), 0.0f, 0.0f, INT_MAX, 0.0f};
   for_row_fast<DT, kStatUnroll>(row, V, v, threadIdx.x, kStatThreads);
   float bv = v.m;
   int bi = v.bi;
   warp_best(bv, bi);
-  float m = v.m, s = v.s0 + v.s1;
-  if (STOCH) warp_merge_ms(m, s, c);
   if (lane == 0) {
     wv[warp] = bv;
     wi[warp] = bi;
-    wm[warp] = m;
-    ws[warp] = s;
   }
   __syncthreads();
   if (warp == 0) {
     bv = lane < kWarps ? wv[lane] : neg_inf();
     bi = lane < kWarps ? wi[lane] : INT_MAX;
     warp_best(bv, bi);
-    if (STOCH) {
-      m = lane < kWarps ? wm[lane] : neg_inf();
-      s = lane < kWarps ? ws[lane] : 0.0f;
-      warp_merge_ms(m, s, c);
-    }
     if (lane == 0) {
       amax[r] = bi == INT_MAX ? 0 : bi;
-      s_m = m;
-      s_s = s;
       if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
     }
   }
-  if (!STOCH) return;
-  __syncthreads();
-  m = s_m;
-  s = s_s;
-  if (isfinite(m) && !isfinite(s)) {
-    // the row holds a NaN: recompute the normaliser with NaN as -inf
-    KeyedSum ks{c, m * c, 0.0f};
-    for_row<DT, 2>(row, V, ks);
-    const float part = warp_sum(ks.s);
-    __syncthreads();
-    if (lane == 0) ws[warp] = part;
-    __syncthreads();
-    s = 0.0f;
-    for (int w = 0; w < kWarps; ++w) s += ws[w];
-  }
-  if (threadIdx.x == 0) {
-    m_out[r] = m;
-    z_out[r] = s;
-  }
 }
 
-template <int DT, bool STOCH>
-int launch_row_stats(const void* logits, int64_t V, int64_t R, float c, int32_t* amax, float* m, float* z,
-                     int32_t* stats, cudaStream_t s) {
-  launch_k(row_stats_kernel<DT, STOCH>, static_cast<unsigned>(R), kStatThreads, 0, s, logits, V, c, amax, m, z,
-           stats);
+template <int DT>
+int launch_row_argmax(const void* logits, int64_t V, int64_t R, int32_t* amax, int32_t* stats, cudaStream_t s) {
+  launch_k(row_argmax_kernel<DT>, static_cast<unsigned>(R), kStatThreads, 0, s, logits, V, amax, stats);
   return launch_status();
 }
 
@@ -534,10 +502,24 @@ struct ResidualWeights {
   }
 };
 
+// Stochastic verify in one persistent launch: the row statistics of every
+// target row (the batched pass) and the walk of every request.  Work is
+// taken from two queues in the workspace (zeroed before the launch): rows
+// in node-major order (every request's root first, then node 1, ...; a
+// child always has a larger node index than its parent, so the rows a walk
+// reaches come in the order it reaches them) and requests.  A cluster walks
+// one request at a time; on entering a node whose row is not done yet,
+// each CTA of the cluster computes queued rows itself until it is (a
+// waiting CTA always has work or waits on a row another running CTA is
+// computing, which never waits, so the launch cannot deadlock; the wait is
+// bounded all the same).  Clusters without a request left compute the
+// remaining rows.  A row's statistics are published with a release store
+// of its flag and read after an acquire load of it.
 template <int DT, class QSrc, int C>
 __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
-    sample_walk_kernel(int N, int64_t V, float c, const void* __restrict__ target,
-                       const float* __restrict__ m_row, const float* __restrict__ z_row, QSrc qsrc,
+    sample_verify_kernel(int B, int N, int64_t V, float c, const void* __restrict__ target,
+                       float* __restrict__ m_row, float* __restrict__ z_row, int32_t* __restrict__ ready,
+                       int32_t* __restrict__ queues, QSrc qsrc,
                        const int32_t* __restrict__ q_row, const int32_t* __restrict__ dtok,
                        const int32_t* __restrict__ ntok, const int32_t* __restrict__ nsib,
                        const float* __restrict__ coins, const float* __restrict__ u_final,
@@ -569,20 +551,122 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
   __shared__ int64_t s_qrow;
   __shared__ float s_m, s_invz, s_nb, s_A, s_cj, s_total;
 
+  __shared__ int s_b, s_item, s_flag;
+  __shared__ float sw_m[kWalkThreads / 32], sw_s[kWalkThreads / 32];
+
   // the C CTAs of a cluster walk request b together: each pass
   // over a row is split between them, everything else is done by each CTA
   // on the same data, so all of them take the same decisions; rank 0 alone
   // counts anomalies and writes the outputs
   const unsigned rank = C > 1 ? cluster_rank() : 0u;
-  const int b = blockIdx.x / C, tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t* const cstats = rank == 0 ? stats : nullptr;
-  const int64_t o = static_cast<int64_t>(b) * N;
+  const int64_t rows = static_cast<int64_t>(B) * N;
+  int32_t* const next_row = queues;
+  int32_t* const next_req = queues + 1;
   int par = 0;  // tile-sum buffer of the next pass
   auto pass = [&](const Weights& w) -> float {
     float* ts = tile_sums + par * ntiles;
     par ^= 1;
     return cdf_tile_pass_split<kWalkThreads, kWalkElems, kRing, C>(w, V, part, ts, ring, rank);
   };
+  // queued row i (node-major): its max and normaliser, then its flag
+  auto stats_row = [&](int64_t i) {
+    const int64_t r = (i % B) * N + i / B;
+    const void* row = static_cast<const char*>(target) + r * V * esz;
+    RowStatVisitor<DT, true> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX, 0.0f};
+    {
+      // the walk's copy ring (idle here): kRing * kChunks 16-byte copies in
+      // flight per thread, in the visiting order of for_row_fast
+      constexpr int kv = Logit<DT>::kVec;
+      const RowSpan sp = row_span<DT>(row, V);
+      const int head = static_cast<int>(sp.head), nvec = static_cast<int>(sp.nvec);
+      if (tid < head) v.visit1(Logit<DT>::load1(row, tid), tid, true);
+      const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+      ring_stream<kWalkThreads, kRing * kChunks>(
+          vp, nvec, ring, [&](const uint4& x, int i) { v.visit_vec(x, head + static_cast<int64_t>(i) * kv, true); });
+      const int64_t t = head + static_cast<int64_t>(nvec) * kv + tid;
+      if (t < V) v.visit1(Logit<DT>::load1(row, t), t, true);
+    }
+    float m = v.m, sum = v.s0 + v.s1;
+    warp_merge_ms(m, sum, c);
+    if (lane == 0) {
+      sw_m[warp] = m;
+      sw_s[warp] = sum;
+    }
+    __syncthreads();
+    m = sw_m[0];
+    sum = sw_s[0];
+#pragma unroll
+    for (int w2 = 1; w2 < kWalkThreads / 32; ++w2) merge_ms(m, sum, sw_m[w2], sw_s[w2], c);
+    if (isfinite(m) && !isfinite(sum)) {
+      // the row holds a NaN: the normaliser again with NaN as -inf
+      KeyedSum ks{c, m * c, 0.0f};
+      for_row<DT, 2>(row, V, ks, tid, kWalkThreads);
+      const float part_s = warp_sum(ks.s);
+      __syncthreads();
+      if (lane == 0) sw_s[warp] = part_s;
+      __syncthreads();
+      sum = 0.0f;
+#pragma unroll
+      for (int w2 = 0; w2 < kWalkThreads / 32; ++w2) sum += sw_s[w2];
+    }
+    if (tid == 0) {
+      if (!isfinite(m)) bump(stats, SPEC_STAT_NONFINITE_ROW);
+      m_row[r] = m;
+      z_row[r] = sum;
+      st_release_gpu(ready + r, 1);
+    }
+    __syncthreads();  // sw_* reused by the next row
+  };
+  // this CTA computes queued rows until row r is done (or, with the queue
+  // empty, waits for the CTA computing it).  Taking other rows while row r
+  // is in flight keeps the HBM stream going; measured at the c3 sizes it
+  // beats waiting idle for r.
+  auto wait_row = [&](int64_t r) {
+    for (;;) {
+      if (tid == 0) {
+        s_flag = ld_acquire_gpu(ready + r);
+        s_item = s_flag ? 0 : atomicAdd(next_row, 1);
+      }
+      __syncthreads();
+      if (s_flag) break;
+      const int64_t item = s_item;
+      __syncthreads();
+      if (item < rows) {
+        stats_row(item);
+        continue;
+      }
+      // every row is taken: row r is in flight on a running CTA
+      if (tid == 0) {
+        const long long t0 = clock64();
+        while (!ld_acquire_gpu(ready + r)) {
+          if (clock64() - t0 > kWaitLimitCycles) {
+            bump(stats, SPEC_STAT_WAIT_TIMEOUT);
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+      __syncthreads();
+      break;
+    }
+  };
+  for (;;) {
+  // next request of this cluster, from rank 0 to every CTA of it
+  if (rank == 0 && tid == 0) {
+    const int nb = atomicAdd(next_req, 1);
+    if (C > 1) {
+#pragma unroll
+      for (int q = 0; q < C; ++q) st_cluster_i32(&s_b, q, nb);
+    } else {
+      s_b = nb;
+    }
+  }
+  if (C > 1) cluster_barrier(); else __syncthreads();
+  const int b = s_b;
+  if (b >= B) break;
+  const int64_t o = static_cast<int64_t>(b) * N;
   for (int i = tid; i < N; i += kWalkThreads) {
     s_dt[i] = __ldg(dtok + o + i);
     s_nt[i] = __ldg(ntok + o + i);
@@ -601,17 +685,17 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     s_path[0] = 0;
   }
   __syncthreads();
-  if (C > 1) cluster_barrier();  // every CTA of the cluster is running
   const float cT = c;
   while (!s_done) {
     // enter node n: children in sibling order, row statistics, q row
+    wait_row(o + s_n);
     if (tid == 0) {
       const int n = s_n;
       int nch = 0;
       for (int ch = s_nt[n]; ch > 0 && ch < N && nch < N; ch = s_ns[ch]) s_ch[nch++] = ch;
       s_nch = nch;
-      const float z = __ldg(z_row + o + n);
-      s_m = __ldg(m_row + o + n);
+      const float z = __ldcg(z_row + o + n);
+      s_m = __ldcg(m_row + o + n);
       s_invz = 1.0f / z;
       s_nb = folded_offset(s_m, c, z);
       s_qrow = q_row ? static_cast<int64_t>(__ldg(q_row + o + n)) : o + n;
@@ -697,26 +781,43 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     }
     __syncthreads();
   }
-  if (C > 1) cluster_barrier();  // no CTA leaves while another may store into it
-  if (rank != 0) return;
-  if (tid == 0) {
-    num_committed[b] = s_len;
-    accept_length[b] = s_acc;
-    next_root[b] = s_len > 0 ? s_com[s_len - 1] : -1;
-    if (walk_info) {
-      walk_info[3 * b] = s_n;
-      walk_info[3 * b + 1] = s_rej;
-      walk_info[3 * b + 2] = s_kind;
+  if (rank == 0) {
+    if (tid == 0) {
+      num_committed[b] = s_len;
+      accept_length[b] = s_acc;
+      next_root[b] = s_len > 0 ? s_com[s_len - 1] : -1;
+      if (walk_info) {
+        walk_info[3 * b] = s_n;
+        walk_info[3 * b + 1] = s_rej;
+        walk_info[3 * b + 2] = s_kind;
+      }
+    }
+    for (int i = tid; i < N; i += kWalkThreads) {
+      committed[o + i] = s_com[i];
+      accept_path[o + i] = s_path[i];
     }
   }
-  for (int i = tid; i < N; i += kWalkThreads) {
-    committed[o + i] = s_com[i];
-    accept_path[o + i] = s_path[i];
+  // every CTA of the cluster is done with this request (its shared state
+  // and its stores into the others) before rank 0 hands out the next one
+  if (C > 1) cluster_barrier(); else __syncthreads();
   }
+  // no request left: the remaining rows
+  for (;;) {
+    if (tid == 0) s_item = atomicAdd(next_row, 1);
+    __syncthreads();
+    const int64_t item = s_item;
+    __syncthreads();
+    if (item >= rows) break;
+    stats_row(item);
+  }
+  if (C > 1) cluster_barrier();  // no CTA leaves while another may store into it
 }
 
+// Workspace: per-row argmax (greedy) or ready flags (stochastic, followed
+// by the two work-queue counters), max and normaliser.
 struct VerifyWs {
-  int32_t* amax;
+  int32_t* amax;   // greedy: argmax per row
+  int32_t* ready;  // stochastic: flag per row, then next_row, next_req (same memory as amax)
   float* m;
   float* z;
 };
@@ -726,7 +827,8 @@ VerifyWs carve(void* ws, int B, int N) {
   char* p = static_cast<char*>(ws);
   VerifyWs w;
   w.amax = reinterpret_cast<int32_t*>(p);
-  p += align256(rows * sizeof(int32_t));
+  w.ready = w.amax;
+  p += align256((rows + 2) * sizeof(int32_t));
   w.m = reinterpret_cast<float*>(p);
   p += align256(rows * sizeof(float));
   w.z = reinterpret_cast<float*>(p);
@@ -757,7 +859,7 @@ using namespace specdec;
 extern "C" size_t spec_verify_ws_size(int B, int N) {
   if (B < 0 || N < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * N;
-  return align256(rows * sizeof(int32_t)) + 2 * align256(rows * sizeof(float));
+  return align256((rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float));
 }
 
 extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void* target_logits,
@@ -775,10 +877,8 @@ extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void
   VerifyWs w = carve(ws, B, N);
   const int64_t rows = static_cast<int64_t>(B) * N;
   int e = dtype == SPEC_BF16
-              ? launch_row_stats<SPEC_BF16, false>(target_logits, V, rows, 0.0f, w.amax, nullptr, nullptr,
-                                                   stats_or_null, s)
-              : launch_row_stats<SPEC_F32, false>(target_logits, V, rows, 0.0f, w.amax, nullptr, nullptr,
-                                                  stats_or_null, s);
+              ? launch_row_argmax<SPEC_BF16>(target_logits, V, rows, w.amax, stats_or_null, s)
+              : launch_row_argmax<SPEC_F32>(target_logits, V, rows, w.amax, stats_or_null, s);
   if (e != SPEC_OK) return e;
   launch_k(greedy_walk_kernel, B, 32, sizeof(int32_t) * 6 * N, s, N, w.amax, draft_token, retrieve_next_token,
            retrieve_next_sibling, budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
@@ -790,6 +890,7 @@ namespace specdec {
 namespace {
 
 // Shared memory of the walk kernel with C CTAs per request.
+// Shared memory of the verify kernel with C CTAs per request.
 template <int DT, class QSrc, int C>
 size_t walk_smem(int N, int64_t V) {
   using Weights = ResidualWeights<DT, typename QSrc::Row>;
@@ -801,11 +902,11 @@ size_t walk_smem(int N, int64_t V) {
          sizeof(int32_t) * 6 * static_cast<int64_t>(N);
 }
 
-// Requests (clusters of C CTAs) the GPU holds at once with this shared
-// memory, or 0 when the kernel cannot be configured.
+// Clusters of C CTAs the GPU holds at once with this shared memory, or 0
+// when the kernel cannot be configured.
 template <int DT, class QSrc, int C>
 int64_t walk_capacity(size_t smem) {
-  auto kernel = sample_walk_kernel<DT, QSrc, C>;
+  auto kernel = sample_verify_kernel<DT, QSrc, C>;
   if (smem > kMaxDynSmem) return 0;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -833,21 +934,21 @@ int64_t walk_capacity(size_t smem) {
 }
 
 template <int DT, class QSrc, int C>
-void launch_walk(int B, size_t smem, cudaStream_t s, int N, int64_t V, const void* target, float c, QSrc qsrc,
-                 const int32_t* q_row, const int32_t* dtok, const int32_t* ntok, const int32_t* nsib,
-                 const float* coins, const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
-                 int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
-                 int32_t* walk_info, int32_t* stats, const VerifyWs& w) {
-  launch_kc(sample_walk_kernel<DT, QSrc, C>, B * C, kWalkThreads, smem, s, C, N, V, c, target, w.m, w.z, qsrc,
-            q_row, dtok, ntok, nsib, coins, u_final, budget, eos, committed, num_committed, accept_length,
-            accept_path, next_root, walk_info, stats);
+void launch_verify(int64_t clusters, size_t smem, cudaStream_t s, int B, int N, int64_t V, const void* target,
+                   float c, QSrc qsrc, const int32_t* q_row, const int32_t* dtok, const int32_t* ntok,
+                   const int32_t* nsib, const float* coins, const float* u_final, const int32_t* budget, int32_t eos,
+                   int32_t* committed, int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
+                   int32_t* next_root, int32_t* walk_info, int32_t* stats, const VerifyWs& w) {
+  const int64_t rows = static_cast<int64_t>(B) * N;
+  launch_kc(sample_verify_kernel<DT, QSrc, C>, static_cast<unsigned>(clusters * C), kWalkThreads, smem, s, C, B, N,
+            V, c, target, w.m, w.z, w.ready, w.ready + rows, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
+            eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats);
 }
 
-// Row statistics of every target row, then the walk.  Each request's walk
-// is split across a cluster of C CTAs: the largest C of 4, 2, 1 whose B
-// clusters the GPU holds at once (a request's passes run one after
-// another, so a second wave of clusters would wait for the first), or 1
-// when none does.
+// One persistent launch (after zeroing the row flags and queue counters):
+// as many clusters as the GPU holds, C CTAs each, the largest C of 4, 2, 1
+// for which every request can have its cluster at once (a request's
+// passes run one after another), else 1.
 template <int DT, class QSrc>
 int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, QSrc qsrc, const int32_t* q_row,
                          const int32_t* dtok, const int32_t* ntok, const int32_t* nsib, const float* coins,
@@ -858,28 +959,23 @@ int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, Q
   const size_t smem4 = walk_smem<DT, QSrc, 4>(N, V), smem2 = walk_smem<DT, QSrc, 2>(N, V),
                smem1 = walk_smem<DT, QSrc, 1>(N, V);
   if (smem1 > kMaxDynSmem) return SPEC_ERR_UNSUPPORTED;  // V in the millions
-  int C = 1;
-  if (walk_capacity<DT, QSrc, 4>(smem4) >= B) {
-    C = 4;
-  } else if (walk_capacity<DT, QSrc, 2>(smem2) >= B) {
-    C = 2;
-  } else if (walk_capacity<DT, QSrc, 1>(smem1) < 1) {
+  const int64_t cap4 = walk_capacity<DT, QSrc, 4>(smem4), cap2 = walk_capacity<DT, QSrc, 2>(smem2),
+                cap1 = walk_capacity<DT, QSrc, 1>(smem1);
+  if (cap1 < 1) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(w.ready, 0, sizeof(int32_t) * static_cast<size_t>(rows + 2), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  }
-  int e = launch_row_stats<DT, true>(target, V, rows, c, w.amax, w.m, w.z, stats, s);
-  if (e != SPEC_OK) return e;
-  if (C == 4)
-    launch_walk<DT, QSrc, 4>(B, smem4, s, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
-                             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
-                             w);
-  else if (C == 2)
-    launch_walk<DT, QSrc, 2>(B, smem2, s, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
-                             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
-                             w);
+  if (cap4 >= B)
+    launch_verify<DT, QSrc, 4>(cap4, smem4, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
+                               budget, eos, committed, num_committed, accept_length, accept_path, next_root,
+                               walk_info, stats, w);
+  else if (cap2 >= B)
+    launch_verify<DT, QSrc, 2>(cap2, smem2, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
+                               budget, eos, committed, num_committed, accept_length, accept_path, next_root,
+                               walk_info, stats, w);
   else
-    launch_walk<DT, QSrc, 1>(B, smem1, s, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
-                             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
-                             w);
+    launch_verify<DT, QSrc, 1>(cap1, smem1, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
+                               budget, eos, committed, num_committed, accept_length, accept_path, next_root,
+                               walk_info, stats, w);
   return launch_status();
 }
 
@@ -1025,10 +1121,8 @@ extern "C" int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, co
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t rows = static_cast<int64_t>(B) * N;
   int e = dtype == SPEC_BF16
-              ? launch_row_stats<SPEC_BF16, false>(target_logits, V, rows, 0.0f, amax, nullptr, nullptr,
-                                                   stats_or_null, s)
-              : launch_row_stats<SPEC_F32, false>(target_logits, V, rows, 0.0f, amax, nullptr, nullptr,
-                                                  stats_or_null, s);
+              ? launch_row_argmax<SPEC_BF16>(target_logits, V, rows, amax, stats_or_null, s)
+              : launch_row_argmax<SPEC_F32>(target_logits, V, rows, amax, stats_or_null, s);
   if (e != SPEC_OK) return e;
   launch_k(greedy_walk_kernel, B, 32, sizeof(int32_t) * 6 * N, s, N, amax, draft_token, retrieve_next_token,
            retrieve_next_sibling, budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,

@@ -190,7 +190,7 @@ def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> in
     n = buf.steps * per_step + 1  # + build_tree
     if buf.kind == "tli":
         n += 3  # the map plan
-    n += 2  # verify: row pass + walk
+    n += 2 if mode == "greedy" else 1  # verify: row argmax + walk, or the one stochastic launch
     if compact:
         n += 1 + (1 if (kv_pool and buf.compact_out is not None) else 0)
     return n
