@@ -89,29 +89,51 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// cp.async of 16 bytes to a shared-memory address given as a 32-bit
+// shared-window offset.
+__device__ __forceinline__ void cp_async16_s(unsigned smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
+}
+
 // Streams the 16-byte items src[i], i = tid, tid + THREADS, ... < n, through
 // this thread's D slots of a cp.async ring (slot s at ring[s * THREADS +
 // tid]), D items in flight; calls f(item, i) in increasing i.  Only the
-// issuing thread reads its slots, so no barrier is needed.
+// issuing thread reads its slots, so no barrier is needed.  The loop runs
+// in rounds of D items (item j uses slot j mod D), so slot addresses are
+// constants; one commit group per item keeps "item j landed" equal to
+// "at most D - 1 groups pending".
 template <int THREADS, int D, class F>
 __device__ __forceinline__ void ring_stream(const uint4* src, int n, uint4* ring, F&& f) {
   const int tid = threadIdx.x;
   uint4* mine = ring + tid;
+  const unsigned sb = static_cast<unsigned>(__cvta_generic_to_shared(mine));
+  const uint4* g = src + tid;
+  const int cnt = n > tid ? (n - tid + THREADS - 1) / THREADS : 0;  // this thread's items
 #pragma unroll
   for (int s = 0; s < D; ++s) {
-    const int i = tid + s * THREADS;
-    if (i < n) cp_async16(mine + s * THREADS, src + i, 16);
-    cp_async_commit();  // one group per item (empty ones keep the count)
-  }
-  int s = 0;
-  for (int i = tid; i < n; i += THREADS) {
-    cp_async_wait<D - 1>();  // item i has landed
-    const uint4 v = mine[s * THREADS];
-    f(v, i);
-    const int nx = i + D * THREADS;
-    if (nx < n) cp_async16(mine + s * THREADS, src + nx, 16);
+    if (s < cnt) cp_async16_s(sb + 16u * s * THREADS, g + s * THREADS);
     cp_async_commit();
-    s = s + 1 == D ? 0 : s + 1;
+  }
+  int j = 0;
+  for (; j + D <= cnt; j += D) {
+    const uint4* gn = g + static_cast<int64_t>(j + D) * THREADS;
+#pragma unroll
+    for (int s = 0; s < D; ++s) {
+      cp_async_wait<D - 1>();  // item j + s has landed
+      const uint4 v = mine[s * THREADS];
+      f(v, tid + (j + s) * THREADS);
+      if (j + s + D < cnt) cp_async16_s(sb + 16u * s * THREADS, gn + s * THREADS);
+      cp_async_commit();
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < D; ++s) {
+    if (j + s < cnt) {
+      cp_async_wait<D - 1>();
+      const uint4 v = mine[s * THREADS];
+      f(v, tid + (j + s) * THREADS);
+      cp_async_commit();
+    }
   }
   cp_async_wait<0>();
 }
