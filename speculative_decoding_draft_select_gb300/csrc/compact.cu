@@ -8,9 +8,9 @@
 // walk-through)" 5.2: the cache is restored to the committed path, and the
 // correction / bonus token has no KV of its own yet.
 //
-// Two launches.  The index kernel (one CTA; one thread per request) does the
-// relabelling or emits the moves, and compacts the freed list across
-// requests with a block scan.  The payload kernel (one CTA per request)
+// Two launches.  The index kernel (one CTA; a group of 8 lanes per request)
+// does the relabelling or emits the moves, and compacts the freed list
+// across requests with a block scan.  The payload kernel (one CTA per request)
 // copies each move's bytes in increasing path order with a barrier between
 // moves, so a source is always read before a later move overwrites it (the
 // path [0, 2, 3] case: node 3 lands where node 2 was).
@@ -48,6 +48,12 @@ __device__ __forceinline__ int block_exclusive_scan_i(int v, int* sh, int& total
   return x - v + (warp > 0 ? sh[warp - 1] : 0);
 }
 
+// A group of kLanes lanes per request (kIndexThreads / kLanes requests per
+// round of the one CTA): the lanes split the request's nodes, pages and path
+// entries, and ballots within the group keep every list in its order.
+constexpr int kLanes = 8;
+constexpr int kGroups = kIndexThreads / kLanes;
+
 __global__ void __launch_bounds__(kIndexThreads)
     compact_index_kernel(int B, int N, int ps, const int32_t* __restrict__ seq_lens,
                          const int32_t* __restrict__ path, const int32_t* __restrict__ acc_len,
@@ -57,72 +63,121 @@ __global__ void __launch_bounds__(kIndexThreads)
   pdl_enter();
   __shared__ int scan_sh[33];
   __shared__ int running;
+  const int lane = threadIdx.x & 31, g = threadIdx.x / kLanes, gl = threadIdx.x % kLanes;
+  // this group's lanes: every collective below names only them, since the
+  // groups of a warp run different trip counts
+  const unsigned gmask = ((1u << kLanes) - 1u) << (lane & ~(kLanes - 1));
+  const unsigned below = (1u << gl) - 1u;
+  auto group_bits = [&](bool p) -> unsigned {  // bit j: lane j of the group
+    return __ballot_sync(gmask, p) >> (lane & ~(kLanes - 1));
+  };
+  auto group_all = [&](bool p) { return group_bits(!p) == 0u; };
   if (threadIdx.x == 0) running = 0;
   __syncthreads();
-  for (int base = 0; base < B; base += kIndexThreads) {
-    const int b = base + threadIdx.x;
-    int cnt = 0;
-    bool valid = false;
-    int64_t sl = 0, nk = 0;
-    int a = 0;
-    const int32_t* pb = path + static_cast<int64_t>(b) * N;
-    int32_t* rt = req_to_token + static_cast<int64_t>(b) * max_ctx;
-    if (b < B) {
-      sl = __ldg(seq_lens + b);
-      a = __ldg(acc_len + b);
-      valid = sl >= 0 && sl + N <= max_ctx && a >= 0 && a < N && __ldg(pb) == 0;
-      for (int i = 1; valid && i <= a; ++i) {
+  for (int base = 0; base < B; base += kGroups) {
+    const int b = base + g;
+    const bool in = b < B;
+    const int64_t o = static_cast<int64_t>(in ? b : 0) * N;
+    const int32_t* pb = path + o;
+    int32_t* rt = req_to_token + static_cast<int64_t>(in ? b : 0) * max_ctx;
+    const int64_t sl = in ? __ldg(seq_lens + b) : 0;
+    const int a = in ? __ldg(acc_len + b) : 0;
+    // validity: a seq_len and accept length in range, a path that starts at
+    // 0 and increases within [0, N)
+    bool valid = in && sl >= 0 && sl + N <= max_ctx && a >= 0 && a < N;
+    if (valid) valid = __ldg(pb) == 0;
+    for (int i0 = 1; i0 <= (in ? a : 0) && i0 < N; i0 += kLanes) {
+      const int i = i0 + gl;
+      bool ok = true;
+      if (valid && i <= a) {
         const int32_t pi = __ldg(pb + i);
-        valid = pi > __ldg(pb + i - 1) && pi < N;
+        ok = pi > __ldg(pb + i - 1) && pi < N;
       }
-      if (!valid) {
-        new_kv_len[b] = -1;
-        num_moves[b] = 0;
-        bump(stats, SPEC_STAT_BAD_REQUEST);
+      valid = group_all(ok) && valid;
+    }
+    const int64_t nk = sl + 1 + a;
+    int cnt = 0;
+    if (in && valid) {
+      if (ps == 1) {
+        cnt = N - 1 - a;
       } else {
-        nk = sl + 1 + a;
-        new_kv_len[b] = static_cast<int32_t>(nk);
-        if (ps == 1) {
-          cnt = N - 1 - a;
-        } else {
-          for (int64_t lp = (sl + ps - 1) / ps; lp * ps < sl + N; ++lp) cnt += lp * ps >= nk;
-        }
-      }
-      for (int i = 0; i < N; ++i) {
-        move_src[static_cast<int64_t>(b) * N + i] = -1;
-        move_dst[static_cast<int64_t>(b) * N + i] = -1;
+        for (int64_t lp = (sl + ps - 1) / ps + gl; lp * ps < sl + N; lp += kLanes) cnt += lp * ps >= nk;
+        for (int off = kLanes / 2; off > 0; off >>= 1) cnt += __shfl_xor_sync(gmask, cnt, off);
       }
     }
+    if (in) {
+      for (int i = gl; i < N; i += kLanes) {
+        move_src[o + i] = -1;
+        move_dst[o + i] = -1;
+      }
+      if (gl == 0) {
+        new_kv_len[b] = valid ? static_cast<int32_t>(nk) : -1;
+        if (!valid) {
+          num_moves[b] = 0;
+          bump(stats, SPEC_STAT_BAD_REQUEST);
+        }
+      }
+    }
+    // freed-list offsets: exclusive scan of the groups' counts
     int total;
-    const int off = running + block_exclusive_scan_i(cnt, scan_sh, total);
-    if (valid) {
-      int w = off;
+    const int mine = gl == 0 ? cnt : 0;
+    const int off0 = running + block_exclusive_scan_i(mine, scan_sh, total);
+    int w = __shfl_sync(gmask, off0, lane & ~(kLanes - 1));
+    if (in && valid) {
       if (ps == 1) {
-        // freed: slots of the nodes off the path, node order (old mapping)
-        int j = 1;
-        for (int n = 1; n < N; ++n) {
-          if (j <= a && __ldg(pb + j) == n) {
-            ++j;
-            continue;
+        // freed: slots of the nodes off the path, in node order (old
+        // mapping); the path is increasing, so node n is on it iff the
+        // merge pointer meets it
+        int j = 1;  // next path entry not below the chunk
+        for (int n0 = 1; n0 < N; n0 += kLanes) {
+          const int n = n0 + gl;
+          while (j <= a && __ldg(pb + j) < n0) ++j;
+          bool on = false;
+          for (int jj = j; jj <= a; ++jj) {
+            const int32_t pj = __ldg(pb + jj);
+            if (pj >= n0 + kLanes) break;
+            on = on || pj == n;
           }
-          freed[w++] = rt[sl + n];
+          const bool off = n < N && !on;
+          const unsigned bits = group_bits(off);
+          const int32_t slot = off ? rt[sl + n] : 0;
+          if (off) freed[w + __popc(bits & below)] = slot;
+          w += __popc(bits);
         }
-        // relabel in increasing i: position sl+path[i] is read before
-        // position sl+i is written, and path[i] >= i
-        for (int i = 1; i <= a; ++i) rt[sl + i] = rt[sl + __ldg(pb + i)];
-        num_moves[b] = 0;
+        __syncwarp(gmask);
+        // relabel: position sl + i takes the slot of sl + path[i]; every
+        // read position path[i] >= i is past every write of earlier chunks,
+        // and a chunk reads all before it writes
+        for (int i0 = 1; i0 <= a; i0 += kLanes) {
+          const int i = i0 + gl;
+          const int32_t v = i <= a ? rt[sl + __ldg(pb + i)] : 0;
+          __syncwarp(gmask);
+          if (i <= a) rt[sl + i] = v;
+        }
+        if (gl == 0) num_moves[b] = 0;
       } else {
+        // moves in increasing i for the path entries not in place
         int m = 0;
-        for (int i = 1; i <= a; ++i) {
-          const int32_t pi = __ldg(pb + i);
-          if (pi == i) continue;
-          move_src[static_cast<int64_t>(b) * N + m] = rt[sl + pi];
-          move_dst[static_cast<int64_t>(b) * N + m] = rt[sl + i];
-          ++m;
+        for (int i0 = 1; i0 <= a; i0 += kLanes) {
+          const int i = i0 + gl;
+          const int32_t pi = i <= a ? __ldg(pb + i) : i;
+          const bool mv = i <= a && pi != i;
+          const unsigned bits = group_bits(mv);
+          if (mv) {
+            move_src[o + m + __popc(bits & below)] = rt[sl + pi];
+            move_dst[o + m + __popc(bits & below)] = rt[sl + i];
+          }
+          m += __popc(bits);
         }
-        num_moves[b] = m;
-        for (int64_t lp = (sl + ps - 1) / ps; lp * ps < sl + N; ++lp)
-          if (lp * ps >= nk) freed[w++] = rt[lp * ps] / ps;
+        if (gl == 0) num_moves[b] = m;
+        // pages first touched by this step at or past the new length
+        for (int64_t lp0 = (sl + ps - 1) / ps; lp0 * ps < sl + N; lp0 += kLanes) {
+          const int64_t lp = lp0 + gl;
+          const bool fr = lp * ps < sl + N && lp * ps >= nk;
+          const unsigned bits = group_bits(fr);
+          if (fr) freed[w + __popc(bits & below)] = rt[lp * ps] / ps;
+          w += __popc(bits);
+        }
       }
     }
     __syncthreads();

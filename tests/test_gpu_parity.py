@@ -487,6 +487,41 @@ def test_compact_parity(ps, with_kv):
     assert int(stats[sd.STATS["bad_request"]]) == int(o["bad"][0])
 
 
+@pytest.mark.parametrize("ps", [1, 4])
+def test_compact_many_requests_and_bad_ones(ps):
+    """More requests than one round of the index kernel (128 lane groups),
+    a path longer than a lane group, and requests the kernel must skip: an
+    accept length out of range, a path that does not increase, a path that
+    does not start at 0, a sequence that would overflow max_ctx."""
+    rng = np.random.default_rng(40 + ps)
+    B, N, max_ctx = 300, 21, 64
+    seq = rng.integers(0, max_ctx - N, B).astype(np.int32)
+    slots = rng.permutation(B * max_ctx).astype(np.int32).reshape(B, max_ctx)
+    acc = rng.integers(0, N, B).astype(np.int32)
+    acc[:4] = [N - 1, N - 1, 13, 0]
+    path = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        path[b, :acc[b] + 1] = [0] + sorted(rng.choice(np.arange(1, N), acc[b], replace=False))
+    acc[5] = N          # out of range
+    acc[6] = max(acc[6], 2)
+    path[6, :3] = [0, 4, 4]  # not increasing
+    path[7, 0] = 1      # does not start at 0
+    seq[8] = max_ctx - N + 1  # overflows max_ctx
+    rt_o = slots.copy()
+    o = oracle.compact_slots(seq, path, acc, rt_o, ps)
+    rt_g = dev(slots)
+    stats = sd.new_stats()
+    g = sd.spec_compact_slots(dev(seq), dev(path), dev(acc), rt_g, ps, stats=stats)
+    torch.cuda.synchronize()
+    for name in ("move_src", "move_dst", "num_moves", "new_kv_len"):
+        np.testing.assert_array_equal(g[name].cpu().numpy(), o[name], err_msg=name)
+    nf = int(g["num_freed"].item())
+    assert nf == len(o["freed"])
+    np.testing.assert_array_equal(g["freed"][:nf].cpu().numpy(), o["freed"])
+    np.testing.assert_array_equal(rt_g.cpu().numpy(), rt_o)
+    assert int(stats[sd.STATS["bad_request"]]) == int(o["bad"][0]) >= 4
+
+
 # --------------------------------------------------------------------- TLI
 
 # Cases: the resident-bitmap kernel with the intersection logits in shared
