@@ -489,12 +489,28 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     if (warp == 0) warp_select_k<1>(lv, li, THREADS, fv, fi);
   } else {
     // threshold: the K-th best of the thread bests (K distinct elements
-    // come before or at it), by K rounds of a warp argmax in warp 0
-    if (warp == 0) {
-      warp_select_k<K>(lv, li, THREADS, fv, fi);
-      if (lane == 0) {
-        s_tv = fv[K - 1];
-        s_ti = fi[K - 1];
+    // come before or at it).  With 128 threads every thread ranks its own
+    // best among them (pairs are distinct but for empty (-inf, INT_MAX)
+    // ones; with fewer than K real bests no thread ranks K-1 and everything
+    // qualifies); with more threads (few rows, 512-thread CTAs) the ranking
+    // costs more than K rounds of a warp argmax in warp 0, measured.
+    if constexpr (THREADS > 128) {
+      if (warp == 0) {
+        warp_select_k<K>(lv, li, THREADS, fv, fi);
+        if (lane == 0) {
+          s_tv = fv[K - 1];
+          s_ti = fi[K - 1];
+        }
+      }
+    } else {
+      const float mv = lv[threadIdx.x];
+      const int mi = li[threadIdx.x];
+      int rk = 0;
+#pragma unroll 8
+      for (int e = 0; e < THREADS; ++e) rk += before(lv[e], li[e], mv, mi) ? 1 : 0;
+      if (rk == K - 1 && mi != INT_MAX) {
+        s_tv = mv;
+        s_ti = mi;
       }
     }
     __syncthreads();
