@@ -98,15 +98,17 @@ struct TopK {
 // a thread whose keys are all -inf ends with bi = INT_MAX and takes its
 // first element afterwards (own_first).  For K == 1 the block's best is the
 // top-1; for K > 1 the thread bests give the pass-B threshold.
-template <int DT>
+template <int DT, bool SECOND = false>
 struct ArgmaxVisitor {
   float c, m, mc, s0, s1;  // mc = m c
   int bi;
+  float m2v;  // SECOND: the largest key of the thread's other elements (NaN skipped)
   __device__ __forceinline__ void reset() {
     m = neg_inf();
     mc = 0.0f;
     s0 = s1 = 0.0f;
     bi = INT_MAX;
+    m2v = neg_inf();
   }
   __device__ __forceinline__ void rescale(float nm) {
     if (m == neg_inf()) {
@@ -123,8 +125,11 @@ struct ArgmaxVisitor {
     if (!ok) return;
     const float xk = order_key(x);
     if (xk > m) {
+      if (SECOND) m2v = m;
       rescale(xk);
       bi = static_cast<int>(idx);
+    } else if (SECOND) {
+      m2v = fmaxf(m2v, xk);
     }
     if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
   }
@@ -143,8 +148,18 @@ struct ArgmaxVisitor {
 #pragma unroll
       for (int j = kv - 1; j >= 0; --j)
         if (x[j] == vmax) j0 = j;
+      if (SECOND) {
+        // the old best and the vector's other elements
+        float sec = m;
+#pragma unroll
+        for (int j = 0; j < kv; ++j)
+          if (j != j0) sec = fmaxf(sec, x[j]);
+        m2v = sec;
+      }
       rescale(vmax);
       bi = static_cast<int>(first) + j0;
+    } else if (SECOND && ok) {
+      m2v = fmaxf(m2v, vmax);
     }
     if (m != neg_inf()) {
       const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
@@ -454,8 +469,9 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
-  // pass A: online softmax and every thread's best element
-  ArgmaxVisitor<DT> st{c};
+  // pass A: online softmax and every thread's best element (and for K > 1
+  // the largest key among its other elements)
+  ArgmaxVisitor<DT, (K > 1)> st{c};
   st.reset();
   for_row_fast<DT, kDraftUnroll>(row, V, st, threadIdx.x, THREADS);
   st.own_first(row, V, threadIdx.x);
@@ -521,7 +537,15 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     float* cv = reinterpret_cast<float*>(dsm);
     int* ci = reinterpret_cast<int*>(cv + kCandCap);
     CandVisitor<DT> cand{tv, ti, cv, ci, &s_cnt};
-    if (cand.qualifies(st.m, st.bi)) s_owner[atomicAdd(&s_nown, 1)] = threadIdx.x;
+    if (cand.qualifies(st.m, st.bi)) {
+      // a thread whose other elements are all below the threshold's key
+      // contributes its best alone; the others are read again
+      if (st.m2v >= tv) {
+        s_owner[atomicAdd(&s_nown, 1)] = threadIdx.x;
+      } else {
+        cand.add(st.m, st.bi);
+      }
+    }
     __syncthreads();
     rescan_owners<DT>(row, V, cand, s_owner, s_nown, THREADS);
     __syncthreads();
