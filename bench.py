@@ -270,7 +270,9 @@ def run_ours(args, cfg, mode, rank, world):
     total_ms_max, tokens_all = reduce_over_ranks(total_ms, committed * args.steps, world, dev)
     value = tokens_all / (total_ms_max / 1e3)
 
-    # dominant kernel: the draft-step softmax/top-k (or TLI constrain) launches
+    peak, peak_kind = hbm_peak()
+    # the draft kernel: the draft-step softmax/top-k (or softmax+draw, or TLI
+    # constrain) launches of steps >= 1, each timed on its own
     if cfg.kind == "tli":
         per_row = cfg.V * 2 + (cfg.V_t * 4 if mode == "sample" else 0)
         kname = "tli_planned_kernel"
@@ -279,24 +281,38 @@ def run_ours(args, cfg, mode, rank, world):
         kname = "softmax_sample_kernel" if (cfg.kind == "chain" and mode == "sample") else DOMINANT
     dom_avg_ms = statistics.mean(dom_ms) if dom_ms else None
     dom_bytes = per_row * statistics.mean(dom_rows) if dom_rows else None
-    peak, peak_kind = hbm_peak()
-    achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9 if dom_ms else None
-    roofline = None
-    if achieved:
-        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
-                    "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    "bytes_per_launch": int(dom_bytes), "avg_launch_us": round(dom_avg_ms * 1e3, 2),
-                    "traffic": ncu_traffic(kname, cfg.name)}
+    draft_roof = None
+    if dom_ms:
+        achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9
+        draft_roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                      "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                      "bytes_per_launch": int(dom_bytes), "avg_launch_us": round(dom_avg_ms * 1e3, 2),
+                      "launches_per_step": len(dom_ms) // max(args.steps, 1),
+                      "traffic": ncu_traffic(kname, cfg.name)}
 
     # the batched verify (row statistics of every target row + tree walk):
-    # target-logit bytes read / its time
+    # target-logit bytes read / its time.  Stochastic: one launch
+    # (sample_verify_kernel; its flag reset is a 4-byte-per-row memset in the
+    # same timed interval); greedy: the argmax pass and the walk.
     verify = None
+    verify_roof = None
     if verify_events:
         v_ms = statistics.mean(a.elapsed_time(b) for a, b in verify_events)
         v_bytes = cfg.B * cfg.N * (cfg.V_t or cfg.V) * (2 if cfg.dtype == torch.bfloat16 else 4)  # target rows
         v_gbs = v_bytes / (v_ms * 1e-3) / 1e9
         verify = {"us_per_step": round(v_ms * 1e3, 2), "logit_bytes": int(v_bytes), "achieved": round(v_gbs, 1),
                   "peak": peak, "unit": "GB/s", "frac": round(v_gbs / peak, 4)}
+        vname = "sample_verify_kernel" if mode == "sample" else "row_argmax_kernel"
+        verify_roof = {"bound": "hbm", "kernel": vname if mode == "sample" else vname + " (+ greedy_walk_kernel)",
+                       "achieved": round(v_gbs, 1), "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                       "frac": round(v_gbs / peak, 4), "bytes_per_launch": int(v_bytes),
+                       "avg_launch_us": round(v_ms * 1e3, 2), "launches_per_step": 1,
+                       "traffic": ncu_traffic(vname, cfg.name)}
+    # the dominant kernel is the one with the larger time per step
+    roofline = draft_roof
+    if verify_roof and (draft_roof is None or verify_roof["avg_launch_us"] >
+                        draft_roof["avg_launch_us"] * draft_roof["launches_per_step"]):
+        roofline = verify_roof
 
     # e2e: host buffers through the same API, copies inside the timed region
     e2e = run_e2e(args, cfg, mode, work, buf, target, step, compact) if not args.no_e2e else None
@@ -315,7 +331,8 @@ def run_ours(args, cfg, mode, rank, world):
                    "l2": "inputs larger than L2 (draft + target logits), no flush"},
         "us_per_step_median": round(statistics.median(step_ms) * 1e3, 2),
         "verified_tokens_per_step": committed, "mean_accept_length": round(accept, 3),
-        "roofline": roofline, "verify": verify, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "roofline": roofline, "rooflines": {"draft": draft_roof, "verify": verify_roof}, "verify": verify,
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "stats": buf.stats.cpu().tolist(),
     }
     return line, work
