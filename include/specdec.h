@@ -194,6 +194,16 @@ int spec_build_tree(int B, int k, int num_steps, int N, const float* pool_score,
 
 /* ----------------------------------------------------------------- verify */
 
+/* The bounded wait the stochastic verify's CTAs use on each other's row
+ * flags, exposed for testing its failure path: one thread waits until
+ * *flag != 0 (acquire load at GPU scope) or limit_cycles SM clock cycles
+ * pass.  *seen = 1 if the flag was seen; on timeout *seen = 0 and
+ * SPEC_STAT_WAIT_TIMEOUT is counted in stats_or_null.  The kernel always
+ * returns, so a flag that nothing sets costs limit_cycles and leaves the
+ * context usable. */
+int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_t* stats_or_null, int32_t* seen,
+                    spec_stream_t stream);
+
 /* Scratch bytes for spec_verify_greedy / spec_verify_sample (per-row
  * max, normaliser and argmax of the target logits). */
 size_t spec_verify_ws_size(int B, int N);

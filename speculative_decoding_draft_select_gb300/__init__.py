@@ -20,7 +20,7 @@ __all__ = [
     "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
     "spec_verify_sample_qlogits", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_plan_bytes", "tli_plan_build", "tli_map_ids",
-    "tli_check_config",
+    "tli_check_config", "spec_wait_probe",
     "new_stats", "new_pool",
 ]
 
@@ -65,6 +65,7 @@ _SIGS = {
     "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P]),
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
+    "spec_wait_probe": (_I, [_P, _I64, _P, _P, _P]),
     "tli_check_config": (_I, [_I, _I, _I]),
 }
 
@@ -402,6 +403,16 @@ def spec_compact_slots(seq_lens, accept_path, accept_length, req_to_token, page_
 
 
 # --------------------------------------------------------------------- TLI
+
+def spec_wait_probe(flag, limit_cycles, stats=None, seen=None):
+    """Runs the verify's bounded flag wait once (see include/specdec.h);
+    returns the int32 device tensor `seen` (1: the flag was set)."""
+    _dev(flag, torch.int32, "flag")
+    _dev(stats, torch.int32, "stats")
+    seen = _out(seen, (1,), torch.int32, flag, "seen")
+    _call("spec_wait_probe", _ptr(flag), int(limit_cycles), _ptr(stats), _ptr(seen), _stream())
+    return seen
+
 
 def tli_plan_bytes(Vd, Vt) -> int:
     n = lib().tli_plan_bytes(int(Vd), int(Vt))

@@ -60,6 +60,26 @@ __host__ __device__ constexpr int walk_ring_depth(int chunks) {
 // launch counts SPEC_STAT_WAIT_TIMEOUT and goes on.
 constexpr long long kWaitLimitCycles = 100000000LL;
 
+// Waits (one thread) until *flag != 0 or `limit` clock cycles pass; a
+// timeout is counted in SPEC_STAT_WAIT_TIMEOUT.  Returns whether the flag
+// was seen.
+__device__ __forceinline__ bool wait_flag(const int* flag, long long limit, int32_t* stats) {
+  const long long t0 = clock64();
+  while (!ld_acquire_gpu(flag)) {
+    if (clock64() - t0 > limit) {
+      bump(stats, SPEC_STAT_WAIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  return true;
+}
+
+__global__ void wait_probe_kernel(const int* flag, long long limit, int32_t* stats, int32_t* seen) {
+  pdl_enter();
+  if (threadIdx.x == 0) *seen = wait_flag(flag, limit, stats) ? 1 : 0;
+}
+
 __device__ __forceinline__ float prob_of(float key, float c, float mc, float invz) {
   return fminf(fast_exp2(fmaf(key, c, -mc)) * invz, 1.0f);
 }
@@ -638,16 +658,7 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
         continue;
       }
       // every row is taken: row r is in flight on a running CTA
-      if (tid == 0) {
-        const long long t0 = clock64();
-        while (!ld_acquire_gpu(ready + r)) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            bump(stats, SPEC_STAT_WAIT_TIMEOUT);
-            break;
-          }
-          __nanosleep(128);
-        }
-      }
+      if (tid == 0) wait_flag(ready + r, kWaitLimitCycles, stats);
       __syncthreads();
       break;
     }
@@ -855,6 +866,14 @@ int check_common(int B, int N, int64_t V, int dtype, const void* target, const i
 }  // namespace specdec
 
 using namespace specdec;
+
+extern "C" int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_t* stats, int32_t* seen,
+                               spec_stream_t stream) {
+  if (!flag || !seen || limit_cycles < 0) return SPEC_ERR_INVALID_ARG;
+  launch_k(wait_probe_kernel, 1, 32, 0, reinterpret_cast<cudaStream_t>(stream), flag,
+           static_cast<long long>(limit_cycles), stats, seen);
+  return launch_status();
+}
 
 extern "C" size_t spec_verify_ws_size(int B, int N) {
   if (B < 0 || N < 1) return 0;

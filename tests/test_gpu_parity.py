@@ -5,6 +5,7 @@ paths, compacted slots) bit-exact; probabilities within 1e-5 absolute; a
 sampled token or acceptance decision may differ only where the oracle's
 uniform lies within 1e-5 of the decision boundary (counted)."""
 import math
+import time
 
 import numpy as np
 import pytest
@@ -520,6 +521,35 @@ def test_compact_many_requests_and_bad_ones(ps):
     np.testing.assert_array_equal(g["freed"][:nf].cpu().numpy(), o["freed"])
     np.testing.assert_array_equal(rt_g.cpu().numpy(), rt_o)
     assert int(stats[sd.STATS["bad_request"]]) == int(o["bad"][0]) >= 4
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """The flag wait of the stochastic verify, on a flag that nothing sets:
+    it gives up after its limit, counts the timeout, and the next launches
+    run normally (a set flag is seen at once)."""
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stats = sd.new_stats()
+    t0 = time.perf_counter()
+    seen = sd.spec_wait_probe(flag, 4_000_000, stats=stats)  # about 2 ms of SM clock
+    torch.cuda.synchronize()
+    assert int(seen.item()) == 0
+    assert int(stats[sd.STATS["wait_timeout"]]) == 1
+    assert time.perf_counter() - t0 < 5.0
+    flag.fill_(1)
+    seen = sd.spec_wait_probe(flag, 4_000_000, stats=stats)
+    torch.cuda.synchronize()
+    assert int(seen.item()) == 1
+    assert int(stats[sd.STATS["wait_timeout"]]) == 1
+    # the context is intact: a verify launch afterwards matches the oracle
+    rng = np.random.default_rng(3)
+    B, N, V = 8, 4, 300
+    target = make_logits(rng, B * N, V, torch.float32).view(B, N, V)
+    draft = rng.integers(0, V, (B, N)).astype(np.int32)
+    nt, ns = chain_meta(B, N)
+    g = sd.spec_verify_greedy(dev(target), dev(draft), dev(nt), dev(ns))
+    o = oracle.verify_greedy(np_logits(target), draft, nt, ns)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(g["committed"].cpu().numpy(), o["committed"])
 
 
 # --------------------------------------------------------------------- TLI
