@@ -168,6 +168,39 @@ int spec_tree_expand(int step, int num_steps, int B, int k, const float* topk_p,
                      int32_t* pool_parent, int32_t* pool_qrow, float* frontier_score,
                      int32_t* frontier_id, spec_stream_t stream);
 
+/* One step of the expansion above, fused into a draft launch: the CTA
+ * that completes a request's rows of the step (its one row at step 0 or
+ * with k = 1, its k rows after) expands the request, so a draft step is
+ * one launch instead of two.  The pool, frontier and step fields are those
+ * of spec_tree_expand; counters is [B] int32, zero before the first fused
+ * step (the expanding CTA returns it to zero), needed when k > 1. */
+typedef struct spec_expand {
+  int step, num_steps, B, k;
+  float* pool_score;
+  int32_t* pool_token;
+  int32_t* pool_parent;
+  int32_t* pool_qrow;
+  float* frontier_score;
+  int32_t* frontier_id;
+  int32_t* counters;
+} spec_expand_t;
+
+/* spec_softmax_topk with the step's pool expansion fused (expand->k == k;
+ * R = expand->B at step 0, expand->B * k after; topk_p / topk_idx laid out
+ * as spec_tree_expand reads them). */
+int spec_softmax_topk_expand(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
+                             float* topk_p, int32_t* topk_idx, float* probs_or_null,
+                             float* row_stats_or_null, int32_t* stats_or_null, const spec_expand_t* expand,
+                             spec_stream_t stream);
+
+/* spec_softmax_sample with the step's pool expansion fused, for chains:
+ * expand->k == 1, R = expand->B, out_prob required (the drawn token and its
+ * probability are the step's top-1). */
+int spec_softmax_sample_expand(const void* logits, int dtype, int64_t R, int64_t V, float T, const float* u,
+                               int32_t* out_token, float* out_prob, float* row_stats_or_null,
+                               float* probs_or_null, int32_t* stats_or_null, const spec_expand_t* expand,
+                               spec_stream_t stream);
+
 /* Tree build ([HB] "Drafting, verification and slots": build_eagle_tree
  * produces the attention mask and positions; [ZS] 5.2 lists the verify input
  * draft_token, positions, custom_mask and retrieve_*).  The N-1 best pool
@@ -395,6 +428,15 @@ int tli_constrain_map_planned(int64_t R, int64_t V_d, int64_t V_t, const void* d
                               const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
                               int32_t* top1_draft, int32_t* top1_target, float* top1_p,
                               float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream);
+
+/* tli_constrain_map_planned with the step's pool expansion fused (a chain:
+ * expand->k == 1, R = expand->B; the mapped top-1 and its probability are
+ * the step's top-1). */
+int tli_constrain_map_planned_expand(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                                     const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
+                                     int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                                     float* q_target_or_null, int32_t* stats_or_null, const spec_expand_t* expand,
+                                     spec_stream_t stream);
 
 /* Id remapping in either direction ([TLI] Modifications:
  * map_target_to_draft_ids / map_draft_to_target_ids): out[i] = table[in[i]]

@@ -62,12 +62,33 @@ _SIGS = {
     "tli_plan_bytes": (_I64, [_I64, _I64]),
     "tli_plan_build": (_I, [_I64, _I64, _P, _P, _P, _P]),
     "tli_constrain_map_planned": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P]),
+    "tli_constrain_map_planned_expand": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P,
+                                              _P]),
+    "spec_softmax_topk_expand": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "spec_softmax_sample_expand": (_I, [_P, _I, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P]),
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
     "spec_wait_probe": (_I, [_P, _I64, _P, _P, _P]),
     "tli_check_config": (_I, [_I, _I, _I]),
 }
+
+
+class _Expand(ctypes.Structure):
+    """spec_expand_t of include/specdec.h."""
+    _fields_ = [("step", ctypes.c_int), ("num_steps", ctypes.c_int), ("B", ctypes.c_int), ("k", ctypes.c_int),
+                ("pool_score", _P), ("pool_token", _P), ("pool_parent", _P), ("pool_qrow", _P),
+                ("frontier_score", _P), ("frontier_id", _P), ("counters", _P)]
+
+
+def _expand(expand):
+    """(pool, step) -> a ctypes pointer to its spec_expand_t (None -> None)."""
+    if expand is None:
+        return None
+    pool, step = expand
+    x = _Expand(int(step), pool["num_steps"], pool["B"], pool["k"], *(pool[n].data_ptr() for n in (
+        "score", "token", "parent", "qrow", "frontier_score", "frontier_id", "counters")))
+    return ctypes.pointer(x)
 
 
 class SpecError(RuntimeError):
@@ -140,9 +161,10 @@ def new_stats(device="cuda"):
 # ------------------------------------------------------------------- draft
 
 def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want_probs=False, row_stats=None,
-                      stats=None):
+                      stats=None, expand=None):
     """logits [R, V] -> (topk_p [R, k] f32, topk_idx [R, k] i32, probs [R, V] f32 or None).
-    row_stats [R, 2] f32 (optional) receives each row's (max, normaliser)."""
+    row_stats [R, 2] f32 (optional) receives each row's (max, normaliser).
+    expand = (pool, step): the step's pool expansion in the same launch."""
     _dev(logits, name="logits")
     V = logits.shape[-1]
     R = logits.numel() // V
@@ -153,13 +175,17 @@ def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want
     _dev(probs, torch.float32, "probs")
     _dev(row_stats, torch.float32, "row_stats")
     _dev(stats, torch.int32, "stats")
-    _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
-          _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _stream())
+    if expand is not None:
+        _call("spec_softmax_topk_expand", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
+              _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _expand(expand), _stream())
+    else:
+        _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
+              _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _stream())
     return topk_p, topk_idx, probs
 
 
 def spec_softmax_sample(logits, T, u, out_token=None, out_prob=None, row_stats=None, probs=None, want_probs=False,
-                        stats=None):
+                        stats=None, expand=None):
     """Draft softmax and one inverse-CDF token per row in one pass:
     logits [R, V], u [R] -> (out_token [R] i32, out_prob [R] f32, probs or
     None); row_stats [R, 2] (optional) receives (max, normaliser)."""
@@ -174,8 +200,12 @@ def spec_softmax_sample(logits, T, u, out_token=None, out_prob=None, row_stats=N
     _dev(probs, torch.float32, "probs")
     _dev(row_stats, torch.float32, "row_stats")
     _dev(stats, torch.int32, "stats")
-    _call("spec_softmax_sample", _ptr(logits), _logit_code(logits), R, V, float(T), _ptr(u), _ptr(out_token),
-          _ptr(out_prob), _ptr(row_stats), _ptr(probs), _ptr(stats), _stream())
+    if expand is not None:
+        _call("spec_softmax_sample_expand", _ptr(logits), _logit_code(logits), R, V, float(T), _ptr(u),
+              _ptr(out_token), _ptr(out_prob), _ptr(row_stats), _ptr(probs), _ptr(stats), _expand(expand), _stream())
+    else:
+        _call("spec_softmax_sample", _ptr(logits), _logit_code(logits), R, V, float(T), _ptr(u), _ptr(out_token),
+              _ptr(out_prob), _ptr(row_stats), _ptr(probs), _ptr(stats), _stream())
     return out_token, out_prob, probs
 
 
@@ -216,6 +246,7 @@ def new_pool(B, k, num_steps, device="cuda"):
         "qrow": torch.empty((B, P), dtype=torch.int32, device=device),
         "frontier_score": torch.empty((B, k), dtype=torch.float32, device=device),
         "frontier_id": torch.empty((B, k), dtype=torch.int32, device=device),
+        "counters": torch.zeros((B,), dtype=torch.int32, device=device),  # fused expansions: zero between steps
         "B": B, "k": k, "num_steps": num_steps, "P": P,
     }
 
@@ -436,7 +467,7 @@ def tli_plan_build(d2t, t2d, plan=None):
 
 
 def tli_constrain_map(draft_logits, d2t, T, t2d=None, want_q=False, top1_draft=None, top1_target=None,
-                      top1_p=None, q_target=None, stats=None, plan=None):
+                      top1_p=None, q_target=None, stats=None, plan=None, expand=None):
     _dev(draft_logits, name="draft_logits")
     _dev(d2t, torch.int32, "d2t")
     _dev(t2d, torch.int32, "t2d")
@@ -455,10 +486,17 @@ def tli_constrain_map(draft_logits, d2t, T, t2d=None, want_q=False, top1_draft=N
     if plan is not None:
         if plan.dtype != torch.uint8 or not plan.is_cuda or plan.numel() < tli_plan_bytes(Vd, Vt):
             raise ValueError("plan must come from tli_plan_build for these vocabulary sizes")
-        _call("tli_constrain_map_planned", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t),
-              _ptr(t2d), _ptr(plan), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target),
-              _ptr(stats), _stream())
+        if expand is not None:
+            _call("tli_constrain_map_planned_expand", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits),
+                  _ptr(d2t), _ptr(t2d), _ptr(plan), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p),
+                  _ptr(q_target), _ptr(stats), _expand(expand), _stream())
+        else:
+            _call("tli_constrain_map_planned", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits),
+                  _ptr(d2t), _ptr(t2d), _ptr(plan), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p),
+                  _ptr(q_target), _ptr(stats), _stream())
     else:
+        if expand is not None:
+            raise ValueError("a fused expansion needs the map plan")
         _call("tli_constrain_map", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t),
               _ptr(t2d), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target),
               _ptr(stats), _stream())

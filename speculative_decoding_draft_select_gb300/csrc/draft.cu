@@ -18,6 +18,7 @@
 
 #include "cdf.cuh"
 #include "common.cuh"
+#include "expand.cuh"
 
 namespace specdec {
 namespace {
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
-                        int32_t* __restrict__ stats) {
+                        int32_t* __restrict__ stats, ExpandArgs ex) {
   pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
   constexpr int kWarps = THREADS / 32;
@@ -582,8 +583,11 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   const float invz = 1.0f / s;
   if (threadIdx.x < k) {
     const int j = threadIdx.x;
+    const float pj = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
     topk_idx[r * k + j] = fi[j];
-    topk_p[r * k + j] = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
+    topk_p[r * k + j] = pj;
+    // a chain's pool expansion (k = 1) by thread 0 from its own outputs
+    if (ex.k == 1) expand_chain(ex, static_cast<int>(r), pj, fi[j]);
   }
   if (threadIdx.x == 0) {
     if (!finite) bump(stats, SPEC_STAT_NONFINITE_ROW);
@@ -593,6 +597,12 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     }
   }
   if (probs != nullptr) write_probs<DT>(row, V, finite, mc, c, invz, probs + r * V);
+  // a tree's pool expansion (k > 1), by the CTA that completes the
+  // request's rows (dsm holds at least k*k keys: 8 KB for K > 1)
+  if (ex.k > 1) {
+    __shared__ int s_last;
+    expand_if_last(ex, r, threadIdx.x < k, topk_p, topk_idx, reinterpret_cast<uint64_t*>(dsm), &s_last);
+  }
 }
 
 // ---------------------------------------------------------------- sampling
@@ -706,7 +716,8 @@ template <int DT>
 __global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
     softmax_sample_kernel(const void* __restrict__ logits, int64_t V64, float c, const float* __restrict__ u,
                           int32_t* __restrict__ out_token, float* __restrict__ out_prob,
-                          float* __restrict__ row_stats, float* __restrict__ probs, int32_t* __restrict__ stats) {
+                          float* __restrict__ row_stats, float* __restrict__ probs, int32_t* __restrict__ stats,
+                          ExpandArgs ex) {
   pdl_enter();
   constexpr int T = kFusedThreads, U = kFusedRounds, kv = Logit<DT>::kVec, kWarps = T / 32;
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
@@ -857,6 +868,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
         row_stats[2 * r] = M;
         row_stats[2 * r + 1] = Z;
       }
+      if (ex.k != 0) expand_chain(ex, static_cast<int>(r), 0.0f, 0);  // the step's pool expansion
     }
     if (probs) write_probs<DT>(row, V64, false, 0.0f, c, 0.0f, probs + r * V64);
     return;
@@ -959,26 +971,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
   if (tid == 0) {
     const int tok = s_tok;
     out_token[r] = tok;
-    if (out_prob)
-      out_prob[r] = W > 0.0f ? fast_exp2(fmaf(order_key(Logit<DT>::load1(row, tok)), c, -Mc)) / W : 0.0f;
+    const float pr = W > 0.0f ? fast_exp2(fmaf(order_key(Logit<DT>::load1(row, tok)), c, -Mc)) / W : 0.0f;
+    if (out_prob) out_prob[r] = pr;
     if (row_stats) {
       row_stats[2 * r] = M;
       row_stats[2 * r + 1] = Z;
     }
+    if (ex.k != 0) expand_chain(ex, static_cast<int>(r), pr, tok);  // the step's pool expansion
   }
   if (probs) write_probs<DT>(row, V64, true, Mc, c, 1.0f / Z, probs + r * V64);
 }
 
 template <int DT, int K, int THREADS>
 int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
+                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
   constexpr size_t smem = draft_smem_bytes<K>();
   if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K, THREADS>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
   launch_k(softmax_topk_kernel<DT, K, THREADS>, static_cast<unsigned>(R), THREADS, smem, s, logits, V, c, k, topk_p,
-           topk_idx, probs, row_stats, stats);
+           topk_idx, probs, row_stats, stats, ex);
   return launch_status();
 }
 
@@ -989,22 +1002,22 @@ constexpr int64_t kFewRows = 2 * 152;
 
 template <int DT, int K>
 int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
+                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
   if (R <= kFewRows)
-    return launch_softmax_topk_t<DT, K, 512>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+    return launch_softmax_topk_t<DT, K, 512>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
   return launch_softmax_topk_t<DT, K, kDraftThreads>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats,
-                                                     s);
+                                                     ex, s);
 }
 
 template <int DT>
 int dispatch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, cudaStream_t s) {
-  if (k <= 1) return launch_softmax_topk<DT, 1>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
-  if (k <= 2) return launch_softmax_topk<DT, 2>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
-  if (k <= 4) return launch_softmax_topk<DT, 4>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
-  if (k <= 8) return launch_softmax_topk<DT, 8>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
-  if (k <= 16) return launch_softmax_topk<DT, 16>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
-  return launch_softmax_topk<DT, 32>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, s);
+                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
+  if (k <= 1) return launch_softmax_topk<DT, 1>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
+  if (k <= 2) return launch_softmax_topk<DT, 2>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
+  if (k <= 4) return launch_softmax_topk<DT, 4>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
+  if (k <= 8) return launch_softmax_topk<DT, 8>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
+  if (k <= 16) return launch_softmax_topk<DT, 16>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
+  return launch_softmax_topk<DT, 32>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
 }
 
 }  // namespace
@@ -1012,32 +1025,62 @@ int dispatch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int
 
 using namespace specdec;
 
-extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
-                                 float* topk_p, int32_t* topk_idx, float* probs_or_null,
-                                 float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+namespace {
+int softmax_topk_impl(const void* logits, int dtype, int64_t R, int64_t V, float T, int k, float* topk_p,
+                      int32_t* topk_idx, float* probs_or_null, float* row_stats_or_null, int32_t* stats_or_null,
+                      const spec_expand_t* expand, spec_stream_t stream) {
   if (R < 0 || V < 1 || k < 1 || k > V || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
   if (R > 0 && (logits == nullptr || topk_p == nullptr || topk_idx == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (k > SPEC_MAX_TOPK || V > SPEC_MAX_VOCAB || R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  ExpandArgs ex = no_expand();
+  if (expand != nullptr) {
+    const int e = expand_args(expand, k, R, ex);
+    if (e != SPEC_OK) return e;
+  }
   if (R == 0) return SPEC_OK;
   const float c = kLog2e / T;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return dtype == SPEC_BF16
              ? dispatch_softmax_topk<SPEC_BF16>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
-                                                row_stats_or_null, stats_or_null, s)
+                                                row_stats_or_null, stats_or_null, ex, s)
              : dispatch_softmax_topk<SPEC_F32>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
-                                               row_stats_or_null, stats_or_null, s);
+                                               row_stats_or_null, stats_or_null, ex, s);
+}
+}  // namespace
+
+extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
+                                 float* topk_p, int32_t* topk_idx, float* probs_or_null,
+                                 float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+  return softmax_topk_impl(logits, dtype, R, V, T, k, topk_p, topk_idx, probs_or_null, row_stats_or_null,
+                           stats_or_null, nullptr, stream);
 }
 
-extern "C" int spec_softmax_sample(const void* logits, int dtype, int64_t R, int64_t V, float T, const float* u,
-                                   int32_t* out_token, float* out_prob_or_null, float* row_stats_or_null,
-                                   float* probs_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+extern "C" int spec_softmax_topk_expand(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
+                                        float* topk_p, int32_t* topk_idx, float* probs_or_null,
+                                        float* row_stats_or_null, int32_t* stats_or_null,
+                                        const spec_expand_t* expand, spec_stream_t stream) {
+  if (expand == nullptr) return SPEC_ERR_INVALID_ARG;
+  return softmax_topk_impl(logits, dtype, R, V, T, k, topk_p, topk_idx, probs_or_null, row_stats_or_null,
+                           stats_or_null, expand, stream);
+}
+
+namespace {
+int softmax_sample_impl(const void* logits, int dtype, int64_t R, int64_t V, float T, const float* u,
+                        int32_t* out_token, float* out_prob_or_null, float* row_stats_or_null, float* probs_or_null,
+                        int32_t* stats_or_null, const spec_expand_t* expand, spec_stream_t stream) {
   if (R < 0 || V < 1 || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
   if (R > 0 && (logits == nullptr || u == nullptr || out_token == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
   if (V > (dtype == SPEC_BF16 ? fused_max_vocab<SPEC_BF16>() : fused_max_vocab<SPEC_F32>()))
     return SPEC_ERR_UNSUPPORTED;
+  ExpandArgs ex = no_expand();
+  if (expand != nullptr) {
+    if (out_prob_or_null == nullptr) return SPEC_ERR_INVALID_ARG;
+    const int e = expand_args(expand, 1, R, ex);
+    if (e != SPEC_OK) return e;
+  }
   if (R == 0) return SPEC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float c = kLog2e / T;
@@ -1051,16 +1094,33 @@ extern "C" int spec_softmax_sample(const void* logits, int dtype, int64_t R, int
                                                  static_cast<int>(smem)) != cudaSuccess)
       return SPEC_ERR_CUDA;
     launch_k(softmax_sample_kernel<SPEC_BF16>, grid, kFusedThreads, smem, s, logits, V, c, u, out_token,
-             out_prob_or_null, row_stats_or_null, probs_or_null, stats_or_null);
+             out_prob_or_null, row_stats_or_null, probs_or_null, stats_or_null, ex);
   } else {
     if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_sample_kernel<SPEC_F32>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem)) != cudaSuccess)
       return SPEC_ERR_CUDA;
     launch_k(softmax_sample_kernel<SPEC_F32>, grid, kFusedThreads, smem, s, logits, V, c, u, out_token,
-             out_prob_or_null, row_stats_or_null, probs_or_null, stats_or_null);
+             out_prob_or_null, row_stats_or_null, probs_or_null, stats_or_null, ex);
   }
   return launch_status();
+}
+}  // namespace
+
+extern "C" int spec_softmax_sample(const void* logits, int dtype, int64_t R, int64_t V, float T, const float* u,
+                                   int32_t* out_token, float* out_prob_or_null, float* row_stats_or_null,
+                                   float* probs_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+  return softmax_sample_impl(logits, dtype, R, V, T, u, out_token, out_prob_or_null, row_stats_or_null,
+                             probs_or_null, stats_or_null, nullptr, stream);
+}
+
+extern "C" int spec_softmax_sample_expand(const void* logits, int dtype, int64_t R, int64_t V, float T,
+                                          const float* u, int32_t* out_token, float* out_prob,
+                                          float* row_stats_or_null, float* probs_or_null, int32_t* stats_or_null,
+                                          const spec_expand_t* expand, spec_stream_t stream) {
+  if (expand == nullptr) return SPEC_ERR_INVALID_ARG;
+  return softmax_sample_impl(logits, dtype, R, V, T, u, out_token, out_prob, row_stats_or_null, probs_or_null,
+                             stats_or_null, expand, stream);
 }
 
 extern "C" int spec_sample(const void* logits_or_null, int dtype, const float* probs_or_null, int64_t R,

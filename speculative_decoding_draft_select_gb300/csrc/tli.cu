@@ -24,6 +24,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "expand.cuh"
 
 namespace specdec {
 namespace {
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                        const int32_t* __restrict__ d2t, const int32_t* __restrict__ t2d,
                        const void* __restrict__ plan, float c, int cap, int32_t* __restrict__ top1_draft,
                        int32_t* __restrict__ top1_target, float* __restrict__ top1_p, float* __restrict__ q,
-                       int32_t* __restrict__ stats) {
+                       int32_t* __restrict__ stats, ExpandArgs ex) {
   pdl_enter();
   using E = typename Elem<DT>::T;
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
@@ -627,12 +628,16 @@ __global__ void __launch_bounds__(kResThreads, 1)
     const bool ok = s_bi != INT_MAX && isfinite(s_bv);
     const float mc = s_m * c, invz = 1.0f / s_s;
     if (tid == 0) {
-      // the top-1 outputs (thread 0 alone; the other warps go on)
+      // the top-1 outputs (thread 0 alone; the other warps go on) and the
+      // step's pool expansion for this row's request (a chain: one row each)
       const int best = ok ? (cpt != nullptr ? id_of_rank(mw, W, s_bi) : s_bi) : -1;
+      const int32_t tgt = ok ? __ldg(d2t + best) : -1;
+      const float pr = ok ? fminf(fast_exp2(fmaf(s_bv, c, -mc)) * invz, 1.0f) : 0.0f;
       top1_draft[r] = best;
-      top1_target[r] = ok ? __ldg(d2t + best) : -1;
-      top1_p[r] = ok ? fminf(fast_exp2(fmaf(s_bv, c, -mc)) * invz, 1.0f) : 0.0f;
+      top1_target[r] = tgt;
+      top1_p[r] = pr;
       if (!ok) bump(stats, SPEC_STAT_EMPTY_INTERSECTION);
+      if (ex.k != 0) expand_chain(ex, static_cast<int>(r), pr, tgt);
     }
     if (q != nullptr) {
       float* out = q + r * Vt;
@@ -722,7 +727,7 @@ __global__ void map_ids_kernel(const int32_t* __restrict__ in, int32_t* __restri
 template <int DT>
 bool launch_planned(int64_t R, int64_t Vd, int64_t Vt, const void* draft, const int32_t* d2t, const int32_t* t2d,
                     const void* plan, float c, int32_t* top1_draft, int32_t* top1_target, float* top1_p, float* q,
-                    int32_t* stats, cudaStream_t s) {
+                    int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
   constexpr int64_t esz = DT == SPEC_BF16 ? 2 : 4;
   int dev = 0, sms = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -754,7 +759,7 @@ bool launch_planned(int64_t R, int64_t Vd, int64_t Vt, const void* draft, const 
   const int64_t slots = static_cast<int64_t>(sms) * per_sm;
   const unsigned grid = static_cast<unsigned>(R < slots ? R : slots);
   launch_k(tli_planned_kernel<DT>, grid, kResThreads, smem, s, R, Vd, Vt, draft, d2t, t2d, plan, c,
-           static_cast<int>(cap), top1_draft, top1_target, top1_p, q, stats);
+           static_cast<int>(cap), top1_draft, top1_target, top1_p, q, stats, ex);
   return true;
 }
 
@@ -808,13 +813,19 @@ extern "C" int tli_plan_build(int64_t V_d, int64_t V_t, const int32_t* d2t, cons
   return launch_status();
 }
 
-extern "C" int tli_constrain_map_planned(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
-                                         const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
-                                         int32_t* top1_draft, int32_t* top1_target, float* top1_p,
-                                         float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+namespace {
+int constrain_planned_impl(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                           const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
+                           int32_t* top1_draft, int32_t* top1_target, float* top1_p, float* q_target_or_null,
+                           int32_t* stats_or_null, const spec_expand_t* expand, spec_stream_t stream) {
   if (R < 0 || V_d < 1 || V_t < 1 || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (V_d > SPEC_MAX_VOCAB || V_t > SPEC_MAX_VOCAB || R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  ExpandArgs ex = no_expand();
+  if (expand != nullptr) {
+    const int e = expand_args(expand, 1, R, ex);
+    if (e != SPEC_OK) return e;
+  }
   if (R == 0) return SPEC_OK;
   if (!draft_logits || !d2t || !plan || !top1_draft || !top1_target || !top1_p) return SPEC_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(plan) & 15) != 0) return SPEC_ERR_INVALID_ARG;
@@ -823,13 +834,38 @@ extern "C" int tli_constrain_map_planned(int64_t R, int64_t V_d, int64_t V_t, co
   const float c = kLog2e / T;
   if (dtype == SPEC_BF16 ? launch_planned<SPEC_BF16>(R, V_d, V_t, draft_logits, d2t, t2d_or_null, plan, c,
                                                      top1_draft, top1_target, top1_p, q_target_or_null,
-                                                     stats_or_null, s)
+                                                     stats_or_null, ex, s)
                          : launch_planned<SPEC_F32>(R, V_d, V_t, draft_logits, d2t, t2d_or_null, plan, c, top1_draft,
-                                                    top1_target, top1_p, q_target_or_null, stats_or_null, s))
+                                                    top1_target, top1_p, q_target_or_null, stats_or_null, ex, s))
     return launch_status();
-  // the bitmap does not fit in shared memory: the per-row kernel
-  return tli_constrain_map(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, T, top1_draft, top1_target, top1_p,
-                           q_target_or_null, stats_or_null, stream);
+  // the bitmap does not fit in shared memory: the per-row kernel, and the
+  // expansion as its own launch
+  const int e = tli_constrain_map(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, T, top1_draft, top1_target,
+                                  top1_p, q_target_or_null, stats_or_null, stream);
+  if (e != SPEC_OK || expand == nullptr) return e;
+  return spec_tree_expand(expand->step, expand->num_steps, expand->B, 1, top1_p, top1_target, expand->pool_score,
+                          expand->pool_token, expand->pool_parent, expand->pool_qrow, expand->frontier_score,
+                          expand->frontier_id, stream);
+}
+}  // namespace
+
+extern "C" int tli_constrain_map_planned(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                                         const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
+                                         int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                                         float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream) {
+  return constrain_planned_impl(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, plan, T, top1_draft, top1_target,
+                                top1_p, q_target_or_null, stats_or_null, nullptr, stream);
+}
+
+extern "C" int tli_constrain_map_planned_expand(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits,
+                                                int dtype, const int32_t* d2t, const int32_t* t2d_or_null,
+                                                const void* plan, float T, int32_t* top1_draft,
+                                                int32_t* top1_target, float* top1_p, float* q_target_or_null,
+                                                int32_t* stats_or_null, const spec_expand_t* expand,
+                                                spec_stream_t stream) {
+  if (expand == nullptr) return SPEC_ERR_INVALID_ARG;
+  return constrain_planned_impl(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, plan, T, top1_draft, top1_target,
+                                top1_p, q_target_or_null, stats_or_null, expand, stream);
 }
 
 extern "C" int tli_map_ids(const int32_t* in, int32_t* out, int64_t n, const int32_t* table, int64_t table_len,

@@ -15,76 +15,16 @@
 #include <climits>
 
 #include "common.cuh"
+#include "expand.cuh"
 
 namespace specdec {
 namespace {
 
-// Sort key for (score desc, pool id asc) as an ascending 64-bit integer.
-// NaN sorts as -inf and -0 as +0, matching float comparison.
-__device__ __forceinline__ uint64_t rank_key(float s, int32_t id) {
-  if (s != s) s = neg_inf();
-  if (s == 0.0f) s = 0.0f;
-  uint32_t u = __float_as_uint(s);
-  uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<uint64_t>(~asc) << 32) | static_cast<uint32_t>(id);
-}
-
-__global__ void tree_expand_kernel(int step, int num_steps, int B, int k, int64_t P,
-                                   const float* __restrict__ topk_p,
-                                   const int32_t* __restrict__ topk_idx, float* pool_score,
-                                   int32_t* pool_token, int32_t* pool_parent, int32_t* pool_qrow,
-                                   float* frontier_score, int32_t* frontier_id) {
+__global__ void tree_expand_kernel(ExpandArgs e, const float* __restrict__ topk_p,
+                                   const int32_t* __restrict__ topk_idx) {
   pdl_enter();
   extern __shared__ uint64_t keys[];
-  const int b = blockIdx.x;
-  const int nc = step == 0 ? k : k * k;
-  const int64_t base = step == 0 ? 1 : 1 + k + static_cast<int64_t>(step - 1) * k * k;
-  float* sc = pool_score + b * P;
-  int32_t* tk = pool_token + b * P;
-  int32_t* pa = pool_parent + b * P;
-  int32_t* qr = pool_qrow + b * P;
-
-  if (step == 0) {
-    for (int64_t i = threadIdx.x; i < P; i += blockDim.x) {
-      sc[i] = i == 0 ? 1.0f : 0.0f;
-      tk[i] = -1;
-      pa[i] = -1;
-      qr[i] = i == 0 ? b : -1;
-    }
-    __syncthreads();
-  }
-  float score = 0.0f;
-  const int c = threadIdx.x;
-  if (c < nc) {
-    int32_t tok, par;
-    if (step == 0) {
-      score = __ldg(topk_p + static_cast<int64_t>(b) * k + c);
-      tok = __ldg(topk_idx + static_cast<int64_t>(b) * k + c);
-      par = 0;
-    } else {
-      const int f = c / k, j = c % k;
-      const int64_t row = static_cast<int64_t>(b) * k + f;
-      score = __fmul_rn(frontier_score[row], __ldg(topk_p + row * k + j));
-      tok = __ldg(topk_idx + row * k + j);
-      par = frontier_id[row];
-    }
-    sc[base + c] = score;
-    tk[base + c] = tok;
-    pa[base + c] = par;
-    keys[c] = rank_key(score, static_cast<int32_t>(base + c));
-  }
-  __syncthreads();  // every frontier read above happens before the writes below
-  if (c < nc) {
-    const uint64_t mine = keys[c];
-    int rank = 0;
-    for (int o = 0; o < nc; ++o) rank += keys[o] < mine;
-    if (rank < k) {
-      frontier_score[static_cast<int64_t>(b) * k + rank] = score;
-      frontier_id[static_cast<int64_t>(b) * k + rank] = static_cast<int32_t>(base + c);
-      if (step + 1 < num_steps)
-        qr[base + c] = B + step * B * k + b * k + rank;
-    }
-  }
+  expand_request(e, blockIdx.x, topk_p, topk_idx, keys);
 }
 
 // Exclusive scan of one int per thread (thread order); returns the total.
@@ -273,9 +213,10 @@ extern "C" int spec_tree_expand(int step, int num_steps, int B, int k, const flo
   if (static_cast<int64_t>(B) * k * num_steps > INT_MAX) return SPEC_ERR_UNSUPPORTED;
   const int nc = step == 0 ? k : k * k;
   const int threads = ((nc + 31) / 32) * 32;
-  launch_k(tree_expand_kernel, B, threads, sizeof(uint64_t) * nc, reinterpret_cast<cudaStream_t>(stream), step,
-           num_steps, B, k, P, topk_p, topk_idx, pool_score, pool_token, pool_parent, pool_qrow, frontier_score,
-           frontier_id);
+  const ExpandArgs e{step, num_steps, B, k, P, pool_score, pool_token, pool_parent, pool_qrow, frontier_score,
+                     frontier_id, nullptr};
+  launch_k(tree_expand_kernel, B, threads, sizeof(uint64_t) * nc, reinterpret_cast<cudaStream_t>(stream), e, topk_p,
+           topk_idx);
   return launch_status();
 }
 

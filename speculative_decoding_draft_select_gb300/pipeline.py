@@ -1,18 +1,17 @@
 """One speculative-decoding step over a batch, composed from the C ABI.
 
-Draft side (one launch pair per draft step), as in "[SGLang] Multi-Layer
-EAGLE" sections 2-3 and "EAGLE speculative decoding in four parts",
-"Drafting, verification and slots":
+Draft side (one launch per draft step: the draft kernel also expands the
+candidate pool for its step, the spec_tree_expand step fused), as in
+"[SGLang] Multi-Layer EAGLE" sections 2-3 and "EAGLE speculative decoding
+in four parts", "Drafting, verification and slots":
   - EAGLE tree:  spec_softmax_topk on the step's draft rows (writing the
                  draft distribution q into the step-major table when the
-                 verify samples), then spec_tree_expand;
+                 verify samples);
   - sampled chain: spec_softmax_sample (q or its row statistics, and the
-                 draw with the step's uniforms, in one pass), then
-                 spec_tree_expand with k = 1;
+                 draw with the step's uniforms, in one pass), k = 1;
   - TLI chain:   tli_plan_build once per step (the vocabulary maps'
                  plan), then per draft step tli_constrain_map with it (q in
-                 target order) and spec_tree_expand with the mapped top-1
-                 (SGLang PR #22883).
+                 target order, the mapped top-1 expanded) (SGLang PR #22883).
 then spec_build_tree.  Verify: spec_verify_greedy, or for sampling either
 spec_verify_sample on the written q table (q_mode "probs") or
 spec_verify_sample_qlogits on the draft logits plus the per-row (max,
@@ -29,7 +28,7 @@ from __future__ import annotations
 import torch
 
 from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity, spec_compact_slots,
-               spec_softmax_sample, spec_softmax_topk, spec_tree_expand, spec_verify_greedy, spec_verify_sample,
+               spec_softmax_sample, spec_softmax_topk, spec_verify_greedy, spec_verify_sample,
                spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map, tli_plan_build, tli_plan_bytes)
 
 
@@ -121,26 +120,20 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
         st = buf.q_stats[a:a + r] if buf.q_stats is not None else None
         if timer is not None:
             timer.begin(s)
+        # each draft launch also expands the candidate pool for its step
         if buf.kind == "tli":
             tli_constrain_map(rows, d2t, T, t2d=t2d, top1_draft=buf.top1_draft[a:a + r],
                               top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
-                              stats=buf.stats, plan=buf.tli_plan)
-            if timer is not None:
-                timer.end(s)
-            spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
+                              stats=buf.stats, plan=buf.tli_plan, expand=(buf.pool, s))
         elif buf.kind == "chain" and buf.sampled:
             # softmax (q or its row statistics) and the draw in one pass
             spec_softmax_sample(rows, T, draft_u[a:a + r], out_token=buf.tok[a:a + r], out_prob=buf.prob[a:a + r],
-                                row_stats=st, probs=qs, stats=buf.stats)
-            if timer is not None:
-                timer.end(s)
-            spec_tree_expand(buf.pool, s, buf.prob[a:a + r], buf.tok[a:a + r])
+                                row_stats=st, probs=qs, stats=buf.stats, expand=(buf.pool, s))
         else:
             spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,
-                              stats=buf.stats)
-            if timer is not None:
-                timer.end(s)
-            spec_tree_expand(buf.pool, s, buf.topk_p[s], buf.topk_idx[s])
+                              stats=buf.stats, expand=(buf.pool, s))
+        if timer is not None:
+            timer.end(s)
     spec_build_tree(buf.pool, buf.N, root_token, seq_lens, out=buf.tree)
     return buf.tree
 
@@ -186,7 +179,7 @@ def capture_step(fn, warm=True):
 
 def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> int:
     """Number of kernel launches one step enqueues."""
-    per_step = 2  # softmax/top-k (or softmax and draw, or TLI constrain) + tree expand
+    per_step = 1  # softmax/top-k (or softmax and draw, or TLI constrain) with the pool expansion
     n = buf.steps * per_step + 1  # + build_tree
     if buf.kind == "tli":
         n += 3  # the map plan

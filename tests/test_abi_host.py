@@ -71,6 +71,14 @@ def test_host_side_argument_checks(lib):
                                          null) == -1
     assert lib.tli_constrain_map_planned(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
                                          null) == 0
+    # fused expansion: no expansion struct, or one whose k or row count does not match the launch
+    assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 4, p16, p16, null, null, null, null, null) == -1
+    assert lib.spec_softmax_sample_expand(p16, 1, 8, 100, 1.0, p16, p16, p16, null, null, null, null, null) == -1
+    pool = sd.new_pool(2, 4, 3, device="cpu")
+    ex = sd._expand((pool, 1))
+    assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 2, p16, p16, null, null, null, ex, null) == -1  # k
+    assert lib.spec_softmax_topk_expand(p16, 1, 7, 100, 1.0, 4, p16, p16, null, null, null, ex, null) == -1  # R
+    assert lib.spec_softmax_sample_expand(p16, 1, 2, 100, 1.0, p16, p16, p16, null, null, null, ex, null) == -1
 
 
 def test_sizes_and_config_check(lib):

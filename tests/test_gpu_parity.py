@@ -523,6 +523,65 @@ def test_compact_many_requests_and_bad_ones(ps):
     assert int(stats[sd.STATS["bad_request"]]) == int(o["bad"][0]) >= 4
 
 
+def _pools_equal(a, b):
+    for n in ("score", "token", "parent", "qrow", "frontier_score", "frontier_id", "counters"):
+        assert torch.equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("B,k,steps,V", [(5, 8, 4, 3000), (9, 4, 3, 1000), (7, 1, 5, 777), (3, 32, 2, 4096),
+                                         (400, 8, 2, 600)])
+def test_fused_expansion_equals_separate_launches(B, k, steps, V):
+    """A draft launch with the step's expansion fused writes the same pool
+    and frontier as the draft launch followed by spec_tree_expand (the last
+    CTA of a request's rows expands it; counters return to zero)."""
+    rng = np.random.default_rng(B * 100 + k)
+    pa, pb = sd.new_pool(B, k, steps), sd.new_pool(B, k, steps)
+    for s in range(steps):
+        R = B if s == 0 else B * k
+        x = dev(make_logits(rng, R, V, torch.bfloat16))
+        ta = sd.spec_softmax_topk(x, 0.8, k)
+        sd.spec_tree_expand(pa, s, ta[0], ta[1])
+        tb = sd.spec_softmax_topk(x, 0.8, k, expand=(pb, s))
+        torch.cuda.synchronize()
+        assert torch.equal(ta[0], tb[0]) and torch.equal(ta[1], tb[1])
+        _pools_equal(pa, pb)
+
+
+def test_fused_expansion_sampled_chain_and_tli():
+    """The same for the fused sampler (chain, k = 1) and the planned TLI
+    kernel."""
+    rng = np.random.default_rng(12)
+    B, steps, V = 33, 4, 5000
+    pa, pb = sd.new_pool(B, 1, steps), sd.new_pool(B, 1, steps)
+    for s in range(steps):
+        x = dev(make_logits(rng, B, V, torch.bfloat16))
+        u = dev(rng.random(B).astype(np.float32))
+        ta = sd.spec_softmax_sample(x, 0.9, u)
+        sd.spec_tree_expand(pa, s, ta[1], ta[0])
+        tb = sd.spec_softmax_sample(x, 0.9, u, expand=(pb, s))
+        torch.cuda.synchronize()
+        assert torch.equal(ta[0], tb[0]) and torch.equal(ta[1], tb[1])
+        _pools_equal(pa, pb)
+    Vd, Vt, K = 4097, 3001, 1500
+    dids = np.sort(rng.choice(Vd, K, replace=False))
+    tids = rng.choice(Vt, K, replace=False)
+    d2t = np.full(Vd, -1, np.int32)
+    d2t[dids] = tids
+    t2d = np.full(Vt, -1, np.int32)
+    t2d[tids] = dids
+    plan = sd.tli_plan_build(dev(d2t), dev(t2d))
+    pa, pb = sd.new_pool(B, 1, steps), sd.new_pool(B, 1, steps)
+    for s in range(steps):
+        x = dev(make_logits(rng, B, Vd, torch.bfloat16))
+        ta = sd.tli_constrain_map(x, dev(d2t), 1.0, t2d=dev(t2d), want_q=True, plan=plan)
+        sd.spec_tree_expand(pa, s, ta[2], ta[1])
+        tb = sd.tli_constrain_map(x, dev(d2t), 1.0, t2d=dev(t2d), want_q=True, plan=plan, expand=(pb, s))
+        torch.cuda.synchronize()
+        for u_, v_ in zip(ta, tb):
+            assert torch.equal(u_, v_)
+        _pools_equal(pa, pb)
+
+
 def test_bounded_wait_runs_out_and_the_context_stays_usable():
     """The flag wait of the stochastic verify, on a flag that nothing sets:
     it gives up after its limit, counts the timeout, and the next launches
