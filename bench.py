@@ -214,19 +214,21 @@ def run_ours(args, cfg, mode, rank, world):
     timer = Timer()
     verify_events = []
 
-    def step(record):
+    def step(record, inp=None):
+        """One step; ``inp`` (e2e) replaces the per-step inputs."""
+        w = dict(work, target=target) if inp is None else dict(work, **inp)
         timer.record = record
-        pl.run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], draft_u=work["draft_u"],
-                     d2t=work.get("d2t"), t2d=work.get("t2d"), timer=timer)
+        pl.run_draft(buf, w["draft_table"], cfg.T, w["root_token"], w["seq_lens"], draft_u=w["draft_u"],
+                     d2t=w.get("d2t"), t2d=w.get("t2d"), timer=timer)
         if record:
             ev = (timing_event(), timing_event())
             ev[0].record(torch.cuda.current_stream())
-        pl.run_verify(buf, target, mode, cfg.T, work["coins"], work["u_final"], work.get("budget"), eos)
+        pl.run_verify(buf, w["target"], mode, cfg.T, w["coins"], w["u_final"], w.get("budget"), eos)
         if record:
             ev[1].record(torch.cuda.current_stream())
             verify_events.append(ev)
         if compact:
-            pl.run_compact(buf, work["seq_lens"], work["req_to_token"], cfg.page_size, kv_pool=kv)
+            pl.run_compact(buf, w["seq_lens"], w["req_to_token"], cfg.page_size, kv_pool=kv)
 
     for _ in range(args.warmup):
         step(False)
@@ -340,12 +342,16 @@ def run_ours(args, cfg, mode, rank, world):
 
 def run_e2e(args, cfg, mode, work, buf, target, step_fn, compact):
     """Per step: pinned-host -> device copies of the step's inputs, the step,
-    device -> host copy of its results."""
+    device -> host copy of its results.  The copies of step i+1 run on a
+    copy stream while step i computes (two device input sets); each step
+    waits for its own inputs, and its results are read back before the
+    step's end is timed."""
     inputs = {"draft_table": work["draft_table"], "target": target, "coins": work["coins"],
               "u_final": work["u_final"], "root_token": work["root_token"], "seq_lens": work["seq_lens"]}
     host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inputs.items()}
     for k, v in inputs.items():
         host[k].copy_(v)
+    dev_sets = [inputs, {k: torch.empty_like(v) for k, v in inputs.items()}]
     outs = {"committed": buf.verify_out["committed"], "num_committed": buf.verify_out["num_committed"],
             "accept_length": buf.verify_out["accept_length"], "next_root": buf.verify_out["next_root"]}
     if compact:
@@ -355,20 +361,40 @@ def run_e2e(args, cfg, mode, work, buf, target, step_fn, compact):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     n = max(1, min(args.steps, 10))
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]   # inputs of set j landed
+    consumed = [torch.cuda.Event() for _ in range(2)]  # set j's step done with its inputs
+
+    def upload(i):
+        j = i % 2
+        with torch.cuda.stream(copy):
+            if i >= 2:
+                copy.wait_event(consumed[j])
+            for k, v in dev_sets[j].items():
+                v.copy_(host[k], non_blocking=True)
+            copied[j].record(copy)
+
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     tokens = 0
-    for _ in range(n):
-        for k, v in inputs.items():
-            v.copy_(host[k], non_blocking=True)
-        step_fn(False)
+    upload(0)
+    for i in range(n):
+        j = i % 2
+        if i + 1 < n:
+            upload(i + 1)
+        compute.wait_event(copied[j])
+        step_fn(False, inp=dev_sets[j])
+        consumed[j].record(compute)
         for k, v in outs.items():
             host_out[k].copy_(v, non_blocking=True)
-        torch.cuda.synchronize()
+        compute.synchronize()
         tokens += int(host_out["num_committed"].sum())
+    torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     return {"value": round(tokens / dt, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(dt / n * 1e3, 3)}
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(dt / n * 1e3, 3),
+            "copy_overlap": "inputs of step i+1 copied while step i computes"}
 
 
 # ---------------------------------------------------------------- reference
