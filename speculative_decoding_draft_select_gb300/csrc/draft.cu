@@ -474,7 +474,8 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   // the largest key among its other elements)
   ArgmaxVisitor<DT, (K > 1)> st{c};
   st.reset();
-  for_row_fast<DT, kDraftUnroll>(row, V, st, threadIdx.x, THREADS);
+  // few rows (512-thread CTAs, about one row per SM): more loads in flight
+  for_row_fast<DT, (THREADS > 128 ? 2 * kDraftUnroll : kDraftUnroll)>(row, V, st, threadIdx.x, THREADS);
   st.own_first(row, V, threadIdx.x);
   lv[threadIdx.x] = st.m;
   li[threadIdx.x] = st.bi;
