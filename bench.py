@@ -168,9 +168,10 @@ def run_ours(args, cfg, mode, rank, world):
     work = generate(cfg, dev)
     compact = bool(cfg.page_size)
     sampled = cfg.kind == "chain" and mode == "sample"
-    q_mode = args.q or ("probs" if cfg.kind == "tli" else "logits")
+    q_mode = args.q or "logits"
     buf = pl.StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, dev, want_q=(mode == "sample"),
-                         sampled=sampled, V_t=cfg.V_t or None, page_size=cfg.page_size, q_mode=q_mode)
+                         sampled=sampled, V_t=cfg.V_t or None, page_size=cfg.page_size, q_mode=q_mode,
+                         q_logit_dtype=cfg.dtype)
     eos = int(work["eos_id"])
     kv = work.get("kv_pool")
     # the target model's output for this tree (deterministic draft -> same tree every step)
@@ -276,7 +277,12 @@ def run_ours(args, cfg, mode, rank, world):
     # the draft kernel: the draft-step softmax/top-k (or softmax+draw, or TLI
     # constrain) launches of steps >= 1, each timed on its own
     if cfg.kind == "tli":
-        per_row = cfg.V * 2 + (cfg.V_t * 4 if mode == "sample" else 0)
+        # the draft row read, and q written in target order: fp32
+        # probabilities, or the partners' logits and the row's (m, Z)
+        q_row = 0
+        if mode == "sample":
+            q_row = cfg.V_t * 4 if q_mode == "probs" else cfg.V_t * (row_bytes // cfg.V) + 8
+        per_row = row_bytes + q_row
         kname = "tli_planned_kernel"
     else:
         per_row = row_bytes + (cfg.V * 4 if buf.q is not None else 0)  # read + written q

@@ -438,6 +438,29 @@ int tli_constrain_map_planned_expand(int64_t R, int64_t V_d, int64_t V_t, const 
                                      float* q_target_or_null, int32_t* stats_or_null, const spec_expand_t* expand,
                                      spec_stream_t stream);
 
+/* tli_constrain_map with the constrained draft distribution written in logit
+ * form instead of fp32 probabilities (half the bytes for bf16 logits), for
+ * spec_verify_sample_qlogits:
+ *   q_logits_target [R, V_t] (dtype) out: element t is the draft logit (its
+ *     raw bits) of t's partner d = t2d[t] when 0 <= d < V_d, -inf otherwise;
+ *   q_stats [R, 2] fp32 out: (m, Z), m the row's largest intersection key
+ *     (NaN counted as -inf; -inf for a row with no finite intersection
+ *     logit) and Z = sum over the intersection of 2^((key - m) log2(e) / T).
+ * spec_verify_sample_qlogits(..., q_logits = q_logits_target, q_dtype =
+ * dtype, q_stats, T_q = T) then reads q[t] = min(2^((key_t - m) log2(e) / T)
+ * / Z, 1), bit for bit the probabilities tli_constrain_map writes.
+ * t2d is required.  plan_or_null: a plan from tli_plan_build (the persistent
+ * kernel of tli_constrain_map_planned) or NULL (the per-row kernel).
+ * expand_or_null: the step's pool expansion, as in
+ * tli_constrain_map_planned_expand.  The top-1 outputs and error behaviour
+ * are those of tli_constrain_map; q_logits_target must be element aligned
+ * (16-byte aligned rows take vector stores). */
+int tli_constrain_map_qlogits(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                              const int32_t* d2t, const int32_t* t2d, const void* plan_or_null, float T,
+                              int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                              void* q_logits_target, float* q_stats, int32_t* stats_or_null,
+                              const spec_expand_t* expand_or_null, spec_stream_t stream);
+
 /* Id remapping in either direction ([TLI] Modifications:
  * map_target_to_draft_ids / map_draft_to_target_ids): out[i] = table[in[i]]
  * when 0 <= in[i] < table_len and that entry is >= 0, else fallback_id (the

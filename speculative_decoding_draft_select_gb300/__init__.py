@@ -19,7 +19,8 @@ __all__ = [
     "spec_softmax_topk", "spec_softmax_sample", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
     "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
     "spec_verify_sample_qlogits", "spec_compact_freed_capacity",
-    "spec_compact_slots", "tli_constrain_map", "tli_plan_bytes", "tli_plan_build", "tli_map_ids",
+    "spec_compact_slots", "tli_constrain_map", "tli_constrain_map_qlogits", "tli_plan_bytes", "tli_plan_build",
+    "tli_map_ids",
     "tli_check_config", "spec_wait_probe",
     "new_stats", "new_pool",
 ]
@@ -64,6 +65,7 @@ _SIGS = {
     "tli_constrain_map_planned": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P]),
     "tli_constrain_map_planned_expand": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                               _P]),
+    "tli_constrain_map_qlogits": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_softmax_topk_expand": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P, _P]),
     "spec_softmax_sample_expand": (_I, [_P, _I, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
@@ -501,6 +503,35 @@ def tli_constrain_map(draft_logits, d2t, T, t2d=None, want_q=False, top1_draft=N
               _ptr(t2d), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_target),
               _ptr(stats), _stream())
     return top1_draft, top1_target, top1_p, q_target
+
+
+def tli_constrain_map_qlogits(draft_logits, d2t, t2d, T, plan=None, top1_draft=None, top1_target=None,
+                              top1_p=None, q_logits=None, q_stats=None, stats=None, expand=None):
+    """tli_constrain_map with q in logit form: q_logits [R, V_t] (the draft
+    dtype, each target id's partner logit, -inf without one) and q_stats
+    [R, 2] (max, normaliser) for spec_verify_sample_qlogits with T_q = T."""
+    _dev(draft_logits, name="draft_logits")
+    _dev(d2t, torch.int32, "d2t")
+    _dev(t2d, torch.int32, "t2d")
+    if t2d is None:
+        raise ValueError("t2d is required")
+    Vd = draft_logits.shape[-1]
+    R = draft_logits.numel() // Vd
+    if d2t.numel() != Vd:
+        raise ValueError("d2t must have V_d entries")
+    Vt = t2d.numel()
+    top1_draft = _out(top1_draft, (R,), torch.int32, draft_logits, "top1_draft")
+    top1_target = _out(top1_target, (R,), torch.int32, draft_logits, "top1_target")
+    top1_p = _out(top1_p, (R,), torch.float32, draft_logits, "top1_p")
+    q_logits = _out(q_logits, (R, Vt), draft_logits.dtype, draft_logits, "q_logits")
+    q_stats = _out(q_stats, (R, 2), torch.float32, draft_logits, "q_stats")
+    _dev(stats, torch.int32, "stats")
+    if plan is not None and (plan.dtype != torch.uint8 or not plan.is_cuda or plan.numel() < tli_plan_bytes(Vd, Vt)):
+        raise ValueError("plan must come from tli_plan_build for these vocabulary sizes")
+    _call("tli_constrain_map_qlogits", R, Vd, Vt, _ptr(draft_logits), _logit_code(draft_logits), _ptr(d2t), _ptr(t2d),
+          _ptr(plan), float(T), _ptr(top1_draft), _ptr(top1_target), _ptr(top1_p), _ptr(q_logits), _ptr(q_stats),
+          _ptr(stats), _expand(expand) if expand is not None else None, _stream())
+    return top1_draft, top1_target, top1_p, q_logits, q_stats
 
 
 def tli_map_ids(ids, table, fallback_id, out=None):

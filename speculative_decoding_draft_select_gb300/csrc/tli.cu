@@ -111,10 +111,56 @@ __device__ __forceinline__ float q_of(const void* row, int32_t d, int64_t Vd, bo
 }
 
 template <int DT>
+struct Elem;
+template <>
+struct Elem<SPEC_BF16> {
+  using T = uint16_t;
+  __device__ __forceinline__ static T at(const uint4& raw, int j) {
+    const uint32_t w = j < 2 ? raw.x : j < 4 ? raw.y : j < 6 ? raw.z : raw.w;
+    return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xffffu));
+  }
+  // x as loaded by Logit<SPEC_BF16>::load1 (a bf16 value widened exactly)
+  __device__ __forceinline__ static T of_value(float x) { return static_cast<uint16_t>(__float_as_uint(x) >> 16); }
+  __device__ __forceinline__ static float value(T e) { return __uint_as_float(static_cast<uint32_t>(e) << 16); }
+};
+template <>
+struct Elem<SPEC_F32> {
+  using T = float;
+  __device__ __forceinline__ static T at(const uint4& raw, int j) {
+    return __uint_as_float(j == 0 ? raw.x : j == 1 ? raw.y : j == 2 ? raw.z : raw.w);
+  }
+  __device__ __forceinline__ static T of_value(float x) { return x; }
+  __device__ __forceinline__ static float value(T e) { return e; }
+};
+
+// Where pass 2 writes the constrained draft distribution in target order
+// (each output optional).  q: fp32 probabilities.  ql and qs: the same
+// distribution in logit form -- ql[t] the draft logit (raw bits) of t's
+// partner t2d[t], -inf without one, and qs = (m, Z), the row's largest
+// intersection key and its normaliser sum 2^((key - m) c); the stochastic
+// verify recomputes q[t] = min(2^((key - m) c) / Z, 1) from them with the
+// operations of the written probabilities, bit for bit.
+struct QOut {
+  float* q;
+  void* ql;
+  float* qs;
+};
+
+// 4 consecutive elements with one streaming 8- or 16-byte store
+__device__ __forceinline__ void st_stream4(uint16_t* p, uint16_t a, uint16_t b, uint16_t c, uint16_t d) {
+  asm volatile("st.global.cs.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16)),
+               "r"(static_cast<uint32_t>(c) | (static_cast<uint32_t>(d) << 16))
+               : "memory");
+}
+__device__ __forceinline__ void st_stream4(float* p, float a, float b, float c, float d) {
+  st_stream(p, make_float4(a, b, c, d));
+}
+
+template <int DT>
 __global__ void __launch_bounds__(kTliThreads)
     tli_constrain_kernel(int64_t Vd, int64_t Vt, const void* __restrict__ draft, const int32_t* __restrict__ d2t,
                          const int32_t* __restrict__ t2d, float c, int32_t* __restrict__ top1_draft,
-                         int32_t* __restrict__ top1_target, float* __restrict__ top1_p, float* __restrict__ q,
+                         int32_t* __restrict__ top1_target, float* __restrict__ top1_p, QOut qo,
                          int32_t* __restrict__ stats) {
   pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
@@ -157,11 +203,31 @@ __global__ void __launch_bounds__(kTliThreads)
       top1_target[r] = ok ? __ldg(d2t + bi) : -1;
       top1_p[r] = ok ? fminf(fast_exp2(fmaf(bv, c, -m * c)) * (1.0f / s), 1.0f) : 0.0f;
       if (!ok) bump(stats, SPEC_STAT_EMPTY_INTERSECTION);
+      if (qo.qs != nullptr) {
+        qo.qs[2 * r] = ok ? m : neg_inf();
+        qo.qs[2 * r + 1] = s;
+      }
     }
   }
   __syncthreads();
-  if (q == nullptr) return;
-  float* out = q + r * Vt;
+  if (qo.ql != nullptr) {
+    // logit form: the partners' logits gathered from the row, -inf without one
+    using E = typename Elem<DT>::T;
+    E* lo = static_cast<E*>(qo.ql) + r * Vt;
+    auto l_of = [&](int32_t d) -> E {
+      return Elem<DT>::of_value(d >= 0 && d < Vd ? Logit<DT>::load1(row, d) : neg_inf());
+    };
+    const bool vl =
+        (reinterpret_cast<uintptr_t>(lo) & (4 * esz - 1)) == 0 && (reinterpret_cast<uintptr_t>(t2d) & 15) == 0;
+    const int nl = vl ? static_cast<int>(Vt / 4) : 0;
+    for (int i = threadIdx.x; i < nl; i += kTliThreads) {
+      const int4 d = __ldg(reinterpret_cast<const int4*>(t2d) + i);
+      st_stream4(lo + 4 * i, l_of(d.x), l_of(d.y), l_of(d.z), l_of(d.w));
+    }
+    for (int64_t t = static_cast<int64_t>(nl) * 4 + threadIdx.x; t < Vt; t += kTliThreads) lo[t] = l_of(__ldg(t2d + t));
+  }
+  if (qo.q == nullptr) return;
+  float* out = qo.q + r * Vt;
   const bool ok = s_best >= 0;
   const float mc = s_m * c, invz = s_invz;
   const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (reinterpret_cast<uintptr_t>(t2d) & 15) == 0;
@@ -329,29 +395,24 @@ __global__ void plan_t2r_kernel(const int32_t* __restrict__ t2d, int64_t Vd, int
 // registers, which the per-element work needs.
 constexpr int kResThreads = 1024;
 constexpr int kResRing = 3;  // 16-byte copies in flight per thread (48 KB of shared memory)
+// 16-byte loads of the rank table in flight per thread in the logit-form
+// pass 2 (register loads: the shared-memory port is busy with the gathers)
+constexpr int kP2Unroll = 4;
 
-template <int DT>
-struct Elem;
-template <>
-struct Elem<SPEC_BF16> {
-  using T = uint16_t;
-  __device__ __forceinline__ static T at(const uint4& raw, int j) {
-    const uint32_t w = j < 2 ? raw.x : j < 4 ? raw.y : j < 6 ? raw.z : raw.w;
-    return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xffffu));
+// f(v, i) for the n 16-byte items src[i], each thread taking i = tid + j
+// THREADS in increasing j, U loads in flight per thread.
+template <int THREADS, int U, class F>
+__device__ __forceinline__ void direct_stream(const uint4* __restrict__ src, int n, F&& f) {
+  int i = threadIdx.x;
+  for (; i + (U - 1) * THREADS < n; i += U * THREADS) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = __ldg(src + i + u * THREADS);
+#pragma unroll
+    for (int u = 0; u < U; ++u) f(v[u], i + u * THREADS);
   }
-  // x as loaded by Logit<SPEC_BF16>::load1 (a bf16 value widened exactly)
-  __device__ __forceinline__ static T of_value(float x) { return static_cast<uint16_t>(__float_as_uint(x) >> 16); }
-  __device__ __forceinline__ static float value(T e) { return __uint_as_float(static_cast<uint32_t>(e) << 16); }
-};
-template <>
-struct Elem<SPEC_F32> {
-  using T = float;
-  __device__ __forceinline__ static T at(const uint4& raw, int j) {
-    return __uint_as_float(j == 0 ? raw.x : j == 1 ? raw.y : j == 2 ? raw.z : raw.w);
-  }
-  __device__ __forceinline__ static T of_value(float x) { return x; }
-  __device__ __forceinline__ static float value(T e) { return e; }
-};
+  for (; i < n; i += THREADS) f(__ldg(src + i), i);
+}
 
 // Bits of ids [first, first + N) from the bitmap (N <= 8).
 template <int N>
@@ -537,7 +598,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
     tli_planned_kernel(int64_t R, int64_t Vd, int64_t Vt, const void* __restrict__ draft,
                        const int32_t* __restrict__ d2t, const int32_t* __restrict__ t2d,
                        const void* __restrict__ plan, float c, int cap, int32_t* __restrict__ top1_draft,
-                       int32_t* __restrict__ top1_target, float* __restrict__ top1_p, float* __restrict__ q,
+                       int32_t* __restrict__ top1_target, float* __restrict__ top1_p, QOut qo,
                        int32_t* __restrict__ stats, ExpandArgs ex) {
   pdl_enter();
   using E = typename Elem<DT>::T;
@@ -560,7 +621,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
     reinterpret_cast<uint4*>(mw)[i] = __ldg(reinterpret_cast<const uint4*>(pv.mw) + i);
   const int K = __ldg(pv.K);
   __syncthreads();
-  E* const cpt = (q != nullptr && K <= cap) ? cpt_buf : nullptr;
+  E* const cpt = ((qo.q != nullptr || qo.ql != nullptr) && K <= cap) ? cpt_buf : nullptr;
   const int32_t* t2r = pv.t2r;
 
   // block merge of the per-thread partials into s_m, s_s, s_bv, s_bi
@@ -637,10 +698,14 @@ __global__ void __launch_bounds__(kResThreads, 1)
       top1_target[r] = tgt;
       top1_p[r] = pr;
       if (!ok) bump(stats, SPEC_STAT_EMPTY_INTERSECTION);
+      if (qo.qs != nullptr) {
+        qo.qs[2 * r] = ok ? s_m : neg_inf();
+        qo.qs[2 * r + 1] = s_s;
+      }
       if (ex.k != 0) expand_chain(ex, static_cast<int>(r), pr, tgt);
     }
-    if (q != nullptr) {
-      float* out = q + r * Vt;
+    if (qo.q != nullptr) {
+      float* out = qo.q + r * Vt;
       const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
       if (!ok) {
         // no finite intersection logit: a zero row
@@ -701,6 +766,51 @@ __global__ void __launch_bounds__(kResThreads, 1)
         for (int64_t t = static_cast<int64_t>(nv) * 4 + tid; t < Vt; t += kResThreads) out[t] = q_at(__ldg(t2d + t));
       }
     }
+    if (qo.ql != nullptr) {
+      // logit form: the partners' logits in target order (raw bits, -inf
+      // without a partner), from the shared intersection logits by rank
+      // or gathered from the row
+      E* lo = static_cast<E*>(qo.ql) + r * Vt;
+      const E ninf = Elem<DT>::of_value(neg_inf());
+      const bool vl = (reinterpret_cast<uintptr_t>(lo) & (4 * esz - 1)) == 0;
+      if (cpt != nullptr) {
+        // branch-free for ranked partners and none (-1); a partner outside
+        // the intersection (-2 - d, rare) is read from the row
+        auto near = [&](int32_t k) -> E {
+          const E v = cpt[k > 0 ? k : 0];
+          return k >= 0 ? v : ninf;
+        };
+        auto far = [&](int32_t k) -> E { return Elem<DT>::of_value(Logit<DT>::load1(row, -2 - k)); };
+        auto l_of = [&](int32_t k) -> E { return k < -1 ? far(k) : near(k); };
+        const int nl = vl ? static_cast<int>(Vt / 4) : 0;
+        direct_stream<kResThreads, kP2Unroll>(reinterpret_cast<const uint4*>(t2r), nl, [&](const uint4& kk, int i) {
+          const int32_t k0 = static_cast<int32_t>(kk.x), k1 = static_cast<int32_t>(kk.y);
+          const int32_t k2 = static_cast<int32_t>(kk.z), k3 = static_cast<int32_t>(kk.w);
+          E e0 = near(k0), e1 = near(k1), e2 = near(k2), e3 = near(k3);
+          if (min(min(k0, k1), min(k2, k3)) < -1) {
+            if (k0 < -1) e0 = far(k0);
+            if (k1 < -1) e1 = far(k1);
+            if (k2 < -1) e2 = far(k2);
+            if (k3 < -1) e3 = far(k3);
+          }
+          st_stream4(lo + 4 * i, e0, e1, e2, e3);
+        });
+        for (int64_t t = static_cast<int64_t>(nl) * 4 + tid; t < Vt; t += kResThreads) lo[t] = l_of(__ldg(t2r + t));
+      } else {
+        auto l_of = [&](int32_t d) -> E {
+          return (d >= 0 && d < Vd) ? Elem<DT>::of_value(Logit<DT>::load1(row, d)) : ninf;
+        };
+        const int nl = (vl && (reinterpret_cast<uintptr_t>(t2d) & 15) == 0) ? static_cast<int>(Vt / 4) : 0;
+        ring_stream<kResThreads, kResRing>(reinterpret_cast<const uint4*>(t2d), nl, ring,
+                                           [&](const uint4& d, int i) {
+                                             st_stream4(lo + 4 * i, l_of(static_cast<int32_t>(d.x)),
+                                                        l_of(static_cast<int32_t>(d.y)),
+                                                        l_of(static_cast<int32_t>(d.z)),
+                                                        l_of(static_cast<int32_t>(d.w)));
+                                           });
+        for (int64_t t = static_cast<int64_t>(nl) * 4 + tid; t < Vt; t += kResThreads) lo[t] = l_of(__ldg(t2d + t));
+      }
+    }
     __syncthreads();  // before the next row overwrites the shared logits and statistics
   }
 }
@@ -726,7 +836,7 @@ __global__ void map_ids_kernel(const int32_t* __restrict__ in, int32_t* __restri
 // otherwise.
 template <int DT>
 bool launch_planned(int64_t R, int64_t Vd, int64_t Vt, const void* draft, const int32_t* d2t, const int32_t* t2d,
-                    const void* plan, float c, int32_t* top1_draft, int32_t* top1_target, float* top1_p, float* q,
+                    const void* plan, float c, int32_t* top1_draft, int32_t* top1_target, float* top1_p, QOut qo,
                     int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
   constexpr int64_t esz = DT == SPEC_BF16 ? 2 : 4;
   int dev = 0, sms = 0, optin = 0;
@@ -759,7 +869,7 @@ bool launch_planned(int64_t R, int64_t Vd, int64_t Vt, const void* draft, const 
   const int64_t slots = static_cast<int64_t>(sms) * per_sm;
   const unsigned grid = static_cast<unsigned>(R < slots ? R : slots);
   launch_k(tli_planned_kernel<DT>, grid, kResThreads, smem, s, R, Vd, Vt, draft, d2t, t2d, plan, c,
-           static_cast<int>(cap), top1_draft, top1_target, top1_p, q, stats, ex);
+           static_cast<int>(cap), top1_draft, top1_target, top1_p, qo, stats, ex);
   return true;
 }
 
@@ -768,26 +878,36 @@ bool launch_planned(int64_t R, int64_t Vd, int64_t Vt, const void* draft, const 
 
 using namespace specdec;
 
-extern "C" int tli_constrain_map(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
-                                 const int32_t* d2t, const int32_t* t2d_or_null, float T, int32_t* top1_draft,
-                                 int32_t* top1_target, float* top1_p, float* q_target_or_null,
-                                 int32_t* stats_or_null, spec_stream_t stream) {
+namespace {
+// The per-row kernel (no plan).
+int constrain_rows(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype, const int32_t* d2t,
+                   const int32_t* t2d_or_null, float T, int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                   QOut qo, int32_t* stats_or_null, spec_stream_t stream) {
   if (R < 0 || V_d < 1 || V_t < 1 || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (V_d > SPEC_MAX_VOCAB || V_t > SPEC_MAX_VOCAB || R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
   if (R == 0) return SPEC_OK;
   if (!draft_logits || !d2t || !top1_draft || !top1_target || !top1_p) return SPEC_ERR_INVALID_ARG;
-  if (q_target_or_null && !t2d_or_null) return SPEC_ERR_INVALID_ARG;
+  if ((qo.q || qo.ql) && !t2d_or_null) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float c = kLog2e / T;
   const unsigned grid = static_cast<unsigned>(R);
   if (dtype == SPEC_BF16)
     launch_k(tli_constrain_kernel<SPEC_BF16>, grid, kTliThreads, 0, s, V_d, V_t, draft_logits, d2t, t2d_or_null, c,
-             top1_draft, top1_target, top1_p, q_target_or_null, stats_or_null);
+             top1_draft, top1_target, top1_p, qo, stats_or_null);
   else
     launch_k(tli_constrain_kernel<SPEC_F32>, grid, kTliThreads, 0, s, V_d, V_t, draft_logits, d2t, t2d_or_null, c,
-             top1_draft, top1_target, top1_p, q_target_or_null, stats_or_null);
+             top1_draft, top1_target, top1_p, qo, stats_or_null);
   return launch_status();
+}
+}  // namespace
+
+extern "C" int tli_constrain_map(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                                 const int32_t* d2t, const int32_t* t2d_or_null, float T, int32_t* top1_draft,
+                                 int32_t* top1_target, float* top1_p, float* q_target_or_null,
+                                 int32_t* stats_or_null, spec_stream_t stream) {
+  return constrain_rows(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, T, top1_draft, top1_target, top1_p,
+                        QOut{q_target_or_null, nullptr, nullptr}, stats_or_null, stream);
 }
 
 extern "C" int64_t tli_plan_bytes(int64_t V_d, int64_t V_t) {
@@ -816,7 +936,7 @@ extern "C" int tli_plan_build(int64_t V_d, int64_t V_t, const int32_t* d2t, cons
 namespace {
 int constrain_planned_impl(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
                            const int32_t* d2t, const int32_t* t2d_or_null, const void* plan, float T,
-                           int32_t* top1_draft, int32_t* top1_target, float* top1_p, float* q_target_or_null,
+                           int32_t* top1_draft, int32_t* top1_target, float* top1_p, QOut qo,
                            int32_t* stats_or_null, const spec_expand_t* expand, spec_stream_t stream) {
   if (R < 0 || V_d < 1 || V_t < 1 || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
@@ -829,19 +949,18 @@ int constrain_planned_impl(int64_t R, int64_t V_d, int64_t V_t, const void* draf
   if (R == 0) return SPEC_OK;
   if (!draft_logits || !d2t || !plan || !top1_draft || !top1_target || !top1_p) return SPEC_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(plan) & 15) != 0) return SPEC_ERR_INVALID_ARG;
-  if (q_target_or_null && !t2d_or_null) return SPEC_ERR_INVALID_ARG;
+  if ((qo.q || qo.ql) && !t2d_or_null) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float c = kLog2e / T;
   if (dtype == SPEC_BF16 ? launch_planned<SPEC_BF16>(R, V_d, V_t, draft_logits, d2t, t2d_or_null, plan, c,
-                                                     top1_draft, top1_target, top1_p, q_target_or_null,
-                                                     stats_or_null, ex, s)
+                                                     top1_draft, top1_target, top1_p, qo, stats_or_null, ex, s)
                          : launch_planned<SPEC_F32>(R, V_d, V_t, draft_logits, d2t, t2d_or_null, plan, c, top1_draft,
-                                                    top1_target, top1_p, q_target_or_null, stats_or_null, ex, s))
+                                                    top1_target, top1_p, qo, stats_or_null, ex, s))
     return launch_status();
   // the bitmap does not fit in shared memory: the per-row kernel, and the
   // expansion as its own launch
-  const int e = tli_constrain_map(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, T, top1_draft, top1_target,
-                                  top1_p, q_target_or_null, stats_or_null, stream);
+  const int e = constrain_rows(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, T, top1_draft, top1_target,
+                               top1_p, qo, stats_or_null, stream);
   if (e != SPEC_OK || expand == nullptr) return e;
   return spec_tree_expand(expand->step, expand->num_steps, expand->B, 1, top1_p, top1_target, expand->pool_score,
                           expand->pool_token, expand->pool_parent, expand->pool_qrow, expand->frontier_score,
@@ -854,7 +973,7 @@ extern "C" int tli_constrain_map_planned(int64_t R, int64_t V_d, int64_t V_t, co
                                          int32_t* top1_draft, int32_t* top1_target, float* top1_p,
                                          float* q_target_or_null, int32_t* stats_or_null, spec_stream_t stream) {
   return constrain_planned_impl(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, plan, T, top1_draft, top1_target,
-                                top1_p, q_target_or_null, stats_or_null, nullptr, stream);
+                                top1_p, QOut{q_target_or_null, nullptr, nullptr}, stats_or_null, nullptr, stream);
 }
 
 extern "C" int tli_constrain_map_planned_expand(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits,
@@ -865,7 +984,37 @@ extern "C" int tli_constrain_map_planned_expand(int64_t R, int64_t V_d, int64_t 
                                                 spec_stream_t stream) {
   if (expand == nullptr) return SPEC_ERR_INVALID_ARG;
   return constrain_planned_impl(R, V_d, V_t, draft_logits, dtype, d2t, t2d_or_null, plan, T, top1_draft, top1_target,
-                                top1_p, q_target_or_null, stats_or_null, expand, stream);
+                                top1_p, QOut{q_target_or_null, nullptr, nullptr}, stats_or_null, expand, stream);
+}
+
+extern "C" int tli_constrain_map_qlogits(int64_t R, int64_t V_d, int64_t V_t, const void* draft_logits, int dtype,
+                                         const int32_t* d2t, const int32_t* t2d, const void* plan_or_null, float T,
+                                         int32_t* top1_draft, int32_t* top1_target, float* top1_p,
+                                         void* q_logits_target, float* q_stats, int32_t* stats_or_null,
+                                         const spec_expand_t* expand_or_null, spec_stream_t stream) {
+  if (R > 0) {
+    const uintptr_t esz = dtype == SPEC_BF16 ? 2 : 4;
+    if (!t2d || !q_logits_target || !q_stats) return SPEC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q_logits_target) & (esz - 1)) != 0 ||
+        (reinterpret_cast<uintptr_t>(q_stats) & 3) != 0)
+      return SPEC_ERR_INVALID_ARG;
+  }
+  const QOut qo{nullptr, q_logits_target, q_stats};
+  if (plan_or_null != nullptr)
+    return constrain_planned_impl(R, V_d, V_t, draft_logits, dtype, d2t, t2d, plan_or_null, T, top1_draft,
+                                  top1_target, top1_p, qo, stats_or_null, expand_or_null, stream);
+  if (expand_or_null != nullptr) {
+    ExpandArgs ex = no_expand();
+    const int e = expand_args(expand_or_null, 1, R, ex);
+    if (e != SPEC_OK) return e;
+  }
+  const int e = constrain_rows(R, V_d, V_t, draft_logits, dtype, d2t, t2d, T, top1_draft, top1_target, top1_p, qo,
+                               stats_or_null, stream);
+  if (e != SPEC_OK || expand_or_null == nullptr || R == 0) return e;
+  return spec_tree_expand(expand_or_null->step, expand_or_null->num_steps, expand_or_null->B, 1, top1_p, top1_target,
+                          expand_or_null->pool_score, expand_or_null->pool_token, expand_or_null->pool_parent,
+                          expand_or_null->pool_qrow, expand_or_null->frontier_score, expand_or_null->frontier_id,
+                          stream);
 }
 
 extern "C" int tli_map_ids(const int32_t* in, int32_t* out, int64_t n, const int32_t* table, int64_t table_len,

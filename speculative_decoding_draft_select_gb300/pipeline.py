@@ -11,7 +11,10 @@ in four parts", "Drafting, verification and slots":
                  draw with the step's uniforms, in one pass), k = 1;
   - TLI chain:   tli_plan_build once per step (the vocabulary maps'
                  plan), then per draft step tli_constrain_map with it (q in
-                 target order, the mapped top-1 expanded) (SGLang PR #22883).
+                 target order, the mapped top-1 expanded) (SGLang PR #22883);
+                 with q_mode "logits", tli_constrain_map_qlogits (the
+                 partners' logits in target order and each row's (max,
+                 normaliser): half the bytes of fp32 q for bf16 logits).
 then spec_build_tree.  Verify: spec_verify_greedy, or for sampling either
 spec_verify_sample on the written q table (q_mode "probs") or
 spec_verify_sample_qlogits on the draft logits plus the per-row (max,
@@ -29,7 +32,8 @@ import torch
 
 from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity, spec_compact_slots,
                spec_softmax_sample, spec_softmax_topk, spec_verify_greedy, spec_verify_sample,
-               spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map, tli_plan_build, tli_plan_bytes)
+               spec_verify_sample_qlogits, spec_verify_ws_size, tli_constrain_map, tli_constrain_map_qlogits,
+               tli_plan_build, tli_plan_bytes)
 
 
 def step_offsets(B, topk, steps):
@@ -45,9 +49,9 @@ class StepBuffers:
     """
 
     def __init__(self, kind, B, topk, steps, N, V, device, want_q, sampled=False, V_t=None, page_size=0,
-                 max_ctx=0, q_mode="probs"):
-        if kind == "tli" and q_mode != "probs":
-            raise ValueError("TLI verification reads q in target order: q_mode must be 'probs'")
+                 max_ctx=0, q_mode="probs", q_logit_dtype=torch.bfloat16):
+        if q_mode not in ("probs", "logits"):
+            raise ValueError("q_mode must be 'probs' or 'logits'")
         self.kind, self.B, self.topk, self.steps, self.N, self.V = kind, B, topk, steps, N, V
         self.sampled, self.want_q, self.q_mode = sampled, want_q, q_mode
         self.Vq = V_t if kind == "tli" else V
@@ -60,8 +64,14 @@ class StepBuffers:
                        for s in range(steps)]
         self.topk_idx = [torch.empty((B * (1 if s == 0 else kk), kk), dtype=torch.int32, device=dev)
                          for s in range(steps)]
-        self.q = (torch.empty((self.rows, self.Vq), dtype=torch.float32, device=dev)
-                  if want_q and q_mode == "probs" else None)
+        # q for the verify: fp32 probabilities ("probs"); in logit form the
+        # draft table itself, or for TLI the draft logits mapped into target
+        # order (q_logit_dtype, the draft table's dtype)
+        self.q = None
+        if want_q and q_mode == "probs":
+            self.q = torch.empty((self.rows, self.Vq), dtype=torch.float32, device=dev)
+        elif want_q and kind == "tli":
+            self.q = torch.empty((self.rows, self.Vq), dtype=q_logit_dtype, device=dev)
         self.q_stats = (torch.empty((self.rows, 2), dtype=torch.float32, device=dev)
                         if want_q and q_mode == "logits" else None)
         self.draft_table = None
@@ -121,7 +131,12 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
         if timer is not None:
             timer.begin(s)
         # each draft launch also expands the candidate pool for its step
-        if buf.kind == "tli":
+        if buf.kind == "tli" and st is not None:
+            # q in logit form: the partners' logits in target order and (m, Z)
+            tli_constrain_map_qlogits(rows, d2t, t2d, T, plan=buf.tli_plan, top1_draft=buf.top1_draft[a:a + r],
+                                      top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_logits=qs,
+                                      q_stats=st, stats=buf.stats, expand=(buf.pool, s))
+        elif buf.kind == "tli":
             tli_constrain_map(rows, d2t, T, t2d=t2d, top1_draft=buf.top1_draft[a:a + r],
                               top1_target=buf.tok[a:a + r], top1_p=buf.prob[a:a + r], q_target=qs,
                               stats=buf.stats, plan=buf.tli_plan, expand=(buf.pool, s))
@@ -144,7 +159,8 @@ def run_verify(buf: StepBuffers, target, mode, T=1.0, coins=None, u_final=None, 
         return spec_verify_greedy(target, t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"],
                                   budget=budget, eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)
     if buf.q_mode == "logits":
-        return spec_verify_sample_qlogits(target, T, buf.draft_table, buf.q_stats, buf.T_draft, t["draft_token"],
+        q_logits = buf.q if buf.kind == "tli" else buf.draft_table
+        return spec_verify_sample_qlogits(target, T, q_logits, buf.q_stats, buf.T_draft, t["draft_token"],
                                           t["retrieve_next_token"], t["retrieve_next_sibling"], coins, u_final,
                                           q_row=t["q_row"], budget=budget, eos_id=eos_id, out=buf.verify_out,
                                           ws=buf.ws, stats=buf.stats)

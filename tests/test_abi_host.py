@@ -71,6 +71,20 @@ def test_host_side_argument_checks(lib):
                                          null) == -1
     assert lib.tli_constrain_map_planned(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
                                          null) == 0
+    # q in logit form: t2d and both outputs required, element-aligned logits, T > 0; R = 0 is a no-op
+    p17 = ctypes.c_void_p(17)
+    assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, null, null, 1.0, p16, p16, p16, p16, p16, null,
+                                         null, null) == -1
+    assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, p16, null, 1.0, p16, p16, p16, null, p16, null,
+                                         null, null) == -1
+    assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, p16, null, 1.0, p16, p16, p16, p16, null, null,
+                                         null, null) == -1
+    assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, p16, null, 1.0, p16, p16, p16, p17, p16, null,
+                                         null, null) == -1
+    assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, p16, p16, 0.0, p16, p16, p16, p16, p16, null,
+                                         null, null) == -1
+    assert lib.tli_constrain_map_qlogits(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
+                                         null, null, null) == 0
     # fused expansion: no expansion struct, or one whose k or row count does not match the launch
     assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 4, p16, p16, null, null, null, null, null) == -1
     assert lib.spec_softmax_sample_expand(p16, 1, 8, 100, 1.0, p16, p16, p16, null, null, null, null, null) == -1
@@ -79,6 +93,9 @@ def test_host_side_argument_checks(lib):
     assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 2, p16, p16, null, null, null, ex, null) == -1  # k
     assert lib.spec_softmax_topk_expand(p16, 1, 7, 100, 1.0, 4, p16, p16, null, null, null, ex, null) == -1  # R
     assert lib.spec_softmax_sample_expand(p16, 1, 2, 100, 1.0, p16, p16, p16, null, null, null, ex, null) == -1
+    for plan in (null, p16):  # k = 4 is not a chain
+        assert lib.tli_constrain_map_qlogits(2, 10, 10, p16, 1, p16, p16, plan, 1.0, p16, p16, p16, p16, p16, null,
+                                             ex, null) == -1
 
 
 def test_sizes_and_config_check(lib):

@@ -315,7 +315,8 @@ def small(cfg_name, **kw):
 
 def run_gpu_pipeline(cfg, work, mode, q_mode="probs"):
     buf = StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, "cuda", want_q=(mode == "sample"),
-                      sampled=(cfg.kind == "chain" and mode == "sample"), V_t=cfg.V_t or None, q_mode=q_mode)
+                      sampled=(cfg.kind == "chain" and mode == "sample"), V_t=cfg.V_t or None, q_mode=q_mode,
+                      q_logit_dtype=cfg.dtype)
     tree = run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"],
                      draft_u=work["draft_u"], d2t=work.get("d2t"), t2d=work.get("t2d"))
     target = assemble_target(work, tree["q_row"])
@@ -356,8 +357,9 @@ SMALL = {
 @pytest.mark.parametrize("name,mode,q_mode", [("c1", "greedy", "probs"), ("c1", "sample", "probs"),
                                               ("c1", "sample", "logits"), ("c2", "greedy", "probs"),
                                               ("c3", "sample", "probs"), ("c3", "sample", "logits"),
-                                              ("c4", "sample", "probs"), ("c5", "greedy", "probs"),
-                                              ("c5", "sample", "probs"), ("c5", "sample", "logits")])
+                                              ("c4", "sample", "probs"), ("c4", "sample", "logits"),
+                                              ("c5", "greedy", "probs"), ("c5", "sample", "probs"),
+                                              ("c5", "sample", "logits")])
 def test_pipeline_small(name, mode, q_mode):
     cfg = small(name, **SMALL[name])
     work = generate(cfg, "cuda")
@@ -366,7 +368,7 @@ def test_pipeline_small(name, mode, q_mode):
 
 
 @pytest.mark.parametrize("name,mode,q_mode", [("c2", "greedy", "probs"), ("c3", "sample", "logits"),
-                                              ("c4", "sample", "probs"), ("c5", "greedy", "probs"),
+                                              ("c4", "sample", "logits"), ("c5", "greedy", "probs"),
                                               ("c5", "sample", "logits")])
 def test_pipeline_full_size_sampled_requests(name, mode, q_mode):
     """Full-size workloads in the bench's launch configuration; the oracle
@@ -427,6 +429,52 @@ def test_q_in_logit_form_equals_written_q(qdtype):
     for n in outs[0]:
         assert torch.equal(outs[0][n], outs[1][n]), n
     assert int(outs[0]["accept_length"].sum()) > 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_tli_q_in_logit_form_equals_written_q(dtype):
+    """The TLI step with q in logit form (the partners' logits in target
+    order and each row's max and normaliser, read by
+    spec_verify_sample_qlogits) verifies exactly as with the fp32 q rows."""
+    cfg = small("c4", **SMALL["c4"]).scaled(dtype=dtype)
+    work = generate(cfg, "cuda")
+    outs = []
+    for q_mode in ("probs", "logits"):
+        buf, tree, out = run_gpu_pipeline(cfg, work, "sample", q_mode)
+        outs.append(({n: v.clone() for n, v in out.items()}, {n: v.clone() for n, v in tree.items()}))
+    for n in outs[0][1]:
+        assert torch.equal(outs[0][1][n], outs[1][1][n]), n
+    for n in outs[0][0]:
+        assert torch.equal(outs[0][0][n], outs[1][0][n]), n
+    assert int(outs[0][0]["accept_length"].sum()) > 0
+
+
+def tli_check_qlogits(x, d2t, t2d, T, o, plan):
+    """tli_constrain_map_qlogits against the oracle: the same top-1 outputs,
+    the partners' logits bit for bit (-inf without a partner), m the top-1
+    logit and Z = 1 / its probability, and the q they define."""
+    Vd, Vt = x.shape[1], len(t2d)
+    td, tt, tp, ql, qs = sd.tli_constrain_map_qlogits(dev(x), dev(d2t), dev(t2d), T, plan=plan)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(td.cpu().numpy(), o["top1_draft"])
+    np.testing.assert_array_equal(tt.cpu().numpy(), o["top1_target"])
+    np.testing.assert_allclose(tp.cpu().numpy(), o["top1_p"], atol=PROB_TOL)
+    ok_t = (t2d >= 0) & (t2d < Vd)
+    want = torch.full((x.shape[0], Vt), float("-inf"), dtype=x.dtype)
+    want[:, torch.from_numpy(np.nonzero(ok_t)[0])] = x[:, torch.from_numpy(t2d[ok_t].astype(np.int64))]
+    ibits = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(ql.cpu().view(ibits), want.view(ibits))
+    qs = qs.cpu().numpy().astype(np.float64)
+    full = o["top1_draft"] >= 0
+    xf = x.float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(qs[full, 0], xf[np.nonzero(full)[0], o["top1_draft"][full]])
+    np.testing.assert_allclose(qs[full, 1], 1.0 / o["top1_p"][full], rtol=1e-5)
+    assert np.all(qs[~full, 0] == -np.inf)
+    key = ql.cpu().float().numpy().astype(np.float64)
+    key[np.isnan(key)] = -np.inf
+    with np.errstate(invalid="ignore", over="ignore"):
+        q = np.where(full[:, None], np.exp((key - qs[:, :1]) / T) / qs[:, 1:], 0.0)
+    np.testing.assert_allclose(np.minimum(q, 1.0), o["q_target"], atol=PROB_TOL)
 
 
 def test_worked_example_monte_carlo_gpu(golden):
@@ -650,6 +698,8 @@ def test_tli_parity(Vd, Vt, K, dtype, R):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(td2.cpu().numpy(), o["top1_draft"])
         np.testing.assert_allclose(tp2.cpu().numpy(), o["top1_p"], atol=PROB_TOL)
+        # q in logit form
+        tli_check_qlogits(x, d2t, t2d, 0.9, o, p)
     ids = np.concatenate([dids[:100], np.setdiff1d(np.arange(Vd), dids)[:50], [-3, Vd, Vd + 9]]).astype(np.int32)
     g = sd.tli_map_ids(dev(ids), dev(d2t), 7)
     np.testing.assert_array_equal(g.cpu().numpy(), oracle.map_ids(ids, d2t, 7))
@@ -681,6 +731,7 @@ def test_tli_t2d_outside_intersection():
         torch.cuda.synchronize()
         np.testing.assert_array_equal(td.cpu().numpy(), o["top1_draft"])
         np.testing.assert_allclose(qt.cpu().numpy(), o["q_target"], atol=PROB_TOL)
+        tli_check_qlogits(x, d2t, t2d, 0.8, o, p)
     assert (o["q_target"][:, free_t[:5]] > 0).all()
 
 
