@@ -9,8 +9,9 @@ in four parts", "Drafting, verification and slots":
                  verify samples);
   - sampled chain: spec_softmax_sample (q or its row statistics, and the
                  draw with the step's uniforms, in one pass), k = 1;
-  - TLI chain:   tli_plan_build once per step (the vocabulary maps'
-                 plan), then per draft step tli_constrain_map with it (q in
+  - TLI chain:   tli_plan_build once per vocabulary-map pair (the maps'
+                 plan, rebuilt when the maps change), then per draft step
+                 tli_constrain_map with it (q in
                  target order, the mapped top-1 expanded) (SGLang PR #22883);
                  with q_mode "logits", tli_constrain_map_qlogits (the
                  partners' logits in target order and each row's (max,
@@ -81,6 +82,7 @@ class StepBuffers:
         self.top1_draft = torch.empty((self.rows,), dtype=torch.int32, device=dev)
         self.tli_plan = (torch.empty(tli_plan_bytes(V, V_t), dtype=torch.uint8, device=dev)
                          if kind == "tli" else None)
+        self.tli_plan_key = None  # the maps the plan was built from
         self.tree = None
         self.ws = torch.empty(max(spec_verify_ws_size(B, N), 256), dtype=torch.uint8, device=dev)
         self.verify_out = None
@@ -121,7 +123,13 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
     B, k = buf.B, buf.topk
     buf.draft_table, buf.T_draft = draft_table, T
     if buf.kind == "tli":
-        tli_plan_build(d2t, t2d, plan=buf.tli_plan)
+        # the plan depends on the vocabulary maps alone (fixed for a model
+        # pair): built on first use and again whenever the maps are other
+        # tensors or were modified in place
+        key = (d2t.data_ptr(), d2t._version, d2t.numel(), t2d.data_ptr(), t2d._version, t2d.numel())
+        if buf.tli_plan_key != key:
+            tli_plan_build(d2t, t2d, plan=buf.tli_plan)
+            buf.tli_plan_key = key
     for s in range(buf.steps):
         r = B * (1 if s == 0 else k)
         a = buf.offs[s]
@@ -197,8 +205,7 @@ def kernels_per_step(buf: StepBuffers, mode, compact: bool, kv_pool: bool) -> in
     """Number of kernel launches one step enqueues."""
     per_step = 1  # softmax/top-k (or softmax and draw, or TLI constrain) with the pool expansion
     n = buf.steps * per_step + 1  # + build_tree
-    if buf.kind == "tli":
-        n += 3  # the map plan
+    # (TLI: the map plan's three launches run only when the maps change)
     n += 2 if mode == "greedy" else 1  # verify: row argmax + walk, or the one stochastic launch
     if compact:
         n += 1 + (1 if (kv_pool and buf.compact_out is not None) else 0)

@@ -449,6 +449,46 @@ def test_tli_q_in_logit_form_equals_written_q(dtype):
     assert int(outs[0][0]["accept_length"].sum()) > 0
 
 
+def test_tli_plan_follows_the_maps():
+    """The pipeline builds the map plan once per pair of maps and builds it
+    again when they change (here in place): after the change, the plan and
+    the draft outputs equal those of fresh buffers."""
+    cfg = small("c4", **SMALL["c4"])
+    work = generate(cfg, "cuda")
+    d2t, t2d = work["d2t"], work["t2d"]
+
+    def fresh():
+        return StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, "cuda", want_q=True, V_t=cfg.V_t,
+                           q_mode="logits", q_logit_dtype=cfg.dtype)
+
+    def draft(buf):
+        tree = run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"], d2t=d2t, t2d=t2d)
+        torch.cuda.synchronize()
+        return {n: v.clone() for n, v in tree.items()}, buf.tok.clone(), buf.q.clone()
+
+    buf = fresh()
+    draft(buf)
+    key, plan0 = buf.tli_plan_key, buf.tli_plan.clone()
+    draft(buf)
+    assert buf.tli_plan_key == key  # same maps: not rebuilt
+    # swap the target partners of two intersection ids, in place
+    ids = torch.nonzero(d2t >= 0).flatten()[:2].tolist()
+    ta, tb = int(d2t[ids[0]]), int(d2t[ids[1]])
+    d2t[ids[0]], d2t[ids[1]] = tb, ta
+    t2d[ta], t2d[tb] = ids[1], ids[0]
+    got = draft(buf)
+    assert buf.tli_plan_key != key
+    assert not torch.equal(buf.tli_plan[16:], plan0[16:])
+    ref_buf = fresh()
+    want = draft(ref_buf)
+    # every byte but the header's three pad words (bytes 4..15, never written)
+    assert torch.equal(buf.tli_plan[:4], ref_buf.tli_plan[:4])
+    assert torch.equal(buf.tli_plan[16:], ref_buf.tli_plan[16:])
+    for n in got[0]:
+        assert torch.equal(got[0][n], want[0][n]), n
+    assert torch.equal(got[1], want[1]) and torch.equal(got[2], want[2])
+
+
 def tli_check_qlogits(x, d2t, t2d, T, o, plan):
     """tli_constrain_map_qlogits against the oracle: the same top-1 outputs,
     the partners' logits bit for bit (-inf without a partner), m the top-1
