@@ -187,7 +187,7 @@ def verify_greedy(target, draft_token, next_token, next_sibling, budget=None, eo
 
 
 def verify_sample(target, T: float, q, draft_token, next_token, next_sibling, coins, u_final,
-                  q_row=None, budget=None, eos: int = -1):
+                  q_row=None, budget=None, eos: int = -1, without_replacement: bool = False):
     x, dt = logits_buffer(target)
     B, N, V = x.shape
     qq = _c(q, np.float32)
@@ -205,7 +205,8 @@ def verify_sample(target, T: float, q, draft_token, next_token, next_sibling, co
         ctypes.c_int(B), ctypes.c_int(N), ctypes.c_int64(V), ctypes.c_int(dt), _p(x), ctypes.c_double(T),
         _p(qq), _p(qr), _p(dtok), _p(nt), _p(ns), _p(co), _p(uf), _p(bud), ctypes.c_int32(eos),
         _p(o["committed"]), _p(o["num_committed"]), _p(o["accept_length"]), _p(o["accept_path"]),
-        _p(o["next_root"]), _p(o["walk_info"]), _p(o["margin"]), _p(counters))
+        _p(o["next_root"]), _p(o["walk_info"]), _p(o["margin"]), _p(counters),
+        ctypes.c_int(1 if without_replacement else 0))
     _check(rc, "verify_sample")
     o["q_zero"], o["residual_fallback"], o["cdf_fallback"], o["nonfinite_rows"] = (int(c) for c in counters)
     return o

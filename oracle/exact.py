@@ -12,7 +12,9 @@ exactly.  It is used to pin the C oracle: the pages' worked example (p = [0.4,
 gives 0.56 / 0.44), and the losslessness claim of the same section (the law of
 the committed tokens equals the target's own autoregressive law) for chains
 and for trees whose children are i.i.d. draws from q, tried sibling by sibling
-against the updated residual.
+against the updated residual -- and, for children drawn without replacement,
+with q renormalised after each rejected sibling (the "without replacement"
+variant of the sibling update).
 """
 from __future__ import annotations
 
@@ -76,50 +78,70 @@ def _add(law: Law, seq: Tuple[int, ...], pr: Fraction) -> None:
         law[seq] = law.get(seq, Fraction(0)) + pr
 
 
-def round_law(m: ToyModels, ctx: Tuple[int, ...], width: int, depth: int) -> Law:
+def without(q: Dist, y: int) -> Dist:
+    """q with token y removed and the rest renormalised (all zero when
+    nothing is left)."""
+    w = [Fraction(0) if v == y else x for v, x in enumerate(q)]
+    return normalise(w) if sum(w) > 0 else tuple(Fraction(0) for _ in w)
+
+
+def round_law(m: ToyModels, ctx: Tuple[int, ...], width: int, depth: int, draws: str = "iid",
+              q_update: str = "fixed") -> Law:
     """Law of the tokens committed in one verification round when every tree
-    node has ``width`` children drawn i.i.d. from q(.|node context) down to
+    node has ``width`` children drawn from q(.|node context) down to
     ``depth`` levels (width 1 = a chain of ``depth`` drafts).  Children are
     tried in sibling order against p_cur, which each rejection replaces with
-    the positive residual; with no child accepted the token is drawn from
-    p_cur; at a leaf the bonus is drawn from p."""
+    the positive residual (p_cur - q_cur)+; with no child accepted the token
+    is drawn from p_cur; at a leaf the bonus is drawn from p.
+
+    draws: "iid" -- the children are i.i.d. draws from q; "without" -- drawn
+    one after another without replacement (each from q with the earlier
+    siblings' tokens removed and renormalised).  q_update: "fixed" -- q_cur
+    stays q for every sibling; "renormalise" -- after a rejection of y,
+    q_cur loses y and is renormalised (the without-replacement update)."""
 
     def node(c: Tuple[int, ...], d: int) -> Law:
-        return siblings(c, m.p(c), width if d > 0 else 0, d)
+        q = m.q(c)
+        return siblings(c, m.p(c), q, q, width if d > 0 else 0, d)
 
-    def siblings(c: Tuple[int, ...], pc: Dist, left: int, d: int) -> Law:
+    def siblings(c: Tuple[int, ...], pc: Dist, qc: Dist, qdraw: Dist, left: int, d: int) -> Law:
         law: Law = {}
-        if left == 0:
+        if left == 0 or sum(qdraw) == 0:
             for t, pt in enumerate(pc):
                 _add(law, (t,), pt)
             return law
-        qd = m.q(c)
-        for y, qy in enumerate(qd):
+        for y, qy in enumerate(qdraw):
             if qy == 0:
                 continue
-            a = min(Fraction(1), pc[y] / qy)
+            a = min(Fraction(1), pc[y] / qc[y]) if qc[y] > 0 else Fraction(1 if pc[y] > 0 else 0)
             if a > 0:
                 for seq, pr in node(c + (y,), d - 1).items():
                     _add(law, (y,) + seq, qy * a * pr)
             if a < 1:
-                r = positive_residual(pc, qd)
-                for seq, pr in siblings(c, r, left - 1, d).items():
+                # a residual without mass (possible only when the draws and
+                # the q update do not match) leaves p_cur as it is
+                massless = sum(max(Fraction(0), a_ - b_) for a_, b_ in zip(pc, qc)) == 0
+                r = pc if massless else positive_residual(pc, qc)
+                qn = without(qc, y) if q_update == "renormalise" else qc
+                dn = without(qdraw, y) if draws == "without" else qdraw
+                for seq, pr in siblings(c, r, qn, dn, left - 1, d).items():
                     _add(law, seq, qy * (1 - a) * pr)
         return law
 
     return node(ctx, depth)
 
 
-def spec_law(m: ToyModels, ctx: Tuple[int, ...], M: int, width: int, depth: int) -> Law:
+def spec_law(m: ToyModels, ctx: Tuple[int, ...], M: int, width: int, depth: int, draws: str = "iid",
+             q_update: str = "fixed") -> Law:
     """Law of the first M committed tokens over as many rounds as needed."""
     if M <= 0:
         return {(): Fraction(1)}
     law: Law = {}
-    for seq, pr in round_law(m, ctx, width, depth).items():
+    for seq, pr in round_law(m, ctx, width, depth, draws, q_update).items():
         if len(seq) >= M:
             _add(law, seq[:M], pr)
         else:
-            for rest, pr2 in spec_law(m, ctx + seq, M - len(seq), width, depth).items():
+            for rest, pr2 in spec_law(m, ctx + seq, M - len(seq), width, depth, draws, q_update).items():
                 _add(law, seq + rest, pr * pr2)
     return law
 

@@ -485,7 +485,12 @@ static int softmax_row(const void* x, int dtype, int64_t base, int64_t V, double
  * ratio, or the CDF boundaries around the drawn token): a GPU may disagree
  * only where this is below its tolerance.
  * counters[0] += q[y] == 0 events, counters[1] += residual fallbacks,
- * counters[2] += CDF fallbacks, counters[3] += non-finite target rows. */
+ * counters[2] += CDF fallbacks, counters[3] += non-finite target rows.
+ * without_replacement != 0: the sibling update for children drawn without
+ * replacement -- q_cur starts as the node's q, each rejection of y first
+ * replaces p_cur by the residual of p_cur and q_cur, then sets q_cur[y] = 0
+ * and renormalises q_cur (all zero once no mass is left); the acceptance
+ * ratio of the next sibling is p_cur[y] / q_cur[y]. */
 int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                          double T, const float* q, const int32_t* q_row_or_null,
                          const int32_t* draft_token, const int32_t* next_token,
@@ -494,12 +499,13 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                          int32_t eos, int32_t* committed, int32_t* num_committed,
                          int32_t* accept_length, int32_t* accept_path,
                          int32_t* next_root, int32_t* walk_info, double* margin,
-                         int64_t* counters)
+                         int64_t* counters, int without_replacement)
 {
     if (B < 0 || N < 1 || V < 1 || !(T > 0.0)) return OR_ERR;
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
-    if (!p || !r) { free(p); free(r); return OR_ERR; }
+    double* qw = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!p || !r || !qw) { free(p); free(r); free(qw); return OR_ERR; }
     for (int b = 0; b < B; ++b) {
         int64_t o = (int64_t)b * N;
         for (int i = 0; i < N; ++i) { committed[o + i] = -1; accept_path[o + i] = -1; }
@@ -516,10 +522,11 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                 if (next_token[o + n] >= 0) {
                     int64_t qrow = q_row_or_null ? q_row_or_null[o + n] : o + n;
                     qn = q + qrow * V;
+                    for (int64_t v = 0; v < V; ++v) qw[v] = (double)qn[v];
                 }
                 for (int32_t c = next_token[o + n]; c >= 0; c = next_sibling[o + c]) {
                     int32_t y = draft_token[o + c];
-                    double qy = (double)qn[y], py = p[y];
+                    double qy = qw[y], py = p[y];
                     double ratio = py / qy;
                     if (qy == 0.0) counters[0]++;
                     double u = (double)coins[o + c];
@@ -528,7 +535,7 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                     ++rejected;
                     double R = 0.0;
                     for (int64_t v = 0; v < V; ++v) {
-                        double d = p[v] - (double)qn[v];
+                        double d = p[v] - qw[v];
                         r[v] = d > 0.0 ? d : 0.0;
                         R += r[v];
                     }
@@ -536,6 +543,12 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                         for (int64_t v = 0; v < V; ++v) p[v] = r[v] / R;
                     else
                         counters[1]++;
+                    if (without_replacement && y >= 0 && y < V) {
+                        double S = 0.0;
+                        qw[y] = 0.0;
+                        for (int64_t v = 0; v < V; ++v) S += qw[v];
+                        for (int64_t v = 0; v < V; ++v) qw[v] = S > 0.0 ? qw[v] / S : 0.0;
+                    }
                 }
                 if (accepted >= 0) {
                     int32_t y = draft_token[o + accepted];
@@ -565,6 +578,7 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
     }
     free(p);
     free(r);
+    free(qw);
     return OR_OK;
 }
 

@@ -414,9 +414,10 @@ def tree_shape(width, depth):
     return np.array(parent), np.array(nt, np.int32), np.array(ns, np.int32)
 
 
-def spec_rounds_with(verify, logP, Q, start, M, width, depth, trials, seed):
-    """Markov toy models: every trial runs rounds of (i.i.d. drafts from q,
-    verify) until M tokens are committed; returns the first M tokens."""
+def spec_rounds_with(verify, logP, Q, start, M, width, depth, trials, seed, draws="iid"):
+    """Markov toy models: every trial runs rounds of (drafts from q, verify)
+    until M tokens are committed; returns the first M tokens.  draws: "iid"
+    or "without" (siblings drawn one after another without replacement)."""
     rng = np.random.default_rng(seed)
     V = logP.shape[0]
     parent, nt, ns = tree_shape(width, depth)
@@ -434,7 +435,15 @@ def spec_rounds_with(verify, logP, Q, start, M, width, depth, trials, seed):
         cdf = np.cumsum(Q.astype(np.float64), 1)
         for n in range(1, N):
             u = rng.random(B)
-            tok[:, n] = np.minimum((u[:, None] >= cdf[tok[:, parent[n]]]).sum(1), V - 1)
+            if draws == "iid":
+                tok[:, n] = np.minimum((u[:, None] >= cdf[tok[:, parent[n]]]).sum(1), V - 1)
+            else:
+                w = Q[tok[:, parent[n]]].astype(np.float64)
+                for m_ in range(1, n):
+                    if parent[m_] == parent[n]:
+                        w[np.arange(B), tok[:, m_]] = 0.0
+                c = np.cumsum(w / w.sum(1, keepdims=True), 1)
+                tok[:, n] = np.minimum((u[:, None] >= c).sum(1), V - 1)
         target = logP[tok]
         qq = Q[tok]
         o = verify(target, qq, tok.astype(np.int32), np.tile(nt, (B, 1)), np.tile(ns, (B, 1)),
@@ -463,6 +472,64 @@ def law_vector(law, V, M):
     for seq, pr in law.items():
         v[np.ravel_multi_index(seq, (V,) * M)] = float(pr)
     return v
+
+
+@pytest.mark.parametrize("V,width,depth,M", [(3, 2, 2, 2), (3, 3, 1, 2), (3, 2, 1, 3), (4, 3, 2, 2), (4, 2, 2, 2)])
+def test_losslessness_exact_without_replacement(V, width, depth, M):
+    """Children drawn without replacement, each rejection followed by
+    q_cur <- q_cur without the rejected token, renormalised: the committed
+    law is exactly the target's.  Keeping q fixed for such draws is not
+    (the test can tell the two updates apart)."""
+    models, _, _ = markov_models(V, seed=10 + width * 7 + depth)
+    target = exact.target_law(models, (0,), M)
+    assert exact.spec_law(models, (0,), M, width, depth, "without", "renormalise") == target
+    if width < V:
+        assert exact.spec_law(models, (0,), M, width, depth, "without", "fixed") != target
+
+
+def test_without_replacement_hand_example():
+    """Two sibling leaves y0 = 1, y1 = 2 under a root with p = [0.3, 0.3, 0.4],
+    q = [0.1, 0.6, 0.3], coins 0.7 and 0.6.  y0: ratio 0.3 / 0.6 = 0.5 <= 0.7,
+    rejected; p_cur = (p - q)+ normalised = [2/3, 0, 1/3].  y1 with q fixed:
+    ratio (1/3) / 0.3 = 1.11 > 0.6, accepted (then the bonus of leaf 2).
+    Without replacement q_cur = [0.1, 0, 0.3] / 0.4 = [0.25, 0, 0.75]: ratio
+    (1/3) / 0.75 = 0.44 <= 0.6, rejected; p_cur = (p_cur - q_cur)+ = [5/12, 0,
+    0] normalised = [1, 0, 0], so the correction is token 0."""
+    p = np.array([0.3, 0.3, 0.4])
+    q = np.zeros((1, 3, 3), np.float32)
+    q[0, 0] = [0.1, 0.6, 0.3]
+    target = np.zeros((1, 3, 3), np.float32)
+    target[0, 0] = np.log(p)
+    target[0, 1:] = 0.0  # leaves: uniform bonus rows
+    draft = np.array([[0, 1, 2]], np.int32)
+    nt = np.array([[1, -1, -1]], np.int32)
+    ns = np.array([[-1, 2, -1]], np.int32)
+    coins = np.array([[0.0, 0.7, 0.6]], np.float32)
+    uf = np.array([0.5], np.float32)
+    with_r = oracle.verify_sample(target, 1.0, q, draft, nt, ns, coins, uf)
+    wo_r = oracle.verify_sample(target, 1.0, q, draft, nt, ns, coins, uf, without_replacement=True)
+    assert with_r["accept_length"][0] == 1 and with_r["committed"][0, 0] == 2
+    assert with_r["num_committed"][0] == 2 and with_r["walk_info"][0, 2] == 2  # then the leaf's bonus
+    assert wo_r["accept_length"][0] == 0 and wo_r["num_committed"][0] == 1 and wo_r["committed"][0, 0] == 0
+    assert wo_r["walk_info"][0, 1] == 2  # both siblings rejected
+    assert min(with_r["margin"][0], wo_r["margin"][0]) > 0.1
+
+
+@pytest.mark.parametrize("width,depth,M", [(2, 2, 2), (3, 1, 2)])
+def test_losslessness_monte_carlo_oracle_without_replacement(width, depth, M):
+    """The C oracle's without-replacement update on children drawn without
+    replacement reproduces the target's law of the first M tokens."""
+    V = 3
+    models, logP, Q = markov_models(V, seed=10 + width * 7 + depth)
+    probs = law_vector(exact.target_law(models, (0,), M), V, M)
+
+    def verify(target, qq, tok, nt, ns, coins, uf):
+        return oracle.verify_sample(np.ascontiguousarray(target), 1.0, qq, tok, nt, ns, coins, uf,
+                                    without_replacement=True)
+
+    seqs = spec_rounds_with(verify, logP, Q, 0, M, width, depth, 100000, seed=77 + width, draws="without")
+    counts = np.bincount(np.ravel_multi_index(seqs.T, (V,) * M), minlength=V ** M)
+    assert chi2_pvalue(counts, probs) > 1e-4
 
 
 @pytest.mark.parametrize("width,depth,M", [(1, 2, 3), (2, 2, 2), (3, 1, 2)])
