@@ -314,6 +314,38 @@ int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, const void* t
                                int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
                                size_t ws_bytes, spec_stream_t stream);
 
+/* Sibling update for children drawn without replacement (the variant the
+ * pages name beside the sibling-sequential residual rule: the rejected token's
+ * q is zeroed and q renormalised).  At a node, q_cur starts as the node's q;
+ * after child y is rejected, p_cur becomes the normalised positive residual
+ * of p_cur and q_cur, then q_cur[y] = 0 and q_cur is renormalised; the next
+ * sibling y' is accepted iff coin < p_cur[y'] / q_cur[y'].  With children
+ * drawn from q without replacement this keeps the target's law exactly.  The
+ * q row is taken as a distribution (it sums to 1): the renormalisation
+ * divides by 1 minus the rejected tokens' q. */
+#define SPEC_VERIFY_WITHOUT_REPLACEMENT 1
+
+/* spec_verify_sample / spec_verify_sample_qlogits with flags: 0 (the same
+ * call) or SPEC_VERIFY_WITHOUT_REPLACEMENT; other bits give
+ * SPEC_ERR_INVALID_ARG. */
+int spec_verify_sample_flags(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                             const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                             const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                             const float* coins, const float* u_final, const int32_t* budget_or_null,
+                             int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                             int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                             int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                             size_t ws_bytes, int flags, spec_stream_t stream);
+int spec_verify_sample_qlogits_flags(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                     const void* q_logits, int q_dtype, const float* q_stats, float T_q,
+                                     const int32_t* q_row_or_null, const int32_t* draft_token,
+                                     const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                     const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                     int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                     int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                     int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                     size_t ws_bytes, int flags, spec_stream_t stream);
+
 /* Greedy verify without caller scratch.  No passage of the pages has a
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory at all -- a plugin that receives only its input and output

@@ -18,7 +18,7 @@ __all__ = [
     "SpecError", "F32", "BF16", "STATS", "lib", "library_path",
     "spec_softmax_topk", "spec_softmax_sample", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
     "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
-    "spec_verify_sample_qlogits", "spec_compact_freed_capacity",
+    "spec_verify_sample_qlogits", "WITHOUT_REPLACEMENT", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_constrain_map_qlogits", "tli_plan_bytes", "tli_plan_build",
     "tli_map_ids",
     "tli_check_config", "spec_wait_probe",
@@ -56,6 +56,10 @@ _SIGS = {
                                 _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_sample_qlogits": (_I, [_I, _I, _I64, _I, _P, _F, _P, _I, _P, _F, _P, _P, _P, _P, _P, _P, _P,
                                         _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_sample_flags": (_I, [_I, _I, _I64, _I, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P,
+                                      _P, _P, _P, _P, _P, _SZ, _I, _P]),
+    "spec_verify_sample_qlogits_flags": (_I, [_I, _I, _I64, _I, _P, _F, _P, _I, _P, _F, _P, _P, _P, _P, _P, _P,
+                                              _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _P]),
     "spec_compact_freed_capacity": (_I64, [_I, _I, _I]),
     "spec_compact_slots": (_I, [_I, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, _I64,
                                 _I64, _P, _P]),
@@ -346,9 +350,14 @@ def spec_verify_greedy_noalloc(target, draft_token, next_token, next_sibling, bu
     return out
 
 
+WITHOUT_REPLACEMENT = 1  # SPEC_VERIFY_WITHOUT_REPLACEMENT
+
+
 def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coins, u_final, q_row=None,
-                       budget=None, eos_id=-1, out=None, ws=None, stats=None):
-    """target [B, N, V]; q fp32 rows of length V (a [rows, V] table with q_row [B, N], or [B, N, V])."""
+                       budget=None, eos_id=-1, out=None, ws=None, stats=None, without_replacement=False):
+    """target [B, N, V]; q fp32 rows of length V (a [rows, V] table with q_row [B, N], or [B, N, V]).
+    without_replacement: the sibling update for children drawn without
+    replacement (spec_verify_sample_flags with SPEC_VERIFY_WITHOUT_REPLACEMENT)."""
     _dev(target, name="target")
     B, N, V = target.shape
     _dev(q, torch.float32, "q")
@@ -363,16 +372,20 @@ def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coin
     _dev(stats, torch.int32, "stats")
     out = _verify_outputs(B, N, target.device, out)
     ws = _workspace(B, N, target.device, ws)
-    _call("spec_verify_sample", B, N, V, _logit_code(target), _ptr(target), float(T), _ptr(q), _ptr(q_row),
-          _ptr(draft_token), _ptr(next_token), _ptr(next_sibling), _ptr(coins), _ptr(u_final), _ptr(budget),
-          int(eos_id), _ptr(out["committed"]), _ptr(out["num_committed"]), _ptr(out["accept_length"]),
-          _ptr(out["accept_path"]), _ptr(out["next_root"]), _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws),
-          ws.numel(), _stream())
+    args = (B, N, V, _logit_code(target), _ptr(target), float(T), _ptr(q), _ptr(q_row), _ptr(draft_token),
+            _ptr(next_token), _ptr(next_sibling), _ptr(coins), _ptr(u_final), _ptr(budget), int(eos_id),
+            _ptr(out["committed"]), _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]),
+            _ptr(out["next_root"]), _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws), ws.numel())
+    if without_replacement:
+        _call("spec_verify_sample_flags", *args, WITHOUT_REPLACEMENT, _stream())
+    else:
+        _call("spec_verify_sample", *args, _stream())
     return out
 
 
 def spec_verify_sample_qlogits(target, T, q_logits, q_stats, T_q, draft_token, next_token, next_sibling, coins,
-                               u_final, q_row=None, budget=None, eos_id=-1, out=None, ws=None, stats=None):
+                               u_final, q_row=None, budget=None, eos_id=-1, out=None, ws=None, stats=None,
+                               without_replacement=False):
     """Stochastic verify with q given as draft-logit rows [rows, V] plus their
     (max, normaliser) [rows, 2] from spec_softmax_topk(row_stats=...)."""
     _dev(target, name="target")
@@ -390,11 +403,15 @@ def spec_verify_sample_qlogits(target, T, q_logits, q_stats, T_q, draft_token, n
     _dev(stats, torch.int32, "stats")
     out = _verify_outputs(B, N, target.device, out)
     ws = _workspace(B, N, target.device, ws)
-    _call("spec_verify_sample_qlogits", B, N, V, _logit_code(target), _ptr(target), float(T), _ptr(q_logits),
-          _logit_code(q_logits), _ptr(q_stats), float(T_q), _ptr(q_row), _ptr(draft_token), _ptr(next_token),
-          _ptr(next_sibling), _ptr(coins), _ptr(u_final), _ptr(budget), int(eos_id), _ptr(out["committed"]),
-          _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]),
-          _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws), ws.numel(), _stream())
+    args = (B, N, V, _logit_code(target), _ptr(target), float(T), _ptr(q_logits), _logit_code(q_logits),
+            _ptr(q_stats), float(T_q), _ptr(q_row), _ptr(draft_token), _ptr(next_token), _ptr(next_sibling),
+            _ptr(coins), _ptr(u_final), _ptr(budget), int(eos_id), _ptr(out["committed"]),
+            _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]),
+            _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws), ws.numel())
+    if without_replacement:
+        _call("spec_verify_sample_qlogits_flags", *args, WITHOUT_REPLACEMENT, _stream())
+    else:
+        _call("spec_verify_sample_qlogits", *args, _stream())
     return out
 
 

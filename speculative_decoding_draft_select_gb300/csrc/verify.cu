@@ -522,6 +522,30 @@ struct ResidualWeights {
   }
 };
 
+// The residual weights of a node after rejections without replacement:
+// those of W except at the ny rejected tokens ys, whose weights stay frozen
+// at fs (the draw's rescan and fallback read element values through here).
+template <class W>
+struct FrozenWeights {
+  W w;
+  const int32_t* ys;
+  const float* fs;
+  int ny;
+  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
+    w.load8(v0, x);
+    for (int i = 0; i < ny; ++i) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (v0 + j == ys[i]) x[j] = fs[i];
+    }
+  }
+  __device__ __forceinline__ float at(int64_t v) const {
+    for (int i = 0; i < ny; ++i)
+      if (v == ys[i]) return fs[i];
+    return w.at(v);
+  }
+};
+
 // Stochastic verify in one persistent launch: the row statistics of every
 // target row (the batched pass) and the walk of every request.  Work is
 // taken from two queues in the workspace (zeroed before the launch): rows
@@ -535,7 +559,7 @@ struct ResidualWeights {
 // bounded all the same).  Clusters without a request left compute the
 // remaining rows.  A row's statistics are published with a release store
 // of its flag and read after an acquire load of it.
-template <int DT, class QSrc, int C>
+template <int DT, class QSrc, int C, bool WOR>
 __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     sample_verify_kernel(int B, int N, int64_t V, float c, const void* __restrict__ target,
                        float* __restrict__ m_row, float* __restrict__ z_row, int32_t* __restrict__ ready,
@@ -548,6 +572,7 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
                        int32_t* next_root, int32_t* walk_info, int32_t* stats) {
   pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
+  constexpr int kTileW = kWalkThreads * kWalkElems;  // tile of the passes and of the draw
   using Weights = ResidualWeights<DT, typename QSrc::Row>;
   constexpr int kChunks = Weights::template chunks<kWalkElems>();
   constexpr int kRing = walk_ring_depth(kChunks);
@@ -566,7 +591,14 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
   int32_t* s_com = s_ns + N;
   int32_t* s_path = s_com + N;
   int32_t* s_ch = s_path + N;
+  // without replacement: the node's rejected tokens, their frozen residual
+  // weights, and per-token corrections of a pass
+  int32_t* s_ry = s_ch + N;
+  float* s_rf = reinterpret_cast<float*>(s_ry + N);
+  float* s_rd = s_rf + N;
   __shared__ float scan_sh[33];
+  __shared__ int s_nry, s_newy;
+  __shared__ float s_S, s_wsum;
   __shared__ int s_n, s_len, s_acc, s_rej, s_kind, s_done, s_nch, s_accept, s_tiles_ok, s_rem;
   __shared__ int64_t s_qrow;
   __shared__ float s_m, s_invz, s_nb, s_A, s_cj, s_total;
@@ -589,6 +621,27 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     float* ts = tile_sums + par * ntiles;
     par ^= 1;
     return cdf_tile_pass_split<kWalkThreads, kWalkElems, kRing, C>(w, V, part, ts, ring, rank);
+  };
+  // without replacement: the mass of the pass just made (its total `all`)
+  // and its tile sums with the node's rejected tokens at their frozen
+  // weights (warp 0, in list order); every CTA of a cluster does the same
+  auto frozen_fix = [&](const Weights& w, float all) -> float {
+    if (warp == 0) {
+      float* ts = tile_sums + (par ^ 1) * ntiles;
+      const int ny = s_nry;
+      for (int e = lane; e < ny; e += 32) s_rd[e] = s_rf[e] - w.at(s_ry[e]);
+      __syncwarp();
+      if (lane == 0) {
+        float W = all;
+        for (int e = 0; e < ny; ++e) {
+          W += s_rd[e];
+          ts[s_ry[e] / kTileW] += s_rd[e];
+        }
+        s_wsum = W;
+      }
+    }
+    __syncthreads();
+    return s_wsum;
   };
   // queued row i (node-major): its max and normaliser, then its flag
   auto stats_row = [&](int64_t i) {
@@ -713,6 +766,8 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
       s_A = 0.0f;
       s_cj = 1.0f;
       s_tiles_ok = 0;
+      s_nry = 0;
+      s_S = 1.0f;
     }
     __syncthreads();
     const int n = s_n, nch = s_nch;
@@ -733,9 +788,23 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     for (int i = 0; i < nch; ++i) {
       if (tid == 0) {
         const float p = p_finite ? prob_of(g_l[i], cT, mc, invz) : 0.0f;
-        const float pc = s_A == 0.0f ? p : fmaxf(0.0f, fmaf(-s_A, g_q[i], p)) / s_cj;
-        const float ratio = pc / g_q[i];
-        if (g_q[i] == 0.0f) bump(cstats, SPEC_STAT_Q_ZERO);
+        float pc, qi = g_q[i];
+        if constexpr (!WOR) {
+          pc = s_A == 0.0f ? p : fmaxf(0.0f, fmaf(-s_A, g_q[i], p)) / s_cj;
+        } else {
+          // a token rejected before keeps its frozen weight and has no q
+          // left; the others: the closed form against q renormalised over
+          // the tokens not rejected (the q row taken as summing to 1)
+          const int32_t y = s_dt[s_ch[i]];
+          int f = -1;
+          for (int e = 0; e < s_nry; ++e)
+            if (s_ry[e] == y) f = e;
+          const float r = f >= 0 ? s_rf[f] : (s_A == 0.0f ? p : fmaxf(0.0f, fmaf(-s_A, g_q[i], p)));
+          pc = (s_A == 0.0f && s_nry == 0) ? p : r / s_cj;
+          qi = (f >= 0 || !(s_S > 0.0f)) ? 0.0f : g_q[i] / s_S;
+        }
+        const float ratio = pc / qi;
+        if (qi == 0.0f) bump(cstats, SPEC_STAT_Q_ZERO);
         s_accept = g_u[i] < ratio;
       }
       __syncthreads();
@@ -744,21 +813,59 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
         break;
       }
       // rejected: mass of the next residual
-      const Weights w{lrow, qrow, V, cT, nb, s_A + s_cj};
-      const float total = pass(w);
-      if (tid == 0) {
-        if (total > 0.0f && isfinite(total)) {
-          s_A = s_A + s_cj;
-          s_cj = total;
-          s_tiles_ok = 1;
-          s_total = total;
-        } else {
-          bump(cstats, SPEC_STAT_RESIDUAL_FALLBACK);
-          s_tiles_ok = 0;
+      if constexpr (!WOR) {
+        const Weights w{lrow, qrow, V, cT, nb, s_A + s_cj};
+        const float total = pass(w);
+        if (tid == 0) {
+          if (total > 0.0f && isfinite(total)) {
+            s_A = s_A + s_cj;
+            s_cj = total;
+            s_tiles_ok = 1;
+            s_total = total;
+          } else {
+            bump(cstats, SPEC_STAT_RESIDUAL_FALLBACK);
+            s_tiles_ok = 0;
+          }
+          ++s_rej;
         }
-        ++s_rej;
+        __syncthreads();
+      } else {
+        // without replacement: A_{j+1} = A_j + W_j / S_j (S_j the q mass not
+        // yet rejected); the rejected token joins the list with its weight
+        // under A_{j+1}, and q loses its mass
+        const float An = s_S > 0.0f ? s_A + s_cj / s_S : s_A;
+        const Weights w{lrow, qrow, V, cT, nb, An};
+        const float all = pass(w);
+        if (tid == 0) {
+          const int32_t y = s_dt[s_ch[i]];
+          bool seen = false;
+          for (int e = 0; e < s_nry; ++e) seen = seen || s_ry[e] == y;
+          s_newy = -1;
+          if (!seen && y >= 0 && y < V) {
+            s_ry[s_nry] = y;
+            s_rf[s_nry] = w.at(y);
+            s_newy = s_nry++;
+            s_S -= g_q[i];
+          }
+        }
+        __syncthreads();
+        const float W = frozen_fix(w, all);
+        if (tid == 0) {
+          if (W > 0.0f && isfinite(W)) {
+            s_A = An;
+            s_cj = W;
+            s_tiles_ok = 1;
+            s_total = W;
+          } else {
+            // no residual mass: p_cur stays, and so does the new token's weight
+            bump(cstats, SPEC_STAT_RESIDUAL_FALLBACK);
+            s_tiles_ok = 0;
+            if (s_newy >= 0) s_rf[s_newy] = Weights{lrow, qrow, V, cT, nb, s_A}.at(s_ry[s_newy]);
+          }
+          ++s_rej;
+        }
+        __syncthreads();
       }
-      __syncthreads();
     }
     if (accepted >= 0) {
       if (tid == 0) {
@@ -781,10 +888,21 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
       total = s_total;  // the last pass's tile sums are in buffer par ^ 1
     } else {
       total = pass(w);
+      if constexpr (WOR) total = frozen_fix(w, total);
     }
-    const int32_t tok =
-        cdf_search<kWalkThreads, Weights, kWalkElems>(w, V, __ldg(u_final + b), tile_sums + (par ^ 1) * ntiles, total,
-                                                      scan_sh, cstats);
+    int32_t tok = -1;
+    bool drawn = false;
+    if constexpr (WOR) {
+      if (s_nry > 0) {
+        const FrozenWeights<Weights> fw{w, s_ry, s_rf, s_nry};
+        tok = cdf_search<kWalkThreads, FrozenWeights<Weights>, kWalkElems>(
+            fw, V, __ldg(u_final + b), tile_sums + (par ^ 1) * ntiles, total, scan_sh, cstats);
+        drawn = true;
+      }
+    }
+    if (!drawn)
+      tok = cdf_search<kWalkThreads, Weights, kWalkElems>(w, V, __ldg(u_final + b), tile_sums + (par ^ 1) * ntiles,
+                                                          total, scan_sh, cstats);
     if (tid == 0) {
       s_com[s_len++] = tok;
       s_kind = nch > 0 ? SPEC_FINAL_CORRECTION : SPEC_FINAL_BONUS;
@@ -910,22 +1028,23 @@ namespace {
 
 // Shared memory of the walk kernel with C CTAs per request.
 // Shared memory of the verify kernel with C CTAs per request.
-template <int DT, class QSrc, int C>
+template <int DT, class QSrc, int C, bool WOR>
 size_t walk_smem(int N, int64_t V) {
   using Weights = ResidualWeights<DT, typename QSrc::Row>;
   constexpr int kChunks = Weights::template chunks<kWalkElems>();
   const int64_t ntiles = (V + kWalkThreads * kWalkElems - 1) / (kWalkThreads * kWalkElems);
   const size_t ring = sizeof(uint4) * walk_ring_depth(kChunks) * kChunks * kWalkThreads;
   const int64_t parts = static_cast<int64_t>(cdf_part_tiles<kWalkThreads, kWalkElems, C>(V)) * kWalkThreads;
-  return ring + sizeof(float) * (2 * ntiles + parts + 3 * static_cast<int64_t>(N)) +
-         sizeof(int32_t) * 6 * static_cast<int64_t>(N);
+  // without replacement: the rejected-token list (ints) and two float arrays
+  return ring + sizeof(float) * (2 * ntiles + parts + (WOR ? 5 : 3) * static_cast<int64_t>(N)) +
+         sizeof(int32_t) * (WOR ? 7 : 6) * static_cast<int64_t>(N);
 }
 
 // Clusters of C CTAs the GPU holds at once with this shared memory, or 0
 // when the kernel cannot be configured.
-template <int DT, class QSrc, int C>
+template <int DT, class QSrc, int C, bool WOR>
 int64_t walk_capacity(size_t smem) {
-  auto kernel = sample_verify_kernel<DT, QSrc, C>;
+  auto kernel = sample_verify_kernel<DT, QSrc, C, WOR>;
   if (smem > kMaxDynSmem) return 0;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -952,15 +1071,15 @@ int64_t walk_capacity(size_t smem) {
   return n;
 }
 
-template <int DT, class QSrc, int C>
+template <int DT, class QSrc, int C, bool WOR>
 void launch_verify(int64_t clusters, size_t smem, cudaStream_t s, int B, int N, int64_t V, const void* target,
                    float c, QSrc qsrc, const int32_t* q_row, const int32_t* dtok, const int32_t* ntok,
                    const int32_t* nsib, const float* coins, const float* u_final, const int32_t* budget, int32_t eos,
                    int32_t* committed, int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
                    int32_t* next_root, int32_t* walk_info, int32_t* stats, const VerifyWs& w) {
   const int64_t rows = static_cast<int64_t>(B) * N;
-  launch_kc(sample_verify_kernel<DT, QSrc, C>, static_cast<unsigned>(clusters * C), kWalkThreads, smem, s, C, B, N,
-            V, c, target, w.m, w.z, w.ready, w.ready + rows, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
+  launch_kc(sample_verify_kernel<DT, QSrc, C, WOR>, static_cast<unsigned>(clusters * C), kWalkThreads, smem, s, C, B,
+            N, V, c, target, w.m, w.z, w.ready, w.ready + rows, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats);
 }
 
@@ -968,48 +1087,66 @@ void launch_verify(int64_t clusters, size_t smem, cudaStream_t s, int B, int N, 
 // as many clusters as the GPU holds, C CTAs each, the largest C of 4, 2, 1
 // for which every request can have its cluster at once (a request's
 // passes run one after another), else 1.
-template <int DT, class QSrc>
-int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, QSrc qsrc, const int32_t* q_row,
-                         const int32_t* dtok, const int32_t* ntok, const int32_t* nsib, const float* coins,
-                         const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
-                         int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
-                         int32_t* walk_info, int32_t* stats, VerifyWs w, cudaStream_t s) {
+template <int DT, class QSrc, bool WOR>
+int launch_sample_verify_t(int B, int N, int64_t V, const void* target, float c, QSrc qsrc, const int32_t* q_row,
+                           const int32_t* dtok, const int32_t* ntok, const int32_t* nsib, const float* coins,
+                           const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
+                           int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                           int32_t* walk_info, int32_t* stats, VerifyWs w, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(B) * N;
-  const size_t smem4 = walk_smem<DT, QSrc, 4>(N, V), smem2 = walk_smem<DT, QSrc, 2>(N, V),
-               smem1 = walk_smem<DT, QSrc, 1>(N, V);
+  const size_t smem4 = walk_smem<DT, QSrc, 4, WOR>(N, V), smem2 = walk_smem<DT, QSrc, 2, WOR>(N, V),
+               smem1 = walk_smem<DT, QSrc, 1, WOR>(N, V);
   if (smem1 > kMaxDynSmem) return SPEC_ERR_UNSUPPORTED;  // V in the millions
-  const int64_t cap4 = walk_capacity<DT, QSrc, 4>(smem4), cap2 = walk_capacity<DT, QSrc, 2>(smem2),
-                cap1 = walk_capacity<DT, QSrc, 1>(smem1);
+  const int64_t cap4 = walk_capacity<DT, QSrc, 4, WOR>(smem4), cap2 = walk_capacity<DT, QSrc, 2, WOR>(smem2),
+                cap1 = walk_capacity<DT, QSrc, 1, WOR>(smem1);
   if (cap1 < 1) return SPEC_ERR_CUDA;
   if (cudaMemsetAsync(w.ready, 0, sizeof(int32_t) * static_cast<size_t>(rows + 2), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (cap4 >= B)
-    launch_verify<DT, QSrc, 4>(cap4, smem4, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
+    launch_verify<DT, QSrc, 4, WOR>(cap4, smem4, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
                                budget, eos, committed, num_committed, accept_length, accept_path, next_root,
                                walk_info, stats, w);
   else if (cap2 >= B)
-    launch_verify<DT, QSrc, 2>(cap2, smem2, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
+    launch_verify<DT, QSrc, 2, WOR>(cap2, smem2, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
                                budget, eos, committed, num_committed, accept_length, accept_path, next_root,
                                walk_info, stats, w);
   else
-    launch_verify<DT, QSrc, 1>(cap1, smem1, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
+    launch_verify<DT, QSrc, 1, WOR>(cap1, smem1, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
                                budget, eos, committed, num_committed, accept_length, accept_path, next_root,
                                walk_info, stats, w);
   return launch_status();
 }
 
+template <int DT, class QSrc>
+int launch_sample_verify(int B, int N, int64_t V, const void* target, float c, QSrc qsrc, const int32_t* q_row,
+                         const int32_t* dtok, const int32_t* ntok, const int32_t* nsib, const float* coins,
+                         const float* u_final, const int32_t* budget, int32_t eos, int32_t* committed,
+                         int32_t* num_committed, int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                         int32_t* walk_info, int32_t* stats, VerifyWs w, int wor, cudaStream_t s) {
+  return wor ? launch_sample_verify_t<DT, QSrc, true>(B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins,
+                                                      u_final, budget, eos, committed, num_committed, accept_length,
+                                                      accept_path, next_root, walk_info, stats, w, s)
+             : launch_sample_verify_t<DT, QSrc, false>(B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins,
+                                                       u_final, budget, eos, committed, num_committed,
+                                                       accept_length, accept_path, next_root, walk_info, stats, w,
+                                                       s);
+}
+
 }  // namespace
 }  // namespace specdec
 
-extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+namespace {
+int verify_sample_impl(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
                                   const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
                                   const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
                                   const float* coins, const float* u_final, const int32_t* budget_or_null,
                                   int32_t eos_id, int32_t* committed, int32_t* num_committed,
                                   int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                                   int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
-                                  size_t ws_bytes, spec_stream_t stream) {
+                                  size_t ws_bytes, int flags, spec_stream_t stream) {
   if (!(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
+  if ((flags & ~SPEC_VERIFY_WITHOUT_REPLACEMENT) != 0) return SPEC_ERR_INVALID_ARG;
+  const int wor = (flags & SPEC_VERIFY_WITHOUT_REPLACEMENT) ? 1 : 0;
   const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
                               retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
                               next_root, ws, ws_bytes);
@@ -1023,11 +1160,40 @@ extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void
                                            retrieve_next_token, retrieve_next_sibling, coins, u_final,
                                            budget_or_null, eos_id, committed, num_committed, accept_length,
                                            accept_path, next_root, walk_info_or_null, stats_or_null,
-                                           carve(ws, B, N), s);
+                                           carve(ws, B, N), wor, s);
   return launch_sample_verify<SPEC_F32>(B, N, V, target_logits, c, qs, q_row_or_null, draft_token,
                                         retrieve_next_token, retrieve_next_sibling, coins, u_final, budget_or_null,
                                         eos_id, committed, num_committed, accept_length, accept_path, next_root,
-                                        walk_info_or_null, stats_or_null, carve(ws, B, N), s);
+                                        walk_info_or_null, stats_or_null, carve(ws, B, N), wor, s);
+}
+}  // namespace
+
+extern "C" int spec_verify_sample(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                  const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                                  const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                  const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                  int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                  int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                  int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                  size_t ws_bytes, spec_stream_t stream) {
+  return verify_sample_impl(B, N, V, dtype, target_logits, T, q, q_row_or_null, draft_token, retrieve_next_token,
+                            retrieve_next_sibling, coins, u_final, budget_or_null, eos_id, committed, num_committed,
+                            accept_length, accept_path, next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, 0,
+                            stream);
+}
+
+extern "C" int spec_verify_sample_flags(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                        const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                                        const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                        const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                        int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                        int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                        int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                        size_t ws_bytes, int flags, spec_stream_t stream) {
+  return verify_sample_impl(B, N, V, dtype, target_logits, T, q, q_row_or_null, draft_token, retrieve_next_token,
+                            retrieve_next_sibling, coins, u_final, budget_or_null, eos_id, committed, num_committed,
+                            accept_length, accept_path, next_root, walk_info_or_null, stats_or_null, ws, ws_bytes,
+                            flags, stream);
 }
 
 namespace specdec {
@@ -1039,17 +1205,18 @@ int sample_verify_qlogits(int B, int N, int64_t V, const void* target, float c, 
                           const int32_t* ntok, const int32_t* nsib, const float* coins, const float* u_final,
                           const int32_t* budget, int32_t eos, int32_t* committed, int32_t* num_committed,
                           int32_t* accept_length, int32_t* accept_path, int32_t* next_root, int32_t* walk_info,
-                          int32_t* stats, VerifyWs w, cudaStream_t s) {
+                          int32_t* stats, VerifyWs w, int wor, cudaStream_t s) {
   const QLogits<QDT> qs{q_logits, q_stats, V, cq};
   return launch_sample_verify<DT>(B, N, V, target, c, qs, q_row, dtok, ntok, nsib, coins, u_final, budget, eos,
                                   committed, num_committed, accept_length, accept_path, next_root, walk_info, stats,
-                                  w, s);
+                                  w, wor, s);
 }
 
 }  // namespace
 }  // namespace specdec
 
-extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+namespace {
+int verify_sample_qlogits_impl(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
                                           const void* q_logits, int q_dtype, const float* q_stats, float T_q,
                                           const int32_t* q_row_or_null, const int32_t* draft_token,
                                           const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
@@ -1057,8 +1224,10 @@ extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, co
                                           int32_t eos_id, int32_t* committed, int32_t* num_committed,
                                           int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                                           int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
-                                          size_t ws_bytes, spec_stream_t stream) {
+                                          size_t ws_bytes, int flags, spec_stream_t stream) {
   if (!(T > 0.0f) || !isfinite(T) || !(T_q > 0.0f) || !isfinite(T_q)) return SPEC_ERR_INVALID_ARG;
+  if ((flags & ~SPEC_VERIFY_WITHOUT_REPLACEMENT) != 0) return SPEC_ERR_INVALID_ARG;
+  const int wor = (flags & SPEC_VERIFY_WITHOUT_REPLACEMENT) ? 1 : 0;
   const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
                               retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
                               next_root, ws, ws_bytes);
@@ -1072,7 +1241,7 @@ extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, co
   return sample_verify_qlogits<DT, QDT>(B, N, V, target_logits, c, q_logits, q_stats, cq, q_row_or_null,        \
                                         draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final, \
                                         budget_or_null, eos_id, committed, num_committed, accept_length,         \
-                                        accept_path, next_root, walk_info_or_null, stats_or_null, w, s)
+                                        accept_path, next_root, walk_info_or_null, stats_or_null, w, wor, s)
   if (dtype == SPEC_BF16) {
     if (q_dtype == SPEC_BF16) SPEC_QL(SPEC_BF16, SPEC_BF16);
     SPEC_QL(SPEC_BF16, SPEC_F32);
@@ -1080,6 +1249,38 @@ extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, co
   if (q_dtype == SPEC_BF16) SPEC_QL(SPEC_F32, SPEC_BF16);
   SPEC_QL(SPEC_F32, SPEC_F32);
 #undef SPEC_QL
+}
+}  // namespace
+
+extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                          const void* q_logits, int q_dtype, const float* q_stats, float T_q,
+                                          const int32_t* q_row_or_null, const int32_t* draft_token,
+                                          const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                          const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                          int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                          int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                          int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                          size_t ws_bytes, spec_stream_t stream) {
+  return verify_sample_qlogits_impl(B, N, V, dtype, target_logits, T, q_logits, q_dtype, q_stats, T_q, q_row_or_null,
+                                    draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
+                                    budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
+                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, 0, stream);
+}
+
+extern "C" int spec_verify_sample_qlogits_flags(int B, int N, int64_t V, int dtype, const void* target_logits,
+                                                float T, const void* q_logits, int q_dtype, const float* q_stats,
+                                                float T_q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                                                const int32_t* retrieve_next_token,
+                                                const int32_t* retrieve_next_sibling, const float* coins,
+                                                const float* u_final, const int32_t* budget_or_null, int32_t eos_id,
+                                                int32_t* committed, int32_t* num_committed, int32_t* accept_length,
+                                                int32_t* accept_path, int32_t* next_root, int32_t* walk_info_or_null,
+                                                int32_t* stats_or_null, void* ws, size_t ws_bytes, int flags,
+                                                spec_stream_t stream) {
+  return verify_sample_qlogits_impl(B, N, V, dtype, target_logits, T, q_logits, q_dtype, q_stats, T_q, q_row_or_null,
+                                    draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
+                                    budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
+                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, flags, stream);
 }
 
 // ------------------------------------------------- greedy verify, no scratch

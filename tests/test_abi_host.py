@@ -61,6 +61,14 @@ def test_host_side_argument_checks(lib):
                                           *([null] * 8), 0, null) == -1
     assert lib.spec_compact_slots(2, 4, 0, *([null] * 4), 16, *([null] * 4), 0, *([null] * 3), 0, 0, null,
                                   null) == -1
+    # verify flags: unknown bits are rejected before anything else is looked at
+    p16 = ctypes.c_void_p(16)
+    assert lib.spec_verify_sample_flags(2, 4, 10, 1, p16, 1.0, *([p16] * 8), -1, *([p16] * 6), null, p16, 1 << 20,
+                                        2, null) == -1
+    assert lib.spec_verify_sample_qlogits_flags(2, 4, 10, 1, p16, 1.0, p16, 1, p16, 1.0, *([p16] * 7), -1,
+                                                *([p16] * 6), null, p16, 1 << 20, 6, null) == -1
+    assert lib.spec_verify_sample_flags(0, 4, 10, 1, *([null] * 1), 1.0, *([null] * 8), -1, *([null] * 8), 0, 1,
+                                        null) == 0
     assert lib.tli_constrain_map(4, 10, 10, null, 1, null, null, 1.0, null, null, null, null, null, null) == -1
     assert lib.tli_map_ids(null, null, -1, null, 0, 0, null) == -1
     # plan: missing or misaligned buffers, planned constrain without a plan

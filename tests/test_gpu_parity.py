@@ -413,6 +413,60 @@ def test_verify_sample_tree_given_q_node_order(B):
     assert int(stats[sd.STATS["q_zero"]]) == o["q_zero"]
 
 
+@pytest.mark.parametrize("B,q_form", [(24, "probs"), (200, "probs"), (400, "probs"), (24, "logits"),
+                                      (400, "logits")])
+def test_verify_sample_without_replacement(B, q_form):
+    """The without-replacement sibling update (q loses each rejected token
+    and is renormalised) against the oracle's, on oracle trees whose
+    siblings sometimes repeat a token (V is small), in each walk layout (4,
+    2 and 1 CTAs per request) and with q written or in logit form."""
+    rng = np.random.default_rng(177 + B)
+    k, steps, N, V = 3, 4, 12, 257
+    opool = oracle.Pool(B, k, steps)
+    for s, (p, idx) in enumerate(oracle_topk_inputs(rng, B, k, steps)):
+        oracle.tree_expand(opool, s, p, np.ascontiguousarray(idx % V, np.int32))
+    t = oracle.build_tree(opool, N, rng.integers(0, V, B).astype(np.int32), np.zeros(B, np.int32))
+    target = make_logits(rng, B * N, V, torch.float32, std=2.0).view(B, N, V)
+    target[:, :, :5] = float("-inf")
+    dl = (target.view(B * N, V) + torch.from_numpy(rng.normal(0, 0.7, (B * N, V)).astype(np.float32)))
+    dl[:, :5] = 0.0
+    dt, par = t["draft_token"], t["parent"]
+    # the draft puts much of its mass on the children it proposed (so that
+    # removing a rejected child's q matters), the target somewhat less
+    for b in range(B):
+        for n in range(1, N):
+            dl[b * N + par[b, n], dt[b, n]] += 3.0
+            target[b, par[b, n], dt[b, n]] += 2.0
+    _, _, q, _ = oracle.softmax_topk(np_logits(dl), 1.0, 1, want_probs=True)
+    q = q.astype(np.float32).reshape(B, N, V)
+    coins = rng.random((B, N)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    stats = sd.new_stats()
+    args = (dev(dt), dev(t["retrieve_next_token"]), dev(t["retrieve_next_sibling"]), dev(coins), dev(uf))
+    if q_form == "probs":
+        g = sd.spec_verify_sample(dev(target), 1.0, dev(q), *args, stats=stats, without_replacement=True)
+    else:
+        st = torch.empty((B * N, 2), dtype=torch.float32, device="cuda")
+        sd.spec_softmax_topk(dev(dl), 1.0, 1, row_stats=st)
+        g = sd.spec_verify_sample_qlogits(dev(target), 1.0, dev(dl), st, 1.0, *args, stats=stats,
+                                          without_replacement=True)
+    o = oracle.verify_sample(np_logits(target), 1.0, q, dt, t["retrieve_next_token"], t["retrieve_next_sibling"],
+                             coins, uf, without_replacement=True)
+    torch.cuda.synchronize()
+    exact = sum(verify_compare(g, o, b, b, "sample") for b in range(B))
+    assert exact >= B - max(1, B // 100)
+    if exact == B:
+        assert int(stats[sd.STATS["q_zero"]]) == o["q_zero"]
+    # the inputs tell the two updates apart
+    o_r = oracle.verify_sample(np_logits(target), 1.0, q, dt, t["retrieve_next_token"], t["retrieve_next_sibling"],
+                               coins, uf)
+    assert any(not np.array_equal(o["committed"][b], o_r["committed"][b]) for b in range(B))
+    # and the default call still follows the fixed-q rule
+    g_r = sd.spec_verify_sample(dev(target), 1.0, dev(q), *args)
+    torch.cuda.synchronize()
+    assert sum(verify_compare(g_r, o_r, b, b, "sample") for b in range(B)) >= B - max(1, B // 100)
+
+
 @pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
 def test_q_in_logit_form_equals_written_q(qdtype):
     """spec_verify_sample_qlogits on (draft logits, row max/normaliser) gives
