@@ -467,6 +467,33 @@ def test_verify_sample_without_replacement(B, q_form):
     assert sum(verify_compare(g_r, o_r, b, b, "sample") for b in range(B)) >= B - max(1, B // 100)
 
 
+@pytest.mark.parametrize("q_mode", ["probs", "logits"])
+def test_pipeline_verify_without_replacement(q_mode):
+    """run_verify(without_replacement=True) is the flagged verify call on
+    the step's buffers."""
+    cfg = small("c3", **SMALL["c3"])
+    work = generate(cfg, "cuda")
+    buf = StepBuffers(cfg.kind, cfg.B, cfg.topk, cfg.steps, cfg.N, cfg.V, "cuda", want_q=True, q_mode=q_mode,
+                      q_logit_dtype=cfg.dtype)
+    tree = run_draft(buf, work["draft_table"], cfg.T, work["root_token"], work["seq_lens"])
+    target = assemble_target(work, tree["q_row"])
+    vargs = (cfg.T, work["coins"], work["u_final"], work.get("budget"), int(work["eos_id"]))
+    got = {n: v.clone() for n, v in run_verify(buf, target, "sample", *vargs, without_replacement=True).items()}
+    t = buf.tree
+    tree_args = (t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"], work["coins"],
+                 work["u_final"])
+    kw = dict(q_row=t["q_row"], budget=work.get("budget"), eos_id=int(work["eos_id"]), without_replacement=True)
+    if q_mode == "logits":
+        want = sd.spec_verify_sample_qlogits(target, cfg.T, buf.draft_table, buf.q_stats, buf.T_draft, *tree_args,
+                                             **kw)
+    else:
+        want = sd.spec_verify_sample(target, cfg.T, buf.q, *tree_args, **kw)
+    torch.cuda.synchronize()
+    for n in got:
+        assert torch.equal(got[n], want[n]), n
+    assert int(got["num_committed"].sum()) > 0
+
+
 @pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
 def test_q_in_logit_form_equals_written_q(qdtype):
     """spec_verify_sample_qlogits on (draft logits, row max/normaliser) gives
