@@ -487,6 +487,45 @@ def test_losslessness_exact_without_replacement(V, width, depth, M):
         assert exact.spec_law(models, (0,), M, width, depth, "without", "fixed") != target
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_without_replacement_closed_form(seed):
+    """The kernel's form of the without-replacement update, in exact
+    arithmetic, against the definition: for rejections of distinct tokens
+    y_0, y_1, ... the definition replaces p_cur by (p_cur - q_cur)+
+    normalised, then removes y_j from q_cur and renormalises.  The closed
+    form keeps A (A_0 = 0), the mass W (W_0 = 1), S = 1 - q(rejected), and
+    for a rejected token its weight at rejection: after rejecting y_j,
+    A <- A + W / S, the weights are max(0, p - A q) off the rejected set and
+    the frozen ones on it, W is their sum.  Both must give the same p_cur and
+    the same acceptance ratio p_cur[y] / q_cur[y] at every step."""
+    rng = np.random.default_rng(seed)
+    V = 7
+    p = exact.normalise([Fraction(int(x)) for x in rng.integers(0, 9, V) + (np.arange(V) == 0)])
+    q = exact.normalise([Fraction(int(x)) for x in rng.integers(1, 9, V)])
+    order = [int(v) for v in rng.permutation(V)[:5]]
+    pc, qc = p, q
+    A, W, S, frozen = Fraction(0), Fraction(1), Fraction(1), {}
+    for y in order:
+        # acceptance ratio of y before its rejection, both ways
+        r_closed = frozen[y] if y in frozen else max(Fraction(0), p[y] - A * q[y])
+        p_closed = r_closed / W
+        q_closed = Fraction(0) if y in frozen else q[y] / S
+        assert p_closed == pc[y] and q_closed == qc[y]
+        # reject y
+        if sum(max(Fraction(0), a - b) for a, b in zip(pc, qc)) == 0:
+            break
+        pc = exact.positive_residual(pc, qc)
+        qc = exact.without(qc, y)
+        A = A + W / S
+        frozen[y] = max(Fraction(0), p[y] - A * q[y])
+        S = S - q[y]
+        w = [frozen[v] if v in frozen else max(Fraction(0), p[v] - A * q[v]) for v in range(V)]
+        W = sum(w)
+        assert tuple(x / W for x in w) == pc
+        if S == 0:
+            break
+
+
 def test_without_replacement_hand_example():
     """Two sibling leaves y0 = 1, y1 = 2 under a root with p = [0.3, 0.3, 0.4],
     q = [0.1, 0.6, 0.3], coins 0.7 and 0.6.  y0: ratio 0.3 / 0.6 = 0.5 <= 0.7,
