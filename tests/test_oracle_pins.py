@@ -488,6 +488,28 @@ def test_losslessness_exact_without_replacement(V, width, depth, M):
 
 
 @pytest.mark.parametrize("seed", range(6))
+def test_residual_closed_form(seed):
+    """The kernel's form of the fixed-q sibling update, in exact arithmetic,
+    against the definition (p_cur <- (p_cur - q)+ normalised after each
+    rejection): with A_0 = 0, W_0 = 1, A_{j+1} = A_j + W_j and W_{j+1} =
+    sum max(0, p - A_{j+1} q), p_cur after j rejections is
+    max(0, p - A_j q) / W_j."""
+    rng = np.random.default_rng(100 + seed)
+    V = 9
+    p = exact.normalise([Fraction(int(x)) for x in rng.integers(0, 9, V) + (np.arange(V) == 0)])
+    q = exact.normalise([Fraction(int(x)) for x in rng.integers(1, 9, V)])
+    pc, A, W = p, Fraction(0), Fraction(1)
+    for _ in range(6):
+        if sum(max(Fraction(0), a - b) for a, b in zip(pc, q)) == 0:
+            break
+        pc = exact.positive_residual(pc, q)
+        A = A + W
+        w = [max(Fraction(0), a - A * b) for a, b in zip(p, q)]
+        W = sum(w)
+        assert tuple(x / W for x in w) == pc
+
+
+@pytest.mark.parametrize("seed", range(6))
 def test_without_replacement_closed_form(seed):
     """The kernel's form of the without-replacement update, in exact
     arithmetic, against the definition: for rejections of distinct tokens
