@@ -187,7 +187,8 @@ def verify_greedy(target, draft_token, next_token, next_sibling, budget=None, eo
 
 
 def verify_sample(target, T: float, q, draft_token, next_token, next_sibling, coins, u_final,
-                  q_row=None, budget=None, eos: int = -1, without_replacement: bool = False):
+                  q_row=None, budget=None, eos: int = -1, without_replacement: bool = False,
+                  top_k: int = 0, top_p: float = 1.0):
     x, dt = logits_buffer(target)
     B, N, V = x.shape
     qq = _c(q, np.float32)
@@ -206,10 +207,25 @@ def verify_sample(target, T: float, q, draft_token, next_token, next_sibling, co
         _p(qq), _p(qr), _p(dtok), _p(nt), _p(ns), _p(co), _p(uf), _p(bud), ctypes.c_int32(eos),
         _p(o["committed"]), _p(o["num_committed"]), _p(o["accept_length"]), _p(o["accept_path"]),
         _p(o["next_root"]), _p(o["walk_info"]), _p(o["margin"]), _p(counters),
-        ctypes.c_int(1 if without_replacement else 0))
+        ctypes.c_int(1 if without_replacement else 0), ctypes.c_int64(int(top_k)), ctypes.c_double(float(top_p)))
     _check(rc, "verify_sample")
     o["q_zero"], o["residual_fallback"], o["cdf_fallback"], o["nonfinite_rows"] = (int(c) for c in counters)
     return o
+
+
+def filter_probs(p, top_k: int = 0, top_p: float = 1.0):
+    """Target-side top-k / top-p filtering of probability rows [..., V]
+    (oracle_filter_probs), returned as a new fp64 array."""
+    x = np.array(p, dtype=np.float64, copy=True)
+    V = x.shape[-1]
+    rows = x.reshape(-1, V)
+    for r in range(rows.shape[0]):
+        row = np.ascontiguousarray(rows[r])
+        rc = lib().oracle_filter_probs(ctypes.c_int64(V), _p(row), ctypes.c_int64(int(top_k)),
+                                       ctypes.c_double(float(top_p)))
+        _check(rc, "filter_probs")
+        rows[r] = row
+    return rows.reshape(x.shape)
 
 
 def compact_slots(seq_lens, accept_path, accept_length, req_to_token, page_size: int,

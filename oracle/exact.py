@@ -64,6 +64,27 @@ def acceptance_masses(p: Dist, q: Dist) -> Tuple[Fraction, Fraction]:
     return acc, rej
 
 
+def filter_probs(p: Dist, top_k: int = 0, top_p: Fraction = Fraction(1)) -> Dist:
+    """Target-side top-k / top-p filtering in exact arithmetic (the rule of
+    the C oracle's oracle_filter_probs): order by (p desc, index asc), keep
+    the first top_k (0: all), then every kept token whose exclusive prefix of
+    the renormalised top-k mass is below top_p (the first always), and
+    renormalise."""
+    order = sorted(range(len(p)), key=lambda v: (-p[v], v))
+    keep = order[:top_k] if 0 < top_k < len(p) else order
+    mk = sum(p[v] for v in keep)
+    if top_p < 1 and mk > 0:
+        kept, prefix = [], Fraction(0)
+        for i, v in enumerate(keep):
+            if i > 0 and not prefix / mk < top_p:
+                break
+            kept.append(v)
+            prefix += p[v]
+        keep = kept
+    m = sum(p[v] for v in keep)
+    return tuple((p[v] / m if v in keep else Fraction(0)) for v in range(len(p)))
+
+
 class ToyModels:
     """A target p(.|context) and a draft q(.|context) over a tiny vocabulary,
     given as exact distributions by two callables on token tuples."""

@@ -471,6 +471,60 @@ static int softmax_row(const void* x, int dtype, int64_t base, int64_t V, double
     return 1;
 }
 
+typedef struct { double p; int64_t id; } prob_t;
+
+/* (p desc, id asc) */
+static int prob_first(const void* a, const void* b)
+{
+    const prob_t* x = (const prob_t*)a;
+    const prob_t* y = (const prob_t*)b;
+    if (x->p > y->p) return -1;
+    if (x->p < y->p) return 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+/* Target-side filtering of a probability row ([ZS] 5.1: with temperature,
+ * top-k or top-p in force the processed probabilities are the ones
+ * verification uses), in place.  Order the tokens by (p desc, index asc).
+ * top_k > 0 keeps the first top_k of them (top_k <= 0 or >= V: all).
+ * top_p < 1 then keeps, in the same order, every kept token whose exclusive
+ * prefix of the top-k mass (renormalised) is below top_p; the first token
+ * always stays, so the token that crosses top_p is kept.  The kept masses are
+ * renormalised; the rest are 0.  A row from which nothing is dropped, and a
+ * row of zeros, stay as they are. */
+int oracle_filter_probs(int64_t V, double* p, int64_t top_k, double top_p)
+{
+    if (V < 1) return OR_ERR;
+    prob_t* o = (prob_t*)malloc(sizeof(prob_t) * (size_t)V);
+    if (!o) return OR_ERR;
+    for (int64_t v = 0; v < V; ++v) { o[v].p = p[v]; o[v].id = v; }
+    qsort(o, (size_t)V, sizeof(prob_t), prob_first);
+    int64_t keep = (top_k > 0 && top_k < V) ? top_k : V;
+    double mk = 0.0;
+    for (int64_t i = 0; i < keep; ++i) mk += o[i].p;
+    if (top_p < 1.0 && mk > 0.0) {
+        double prefix = 0.0;
+        int64_t n = 0;
+        for (int64_t i = 0; i < keep; ++i) {
+            if (i > 0 && !(prefix / mk < top_p)) break;
+            prefix += o[i].p;
+            n = i + 1;
+        }
+        keep = n;
+    }
+    if (keep == V) {  /* nothing dropped: the row stays as it is */
+        free(o);
+        return OR_OK;
+    }
+    double m = 0.0;
+    for (int64_t i = 0; i < keep; ++i) m += o[i].p;
+    for (int64_t v = 0; v < V; ++v) p[v] = 0.0;
+    if (m > 0.0)
+        for (int64_t i = 0; i < keep; ++i) p[o[i].id] = o[i].p / m;
+    free(o);
+    return OR_OK;
+}
+
 /* [ZS] 5.1: a draft y drawn from q is accepted with probability
  * min(1, p[y]/q[y]) (here: coin < p[y]/q[y]); on rejection the token comes
  * from the normalised positive residual (p - q)+; after full acceptance the
@@ -490,7 +544,9 @@ static int softmax_row(const void* x, int dtype, int64_t base, int64_t V, double
  * replacement -- q_cur starts as the node's q, each rejection of y first
  * replaces p_cur by the residual of p_cur and q_cur, then sets q_cur[y] = 0
  * and renormalises q_cur (all zero once no mass is left); the acceptance
- * ratio of the next sibling is p_cur[y] / q_cur[y]. */
+ * ratio of the next sibling is p_cur[y] / q_cur[y].
+ * top_k / top_p: target-side filtering (oracle_filter_probs) of every target
+ * row after its softmax; top_k <= 0 and top_p >= 1 leave p as it is. */
 int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                          double T, const float* q, const int32_t* q_row_or_null,
                          const int32_t* draft_token, const int32_t* next_token,
@@ -499,13 +555,14 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                          int32_t eos, int32_t* committed, int32_t* num_committed,
                          int32_t* accept_length, int32_t* accept_path,
                          int32_t* next_root, int32_t* walk_info, double* margin,
-                         int64_t* counters, int without_replacement)
+                         int64_t* counters, int without_replacement, int64_t top_k, double top_p)
 {
     if (B < 0 || N < 1 || V < 1 || !(T > 0.0)) return OR_ERR;
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     double* qw = (double*)malloc(sizeof(double) * (size_t)V);
     if (!p || !r || !qw) { free(p); free(r); free(qw); return OR_ERR; }
+    const int filtered = (top_k > 0 && top_k < V) || top_p < 1.0;
     for (int b = 0; b < B; ++b) {
         int64_t o = (int64_t)b * N;
         for (int i = 0; i < N; ++i) { committed[o + i] = -1; accept_path[o + i] = -1; }
@@ -516,6 +573,7 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
         accept_path[o] = 0;
         if (rem > 0) {
             if (!softmax_row(target, dtype, o * V, V, T, p)) counters[3]++;
+            if (filtered) oracle_filter_probs(V, p, top_k, top_p);
             for (;;) {
                 int32_t accepted = -1;
                 const float* qn = NULL;
@@ -557,6 +615,7 @@ int oracle_verify_sample(int B, int N, int64_t V, int dtype, const void* target,
                     n = accepted;
                     if (y == eos || len == rem) { kind = KIND_NONE; break; }
                     if (!softmax_row(target, dtype, (o + n) * V, V, T, p)) counters[3]++;
+                    if (filtered) oracle_filter_probs(V, p, top_k, top_p);
                     continue;
                 }
                 int32_t t;

@@ -487,6 +487,72 @@ def test_losslessness_exact_without_replacement(V, width, depth, M):
         assert exact.spec_law(models, (0,), M, width, depth, "without", "fixed") != target
 
 
+def test_filter_probs_hand_examples():
+    """Target-side filtering, worked by hand on p = [0.1, 0.2, 0.5, 0.2]:
+    order 2, 1, 3, 0 (the tie 0.2 / 0.2 goes to the lower index).  top-k 3:
+    {2, 1, 3}, mass 0.9 -> [0, 2/9, 5/9, 2/9].  Then top-p 0.6 on that:
+    prefixes 0, 5/9 < 0.6 keep 2 and 1, 7/9 drops 3 -> [0, 2/7, 5/7, 0].  top-p
+    0.5 alone: the first token carries 0.5, so only it stays -> [0, 0, 1, 0]."""
+    p = np.array([0.1, 0.2, 0.5, 0.2])
+    np.testing.assert_allclose(oracle.filter_probs(p, 3), [0, 2 / 9, 5 / 9, 2 / 9], atol=1e-15)
+    np.testing.assert_allclose(oracle.filter_probs(p, 3, 0.6), [0, 2 / 7, 5 / 7, 0], atol=1e-15)
+    np.testing.assert_allclose(oracle.filter_probs(p, 0, 0.5), [0, 0, 1, 0], atol=1e-15)
+    np.testing.assert_array_equal(oracle.filter_probs(p, 0, 1.0), p)
+    np.testing.assert_array_equal(oracle.filter_probs(p, 4, 1.0), p)
+    np.testing.assert_allclose(oracle.filter_probs(p, 1, 1.0), [0, 0, 1, 0], atol=1e-15)
+    np.testing.assert_array_equal(oracle.filter_probs(np.zeros(4), 2, 0.5), np.zeros(4))
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_filter_probs_properties(seed):
+    """Kept tokens precede dropped ones in (p desc, index asc); top-k keeps at
+    most k; top-p keeps the shortest prefix whose mass reaches top_p of the
+    top-k mass; the result sums to 1 and equals the exact-arithmetic rule."""
+    rng = np.random.default_rng(seed)
+    V = 50
+    w = rng.integers(0, 20, V)
+    w[rng.integers(0, V, 5)] = 7  # ties
+    p = w / w.sum()
+    for k, tp in ((0, 0.8), (10, 1.0), (10, 0.5), (3, 0.99), (0, 0.3)):
+        f = oracle.filter_probs(p, k, tp)
+        order = sorted(range(V), key=lambda v: (-p[v], v))
+        kept = [v for v in order if f[v] > 0]
+        assert kept == order[:len(kept)] or all(p[v] == 0 for v in order[len(kept):])
+        if k:
+            assert len(kept) <= k
+        assert abs(f.sum() - 1.0) < 1e-12
+        top = order[:k] if k else order
+        mk = p[top].sum()
+        if tp < 1.0:
+            mass = p[kept].sum() / mk
+            assert mass >= tp - 1e-12 or len(kept) == len([v for v in top if p[v] > 0])
+            assert (p[kept].sum() - p[kept[-1]]) / mk < tp
+        want = exact.filter_probs(tuple(Fraction(int(x), int(w.sum())) for x in w), k,
+                                  Fraction(tp).limit_denominator(1000))
+        np.testing.assert_allclose(f, [float(x) for x in want], atol=1e-12)
+
+
+@pytest.mark.parametrize("top_k,top_p", [(2, 1.0), (0, 0.7), (3, 0.8)])
+def test_filtered_verify_law_monte_carlo_oracle(top_k, top_p):
+    """With target-side filtering, the committed law of speculative rounds
+    (i.i.d. drafts from q, a tree of width 2 and depth 2) is the law of
+    sampling the filtered target alone."""
+    V, width, depth, M = 4, 2, 2, 2
+    models, logP, Q = markov_models(V, seed=40 + top_k)
+    tp = Fraction(top_p).limit_denominator(1000)
+    P = [exact.filter_probs(models.p((v,)), top_k, tp) for v in range(V)]
+    filtered = exact.ToyModels(V, lambda c: P[c[-1]], models.q)
+    probs = law_vector(exact.target_law(filtered, (0,), M), V, M)
+
+    def verify(target, qq, tok, nt, ns, coins, uf):
+        return oracle.verify_sample(np.ascontiguousarray(target), 1.0, qq, tok, nt, ns, coins, uf, top_k=top_k,
+                                    top_p=top_p)
+
+    seqs = spec_rounds_with(verify, logP, Q, 0, M, width, depth, 100000, seed=5 + top_k)
+    counts = np.bincount(np.ravel_multi_index(seqs.T, (V,) * M), minlength=V ** M)
+    assert chi2_pvalue(counts, probs) > 1e-4
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_residual_closed_form(seed):
     """The kernel's form of the fixed-q sibling update, in exact arithmetic,
