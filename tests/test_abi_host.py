@@ -33,6 +33,25 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(sd._SIGS) >= set(names)
 
 
+def test_binding_exports_exist_and_refuse_host_tensors():
+    """Every name the binding exports exists, and the calls refuse host
+    (CPU) tensors before touching the library: there is no CPU path."""
+    import torch
+    for n in sd.__all__:
+        assert hasattr(sd, n), n
+    x = torch.zeros((2, 8))
+    with pytest.raises(ValueError):
+        sd.spec_softmax_topk(x, 1.0, 2)
+    ids = torch.zeros(8, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        sd.tli_constrain_map_qlogits(x, ids, ids, 1.0)
+    tgt = torch.zeros((1, 2, 8))
+    tok = torch.zeros((1, 2), dtype=torch.int32)
+    with pytest.raises(ValueError):
+        sd.spec_verify_sample(tgt, 1.0, torch.zeros((1, 2, 8)), tok, tok, tok, torch.zeros((1, 2)), torch.zeros(1),
+                              without_replacement=True)
+
+
 def test_host_side_argument_checks(lib):
     null = None
     # k > V, T <= 0, bad dtype, null pointers
