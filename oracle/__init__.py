@@ -74,7 +74,10 @@ def pool_size(k: int, num_steps: int) -> int:
     return int(lib().oracle_pool_size(ctypes.c_int(k), ctypes.c_int(num_steps)))
 
 
-def softmax_topk(logits, T: float, k: int, want_probs: bool = False):
+def softmax_topk(logits, T: float, k: int, want_probs: bool = False, score_T=None):
+    """Top-k of each row with their probabilities at ``score_T`` (None: at
+    T), and optionally the full distribution at T (oracle_softmax_topk)."""
+    score_T = T if score_T is None else score_T
     x, dt = logits_buffer(logits)
     V = x.shape[-1]
     R = x.size // V
@@ -83,7 +86,8 @@ def softmax_topk(logits, T: float, k: int, want_probs: bool = False):
     probs = np.zeros((R, V), np.float64) if want_probs else None
     flag = np.zeros(R, np.int32)
     rc = lib().oracle_softmax_topk(_p(x), ctypes.c_int(dt), ctypes.c_int64(R), ctypes.c_int64(V),
-                                   ctypes.c_double(T), ctypes.c_int(k), _p(topk_p), _p(topk_idx),
+                                   ctypes.c_double(T), ctypes.c_double(score_T), ctypes.c_int(k),
+                                   _p(topk_p), _p(topk_idx),
                                    _p(probs), _p(flag))
     _check(rc, "softmax_topk")
     return topk_p, topk_idx, probs, flag

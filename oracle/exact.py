@@ -69,7 +69,10 @@ def filter_probs(p: Dist, top_k: int = 0, top_p: Fraction = Fraction(1)) -> Dist
     the C oracle's oracle_filter_probs): order by (p desc, index asc), keep
     the first top_k (0: all), then every kept token whose exclusive prefix of
     the renormalised top-k mass is below top_p (the first always), and
-    renormalise."""
+    renormalise.  A row with no mass is returned unchanged, as the C oracle
+    leaves it."""
+    if sum(p) == 0:
+        return tuple(p)
     order = sorted(range(len(p)), key=lambda v: (-p[v], v))
     keep = order[:top_k] if 0 < top_k < len(p) else order
     mk = sum(p[v] for v in keep)

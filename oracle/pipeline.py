@@ -16,6 +16,13 @@ from . import build_tree, compact_slots, sample, softmax_topk, tli_constrain_map
 from . import verify_greedy, verify_sample, Pool
 
 
+# "[SGLang] Multi-Layer EAGLE" section 3: the draft loop's scores are the
+# top-k of a plain softmax of the draft logits (no temperature).  The
+# temperature of zero-to-sglang ch.10 5.1 applies to the stored draft
+# distribution q that acceptance reads.
+SCORE_T = 1.0
+
+
 def np_logits(t: torch.Tensor) -> np.ndarray:
     """float32 array, or uint16 array of bf16 bit patterns."""
     t = t.detach().cpu().contiguous()
@@ -92,7 +99,7 @@ def run_request(cfg, d, mode, compact=False):
             tok, prob, _, _ = sample(u, logits=x, T=T)
             tree_expand(pool, s, prob.astype(np.float32), tok)
         else:
-            tp, ti, probs, _ = softmax_topk(x, T, cfg.topk, want_probs=want_q)
+            tp, ti, probs, _ = softmax_topk(x, T, cfg.topk, want_probs=want_q, score_T=SCORE_T)
             tree_expand(pool, s, tp.astype(np.float32), ti)
         if want_q:
             for i, r in enumerate(rows):

@@ -76,17 +76,21 @@ static double order_key(double x) { return isnan(x) ? -INFINITY : x; }
 
 /* ------------------------------------------------- softmax and top-k (A1) */
 
-/* [ML] section 3: probs = softmax(logits); topk_p, topk_index = top-k(probs).
- * [ZS] 5.1: with a temperature the stored probabilities are the processed
- * ones, p_v = exp((l_v - max l)/T) / sum_u exp((l_u - max l)/T).
- * Top-k is taken on the logits (same order as on the probabilities, no
+/* [ML] section 3: each draft step takes probs = softmax(logits) and then
+ * topk_p, topk_index = top-k(probs); those topk_p are the tree scores, so
+ * they come from a plain softmax: T_score = 1 in the draft loop.
+ * [ZS] 5.1: the draft distribution q that verification reads is the
+ * processed one, p_v = exp((l_v - max l)/T) / sum_u exp((l_u - max l)/T),
+ * written to probs_or_null at the temperature T.
+ * topk_p are the top-k tokens' probabilities under T_score.  Top-k is taken
+ * on the logits (same order as on the probabilities at any temperature, no
  * rounding ties), by (logit desc, index asc).  A row whose maximum is not
  * finite gets probability 0 everywhere and row_flag = 1. */
 int oracle_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V,
-                        double T, int k, double* topk_p, int32_t* topk_idx,
-                        double* probs_or_null, int32_t* row_flag)
+                        double T, double T_score, int k, double* topk_p,
+                        int32_t* topk_idx, double* probs_or_null, int32_t* row_flag)
 {
-    if (R < 0 || V <= 0 || k < 0 || k > V || !(T > 0.0)) return OR_ERR;
+    if (R < 0 || V <= 0 || k < 0 || k > V || !(T > 0.0) || !(T_score > 0.0)) return OR_ERR;
     char* taken = (char*)malloc((size_t)V);
     if (!taken) return OR_ERR;
     for (int64_t r = 0; r < R; ++r) {
@@ -97,10 +101,13 @@ int oracle_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V,
             if (x > m) m = x;
         }
         int finite = isfinite(m);
-        double Z = 0.0;
+        double Z = 0.0, Zs = 0.0;  /* normalisers at T and at T_score */
         if (finite)
-            for (int64_t v = 0; v < V; ++v)
-                Z += exp((order_key(logit_at(logits, dtype, base + v)) - m) / T);
+            for (int64_t v = 0; v < V; ++v) {
+                double x = order_key(logit_at(logits, dtype, base + v));
+                Z += exp((x - m) / T);
+                Zs += exp((x - m) / T_score);
+            }
         memset(taken, 0, (size_t)V);
         for (int j = 0; j < k; ++j) {
             int64_t best = -1;
@@ -112,7 +119,7 @@ int oracle_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V,
             }
             taken[best] = 1;
             topk_idx[r * k + j] = (int32_t)best;
-            topk_p[r * k + j] = finite ? exp((bx - m) / T) / Z : 0.0;
+            topk_p[r * k + j] = finite ? exp((bx - m) / T_score) / Zs : 0.0;
         }
         if (probs_or_null)
             for (int64_t v = 0; v < V; ++v)

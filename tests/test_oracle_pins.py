@@ -114,6 +114,37 @@ def test_tree_hand_example():
     assert list(t4["draft_token"][0]) == [7, 10, 20, 11]
 
 
+def test_tree_scores_use_a_plain_softmax():
+    """[SGLang] Multi-Layer EAGLE, section 3: the draft loop scores the tree
+    with the top-k of a plain softmax (no temperature); the temperature of
+    zero-to-sglang ch.10 5.1 belongs to the stored q.  Hand-worked case (k=2,
+    2 steps, N=3) where the two temperatures grow different trees.
+
+    Root row logits [0, -0.5]; the row of the root's best child a: [0, -0.2].
+      T=1:   p(a) = 1/(1+e^-0.5) = 0.6224593, p(b) = 0.3775407,
+             p(a0 | a) = 1/(1+e^-0.2) = 0.5498340,
+             score(a0) = 0.3422493 < score(b)  ->  nodes {a, b}.
+      T=0.7: p(a) = 1/(1+e^(-0.5/0.7)) = 0.6713475, p(b) = 0.3286525,
+             p(a0 | a) = 1/(1+e^(-0.2/0.7)) = 0.5709466,
+             score(a0) = 0.3833035 > score(b)  ->  nodes {a, a0}."""
+    root = np.array([[0.0, -0.5]], np.float32)
+    step1 = np.array([[0.0, -0.2], [0.0, -0.2]], np.float32)  # frontier slots a, b
+    expect = {1.0: ([0.6224593, 0.3775407], [0.5498340, 0.4501660], [7, 0, 1], [-1, 0, 0]),
+              0.7: ([0.6713475, 0.3286525], [0.5709466, 0.4290534], [7, 0, 0], [-1, 0, 1])}
+    for score_T, (p0, p1, tokens, parents) in expect.items():
+        # q's temperature (T) is held at 0.7: only score_T moves the tree
+        tp0, ti0, q0, _ = oracle.softmax_topk(root, 0.7, 2, want_probs=True, score_T=score_T)
+        tp1, ti1, _, _ = oracle.softmax_topk(step1, 0.7, 2, score_T=score_T)
+        np.testing.assert_allclose(tp0[0], p0, atol=1e-7)
+        np.testing.assert_allclose(tp1[0], p1, atol=1e-7)
+        np.testing.assert_allclose(q0[0], [0.6713475, 0.3286525], atol=1e-7)  # q at T=0.7 either way
+        _, t = _run_tree([(tp0[0], ti0[0]), (tp1, ti1)], 2, 2, 3)
+        assert list(t["draft_token"][0]) == tokens, score_T
+        assert list(t["parent"][0]) == parents, score_T
+    from oracle.pipeline import SCORE_T
+    assert SCORE_T == 1.0
+
+
 def _random_topk(rng, rows, k):
     p = np.sort(rng.uniform(0.01, 1.0, (rows, k)).astype(np.float32), axis=1)[:, ::-1]
     p = np.ascontiguousarray(p / np.float32(k))
@@ -501,6 +532,8 @@ def test_filter_probs_hand_examples():
     np.testing.assert_array_equal(oracle.filter_probs(p, 4, 1.0), p)
     np.testing.assert_allclose(oracle.filter_probs(p, 1, 1.0), [0, 0, 1, 0], atol=1e-15)
     np.testing.assert_array_equal(oracle.filter_probs(np.zeros(4), 2, 0.5), np.zeros(4))
+    zero = (Fraction(0),) * 4  # the exact-arithmetic statement leaves a massless row as it is too
+    assert exact.filter_probs(zero, 2, Fraction(1, 2)) == zero
 
 
 @pytest.mark.parametrize("seed", range(5))
