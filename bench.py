@@ -47,6 +47,47 @@ def default_mode(cfg):
     return cfg.modes[-1]
 
 
+def config_dict(cfg, mode, q_mode, world):
+    """The workload's description; the same dict for both arms."""
+    return {"workload": describe(cfg, mode), "B": cfg.B, "topk": cfg.topk, "num_steps": cfg.steps,
+            "N": cfg.N, "V": cfg.V, "mode": mode, "T": cfg.T, "q": q_mode if mode == "sample" else None,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (draft + target logits), no flush" if input_bytes(cfg) > L2_BYTES
+            else "inputs fit in L2: warm (resident) figures; cold figures with a 512 MB scrub under 'cold'"}
+
+
+L2_BYTES = 129 * 2 ** 20
+SCRUB_BYTES = 512 * 2 ** 20
+
+
+def input_bytes(cfg):
+    esz = 2 if cfg.dtype == torch.bfloat16 else 4
+    return (cfg.table_rows * cfg.V + cfg.B * cfg.N * (cfg.V_t or cfg.V)) * esz
+
+
+def host_info():
+    """Host cores and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model, "machine": platform.machine()}
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -156,13 +197,18 @@ def reduce_over_ranks(total_ms, tokens, world, device):
     return float(span.item()), float(tok.item())
 
 
-def run_ours(args, cfg, mode, rank, world):
+def run_ours(args, cfg, mode, rank, world, steps=None, warmup=None, flush=False, do_e2e=True):
+    """Time ``steps`` whole steps of one workload (after ``warmup``).  flush:
+    write a 512 MB scrub buffer before every timed step (outside the step's
+    events), so that inputs that fit in L2 are read cold."""
     import speculative_decoding_draft_select_gb300 as sd
     from speculative_decoding_draft_select_gb300 import pipeline as pl
     from speculative_decoding_draft_select_gb300.build import build
 
     build()
     sd.lib()
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = rank_config(cfg, rank, world)
     work = generate(cfg, dev)
@@ -231,7 +277,7 @@ def run_ours(args, cfg, mode, rank, world):
         if compact:
             pl.run_compact(buf, w["seq_lens"], w["req_to_token"], cfg.page_size, kv_pool=kv)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step(False)
     torch.cuda.synchronize()
     if world > 1:
@@ -242,16 +288,19 @@ def run_ours(args, cfg, mode, rank, world):
     # replayed once untimed first
     graphs = None
     if use_graph:
-        graphs = [pl.capture_step(lambda: step(True), warm=False) for _ in range(args.steps)]
+        graphs = [pl.capture_step(lambda: step(True), warm=False) for _ in range(steps)]
         for g in graphs:
             g.replay()
         torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    scrub = torch.empty(SCRUB_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     committed = 0
     with ClockSampler(torch.cuda.current_device()) as clk:
         t0 = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(steps):
+            if scrub is not None:
+                scrub.fill_(i & 0xFF)  # evicts the step's inputs from L2
             starts[i].record(stream)
             if graphs is not None:
                 graphs[i].replay()
@@ -264,13 +313,15 @@ def run_ours(args, cfg, mode, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = starts[0].elapsed_time(ends[-1])
+    # steps back to back: first start to last end; with a flush between
+    # steps, the sum of the steps' own intervals (the scrubs left out)
+    total_ms = sum(step_ms) if flush else starts[0].elapsed_time(ends[-1])
     committed = int(buf.verify_out["num_committed"].sum().item())
     accept = float(buf.verify_out["accept_length"].float().mean().item())
     dom_ms = [ev[0].elapsed_time(ev[1]) for ev, _ in dom_events]
     dom_rows = [r for _, r in dom_events]
 
-    total_ms_max, tokens_all = reduce_over_ranks(total_ms, committed * args.steps, world, dev)
+    total_ms_max, tokens_all = reduce_over_ranks(total_ms, committed * steps, world, dev)
     value = tokens_all / (total_ms_max / 1e3)
 
     peak, peak_kind = hbm_peak()
@@ -295,7 +346,7 @@ def run_ours(args, cfg, mode, rank, world):
         draft_roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                       "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                       "bytes_per_launch": int(dom_bytes), "avg_launch_us": round(dom_avg_ms * 1e3, 2),
-                      "launches_per_step": len(dom_ms) // max(args.steps, 1),
+                      "launches_per_step": len(dom_ms) // max(steps, 1),
                       "traffic": ncu_traffic(kname, cfg.name)}
 
     # the batched verify (row statistics of every target row + tree walk):
@@ -323,27 +374,25 @@ def run_ours(args, cfg, mode, rank, world):
         roofline = verify_roof
 
     # e2e: host buffers through the same API, copies inside the timed region
-    e2e = run_e2e(args, cfg, mode, work, buf, target, step, compact) if not args.no_e2e else None
+    e2e = run_e2e(args, cfg, mode, work, buf, target, step, compact) if (do_e2e and not args.no_e2e) else None
 
-    launches = pl.kernels_per_step(buf, mode, compact, kv is not None) * args.steps
+    launches = pl.kernels_per_step(buf, mode, compact, kv is not None) * steps
     clocks = clk.summary()
-    ms_per_step = total_ms_max / args.steps
+    ms_per_step = total_ms_max / steps
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "input_dtype": str(cfg.dtype).replace("torch.", ""),
         "data": "synthetic (seeded; shapes and value distributions of the workload, no model weights)",
-        "config": {"workload": describe(cfg, mode), "B": cfg.B, "topk": cfg.topk, "num_steps": cfg.steps,
-                   "N": cfg.N, "V": cfg.V, "mode": mode, "T": cfg.T, "q": q_mode if mode == "sample" else None,
-                   "parallelism": f"replicas x{world}", "cuda_graph": graphs is not None,
-                   "l2": "inputs larger than L2 (draft + target logits), no flush"},
+        "config": config_dict(cfg, mode, q_mode, world), "cuda_graph": graphs is not None,
+        "l2_flush": flush,
         "us_per_step_median": round(statistics.median(step_ms) * 1e3, 2),
         "verified_tokens_per_step": committed, "mean_accept_length": round(accept, 3),
         "roofline": roofline, "rooflines": {"draft": draft_roof, "verify": verify_roof}, "verify": verify,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "stats": buf.stats.cpu().tolist(),
     }
-    return line, work
+    return line, work, buf
 
 
 def run_e2e(args, cfg, mode, work, buf, target, step_fn, compact):
@@ -400,59 +449,105 @@ def run_e2e(args, cfg, mode, work, buf, target, step_fn, compact):
     dt = time.perf_counter() - t0
     return {"value": round(tokens / dt, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(dt / n * 1e3, 3),
+            "h2d_gbs": round(h2d / (dt / n) / 1e9, 1),
             "copy_overlap": "inputs of step i+1 copied while step i computes"}
 
 
 # ---------------------------------------------------------------- reference
 
 
-def oracle_sample(cfg, mode, work, budget_s):
-    """The CPU oracle, single-threaded, on as many requests as fit in
-    ``budget_s`` seconds of oracle time (at least one)."""
+def oracle_sample(cfg, mode, work, budget_s, start=0, kv_host=None, keep=None):
+    """The CPU oracle, single-threaded, on requests start, start+1, ... (mod
+    B) until ``budget_s`` seconds of oracle time are spent (at least one).
+    kv_host: the slot payload pool as a host array, moved in place by the
+    oracle's compaction.  keep: a list that receives (b, oracle outputs)."""
     from oracle.pipeline import fetch_request, run_request
 
     tokens, secs, reqs = 0, 0.0, 0
-    for b in range(cfg.B):
+    for i in range(cfg.B):
+        b = (start + i) % cfg.B
         d = fetch_request(cfg, work, b)
         t0 = time.perf_counter()
-        _, _, _, v, _ = run_request(cfg, d, mode, compact=bool(cfg.page_size))
+        tree, _, _, v, _ = run_request(cfg, d, mode, compact=bool(cfg.page_size), kv_pool=kv_host)
         secs += time.perf_counter() - t0
         tokens += int(v["num_committed"][0])
         reqs += 1
+        if keep is not None:
+            keep.append((b, tree, v))
         if secs >= budget_s:
             break
     return tokens, secs, reqs
 
 
-def cpu_baseline(cfg, mode, work, budget_s=15.0):
-    tokens, secs, reqs = oracle_sample(cfg, mode, work, budget_s)
-    return {"value": round(tokens / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+VERIFY_FIELDS = ("committed", "num_committed", "accept_length", "accept_path", "next_root", "walk_info")
+
+
+def compare_with_oracle(cfg, mode, buf, kept, boundary=1e-5):
+    """The GPU step's tree and verify outputs against the oracle's, request
+    by request: exact, differing only within ``boundary`` of a stochastic
+    decision boundary (the oracle's margin), or a mismatch."""
+    import numpy as np
+    tree = {k: v.cpu().numpy() for k, v in buf.tree.items()}
+    out = {k: v.cpu().numpy() for k, v in buf.verify_out.items()}
+    exact = near = bad = 0
+    for b, ot, o in kept:
+        same_tree = all(np.array_equal(tree[k][b], ot[k][0] + (b * cfg.N if k == "retrieve_index" else 0))
+                        for k in ("draft_token", "parent", "positions", "retrieve_index", "retrieve_next_token",
+                                  "retrieve_next_sibling"))
+        same = same_tree and all(np.array_equal(out[k][b], o[k][0]) for k in VERIFY_FIELDS)
+        if same:
+            exact += 1
+        elif same_tree and mode == "sample" and o["margin"][0] < boundary:
+            near += 1
+        else:
+            bad += 1
+    return {"compared": len(kept), "exact": exact, "boundary": near, "mismatch": bad,
+            "rule": "a request may differ only where the oracle's uniform lies within 1e-5 of a decision boundary"}
+
+
+def cpu_baseline(cfg, mode, work, buf=None, budget_s=15.0):
+    keep = [] if buf is not None else None
+    tokens, secs, reqs = oracle_sample(cfg, mode, work, budget_s, keep=keep)
+    line = {"value": round(tokens / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{reqs} of {cfg.B} requests of {cfg.name}, one at a time (full draft, tree, verify"
-                      f"{', compaction index work' if cfg.page_size else ''}); {tokens} tokens in {secs:.2f} s"}
+                      f"{', compaction index work' if cfg.page_size else ''}); {tokens} tokens in {secs:.2f} s",
+            "host": host_info()}
+    parity = compare_with_oracle(cfg, mode, buf, keep) if buf is not None else None
+    return line, parity
 
 
-def run_reference(args, cfg, mode, rank):
+def run_reference(args, cfg, mode, rank, world):
+    """The oracle as the reference arm: each timed step is a bounded sample
+    of the workload's requests (consecutive steps take consecutive
+    requests), timed on one host core, including the compaction's payload
+    moves on a host copy of the slot pool."""
     if rank != 0:
         return None
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    work = generate(cfg.scaled(bytes_per_slot=0), dev)
+    work = generate(cfg, dev)
+    kv_host = work["kv_pool"].cpu().numpy() if "kv_pool" in work else None
     per_step_budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    nxt = 0
     for _ in range(args.warmup):
-        oracle_sample(cfg, mode, work, per_step_budget / 4)
+        _, _, r = oracle_sample(cfg, mode, work, per_step_budget / 4, start=nxt, kv_host=kv_host)
+        nxt += r
     tok, sec = 0, 0.0
     reqs = 0
     for _ in range(args.steps):
-        t, s, r = oracle_sample(cfg, mode, work, per_step_budget)
-        tok, sec, reqs = tok + t, sec + s, reqs + r
+        t, s, r = oracle_sample(cfg, mode, work, per_step_budget, start=nxt, kv_host=kv_host)
+        tok, sec, reqs, nxt = tok + t, sec + s, reqs + r, nxt + r
     value = tok / sec
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
+        "ms_per_step_kind": (f"oracle time of one bounded sample per step ({reqs / args.steps:.1f} of "
+                             f"{cfg.B} requests on average), not of the whole batch"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; same generator as the GPU arm)",
-        "config": {"workload": describe(cfg, mode), "B": cfg.B, "mode": mode},
+        "config": config_dict(cfg, mode, args.q or "logits", world),
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{reqs} requests over {args.steps} steps, one at a time, fp64 C oracle"},
+                         "sample": f"{reqs} requests over {args.steps} steps, one at a time, fp64 C oracle",
+                         "host": host_info()},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -471,6 +566,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--no-graph", action="store_true", help="launch every kernel eagerly (no CUDA graph)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure only the chosen workload (by default the c3 line also carries c1, c2, c4, c5)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -484,7 +581,7 @@ def main():
     mode = args.mode or default_mode(cfg)
 
     if args.impl == "reference":
-        line = run_reference(args, cfg, mode, rank)
+        line = run_reference(args, cfg, mode, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
         return
@@ -492,13 +589,54 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    line, work = run_ours(args, cfg, mode, rank, world)
+    line, work, buf = run_ours(args, cfg, mode, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(cfg, mode, work)
+            line["cpu_baseline"], line["boundary_cases"] = cpu_baseline(cfg, mode, work, buf)
+        del work, buf
+        torch.cuda.empty_cache()
+        if not args.no_configs and world == 1 and args.config == "c3" and not args.batch:
+            line["configs"] = other_configs(args)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# the other workloads, each measured after the headline one (same process,
+# one at a time); those whose inputs fit in L2 also cold
+OTHER_CONFIGS = [("c1", "greedy"), ("c1", "sample"), ("c2", "greedy"), ("c4", "sample"), ("c5", "greedy"),
+                 ("c5", "sample")]
+
+
+def summarize(line):
+    v, d = line["verify"], line["rooflines"]["draft"]
+    out = {"workload": line["config"]["workload"], "tokens_per_s": line["value"], "ms_per_step": line["ms_per_step"],
+           "steps": line["steps"], "mean_accept_length": line["mean_accept_length"],
+           "verify": None if v is None else {"us": v["us_per_step"], "gbs": v["achieved"], "frac": v["frac"],
+                                              "logit_bytes": v["logit_bytes"]},
+           "draft": None if d is None else {"kernel": d["kernel"], "avg_launch_us": d["avg_launch_us"],
+                                             "launches_per_step": d["launches_per_step"], "gbs": d["achieved"],
+                                             "frac": d["frac"]},
+           "clocks": line["clocks"], "stats": line["stats"]}
+    return out
+
+
+def other_configs(args):
+    res = {}
+    for name, mode in OTHER_CONFIGS:
+        cfg = CONFIGS[name]
+        steps = max(3, min(args.steps, 10))
+        warm, w, b = run_ours(args, cfg, mode, 0, 1, steps=steps, warmup=3, do_e2e=False)
+        del w, b
+        entry = summarize(warm)
+        if input_bytes(cfg) <= L2_BYTES:
+            cold, w, b = run_ours(args, cfg, mode, 0, 1, steps=steps, warmup=3, flush=True, do_e2e=False)
+            del w, b
+            entry["cold"] = {k: summarize(cold)[k] for k in ("tokens_per_s", "ms_per_step", "verify", "draft",
+                                                             "clocks")}
+        torch.cuda.empty_cache()
+        res[f"{name}_{mode}"] = entry
+    return res
 
 
 if __name__ == "__main__":

@@ -86,23 +86,29 @@ typedef struct CUstream_st* spec_stream_t; /* same object as cudaStream_t */
 /* ------------------------------------------------------------------ draft */
 
 /* Draft-step softmax and top-k.  [ML] section 3: probs = softmax(logits),
- * then top-k; [ZS] 5.1: with a temperature, the stored probabilities are the
- * processed ones.
+ * then top-k; the top-k probabilities are the tree scores, from a plain
+ * softmax (T_score = 1 in the draft loop).  [ZS] 5.1: with a temperature,
+ * the stored draft distribution q is the processed one (temperature T).
  *   logits     [R, V] (dtype), row-major.
- *   T          temperature > 0; p_v = exp((l_v - max l)/T) / sum_u exp(...).
+ *   T          temperature > 0 of q (probs_or_null, row_stats_or_null):
+ *              p_v = exp((l_v - max l)/T) / sum_u exp((l_u - max l)/T).
+ *   T_score    temperature > 0 of topk_p (the same formula at T_score).
+ *              When q is written and T_score != T, the one pass over the
+ *              row keeps a normaliser at each temperature.
  *   k          1 <= k <= min(V, SPEC_MAX_TOPK).
- *   topk_p     [R, k] fp32 out: probabilities of the top-k tokens.
- *   topk_idx   [R, k] int32 out: indices by (logit desc, index asc).
- *   probs_or_null [R, V] fp32 out (optional): the full distribution (the
- *              draft distribution q that stochastic verify reads).
+ *   topk_p     [R, k] fp32 out: probabilities of the top-k tokens at T_score.
+ *   topk_idx   [R, k] int32 out: indices by (logit desc, index asc), the
+ *              same at every temperature.
+ *   probs_or_null [R, V] fp32 out (optional): the full distribution at T
+ *              (the draft distribution q that stochastic verify reads).
  *   row_stats_or_null [R, 2] fp32 out (optional): the row's maximum m and
  *              normaliser Z = sum 2^((l - m) log2(e)/T), from which
  *              spec_verify_sample_qlogits recomputes exactly the values
  *              probs_or_null would hold.
  * A row whose maximum is not finite gets zero probabilities and counts in
  * SPEC_STAT_NONFINITE_ROW. */
-int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
-                      float* topk_p, int32_t* topk_idx, float* probs_or_null,
+int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, float T_score,
+                      int k, float* topk_p, int32_t* topk_idx, float* probs_or_null,
                       float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream);
 
 /* Draft sampling with caller uniforms (chain drafts drawn from q; [ZS] 5.1
@@ -188,8 +194,8 @@ typedef struct spec_expand {
 /* spec_softmax_topk with the step's pool expansion fused (expand->k == k;
  * R = expand->B at step 0, expand->B * k after; topk_p / topk_idx laid out
  * as spec_tree_expand reads them). */
-int spec_softmax_topk_expand(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
-                             float* topk_p, int32_t* topk_idx, float* probs_or_null,
+int spec_softmax_topk_expand(const void* logits, int dtype, int64_t R, int64_t V, float T,
+                             float T_score, int k, float* topk_p, int32_t* topk_idx, float* probs_or_null,
                              float* row_stats_or_null, int32_t* stats_or_null, const spec_expand_t* expand,
                              spec_stream_t stream);
 

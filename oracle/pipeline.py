@@ -79,9 +79,11 @@ def fetch_request(cfg, work, b):
     return d
 
 
-def run_request(cfg, d, mode, compact=False):
+def run_request(cfg, d, mode, compact=False, kv_pool=None):
     """Oracle step for one fetched request: returns (tree, q rows keyed by
-    draft-table row, target [N, V], verify outputs, compaction outputs)."""
+    draft-table row, target [N, V], verify outputs, compaction outputs).
+    kv_pool (uint8 [slots, bytes], host): the whole slot payload pool, whose
+    moved slots the compaction copies in place."""
     b, T, N = d["b"], cfg.T, cfg.N
     want_q = mode == "sample"
     sampled = cfg.kind == "chain" and mode == "sample"
@@ -126,5 +128,6 @@ def run_request(cfg, d, mode, compact=False):
                           tree["retrieve_next_sibling"], d["coins"], d["u_final"], budget=budget, eos=d["eos"])
     c = None
     if compact and "req_to_token" in d:
-        c = compact_slots(d["seq_lens"], v["accept_path"], v["accept_length"], d["req_to_token"], cfg.page_size)
+        c = compact_slots(d["seq_lens"], v["accept_path"], v["accept_length"], d["req_to_token"], cfg.page_size,
+                          kv_pool=kv_pool)
     return tree, q, target, v, c

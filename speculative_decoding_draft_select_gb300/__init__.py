@@ -43,7 +43,7 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 
 _SIGS = {
-    "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P]),
+    "spec_softmax_topk": (_I, [_P, _I, _I64, _I64, _F, _F, _I, _P, _P, _P, _P, _P, _P]),
     "spec_sample": (_I, [_P, _I, _P, _I64, _I64, _F, _P, _P, _P, _P, _P, _P]),
     "spec_softmax_sample": (_I, [_P, _I, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P]),
     "spec_tree_pool_size": (_I64, [_I, _I]),
@@ -70,7 +70,7 @@ _SIGS = {
     "tli_constrain_map_planned_expand": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                               _P]),
     "tli_constrain_map_qlogits": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "spec_softmax_topk_expand": (_I, [_P, _I, _I64, _I64, _F, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "spec_softmax_topk_expand": (_I, [_P, _I, _I64, _I64, _F, _F, _I, _P, _P, _P, _P, _P, _P, _P]),
     "spec_softmax_sample_expand": (_I, [_P, _I, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P]),
@@ -167,10 +167,12 @@ def new_stats(device="cuda"):
 # ------------------------------------------------------------------- draft
 
 def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want_probs=False, row_stats=None,
-                      stats=None, expand=None):
+                      stats=None, expand=None, score_T=None):
     """logits [R, V] -> (topk_p [R, k] f32, topk_idx [R, k] i32, probs [R, V] f32 or None).
-    row_stats [R, 2] f32 (optional) receives each row's (max, normaliser).
+    probs and row_stats [R, 2] f32 (optional: each row's (max, normaliser))
+    are at temperature T; topk_p at score_T (None: T).
     expand = (pool, step): the step's pool expansion in the same launch."""
+    score_T = T if score_T is None else score_T
     _dev(logits, name="logits")
     V = logits.shape[-1]
     R = logits.numel() // V
@@ -182,10 +184,12 @@ def spec_softmax_topk(logits, T, k, topk_p=None, topk_idx=None, probs=None, want
     _dev(row_stats, torch.float32, "row_stats")
     _dev(stats, torch.int32, "stats")
     if expand is not None:
-        _call("spec_softmax_topk_expand", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
+        _call("spec_softmax_topk_expand", _ptr(logits), _logit_code(logits), R, V, float(T), float(score_T), int(k),
+              _ptr(topk_p),
               _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _expand(expand), _stream())
     else:
-        _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), int(k), _ptr(topk_p),
+        _call("spec_softmax_topk", _ptr(logits), _logit_code(logits), R, V, float(T), float(score_T), int(k),
+              _ptr(topk_p),
               _ptr(topk_idx), _ptr(probs), _ptr(row_stats), _ptr(stats), _stream())
     return topk_p, topk_idx, probs
 

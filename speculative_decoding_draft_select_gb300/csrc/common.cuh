@@ -155,6 +155,16 @@ __device__ __forceinline__ float2 exp2_sum_pairs(float2 s, const float* x, float
   return s;
 }
 
+// s + (sum over j of 2^(x_j c.x - mc.x), sum over j of 2^(x_j c.y - mc.y)):
+// one element's terms at two temperatures side by side in a register pair.
+template <int N>
+__device__ __forceinline__ float2 exp2_sum_two(float2 s, const float* x, float2 c, float2 mc) {
+  const float2 nmc = make_float2(-mc.x, -mc.y);
+#pragma unroll
+  for (int j = 0; j < N; ++j) s = add2(s, exp2_2(fma2(splat(x[j]), c, nmc)));
+  return s;
+}
+
 // Programmatic dependent launch.  Every kernel of the library is launched
 // (launch_k) so that it may be scheduled before the previous kernel on the
 // stream has finished; pdl_enter, its first statement, waits until that

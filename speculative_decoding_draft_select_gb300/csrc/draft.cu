@@ -6,6 +6,11 @@
 // stored draft distribution is the processed one (temperature applied), and
 // drafts are drawn from it.
 //
+// The tree scores are the top-k probabilities of a plain softmax (the
+// Multi-Layer EAGLE page, section 3: no temperature), while the stored q is
+// at the temperature T (zero-to-sglang 5.1).  When a launch writes q and the
+// two temperatures differ, the pass keeps a normaliser for each.
+//
 // One CTA streams one logit row with 16-byte loads (8 in flight per thread).
 // That pass gives each thread's online softmax partials (max, sum of
 // 2^((x - max) * log2e / T)) and its best element.  The K-th best of the
@@ -102,14 +107,18 @@ struct TopK {
 // a thread whose keys are all -inf ends with bi = INT_MAX and takes its
 // first element afterwards (own_first).  For K == 1 the block's best is the
 // top-1; for K > 1 the thread bests give the pass-B threshold.
-template <int DT, bool SECOND = false>
+//
+// TWO: a second normaliser at another temperature, c1 = log2(e) / T_score:
+// s0 then sums 2^((x - m) c) and s1 sums 2^((x - m) c1); without it s0 and s1
+// are two halves of the one sum at c.
+template <int DT, bool SECOND = false, bool TWO = false>
 struct ArgmaxVisitor {
-  float c, m, mc, s0, s1;  // mc = m c
+  float c, c1, m, mc, mc1, s0, s1;  // mc = m c, mc1 = m c1
   int bi;
   float m2v;  // SECOND: the largest key of the thread's other elements (NaN skipped)
   __device__ __forceinline__ void reset() {
     m = neg_inf();
-    mc = 0.0f;
+    mc = mc1 = 0.0f;
     s0 = s1 = 0.0f;
     bi = INT_MAX;
     m2v = neg_inf();
@@ -117,6 +126,9 @@ struct ArgmaxVisitor {
   __device__ __forceinline__ void rescale(float nm) {
     if (m == neg_inf()) {
       s0 = s1 = 0.0f;
+    } else if (TWO) {
+      s0 *= fast_exp2((m - nm) * c);
+      s1 *= fast_exp2((m - nm) * c1);
     } else {
       const float f = fast_exp2((m - nm) * c);
       s0 *= f;
@@ -124,6 +136,7 @@ struct ArgmaxVisitor {
     }
     m = nm;
     mc = nm * c;
+    if (TWO) mc1 = nm * c1;
   }
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
     if (!ok) return;
@@ -135,7 +148,10 @@ struct ArgmaxVisitor {
     } else if (SECOND) {
       m2v = fmaxf(m2v, xk);
     }
-    if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
+    if (m != neg_inf()) {
+      s0 += fast_exp2(fmaf(xk, c, -mc));
+      if (TWO) s1 += fast_exp2(fmaf(xk, c1, -mc1));
+    }
   }
   __device__ __forceinline__ void visit_vec(const uint4& raw, int64_t first, bool ok) {
     constexpr int kv = Logit<DT>::kVec;
@@ -166,7 +182,8 @@ struct ArgmaxVisitor {
       m2v = fmaxf(m2v, vmax);
     }
     if (m != neg_inf()) {
-      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
+      const float2 a = TWO ? exp2_sum_two<kv>(make_float2(s0, s1), x, make_float2(c, c1), make_float2(mc, mc1))
+                           : exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
       s0 = a.x;
       s1 = a.y;
     }
@@ -451,9 +468,12 @@ constexpr size_t draft_smem_bytes() {
 // whose best reaches the threshold (about K of them), collecting the
 // elements before or at it; the exact top-K is ranked among them.  All
 // reductions are fixed-order.
-template <int DT, int K, int THREADS>
+//
+// c = log2(e) / T is the temperature of probs and row_stats (q); with TWO,
+// topk_p are at c1 = log2(e) / T_score (the tree scores), else at c.
+template <int DT, int K, int THREADS, bool TWO>
 __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
-    softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, int k,
+    softmax_topk_kernel(const void* __restrict__ logits, int64_t V, float c, float c1, int k,
                         float* __restrict__ topk_p, int32_t* __restrict__ topk_idx,
                         float* __restrict__ probs, float* __restrict__ row_stats,
                         int32_t* __restrict__ stats, ExpandArgs ex) {
@@ -475,7 +495,7 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   const void* row = static_cast<const char*>(logits) + r * V * esz;
   // pass A: online softmax and every thread's best element (and for K > 1
   // the largest key among its other elements)
-  ArgmaxVisitor<DT, (K > 1)> st{c};
+  ArgmaxVisitor<DT, (K > 1), TWO> st{c, c1};
   st.reset();
   for_row_fast<DT, kDraftUnroll>(row, V, st, threadIdx.x, THREADS);
   st.own_first(row, V, threadIdx.x);
@@ -491,10 +511,12 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     fv[threadIdx.x] = neg_inf();
     fi[threadIdx.x] = INT_MAX;
   }
-  float m = st.m, s = st.s0 + st.s1;
+  float m = st.m, s = TWO ? st.s0 : st.s0 + st.s1;
+  float m1 = st.m, s1 = st.s1;  // TWO: the score temperature's normaliser
   block_ms<0>(m, s, c, sm, ss);  // its barriers also publish lv / li
-  if (isfinite(m) && !isfinite(s)) {
-    // the row holds a NaN: recompute the normaliser with NaN as -inf
+  if (TWO) block_ms<0>(m1, s1, c1, sm, ss);  // m1 == m: the same keys
+  if (isfinite(m) && !(isfinite(s) && (!TWO || isfinite(s1)))) {
+    // the row holds a NaN: recompute the normalisers with NaN as -inf
     KeyedSum ks{c, m * c, 0.0f};
     for_row<DT, 2>(row, V, ks);
     const float part = warp_sum(ks.s);
@@ -504,7 +526,19 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
     float tot = 0.0f;
     for (int w2 = 0; w2 < kWarps; ++w2) tot += ss[w2];
     s = tot;
+    if (TWO) {
+      KeyedSum ks1{c1, m * c1, 0.0f};
+      for_row<DT, 2>(row, V, ks1);
+      const float part1 = warp_sum(ks1.s);
+      __syncthreads();
+      if (lane == 0) ss[warp] = part1;
+      __syncthreads();
+      float tot1 = 0.0f;
+      for (int w2 = 0; w2 < kWarps; ++w2) tot1 += ss[w2];
+      s1 = tot1;
+    }
   }
+  if (!TWO) s1 = s;
   if constexpr (K == 1) {
     if (warp == 0) warp_select_k<1>(lv, li, THREADS, fv, fi);
   } else {
@@ -586,7 +620,9 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   const float invz = 1.0f / s;
   if (threadIdx.x < k) {
     const int j = threadIdx.x;
-    const float pj = finite ? fminf(fast_exp2(fmaf(fv[j], c, -mc)) * invz, 1.0f) : 0.0f;
+    // the score: at c1 with TWO, else at c (c1 == c or no q written)
+    const float cs = TWO ? c1 : c;
+    const float pj = finite ? fminf(fast_exp2(fmaf(fv[j], cs, -(m * cs))) * (TWO ? 1.0f / s1 : invz), 1.0f) : 0.0f;
     topk_idx[r * k + j] = fi[j];
     topk_p[r * k + j] = pj;
     // a chain's pool expansion (k = 1) by thread 0 from its own outputs
@@ -985,17 +1021,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
   if (probs) write_probs<DT>(row, V64, true, Mc, c, 1.0f / Z, probs + r * V64);
 }
 
-template <int DT, int K, int THREADS>
-int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
+template <int DT, int K, int THREADS, bool TWO>
+int launch_softmax_topk_t2(const void* logits, int64_t R, int64_t V, float c, float c1, int k, float* topk_p,
+                           int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex,
+                           cudaStream_t s) {
   constexpr size_t smem = draft_smem_bytes<K>();
-  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K, THREADS>,
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(softmax_topk_kernel<DT, K, THREADS, TWO>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  launch_k(softmax_topk_kernel<DT, K, THREADS>, static_cast<unsigned>(R), THREADS, smem, s, logits, V, c, k, topk_p,
-           topk_idx, probs, row_stats, stats, ex);
+  launch_k(softmax_topk_kernel<DT, K, THREADS, TWO>, static_cast<unsigned>(R), THREADS, smem, s, logits, V, c, c1, k,
+           topk_p, topk_idx, probs, row_stats, stats, ex);
   return launch_status();
+}
+
+// c: the temperature of q (probs, row_stats); c1: that of topk_p.  The
+// two-normaliser instance runs only when q is written at another
+// temperature than the scores.
+template <int DT, int K, int THREADS>
+int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, float c1, int k, float* topk_p,
+                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex,
+                          cudaStream_t s) {
+  const bool want_q = probs != nullptr || row_stats != nullptr;
+  if (want_q && c != c1)
+    return launch_softmax_topk_t2<DT, K, THREADS, true>(logits, R, V, c, c1, k, topk_p, topk_idx, probs, row_stats,
+                                                        stats, ex, s);
+  const float cc = want_q ? c : c1;
+  return launch_softmax_topk_t2<DT, K, THREADS, false>(logits, R, V, cc, cc, k, topk_p, topk_idx, probs, row_stats,
+                                                       stats, ex, s);
 }
 
 // One CTA per row.  With few rows (at most two per SM of a 152-SM GB300)
@@ -1004,23 +1057,29 @@ int launch_softmax_topk_t(const void* logits, int64_t R, int64_t V, float c, int
 constexpr int64_t kFewRows = 2 * 152;
 
 template <int DT, int K>
-int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
+int launch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, float c1, int k, float* topk_p,
+                        int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex,
+                        cudaStream_t s) {
   if (R <= kFewRows)
-    return launch_softmax_topk_t<DT, K, 512>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
-  return launch_softmax_topk_t<DT, K, kDraftThreads>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats,
-                                                     ex, s);
+    return launch_softmax_topk_t<DT, K, 512>(logits, R, V, c, c1, k, topk_p, topk_idx, probs, row_stats, stats, ex,
+                                             s);
+  return launch_softmax_topk_t<DT, K, kDraftThreads>(logits, R, V, c, c1, k, topk_p, topk_idx, probs, row_stats,
+                                                     stats, ex, s);
 }
 
 template <int DT>
-int dispatch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int k, float* topk_p,
-                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex, cudaStream_t s) {
-  if (k <= 1) return launch_softmax_topk<DT, 1>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
-  if (k <= 2) return launch_softmax_topk<DT, 2>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
-  if (k <= 4) return launch_softmax_topk<DT, 4>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
-  if (k <= 8) return launch_softmax_topk<DT, 8>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
-  if (k <= 16) return launch_softmax_topk<DT, 16>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
-  return launch_softmax_topk<DT, 32>(logits, R, V, c, k, topk_p, topk_idx, probs, row_stats, stats, ex, s);
+int dispatch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, float c1, int k, float* topk_p,
+                          int32_t* topk_idx, float* probs, float* row_stats, int32_t* stats, const ExpandArgs& ex,
+                          cudaStream_t s) {
+#define SPEC_TOPK_CASE(KK)                                                                                   \
+  return launch_softmax_topk<DT, KK>(logits, R, V, c, c1, k, topk_p, topk_idx, probs, row_stats, stats, ex, s)
+  if (k <= 1) SPEC_TOPK_CASE(1);
+  if (k <= 2) SPEC_TOPK_CASE(2);
+  if (k <= 4) SPEC_TOPK_CASE(4);
+  if (k <= 8) SPEC_TOPK_CASE(8);
+  if (k <= 16) SPEC_TOPK_CASE(16);
+  SPEC_TOPK_CASE(32);
+#undef SPEC_TOPK_CASE
 }
 
 }  // namespace
@@ -1029,10 +1088,11 @@ int dispatch_softmax_topk(const void* logits, int64_t R, int64_t V, float c, int
 using namespace specdec;
 
 namespace {
-int softmax_topk_impl(const void* logits, int dtype, int64_t R, int64_t V, float T, int k, float* topk_p,
-                      int32_t* topk_idx, float* probs_or_null, float* row_stats_or_null, int32_t* stats_or_null,
-                      const spec_expand_t* expand, spec_stream_t stream) {
+int softmax_topk_impl(const void* logits, int dtype, int64_t R, int64_t V, float T, float T_score, int k,
+                      float* topk_p, int32_t* topk_idx, float* probs_or_null, float* row_stats_or_null,
+                      int32_t* stats_or_null, const spec_expand_t* expand, spec_stream_t stream) {
   if (R < 0 || V < 1 || k < 1 || k > V || !(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
+  if (!(T_score > 0.0f) || !isfinite(T_score)) return SPEC_ERR_INVALID_ARG;
   if (R > 0 && (logits == nullptr || topk_p == nullptr || topk_idx == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (k > SPEC_MAX_TOPK || V > SPEC_MAX_VOCAB || R > INT_MAX) return SPEC_ERR_UNSUPPORTED;
@@ -1042,29 +1102,29 @@ int softmax_topk_impl(const void* logits, int dtype, int64_t R, int64_t V, float
     if (e != SPEC_OK) return e;
   }
   if (R == 0) return SPEC_OK;
-  const float c = kLog2e / T;
+  const float c = kLog2e / T, c1 = T_score == T ? c : kLog2e / T_score;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return dtype == SPEC_BF16
-             ? dispatch_softmax_topk<SPEC_BF16>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
+             ? dispatch_softmax_topk<SPEC_BF16>(logits, R, V, c, c1, k, topk_p, topk_idx, probs_or_null,
                                                 row_stats_or_null, stats_or_null, ex, s)
-             : dispatch_softmax_topk<SPEC_F32>(logits, R, V, c, k, topk_p, topk_idx, probs_or_null,
+             : dispatch_softmax_topk<SPEC_F32>(logits, R, V, c, c1, k, topk_p, topk_idx, probs_or_null,
                                                row_stats_or_null, stats_or_null, ex, s);
 }
 }  // namespace
 
-extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
+extern "C" int spec_softmax_topk(const void* logits, int dtype, int64_t R, int64_t V, float T, float T_score, int k,
                                  float* topk_p, int32_t* topk_idx, float* probs_or_null,
                                  float* row_stats_or_null, int32_t* stats_or_null, spec_stream_t stream) {
-  return softmax_topk_impl(logits, dtype, R, V, T, k, topk_p, topk_idx, probs_or_null, row_stats_or_null,
+  return softmax_topk_impl(logits, dtype, R, V, T, T_score, k, topk_p, topk_idx, probs_or_null, row_stats_or_null,
                            stats_or_null, nullptr, stream);
 }
 
-extern "C" int spec_softmax_topk_expand(const void* logits, int dtype, int64_t R, int64_t V, float T, int k,
-                                        float* topk_p, int32_t* topk_idx, float* probs_or_null,
+extern "C" int spec_softmax_topk_expand(const void* logits, int dtype, int64_t R, int64_t V, float T, float T_score,
+                                        int k, float* topk_p, int32_t* topk_idx, float* probs_or_null,
                                         float* row_stats_or_null, int32_t* stats_or_null,
                                         const spec_expand_t* expand, spec_stream_t stream) {
   if (expand == nullptr) return SPEC_ERR_INVALID_ARG;
-  return softmax_topk_impl(logits, dtype, R, V, T, k, topk_p, topk_idx, probs_or_null, row_stats_or_null,
+  return softmax_topk_impl(logits, dtype, R, V, T, T_score, k, topk_p, topk_idx, probs_or_null, row_stats_or_null,
                            stats_or_null, expand, stream);
 }
 

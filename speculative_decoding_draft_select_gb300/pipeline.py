@@ -37,6 +37,12 @@ from . import (new_pool, new_stats, spec_build_tree, spec_compact_freed_capacity
                tli_plan_build, tli_plan_bytes)
 
 
+# The draft loop's tree scores are the top-k of a plain softmax ("[SGLang]
+# Multi-Layer EAGLE", section 3); the temperature (zero-to-sglang ch.10 5.1)
+# belongs to the stored q.
+SCORE_T = 1.0
+
+
 def step_offsets(B, topk, steps):
     offs = [0] + [B + (s - 1) * B * topk for s in range(1, steps)]
     return offs, B + (steps - 1) * B * topk
@@ -154,7 +160,7 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
                                 row_stats=st, probs=qs, stats=buf.stats, expand=(buf.pool, s))
         else:
             spec_softmax_topk(rows, T, k, topk_p=buf.topk_p[s], topk_idx=buf.topk_idx[s], probs=qs, row_stats=st,
-                              stats=buf.stats, expand=(buf.pool, s))
+                              stats=buf.stats, expand=(buf.pool, s), score_T=SCORE_T)
         if timer is not None:
             timer.end(s)
     spec_build_tree(buf.pool, buf.N, root_token, seq_lens, out=buf.tree)

@@ -8,6 +8,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+# Stochastic decisions the parity tests excused because the oracle's uniform
+# lay within the tolerance of a decision boundary: (test, excused, compared).
+BOUNDARY_CASES = []
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
 
@@ -20,3 +25,21 @@ def golden():
         with open(os.path.join(ROOT, "tests", "golden", name)) as f:
             return json.load(f)
     return load
+
+
+@pytest.fixture(scope="session")
+def boundary_report():
+    """Record (label, excused, compared) for the terminal summary."""
+    def add(label, excused, compared):
+        BOUNDARY_CASES.append((label, int(excused), int(compared)))
+    return add
+
+
+def pytest_terminal_summary(terminalreporter):
+    if not BOUNDARY_CASES:
+        return
+    tr = terminalreporter
+    total = sum(e for _, e, _ in BOUNDARY_CASES)
+    tr.write_sep("-", f"boundary-excused stochastic decisions: {total}")
+    for label, excused, compared in BOUNDARY_CASES:
+        tr.write_line(f"{label}: {excused} of {compared} requests differ only within 1e-5 of a decision boundary")

@@ -52,25 +52,16 @@ def test_binding_exports_exist_and_refuse_host_tensors():
                               without_replacement=True)
 
 
-def test_host_side_argument_checks(lib):
+def test_host_side_argument_checks_null_pointers(lib):
+    """Checks reached with null pointers only: nothing here can launch."""
     null = None
-    # k > V, T <= 0, bad dtype, null pointers
-    assert lib.spec_softmax_topk(null, 1, 4, 3, 1.0, 4, null, null, null, null, null, null) == -1
-    assert lib.spec_softmax_topk(null, 1, 4, 8, 0.0, 2, null, null, null, null, null, null) == -1
-    assert lib.spec_softmax_topk(null, 1, 4, 8, 1.0, 2, null, null, null, null, null, null) == -1
-    assert lib.spec_softmax_topk(ctypes.c_void_p(16), 7, 4, 8, 1.0, 2, ctypes.c_void_p(16), ctypes.c_void_p(16),
-                                 null, null, null, null) == -2
-    assert lib.spec_softmax_topk(ctypes.c_void_p(16), 1, 4, 100, 1.0, 33, ctypes.c_void_p(16),
-                                 ctypes.c_void_p(16), null, null, null, null) == -2  # k above the limit
-    # fused softmax + draw: T <= 0, bad dtype, a vocabulary beyond its shared-memory tiles
-    p16 = ctypes.c_void_p(16)
-    assert lib.spec_softmax_sample(p16, 1, 4, 8, 0.0, p16, p16, null, null, null, null, null) == -1
-    assert lib.spec_softmax_sample(p16, 5, 4, 8, 1.0, p16, p16, null, null, null, null, null) == -2
-    assert lib.spec_softmax_sample(p16, 1, 4, 524289, 1.0, p16, p16, null, null, null, null, null) == -2
-    assert lib.spec_softmax_sample(p16, 0, 4, 262145, 1.0, p16, p16, null, null, null, null, null) == -2
+    # k > V, T <= 0, T_score <= 0, null pointers
+    assert lib.spec_softmax_topk(null, 1, 4, 3, 1.0, 1.0, 4, null, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 0.0, 1.0, 2, null, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 1.0, 0.0, 2, null, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 4, 8, 1.0, 1.0, 2, null, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk(null, 1, 0, 8, 1.0, 1.0, 2, null, null, null, null, null, null) == 0
     assert lib.spec_softmax_sample(null, 1, 0, 8, 1.0, null, null, null, null, null, null, null) == 0
-    # empty batches are no-ops
-    assert lib.spec_softmax_topk(null, 1, 0, 8, 1.0, 2, null, null, null, null, null, null) == 0
     assert lib.spec_tree_expand(0, 2, 4, 0, null, null, null, null, null, null, null, null, null) == -1
     assert lib.spec_tree_expand(2, 2, 4, 2, null, null, null, null, null, null, null, null, null) == -1
     assert lib.spec_build_tree(1, 2, 2, 8, *([null] * 15)) == -1  # N > P = 7
@@ -80,24 +71,48 @@ def test_host_side_argument_checks(lib):
                                           *([null] * 8), 0, null) == -1
     assert lib.spec_compact_slots(2, 4, 0, *([null] * 4), 16, *([null] * 4), 0, *([null] * 3), 0, 0, null,
                                   null) == -1
-    # verify flags: unknown bits are rejected before anything else is looked at
-    p16 = ctypes.c_void_p(16)
-    assert lib.spec_verify_sample_flags(2, 4, 10, 1, p16, 1.0, *([p16] * 8), -1, *([p16] * 6), null, p16, 1 << 20,
-                                        2, null) == -1
-    assert lib.spec_verify_sample_qlogits_flags(2, 4, 10, 1, p16, 1.0, p16, 1, p16, 1.0, *([p16] * 7), -1,
-                                                *([p16] * 6), null, p16, 1 << 20, 6, null) == -1
     assert lib.spec_verify_sample_flags(0, 4, 10, 1, *([null] * 1), 1.0, *([null] * 8), -1, *([null] * 8), 0, 1,
                                         null) == 0
     assert lib.tli_constrain_map(4, 10, 10, null, 1, null, null, 1.0, null, null, null, null, null, null) == -1
     assert lib.tli_map_ids(null, null, -1, null, 0, 0, null) == -1
-    # plan: missing or misaligned buffers, planned constrain without a plan
     assert lib.tli_plan_build(10, 10, null, null, null, null) == -1
+    assert lib.tli_constrain_map_planned(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
+                                         null) == 0
+    assert lib.tli_constrain_map_qlogits(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
+                                         null, null, null) == 0
+
+
+def _cuda_present():
+    import torch
+    return torch.cuda.is_available()
+
+
+@pytest.mark.skipif(_cuda_present(), reason="made-up addresses are passed only where no GPU could run a kernel")
+def test_host_side_argument_checks(lib):
+    """Checks that need non-null (made-up) addresses to get past the null
+    tests.  Each must return before any launch; run only without a GPU, so
+    that a check that regressed gives a wrong return code, never a kernel
+    reading a made-up address."""
+    null = None
+    p16 = ctypes.c_void_p(16)
+    # bad dtype, k above the limit
+    assert lib.spec_softmax_topk(p16, 7, 4, 8, 1.0, 1.0, 2, p16, p16, null, null, null, null) == -2
+    assert lib.spec_softmax_topk(p16, 1, 4, 100, 1.0, 1.0, 33, p16, p16, null, null, null, null) == -2
+    # fused softmax + draw: T <= 0, bad dtype, a vocabulary beyond its shared-memory tiles
+    assert lib.spec_softmax_sample(p16, 1, 4, 8, 0.0, p16, p16, null, null, null, null, null) == -1
+    assert lib.spec_softmax_sample(p16, 5, 4, 8, 1.0, p16, p16, null, null, null, null, null) == -2
+    assert lib.spec_softmax_sample(p16, 1, 4, 524289, 1.0, p16, p16, null, null, null, null, null) == -2
+    assert lib.spec_softmax_sample(p16, 0, 4, 262145, 1.0, p16, p16, null, null, null, null, null) == -2
+    # verify flags: unknown bits are rejected before anything else is looked at
+    assert lib.spec_verify_sample_flags(2, 4, 10, 1, p16, 1.0, *([p16] * 8), -1, *([p16] * 6), null, p16, 1 << 20,
+                                        2, null) == -1
+    assert lib.spec_verify_sample_qlogits_flags(2, 4, 10, 1, p16, 1.0, p16, 1, p16, 1.0, *([p16] * 7), -1,
+                                                *([p16] * 6), null, p16, 1 << 20, 6, null) == -1
+    # plan: misaligned buffers, planned constrain without a plan
     assert lib.tli_plan_build(10, 10, p16, p16, ctypes.c_void_p(24), null) == -1
     assert lib.tli_plan_build(1 << 23, 10, p16, p16, p16, null) == -2
     assert lib.tli_constrain_map_planned(4, 10, 10, p16, 1, p16, p16, null, 1.0, p16, p16, p16, null, null,
                                          null) == -1
-    assert lib.tli_constrain_map_planned(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
-                                         null) == 0
     # q in logit form: t2d and both outputs required, element-aligned logits, T > 0; R = 0 is a no-op
     p17 = ctypes.c_void_p(17)
     assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, null, null, 1.0, p16, p16, p16, p16, p16, null,
@@ -110,15 +125,13 @@ def test_host_side_argument_checks(lib):
                                          null, null) == -1
     assert lib.tli_constrain_map_qlogits(4, 10, 10, p16, 1, p16, p16, p16, 0.0, p16, p16, p16, p16, p16, null,
                                          null, null) == -1
-    assert lib.tli_constrain_map_qlogits(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
-                                         null, null, null) == 0
     # fused expansion: no expansion struct, or one whose k or row count does not match the launch
-    assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 4, p16, p16, null, null, null, null, null) == -1
+    assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 1.0, 4, p16, p16, null, null, null, null, null) == -1
     assert lib.spec_softmax_sample_expand(p16, 1, 8, 100, 1.0, p16, p16, p16, null, null, null, null, null) == -1
     pool = sd.new_pool(2, 4, 3, device="cpu")
     ex = sd._expand((pool, 1))
-    assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 2, p16, p16, null, null, null, ex, null) == -1  # k
-    assert lib.spec_softmax_topk_expand(p16, 1, 7, 100, 1.0, 4, p16, p16, null, null, null, ex, null) == -1  # R
+    assert lib.spec_softmax_topk_expand(p16, 1, 8, 100, 1.0, 1.0, 2, p16, p16, null, null, null, ex, null) == -1  # k
+    assert lib.spec_softmax_topk_expand(p16, 1, 7, 100, 1.0, 1.0, 4, p16, p16, null, null, null, ex, null) == -1  # R
     assert lib.spec_softmax_sample_expand(p16, 1, 2, 100, 1.0, p16, p16, p16, null, null, null, ex, null) == -1
     for plan in (null, p16):  # k = 4 is not a chain
         assert lib.tli_constrain_map_qlogits(2, 10, 10, p16, 1, p16, p16, plan, 1.0, p16, p16, p16, p16, p16, null,

@@ -47,9 +47,12 @@ def test_single_rank_is_the_identity():
 
 def test_reference_arm_runs_on_rank_zero_only():
     from types import SimpleNamespace
-    args = SimpleNamespace(steps=1, warmup=1)
-    assert bench.run_reference(args, CONFIGS["c1"], "sample", 1) is None
-    line = bench.run_reference(args, CONFIGS["c1"], "sample", 0)
+    args = SimpleNamespace(steps=1, warmup=1, q=None)
+    assert bench.run_reference(args, CONFIGS["c1"], "sample", 1, 2) is None
+    line = bench.run_reference(args, CONFIGS["c1"], "sample", 0, 1)
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
+    # the same config dict as the GPU arm prints for this workload
+    assert line["config"] == bench.config_dict(CONFIGS["c1"], "sample", "logits", 1)
+    assert line["cpu_baseline"]["host"]["nproc"] >= 1

@@ -3,12 +3,15 @@ device memory (a plugin handed only its input and output buffers by a host
 framework that owns all device memory, or a path that must not call
 cudaMalloc).  Its scratch is a fixed array inside the library, so its output
 must equal spec_verify_greedy's (with caller scratch) exactly, call after
-call, even though every call reuses the same array."""
+call, even though every call reuses the same array -- and both must equal the
+CPU oracle's greedy commit."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import speculative_decoding_draft_select_gb300 as sd
+from oracle.pipeline import np_logits
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +62,11 @@ def test_noalloc_matches_scratch_entry_point_on_consecutive_calls(dtype):
         for name in OUTPUTS:
             assert torch.equal(got[name], ref[name]), name
         assert int(ref["accept_length"].max()) >= 2
+        o = oracle.verify_greedy(np_logits(target), tree["draft_token"].cpu().numpy(),
+                                 tree["retrieve_next_token"].cpu().numpy(), tree["retrieve_next_sibling"].cpu().numpy(),
+                                 budget=budget.cpu().numpy(), eos=7)
+        for name in OUTPUTS:
+            np.testing.assert_array_equal(got[name].cpu().numpy(), o[name], err_msg=name)
 
 
 def test_noalloc_rejects_batches_above_its_array():
