@@ -497,7 +497,7 @@ def compare_with_oracle(cfg, mode, buf, kept, boundary=1e-5):
         same = same_tree and all(np.array_equal(out[k][b], o[k][0]) for k in VERIFY_FIELDS)
         if same:
             exact += 1
-        elif same_tree and mode == "sample" and o["margin"][0] < boundary:
+        elif (same_tree and mode == "sample" and o["margin"][0] < boundary) or o["draft_margin"] < boundary:
             near += 1
         else:
             bad += 1

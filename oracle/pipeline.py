@@ -82,6 +82,10 @@ def fetch_request(cfg, work, b):
 def run_request(cfg, d, mode, compact=False, kv_pool=None):
     """Oracle step for one fetched request: returns (tree, q rows keyed by
     draft-table row, target [N, V], verify outputs, compaction outputs).
+    The verify outputs carry "draft_margin": the smallest distance of a
+    sampled draft's uniform to a CDF boundary of its draw (inf for drafts
+    taken by top-k), so that a draft sampled differently can be told apart
+    from an error.
     kv_pool (uint8 [slots, bytes], host): the whole slot payload pool, whose
     moved slots the compaction copies in place."""
     b, T, N = d["b"], cfg.T, cfg.N
@@ -89,6 +93,7 @@ def run_request(cfg, d, mode, compact=False, kv_pool=None):
     sampled = cfg.kind == "chain" and mode == "sample"
     pool = Pool(1, cfg.topk, cfg.steps)
     q = {}
+    draft_margin = np.inf  # the draft draws' closest approach to a CDF boundary
     for s, rows in enumerate(d["rows"]):
         x = np.stack([d["draft"][r] for r in rows])
         if cfg.kind == "tli":
@@ -98,7 +103,8 @@ def run_request(cfg, d, mode, compact=False, kv_pool=None):
         elif sampled:
             _, _, probs, _ = softmax_topk(x, T, 1, want_probs=True)
             u = np.array([d["draft_u"][r] for r in rows], np.float32)
-            tok, prob, _, _ = sample(u, logits=x, T=T)
+            tok, prob, margin, _ = sample(u, logits=x, T=T)
+            draft_margin = min(draft_margin, float(margin.min()))
             tree_expand(pool, s, prob.astype(np.float32), tok)
         else:
             tp, ti, probs, _ = softmax_topk(x, T, cfg.topk, want_probs=want_q, score_T=SCORE_T)
@@ -126,6 +132,7 @@ def run_request(cfg, d, mode, compact=False, kv_pool=None):
                 qn[0, n] = q[int(r)].astype(np.float32)
         v = verify_sample(target[None], T, qn, tree["draft_token"], tree["retrieve_next_token"],
                           tree["retrieve_next_sibling"], d["coins"], d["u_final"], budget=budget, eos=d["eos"])
+    v["draft_margin"] = draft_margin
     c = None
     if compact and "req_to_token" in d:
         c = compact_slots(d["seq_lens"], v["accept_path"], v["accept_length"], d["req_to_token"], cfg.page_size,

@@ -370,14 +370,15 @@ def compare_pipeline(cfg, work, mode, reqs, q_mode="probs"):
     reqs = list(reqs)
     exact = boundary = 0
     host_tree = {name: tree[name].cpu().numpy() for name in tree}
+    names = ("draft_token", "parent", "positions", "tree_mask", "retrieve_index", "retrieve_next_token",
+             "retrieve_next_sibling", "q_row")
     for b, (ot, q, target, o, _) in zip(reqs, _oracle_requests(cfg, work, mode, reqs)):
-        for name in ("draft_token", "parent", "positions", "tree_mask", "retrieve_index", "retrieve_next_token",
-                     "retrieve_next_sibling", "q_row"):
-            gv = host_tree[name][b]
-            ov = ot[name][0]
-            if name == "retrieve_index":
-                ov = ov + b * cfg.N
-            np.testing.assert_array_equal(gv, ov, err_msg=f"{cfg.name} {name} request {b}")
+        ov = {name: ot[name][0] + (b * cfg.N if name == "retrieve_index" else 0) for name in names}
+        if not all(np.array_equal(host_tree[name][b], ov[name]) for name in names) and o["draft_margin"] < BOUNDARY:
+            boundary += 1  # a draft drawn within the tolerance of a CDF boundary: the tree may differ
+            continue
+        for name in names:
+            np.testing.assert_array_equal(host_tree[name][b], ov[name], err_msg=f"{cfg.name} {name} request {b}")
         if verify_compare(out, o, b, 0, mode):
             exact += 1
         else:
