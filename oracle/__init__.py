@@ -289,6 +289,28 @@ def tli_constrain_map(draft_logits, d2t, t2d, T: float, want_q: bool = False):
     return o
 
 
+def pruned_head(hidden, weight, ids, d2t, T: float, want_logits: bool = False):
+    """The pruned draft LM head (oracle_pruned_head): hidden [M, H] and
+    weight [K, H] (float32, or uint16 bf16 bits), ids [K], d2t [V_d]."""
+    h, hdt = logits_buffer(hidden)
+    w, wdt = logits_buffer(weight)
+    M, H = h.shape
+    K = w.shape[0]
+    assert w.shape[1] == H
+    idv = _c(ids, np.int32)
+    d2 = _c(d2t, np.int32)
+    o = {"logits": np.zeros((M, K), np.float64) if want_logits else None,
+         "top1_rank": np.zeros(M, np.int32), "top1_draft": np.zeros(M, np.int32),
+         "top1_target": np.zeros(M, np.int32), "top1_p": np.zeros(M, np.float64),
+         "row_max": np.zeros(M, np.float64), "row_z": np.zeros(M, np.float64), "row_flag": np.zeros(M, np.int32)}
+    rc = lib().oracle_pruned_head(
+        ctypes.c_int64(M), ctypes.c_int64(H), ctypes.c_int64(K), _p(h), ctypes.c_int(hdt), _p(w), ctypes.c_int(wdt),
+        _p(idv), _p(d2), ctypes.c_double(T), _p(o["logits"]), _p(o["top1_rank"]), _p(o["top1_draft"]),
+        _p(o["top1_target"]), _p(o["top1_p"]), _p(o["row_max"]), _p(o["row_z"]), _p(o["row_flag"]))
+    _check(rc, "pruned_head")
+    return o
+
+
 def tli_plan(d2t, t2d):
     """The TLI map plan of (d2t, t2d): K, bitmap words, intersection ids
     before each word, each target's partner rank (layout of tli_plan_build;

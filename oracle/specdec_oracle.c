@@ -783,6 +783,69 @@ int oracle_tli_constrain_map(int64_t R, int64_t Vd, int64_t Vt, const void* draf
     return OR_OK;
 }
 
+/* [TLI] "Modifications", _try_prune_draft_lm_head / _PrunedReindexLMHead:
+ * with the vocabulary intersection fixed, the draft LM head keeps only the
+ * weight rows of the intersection's draft ids, so each draft row's logits are
+ * computed for those K ids alone (O(M K H) instead of O(M V_d H)), in the
+ * order of the weight rows (the ascending intersection ids); the constrained
+ * top-1, its mapping to the target vocabulary and the constrained draft
+ * distribution then follow as in oracle_tli_constrain_map, over those K
+ * logits.
+ *   hidden [M, H] (hdtype), weight [K, H] (wdtype): logits[m][k] =
+ *     sum over h of hidden[m][h] * weight[k][h], in fp64, h in order.
+ *   ids [K]: the draft id of weight row k; d2t [V_d] as in
+ *     oracle_tli_constrain_map.
+ *   top1_rank [M]: the weight row of the largest logit (ties: the lower row,
+ *     which is the lower draft id); top1_draft = ids[rank], top1_target =
+ *     d2t[ids[rank]]; top1_p: its probability at temperature T;
+ *     row_max, row_z: the row's max logit and sum of exp((l - max)/T).
+ *   logits_or_null [M, K] fp64.
+ * NaN logits count as -inf; a row with no finite logit gets rank -1,
+ * probability 0 and row_flag 1. */
+int oracle_pruned_head(int64_t M, int64_t H, int64_t K, const void* hidden, int hdtype,
+                       const void* weight, int wdtype, const int32_t* ids, const int32_t* d2t,
+                       double T, double* logits_or_null, int32_t* top1_rank, int32_t* top1_draft,
+                       int32_t* top1_target, double* top1_p, double* row_max, double* row_z,
+                       int32_t* row_flag)
+{
+    if (M < 0 || H < 1 || K < 1 || !(T > 0.0)) return OR_ERR;
+    double* l = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!l) return OR_ERR;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                acc += logit_at(hidden, hdtype, m * H + h) * logit_at(weight, wdtype, k * H + h);
+            l[k] = acc;
+            if (logits_or_null) logits_or_null[m * K + k] = acc;
+        }
+        int64_t best = -1;
+        double mx = -INFINITY;
+        for (int64_t k = 0; k < K; ++k) {
+            double x = order_key(l[k]);
+            if (best < 0 || x > mx) { best = k; mx = x; }
+        }
+        row_max[m] = mx;
+        if (!isfinite(mx)) {
+            top1_rank[m] = top1_draft[m] = top1_target[m] = -1;
+            top1_p[m] = 0.0;
+            row_z[m] = 0.0;
+            row_flag[m] = 1;
+            continue;
+        }
+        double Z = 0.0;
+        for (int64_t k = 0; k < K; ++k) Z += exp((order_key(l[k]) - mx) / T);
+        top1_rank[m] = (int32_t)best;
+        top1_draft[m] = ids[best];
+        top1_target[m] = d2t[ids[best]];
+        top1_p[m] = 1.0 / Z;
+        row_z[m] = Z;
+        row_flag[m] = 0;
+    }
+    free(l);
+    return OR_OK;
+}
+
 /* The map plan of a vocabulary pair, written out from its definition (the
  * layout that tli_plan_build fills; [TLI] "Modifications": vocab_mapping.py
  * builds the id maps once per model pair, and the plan restates them):

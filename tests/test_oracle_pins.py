@@ -916,3 +916,55 @@ def test_tli_config_constraints(golden):
         assert oracle.tli_check_config(*c)
     for c in g["invalid"]:
         assert not oracle.tli_check_config(*c)
+
+
+# ----------------------------------------------------- pruned draft LM head
+
+def test_pruned_head_hand_example():
+    """[TLI] Modifications (_try_prune_draft_lm_head): logits only for the
+    intersection's weight rows.  Worked by hand: hidden [1, 0.5] against
+    weight rows [1, 0], [0, 2], [1, 1] gives logits [1, 1, 1.5]; the top-1 is
+    row 2 (draft id 9, target id 4) with p = 1 / (1 + 2 e^-0.5) = 0.4518628.
+    hidden [2, 0] gives [2, 0, 2]: the tie goes to row 0 (the lower draft id)."""
+    hidden = np.array([[1.0, 0.5], [2.0, 0.0]], np.float32)
+    weight = np.array([[1.0, 0.0], [0.0, 2.0], [1.0, 1.0]], np.float32)
+    ids = np.array([3, 7, 9], np.int32)
+    d2t = np.full(12, -1, np.int32)
+    d2t[[3, 7, 9]] = [11, 0, 4]
+    o = oracle.pruned_head(hidden, weight, ids, d2t, 1.0, want_logits=True)
+    np.testing.assert_array_equal(o["logits"], [[1.0, 1.0, 1.5], [2.0, 0.0, 2.0]])
+    assert list(o["top1_rank"]) == [2, 0]
+    assert list(o["top1_draft"]) == [9, 3] and list(o["top1_target"]) == [4, 11]
+    assert abs(o["top1_p"][0] - 0.4518628) < 1e-7
+    # row 2: p of each tied top = 1 / (2 + e^-2) = 1 / 2.1353353 = 0.4683105
+    assert abs(o["top1_p"][1] - 0.4683105) < 1e-7
+    assert list(o["row_flag"]) == [0, 0]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_pruned_head_equals_constrain_on_the_full_row(seed):
+    """With integer-valued inputs every product and sum is exact, so the
+    pruned head must equal the TLI constraint applied to the full draft row
+    (the K logits at their draft ids, -inf elsewhere) -- a transposed or
+    misindexed weight operand, or a rank / id mix-up, fails here.  The logits
+    also equal an fp64 matrix product computed independently."""
+    rng = np.random.default_rng(seed)
+    M, H, K, Vd, Vt = 7, 24, 50, 300, 80
+    hidden = rng.integers(-3, 4, (M, H)).astype(np.float32)
+    weight = rng.integers(-2, 3, (K, H)).astype(np.float32)
+    ids = np.sort(rng.choice(Vd, K, replace=False)).astype(np.int32)
+    d2t = np.full(Vd, -1, np.int32)
+    d2t[ids] = rng.choice(Vt, K, replace=False)
+    t2d = np.full(Vt, -1, np.int32)
+    t2d[d2t[ids]] = ids
+    T = 0.9
+    o = oracle.pruned_head(bf16_bits(hidden), bf16_bits(weight), ids, d2t, T, want_logits=True)
+    np.testing.assert_array_equal(o["logits"], hidden.astype(np.float64) @ weight.astype(np.float64).T)
+    full = np.full((M, Vd), -np.inf, np.float32)
+    full[:, ids] = o["logits"].astype(np.float32)
+    c = oracle.tli_constrain_map(full, d2t, t2d, T)
+    np.testing.assert_array_equal(o["top1_draft"], c["top1_draft"])
+    np.testing.assert_array_equal(o["top1_target"], c["top1_target"])
+    np.testing.assert_allclose(o["top1_p"], c["top1_p"], rtol=1e-12)
+    np.testing.assert_array_equal(ids[o["top1_rank"]], o["top1_draft"])
+    np.testing.assert_allclose(o["row_z"], np.exp((o["logits"] - o["row_max"][:, None]) / T).sum(1), rtol=1e-12)
