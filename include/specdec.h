@@ -244,7 +244,8 @@ int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_t* stats_or
                     spec_stream_t stream);
 
 /* Scratch bytes for spec_verify_greedy / spec_verify_sample (per-row
- * max, normaliser and argmax of the target logits). */
+ * max, normaliser and argmax of the target logits, and the chain verify's
+ * per-request state). */
 size_t spec_verify_ws_size(int B, int N);
 
 /* Greedy verify ([ZS] 4.1 greedy_commit, generalised to trees).  One pass
@@ -331,9 +332,22 @@ int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, const void* t
  * divides by 1 minus the rejected tokens' q. */
 #define SPEC_VERIFY_WITHOUT_REPLACEMENT 1
 
+/* The caller's trees are chains: every node has at most one child (topk = 1
+ * drafting, [ZS] 3.3's k drafts in a row).  The acceptance test at node n
+ * then reads only row n, q row n and the child's coin, so the launch tests
+ * every node right after its row's statistics and resolves each request as
+ * soon as the rows on its path are done; the one draw a request needs (the
+ * residual at its first rejection, or p at its leaf) is cut into chunks that
+ * any CTA takes.  The rule and every decision's arithmetic are those of the
+ * tree walk; only the order of the draw's partial sums differs, so a drawn
+ * token can differ only at a CDF boundary.  A node with more than one child
+ * has only its first child tested and counts SPEC_STAT_BAD_REQUEST.  With one
+ * child per node, SPEC_VERIFY_WITHOUT_REPLACEMENT changes nothing. */
+#define SPEC_VERIFY_CHAIN 2
+
 /* spec_verify_sample / spec_verify_sample_qlogits with flags: 0 (the same
- * call) or SPEC_VERIFY_WITHOUT_REPLACEMENT; other bits give
- * SPEC_ERR_INVALID_ARG. */
+ * call), SPEC_VERIFY_WITHOUT_REPLACEMENT and / or SPEC_VERIFY_CHAIN; other
+ * bits give SPEC_ERR_INVALID_ARG. */
 int spec_verify_sample_flags(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
                              const float* q, const int32_t* q_row_or_null, const int32_t* draft_token,
                              const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
@@ -351,6 +365,33 @@ int spec_verify_sample_qlogits_flags(int B, int N, int64_t V, int dtype, const v
                                      int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                                      int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
                                      size_t ws_bytes, int flags, spec_stream_t stream);
+
+/* The committed ids mapped back to the draft vocabulary in the same launch
+ * ([TLI] Modifications: map_target_to_draft_ids, applied to the accepted and
+ * drawn target ids before the next draft step; hook
+ * forward_draft_extend_after_decode).  out[b*N + i] = table[committed[b*N +
+ * i]] when that id is in [0, table_len) and the entry is >= 0, else
+ * fallback_id; -1 where committed is -1. */
+typedef struct spec_id_map {
+  const int32_t* table;  /* [table_len] device, e.g. t2d */
+  int64_t table_len;
+  int32_t fallback_id;
+  int32_t* out;          /* [B, N] device */
+} spec_id_map_t;
+
+/* spec_verify_sample_qlogits_flags with the id map above fused into its
+ * epilogue.  flags must include SPEC_VERIFY_CHAIN (TLI drafts are chains:
+ * tli_check_config); SPEC_ERR_INVALID_ARG otherwise, or for a NULL map,
+ * table or out, or table_len < 1. */
+int spec_verify_sample_qlogits_mapped(int B, int N, int64_t V, int dtype, const void* target_logits, float T,
+                                      const void* q_logits, int q_dtype, const float* q_stats, float T_q,
+                                      const int32_t* q_row_or_null, const int32_t* draft_token,
+                                      const int32_t* retrieve_next_token, const int32_t* retrieve_next_sibling,
+                                      const float* coins, const float* u_final, const int32_t* budget_or_null,
+                                      int32_t eos_id, int32_t* committed, int32_t* num_committed,
+                                      int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
+                                      int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
+                                      size_t ws_bytes, int flags, const spec_id_map_t* map, spec_stream_t stream);
 
 /* Greedy verify without caller scratch.  No passage of the pages has a
  * counterpart: this entry point exists for callers that cannot allocate
@@ -505,6 +546,37 @@ int tli_constrain_map_qlogits(int64_t R, int64_t V_d, int64_t V_t, const void* d
  * unk id, or eos for models without one). */
 int tli_map_ids(const int32_t* in, int32_t* out, int64_t n, const int32_t* table,
                 int64_t table_len, int32_t fallback_id, spec_stream_t stream);
+
+/* Pruned draft LM head ([TLI] Modifications: _try_prune_draft_lm_head /
+ * _PrunedReindexLMHead keep only the LM-head weight rows of the
+ * intersection's draft ids, so the draft logits cost O(M K H) instead of
+ * O(M V_d H); the constrained top-1 and its mapping follow as in
+ * tli_constrain_map, over those K logits).  A tensor-core GEMM (tcgen05,
+ * bf16 operands, fp32 accumulation in tensor memory) with the reduction
+ * fused into its epilogue:
+ *   logits[m][k] = sum over h of hidden[m][h] * weight[k][h].
+ *   hidden [M, H] bf16, weight [K, H] bf16 (row k: the LM-head row of draft
+ *     id ids[k]), both row-major, 16-byte aligned, H a multiple of 8
+ *     (SPEC_ERR_UNSUPPORTED otherwise).
+ *   ids [K] int32: the draft id of each weight row, ascending (so ties, which
+ *     go to the lower row, go to the lower draft id); d2t [V_d].
+ *   top1_draft / top1_target [M] int32: ids[k*] and d2t[ids[k*]] of the
+ *     largest logit; top1_p [M]: its probability at temperature T over the K
+ *     logits; top1_rank_or_null [M]: k*.
+ *   row_stats_or_null [M, 2] fp32: each row's max logit and
+ *     sum 2^((l - max) log2(e)/T).
+ *   logits_or_null [M, K] fp32: the logits themselves.
+ *   ws: tli_pruned_head_ws_size(M, K) bytes, 256-byte aligned (per-tile
+ *     partials of the reduction).
+ * A row with no finite logit gets -1 ids, probability 0 and counts in
+ * SPEC_STAT_EMPTY_INTERSECTION.  Its waits are bounded: one that runs out is
+ * counted in SPEC_STAT_WAIT_TIMEOUT (results void). */
+size_t tli_pruned_head_ws_size(int64_t M, int64_t K);
+int tli_pruned_head(int64_t M, int64_t H, int64_t K, const void* hidden, const void* weight,
+                    const int32_t* ids, const int32_t* d2t, int64_t V_d, float T, int32_t* top1_draft,
+                    int32_t* top1_target, float* top1_p, int32_t* top1_rank_or_null,
+                    float* row_stats_or_null, float* logits_or_null, int32_t* stats_or_null, void* ws,
+                    size_t ws_bytes, spec_stream_t stream);
 
 /* TLI configuration check ([TLI] Modifications, server_args validation):
  * SPEC_OK iff topk == 1, num_steps >= 1 and num_draft_tokens ==

@@ -18,10 +18,10 @@ __all__ = [
     "SpecError", "F32", "BF16", "STATS", "lib", "library_path",
     "spec_softmax_topk", "spec_softmax_sample", "spec_sample", "spec_tree_pool_size", "spec_tree_expand", "spec_build_tree",
     "spec_verify_ws_size", "spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_sample",
-    "spec_verify_sample_qlogits", "WITHOUT_REPLACEMENT", "spec_compact_freed_capacity",
+    "spec_verify_sample_qlogits", "WITHOUT_REPLACEMENT", "CHAIN", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_constrain_map_qlogits", "tli_plan_bytes", "tli_plan_build",
     "tli_map_ids",
-    "tli_check_config", "spec_wait_probe",
+    "tli_check_config", "tli_pruned_head", "spec_wait_probe",
     "new_stats", "new_pool",
 ]
 
@@ -72,11 +72,15 @@ _SIGS = {
     "tli_constrain_map_qlogits": (_I, [_I64, _I64, _I64, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_softmax_topk_expand": (_I, [_P, _I, _I64, _I64, _F, _F, _I, _P, _P, _P, _P, _P, _P, _P]),
     "spec_softmax_sample_expand": (_I, [_P, _I, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "spec_verify_sample_qlogits_mapped": (_I, [_I, _I, _I64, _I, _P, _F, _P, _I, _P, _F, _P, _P, _P, _P, _P, _P,
+                                               _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _P, _P]),
     "spec_verify_greedy_noalloc": (_I, [_I, _I, _I64, _I, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P]),
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
     "spec_wait_probe": (_I, [_P, _I64, _P, _P, _P]),
     "tli_check_config": (_I, [_I, _I, _I]),
+    "tli_pruned_head_ws_size": (_SZ, [_I64, _I64]),
+    "tli_pruned_head": (_I, [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
 }
 
 
@@ -355,13 +359,16 @@ def spec_verify_greedy_noalloc(target, draft_token, next_token, next_sibling, bu
 
 
 WITHOUT_REPLACEMENT = 1  # SPEC_VERIFY_WITHOUT_REPLACEMENT
+CHAIN = 2  # SPEC_VERIFY_CHAIN
 
 
 def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coins, u_final, q_row=None,
-                       budget=None, eos_id=-1, out=None, ws=None, stats=None, without_replacement=False):
+                       budget=None, eos_id=-1, out=None, ws=None, stats=None, without_replacement=False,
+                       chain=False):
     """target [B, N, V]; q fp32 rows of length V (a [rows, V] table with q_row [B, N], or [B, N, V]).
     without_replacement: the sibling update for children drawn without
-    replacement (spec_verify_sample_flags with SPEC_VERIFY_WITHOUT_REPLACEMENT)."""
+    replacement (spec_verify_sample_flags with SPEC_VERIFY_WITHOUT_REPLACEMENT);
+    chain: the trees are chains (SPEC_VERIFY_CHAIN: the chain verify launch)."""
     _dev(target, name="target")
     B, N, V = target.shape
     _dev(q, torch.float32, "q")
@@ -380,8 +387,9 @@ def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coin
             _ptr(next_token), _ptr(next_sibling), _ptr(coins), _ptr(u_final), _ptr(budget), int(eos_id),
             _ptr(out["committed"]), _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]),
             _ptr(out["next_root"]), _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws), ws.numel())
-    if without_replacement:
-        _call("spec_verify_sample_flags", *args, WITHOUT_REPLACEMENT, _stream())
+    flags = (WITHOUT_REPLACEMENT if without_replacement else 0) | (CHAIN if chain else 0)
+    if flags:
+        _call("spec_verify_sample_flags", *args, flags, _stream())
     else:
         _call("spec_verify_sample", *args, _stream())
     return out
@@ -389,9 +397,12 @@ def spec_verify_sample(target, T, q, draft_token, next_token, next_sibling, coin
 
 def spec_verify_sample_qlogits(target, T, q_logits, q_stats, T_q, draft_token, next_token, next_sibling, coins,
                                u_final, q_row=None, budget=None, eos_id=-1, out=None, ws=None, stats=None,
-                               without_replacement=False):
+                               without_replacement=False, chain=False, id_map=None):
     """Stochastic verify with q given as draft-logit rows [rows, V] plus their
-    (max, normaliser) [rows, 2] from spec_softmax_topk(row_stats=...)."""
+    (max, normaliser) [rows, 2] from spec_softmax_topk(row_stats=...).
+    id_map = (table, fallback_id) (chains only): the committed ids are also
+    mapped through table into out["committed_mapped"] in the same launch
+    (spec_verify_sample_qlogits_mapped; TLI's target-to-draft map)."""
     _dev(target, name="target")
     B, N, V = target.shape
     _dev(q_logits, name="q_logits")
@@ -412,11 +423,26 @@ def spec_verify_sample_qlogits(target, T, q_logits, q_stats, T_q, draft_token, n
             _ptr(coins), _ptr(u_final), _ptr(budget), int(eos_id), _ptr(out["committed"]),
             _ptr(out["num_committed"]), _ptr(out["accept_length"]), _ptr(out["accept_path"]), _ptr(out["next_root"]),
             _ptr(out.get("walk_info")), _ptr(stats), _ptr(ws), ws.numel())
-    if without_replacement:
-        _call("spec_verify_sample_qlogits_flags", *args, WITHOUT_REPLACEMENT, _stream())
+    flags = (WITHOUT_REPLACEMENT if without_replacement else 0) | (CHAIN if chain else 0)
+    if id_map is not None:
+        table, fallback = id_map
+        _dev(table, torch.int32, "id_map table")
+        if "committed_mapped" not in out:
+            out["committed_mapped"] = torch.empty((B, N), dtype=torch.int32, device=target.device)
+        m = SpecIdMap(ctypes.c_void_p(table.data_ptr()), table.numel(), int(fallback),
+                      ctypes.c_void_p(out["committed_mapped"].data_ptr()))
+        _call("spec_verify_sample_qlogits_mapped", *args, flags, ctypes.byref(m), _stream())
+    elif flags:
+        _call("spec_verify_sample_qlogits_flags", *args, flags, _stream())
     else:
         _call("spec_verify_sample_qlogits", *args, _stream())
     return out
+
+
+class SpecIdMap(ctypes.Structure):
+    """spec_id_map_t"""
+    _fields_ = [("table", ctypes.c_void_p), ("table_len", ctypes.c_int64), ("fallback_id", ctypes.c_int32),
+                ("out", ctypes.c_void_p)]
 
 
 # -------------------------------------------------------------- compaction
@@ -560,6 +586,38 @@ def tli_map_ids(ids, table, fallback_id, out=None):
     _dev(table, torch.int32, "table")
     out = _out(out, ids.shape, torch.int32, ids, "out")
     _call("tli_map_ids", _ptr(ids), _ptr(out), ids.numel(), _ptr(table), table.numel(), int(fallback_id), _stream())
+    return out
+
+
+def tli_pruned_head(hidden, weight, ids, d2t, T, want_logits=False, out=None, ws=None, stats=None):
+    """Pruned draft LM head on the tensor cores: hidden [M, H] and weight
+    [K, H] bf16 (row k belongs to draft id ids[k]), d2t [V_d].  Returns a
+    dict with top1_draft, top1_target, top1_rank [M] int32, top1_p [M],
+    row_stats [M, 2] and, with want_logits, logits [M, K] fp32."""
+    _dev(hidden, torch.bfloat16, "hidden")
+    _dev(weight, torch.bfloat16, "weight")
+    _dev(ids, torch.int32, "ids")
+    _dev(d2t, torch.int32, "d2t")
+    _dev(stats, torch.int32, "stats")
+    M, H = hidden.shape
+    K = weight.shape[0]
+    if weight.shape[1] != H or ids.numel() != K:
+        raise ValueError("weight must be [K, H] and ids [K]")
+    dev = hidden.device
+    if out is None:
+        out = {"top1_draft": torch.empty(M, dtype=torch.int32, device=dev),
+               "top1_target": torch.empty(M, dtype=torch.int32, device=dev),
+               "top1_rank": torch.empty(M, dtype=torch.int32, device=dev),
+               "top1_p": torch.empty(M, dtype=torch.float32, device=dev),
+               "row_stats": torch.empty((M, 2), dtype=torch.float32, device=dev)}
+        if want_logits:
+            out["logits"] = torch.empty((M, K), dtype=torch.float32, device=dev)
+    need = int(lib().tli_pruned_head_ws_size(M, K))
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _call("tli_pruned_head", M, H, K, _ptr(hidden), _ptr(weight), _ptr(ids), _ptr(d2t), d2t.numel(), float(T),
+          _ptr(out["top1_draft"]), _ptr(out["top1_target"]), _ptr(out["top1_p"]), _ptr(out.get("top1_rank")),
+          _ptr(out.get("row_stats")), _ptr(out.get("logits")), _ptr(stats), _ptr(ws), ws.numel(), _stream())
     return out
 
 

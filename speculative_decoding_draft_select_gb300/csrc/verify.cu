@@ -31,126 +31,17 @@
 #include <climits>
 
 #include "cdf.cuh"
+#include "chain.h"
 #include "common.cuh"
+#include "walk.cuh"
 
 namespace specdec {
 namespace {
-
-#ifndef SPEC_WALK_THREADS
-#define SPEC_WALK_THREADS 128
-#endif
-#ifndef SPEC_WALK_ELEMS
-#define SPEC_WALK_ELEMS 16
-#endif
-// The stochastic walk: a cluster of 1, 2 or 4 CTAs of kWalkThreads threads
-// per request.
-constexpr int kWalkThreads = SPEC_WALK_THREADS;
-constexpr int kWalkElems = SPEC_WALK_ELEMS;  // consecutive elements per thread in a tile
-constexpr size_t kMaxDynSmem = 227 * 1024;  // opt-in shared memory of one CTA
-
-// Tiles each walk thread keeps in flight: 2 to 8, the ring at most 32 KB per
-// CTA (four CTAs share an SM).
-__host__ __device__ constexpr int walk_ring_depth(int chunks) {
-  return 32768 / (chunks * kWalkThreads * 16) > 8   ? 8
-         : 32768 / (chunks * kWalkThreads * 16) < 2 ? 2
-                                                     : 32768 / (chunks * kWalkThreads * 16);
-}
-
-// Bound on a wait for another CTA's row (about 50 ms at 2 GHz); past it the
-// launch counts SPEC_STAT_WAIT_TIMEOUT and goes on.
-constexpr long long kWaitLimitCycles = 100000000LL;
-
-// Waits (one thread) until *flag != 0 or `limit` clock cycles pass; a
-// timeout is counted in SPEC_STAT_WAIT_TIMEOUT.  Returns whether the flag
-// was seen.
-__device__ __forceinline__ bool wait_flag(const int* flag, long long limit, int32_t* stats) {
-  const long long t0 = clock64();
-  while (!ld_acquire_gpu(flag)) {
-    if (clock64() - t0 > limit) {
-      bump(stats, SPEC_STAT_WAIT_TIMEOUT);
-      return false;
-    }
-    __nanosleep(128);
-  }
-  return true;
-}
 
 __global__ void wait_probe_kernel(const int* flag, long long limit, int32_t* stats, int32_t* seen) {
   pdl_enter();
   if (threadIdx.x == 0) *seen = wait_flag(flag, limit, stats) ? 1 : 0;
 }
-
-__device__ __forceinline__ float prob_of(float key, float c, float mc, float invz) {
-  return fminf(fast_exp2(fmaf(key, c, -mc)) * invz, 1.0f);
-}
-
-// Per-thread row statistics: running max m (NaN ignored), the first index
-// holding it, and for sampling s = sum 2^((x - m) c) in two accumulators
-// (shorter dependency chains).  A NaN element turns s into NaN; the kernel
-// then recomputes s for that row with NaN as -inf.
-template <int DT, bool STOCH>
-struct RowStatVisitor {
-  float c, m, s0, s1;
-  int bi;
-  float mc;  // m c
-  __device__ __forceinline__ void rescale(float nm) {
-    if (STOCH) {
-      if (m == neg_inf()) {
-        s0 = s1 = 0.0f;
-      } else {
-        const float f = fast_exp2((m - nm) * c);
-        s0 *= f;
-        s1 *= f;
-      }
-      mc = nm * c;
-    }
-    m = nm;
-  }
-  __device__ __forceinline__ void visit1(float x, int64_t idx, bool ok) {
-    if (!ok) return;
-    const float xk = order_key(x);
-    if (xk > m) {
-      rescale(xk);
-      bi = static_cast<int>(idx);
-    }
-    if (STOCH && m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
-  }
-  __device__ __forceinline__ void visit_vec(const uint4& w, int64_t first, bool) {
-    constexpr int kv = Logit<DT>::kVec;
-    float x[kv];
-    unpack<DT>(w, x);
-    float vmax;
-    if (DT == SPEC_BF16) {
-      vmax = max8_bf16(w);
-    } else {
-      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
-    }
-    if (vmax > m) {
-      int j0 = 0;
-#pragma unroll
-      for (int j = kv - 1; j >= 0; --j)
-        if (x[j] == vmax) j0 = j;
-      rescale(vmax);
-      bi = static_cast<int>(first) + j0;
-    }
-    if (STOCH && m != neg_inf()) {
-      const float2 a = exp2_sum_pairs<kv>(make_float2(s0, s1), x, c, mc);
-      s0 = a.x;
-      s1 = a.y;
-    }
-  }
-};
-
-// Sum of 2^((key(x) - m) c) over a row with NaN as -inf (the slow path for
-// rows that contain NaN).
-struct KeyedSum {
-  float c, mc, s;
-  template <int N>
-  __device__ __forceinline__ void visit(const float* x, int64_t) {
-#pragma unroll
-    for (int j = 0; j < N; ++j) s += fast_exp2(fmaf(order_key(x[j]), c, -mc));
-  }
-};
 
 constexpr int kStatThreads = 256;
 constexpr int kStatUnroll = 8;  // 16-byte loads in flight per thread
@@ -266,261 +157,6 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
 }
 
 // -------------------------------------------------------- stochastic walk
-
-// Where a node's draft distribution q comes from.
-//   QProbs:     materialised fp32 rows (q[v] read directly).
-//   QLogits<D>: the draft logits row and that row's (max, normaliser) as the
-//               draft softmax wrote them.  q_at(y), used by the acceptance
-//               test, takes the same fp32 operations as the written
-//               probabilities, so both forms give bit-identical q[y].
-// The residual sweeps need q for a whole row; there (load8, ring_q8,
-// sweep_at) the normaliser is folded into the exponent,
-// q[v] = 2^(l_v c + nb), nb = -(max c + log2 Z), one operation fewer per
-// element.  Rows whose 16-byte chunks start aligned are streamed through the
-// walk's shared-memory ring (issue / ring_q8), others with direct loads.
-
-__device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-// Exponent offset nb of a row's softmax: p(x) = 2^(x c + nb); -inf when the
-// row has no finite max, which makes every probability 0 (a NaN logit gives
-// NaN, which the residual's max(0, .) turns into 0).
-__device__ __forceinline__ float folded_offset(float m, float c, float z) {
-  return (isfinite(m) && z > 0.0f && isfinite(z)) ? -fmaf(m, c, log2f(z)) : neg_inf();
-}
-
-// 8 logits [v0, v0 + 8) of a row as floats (NaN kept); past V: -inf.
-template <int DT>
-__device__ __forceinline__ void raw8_global(const void* row, int64_t V, int64_t v0, float* x) {
-  constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  const char* p = static_cast<const char*>(row) + v0 * esz;
-  if (v0 + 8 <= V && aligned16(p)) {
-    if (DT == SPEC_BF16) {
-      unpack<SPEC_BF16>(__ldg(reinterpret_cast<const uint4*>(p)), x);
-    } else {
-      unpack<SPEC_F32>(__ldg(reinterpret_cast<const uint4*>(p)), x);
-      unpack<SPEC_F32>(__ldg(reinterpret_cast<const uint4*>(p) + 1), x + 4);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = v0 + j < V ? Logit<DT>::load1(row, v0 + j) : neg_inf();
-  }
-}
-
-// Group g (elements [8g, 8g + 8)) of a thread's ring chunks of one row, as
-// floats.  DT: logits (bf16 or fp32).
-template <int DT>
-__device__ __forceinline__ void ring8(const uint4* slot, int stride, int g, float* x) {
-  if (DT == SPEC_BF16) {
-    unpack<SPEC_BF16>(slot[g * stride], x);
-  } else {
-    unpack<SPEC_F32>(slot[(2 * g) * stride], x);
-    unpack<SPEC_F32>(slot[(2 * g + 1) * stride], x + 4);
-  }
-}
-
-__device__ __forceinline__ void mask_past(float* x, int64_t v0, int64_t V, float fill) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (v0 + j >= V) x[j] = fill;
-}
-
-struct QRowProbs {
-  static constexpr int kEsz = 4;
-  const float* row;  // nullptr: no row (q = 0)
-  int64_t V;
-  __device__ __forceinline__ float q_at(int64_t v) const { return row ? __ldg(row + v) : 0.0f; }
-  __device__ __forceinline__ float sweep_at(int64_t v) const { return q_at(v); }
-  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
-    if (row) {
-      load8_f32(row, V, v0, x);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-    }
-  }
-  __device__ __forceinline__ bool ring_ok() const { return row == nullptr || aligned16(row); }
-  template <int E>
-  __device__ __forceinline__ void issue(uint4* slot, int stride, int64_t v0) const {
-    if (row) issue_row<E, 4>(slot, stride, row, V, v0);
-  }
-  // q of group g from the ring (zero-filled past V)
-  __device__ __forceinline__ void ring_q8(const uint4* slot, int stride, int g, int64_t, bool, float* x) const {
-    if (row) {
-      ring8<SPEC_F32>(slot, stride, g, x);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-    }
-  }
-};
-
-struct QProbs {
-  using Row = QRowProbs;
-  const float* q;
-  int64_t V;
-  __device__ __forceinline__ QRowProbs row(int64_t r) const { return {r >= 0 ? q + r * V : nullptr, V}; }
-};
-
-template <int QDT>
-struct QRowLogits {
-  static constexpr int kEsz = QDT == SPEC_BF16 ? 2 : 4;
-  const void* row;  // nullptr: no row, or a row whose max is not finite (q = 0)
-  int64_t V;
-  float c, mc, invz, nb;
-  __device__ __forceinline__ float q_at(int64_t v) const {
-    return row ? prob_of(order_key(Logit<QDT>::load1(row, v)), c, mc, invz) : 0.0f;
-  }
-  __device__ __forceinline__ float sweep_at(int64_t v) const {
-    return row ? fast_exp2(fmaf(order_key(Logit<QDT>::load1(row, v)), c, nb)) : 0.0f;
-  }
-  // 8 q values from 8 logits (NaN as -inf), in the packed form of the sweeps
-  __device__ __forceinline__ void probs8(float* x) const {
-    const float2 c2 = splat(c), nb2 = splat(nb);
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      const float2 e = exp2_2(fma2(make_float2(order_key(x[j]), order_key(x[j + 1])), c2, nb2));
-      x[j] = e.x;
-      x[j + 1] = e.y;
-    }
-  }
-  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
-    if (row) {
-      raw8_global<QDT>(row, V, v0, x);
-      probs8(x);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-    }
-  }
-  __device__ __forceinline__ bool ring_ok() const { return row == nullptr || aligned16(row); }
-  template <int E>
-  __device__ __forceinline__ void issue(uint4* slot, int stride, int64_t v0) const {
-    if (row) issue_row<E, kEsz>(slot, stride, row, V, v0);
-  }
-  __device__ __forceinline__ void ring_q8(const uint4* slot, int stride, int g, int64_t v0, bool full,
-                                          float* x) const {
-    if (row) {
-      ring8<QDT>(slot, stride, g, x);
-      if (!full) mask_past(x, v0, V, neg_inf());
-      probs8(x);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-    }
-  }
-};
-
-template <int QDT>
-struct QLogits {
-  using Row = QRowLogits<QDT>;
-  const void* q;
-  const float* stats;  // [rows, 2]: max, normaliser
-  int64_t V;
-  float c;
-  __device__ __forceinline__ QRowLogits<QDT> row(int64_t r) const {
-    constexpr int esz = QDT == SPEC_BF16 ? 2 : 4;
-    if (r < 0) return {nullptr, V, c, 0.0f, 0.0f, 0.0f};
-    const float m = __ldg(stats + 2 * r), z = __ldg(stats + 2 * r + 1);
-    if (!isfinite(m)) return {nullptr, V, c, 0.0f, 0.0f, 0.0f};
-    return {static_cast<const char*>(q) + r * V * esz, V, c, m * c, 1.0f / z, folded_offset(m, c, z)};
-  }
-};
-
-// Weights of the current distribution at a node for the sweeps: p (A == 0)
-// or the unnormalised residual max(0, p - A q), with p(v) = 2^(l_v c + nb).
-// Element values are computed two at a time with the packed fp32
-// instructions; load8 (per element, for the draw), ring_sum and load_sum
-// (sums for the tile pass) give the same values.
-template <int DT, class QRow>
-struct ResidualWeights {
-  static constexpr int kTargetEsz = DT == SPEC_BF16 ? 2 : 4;
-  template <int E>
-  __host__ __device__ static constexpr int target_chunks() {
-    return E * kTargetEsz / 16;
-  }
-  template <int E>
-  __host__ __device__ static constexpr int chunks() {
-    return E * (kTargetEsz + QRow::kEsz) / 16;
-  }
-  const void* lrow;
-  QRow qrow;
-  int64_t V;
-  float c, nb, A;
-  // x <- weights of 8 elements from logits l (and q values when A != 0)
-  __device__ __forceinline__ void values8(float* l, const float* q) const {
-    const float2 c2 = splat(c), nb2 = splat(nb), na2 = splat(-A);
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      float2 r = exp2_2(fma2(make_float2(l[j], l[j + 1]), c2, nb2));
-      if (q != nullptr) r = fma2(na2, make_float2(q[j], q[j + 1]), r);
-      l[j] = fmaxf(0.0f, r.x);
-      l[j + 1] = fmaxf(0.0f, r.y);
-    }
-  }
-  __device__ __forceinline__ static float2 acc8(float2 acc, const float* x) {
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) acc = add2(acc, make_float2(x[j], x[j + 1]));
-    return acc;
-  }
-  __device__ __forceinline__ void load8(int64_t v0, float* x) const {
-    raw8_global<DT>(lrow, V, v0, x);
-    if (A != 0.0f) {
-      float q[8];
-      qrow.load8(v0, q);
-      values8(x, q);
-    } else {
-      values8(x, nullptr);
-    }
-  }
-  __device__ __forceinline__ float at(int64_t v) const {
-    const float p = fast_exp2(fmaf(Logit<DT>::load1(lrow, v), c, nb));
-    return fmaxf(0.0f, A != 0.0f ? fmaf(-A, qrow.sweep_at(v), p) : p);
-  }
-  template <int E>
-  __device__ __forceinline__ float load_sum(int64_t v0) const {
-    float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int g = 0; g < E / 8; ++g) {
-      float x[8];
-      load8(v0 + 8 * g, x);
-      acc = acc8(acc, x);
-    }
-    return acc.x + acc.y;
-  }
-  __device__ __forceinline__ bool ring_ok() const { return aligned16(lrow) && (A == 0.0f || qrow.ring_ok()); }
-  template <int E>
-  __device__ __forceinline__ void issue(uint4* slot, int stride, int64_t v0) const {
-    issue_row<E, kTargetEsz>(slot, stride, lrow, V, v0);
-    if (A != 0.0f) qrow.template issue<E>(slot + target_chunks<E>() * stride, stride, v0);
-  }
-  template <int E>
-  __device__ __forceinline__ float ring_sum(const uint4* slot, int stride, int64_t v0) const {
-    const bool full = v0 + E <= V;
-    const uint4* qslot = slot + target_chunks<E>() * stride;
-    float2 acc = make_float2(0.0f, 0.0f);
-    if (A != 0.0f) {
-#pragma unroll
-      for (int g = 0; g < E / 8; ++g) {
-        float x[8], q[8];
-        ring8<DT>(slot, stride, g, x);
-        if (!full) mask_past(x, v0 + 8 * g, V, neg_inf());
-        qrow.ring_q8(qslot, stride, g, v0 + 8 * g, full, q);
-        values8(x, q);
-        acc = acc8(acc, x);
-      }
-    } else {
-#pragma unroll
-      for (int g = 0; g < E / 8; ++g) {
-        float x[8];
-        ring8<DT>(slot, stride, g, x);
-        if (!full) mask_past(x, v0 + 8 * g, V, neg_inf());
-        values8(x, nullptr);
-        acc = acc8(acc, x);
-      }
-    }
-    return acc.x + acc.y;
-  }
-};
 
 // The residual weights of a node after rejections without replacement:
 // those of W except at the ny rejected tokens ys, whose weights stay frozen
@@ -949,6 +585,7 @@ struct VerifyWs {
   int32_t* ready;  // stochastic: flag per row, then next_row, next_req (same memory as amax)
   float* m;
   float* z;
+  void* req;       // chain verify: per-request state (chain_ws_bytes)
 };
 
 VerifyWs carve(void* ws, int B, int N) {
@@ -961,6 +598,8 @@ VerifyWs carve(void* ws, int B, int N) {
   w.m = reinterpret_cast<float*>(p);
   p += align256(rows * sizeof(float));
   w.z = reinterpret_cast<float*>(p);
+  p += align256(rows * sizeof(float));
+  w.req = p;
   return w;
 }
 
@@ -996,7 +635,7 @@ extern "C" int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_
 extern "C" size_t spec_verify_ws_size(int B, int N) {
   if (B < 0 || N < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * N;
-  return align256((rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float));
+  return align256((rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float)) + chain_ws_bytes(B);
 }
 
 extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void* target_logits,
@@ -1145,7 +784,7 @@ int verify_sample_impl(int B, int N, int64_t V, int dtype, const void* target_lo
                                   int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
                                   size_t ws_bytes, int flags, spec_stream_t stream) {
   if (!(T > 0.0f) || !isfinite(T)) return SPEC_ERR_INVALID_ARG;
-  if ((flags & ~SPEC_VERIFY_WITHOUT_REPLACEMENT) != 0) return SPEC_ERR_INVALID_ARG;
+  if ((flags & ~(SPEC_VERIFY_WITHOUT_REPLACEMENT | SPEC_VERIFY_CHAIN)) != 0) return SPEC_ERR_INVALID_ARG;
   const int wor = (flags & SPEC_VERIFY_WITHOUT_REPLACEMENT) ? 1 : 0;
   const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
                               retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
@@ -1154,6 +793,15 @@ int verify_sample_impl(int B, int N, int64_t V, int dtype, const void* target_lo
   if (!q || !coins || !u_final) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float c = kLog2e / T;
+  if (flags & SPEC_VERIFY_CHAIN) {
+    // one child per node: without replacement is the same rule
+    const VerifyWs w = carve(ws, B, N);
+    const ChainIO io{q_row_or_null, draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
+                     budget_or_null, eos_id, committed, num_committed, accept_length, accept_path, next_root,
+                     walk_info_or_null, stats_or_null, nullptr, 0, -1, nullptr};
+    return chain_verify(dtype, B, N, V, target_logits, c, ChainQ{0, q, nullptr, 0.0f}, io, w.ready, w.m, w.z, w.req,
+                        s);
+  }
   const QProbs qs{q, V};
   if (dtype == SPEC_BF16)
     return launch_sample_verify<SPEC_BF16>(B, N, V, target_logits, c, qs, q_row_or_null, draft_token,
@@ -1224,9 +872,13 @@ int verify_sample_qlogits_impl(int B, int N, int64_t V, int dtype, const void* t
                                           int32_t eos_id, int32_t* committed, int32_t* num_committed,
                                           int32_t* accept_length, int32_t* accept_path, int32_t* next_root,
                                           int32_t* walk_info_or_null, int32_t* stats_or_null, void* ws,
-                                          size_t ws_bytes, int flags, spec_stream_t stream) {
+                                          size_t ws_bytes, int flags, const spec_id_map_t* map,
+                                          spec_stream_t stream) {
   if (!(T > 0.0f) || !isfinite(T) || !(T_q > 0.0f) || !isfinite(T_q)) return SPEC_ERR_INVALID_ARG;
-  if ((flags & ~SPEC_VERIFY_WITHOUT_REPLACEMENT) != 0) return SPEC_ERR_INVALID_ARG;
+  if ((flags & ~(SPEC_VERIFY_WITHOUT_REPLACEMENT | SPEC_VERIFY_CHAIN)) != 0) return SPEC_ERR_INVALID_ARG;
+  if (map != nullptr && (!(flags & SPEC_VERIFY_CHAIN) || map->table == nullptr || map->table_len < 1 ||
+                         map->out == nullptr))
+    return SPEC_ERR_INVALID_ARG;
   const int wor = (flags & SPEC_VERIFY_WITHOUT_REPLACEMENT) ? 1 : 0;
   const int rc = check_common(B, N, V, dtype, target_logits, draft_token, retrieve_next_token,
                               retrieve_next_sibling, committed, num_committed, accept_length, accept_path,
@@ -1237,6 +889,15 @@ int verify_sample_qlogits_impl(int B, int N, int64_t V, int dtype, const void* t
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float c = kLog2e / T, cq = kLog2e / T_q;
   const VerifyWs w = carve(ws, B, N);
+  if (flags & SPEC_VERIFY_CHAIN) {
+    const ChainIO io{q_row_or_null, draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
+                     budget_or_null, eos_id, committed, num_committed, accept_length, accept_path, next_root,
+                     walk_info_or_null, stats_or_null,
+                     map ? map->table : nullptr, map ? map->table_len : 0, map ? map->fallback_id : -1,
+                     map ? map->out : nullptr};
+    return chain_verify(dtype, B, N, V, target_logits, c, ChainQ{q_dtype == SPEC_BF16 ? 1 : 2, q_logits, q_stats, cq},
+                        io, w.ready, w.m, w.z, w.req, s);
+  }
 #define SPEC_QL(DT, QDT)                                                                                         \
   return sample_verify_qlogits<DT, QDT>(B, N, V, target_logits, c, q_logits, q_stats, cq, q_row_or_null,        \
                                         draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final, \
@@ -1264,7 +925,7 @@ extern "C" int spec_verify_sample_qlogits(int B, int N, int64_t V, int dtype, co
   return verify_sample_qlogits_impl(B, N, V, dtype, target_logits, T, q_logits, q_dtype, q_stats, T_q, q_row_or_null,
                                     draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
                                     budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
-                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, 0, stream);
+                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, 0, nullptr, stream);
 }
 
 extern "C" int spec_verify_sample_qlogits_flags(int B, int N, int64_t V, int dtype, const void* target_logits,
@@ -1280,7 +941,25 @@ extern "C" int spec_verify_sample_qlogits_flags(int B, int N, int64_t V, int dty
   return verify_sample_qlogits_impl(B, N, V, dtype, target_logits, T, q_logits, q_dtype, q_stats, T_q, q_row_or_null,
                                     draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
                                     budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
-                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, flags, stream);
+                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, flags, nullptr,
+                                    stream);
+}
+
+extern "C" int spec_verify_sample_qlogits_mapped(int B, int N, int64_t V, int dtype, const void* target_logits,
+                                                 float T, const void* q_logits, int q_dtype, const float* q_stats,
+                                                 float T_q, const int32_t* q_row_or_null, const int32_t* draft_token,
+                                                 const int32_t* retrieve_next_token,
+                                                 const int32_t* retrieve_next_sibling, const float* coins,
+                                                 const float* u_final, const int32_t* budget_or_null, int32_t eos_id,
+                                                 int32_t* committed, int32_t* num_committed, int32_t* accept_length,
+                                                 int32_t* accept_path, int32_t* next_root, int32_t* walk_info_or_null,
+                                                 int32_t* stats_or_null, void* ws, size_t ws_bytes, int flags,
+                                                 const spec_id_map_t* map, spec_stream_t stream) {
+  if (map == nullptr) return SPEC_ERR_INVALID_ARG;
+  return verify_sample_qlogits_impl(B, N, V, dtype, target_logits, T, q_logits, q_dtype, q_stats, T_q, q_row_or_null,
+                                    draft_token, retrieve_next_token, retrieve_next_sibling, coins, u_final,
+                                    budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
+                                    next_root, walk_info_or_null, stats_or_null, ws, ws_bytes, flags, map, stream);
 }
 
 // ------------------------------------------------- greedy verify, no scratch

@@ -168,11 +168,14 @@ def run_draft(buf: StepBuffers, draft_table, T, root_token, seq_lens, draft_u=No
 
 
 def run_verify(buf: StepBuffers, target, mode, T=1.0, coins=None, u_final=None, budget=None, eos_id=-1,
-               without_replacement=False):
+               without_replacement=False, chain=None):
     """Greedy or stochastic verify of buf.tree against target [B, N, V];
     without_replacement selects the stochastic sibling update for children
-    drawn without replacement (q renormalised without each rejected child)."""
+    drawn without replacement (q renormalised without each rejected child).
+    chain (default: the drafts are chains, topk 1) selects the chain verify
+    launch for stochastic verification."""
     t = buf.tree
+    chain = buf.topk == 1 if chain is None else chain
     if mode == "greedy":
         return spec_verify_greedy(target, t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"],
                                   budget=budget, eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)
@@ -181,11 +184,12 @@ def run_verify(buf: StepBuffers, target, mode, T=1.0, coins=None, u_final=None, 
         return spec_verify_sample_qlogits(target, T, q_logits, buf.q_stats, buf.T_draft, t["draft_token"],
                                           t["retrieve_next_token"], t["retrieve_next_sibling"], coins, u_final,
                                           q_row=t["q_row"], budget=budget, eos_id=eos_id, out=buf.verify_out,
-                                          ws=buf.ws, stats=buf.stats, without_replacement=without_replacement)
+                                          ws=buf.ws, stats=buf.stats, without_replacement=without_replacement,
+                                          chain=chain)
     return spec_verify_sample(target, T, buf.q, t["draft_token"], t["retrieve_next_token"],
                               t["retrieve_next_sibling"], coins, u_final, q_row=t["q_row"], budget=budget,
                               eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats,
-                              without_replacement=without_replacement)
+                              without_replacement=without_replacement, chain=chain)
 
 
 def run_compact(buf: StepBuffers, seq_lens, req_to_token, page_size, kv_pool=None):

@@ -548,6 +548,86 @@ def test_verify_sample_fallbacks_and_counters(B):
     assert st[sd.STATS["wait_timeout"]] == 0
 
 
+@pytest.mark.parametrize("B,N,V,q_form", [(8, 4, 33, "probs"), (96, 5, 4097, "probs"), (300, 16, 2053, "logits"),
+                                          (1100, 3, 777, "probs"), (40, 5, 128256, "logits"),
+                                          (64, 16, 30001, "logits")])
+def test_chain_verify_parity(B, N, V, q_form, boundary_report):
+    """The chain verify launch (SPEC_VERIFY_CHAIN: every node's test right
+    after its row, the draw cut into chunk items) against the oracle on
+    chains: drafts drawn from q, EOS planted in the target, budgets (zero
+    included), q[y] = 0 children, a non-finite row, and q = 2p rows (no
+    residual mass).  Every output and every counter is compared; a request
+    may differ only within 1e-5 of a decision boundary."""
+    rng = np.random.default_rng(B * 31 + N + V)
+    T = 0.8
+    eos = 5
+    nt, ns = chain_meta(B, N)
+    target = rng.normal(0, 2.5, (B, N, V)).astype(np.float32)
+    target[rng.random((B, N)) < 0.05, eos] = 30.0  # EOS rows
+    dl = target + rng.normal(0, 0.7, (B, N, V)).astype(np.float32)
+    q = _softmax64(dl, T).astype(np.float32)
+    p = _softmax64(target, T).astype(np.float32)
+    dt = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for n in range(1, N):
+            w = q[b, n - 1].astype(np.float64)
+            dt[b, n] = rng.choice(V, p=w / w.sum())
+    coins = rng.random((B, N)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    budget = rng.integers(0, N + 2, B).astype(np.int32)
+    budget[1] = 0
+    q[2, 0, dt[2, 1]] = 0.0  # q[y] = 0 with p[y] > 0
+    budget[2] = N
+    coins[3, 1:] = 0.0       # request 3 accepts everything it can
+    target[3, N - 1] = -np.inf  # ... up to a leaf row without a finite logit
+    budget[3] = N + 5
+    q[4, 0] = 2 * p[4, 0]    # no residual mass at request 4's root
+    coins[4, 1] = 0.9
+    budget[4] = N
+    stats = sd.new_stats()
+    if q_form == "probs":
+        out = sd.spec_verify_sample(dev(target), T, dev(q), dev(dt), dev(nt), dev(ns), dev(coins), dev(uf),
+                                    budget=dev(budget), eos_id=eos, stats=stats, chain=True)
+    else:
+        # q in logit form: the draft logits with their (max, normaliser) at T
+        dlt = dev(dl.reshape(B * N, V))
+        rs = torch.empty((B * N, 2), device="cuda")
+        sd.spec_softmax_topk(dlt, T, 1, row_stats=rs)
+        out = sd.spec_verify_sample_qlogits(dev(target), T, dlt, rs, T, dev(dt), dev(nt), dev(ns), dev(coins),
+                                            dev(uf), budget=dev(budget), eos_id=eos, stats=stats, chain=True)
+        # the oracle reads the same q values the logit form gives (the GPU's
+        # own written probabilities would equal them bit for bit)
+        qprobs = torch.empty((B * N, V), device="cuda")
+        sd.spec_softmax_topk(dlt, T, 1, probs=qprobs)
+        q = qprobs.view(B, N, V).cpu().numpy()
+    o = oracle.verify_sample(target, T, q, dt, nt, ns, coins, uf, budget=budget, eos=eos)
+    torch.cuda.synchronize()
+    exact = sum(verify_compare(out, o, b, b, "sample") for b in range(B))
+    boundary_report(f"chain verify B={B} N={N} V={V} q={q_form}", B - exact, B)
+    assert exact >= B - max(1, B // 100)
+    if q_form == "logits":
+        # the same launch with the committed ids mapped back through a table
+        # (TLI's target-to-draft map, fused): identical outputs plus the map
+        table = rng.integers(-1, 3 * V, V + 7).astype(np.int32)
+        out2 = sd.spec_verify_sample_qlogits(dev(target), T, dlt, rs, T, dev(dt), dev(nt), dev(ns), dev(coins),
+                                             dev(uf), budget=dev(budget), eos_id=eos, chain=True,
+                                             id_map=(dev(table), 77))
+        torch.cuda.synchronize()
+        for name in ("committed", "num_committed", "accept_length", "accept_path", "next_root", "walk_info"):
+            assert torch.equal(out2[name], out[name]), name
+        com = out2["committed"].cpu().numpy()
+        want = np.where(com >= 0, oracle.map_ids(com, table, 77), -1)
+        np.testing.assert_array_equal(out2["committed_mapped"].cpu().numpy(), want)
+    st = stats.cpu().numpy()
+    for name in ("q_zero", "residual_fallback", "cdf_fallback"):
+        assert st[sd.STATS[name]] == o[name], name
+    assert st[sd.STATS["nonfinite_row"]] == int((~np.isfinite(np.where(np.isnan(target), -np.inf, target).max(-1))).sum())
+    assert st[sd.STATS["wait_timeout"]] == 0 and st[sd.STATS["bad_request"]] == 0
+    assert int(out["num_committed"][1]) == 0
+    if q_form == "probs":
+        assert o["q_zero"] >= 1 and o["residual_fallback"] >= 1
+
+
 @pytest.mark.parametrize("B,q_form", [(24, "probs"), (200, "probs"), (400, "probs"), (24, "logits"),
                                       (400, "logits")])
 def test_verify_sample_without_replacement(B, q_form):
@@ -1116,3 +1196,79 @@ def test_captured_step_replays_the_eager_step(name, mode, q_mode):
     replayed = outputs()
     for k in eager:
         assert torch.equal(eager[k], replayed[k]), k
+
+
+# ------------------------------------------------------ pruned draft LM head
+
+def _head_inputs(rng, M, H, K, Vd, Vt):
+    hidden = torch.from_numpy(rng.normal(0, 1, (M, H)).astype(np.float32)).to(torch.bfloat16)
+    weight = torch.from_numpy(rng.normal(0, 3 / math.sqrt(H), (K, H)).astype(np.float32)).to(torch.bfloat16)
+    ids = np.sort(rng.choice(Vd, K, replace=False)).astype(np.int32)
+    d2t = np.full(Vd, -1, np.int32)
+    d2t[ids] = rng.choice(Vt, K, replace=False)
+    return hidden, weight, ids, d2t
+
+
+def _head_compare(g, o, hidden, weight, rows, T):
+    """GPU pruned-head outputs of `rows` against the oracle's.  Logits: within
+    the fp32 accumulation bound H * 2^-24 * sum |hidden * weight| (any
+    summation order); the top-1 may differ only where the oracle's two
+    logits lie within that bound of each other (counted); the probability
+    and normaliser within what that bound allows."""
+    h64 = np.abs(hidden.float().numpy().astype(np.float64))[rows]
+    w64 = np.abs(weight.float().numpy().astype(np.float64))
+    H = hidden.shape[1]
+    bound = H * 2.0 ** -24 * (h64 @ w64.T) + 1e-6
+    if "logits" in g:
+        gl = g["logits"].cpu().numpy().astype(np.float64)[rows]
+        assert np.all(np.abs(gl - o["logits"]) <= bound), np.max(np.abs(gl - o["logits"]) / bound)
+    near = 0
+    gr = g["top1_rank"].cpu().numpy()[rows]
+    for i in range(len(rows)):
+        if gr[i] != o["top1_rank"][i]:
+            a, b = gr[i], o["top1_rank"][i]
+            assert abs(o["logits"][i, a] - o["logits"][i, b]) <= bound[i, a] + bound[i, b], (i, a, b)
+            near += 1
+            continue
+        assert g["top1_draft"][rows[i]].item() == o["top1_draft"][i]
+        assert g["top1_target"][rows[i]].item() == o["top1_target"][i]
+        d = 2 * bound[i].max() / T
+        np.testing.assert_allclose(g["top1_p"][rows[i]].item(), o["top1_p"][i], rtol=math.expm1(d) + 1e-6, atol=1e-7)
+        st = g["row_stats"][rows[i]].cpu().numpy()
+        assert abs(st[0] - o["row_max"][i]) <= bound[i].max()
+        np.testing.assert_allclose(st[1], o["row_z"][i], rtol=math.expm1(d) + 1e-6)
+    return near
+
+
+@pytest.mark.parametrize("M,H,K", [(1, 64, 128), (256, 896, 5000), (100, 512, 3001), (300, 256, 1000),
+                                   (7, 200, 129), (256, 96, 260)])
+def test_pruned_head_parity(M, H, K):
+    """The tcgen05 pruned LM head against the oracle's fp64 product: one and
+    several N tiles (ragged last tile), one or two 128-row halves, a second
+    group of hidden rows (M = 300), H not a multiple of the 64-column slab."""
+    rng = np.random.default_rng(M * 7 + H + K)
+    Vd, Vt = 2 * K + 17, K + 5
+    hidden, weight, ids, d2t = _head_inputs(rng, M, H, K, Vd, Vt)
+    T = 0.9
+    stats = sd.new_stats()
+    g = sd.tli_pruned_head(dev(hidden), dev(weight), dev(ids), dev(d2t), T, want_logits=True, stats=stats)
+    torch.cuda.synchronize()
+    o = oracle.pruned_head(np_logits(hidden), np_logits(weight), ids, d2t, T, want_logits=True)
+    near = _head_compare(g, o, hidden, weight, np.arange(M), T)
+    assert near <= max(1, M // 50)
+    assert int(stats[sd.STATS["wait_timeout"]]) == 0
+
+
+def test_pruned_head_full_size_sampled_rows():
+    """The TLI workload's shapes: 256 draft rows, H = 896 (a 0.5B draft
+    model's hidden size), K = 60000 intersection rows; the oracle recomputes
+    sampled rows from both 128-row halves."""
+    rng = np.random.default_rng(60000)
+    M, H, K = 256, 896, 60000
+    hidden, weight, ids, d2t = _head_inputs(rng, M, H, K, 151936, 128256)
+    T = 1.0
+    g = sd.tli_pruned_head(dev(hidden), dev(weight), dev(ids), dev(d2t), T, want_logits=True)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 200, 255])
+    o = oracle.pruned_head(np_logits(hidden[rows]), np_logits(weight), ids, d2t, T, want_logits=True)
+    assert _head_compare(g, o, hidden, weight, rows, T) <= 1
