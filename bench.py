@@ -566,6 +566,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--no-graph", action="store_true", help="launch every kernel eagerly (no CUDA graph)")
+    ap.add_argument("--head-only", action="store_true",
+                    help="time only the pruned draft LM head (the TLI workload's tensor-core GEMM) and print it")
     ap.add_argument("--no-configs", action="store_true",
                     help="measure only the chosen workload (by default the c3 line also carries c1, c2, c4, c5)")
     args = ap.parse_args()
@@ -587,6 +589,11 @@ def main():
         return
 
     torch.cuda.set_device(local)
+    if args.head_only:
+        from speculative_decoding_draft_select_gb300.build import build
+        build()
+        print(json.dumps(pruned_head_leg()), flush=True)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     line, work, buf = run_ours(args, cfg, mode, rank, world)
@@ -621,8 +628,69 @@ def summarize(line):
     return out
 
 
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def pruned_head_leg(M=256, H=896, K=60000, Vd=151936, Vt=128256, launches=20):
+    """The TLI draft step with the pruned LM head (tli_pruned_head): the
+    hidden states [M, H] of one draft step times the K intersection rows of a
+    synthetic bf16 LM head [K, H] (H = 896, a 0.5B draft model's width), top-1
+    and softmax statistics fused.  Timed per launch with CUDA events, cold
+    (a 512 MB scrub before each launch: the 107.5 MB of weights would
+    otherwise stay in L2) and warm."""
+    import speculative_decoding_draft_select_gb300 as sd
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(1004 * 1009 + 77)
+    hidden = torch.randn((M, H), generator=g, device=dev).to(torch.bfloat16)
+    weight = (torch.randn((K, H), generator=g, device=dev) * (3.0 / H ** 0.5)).to(torch.bfloat16)
+    ids = torch.sort(torch.randperm(Vd, generator=g, device=dev)[:K]).values.to(torch.int32)
+    d2t = torch.full((Vd,), -1, dtype=torch.int32, device=dev)
+    d2t[ids.long()] = torch.randperm(Vt, generator=g, device=dev)[:K].to(torch.int32)
+    out = sd.tli_pruned_head(hidden, weight, ids, d2t, 1.0)
+    ws = torch.empty(max(int(sd.lib().tli_pruned_head_ws_size(M, K)), 256), dtype=torch.uint8, device=dev)
+    scrub = torch.empty(SCRUB_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for mode in ("cold", "warm"):
+        for _ in range(3):
+            sd.tli_pruned_head(hidden, weight, ids, d2t, 1.0, out=out, ws=ws)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+        for a, b in ev:
+            if mode == "cold":
+                scrub.fill_(1)
+            a.record(stream)
+            sd.tli_pruned_head(hidden, weight, ids, d2t, 1.0, out=out, ws=ws)
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        flops = 2.0 * M * K * H
+        byts = (K * H + M * H) * 2
+        tpk, tsrc = tensor_peak()
+        hpk, _ = hbm_peak()
+        res[mode] = {"us": round(us, 2), "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+                     "tensor_frac": round(flops / (us * 1e-6) / 1e12 / tpk, 4),
+                     "gbs": round(byts / (us * 1e-6) / 1e9, 1), "hbm_frac": round(byts / (us * 1e-6) / 1e9 / hpk, 4)}
+    res.update({"workload": f"pruned draft LM head M={M} H={H} K={K} bf16, tcgen05 GEMM + fused top-1 and softmax "
+                            f"statistics (2 launches: GEMM with epilogue, partial merge)",
+                "flops_per_launch": 2 * M * K * H, "bytes_per_launch": (K * H + M * H) * 2,
+                "tensor_peak_tflops": tensor_peak()[0], "tensor_peak_source": tensor_peak()[1]})
+    return res
+
+
 def other_configs(args):
     res = {}
+    try:
+        res["c4_pruned_head"] = pruned_head_leg()
+    except Exception as e:  # reported, not hidden
+        res["c4_pruned_head"] = {"error": f"{type(e).__name__}: {e}"}
+    torch.cuda.empty_cache()
     for name, mode in OTHER_CONFIGS:
         cfg = CONFIGS[name]
         steps = max(3, min(args.steps, 10))

@@ -418,6 +418,23 @@ int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, const void* t
                                int32_t* walk_info_or_null, int32_t* stats_or_null,
                                spec_stream_t stream);
 
+/* Target-side top-k / top-p filtering ([ZS] 5.1: with temperature, top-k or
+ * top-p in force, verification uses the processed target probabilities), in
+ * place on logit rows.  Per row, with p = softmax(row / T) and tokens ordered
+ * by (p desc, index asc) -- the order of the logits: top_k > 0 (and < V)
+ * keeps the first top_k; top_p < 1 then keeps every token whose exclusive
+ * prefix mass is below top_p times the top-k mass (the first token always
+ * stays; top_p <= 0 keeps it alone).  Every other logit is set to -inf, so
+ * softmax of the filtered row is the renormalised filtered p, and
+ * spec_verify_sample / spec_verify_sample_qlogits run on the filtered rows
+ * verify against it.  NaN counts as -inf; rows without a finite maximum are
+ * left as they are (SPEC_STAT_NONFINITE_ROW).  Masses are compared in 2^-40
+ * fixed point (exact sums, a deterministic cut).
+ *   logits [R, V] (dtype), modified in place.  top_k <= 0 and top_p >= 1:
+ *   nothing to do. */
+int spec_filter_logits(void* logits, int dtype, int64_t R, int64_t V, float T, int64_t top_k, float top_p,
+                       int32_t* stats_or_null, spec_stream_t stream);
+
 /* ------------------------------------------------------------- compaction */
 
 /* Capacity (entries) the freed list of spec_compact_slots needs. */

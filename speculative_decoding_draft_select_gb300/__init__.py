@@ -21,7 +21,7 @@ __all__ = [
     "spec_verify_sample_qlogits", "WITHOUT_REPLACEMENT", "CHAIN", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_constrain_map_qlogits", "tli_plan_bytes", "tli_plan_build",
     "tli_map_ids",
-    "tli_check_config", "tli_pruned_head", "spec_wait_probe",
+    "tli_check_config", "tli_pruned_head", "spec_filter_logits", "spec_wait_probe",
     "new_stats", "new_pool",
 ]
 
@@ -79,6 +79,7 @@ _SIGS = {
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
     "spec_wait_probe": (_I, [_P, _I64, _P, _P, _P]),
     "tli_check_config": (_I, [_I, _I, _I]),
+    "spec_filter_logits": (_I, [_P, _I, _I64, _I64, _F, _I64, _F, _P, _P]),
     "tli_pruned_head_ws_size": (_SZ, [_I64, _I64]),
     "tli_pruned_head": (_I, [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
 }
@@ -443,6 +444,19 @@ class SpecIdMap(ctypes.Structure):
     """spec_id_map_t"""
     _fields_ = [("table", ctypes.c_void_p), ("table_len", ctypes.c_int64), ("fallback_id", ctypes.c_int32),
                 ("out", ctypes.c_void_p)]
+
+
+def spec_filter_logits(logits, T, top_k=0, top_p=1.0, stats=None):
+    """Target-side top-k / top-p filtering of logit rows [..., V], in place:
+    logits outside the kept set become -inf (spec_filter_logits).  Returns
+    the same tensor."""
+    _dev(logits, name="logits")
+    _dev(stats, torch.int32, "stats")
+    V = logits.shape[-1]
+    R = logits.numel() // V
+    _call("spec_filter_logits", _ptr(logits), _logit_code(logits), R, V, float(T), int(top_k), float(top_p),
+          _ptr(stats), _stream())
+    return logits
 
 
 # -------------------------------------------------------------- compaction

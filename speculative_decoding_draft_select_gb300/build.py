@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecdec.so")
-SOURCES = ["draft.cu", "tree.cu", "verify.cu", "chain.cu", "compact.cu", "tli.cu", "head.cu"]
+SOURCES = ["draft.cu", "tree.cu", "verify.cu", "chain.cu", "compact.cu", "tli.cu", "head.cu", "filter.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-I", INCLUDE, "-I", CSRC]

@@ -61,8 +61,9 @@ struct ChainParams {
   float* m_row;
   float* z_row;
   // per-request workspace
-  int32_t* cnt;  // [0] next row, [1] first slot with chunks left (a hint), [2] slots reserved, [3] resolved
-  int32_t *state, *done, *slot_req, *slot_ready, *node, *len, *kind, *rows_done, *taken;
+  int32_t* cnt;  // [0] next row, [1] draw items claimed, [2] slots reserved, [3] requests resolved
+  int32_t *state, *done, *slot_req, *slot_ready, *node, *len, *kind, *rows_done;
+  int32_t* front;  // per request: len * 4096 + node of the deepest accepted node seen with every row before it done
   float* A;     // 0: draw from p (bonus), 1: from the residual after one rejection
   float* ctot;  // [B][kMaxChunks] chunk totals of the draw
   int ntiles, tpc, nchunks;
@@ -83,41 +84,39 @@ __device__ __forceinline__ void atom_add_release(int32_t* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// A draw item (slot * nchunks + chunk), or -1 when every chunk of every
-// reserved slot is taken.  Each slot hands out its chunks from its own
-// counter (one atomic add per take, no retries); an exhausted slot moves the
-// shared hint past it.
-__device__ int take_draw(const ChainParams& p) {
-  const int reserved = ld_acquire_gpu(p.cnt + 2);
-  for (int k = ld_volatile(p.cnt + 1); k < reserved; ++k) {
-    const int t = atomicAdd(p.taken + k, 1);
-    if (t < p.nchunks) return k * p.nchunks + t;
-    atomicMax(p.cnt + 1, k + 1);
-  }
-  return -1;
-}
+// Draw items are numbered slot * nchunks + chunk in the order slots are
+// reserved, and claimed with one atomic add on a single counter (no
+// retries).  A claim may run ahead of the reservations; the claimer then
+// holds it until its slot is reserved, or drops it once every request is
+// resolved without that slot.
 
-// Thread 0: walk request b over the published row flags; if every row on
-// its path is done, claim the request, write what the walk committed, and
-// either finish it (a stop without a draw) or queue its draw.
 // The committed id y through the caller's map ([TLI] Modifications,
 // map_target_to_draft_ids: unmapped ids take the fallback id).
 __device__ __forceinline__ int32_t mapped_id(const ChainIO& io, int32_t y) {
   return (y >= 0 && y < io.map_len && __ldg(io.map_table + y) >= 0) ? __ldg(io.map_table + y) : io.map_fallback;
 }
 
-__device__ void try_resolve(const ChainParams& p, int b) {
-  if (ld_acquire_gpu(p.state + b) != 0) return;
+// Returns true when the caller (the CTA that finished row `row_node` of b,
+// allowed by `here_ok`) is to draw the request itself: it resolved here, at
+// that very row.
+__device__ bool try_resolve(const ChainParams& p, int b, int row_node, bool here_ok) {
+  if (ld_acquire_gpu(p.state + b) != 0) return false;
   const ChainIO& io = p.io;
   const int N = p.N;
   const int64_t o = static_cast<int64_t>(b) * N;
   const int rem = io.budget ? __ldg(io.budget + b) : INT_MAX;
-  int n = 0, len = 0, kind = SPEC_FINAL_ACCEPTED, qz = 0, multi = 0;
+  // resume from the deepest accepted node an earlier attempt reached
+  const int fr = ld_volatile(p.front + b);
+  int n = fr & 4095, len = fr >> 12, kind = SPEC_FINAL_ACCEPTED, multi = 0;
   float A = -1.0f;  // no draw
-  if (rem > 0) {
+  if (rem > 0 && !(len > 0 && len >= rem)) {
     for (;;) {
       const int f = ld_acquire_gpu(p.ready + o + n);
-      if (!(f & kRowDone)) return;  // a row on the path is not done: its CTA resolves later
+      if (!(f & kRowDone)) {
+        // a row on the path is not done: its CTA resolves later
+        if (len > (fr >> 12)) atomicMax(p.front + b, len * 4096 + n);
+        return false;
+      }
       multi |= f & kRowMulti;
       if (f & kRowLeaf) {
         A = 0.0f;
@@ -127,7 +126,6 @@ __device__ void try_resolve(const ChainParams& p, int b) {
       // a chain of N nodes reaches its leaf after N - 1 accepted drafts; a
       // longer walk (links that loop) stops here, so every index stays below N
       if (len >= N - 1) break;
-      qz += (f & kRowQZero) ? 1 : 0;
       if (!(f & kRowAccept)) {
         A = 1.0f;
         kind = SPEC_FINAL_CORRECTION;
@@ -140,11 +138,16 @@ __device__ void try_resolve(const ChainParams& p, int b) {
       if (y == io.eos || len == rem) break;
     }
   }
-  if (atomicCAS(p.state + b, 0, 1) != 0) return;  // another CTA resolved it
-  int node = 0;
+  if (atomicCAS(p.state + b, 0, 1) != 0) return false;  // another CTA resolved it
+  // the owner walks the path once more for the outputs and the q[y] = 0
+  // tests on it (the rows on it are done and visible)
+  int node = 0, qz = 0, multi2 = 0;
   io.accept_path[o] = 0;
   for (int i = 0; i < N; ++i) {
     if (i < len) {
+      const int f = ld_acquire_gpu(p.ready + o + node);
+      qz += (f & kRowQZero) ? 1 : 0;
+      multi2 |= f & kRowMulti;
       const int ch = __ldg(io.ntok + o + node);
       const int32_t y = __ldg(io.dtok + o + ch);
       io.committed[o + i] = y;
@@ -157,8 +160,9 @@ __device__ void try_resolve(const ChainParams& p, int b) {
       if (i + 1 < N) io.accept_path[o + i + 1] = -1;
     }
   }
+  if (kind == SPEC_FINAL_CORRECTION && (ld_acquire_gpu(p.ready + o + n) & kRowQZero)) ++qz;  // the rejected test
   if (qz) bump(io.stats, SPEC_STAT_Q_ZERO, qz);
-  if (multi) bump(io.stats, SPEC_STAT_BAD_REQUEST);
+  if (multi | multi2) bump(io.stats, SPEC_STAT_BAD_REQUEST);
   if (A < 0.0f) {
     io.num_committed[b] = len;
     io.accept_length[b] = len;
@@ -169,16 +173,21 @@ __device__ void try_resolve(const ChainParams& p, int b) {
       io.walk_info[3 * b + 2] = SPEC_FINAL_ACCEPTED;
     }
     atom_add_release(p.cnt + 3, 1);
-    return;
+    return false;
   }
   p.node[b] = n;
   p.len[b] = len;
   p.kind[b] = kind;
   p.A[b] = A;
+  if (here_ok && n == row_node) {
+    atom_add_release(p.cnt + 3, 1);  // resolved; this CTA draws it
+    return true;
+  }
   const int k = atomicAdd(p.cnt + 2, 1);  // a draw slot; its items become takeable now
   p.slot_req[k] = b;
   st_release_gpu(p.slot_ready + k, 1);     // publishes node, len, kind, A and the slot
   atom_add_release(p.cnt + 3, 1);          // after the reservation: whoever sees every request resolved sees the slot
+  return false;
 }
 
 template <int DT, class QSrc>
@@ -186,14 +195,16 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
   pdl_enter();
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4, kWarps = kCT / 32;
   using Weights = ResidualWeights<DT, typename QSrc::Row>;
-  extern __shared__ uint4 ring[];  // kRingItems * kCT slots
+  extern __shared__ uint4 ring[];  // kRingItems * kCT slots, then the in-place draw's partials and tile sums
+  float* part = reinterpret_cast<float*>(ring + kRingItems * kCT);
+  float* tsum = part + cdf_part_tiles<kCT, kCE, 1>(p.V) * kCT;
   __shared__ float sw_m[kWarps], sw_s[kWarps];
-  __shared__ float red[kBatch][kWarps];
+  __shared__ float red[kBatch][kWarps];  // tile sums of a chunk pass, by warp
   __shared__ float tile_sh[kMaxChunkTiles];
   __shared__ float ctot_sh[kMaxChunks];
   __shared__ float scan_sh[33];
   __shared__ float s_tot, s_A;
-  __shared__ int s_what, s_item, s_last, s_tok, s_b, s_n;
+  __shared__ int s_what, s_item, s_last, s_tok, s_b, s_n, s_here;
   const ChainIO& io = p.io;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B, N = p.N;
@@ -201,25 +212,46 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
   const float c = p.c;
   long long idle0 = 0;
   bool idle = false;
+  int pend = -1;  // thread 0: a claimed draw item whose slot is not reserved yet
 
   // tile sums of chunk j of a draw row into tile_sh (thread 0), their total
-  // in tile order to every thread
+  // in tile order to every thread.  Each thread copies its elements of D
+  // tiles at once into its slots of the copy ring (D = what the ring holds
+  // at this operand width), then sums them; rows that are not 16-byte
+  // aligned take direct loads.
+  constexpr int K = Weights::template chunks<kCE>();
+  constexpr int D = kRingItems / K < 1 ? 1 : (kRingItems / K > kBatch ? kBatch : kRingItems / K);
   auto chunk_pass = [&](const Weights& w, int j) -> float {
     const int t0 = j * p.tpc, t1 = min(p.ntiles, t0 + p.tpc);
+    const bool rg = w.ring_ok();
+    uint4* mine = ring + tid;
     float tot = 0.0f;
-    for (int t = t0; t < t1; t += kBatch) {
-      float ps[kBatch];
+    for (int t = t0; t < t1; t += D) {
+      float ps[D];
+      if (rg) {
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        ps[u] = t + u < t1 ? w.template load_sum<kCE>(static_cast<int64_t>(t + u) * kTile + tid * kCE) : 0.0f;
+        for (int u = 0; u < D; ++u)
+          if (t + u < t1) w.template issue<kCE>(mine + u * K * kCT, kCT, static_cast<int64_t>(t + u) * kTile + tid * kCE);
+        cp_async_commit();
+        cp_async_wait<0>();
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < D; ++u)
+          ps[u] = t + u < t1 ? w.template ring_sum<kCE>(mine + u * K * kCT, kCT,
+                                                         static_cast<int64_t>(t + u) * kTile + tid * kCE)
+                             : 0.0f;
+      } else {
+#pragma unroll
+        for (int u = 0; u < D; ++u)
+          ps[u] = t + u < t1 ? w.template load_sum<kCE>(static_cast<int64_t>(t + u) * kTile + tid * kCE) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < D; ++u) {
         const float s = warp_sum(ps[u]);
         if (lane == 0) red[u][warp] = s;
       }
       __syncthreads();
       if (tid == 0) {
-        for (int u = 0; u < kBatch && t + u < t1; ++u) {
+        for (int u = 0; u < D && t + u < t1; ++u) {
           float ts = 0.0f;
 #pragma unroll
           for (int w2 = 0; w2 < kWarps; ++w2) ts += red[u][w2];
@@ -259,24 +291,116 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     __syncthreads();
   };
 
+  // the last outputs of request b, drawn token tok at node n (thread 0)
+  auto write_draw = [&](int b, int n, int tok) {
+    const int64_t o = static_cast<int64_t>(b) * N;
+    const int len = __ldcg(p.len + b), kind = __ldcg(p.kind + b);
+    io.committed[o + len] = tok;
+    if (io.committed_mapped) io.committed_mapped[o + len] = mapped_id(io, tok);
+    io.num_committed[b] = len + 1;
+    io.accept_length[b] = len;
+    io.next_root[b] = tok;
+    if (io.walk_info) {
+      io.walk_info[3 * b] = n;
+      io.walk_info[3 * b + 1] = kind == SPEC_FINAL_CORRECTION ? 1 : 0;
+      io.walk_info[3 * b + 2] = kind;
+    }
+  };
+
+  // the inverse-CDF draw of request b at node n from the chunk totals in
+  // ctot_sh (every CTA takes the same operations in the same order), then
+  // the request's last outputs
+  auto finish_draw = [&](int b, int n, Weights w) {
+    if (tid == 0) s_tok = INT_MAX;
+    __syncthreads();
+    float W = 0.0f;
+    for (int q = 0; q < p.nchunks; ++q) W += ctot_sh[q];
+    if (w.A != 0.0f && !(W > 0.0f && isfinite(W))) {
+      // no residual mass: the draw is from p itself (counted)
+      if (tid == 0) bump(io.stats, SPEC_STAT_RESIDUAL_FALLBACK);
+      w.A = 0.0f;
+      for (int q = 0; q < p.nchunks; ++q) {
+        const float t = chunk_pass(w, q);
+        if (tid == 0) ctot_sh[q] = t;
+      }
+      __syncthreads();
+      W = 0.0f;
+      for (int q = 0; q < p.nchunks; ++q) W += ctot_sh[q];
+    }
+    const float target = __ldg(io.u_final + b) * W;
+    if (W > 0.0f && isfinite(W)) {
+      float prefix = 0.0f;
+      for (int q = 0; q < p.nchunks; ++q) {
+        const float after = prefix + ctot_sh[q];
+        if (!(after > target)) {
+          prefix = after;
+          continue;
+        }
+        chunk_pass(w, q);  // the chunk's tile sums again, as its pass made them
+        const int t0 = q * p.tpc, nt = min(p.ntiles, t0 + p.tpc) - t0;
+        for (int i = 0; i < nt; ++i) {
+          const float a2 = prefix + tile_sh[i];
+          if (a2 > target) {
+            rescan_tile(w, t0 + i, prefix, target);
+            if (s_tok != INT_MAX) break;
+          }
+          prefix = a2;
+        }
+        if (s_tok != INT_MAX) break;
+      }
+    }
+    __syncthreads();
+    if (s_tok == INT_MAX) {
+      // rounding left no crossing (or no mass): the last index of positive weight
+      __syncthreads();
+      if (tid == 0) s_tok = -1;
+      __syncthreads();
+      for (int64_t v = tid; v < V; v += kCT)
+        if (w.at(v) > 0.0f) atomicMax(&s_tok, static_cast<int>(v));
+      __syncthreads();
+      if (tid == 0) {
+        if (s_tok < 0) s_tok = 0;
+        bump(io.stats, SPEC_STAT_CDF_FALLBACK);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) write_draw(b, n, s_tok);
+    __syncthreads();
+  };
+
+  // the weights a request's draw reads: the residual at a rejected node
+  // (A = 1), or p at a leaf (A = 0)
+  auto draw_weights = [&](int b, int n, float A) -> Weights {
+    const int64_t rr = static_cast<int64_t>(b) * N + n;
+    const void* row = static_cast<const char*>(p.target) + rr * V * esz;
+    const float m = __ldcg(p.m_row + rr), z = __ldcg(p.z_row + rr);
+    const auto qrow = qsrc.row(A != 0.0f ? (io.q_row ? static_cast<int64_t>(__ldg(io.q_row + rr)) : rr) : -1);
+    return Weights{row, qrow, V, c, folded_offset(m, c, z), A};
+  };
+
   for (;;) {
     if (tid == 0) {
+      // rows first: the batched pass is the critical path; then draw items
       int what = 3, item = 0;
-      // read before the draw queue: if every request was resolved by then,
-      // an empty queue means every draw item is taken
-      const bool all_resolved = ld_acquire_gpu(p.cnt + 3) >= B;
-      const int it = take_draw(p);
-      if (it >= 0) {
-        what = 1;
-        item = it;
+      const int r = ld_volatile(p.cnt) < rows ? atomicAdd(p.cnt, 1) : static_cast<int>(rows);
+      if (r < rows) {
+        what = 2;
+        item = r;
       } else {
-        const int r = ld_volatile(p.cnt) < rows ? atomicAdd(p.cnt, 1) : static_cast<int>(rows);
-        if (r < rows) {
-          what = 2;
-          item = r;
+        // read first: if every request was resolved by then, the reserved
+        // slots are final
+        const bool all_resolved = ld_acquire_gpu(p.cnt + 3) >= B;
+        const int reserved = ld_acquire_gpu(p.cnt + 2);
+        if (pend < 0 && ld_volatile(p.cnt + 1) < reserved * p.nchunks) pend = atomicAdd(p.cnt + 1, 1);
+        if (pend >= 0 && pend / p.nchunks < reserved) {
+          what = 1;
+          item = pend;
+          pend = -1;
         } else if (all_resolved) {
-          what = 0;
-        } else {
+          pend = -1;  // its slot will never be reserved
+          if (ld_volatile(p.cnt + 1) >= reserved * p.nchunks) what = 0;
+        }
+        if (what == 3) {
           // nothing to take yet: rows or resolutions are in flight on
           // running CTAs, which never wait; bounded all the same
           if (!idle) {
@@ -364,9 +488,28 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
         // the request's rows are counted on one word: of two CTAs finishing
         // rows of request b, the one counting later sees the other's flag
         atom_add_acq_rel(p.rows_done + b, 1);
-        try_resolve(p, b);
+        // while many rows remain, a request resolved at this very row is
+        // drawn here at once (its target row is still in L2); near the end of
+        // the batched pass its draw is cut into chunks for every CTA
+        const bool here_ok = rows - ld_volatile(p.cnt) >= 2 * static_cast<int64_t>(gridDim.x);
+        s_here = try_resolve(p, b, n, here_ok) ? 1 : 0;
+        if (s_here) s_A = __ldcg(p.A + b);
       }
       __syncthreads();  // sw_* reused by the next row
+      if (s_here) {
+        // the tree walk's own pass and draw (one CTA): the row streamed
+        // through the copy ring, tile sums in tile order, then the search
+        Weights w = draw_weights(b, n, s_A);
+        float total = cdf_tile_pass_split<kCT, kCE, walk_ring_depth(K), 1>(w, V, part, tsum, ring, 0u);
+        if (w.A != 0.0f && !(total > 0.0f && isfinite(total))) {
+          if (tid == 0) bump(io.stats, SPEC_STAT_RESIDUAL_FALLBACK);
+          w.A = 0.0f;
+          total = cdf_tile_pass_split<kCT, kCE, walk_ring_depth(K), 1>(w, V, part, tsum, ring, 0u);
+        }
+        const int32_t tok = cdf_search<kCT, Weights, kCE>(w, V, __ldg(io.u_final + b), tsum, total, scan_sh, io.stats);
+        if (tid == 0) write_draw(b, n, tok);
+        __syncthreads();
+      }
       continue;
     }
 
@@ -384,12 +527,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     __syncthreads();
     if (s_b < 0) continue;
     const int b = s_b, n = s_n, j = item % p.nchunks;
-    const float A = s_A;
-    const int64_t o = static_cast<int64_t>(b) * N, rr = o + n;
-    const void* row = static_cast<const char*>(p.target) + rr * V * esz;
-    const float m = __ldcg(p.m_row + rr), z = __ldcg(p.z_row + rr);
-    const auto qrow = qsrc.row(A != 0.0f ? (io.q_row ? static_cast<int64_t>(__ldg(io.q_row + rr)) : rr) : -1);
-    Weights w{row, qrow, V, c, folded_offset(m, c, z), A};
+    const Weights w = draw_weights(b, n, s_A);
     const float tot = chunk_pass(w, j);
     if (tid == 0) {
       p.ctot[static_cast<int64_t>(b) * kMaxChunks + j] = tot;
@@ -400,73 +538,8 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     if (!s_last) continue;
     // the last chunk of request b: the inverse-CDF draw
     if (tid < p.nchunks) ctot_sh[tid] = __ldcg(p.ctot + static_cast<int64_t>(b) * kMaxChunks + tid);
-    if (tid == 0) s_tok = INT_MAX;
     __syncthreads();
-    float W = 0.0f;
-    for (int q = 0; q < p.nchunks; ++q) W += ctot_sh[q];
-    if (w.A != 0.0f && !(W > 0.0f && isfinite(W))) {
-      // no residual mass: the draw is from p itself (counted)
-      if (tid == 0) bump(io.stats, SPEC_STAT_RESIDUAL_FALLBACK);
-      w.A = 0.0f;
-      for (int q = 0; q < p.nchunks; ++q) {
-        const float t = chunk_pass(w, q);
-        if (tid == 0) ctot_sh[q] = t;
-      }
-      __syncthreads();
-      W = 0.0f;
-      for (int q = 0; q < p.nchunks; ++q) W += ctot_sh[q];
-    }
-    const float target = __ldg(io.u_final + b) * W;
-    if (W > 0.0f && isfinite(W)) {
-      float prefix = 0.0f;
-      for (int q = 0; q < p.nchunks; ++q) {
-        const float after = prefix + ctot_sh[q];
-        if (!(after > target)) {
-          prefix = after;
-          continue;
-        }
-        chunk_pass(w, q);  // the chunk's tile sums again, as its item made them
-        const int t0 = q * p.tpc, nt = min(p.ntiles, t0 + p.tpc) - t0;
-        for (int i = 0; i < nt; ++i) {
-          const float a2 = prefix + tile_sh[i];
-          if (a2 > target) {
-            rescan_tile(w, t0 + i, prefix, target);
-            if (s_tok != INT_MAX) break;
-          }
-          prefix = a2;
-        }
-        if (s_tok != INT_MAX) break;
-      }
-    }
-    __syncthreads();
-    if (s_tok == INT_MAX) {
-      // rounding left no crossing (or no mass): the last index of positive weight
-      __syncthreads();
-      if (tid == 0) s_tok = -1;
-      __syncthreads();
-      for (int64_t v = tid; v < V; v += kCT)
-        if (w.at(v) > 0.0f) atomicMax(&s_tok, static_cast<int>(v));
-      __syncthreads();
-      if (tid == 0) {
-        if (s_tok < 0) s_tok = 0;
-        bump(io.stats, SPEC_STAT_CDF_FALLBACK);
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const int tok = s_tok, len = __ldcg(p.len + b), kind = __ldcg(p.kind + b);
-      io.committed[o + len] = tok;
-      if (io.committed_mapped) io.committed_mapped[o + len] = mapped_id(io, tok);
-      io.num_committed[b] = len + 1;
-      io.accept_length[b] = len;
-      io.next_root[b] = tok;
-      if (io.walk_info) {
-        io.walk_info[3 * b] = n;
-        io.walk_info[3 * b + 1] = kind == SPEC_FINAL_CORRECTION ? 1 : 0;
-        io.walk_info[3 * b + 2] = kind;
-      }
-    }
-    __syncthreads();
+    finish_draw(b, n, w);
   }
 }
 
@@ -492,7 +565,11 @@ ReqWs carve_req(void* ws, int B) {
 template <int DT, class QSrc>
 int launch_chain(ChainParams& p, const QSrc& qsrc, cudaStream_t s) {
   auto kernel = chain_verify_kernel<DT, QSrc>;
-  const size_t smem = sizeof(uint4) * kRingItems * kCT;
+  const size_t smem = sizeof(uint4) * kRingItems * kCT +
+                      sizeof(float) * (static_cast<size_t>(cdf_part_tiles<kCT, kCE, 1>(p.V)) * kCT + p.ntiles);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   int dev = 0, sms = 0, per = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                  cudaSuccess ||
@@ -540,7 +617,7 @@ int chain_verify(int dtype, int B, int N, int64_t V, const void* target, float c
   p.len = p.node + B;
   p.kind = p.len + B;
   p.rows_done = p.kind + B;
-  p.taken = p.rows_done + B;
+  p.front = p.rows_done + B;
   p.A = r.A;
   p.ctot = r.ctot;
   const int64_t ntiles = (V + kTile - 1) / kTile;

@@ -38,7 +38,9 @@
 namespace specdec {
 namespace {
 
-constexpr int kHeadThreads = 256;
+constexpr int kHeadThreads = 384;  // warps: 0 TMA, 1 MMA, 2 tensor memory, 3 idle, 4-11 epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kSubRows = 16;  // rows of the boxes a trimmed tile is loaded in
 constexpr int kBM = 128;  // rows of an accumulator (hidden rows)
 constexpr int kBN = 128;  // weight rows of a tile
 constexpr int kBK = 64;   // H columns per stage: 128 bytes, one swizzle row
@@ -46,7 +48,7 @@ constexpr int kStages = 4;
 constexpr int kSlab = kBM * kBK * 2;  // bytes of one 128-row slab (16 KB)
 constexpr int kStageBytes = 3 * kSlab;
 constexpr int kUmmaK = 16;  // K of one bf16 MMA instruction (32 bytes)
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;  // two buffers x two 128-row halves x 128 columns
 constexpr size_t kHeadSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;  // + alignment slack
 constexpr long long kHeadWaitCycles = 20000000LL;  // about 10 ms at 2 GHz
 
@@ -114,15 +116,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // operands K-major, no negation: D format (bits 4-5) 1 = fp32, A and B
 // formats (bits 7-9, 10-12) 1 = bf16, N >> 3 (bits 17-22), M >> 4 (bits
 // 24-28).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+// (N is added per tile: the rows of a trimmed last tile.)
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBM >> 4) << 24);
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -144,32 +147,52 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Persistent: CTA i owns weight rows [i R, min(K, (i + 1) R)), R a multiple
+// of 16 chosen so that every SM gets one slice (the MMA work is balanced),
+// processed in tiles of up to 128 rows; a trimmed last tile (a multiple of 16
+// rows) is loaded in 16-row boxes and multiplied with N = its rows.  The two
+// accumulator buffers in tensor memory (columns [0, 256) and [256, 512), each
+// two 128-row halves of 128 columns) let the epilogue of tile t run while the
+// MMAs of tile t + 1 fill the other buffer ("tmem full" / "tmem empty"
+// mbarriers).  The epilogue is 8 warps: warp 4 + e reads the lane quarter e %
+// 4 and the columns [64 (e / 4), 64 (e / 4) + 64) of the tile, and writes
+// one partial per (row, tile, column half); slots without columns get the
+// neutral partial, so the merge reads every slot.
 __global__ void __launch_bounds__(kHeadThreads, 1)
-    pruned_head_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_constant__ CUtensorMap tm_weight,
-                       int M, int K, int H, float c, int ntiles, float4* __restrict__ partial,
-                       float* __restrict__ logits, int32_t* __restrict__ stats) {
+    pruned_head_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_constant__ CUtensorMap tm_w128,
+                       const __grid_constant__ CUtensorMap tm_w16, int M, int K, int H, float c, int rows_per_cta,
+                       int tiles_per_cta, float4* __restrict__ partial, float* __restrict__ logits,
+                       int32_t* __restrict__ stats) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   // stage s: hidden rows [0, 128) at s * kStageBytes, rows [128, 256) after
   // it, the weight slab last; every slab 1024-byte aligned (swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], acc_bar;
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_consumed;
+  __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, n0 = tile * kBN;
+  const int r0 = blockIdx.x * rows_per_cta, r1 = min(K, r0 + rows_per_cta);
+  const int ntile = r1 > r0 ? (r1 - r0 + kBN - 1) / kBN : 0;
   const int m_base = blockIdx.y * 2 * kBM;
   const int nM = M - m_base > kBM ? 2 : 1;
   const int nkb = (H + kBK - 1) / kBK;
+  const int nslots = gridDim.x * 2;  // one partial per (row, CTA, column half)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&acc_bar, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&tfull_bar[j], 1);
+      mbar_init(&tempty_bar[j], kEpiWarps);
+    }
     s_abort = 0;
-    s_consumed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 2) {
@@ -184,100 +207,134 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0 && lane == 0) {
-    // producer
-    int issued = 0;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t it = static_cast<uint32_t>(kb / kStages);
-      if (!mbar_wait(&empty_bar[s], (it & 1u) ^ 1u, kHeadWaitCycles)) {
-        atomicExch(&s_abort, 1);
-        break;
+    // producer: the stage ring runs on across the tiles
+    int g = 0, issued = 0, consumed_hint = 0;
+    for (int t = 0; t < ntile && !*reinterpret_cast<volatile int*>(&s_abort); ++t) {
+      const int n0 = r0 + t * kBN, nr16 = (min(kBN, r1 - n0) + 15) & ~15;
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait(&empty_bar[s], (static_cast<uint32_t>(g / kStages) & 1u) ^ 1u, kHeadWaitCycles)) {
+          atomicExch(&s_abort, 1);
+          break;
+        }
+        consumed_hint = g - kStages + 1;
+        uint8_t* st = smem + static_cast<size_t>(s) * kStageBytes;
+        mbar_expect_tx(&full_bar[s], static_cast<uint32_t>(nM * kSlab + nr16 * kBK * 2));
+        tma_load_2d(st, &tm_hidden, &full_bar[s], kb * kBK, m_base);
+        if (nM == 2) tma_load_2d(st + kSlab, &tm_hidden, &full_bar[s], kb * kBK, m_base + kBM);
+        if (nr16 == kBN) {
+          tma_load_2d(st + 2 * kSlab, &tm_w128, &full_bar[s], kb * kBK, n0);
+        } else {
+          for (int i = 0; i < nr16 / kSubRows; ++i)
+            tma_load_2d(st + 2 * kSlab + i * kSubRows * kBK * 2, &tm_w16, &full_bar[s], kb * kBK, n0 + i * kSubRows);
+        }
+        issued = g + 1;
       }
-      uint8_t* st = smem + static_cast<size_t>(s) * kStageBytes;
-      mbar_expect_tx(&full_bar[s], static_cast<uint32_t>((nM + 1) * kSlab));
-      tma_load_2d(st, &tm_hidden, &full_bar[s], kb * kBK, m_base);
-      if (nM == 2) tma_load_2d(st + kSlab, &tm_hidden, &full_bar[s], kb * kBK, m_base + kBM);
-      tma_load_2d(st + 2 * kSlab, &tm_weight, &full_bar[s], kb * kBK, n0);
-      issued = kb + 1;
     }
-    // after an abort: copies issued but never consumed land before exit
+    // after an abort: copies issued but possibly never consumed land before exit
     if (*reinterpret_cast<volatile int*>(&s_abort))
-      for (int kb = *reinterpret_cast<volatile int*>(&s_consumed); kb < issued; ++kb)
-        mbar_wait(&full_bar[kb % kStages], static_cast<uint32_t>(kb / kStages) & 1u, kHeadWaitCycles);
+      for (int q = consumed_hint > 0 ? consumed_hint : 0; q < issued; ++q)
+        mbar_wait(&full_bar[q % kStages], static_cast<uint32_t>(q / kStages) & 1u, kHeadWaitCycles);
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % kStages;
-      if (*reinterpret_cast<volatile int*>(&s_abort) ||
-          !mbar_wait(&full_bar[s], static_cast<uint32_t>(kb / kStages) & 1u, kHeadWaitCycles)) {
+    int g = 0;
+    for (int t = 0; t < ntile && !*reinterpret_cast<volatile int*>(&s_abort); ++t) {
+      const int j = t & 1;
+      const int n0 = r0 + t * kBN, nr16 = (min(kBN, r1 - n0) + 15) & ~15;
+      if (!mbar_wait(&tempty_bar[j], (static_cast<uint32_t>(t >> 1) & 1u) ^ 1u, kHeadWaitCycles)) {
         atomicExch(&s_abort, 1);
         break;
       }
       tc_fence_after();
-      const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * kStageBytes);
+      const uint32_t idesc = kIdescBase | (static_cast<uint32_t>(nr16 >> 3) << 17);
+      const uint32_t acc0 = tmem + static_cast<uint32_t>(j * 2 * kBN);
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait(&full_bar[s], static_cast<uint32_t>(g / kStages) & 1u, kHeadWaitCycles)) {
+          atomicExch(&s_abort, 1);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * kStageBytes);
 #pragma unroll
-      for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-        const uint64_t bdesc = sw128_desc(st + 2 * kSlab + kk * kUmmaK * 2);
-        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-        tc_mma(tmem, sw128_desc(st + kk * kUmmaK * 2), bdesc, acc);
-        if (nM == 2) tc_mma(tmem + kBN, sw128_desc(st + kSlab + kk * kUmmaK * 2), bdesc, acc);
+        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+          const uint64_t bdesc = sw128_desc(st + 2 * kSlab + kk * kUmmaK * 2);
+          const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+          tc_mma(acc0, sw128_desc(st + kk * kUmmaK * 2), bdesc, idesc, acc);
+          if (nM == 2) tc_mma(acc0 + kBN, sw128_desc(st + kSlab + kk * kUmmaK * 2), bdesc, idesc, acc);
+        }
+        tc_commit(&empty_bar[s]);  // the stage is free once these MMAs have read it
       }
-      tc_commit(&empty_bar[s]);  // the stage is free once these MMAs have read it
-      *reinterpret_cast<volatile int*>(&s_consumed) = kb + 1;
+      tc_commit(&tfull_bar[j]);  // buffer j holds tile t
     }
-    tc_commit(&acc_bar);  // the accumulators are complete
   } else if (warp >= 4) {
-    // epilogue: warp 4 + q reads tensor-memory lanes [32 q, 32 q + 32)
-    const int q = warp & 3;
-    const bool ok = mbar_wait(&acc_bar, 0u, kHeadWaitCycles) && !*reinterpret_cast<volatile int*>(&s_abort);
-    tc_fence_after();
-    if (!ok) {
-      atomicExch(&s_abort, 1);
-    } else {
-      for (int h = 0; h < nM; ++h) {
+    // epilogue: each thread keeps its rows' partials over the CTA's tiles and
+    // writes them once
+    const int e = warp - 4, q = warp & 3, grp = e >> 2;
+    const int slot = blockIdx.x * 2 + grp;
+    float mx[2] = {neg_inf(), neg_inf()}, sum[2] = {0.0f, 0.0f}, bv[2] = {neg_inf(), neg_inf()};
+    int bi[2] = {INT_MAX, INT_MAX};
+    for (int t = 0; t < ntile; ++t) {
+      const int n0 = r0 + t * kBN, nr = min(kBN, r1 - n0);
+      const int c_begin = grp * 64, c_end = min(nr, c_begin + 64);
+      const int j = t & 1;
+      bool ok = mbar_wait(&tfull_bar[j], static_cast<uint32_t>(t >> 1) & 1u, kHeadWaitCycles) &&
+                !*reinterpret_cast<volatile int*>(&s_abort);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-wide: the whole warp reads or none
+      if (!ok && lane == 0) atomicExch(&s_abort, 1);
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (h >= nM || !ok) continue;
         const int row = m_base + h * kBM + q * 32 + lane;
-        float mx = neg_inf(), sum = 0.0f, bv = neg_inf();
-        int bi = INT_MAX;
 #pragma unroll 1
-        for (int cb = 0; cb < kBN / 16; ++cb) {
+        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
           uint32_t r[16];
-          tc_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * kBN + cb * 16), r);
-          const int col0 = n0 + cb * 16;
+          tc_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * 2 * kBN + h * kBN + c0), r);
+          const int col0 = n0 + c0;
           float x[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = col0 + j < K ? order_key(__uint_as_float(r[j])) : neg_inf();
+          for (int jj = 0; jj < 16; ++jj) x[jj] = c0 + jj < c_end ? order_key(__uint_as_float(r[jj])) : neg_inf();
           if (logits != nullptr && row < M) {
             float* out = logits + static_cast<int64_t>(row) * K + col0;
-            if (col0 + 16 <= K && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+            if (c0 + 16 <= c_end && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
 #pragma unroll
-              for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(out + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                                  __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+              for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(out + jj) =
+                    make_float4(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1]), __uint_as_float(r[jj + 2]),
+                                __uint_as_float(r[jj + 3]));
             } else {
-              for (int j = 0; j < 16 && col0 + j < K; ++j) out[j] = __uint_as_float(r[j]);
+              for (int jj = 0; jj < 16 && c0 + jj < c_end; ++jj) out[jj] = __uint_as_float(r[jj]);
             }
           }
           float cm = neg_inf();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            cm = fmaxf(cm, x[j]);
-            if (x[j] > bv) {  // columns in increasing order: the first largest stays
-              bv = x[j];
-              bi = col0 + j;
+          for (int jj = 0; jj < 16; ++jj) {
+            cm = fmaxf(cm, x[jj]);
+            if (x[jj] > bv[h]) {  // columns in increasing order: the first largest stays
+              bv[h] = x[jj];
+              bi[h] = col0 + jj;
             }
           }
-          if (cm > mx) {
-            sum = mx == neg_inf() ? 0.0f : sum * fast_exp2((mx - cm) * c);
-            mx = cm;
+          if (cm > mx[h]) {
+            sum[h] = mx[h] == neg_inf() ? 0.0f : sum[h] * fast_exp2((mx[h] - cm) * c);
+            mx[h] = cm;
           }
-          if (mx != neg_inf()) {
-            const float mc = mx * c;
+          if (mx[h] != neg_inf()) {
+            const float mc = mx[h] * c;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) sum += fast_exp2(fmaf(x[j], c, -mc));
+            for (int jj = 0; jj < 16; ++jj) sum[h] += fast_exp2(fmaf(x[jj], c, -mc));
           }
         }
-        if (row < M) partial[static_cast<int64_t>(row) * ntiles + tile] = make_float4(mx, sum, bv, __int_as_float(bi));
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[j]);  // buffer j may be refilled
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = m_base + h * kBM + q * 32 + lane;
+      if (h < nM && row < M) partial[static_cast<int64_t>(row) * nslots + slot] = make_float4(mx[h], sum[h], bv[h], __int_as_float(bi[h]));
     }
   }
   tc_fence_before();
@@ -289,24 +346,26 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   if (threadIdx.x == 0 && s_abort) bump(stats, SPEC_STAT_WAIT_TIMEOUT);
 }
 
-// One warp per row: the row's tile partials merged in tile order (lanes
-// take tiles lane, lane + 32, ...; then a fixed butterfly), then its top-1
-// mapped to draft and target ids.
+// One CTA per row: the row's partials merged in slot order (thread t takes
+// slots t, t + 256, ...; then warps, then the CTA, in fixed orders), then
+// its top-1 mapped to draft and target ids.
 constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads)
-    head_merge_kernel(int M, int ntiles, float c, const float4* __restrict__ partial, const int32_t* __restrict__ ids,
+    head_merge_kernel(int M, int nslots, float c, const float4* __restrict__ partial, const int32_t* __restrict__ ids,
                       const int32_t* __restrict__ d2t, int64_t Vd, int32_t* __restrict__ top1_rank,
                       int32_t* __restrict__ top1_draft, int32_t* __restrict__ top1_target, float* __restrict__ top1_p,
                       float* __restrict__ row_stats, int32_t* __restrict__ stats) {
   pdl_enter();
+  constexpr int kWarps = kMergeThreads / 32;
+  __shared__ float sm[kWarps], ss[kWarps], sv[kWarps];
+  __shared__ int si[kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (kMergeThreads / 32) + warp;
-  if (row >= M) return;
+  const int row = blockIdx.x;
   float m = neg_inf(), s = 0.0f, bv = neg_inf();
   int bi = INT_MAX;
-  for (int t = lane; t < ntiles; t += 32) {
-    const float4 p = partial[static_cast<int64_t>(row) * ntiles + t];
+  for (int t = threadIdx.x; t < nslots; t += kMergeThreads) {
+    const float4 p = __ldg(partial + static_cast<int64_t>(row) * nslots + t);
     merge_ms(m, s, p.x, p.y, c);
     const int pi = __float_as_int(p.w);
     if (before(p.z, pi, bv, bi)) {
@@ -316,7 +375,25 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
   warp_merge_ms(m, s, c);
   warp_best(bv, bi);
-  if (lane != 0) return;
+  if (lane == 0) {
+    sm[warp] = m;
+    ss[warp] = s;
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  m = sm[0];
+  s = ss[0];
+  bv = sv[0];
+  bi = si[0];
+  for (int w = 1; w < kWarps; ++w) {
+    merge_ms(m, s, sm[w], ss[w], c);
+    if (before(sv[w], si[w], bv, bi)) {
+      bv = sv[w];
+      bi = si[w];
+    }
+  }
   const bool finite = isfinite(m) && bi != INT_MAX;
   if (!finite) bump(stats, SPEC_STAT_EMPTY_INTERSECTION);
   const int32_t d = finite ? __ldg(ids + bi) : -1;
@@ -349,18 +426,39 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// Tensor map of a row-major bf16 matrix [rows, cols]: boxes of 128 rows x
-// 64 columns (128 bytes), 128-byte swizzle, zero fill out of bounds.
-bool bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+// Tensor map of a row-major bf16 matrix [rows, cols]: boxes of box_rows
+// rows x 64 columns (128 bytes), 128-byte swizzle, zero fill out of bounds.
+bool bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
   const EncodeTiledFn fn = encode_tiled();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The split of the K weight rows over the CTAs: one slice of R rows (a
+// multiple of 16) per SM of the current device.
+struct HeadSplit {
+  int rows_per_cta, grid, tiles_per_cta, nslots;
+};
+
+bool head_split(int64_t K, HeadSplit& h) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess || sms < 1) {
+    cudaGetLastError();
+    return false;
+  }
+  const int64_t per = ((K + sms - 1) / sms + kSubRows - 1) / kSubRows * kSubRows;
+  h.rows_per_cta = static_cast<int>(per);
+  h.grid = static_cast<int>((K + per - 1) / per);
+  h.tiles_per_cta = static_cast<int>((per + kBN - 1) / kBN);
+  h.nslots = h.grid * 2;
+  return true;
 }
 
 }  // namespace
@@ -369,9 +467,9 @@ bool bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
 using namespace specdec;
 
 extern "C" size_t tli_pruned_head_ws_size(int64_t M, int64_t K) {
-  if (M < 0 || K < 1) return 0;
-  const int64_t ntiles = (K + kBN - 1) / kBN;
-  return align256(static_cast<size_t>(M) * static_cast<size_t>(ntiles) * sizeof(float4));
+  HeadSplit h;
+  if (M < 0 || K < 1 || !head_split(K, h)) return 0;
+  return align256(static_cast<size_t>(M) * static_cast<size_t>(h.nslots) * sizeof(float4));
 }
 
 extern "C" int tli_pruned_head(int64_t M, int64_t H, int64_t K, const void* hidden, const void* weight,
@@ -388,22 +486,25 @@ extern "C" int tli_pruned_head(int64_t M, int64_t H, int64_t K, const void* hidd
     return SPEC_ERR_UNSUPPORTED;
   if (K > INT_MAX - kBN || H > INT_MAX || M > 65535LL * 2 * kBM) return SPEC_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return SPEC_ERR_INVALID_ARG;
-  if (ws_bytes < tli_pruned_head_ws_size(M, K)) return SPEC_ERR_WORKSPACE;
-  CUtensorMap tm_h, tm_w;
-  if (!bf16_map(&tm_h, hidden, M, H) || !bf16_map(&tm_w, weight, K, H)) return SPEC_ERR_CUDA;
+  HeadSplit hs;
+  if (!head_split(K, hs)) return SPEC_ERR_CUDA;
+  if (ws_bytes < static_cast<size_t>(M) * static_cast<size_t>(hs.nslots) * sizeof(float4)) return SPEC_ERR_WORKSPACE;
+  CUtensorMap tm_h, tm_w128, tm_w16;
+  if (!bf16_map(&tm_h, hidden, M, H, kBM) || !bf16_map(&tm_w128, weight, K, H, kBN) ||
+      !bf16_map(&tm_w16, weight, K, H, kSubRows))
+    return SPEC_ERR_CUDA;
   static const bool smem_ok =
       cudaFuncSetAttribute(pruned_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kHeadSmem)) == cudaSuccess;
   if (!smem_ok) return SPEC_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int ntiles = static_cast<int>((K + kBN - 1) / kBN);
   const float c = kLog2e / T;
   float4* partial = static_cast<float4*>(ws);
-  launch_k(pruned_head_kernel, dim3(ntiles, static_cast<unsigned>((M + 2 * kBM - 1) / (2 * kBM))), kHeadThreads,
-           kHeadSmem, s, tm_h, tm_w, static_cast<int>(M), static_cast<int>(K), static_cast<int>(H), c, ntiles,
-           partial, logits_or_null, stats_or_null);
+  launch_k(pruned_head_kernel, dim3(hs.grid, static_cast<unsigned>((M + 2 * kBM - 1) / (2 * kBM))), kHeadThreads,
+           kHeadSmem, s, tm_h, tm_w128, tm_w16, static_cast<int>(M), static_cast<int>(K), static_cast<int>(H), c,
+           hs.rows_per_cta, hs.tiles_per_cta, partial, logits_or_null, stats_or_null);
   if (launch_status() != SPEC_OK) return SPEC_ERR_CUDA;
-  launch_k(head_merge_kernel, static_cast<unsigned>((M + 7) / 8), kMergeThreads, 0, s, static_cast<int>(M), ntiles,
+  launch_k(head_merge_kernel, static_cast<unsigned>(M), kMergeThreads, 0, s, static_cast<int>(M), hs.nslots,
            c, static_cast<const float4*>(partial), ids, d2t, V_d, top1_rank_or_null, top1_draft, top1_target, top1_p,
            row_stats_or_null, stats_or_null);
   return launch_status();

@@ -1272,3 +1272,95 @@ def test_pruned_head_full_size_sampled_rows():
     rows = np.array([0, 1, 127, 128, 200, 255])
     o = oracle.pruned_head(np_logits(hidden[rows]), np_logits(weight), ids, d2t, T, want_logits=True)
     assert _head_compare(g, o, hidden, weight, rows, T) <= 1
+
+
+# ------------------------------------------------- target-side filtering
+
+FILTERS = [(1, 1.0), (5, 1.0), (0, 0.9), (20, 0.8), (0, 0.0), (3, 0.5), (0, 0.3)]
+
+
+@pytest.mark.parametrize("V,dtype", [(257, torch.float32), (4097, torch.bfloat16), (32000, torch.bfloat16),
+                                     (1000, torch.float32)])
+@pytest.mark.parametrize("top_k,top_p", FILTERS)
+def test_filter_logits_kept_set(V, dtype, top_k, top_p):
+    """The GPU filter keeps exactly the tokens the oracle's filter keeps
+    (ties at the cut included: rows with long runs of equal logits), and
+    leaves the kept logits untouched."""
+    rng = np.random.default_rng(V + 31 * top_k + int(100 * top_p))
+    R, T = 9, 0.8
+    x = make_logits(rng, R, V, dtype, std=2.0)
+    xf = x.float()
+    xf[1, : V // 2] = xf[1].max()          # a long run tied at the top
+    xf[2, 7:40] = xf[2, 7]                # ties inside the row
+    xf[3, 100 % V] = float("nan")
+    x = xf.to(dtype)
+    g = sd.spec_filter_logits(dev(x.clone()), T, top_k, top_p)
+    torch.cuda.synchronize()
+    _, _, probs, _ = oracle.softmax_topk(np_logits(x), T, 1, want_probs=True)
+    # the C ABI takes top_p in fp32: the oracle gets the same value (rows of
+    # equal logits put the cut exactly at prefix / mass = top_p)
+    kept = oracle.filter_probs(probs, top_k, float(np.float32(top_p))) > 0
+    gk = torch.isfinite(g.float()).cpu().numpy() & ~np.isnan(g.float().cpu().numpy())
+    np.testing.assert_array_equal(gk, kept)
+    same = g.cpu()[torch.from_numpy(kept)]
+    assert torch.equal(same, x[torch.from_numpy(kept)])
+
+
+@pytest.mark.parametrize("top_k,top_p", [(3, 1.0), (0, 0.8), (8, 0.6)])
+@pytest.mark.parametrize("chain", [False, True])
+def test_filtered_verify_parity(top_k, top_p, chain):
+    """Filtered logits through the stochastic verify (tree walk, or the chain
+    launch) against the oracle's verify with the same top-k / top-p."""
+    rng = np.random.default_rng(7 + top_k + int(10 * top_p) + (100 if chain else 0))
+    B, V, T = 64, 2053, 0.9
+    if chain:
+        N = 5
+        nt, ns = chain_meta(B, N)
+        parent = np.array([-1] + list(range(N - 1)))
+    else:
+        N = 7  # root -> 1, 2; 1 -> 3, 4; 2 -> 5, 6
+        nt = np.tile(np.array([1, 3, 5, -1, -1, -1, -1], np.int32), (B, 1))
+        ns = np.tile(np.array([-1, 2, -1, 4, -1, 6, -1], np.int32), (B, 1))
+        parent = np.array([-1, 0, 0, 1, 1, 2, 2])
+    target = rng.normal(0, 2.0, (B, N, V)).astype(np.float32)
+    q = _softmax64(target + rng.normal(0, 0.5, (B, N, V)).astype(np.float32), T).astype(np.float32)
+    dt = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for n in range(1, N):
+            w = q[b, parent[n]].astype(np.float64)
+            dt[b, n] = rng.choice(V, p=w / w.sum())
+    coins = rng.random((B, N)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    tf = sd.spec_filter_logits(dev(target), T, top_k, top_p)
+    g = sd.spec_verify_sample(tf, T, dev(q), dev(dt), dev(nt), dev(ns), dev(coins), dev(uf), chain=chain)
+    o = oracle.verify_sample(target, T, q, dt, nt, ns, coins, uf, top_k=top_k, top_p=float(np.float32(top_p)))
+    torch.cuda.synchronize()
+    exact = sum(verify_compare(g, o, b, b, "sample") for b in range(B))
+    assert exact >= B - 1
+
+
+@pytest.mark.parametrize("top_k,top_p", [(2, 1.0), (0, 0.7), (3, 0.8)])
+def test_filtered_verify_law_monte_carlo_gpu(top_k, top_p):
+    """With target-side filtering on the GPU (filter, then verify), the
+    committed law of speculative rounds with i.i.d. drafts (tree of width 2,
+    depth 2) is the law of sampling the filtered target alone."""
+    from fractions import Fraction
+    from oracle import exact
+    from test_oracle_pins import chi2_pvalue, law_vector, markov_models, spec_rounds_with
+    V, width, depth, M = 4, 2, 2, 2
+    models, logP, Q = markov_models(V, seed=40 + top_k)
+    tp = Fraction(top_p).limit_denominator(1000)
+    P = [exact.filter_probs(models.p((v,)), top_k, tp) for v in range(V)]
+    filtered = exact.ToyModels(V, lambda c: P[c[-1]], models.q)
+    probs = law_vector(exact.target_law(filtered, (0,), M), V, M)
+
+    def verify(target, qq, tok, nt, ns, coins, uf):
+        t = sd.spec_filter_logits(dev(np.ascontiguousarray(target, np.float32)), 1.0, top_k, top_p)
+        g = sd.spec_verify_sample(t, 1.0, dev(np.ascontiguousarray(qq, np.float32)), dev(tok), dev(nt), dev(ns),
+                                  dev(coins), dev(uf))
+        torch.cuda.synchronize()
+        return {k: v.cpu().numpy() for k, v in g.items()}
+
+    seqs = spec_rounds_with(verify, logP, Q, 0, M, width, depth, 100000, seed=5 + top_k)
+    counts = np.bincount(np.ravel_multi_index(seqs.T, (V,) * M), minlength=V ** M)
+    assert chi2_pvalue(counts, probs) > 1e-4
