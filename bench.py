@@ -361,7 +361,7 @@ def run_ours(args, cfg, mode, rank, world, steps=None, warmup=None, flush=False,
         v_gbs = v_bytes / (v_ms * 1e-3) / 1e9
         verify = {"us_per_step": round(v_ms * 1e3, 2), "logit_bytes": int(v_bytes), "achieved": round(v_gbs, 1),
                   "peak": peak, "unit": "GB/s", "frac": round(v_gbs / peak, 4)}
-        vname = ("chain_verify_kernel" if cfg.topk == 1 else "sample_verify_kernel") if mode == "sample" else "row_argmax_kernel"
+        vname = "sample_verify_kernel" if mode == "sample" else "row_argmax_kernel"
         verify_roof = {"bound": "hbm", "kernel": vname if mode == "sample" else vname + " (+ greedy_walk_kernel)",
                        "achieved": round(v_gbs, 1), "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                        "frac": round(v_gbs / peak, 4), "bytes_per_launch": int(v_bytes),

@@ -70,6 +70,7 @@ typedef struct CUstream_st* spec_stream_t; /* same object as cudaStream_t */
 #define SPEC_STAT_EMPTY_INTERSECTION 4/* TLI row with no finite intersection logit */
 #define SPEC_STAT_BAD_REQUEST 5       /* compaction input out of range; request skipped */
 #define SPEC_STAT_WAIT_TIMEOUT 6      /* a CTA gave up waiting on another's row (results void) */
+#define SPEC_STAT_BOUNDS 7            /* debug build only: an index outside its buffer (access skipped) */
 #define SPEC_NUM_STATS 8
 
 /* Limits (checked on the host; SPEC_ERR_UNSUPPORTED beyond them). */
@@ -242,6 +243,20 @@ int spec_build_tree(int B, int k, int num_steps, int N, const float* pool_score,
  * context usable. */
 int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_t* stats_or_null, int32_t* seen,
                     spec_stream_t stream);
+
+/* Bounds-check count of the debug build, libspecdec_debug.so (the same
+ * sources compiled with -DSPEC_DEBUG).  No page of the method has a
+ * counterpart: it stands in for a memory checker.  In that build every kernel
+ * tests the indices it reads and writes through that depend on its inputs
+ * (token ids, node links, row numbers, pool and slot ids, chunk and slot
+ * counters, shared-memory positions) against the extent of the buffer they
+ * index, skips an access that falls outside and counts it: in
+ * SPEC_STAT_BOUNDS of the call's stats_or_null, and in a device counter
+ * kept per source file.  spec_debug_bounds synchronises the device, writes
+ * the sum of those counters since the last reset to *count and zeroes them
+ * when reset != 0.  The release library returns SPEC_ERR_UNSUPPORTED and
+ * writes nothing. */
+int spec_debug_bounds(int64_t* count, int reset);
 
 /* Scratch bytes for spec_verify_greedy / spec_verify_sample (per-row
  * max, normaliser and argmax of the target logits, and the chain verify's

@@ -5,7 +5,9 @@ the GPU, are contiguous and have the expected dtype, allocates outputs the
 caller did not pass (torch.empty on the same device), and calls the C entry
 point of the same name on torch's current CUDA stream.  All computation runs
 in the library's CUDA kernels; there is no CPU path.  If the library is not
-built, the first call raises.
+built, the first call raises.  With SPECDEC_DEBUG=1 in the environment the
+bounds-checking build, libspecdec_debug.so, is loaded instead (build it with
+build(debug=True)); spec_debug_bounds reads its count.
 """
 from __future__ import annotations
 
@@ -21,18 +23,19 @@ __all__ = [
     "spec_verify_sample_qlogits", "WITHOUT_REPLACEMENT", "CHAIN", "spec_compact_freed_capacity",
     "spec_compact_slots", "tli_constrain_map", "tli_constrain_map_qlogits", "tli_plan_bytes", "tli_plan_build",
     "tli_map_ids",
-    "tli_check_config", "tli_pruned_head", "spec_filter_logits", "spec_wait_probe",
+    "tli_check_config", "tli_pruned_head", "spec_filter_logits", "spec_wait_probe", "spec_debug_bounds",
     "new_stats", "new_pool",
 ]
 
 F32 = 0
 BF16 = 1
 STATS = {"nonfinite_row": 0, "q_zero": 1, "residual_fallback": 2, "cdf_fallback": 3,
-         "empty_intersection": 4, "bad_request": 5, "wait_timeout": 6}
+         "empty_intersection": 4, "bad_request": 5, "wait_timeout": 6, "bounds": 7}
 NUM_STATS = 8
 _ERRORS = {-1: "invalid argument", -2: "unsupported", -3: "CUDA launch failed", -4: "workspace too small"}
 
-library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecdec.so")
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                            "libspecdec_debug.so" if os.environ.get("SPECDEC_DEBUG") == "1" else "libspecdec.so")
 _lib = None
 
 _P = ctypes.c_void_p
@@ -78,6 +81,7 @@ _SIGS = {
                                         _P]),
     "tli_map_ids": (_I, [_P, _P, _I64, _P, _I64, _I32, _P]),
     "spec_wait_probe": (_I, [_P, _I64, _P, _P, _P]),
+    "spec_debug_bounds": (_I, [_P, _I]),
     "tli_check_config": (_I, [_I, _I, _I]),
     "spec_filter_logits": (_I, [_P, _I, _I64, _I64, _F, _I64, _F, _P, _P]),
     "tli_pruned_head_ws_size": (_SZ, [_I64, _I64]),
@@ -506,6 +510,15 @@ def spec_wait_probe(flag, limit_cycles, stats=None, seen=None):
     seen = _out(seen, (1,), torch.int32, flag, "seen")
     _call("spec_wait_probe", _ptr(flag), int(limit_cycles), _ptr(stats), _ptr(seen), _stream())
     return seen
+
+
+def spec_debug_bounds(reset=False) -> int:
+    """Out-of-range indices the debug build's kernels have met since the
+    last reset (synchronises the device); SpecError (unsupported) from the
+    release library."""
+    n = ctypes.c_int64(0)
+    _call("spec_debug_bounds", ctypes.byref(n), 1 if reset else 0)
+    return int(n.value)
 
 
 def tli_plan_bytes(Vd, Vt) -> int:

@@ -14,6 +14,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecdec.so")
+# the bounds-checking build (-DSPEC_DEBUG): every input-dependent index is
+# tested against its buffer and violations are counted (spec_debug_bounds)
+DEBUG_OUT_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libspecdec_debug.so")
 SOURCES = ["draft.cu", "tree.cu", "verify.cu", "chain.cu", "compact.cu", "tli.cu", "head.cu", "filter.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -38,16 +42,20 @@ def _stale(target: str) -> bool:
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile (if sources changed) and return the library path."""
-    if not force and not _stale(LIB):
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    """Compile (if sources changed) and return the library path; debug
+    builds libspecdec_debug.so, the bounds-checking variant."""
+    lib, out_dir = (DEBUG_LIB, DEBUG_OUT_DIR) if debug else (LIB, OUT_DIR)
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra.append("-DSPEC_DEBUG")
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -59,14 +67,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if verbose or ptxas_info:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -115,7 +115,7 @@ __device__ float cdf_tile_pass_split(const W& w, int64_t V64, float* part, float
 #pragma unroll
       for (int j = 0; j < kWarps; ++j) s += part[(i % P) * THREADS + j * 32 + lane];
       s = warp_sum(s);
-      if (lane == 0) {
+      if (lane == 0 && spec_in(r + C * i, ntiles, nullptr)) {
         const int t = r + C * i;
         if (C == 1) {
           tile_sum[t] = s;

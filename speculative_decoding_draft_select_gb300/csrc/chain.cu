@@ -36,11 +36,26 @@ namespace {
 constexpr int kCT = kWalkThreads;  // threads of a CTA
 constexpr int kCE = kWalkElems;    // consecutive elements per thread in a tile
 constexpr int kTile = kCT * kCE;
-constexpr int kRingItems = 16;     // 16-byte copies in flight per thread (row statistics)
+#ifndef SPEC_CHAIN_RING
+#define SPEC_CHAIN_RING 16
+#endif
+#ifndef SPEC_CHAIN_SPLIT
+#define SPEC_CHAIN_SPLIT 1
+#endif
+#ifndef SPEC_CHAIN_CTAS_PER_SM
+#define SPEC_CHAIN_CTAS_PER_SM 5
+#endif
+#ifndef SPEC_CHAIN_HERE
+#define SPEC_CHAIN_HERE 0  // draws in place measured slower at B=1024 x 16 (798 vs 833 us) and at B=256 x 5
+#endif
+constexpr int kRingItems = SPEC_CHAIN_RING;  // 16-byte copies in flight per thread (row statistics)
+// pieces a row's statistics are cut into (each a work item; the CTA that
+// finishes a row's last piece merges them in piece order)
+constexpr int kSplit = SPEC_CHAIN_SPLIT;
+static_assert(kSplit == 1 || kSplit == 2, "a row is one or two pieces");
 constexpr int kMaxChunks = 64;     // draw items per request, at most
-constexpr int kMinChunkTiles = 4;
+constexpr int kMinChunkTiles = 8;  // a draw item streams at least 8 tiles (the fixed cost of an item amortised)
 constexpr int kMaxChunkTiles = 32;  // (SPEC_MAX_VOCAB / kTile) / kMaxChunks
-constexpr int kBatch = 4;           // tiles whose loads a chunk pass issues together
 constexpr int kCounters = 8;
 
 // row flag bits (a row's flag is published with them after its statistics)
@@ -66,7 +81,10 @@ struct ChainParams {
   int32_t* front;  // per request: len * 4096 + node of the deepest accepted node seen with every row before it done
   float* A;     // 0: draw from p (bonus), 1: from the residual after one rejection
   float* ctot;  // [B][kMaxChunks] chunk totals of the draw
+  int32_t* half_done;  // [B N] halves of the row done
+  float* half_ms;      // [B N][2][2] each half's (max, sum)
   int ntiles, tpc, nchunks;
+  int64_t half;  // elements of a row's first half (a multiple of 8)
 };
 
 __device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
@@ -92,6 +110,13 @@ __device__ __forceinline__ void atom_add_release(int32_t* p, int v) {
 
 // The committed id y through the caller's map ([TLI] Modifications,
 // map_target_to_draft_ids: unmapped ids take the fallback id).
+// draft-table row of target row rr (the table's row count is not an
+// argument: the debug build checks the sign only)
+__device__ __forceinline__ int64_t q_row_of(const ChainIO& io, int64_t rr) {
+  const int64_t r = io.q_row ? static_cast<int64_t>(__ldg(io.q_row + rr)) : rr;
+  return spec_in(r, INT64_MAX, io.stats) ? r : -1;
+}
+
 __device__ __forceinline__ int32_t mapped_id(const ChainIO& io, int32_t y) {
   return (y >= 0 && y < io.map_len && __ldg(io.map_table + y) >= 0) ? __ldg(io.map_table + y) : io.map_fallback;
 }
@@ -144,6 +169,7 @@ __device__ bool try_resolve(const ChainParams& p, int b, int row_node, bool here
   int node = 0, qz = 0, multi2 = 0;
   io.accept_path[o] = 0;
   for (int i = 0; i < N; ++i) {
+    if (!spec_in(o + i, static_cast<int64_t>(p.B) * N, io.stats)) break;
     if (i < len) {
       const int f = ld_acquire_gpu(p.ready + o + node);
       qz += (f & kRowQZero) ? 1 : 0;
@@ -184,6 +210,7 @@ __device__ bool try_resolve(const ChainParams& p, int b, int row_node, bool here
     return true;
   }
   const int k = atomicAdd(p.cnt + 2, 1);  // a draw slot; its items become takeable now
+  if (!spec_in(k, p.B, io.stats)) return false;
   p.slot_req[k] = b;
   st_release_gpu(p.slot_ready + k, 1);     // publishes node, len, kind, A and the slot
   atom_add_release(p.cnt + 3, 1);          // after the reservation: whoever sees every request resolved sees the slot
@@ -198,9 +225,11 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
   extern __shared__ uint4 ring[];  // kRingItems * kCT slots, then the in-place draw's partials and tile sums
   float* part = reinterpret_cast<float*>(ring + kRingItems * kCT);
   float* tsum = part + cdf_part_tiles<kCT, kCE, 1>(p.V) * kCT;
+  if (!spec_smem_ok(reinterpret_cast<char*>(tsum + (p.V + kTile - 1) / kTile) - reinterpret_cast<char*>(ring),
+                    p.io.stats))
+    return;
   __shared__ float sw_m[kWarps], sw_s[kWarps];
-  __shared__ float red[kBatch][kWarps];  // tile sums of a chunk pass, by warp
-  __shared__ float tile_sh[kMaxChunkTiles];
+  __shared__ float tile_sh[kMaxChunkTiles];  // tile sums of one chunk
   __shared__ float ctot_sh[kMaxChunks];
   __shared__ float scan_sh[33];
   __shared__ float s_tot, s_A;
@@ -214,58 +243,16 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
   bool idle = false;
   int pend = -1;  // thread 0: a claimed draw item whose slot is not reserved yet
 
-  // tile sums of chunk j of a draw row into tile_sh (thread 0), their total
-  // in tile order to every thread.  Each thread copies its elements of D
-  // tiles at once into its slots of the copy ring (D = what the ring holds
-  // at this operand width), then sums them; rows that are not 16-byte
-  // aligned take direct loads.
+  // tile sums of chunk j of a draw row into tile_sh, their total (in tile
+  // order) to every thread: the chunk's tiles, a tile-aligned piece of the
+  // row, streamed by the walk's own pass through the copy ring
   constexpr int K = Weights::template chunks<kCE>();
-  constexpr int D = kRingItems / K < 1 ? 1 : (kRingItems / K > kBatch ? kBatch : kRingItems / K);
+  // tiles in flight per thread in the draw passes: what the ring holds
+  constexpr int kDR = walk_ring_depth(K) < kRingItems / K ? walk_ring_depth(K) : (kRingItems / K < 1 ? 1 : kRingItems / K);
   auto chunk_pass = [&](const Weights& w, int j) -> float {
-    const int t0 = j * p.tpc, t1 = min(p.ntiles, t0 + p.tpc);
-    const bool rg = w.ring_ok();
-    uint4* mine = ring + tid;
-    float tot = 0.0f;
-    for (int t = t0; t < t1; t += D) {
-      float ps[D];
-      if (rg) {
-#pragma unroll
-        for (int u = 0; u < D; ++u)
-          if (t + u < t1) w.template issue<kCE>(mine + u * K * kCT, kCT, static_cast<int64_t>(t + u) * kTile + tid * kCE);
-        cp_async_commit();
-        cp_async_wait<0>();
-#pragma unroll
-        for (int u = 0; u < D; ++u)
-          ps[u] = t + u < t1 ? w.template ring_sum<kCE>(mine + u * K * kCT, kCT,
-                                                         static_cast<int64_t>(t + u) * kTile + tid * kCE)
-                             : 0.0f;
-      } else {
-#pragma unroll
-        for (int u = 0; u < D; ++u)
-          ps[u] = t + u < t1 ? w.template load_sum<kCE>(static_cast<int64_t>(t + u) * kTile + tid * kCE) : 0.0f;
-      }
-#pragma unroll
-      for (int u = 0; u < D; ++u) {
-        const float s = warp_sum(ps[u]);
-        if (lane == 0) red[u][warp] = s;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        for (int u = 0; u < D && t + u < t1; ++u) {
-          float ts = 0.0f;
-#pragma unroll
-          for (int w2 = 0; w2 < kWarps; ++w2) ts += red[u][w2];
-          tile_sh[t + u - t0] = ts;
-          tot += ts;
-        }
-      }
-      __syncthreads();
-    }
-    if (tid == 0) s_tot = tot;
-    __syncthreads();
-    const float r = s_tot;
-    __syncthreads();
-    return r;
+    const int64_t e0 = static_cast<int64_t>(j) * p.tpc * kTile;
+    const int64_t n = min(V, e0 + static_cast<int64_t>(p.tpc) * kTile) - e0;
+    return cdf_tile_pass_split<kCT, kCE, kDR, 1>(w.sub(e0, n), n, part, tile_sh, ring, 0u);
   };
 
   // the first element of tile t whose running prefix (from `prefix`)
@@ -295,6 +282,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
   auto write_draw = [&](int b, int n, int tok) {
     const int64_t o = static_cast<int64_t>(b) * N;
     const int len = __ldcg(p.len + b), kind = __ldcg(p.kind + b);
+    if (!spec_in(len, N, io.stats)) return;
     io.committed[o + len] = tok;
     if (io.committed_mapped) io.committed_mapped[o + len] = mapped_id(io, tok);
     io.num_committed[b] = len + 1;
@@ -374,7 +362,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     const int64_t rr = static_cast<int64_t>(b) * N + n;
     const void* row = static_cast<const char*>(p.target) + rr * V * esz;
     const float m = __ldcg(p.m_row + rr), z = __ldcg(p.z_row + rr);
-    const auto qrow = qsrc.row(A != 0.0f ? (io.q_row ? static_cast<int64_t>(__ldg(io.q_row + rr)) : rr) : -1);
+    const auto qrow = qsrc.row(A != 0.0f ? q_row_of(io, rr) : -1);
     return Weights{row, qrow, V, c, folded_offset(m, c, z), A};
   };
 
@@ -382,8 +370,8 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     if (tid == 0) {
       // rows first: the batched pass is the critical path; then draw items
       int what = 3, item = 0;
-      const int r = ld_volatile(p.cnt) < rows ? atomicAdd(p.cnt, 1) : static_cast<int>(rows);
-      if (r < rows) {
+      const int r = ld_volatile(p.cnt) < kSplit * rows ? atomicAdd(p.cnt, 1) : static_cast<int>(kSplit * rows);
+      if (r < kSplit * rows) {
         what = 2;
         item = r;
       } else {
@@ -424,21 +412,26 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     if (what == 3) continue;
 
     if (what == 2) {
-      // ---------------------------------------------------------- a row
-      const int b = item % B, n = item / B;
+      // ------------------------------------------------ a row (or a piece)
+      // item = kSplit * (node-major row) + piece; the CTA finishing a row's
+      // last piece merges the pieces in order and tests the node's child
+      const int ri = kSplit == 2 ? item >> 1 : item, hf = kSplit == 2 ? item & 1 : 0;
+      const int b = ri % B, n = ri / B;
       const int64_t o = static_cast<int64_t>(b) * N, rr = o + n;
       const void* row = static_cast<const char*>(p.target) + rr * V * esz;
+      const int64_t h0 = hf * p.half, hlen = (hf ? V : p.half) - h0;
+      const void* hrow = static_cast<const char*>(row) + h0 * esz;
       RowStatVisitor<DT, true> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX, 0.0f};
       {
         constexpr int kv = Logit<DT>::kVec;
-        const RowSpan sp = row_span<DT>(row, V);
+        const RowSpan sp = row_span<DT>(hrow, hlen);
         const int head = static_cast<int>(sp.head), nvec = static_cast<int>(sp.nvec);
-        if (tid < head) v.visit1(Logit<DT>::load1(row, tid), tid, true);
-        const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+        if (tid < head) v.visit1(Logit<DT>::load1(hrow, tid), tid, true);
+        const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(hrow) + sp.head * esz);
         ring_stream<kCT, kRingItems>(vp, nvec, ring,
                                      [&](const uint4& x, int i) { v.visit_vec(x, head + static_cast<int64_t>(i) * kv, true); });
         const int64_t t = head + static_cast<int64_t>(nvec) * kv + tid;
-        if (t < V) v.visit1(Logit<DT>::load1(row, t), t, true);
+        if (t < hlen) v.visit1(Logit<DT>::load1(hrow, t), t, true);
       }
       float m = v.m, sum = v.s0 + v.s1;
       warp_merge_ms(m, sum, c);
@@ -451,6 +444,20 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
       sum = sw_s[0];
 #pragma unroll
       for (int w2 = 1; w2 < kWarps; ++w2) merge_ms(m, sum, sw_m[w2], sw_s[w2], c);
+      if (kSplit == 2) {
+        if (tid == 0) {
+          p.half_ms[4 * rr + 2 * hf] = m;
+          p.half_ms[4 * rr + 2 * hf + 1] = sum;
+          // acq_rel: the second half's CTA sees the first half's partials
+          s_last = atom_add_acq_rel(p.half_done + rr, 1) == 1;
+        }
+        __syncthreads();
+        if (!s_last) continue;
+        // both halves: (max, sum) of half 0 merged with half 1's, in that order
+        m = __ldcg(p.half_ms + 4 * rr);
+        sum = __ldcg(p.half_ms + 4 * rr + 1);
+        merge_ms(m, sum, __ldcg(p.half_ms + 4 * rr + 2), __ldcg(p.half_ms + 4 * rr + 3), c);
+      }
       if (isfinite(m) && !isfinite(sum)) {
         // the row holds a NaN: the normaliser again with NaN as -inf
         KeyedSum ks{c, m * c, 0.0f};
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
           if (__ldg(io.nsib + o + ch) >= 0) bits |= kRowMulti;  // only the first child is tested
           const int32_t y = __ldg(io.dtok + o + ch);
           const bool ok = y >= 0 && y < V;
-          const auto qrow = qsrc.row(io.q_row ? static_cast<int64_t>(__ldg(io.q_row + rr)) : rr);
+          const auto qrow = qsrc.row(q_row_of(io, rr));
           const float l = ok ? order_key(Logit<DT>::load1(row, y)) : neg_inf();
           const float qi = ok ? qrow.q_at(y) : 0.0f;
           const float pr = isfinite(m) ? prob_of(l, c, m * c, 1.0f / sum) : 0.0f;
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
         // while many rows remain, a request resolved at this very row is
         // drawn here at once (its target row is still in L2); near the end of
         // the batched pass its draw is cut into chunks for every CTA
-        const bool here_ok = rows - ld_volatile(p.cnt) >= 2 * static_cast<int64_t>(gridDim.x);
+        const bool here_ok = SPEC_CHAIN_HERE && kSplit * rows - ld_volatile(p.cnt) >= static_cast<int64_t>(gridDim.x);
         s_here = try_resolve(p, b, n, here_ok) ? 1 : 0;
         if (s_here) s_A = __ldcg(p.A + b);
       }
@@ -500,11 +507,11 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
         // the tree walk's own pass and draw (one CTA): the row streamed
         // through the copy ring, tile sums in tile order, then the search
         Weights w = draw_weights(b, n, s_A);
-        float total = cdf_tile_pass_split<kCT, kCE, walk_ring_depth(K), 1>(w, V, part, tsum, ring, 0u);
+        float total = cdf_tile_pass_split<kCT, kCE, kDR, 1>(w, V, part, tsum, ring, 0u);
         if (w.A != 0.0f && !(total > 0.0f && isfinite(total))) {
           if (tid == 0) bump(io.stats, SPEC_STAT_RESIDUAL_FALLBACK);
           w.A = 0.0f;
-          total = cdf_tile_pass_split<kCT, kCE, walk_ring_depth(K), 1>(w, V, part, tsum, ring, 0u);
+          total = cdf_tile_pass_split<kCT, kCE, kDR, 1>(w, V, part, tsum, ring, 0u);
         }
         const int32_t tok = cdf_search<kCT, Weights, kCE>(w, V, __ldg(io.u_final + b), tsum, total, scan_sh, io.stats);
         if (tid == 0) write_draw(b, n, tok);
@@ -529,7 +536,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
     const int b = s_b, n = s_n, j = item % p.nchunks;
     const Weights w = draw_weights(b, n, s_A);
     const float tot = chunk_pass(w, j);
-    if (tid == 0) {
+    if (tid == 0 && spec_in(j, kMaxChunks, io.stats)) {
       p.ctot[static_cast<int64_t>(b) * kMaxChunks + j] = tot;
       // acq_rel: the last chunk's CTA sees every other chunk's total
       s_last = atom_add_acq_rel(p.done + b, 1) == p.nchunks - 1;
@@ -544,21 +551,25 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
 }
 
 struct ReqWs {
-  int32_t* ints;  // counters, then 9 arrays of B
+  int32_t* ints;  // counters, then 9 arrays of B, then B N half counters
   size_t int_bytes;
   float* A;
   float* ctot;
+  float* half_ms;
 };
 
-ReqWs carve_req(void* ws, int B) {
+ReqWs carve_req(void* ws, int B, int N) {
   char* q = static_cast<char*>(ws);
+  const size_t rows = static_cast<size_t>(B) * N;
   ReqWs r;
   r.ints = reinterpret_cast<int32_t*>(q);
-  r.int_bytes = sizeof(int32_t) * (kCounters + 9 * static_cast<size_t>(B));
+  r.int_bytes = sizeof(int32_t) * (kCounters + 9 * static_cast<size_t>(B) + rows);
   q += align256(r.int_bytes);
   r.A = reinterpret_cast<float*>(q);
   q += align256(sizeof(float) * static_cast<size_t>(B));
   r.ctot = reinterpret_cast<float*>(q);
+  q += align256(sizeof(float) * kMaxChunks * static_cast<size_t>(B));
+  r.half_ms = reinterpret_cast<float*>(q);
   return r;
 }
 
@@ -570,6 +581,9 @@ int launch_chain(ChainParams& p, const QSrc& qsrc, cudaStream_t s) {
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  // as much shared memory as the SM has (more CTAs resident: more rows in flight)
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   int dev = 0, sms = 0, per = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                  cudaSuccess ||
@@ -579,7 +593,10 @@ int launch_chain(ChainParams& p, const QSrc& qsrc, cudaStream_t s) {
   }
   // persistent: every CTA resident at once (no CTA ever waits on one that
   // has not started); no more CTAs than there are rows and draw items
-  const int64_t items = static_cast<int64_t>(p.B) * p.N + static_cast<int64_t>(p.B) * p.nchunks;
+  // (a grid larger than what is resident at once is safe too: a CTA waits
+  // only on work running CTAs have taken)
+  if (SPEC_CHAIN_CTAS_PER_SM > per) per = SPEC_CHAIN_CTAS_PER_SM;
+  const int64_t items = kSplit * static_cast<int64_t>(p.B) * p.N + static_cast<int64_t>(p.B) * p.nchunks;
   const int64_t grid = std::min<int64_t>(static_cast<int64_t>(sms) * per, items);
   launch_k(kernel, static_cast<unsigned>(grid), kCT, smem, s, p, qsrc);
   return launch_status();
@@ -587,11 +604,11 @@ int launch_chain(ChainParams& p, const QSrc& qsrc, cudaStream_t s) {
 
 }  // namespace
 
-size_t chain_ws_bytes(int B) {
-  if (B < 0) return 0;
-  const size_t b = static_cast<size_t>(B);
-  return align256(sizeof(int32_t) * (kCounters + 9 * b)) + align256(sizeof(float) * b) +
-         align256(sizeof(float) * kMaxChunks * b);
+size_t chain_ws_bytes(int B, int N) {
+  if (B < 0 || N < 1) return 0;
+  const size_t b = static_cast<size_t>(B), rows = b * static_cast<size_t>(N);
+  return align256(sizeof(int32_t) * (kCounters + 9 * b + rows)) + align256(sizeof(float) * b) +
+         align256(sizeof(float) * kMaxChunks * b) + align256(sizeof(float) * 4 * rows);
 }
 
 int chain_verify(int dtype, int B, int N, int64_t V, const void* target, float c, const ChainQ& q,
@@ -607,7 +624,7 @@ int chain_verify(int dtype, int B, int N, int64_t V, const void* target, float c
   p.ready = ready;
   p.m_row = m_row;
   p.z_row = z_row;
-  const ReqWs r = carve_req(req_ws, B);
+  const ReqWs r = carve_req(req_ws, B, N);
   p.cnt = r.ints;
   p.state = p.cnt + kCounters;
   p.done = p.state + B;
@@ -618,6 +635,10 @@ int chain_verify(int dtype, int B, int N, int64_t V, const void* target, float c
   p.kind = p.len + B;
   p.rows_done = p.kind + B;
   p.front = p.rows_done + B;
+  p.half_done = p.front + B;
+  p.half_ms = r.half_ms;
+  p.half = kSplit == 2 ? ((V + 1) / 2 + 7) / 8 * 8 : V;
+  if (p.half > V) p.half = V;
   p.A = r.A;
   p.ctot = r.ctot;
   const int64_t ntiles = (V + kTile - 1) / kTile;

@@ -35,7 +35,7 @@ struct ChainIO {
 
 // Bytes of per-request workspace the chain verify needs beyond the per-row
 // flags, maxima and normalisers.
-size_t chain_ws_bytes(int B);
+size_t chain_ws_bytes(int B, int N);
 
 // Enqueues the chain verify on s.  ready: B*N ints (zeroed here), m_row /
 // z_row: B*N floats, req_ws: chain_ws_bytes(B) bytes, 256-byte aligned.

@@ -155,13 +155,44 @@ __device__ __forceinline__ float2 exp2_sum_pairs(float2 s, const float* x, float
   return s;
 }
 
+// 2^x on the FMA pipe (x <= 0; 0 below -125 and for NaN).  x = n + f, n
+// the nearest integer (adding 1.5 * 2^23 rounds it into the low mantissa
+// bits) and |f| <= 1/2; 2^f by a degree-5 polynomial fitted to 2^f on
+// [-1/2, 1/2] by weighted least squares on the relative error (2.4e-7 at
+// most in fp32 Horner steps, the size of ex2.approx's own error); 2^n is
+// added to the exponent field.
+__device__ __forceinline__ float soft_exp2(float x) {
+  const float xc = fmaxf(x, -125.0f);
+  const float t = xc + 12582912.0f;
+  const float f = xc - (t - 12582912.0f);
+  float p = 0.00132765f;
+  p = fmaf(p, f, 0.00967554f);
+  p = fmaf(p, f, 0.05550713f);
+  p = fmaf(p, f, 0.2402212f);
+  p = fmaf(p, f, 0.69314694f);
+  p = fmaf(p, f, 1.0000001f);
+  const int e = static_cast<int>(static_cast<unsigned>(__float_as_int(t) - 0x4B400000) << 23);
+  return x >= -125.0f ? __int_as_float(__float_as_int(p) + e) : 0.0f;
+}
+
+#ifndef SPEC_SOFT_EXP_MASK
+#define SPEC_SOFT_EXP_MASK 0x00
+#endif
+
 // s + (sum over j of 2^(x_j c.x - mc.x), sum over j of 2^(x_j c.y - mc.y)):
 // one element's terms at two temperatures side by side in a register pair.
+// Two exponentials per element would make the MUFU pipe (16 per clock per
+// SM) the bound of a row stream; the second one of the elements j in
+// SPEC_SOFT_EXP_MASK runs on the FMA pipe instead.
 template <int N>
 __device__ __forceinline__ float2 exp2_sum_two(float2 s, const float* x, float2 c, float2 mc) {
   const float2 nmc = make_float2(-mc.x, -mc.y);
 #pragma unroll
-  for (int j = 0; j < N; ++j) s = add2(s, exp2_2(fma2(splat(x[j]), c, nmc)));
+  for (int j = 0; j < N; ++j) {
+    const float2 a = fma2(splat(x[j]), c, nmc);
+    const float e1 = ((SPEC_SOFT_EXP_MASK >> (j & 7)) & 1) ? soft_exp2(a.y) : fast_exp2(a.y);
+    s = add2(s, make_float2(fast_exp2(a.x), e1));
+  }
   return s;
 }
 
@@ -407,6 +438,58 @@ __device__ __forceinline__ float block_inclusive_scan(float v, float* sh, float&
 __device__ __forceinline__ void bump(int32_t* stats, int slot, int n = 1) {
   if (stats != nullptr && n != 0) atomicAdd(stats + slot, n);
 }
+
+// Bounds checks of the debug build (compiled with -DSPEC_DEBUG, the library
+// libspecdec_debug.so): spec_in(i, n, stats) is whether 0 <= i < n; an index
+// outside its buffer is counted (in this module's device counter, which
+// spec_debug_bounds sums over the library's modules, and in the caller's
+// SPEC_STAT_BOUNDS slot when it passes stats) and the caller skips the
+// access: no trap, no assert.  In the release build it is true and costs
+// nothing.
+#ifdef SPEC_DEBUG
+// each .cu file is a device module of its own, with its own counter
+static __device__ unsigned int g_spec_bounds;
+
+__device__ __forceinline__ bool spec_in(int64_t i, int64_t n, int32_t* stats) {
+  if (i >= 0 && i < n) return true;
+  atomicAdd(&g_spec_bounds, 1u);
+  bump(stats, SPEC_STAT_BOUNDS);
+  return false;
+}
+
+// Host: adds this module's count to *total (and zeroes it when reset).
+using BoundsReader = int (*)(int64_t* total, int reset);
+void register_bounds_reader(BoundsReader r);  // defined once, in verify.cu
+
+namespace {
+int read_module_bounds(int64_t* total, int reset) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_spec_bounds, sizeof(v)) != cudaSuccess) return SPEC_ERR_CUDA;
+  *total += v;
+  if (reset) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_spec_bounds, &z, sizeof(z)) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+struct BoundsRegistration {
+  BoundsRegistration() { register_bounds_reader(read_module_bounds); }
+};
+const BoundsRegistration bounds_registration;
+}  // namespace
+
+// Whether the first `bytes` of dynamic shared memory that a kernel carves
+// up lie within what its launch gave it (the same answer in every CTA of a
+// launch, so a kernel may return on false without stranding a barrier).
+__device__ __forceinline__ bool spec_smem_ok(size_t bytes, int32_t* stats) {
+  uint32_t have;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(have));
+  return bytes == 0 || spec_in(static_cast<int64_t>(bytes) - 1, have, stats);
+}
+#else
+__device__ __forceinline__ bool spec_in(int64_t, int64_t, int32_t*) { return true; }
+__device__ __forceinline__ bool spec_smem_ok(size_t, int32_t*) { return true; }
+#endif
 
 // Aligned vector span of a row: elements [head, head + nvec*kVec) start on a
 // 16-byte boundary; [0, head) and the rest are handled one by one.

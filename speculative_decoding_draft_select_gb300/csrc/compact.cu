@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(kIndexThreads)
     compact_index_kernel(int B, int N, int ps, const int32_t* __restrict__ seq_lens,
                          const int32_t* __restrict__ path, const int32_t* __restrict__ acc_len,
                          int32_t* req_to_token, int64_t max_ctx, int32_t* move_src, int32_t* move_dst,
-                         int32_t* num_moves, int32_t* freed, int32_t* num_freed, int32_t* new_kv_len,
-                         int32_t* stats) {
+                         int32_t* num_moves, int32_t* freed, int64_t freed_cap, int32_t* num_freed,
+                         int32_t* new_kv_len, int32_t* stats) {
   pdl_enter();
   __shared__ int scan_sh[33];
   __shared__ int running;
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kIndexThreads)
           const bool off = n < N && !on;
           const unsigned bits = group_bits(off);
           const int32_t slot = off ? rt[sl + n] : 0;
-          if (off) freed[w + __popc(bits & below)] = slot;
+          if (off && spec_in(w + __popc(bits & below), freed_cap, stats)) freed[w + __popc(bits & below)] = slot;
           w += __popc(bits);
         }
         __syncwarp(gmask);
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kIndexThreads)
           const int32_t pi = i <= a ? __ldg(pb + i) : i;
           const bool mv = i <= a && pi != i;
           const unsigned bits = group_bits(mv);
-          if (mv) {
+          if (mv && spec_in(m + __popc(bits & below), N, stats)) {
             move_src[o + m + __popc(bits & below)] = rt[sl + pi];
             move_dst[o + m + __popc(bits & below)] = rt[sl + i];
           }
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kIndexThreads)
           const int64_t lp = lp0 + gl;
           const bool fr = lp * ps < sl + N && lp * ps >= nk;
           const unsigned bits = group_bits(fr);
-          if (fr) freed[w + __popc(bits & below)] = rt[lp * ps] / ps;
+          if (fr && spec_in(w + __popc(bits & below), freed_cap, stats)) freed[w + __popc(bits & below)] = rt[lp * ps] / ps;
           w += __popc(bits);
         }
       }
@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kCopyThreads)
   pdl_enter();
   const int b = blockIdx.x;
   const int nm = num_moves[b];
+  if (!spec_in(nm, N + 1, stats)) return;
   const bool vec = (bps & 15) == 0 && (reinterpret_cast<uintptr_t>(kv) & 15) == 0;
   for (int m = 0; m < nm; ++m) {
     const int32_t src = move_src[static_cast<int64_t>(b) * N + m];
@@ -244,7 +245,8 @@ extern "C" int spec_compact_slots(int B, int N, int page_size, const int32_t* se
   if (kv_pool_or_null && (num_slots < 1 || bytes_per_slot < 1)) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   launch_k(compact_index_kernel, 1, kIndexThreads, 0, s, B, N, page_size, seq_lens, accept_path, accept_length,
-           req_to_token, max_ctx, move_src, move_dst, num_moves, freed, num_freed, new_kv_len, stats_or_null);
+           req_to_token, max_ctx, move_src, move_dst, num_moves, freed, freed_capacity, num_freed, new_kv_len,
+           stats_or_null);
   int e = launch_status();
   if (e != SPEC_OK || B == 0 || !kv_pool_or_null || page_size == 1) return e;
   launch_k(compact_payload_kernel, B, kCopyThreads, 0, s, N, move_src, move_dst, num_moves,

@@ -457,7 +457,7 @@ __device__ __forceinline__ void write_probs(const void* row, int64_t V, bool fin
 }
 
 template <int K>
-constexpr size_t draft_smem_bytes() {
+__host__ __device__ constexpr size_t draft_smem_bytes() {
   return K == 1 ? 16 : kCandCap * (sizeof(float) + sizeof(int));
 }
 
@@ -493,6 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1024 / THREADS)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t r = blockIdx.x;
   const void* row = static_cast<const char*>(logits) + r * V * esz;
+  if (!spec_smem_ok(draft_smem_bytes<K>(), stats)) return;
   // pass A: online softmax and every thread's best element (and for K > 1
   // the largest key among its other elements)
   ArgmaxVisitor<DT, (K > 1), TWO> st{c, c1};
@@ -697,6 +698,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   const int64_t ntiles = (V + kSampleThreads * 8 - 1) / (kSampleThreads * 8);
   float* tile_sum = dyn;
   float* red = dyn + ntiles;
+  if (!spec_smem_ok(sizeof(float) * cdf_smem_floats<kSampleThreads>(V), stats)) return;
   const int64_t r = blockIdx.x;
   float* op = out_prob ? out_prob + r : nullptr;
   if (FROM_PROBS) {
@@ -771,6 +773,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1024 / kFusedThreads)
   const int V = static_cast<int>(V64), head = static_cast<int>(sp.head), nvec = static_cast<int>(sp.nvec);
   const int tail0 = head + nvec * kv, ntiles = (nvec + U * T - 1) / (U * T);
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + sp.head * esz);
+  if (!spec_smem_ok(sizeof(float) * ntiles * T, stats) || !spec_in(ntiles + 1, kFusedMaxTiles + 2, stats)) return;
 
   float m = neg_inf(), mc = 0.0f, s = 0.0f, hs = 0.0f, tl = 0.0f;
   if (tid < head) {  // head < kv <= T

@@ -77,6 +77,7 @@ __device__ __forceinline__ void expand_request(const ExpandArgs& e, int b, const
       tok = __ldcg(topk_idx + row * k + j);
       par = e.frontier_id[row];
     }
+    if (!spec_in(base + c, P, nullptr)) continue;
     sc[base + c] = score;
     tk[base + c] = tok;
     pa[base + c] = par;
@@ -87,7 +88,7 @@ __device__ __forceinline__ void expand_request(const ExpandArgs& e, int b, const
     const uint64_t mine = keys[c];
     int rank = 0;
     for (int o = 0; o < nc; ++o) rank += keys[o] < mine;
-    if (rank < k) {
+    if (rank < k && spec_in(base + c, P, nullptr)) {
       e.frontier_score[static_cast<int64_t>(b) * k + rank] = sc[base + c];
       e.frontier_id[static_cast<int64_t>(b) * k + rank] = static_cast<int32_t>(base + c);
       if (step + 1 < e.num_steps) qr[base + c] = e.B + step * e.B * k + b * k + rank;
@@ -123,6 +124,7 @@ __device__ __forceinline__ void expand_chain(const ExpandArgs& e, int b, float p
     par = e.frontier_id[b];
     base = 1 + step;
   }
+  if (!spec_in(base, P, nullptr)) return;
   sc[base] = score;
   tk[base] = tok;
   pa[base] = par;

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kFT) filter_kernel(void* __restrict__ logits, 
         }
       }
     }
-    if (cut_idx >= V) continue;  // nothing dropped
+    if (!spec_in(cut_idx, V + 1, stats) || cut_idx >= V) continue;  // nothing dropped
     // every element after the cut becomes -inf
     for (int64_t v = threadIdx.x; v < V; v += kFT) {
       const uint32_t k = FKey<DT>::of(logit_at<DT>(row, v));

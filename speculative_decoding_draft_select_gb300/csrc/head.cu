@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   // stage s: hidden rows [0, 128) at s * kStageBytes, rows [128, 256) after
   // it, the weight slab last; every slab 1024-byte aligned (swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (!spec_smem_ok((smem - smem_raw) + static_cast<size_t>(kStages) * kStageBytes, stats)) return;
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           float x[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) x[jj] = c0 + jj < c_end ? order_key(__uint_as_float(r[jj])) : neg_inf();
-          if (logits != nullptr && row < M) {
+          if (logits != nullptr && row < M && spec_in(n0 + c_end - 1, K, stats)) {
             float* out = logits + static_cast<int64_t>(row) * K + col0;
             if (c0 + 16 <= c_end && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
 #pragma unroll
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = m_base + h * kBM + q * 32 + lane;
-      if (h < nM && row < M) partial[static_cast<int64_t>(row) * nslots + slot] = make_float4(mx[h], sum[h], bv[h], __int_as_float(bi[h]));
+      if (h < nM && row < M && spec_in(slot, nslots, stats)) partial[static_cast<int64_t>(row) * nslots + slot] = make_float4(mx[h], sum[h], bv[h], __int_as_float(bi[h]));
     }
   }
   tc_fence_before();
@@ -352,7 +353,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads)
-    head_merge_kernel(int M, int nslots, float c, const float4* __restrict__ partial, const int32_t* __restrict__ ids,
+    head_merge_kernel(int M, int K, int nslots, float c, const float4* __restrict__ partial,
+                      const int32_t* __restrict__ ids,
                       const int32_t* __restrict__ d2t, int64_t Vd, int32_t* __restrict__ top1_rank,
                       int32_t* __restrict__ top1_draft, int32_t* __restrict__ top1_target, float* __restrict__ top1_p,
                       float* __restrict__ row_stats, int32_t* __restrict__ stats) {
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
   const bool finite = isfinite(m) && bi != INT_MAX;
   if (!finite) bump(stats, SPEC_STAT_EMPTY_INTERSECTION);
-  const int32_t d = finite ? __ldg(ids + bi) : -1;
+  const int32_t d = finite && spec_in(bi, K, stats) ? __ldg(ids + bi) : -1;
   if (top1_rank) top1_rank[row] = finite ? bi : -1;
   top1_draft[row] = d;
   top1_target[row] = (d >= 0 && d < Vd) ? __ldg(d2t + d) : -1;
@@ -504,7 +506,8 @@ extern "C" int tli_pruned_head(int64_t M, int64_t H, int64_t K, const void* hidd
            kHeadSmem, s, tm_h, tm_w128, tm_w16, static_cast<int>(M), static_cast<int>(K), static_cast<int>(H), c,
            hs.rows_per_cta, hs.tiles_per_cta, partial, logits_or_null, stats_or_null);
   if (launch_status() != SPEC_OK) return SPEC_ERR_CUDA;
-  launch_k(head_merge_kernel, static_cast<unsigned>(M), kMergeThreads, 0, s, static_cast<int>(M), hs.nslots,
+  launch_k(head_merge_kernel, static_cast<unsigned>(M), kMergeThreads, 0, s, static_cast<int>(M), static_cast<int>(K),
+           hs.nslots,
            c, static_cast<const float4*>(partial), ids, d2t, V_d, top1_rank_or_null, top1_draft, top1_target, top1_p,
            row_stats_or_null, stats_or_null);
   return launch_status();

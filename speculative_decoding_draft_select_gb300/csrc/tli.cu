@@ -450,9 +450,11 @@ template <int DT>
 struct CompactWriter {
   const uint2* mw;
   typename Elem<DT>::T* cpt;
+  int K;  // entries of cpt (the debug build's bounds)
   __device__ __forceinline__ void visit1(float x, int64_t idx, bool) {
     const int id = static_cast<int>(idx);
-    if ((mw[id >> 5].x >> (id & 31)) & 1u) cpt[rank_before(mw, id)] = Elem<DT>::of_value(x);
+    if (((mw[id >> 5].x >> (id & 31)) & 1u) && spec_in(rank_before(mw, id), K, nullptr))
+      cpt[rank_before(mw, id)] = Elem<DT>::of_value(x);
   }
   __device__ __forceinline__ void visit_vec(const uint4& raw, int first) {
     constexpr int kv = Logit<DT>::kVec;
@@ -465,7 +467,7 @@ struct CompactWriter {
     int r = static_cast<int>(e.y) + __popc(e.x & ((1u << sh) - 1u));
 #pragma unroll
     for (int j = 0; j < kv; ++j)
-      if ((b >> j) & 1u) cpt[r++] = Elem<DT>::at(raw, j);
+      if (((b >> j) & 1u) && spec_in(r, K, nullptr)) cpt[r++] = Elem<DT>::at(raw, j);
   }
 };
 
@@ -621,7 +623,11 @@ __global__ void __launch_bounds__(kResThreads, 1)
     reinterpret_cast<uint4*>(mw)[i] = __ldg(reinterpret_cast<const uint4*>(pv.mw) + i);
   const int K = __ldg(pv.K);
   __syncthreads();
-  E* const cpt = ((qo.q != nullptr || qo.ql != nullptr) && K <= cap) ? cpt_buf : nullptr;
+  if (!spec_smem_ok(reinterpret_cast<unsigned char*>(cpt_buf) - res_dsm, stats) || !spec_in(K, Vd + 1, stats)) return;
+  E* const cpt = ((qo.q != nullptr || qo.ql != nullptr) && K <= cap &&
+                  spec_smem_ok(reinterpret_cast<unsigned char*>(cpt_buf + K) - res_dsm, stats))
+                     ? cpt_buf
+                     : nullptr;
   const int32_t* t2r = pv.t2r;
 
   // block merge of the per-thread partials into s_m, s_s, s_bv, s_bi
@@ -655,7 +661,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
   for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
     const void* row = static_cast<const char*>(draft) + r * Vd * esz;
     if (cpt != nullptr) {
-      CompactWriter<DT> cw{mw, cpt};
+      CompactWriter<DT> cw{mw, cpt, K};
       ring_row<DT>(row, Vd, ring, cw);
       __syncthreads();  // the K intersection logits, in id order
       StatVisitor<DT> st{c, neg_inf(), 0.0f, 0.0f, 0.0f, INT_MAX};
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
       // the top-1 outputs (thread 0 alone; the other warps go on) and the
       // step's pool expansion for this row's request (a chain: one row each)
       const int best = ok ? (cpt != nullptr ? id_of_rank(mw, W, s_bi) : s_bi) : -1;
-      const int32_t tgt = ok ? __ldg(d2t + best) : -1;
+      const int32_t tgt = ok && spec_in(best, Vd, stats) ? __ldg(d2t + best) : -1;
       const float pr = ok ? fminf(fast_exp2(fmaf(s_bv, c, -mc)) * invz, 1.0f) : 0.0f;
       top1_draft[r] = best;
       top1_target[r] = tgt;
@@ -716,11 +722,12 @@ __global__ void __launch_bounds__(kResThreads, 1)
         // probability needs no clamp (a partner outside the intersection,
         // read from the row, does)
         auto q_far = [&](int32_t k) -> float {
+          if (!spec_in(-2 - k, Vd, stats)) return 0.0f;
           return fminf(fast_exp2(fmaf(order_key(Logit<DT>::load1(row, -2 - k)), c, -mc)) * invz, 1.0f);
         };
         auto q_pair = [&](int32_t k0, int32_t k1) -> float2 {
-          const float2 x = make_float2(order_key(Elem<DT>::value(cpt[k0 > 0 ? k0 : 0])),
-                                       order_key(Elem<DT>::value(cpt[k1 > 0 ? k1 : 0])));
+          const float2 x = make_float2(order_key(Elem<DT>::value(cpt[k0 > 0 && spec_in(k0, K, stats) ? k0 : 0])),
+                                       order_key(Elem<DT>::value(cpt[k1 > 0 && spec_in(k1, K, stats) ? k1 : 0])));
           const float2 y = fma2(x, splat(c), splat(-mc));
           const float2 p = fma2(exp2_2(y), splat(invz), splat(0.0f));
           return make_float2(k0 >= 0 ? p.x : 0.0f, k1 >= 0 ? p.y : 0.0f);
@@ -744,7 +751,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                                            });
         for (int64_t t = static_cast<int64_t>(nv) * 4 + tid; t < Vt; t += kResThreads) {
           const int32_t k = __ldg(t2r + t);
-          out[t] = k >= 0 ? fast_exp2(fmaf(order_key(Elem<DT>::value(cpt[k])), c, -mc)) * invz
+          out[t] = k >= 0 ? fast_exp2(fmaf(order_key(Elem<DT>::value(cpt[spec_in(k, K, stats) ? k : 0])), c, -mc)) * invz
                           : (k == -1 ? 0.0f : q_far(k));
         }
       } else {
@@ -777,10 +784,12 @@ __global__ void __launch_bounds__(kResThreads, 1)
         // branch-free for ranked partners and none (-1); a partner outside
         // the intersection (-2 - d, rare) is read from the row
         auto near = [&](int32_t k) -> E {
-          const E v = cpt[k > 0 ? k : 0];
+          const E v = cpt[k > 0 && spec_in(k, K, stats) ? k : 0];
           return k >= 0 ? v : ninf;
         };
-        auto far = [&](int32_t k) -> E { return Elem<DT>::of_value(Logit<DT>::load1(row, -2 - k)); };
+        auto far = [&](int32_t k) -> E {
+          return spec_in(-2 - k, Vd, stats) ? Elem<DT>::of_value(Logit<DT>::load1(row, -2 - k)) : ninf;
+        };
         auto l_of = [&](int32_t k) -> E { return k < -1 ? far(k) : near(k); };
         const int nl = vl ? static_cast<int>(Vt / 4) : 0;
         direct_stream<kResThreads, kP2Unroll>(reinterpret_cast<const uint4*>(t2r), nl, [&](const uint4& kk, int i) {

@@ -24,6 +24,7 @@ __global__ void tree_expand_kernel(ExpandArgs e, const float* __restrict__ topk_
                                    const int32_t* __restrict__ topk_idx) {
   pdl_enter();
   extern __shared__ uint64_t keys[];
+  if (!spec_smem_ok(sizeof(uint64_t) * (e.step == 0 ? e.k : e.k * e.k), nullptr)) return;
   expand_request(e, blockIdx.x, topk_p, topk_idx, keys);
 }
 
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kBuildThreads)
   int32_t* npid = node_of + P;                                // [N]
   int32_t* npar = npid + N;                                   // [N]
   int32_t* nxt = npar + N;                                    // [N]
+  if (!spec_smem_ok(reinterpret_cast<char*>(nxt + N) - reinterpret_cast<char*>(dyn), nullptr)) return;
   __shared__ int scan_sh[33];
   const int b = blockIdx.x;
   const int nt = blockDim.x;
@@ -110,7 +112,8 @@ __global__ void __launch_bounds__(kBuildThreads)
         __syncthreads();
       }
     }
-    for (int64_t r = threadIdx.x; r < N - 1; r += nt) node_of[static_cast<uint32_t>(keys[r])] = 1;
+    for (int64_t r = threadIdx.x; r < N - 1; r += nt)
+      if (spec_in(static_cast<uint32_t>(keys[r]), P, nullptr)) node_of[static_cast<uint32_t>(keys[r])] = 1;
   }
   __syncthreads();
   // 2. the root and the selected candidates, numbered in pool-id order
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kBuildThreads)
   int total;
   int idx = block_exclusive_scan_int(cnt, scan_sh, total);
   for (int64_t i = lo; i < hi; ++i) {
-    if (node_of[i]) {
+    if (node_of[i] && spec_in(idx, N, nullptr)) {
       npid[idx] = static_cast<int32_t>(i);
       node_of[i] = idx++;
     } else {
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(kBuildThreads)
   const int64_t o = static_cast<int64_t>(b) * N;
   for (int n = threadIdx.x; n < N; n += nt) {
     const int32_t pid = npid[n];
+    if (!spec_in(pid, P, nullptr)) continue;
     int32_t par = -1;
     if (n > 0) {
       const int32_t pp = __ldg(pa + pid);

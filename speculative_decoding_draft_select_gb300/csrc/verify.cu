@@ -29,6 +29,7 @@
 // The last residual pass also leaves the per-tile sums the inverse-CDF draw
 // needs, so a correction token costs one row sweep plus one tile rescan.
 #include <climits>
+#include <vector>
 
 #include "cdf.cuh"
 #include "chain.h"
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kStatThreads, 1024 / kStatThreads)
     bv = lane < kWarps ? wv[lane] : neg_inf();
     bi = lane < kWarps ? wi[lane] : INT_MAX;
     warp_best(bv, bi);
-    if (lane == 0) {
+    if (lane == 0 && spec_in(r, gridDim.x, stats)) {
       amax[r] = bi == INT_MAX ? 0 : bi;
       if (!isfinite(bv)) bump(stats, SPEC_STAT_NONFINITE_ROW);
     }
@@ -97,7 +98,7 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
                                    const int32_t* __restrict__ ntok, const int32_t* __restrict__ nsib,
                                    const int32_t* __restrict__ budget, int32_t eos, int32_t* committed,
                                    int32_t* num_committed, int32_t* accept_length, int32_t* accept_path,
-                                   int32_t* next_root, int32_t* walk_info) {
+                                   int32_t* next_root, int32_t* walk_info, int32_t* stats) {
   pdl_enter();
   extern __shared__ int32_t sh[];
   int32_t *s_am = sh, *s_dt = sh + N, *s_nt = sh + 2 * N, *s_ns = sh + 3 * N, *s_com = sh + 4 * N,
@@ -128,7 +129,8 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
         }
         ++rej;
       }
-      if (found >= 0) s_path[++acc] = found;
+      // (links that loop cannot push the path past N entries)
+      if (found >= 0 && acc + 1 < N) s_path[++acc] = found;
       if (t == eos || len == rem || found < 0) {
         if (found >= 0) {
           kind = SPEC_FINAL_ACCEPTED;
@@ -151,6 +153,7 @@ __global__ void greedy_walk_kernel(int N, const int32_t* __restrict__ amax, cons
   }
   __syncwarp();
   for (int i = lane; i < N; i += 32) {
+    if (!spec_in(o + i, static_cast<int64_t>(gridDim.x) * N, stats)) continue;
     committed[o + i] = s_com[i];
     accept_path[o + i] = s_path[i];
   }
@@ -232,6 +235,11 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
   int32_t* s_ry = s_ch + N;
   float* s_rf = reinterpret_cast<float*>(s_ry + N);
   float* s_rd = s_rf + N;
+  // (the rejected-token arrays exist only without replacement)
+  if (!spec_smem_ok(reinterpret_cast<char*>(WOR ? reinterpret_cast<int32_t*>(s_rd + N) : s_ch + N) -
+                        reinterpret_cast<char*>(dyn_ring),
+                    stats))
+    return;
   __shared__ float scan_sh[33];
   __shared__ int s_nry, s_newy;
   __shared__ float s_S, s_wsum;
@@ -322,9 +330,11 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     }
     if (tid == 0) {
       if (!isfinite(m)) bump(stats, SPEC_STAT_NONFINITE_ROW);
-      m_row[r] = m;
-      z_row[r] = sum;
-      st_release_gpu(ready + r, 1);
+      if (spec_in(r, rows, stats)) {
+        m_row[r] = m;
+        z_row[r] = sum;
+        st_release_gpu(ready + r, 1);
+      }
     }
     __syncthreads();  // sw_* reused by the next row
   };
@@ -399,6 +409,9 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
       s_invz = 1.0f / z;
       s_nb = folded_offset(s_m, c, z);
       s_qrow = q_row ? static_cast<int64_t>(__ldg(q_row + o + n)) : o + n;
+      // a node with children needs its draft row (the table's row count is
+      // not an argument: only the sign is checked)
+      if (nch > 0 && !spec_in(s_qrow, INT64_MAX, stats)) s_qrow = -1;
       s_A = 0.0f;
       s_cj = 1.0f;
       s_tiles_ok = 0;
@@ -477,7 +490,7 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
           bool seen = false;
           for (int e = 0; e < s_nry; ++e) seen = seen || s_ry[e] == y;
           s_newy = -1;
-          if (!seen && y >= 0 && y < V) {
+          if (!seen && y >= 0 && y < V && spec_in(s_nry, N, cstats)) {
             s_ry[s_nry] = y;
             s_rf[s_nry] = w.at(y);
             s_newy = s_nry++;
@@ -507,7 +520,7 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
       if (tid == 0) {
         const int32_t y = s_dt[accepted];
         s_com[s_len++] = y;
-        s_path[++s_acc] = accepted;
+        if (s_acc + 1 < N) s_path[++s_acc] = accepted;  // (links that loop cannot push the path past N)
         s_n = accepted;
         if (y == eos || s_len == s_rem || s_len >= N) {
           s_kind = SPEC_FINAL_ACCEPTED;
@@ -558,6 +571,7 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
       }
     }
     for (int i = tid; i < N; i += kWalkThreads) {
+      if (!spec_in(o + i, static_cast<int64_t>(B) * N, stats)) continue;
       committed[o + i] = s_com[i];
       accept_path[o + i] = s_path[i];
     }
@@ -624,6 +638,36 @@ int check_common(int B, int N, int64_t V, int dtype, const void* target, const i
 
 using namespace specdec;
 
+#ifdef SPEC_DEBUG
+namespace specdec {
+namespace {
+std::vector<BoundsReader>& bounds_readers() {
+  static std::vector<BoundsReader> r;
+  return r;
+}
+}  // namespace
+void register_bounds_reader(BoundsReader r) { bounds_readers().push_back(r); }
+}  // namespace specdec
+#endif
+
+extern "C" int spec_debug_bounds(int64_t* count, int reset) {
+#ifdef SPEC_DEBUG
+  if (count == nullptr) return SPEC_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPEC_ERR_CUDA;
+  int64_t total = 0;
+  for (auto r : specdec::bounds_readers()) {
+    const int rc = r(&total, reset);
+    if (rc != SPEC_OK) return rc;
+  }
+  *count = total;
+  return SPEC_OK;
+#else
+  (void)count;
+  (void)reset;
+  return SPEC_ERR_UNSUPPORTED;
+#endif
+}
+
 extern "C" int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_t* stats, int32_t* seen,
                                spec_stream_t stream) {
   if (!flag || !seen || limit_cycles < 0) return SPEC_ERR_INVALID_ARG;
@@ -635,7 +679,7 @@ extern "C" int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_
 extern "C" size_t spec_verify_ws_size(int B, int N) {
   if (B < 0 || N < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * N;
-  return align256((rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float)) + chain_ws_bytes(B);
+  return align256((rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float)) + chain_ws_bytes(B, N);
 }
 
 extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void* target_logits,
@@ -658,7 +702,7 @@ extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void
   if (e != SPEC_OK) return e;
   launch_k(greedy_walk_kernel, B, 32, sizeof(int32_t) * 6 * N, s, N, w.amax, draft_token, retrieve_next_token,
            retrieve_next_sibling, budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
-           next_root, walk_info_or_null);
+           next_root, walk_info_or_null, stats_or_null);
   return launch_status();
 }
 
@@ -1025,6 +1069,6 @@ extern "C" int spec_verify_greedy_noalloc(int B, int N, int64_t V, int dtype, co
   if (e != SPEC_OK) return e;
   launch_k(greedy_walk_kernel, B, 32, sizeof(int32_t) * 6 * N, s, N, amax, draft_token, retrieve_next_token,
            retrieve_next_sibling, budget_or_null, eos_id, committed, num_committed, accept_length, accept_path,
-           next_root, walk_info_or_null);
+           next_root, walk_info_or_null, stats_or_null);
   return launch_status();
 }

@@ -191,6 +191,8 @@ struct QRowProbs {
   static constexpr int kEsz = 4;
   const float* row;  // nullptr: no row (q = 0)
   int64_t V;
+  // elements [e0, e0 + n) as a row of their own
+  __device__ __forceinline__ QRowProbs sub(int64_t e0, int64_t n) const { return {row ? row + e0 : nullptr, n}; }
   __device__ __forceinline__ float q_at(int64_t v) const { return row ? __ldg(row + v) : 0.0f; }
   __device__ __forceinline__ float sweep_at(int64_t v) const { return q_at(v); }
   __device__ __forceinline__ void load8(int64_t v0, float* x) const {
@@ -230,6 +232,10 @@ struct QRowLogits {
   const void* row;  // nullptr: no row, or a row whose max is not finite (q = 0)
   int64_t V;
   float c, mc, invz, nb;
+  // elements [e0, e0 + n) as a row of their own (same max and normaliser)
+  __device__ __forceinline__ QRowLogits sub(int64_t e0, int64_t n) const {
+    return {row ? static_cast<const char*>(row) + e0 * kEsz : nullptr, n, c, mc, invz, nb};
+  }
   __device__ __forceinline__ float q_at(int64_t v) const {
     return row ? prob_of(order_key(Logit<QDT>::load1(row, v)), c, mc, invz) : 0.0f;
   }
@@ -309,6 +315,10 @@ struct ResidualWeights {
   QRow qrow;
   int64_t V;
   float c, nb, A;
+  // the weights of elements [e0, e0 + n) as a row of their own
+  __device__ __forceinline__ ResidualWeights sub(int64_t e0, int64_t n) const {
+    return {static_cast<const char*>(lrow) + e0 * kTargetEsz, qrow.sub(e0, n), n, c, nb, A};
+  }
   // x <- weights of 8 elements from logits l (and q values when A != 0)
   __device__ __forceinline__ void values8(float* l, const float* q) const {
     const float2 c2 = splat(c), nb2 = splat(nb), na2 = splat(-A);

@@ -172,10 +172,12 @@ def run_verify(buf: StepBuffers, target, mode, T=1.0, coins=None, u_final=None, 
     """Greedy or stochastic verify of buf.tree against target [B, N, V];
     without_replacement selects the stochastic sibling update for children
     drawn without replacement (q renormalised without each rejected child).
-    chain (default: the drafts are chains, topk 1) selects the chain verify
-    launch for stochastic verification."""
+    chain selects the chain verify launch (SPEC_VERIFY_CHAIN) for the
+    stochastic verify of chains; the default is the tree walk, which measured
+    faster on chains too (B=256 x 5 nodes: 117 vs 128 us; B=1024 x 16: 725 vs
+    798 us)."""
     t = buf.tree
-    chain = buf.topk == 1 if chain is None else chain
+    chain = False if chain is None else chain
     if mode == "greedy":
         return spec_verify_greedy(target, t["draft_token"], t["retrieve_next_token"], t["retrieve_next_sibling"],
                                   budget=budget, eos_id=eos_id, out=buf.verify_out, ws=buf.ws, stats=buf.stats)

@@ -35,6 +35,21 @@ def boundary_report():
     return add
 
 
+@pytest.fixture(autouse=True)
+def _debug_bounds(request):
+    """Under the bounds-checking build (SPECDEC_DEBUG=1) every GPU test ends
+    with no out-of-range index met by any kernel it launched."""
+    if os.environ.get("SPECDEC_DEBUG") != "1" or request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import speculative_decoding_draft_select_gb300 as sd
+    assert sd.library_path.endswith("libspecdec_debug.so")
+    sd.spec_debug_bounds(reset=True)
+    yield
+    n = sd.spec_debug_bounds(reset=True)
+    assert n == 0, f"{n} out-of-range indices met under the bounds-checking build"
+
+
 def pytest_terminal_summary(terminalreporter):
     if not BOUNDARY_CASES:
         return

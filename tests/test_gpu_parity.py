@@ -475,6 +475,53 @@ def _softmax64(x, T):
     return np.where(z > 0, e / np.where(z > 0, z, 1.0), 0.0)
 
 
+def _check_walk_outputs(out, B, N, V):
+    """Well-formed verify outputs: 1..N tokens in [0, V) then -1 padding, an
+    accepted path from the root of at most num_committed nodes in [1, N)."""
+    com = out["committed"].cpu().numpy()
+    nc = out["num_committed"].cpu().numpy()
+    acc = out["accept_length"].cpu().numpy()
+    path = out["accept_path"].cpu().numpy()
+    for b in range(B):
+        n = int(nc[b])
+        assert 1 <= n <= N
+        assert ((com[b, :n] >= 0) & (com[b, :n] < V)).all() and (com[b, n:] == -1).all()
+        a = int(acc[b])
+        assert 0 <= a <= n and a < N
+        assert path[b, 0] == 0 and ((path[b, 1:a + 1] >= 1) & (path[b, 1:a + 1] < N)).all()
+        assert (path[b, a + 1:] == -1).all()
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_verify_links_that_loop_stay_in_bounds(mode):
+    """Retrieve links that are not a tree (a sibling cycle among the root's
+    children, a child that points back to an earlier node, a node that is
+    its own first child and sibling): the walks bound every link chain by N
+    hops and every path by N entries, so the launch ends with well-formed
+    outputs (the parity suite's adversarial case for the bounds checks)."""
+    rng = np.random.default_rng(4242)
+    B, N, V, T = 16, 6, 257, 1.0
+    nt = np.tile(np.array([1, 3, 1, 3, -1, -1], np.int32), (B, 1))
+    ns = np.tile(np.array([-1, 2, 1, 3, -1, -1], np.int32), (B, 1))
+    target = rng.normal(0, 2, (B, N, V)).astype(np.float32)
+    am = target.argmax(-1)
+    # drafts mostly agree with the argmax of the row they are tested on
+    draft = rng.integers(0, V, (B, N)).astype(np.int32)
+    for n, par in ((1, 0), (2, 0), (3, 1)):
+        agree = rng.random(B) < 0.7
+        draft[agree, n] = am[agree, par]
+    tgt = dev(torch.from_numpy(target))
+    if mode == "greedy":
+        out = sd.spec_verify_greedy(tgt, dev(draft), dev(nt), dev(ns))
+    else:
+        q = _softmax64(target + rng.normal(0, 0.3, target.shape), T).astype(np.float32)
+        coins = rng.random((B, N)).astype(np.float32)
+        u_final = rng.random(B).astype(np.float32)
+        out = sd.spec_verify_sample(tgt, T, dev(q), dev(draft), dev(nt), dev(ns), dev(coins), dev(u_final))
+    torch.cuda.synchronize()
+    _check_walk_outputs(out, B, N, V)
+
+
 @pytest.mark.parametrize("B", [8, 200])
 def test_verify_sample_fallbacks_and_counters(B):
     """zero-to-sglang ch.10 5.1 asks for numerical validity checks in finite
