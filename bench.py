@@ -561,6 +561,7 @@ def main():
     ap.add_argument("--mode", default=None, choices=[None, "greedy", "sample"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--filter-only", action="store_true", help="time target-side filtering alone")
     ap.add_argument("--q", default=None, choices=[None, "logits", "probs"],
                     help="draft distribution for stochastic verify: logit rows + row stats, or written fp32 rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -589,6 +590,11 @@ def main():
         return
 
     torch.cuda.set_device(local)
+    if args.filter_only:
+        from speculative_decoding_draft_select_gb300.build import build
+        build()
+        print(json.dumps(filter_leg(B=args.batch or 128)), flush=True)
+        return
     if args.head_only:
         from speculative_decoding_draft_select_gb300.build import build
         build()
@@ -684,6 +690,42 @@ def pruned_head_leg(M=256, H=896, K=60000, Vd=151936, Vt=128256, launches=20):
     return res
 
 
+def filter_leg(B=128, N=64, V=128256, T=0.7, top_k=50, top_p=0.9, launches=10):
+    """Target-side top-k / top-p filtering (spec_filter_logits) of the c3
+    target logits [B*N, V] bf16 in place, timed per launch with CUDA events.
+    Each launch gets a fresh copy of the unfiltered logits first (untimed;
+    2.1 GB, so L2 holds none of it).  Algorithmic bytes: every row read once
+    and every dropped element written once."""
+    import speculative_decoding_draft_select_gb300 as sd
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(1003 * 1009 + 55)
+    src = (torch.randn((B * N, V), generator=g, device=dev) * 3.0).to(torch.bfloat16)
+    x = torch.empty_like(src)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        x.copy_(src)
+        sd.spec_filter_logits(x, T, top_k, top_p)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    for a, b in ev:
+        x.copy_(src)
+        a.record(stream)
+        sd.spec_filter_logits(x, T, top_k, top_p)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    dropped = int(torch.isinf(x).sum()) - int(torch.isinf(src).sum())
+    byts = B * N * V * 2 + dropped * 2
+    hpk, hsrc = hbm_peak()
+    gbs = byts / (us * 1e-6) / 1e9
+    del src, x
+    torch.cuda.empty_cache()
+    return {"workload": f"target-side filtering of the c3 target logits: {B * N} rows x V={V} bf16 in place, "
+                        f"T={T}, top_k={top_k}, top_p={top_p}",
+            "us": round(us, 2), "bytes_per_launch": byts, "dropped_per_row": round(dropped / (B * N), 1),
+            "gbs": round(gbs, 1), "hbm_frac": round(gbs / hpk, 4), "peak_source": hsrc}
+
+
 def other_configs(args):
     res = {}
     try:
@@ -691,6 +733,10 @@ def other_configs(args):
     except Exception as e:  # reported, not hidden
         res["c4_pruned_head"] = {"error": f"{type(e).__name__}: {e}"}
     torch.cuda.empty_cache()
+    try:
+        res["c3_filter"] = filter_leg()
+    except Exception as e:  # reported, not hidden
+        res["c3_filter"] = {"error": f"{type(e).__name__}: {e}"}
     for name, mode in OTHER_CONFIGS:
         cfg = CONFIGS[name]
         steps = max(3, min(args.steps, 10))

@@ -155,44 +155,15 @@ __device__ __forceinline__ float2 exp2_sum_pairs(float2 s, const float* x, float
   return s;
 }
 
-// 2^x on the FMA pipe (x <= 0; 0 below -125 and for NaN).  x = n + f, n
-// the nearest integer (adding 1.5 * 2^23 rounds it into the low mantissa
-// bits) and |f| <= 1/2; 2^f by a degree-5 polynomial fitted to 2^f on
-// [-1/2, 1/2] by weighted least squares on the relative error (2.4e-7 at
-// most in fp32 Horner steps, the size of ex2.approx's own error); 2^n is
-// added to the exponent field.
-__device__ __forceinline__ float soft_exp2(float x) {
-  const float xc = fmaxf(x, -125.0f);
-  const float t = xc + 12582912.0f;
-  const float f = xc - (t - 12582912.0f);
-  float p = 0.00132765f;
-  p = fmaf(p, f, 0.00967554f);
-  p = fmaf(p, f, 0.05550713f);
-  p = fmaf(p, f, 0.2402212f);
-  p = fmaf(p, f, 0.69314694f);
-  p = fmaf(p, f, 1.0000001f);
-  const int e = static_cast<int>(static_cast<unsigned>(__float_as_int(t) - 0x4B400000) << 23);
-  return x >= -125.0f ? __int_as_float(__float_as_int(p) + e) : 0.0f;
-}
-
-#ifndef SPEC_SOFT_EXP_MASK
-#define SPEC_SOFT_EXP_MASK 0x00
-#endif
-
 // s + (sum over j of 2^(x_j c.x - mc.x), sum over j of 2^(x_j c.y - mc.y)):
 // one element's terms at two temperatures side by side in a register pair.
-// Two exponentials per element would make the MUFU pipe (16 per clock per
-// SM) the bound of a row stream; the second one of the elements j in
-// SPEC_SOFT_EXP_MASK runs on the FMA pipe instead.
+// (A polynomial 2^x on the FMA pipe for half of the second terms, to relieve
+// the MUFU pipe, measured slower: the row stream is issue-bound.)
 template <int N>
 __device__ __forceinline__ float2 exp2_sum_two(float2 s, const float* x, float2 c, float2 mc) {
   const float2 nmc = make_float2(-mc.x, -mc.y);
 #pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const float2 a = fma2(splat(x[j]), c, nmc);
-    const float e1 = ((SPEC_SOFT_EXP_MASK >> (j & 7)) & 1) ? soft_exp2(a.y) : fast_exp2(a.y);
-    s = add2(s, make_float2(fast_exp2(a.x), e1));
-  }
+  for (int j = 0; j < N; ++j) s = add2(s, exp2_2(fma2(splat(x[j]), c, nmc)));
   return s;
 }
 

@@ -379,13 +379,12 @@ __global__ void plan_t2r_kernel(const int32_t* __restrict__ t2d, int64_t Vd, int
 // sizes) walking rows blockIdx.x, blockIdx.x + gridDim.x, ...; the bitmap
 // is copied into shared memory once.  Per row, when the K intersection
 // logits fit in shared memory:
-//   pass 1   streams the row through a per-thread cp.async ring and copies
-//            every intersection logit to its rank (id order);
-//   pass 1b  the masked online softmax and best element over those K
-//            values alone (no per-element mask, 40% of the elements at
-//            the c4 sizes);
-//   pass 2   streams t2r through the ring and writes q in target order,
-//            each gather a shared-memory read.
+//   pass 1   streams the row through a per-thread cp.async ring, copies
+//            every intersection logit to its rank (id order) and keeps the
+//            masked online softmax and best element of those logits;
+//   pass 2   streams t2r and writes q in target order, each gather a
+//            shared-memory read (logit form: warps 1.. only, while thread 0
+//            writes the top-1 outputs).
 // Otherwise (no q wanted, or more intersection logits than fit) pass 1
 // masks with the bitmap and pass 2 gathers from the row in global memory
 // (L2), t2d streamed through the ring.  Results are those of tli_constrain_kernel.
@@ -394,7 +393,14 @@ __global__ void plan_t2r_kernel(const int32_t* __restrict__ t2d, int64_t Vd, int
 // flight per thread): the row and the t2r stream stay in flight without
 // registers, which the per-element work needs.
 constexpr int kResThreads = 1024;
-constexpr int kResRing = 3;  // 16-byte copies in flight per thread (48 KB of shared memory)
+// 16-byte copies in flight per thread (16 KB of shared memory each): 4 measured
+// slightly faster than 3 per row (the row stream is bound by bytes in flight),
+// and at V_d = 151936 still leaves room for 63952 intersection logits
+constexpr int kResRing = 4;
+// warps left out of the logit-form pass 2: warp 0 writes the row's top-1
+// outputs meanwhile (global loads and stores, about 3 us), so that latency no
+// longer holds up the row's end (row span of a c4 launch 54 -> 47 us)
+constexpr int kP2Skip = 1;
 // 16-byte loads of the rank table in flight per thread in the logit-form
 // pass 2 (register loads: the shared-memory port is busy with the gathers)
 constexpr int kP2Unroll = 4;
@@ -402,8 +408,8 @@ constexpr int kP2Unroll = 4;
 // f(v, i) for the n 16-byte items src[i], each thread taking i = tid + j
 // THREADS in increasing j, U loads in flight per thread.
 template <int THREADS, int U, class F>
-__device__ __forceinline__ void direct_stream(const uint4* __restrict__ src, int n, F&& f) {
-  int i = threadIdx.x;
+__device__ __forceinline__ void direct_stream(const uint4* __restrict__ src, int n, F&& f, int tid) {
+  int i = tid;
   for (; i + (U - 1) * THREADS < n; i += U * THREADS) {
     uint4 v[U];
 #pragma unroll
@@ -427,56 +433,17 @@ __device__ __forceinline__ int rank_before(const uint2* mw, int id) {
   const uint2 e = mw[id >> 5];
   return static_cast<int>(e.y) + __popc(e.x & ((1u << (id & 31)) - 1u));
 }
-// The intersection id of rank k (0 <= k < K): the last word whose count of
-// earlier set bits is <= k holds it.
-__device__ int id_of_rank(const uint2* mw, int W, int k) {
-  int lo = 0, hi = W - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int>(mw[mid].y) <= k) lo = mid; else hi = mid - 1;
-  }
-  int n = k - static_cast<int>(mw[lo].y);
-  const uint32_t x = mw[lo].x;
-  for (int j = 0; j < 32; ++j)
-    if ((x >> j) & 1u) {
-      if (n == 0) return 32 * lo + j;
-      --n;
-    }
-  return -1;  // not reached for k < K
-}
-
-// Pass 1 (compacting): every intersection logit of the row to cpt[rank].
+// Pass 1 (compacting) with the row's statistics: every intersection logit
+// of the row to cpt[rank] (id order) and, over the same logits, the masked
+// online softmax and best element (value desc, id asc) of the thread's
+// elements in increasing index order (NaN as -inf).  The stream is bound by
+// the bytes in flight, so the statistics ride along instead of taking a
+// pass over the compacted logits of their own (4.8 us per c4 row).
 template <int DT>
-struct CompactWriter {
+struct CompactStatWriter {
   const uint2* mw;
   typename Elem<DT>::T* cpt;
   int K;  // entries of cpt (the debug build's bounds)
-  __device__ __forceinline__ void visit1(float x, int64_t idx, bool) {
-    const int id = static_cast<int>(idx);
-    if (((mw[id >> 5].x >> (id & 31)) & 1u) && spec_in(rank_before(mw, id), K, nullptr))
-      cpt[rank_before(mw, id)] = Elem<DT>::of_value(x);
-  }
-  __device__ __forceinline__ void visit_vec(const uint4& raw, int first) {
-    constexpr int kv = Logit<DT>::kVec;
-    const int w = first >> 5, sh = first & 31;
-    const uint2 e = mw[w];
-    uint32_t b = e.x >> sh;
-    if (sh > 32 - kv) b |= mw[w + 1].x << (32 - sh);  // the vector crosses into word w + 1
-    b &= (1u << kv) - 1u;
-    if (b == 0u) return;
-    int r = static_cast<int>(e.y) + __popc(e.x & ((1u << sh) - 1u));
-#pragma unroll
-    for (int j = 0; j < kv; ++j)
-      if (((b >> j) & 1u) && spec_in(r, K, nullptr)) cpt[r++] = Elem<DT>::at(raw, j);
-  }
-};
-
-// Pass 1b: online softmax partials and best element (value desc, index
-// asc) of a thread's elements in increasing index order; NaN is skipped by
-// the max and poisons the sum (the caller then recomputes the sum with NaN
-// as -inf).
-template <int DT>
-struct StatVisitor {
   float c, m, mc, s0, s1;
   int bi;
   __device__ __forceinline__ void rescale(float nm) {
@@ -490,22 +457,37 @@ struct StatVisitor {
     m = nm;
     mc = nm * c;
   }
-  __device__ __forceinline__ void visit1(float x, int idx) {
-    if (x > m) {
-      rescale(x);
-      bi = idx;
+  __device__ __forceinline__ void visit1(float x, int64_t idx, bool) {
+    const int id = static_cast<int>(idx);
+    if (!((mw[id >> 5].x >> (id & 31)) & 1u)) return;
+    const int r = rank_before(mw, id);
+    if (spec_in(r, K, nullptr)) cpt[r] = Elem<DT>::of_value(x);
+    const float xk = order_key(x);
+    if (xk > m) {
+      rescale(xk);
+      bi = id;
     }
-    if (m != neg_inf()) s0 += fast_exp2(fmaf(x, c, -mc));
+    if (m != neg_inf()) s0 += fast_exp2(fmaf(xk, c, -mc));
   }
   __device__ __forceinline__ void visit_vec(const uint4& raw, int first) {
     constexpr int kv = Logit<DT>::kVec;
+    const int w = first >> 5, sh = first & 31;
+    const uint2 e = mw[w];
+    uint32_t b = e.x >> sh;
+    if (sh > 32 - kv) b |= mw[w + 1].x << (32 - sh);  // the vector crosses into word w + 1
+    b &= (1u << kv) - 1u;
+    if (b == 0u) return;
+    int r = static_cast<int>(e.y) + __popc(e.x & ((1u << sh) - 1u));
+#pragma unroll
+    for (int j = 0; j < kv; ++j)
+      if (((b >> j) & 1u) && spec_in(r, K, nullptr)) cpt[r++] = Elem<DT>::at(raw, j);
     float x[kv];
     unpack<DT>(raw, x);
-    float vmax;
-    if (DT == SPEC_BF16) {
-      vmax = max8_bf16(raw);
-    } else {
-      vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[kv - 1]));
+    float vmax = neg_inf();
+#pragma unroll
+    for (int j = 0; j < kv; ++j) {
+      x[j] = ((b >> j) & 1u) ? order_key(x[j]) : neg_inf();
+      vmax = fmaxf(vmax, x[j]);
     }
     if (vmax > m) {
       int j0 = 0;
@@ -605,14 +587,12 @@ __global__ void __launch_bounds__(kResThreads, 1)
   pdl_enter();
   using E = typename Elem<DT>::T;
   constexpr int esz = DT == SPEC_BF16 ? 2 : 4;
-  constexpr int kv = Logit<DT>::kVec;
   constexpr int kWarps = kResThreads / 32;
   extern __shared__ __align__(16) unsigned char res_dsm[];
   __shared__ float wm[kWarps], ws[kWarps], wv[kWarps];
   __shared__ int wi[kWarps];
   __shared__ float s_m, s_s, s_bv;
   __shared__ int s_bi;
-  const int W = static_cast<int>((Vd + 31) / 32);
   const int Wp = static_cast<int>(plan_words(Vd));
   const PlanView pv = plan_view(const_cast<void*>(plan), Vd);
   uint4* ring = reinterpret_cast<uint4*>(res_dsm);  // kResRing slots per thread
@@ -661,43 +641,22 @@ __global__ void __launch_bounds__(kResThreads, 1)
   for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
     const void* row = static_cast<const char*>(draft) + r * Vd * esz;
     if (cpt != nullptr) {
-      CompactWriter<DT> cw{mw, cpt, K};
+      CompactStatWriter<DT> cw{mw, cpt, K, c, neg_inf(), 0.0f, 0.0f, 0.0f, INT_MAX};
       ring_row<DT>(row, Vd, ring, cw);
-      __syncthreads();  // the K intersection logits, in id order
-      StatVisitor<DT> st{c, neg_inf(), 0.0f, 0.0f, 0.0f, INT_MAX};
-      const int nvk = K / kv;
-      const uint4* cv = reinterpret_cast<const uint4*>(cpt);
-      for (int i = tid; i < nvk; i += kResThreads) st.visit_vec(cv[i], i * kv);
-      for (int k = nvk * kv + tid; k < K; k += kResThreads) st.visit1(Elem<DT>::value(cpt[k]), k);
-      merge(st.m, st.s0 + st.s1, st.m, st.bi);
-      if (isfinite(s_m) && !isfinite(s_s)) {
-        // a NaN among the intersection logits: the sum again with NaN as -inf
-        const float mc = s_m * c;
-        float part = 0.0f;
-        for (int k = tid; k < K; k += kResThreads) part += fast_exp2(fmaf(order_key(Elem<DT>::value(cpt[k])), c, -mc));
-        part = warp_sum(part);
-        if (lane == 0) ws[warp] = part;
-        __syncthreads();
-        if (tid == 0) {
-          float tot = 0.0f;
-          for (int w2 = 0; w2 < kWarps; ++w2) tot += ws[w2];
-          s_s = tot;
-        }
-        __syncthreads();
-      }
+      // (the merge's barriers also complete the compacted logits)
+      merge(cw.m, cw.s0 + cw.s1, cw.m, cw.bi);
     } else {
       BitmapMaskedVisitor<DT> st{mw, c, neg_inf(), 0.0f, 0.0f, 0.0f, INT_MAX};
       ring_row<DT>(row, Vd, ring, st);
       merge(st.m, st.s0 + st.s1, st.m, st.bi);
     }
-    // the row's statistics for every thread; s_bi is a rank (compacted)
-    // or an id
+    // the row's statistics for every thread; s_bi is the best draft id
     const bool ok = s_bi != INT_MAX && isfinite(s_bv);
     const float mc = s_m * c, invz = 1.0f / s_s;
     if (tid == 0) {
       // the top-1 outputs (thread 0 alone; the other warps go on) and the
       // step's pool expansion for this row's request (a chain: one row each)
-      const int best = ok ? (cpt != nullptr ? id_of_rank(mw, W, s_bi) : s_bi) : -1;
+      const int best = ok ? s_bi : -1;
       const int32_t tgt = ok && spec_in(best, Vd, stats) ? __ldg(d2t + best) : -1;
       const float pr = ok ? fminf(fast_exp2(fmaf(s_bv, c, -mc)) * invz, 1.0f) : 0.0f;
       top1_draft[r] = best;
@@ -792,7 +751,10 @@ __global__ void __launch_bounds__(kResThreads, 1)
         };
         auto l_of = [&](int32_t k) -> E { return k < -1 ? far(k) : near(k); };
         const int nl = vl ? static_cast<int>(Vt / 4) : 0;
-        direct_stream<kResThreads, kP2Unroll>(reinterpret_cast<const uint4*>(t2r), nl, [&](const uint4& kk, int i) {
+        constexpr int kP2T = kResThreads - 32 * kP2Skip;
+        const int p2 = tid - 32 * kP2Skip;
+        if (p2 >= 0) {
+        direct_stream<kP2T, kP2Unroll>(reinterpret_cast<const uint4*>(t2r), nl, [&](const uint4& kk, int i) {
           const int32_t k0 = static_cast<int32_t>(kk.x), k1 = static_cast<int32_t>(kk.y);
           const int32_t k2 = static_cast<int32_t>(kk.z), k3 = static_cast<int32_t>(kk.w);
           E e0 = near(k0), e1 = near(k1), e2 = near(k2), e3 = near(k3);
@@ -803,8 +765,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
             if (k3 < -1) e3 = far(k3);
           }
           st_stream4(lo + 4 * i, e0, e1, e2, e3);
-        });
-        for (int64_t t = static_cast<int64_t>(nl) * 4 + tid; t < Vt; t += kResThreads) lo[t] = l_of(__ldg(t2r + t));
+        }, p2);
+        for (int64_t t = static_cast<int64_t>(nl) * 4 + p2; t < Vt; t += kP2T) lo[t] = l_of(__ldg(t2r + t));
+        }
       } else {
         auto l_of = [&](int32_t d) -> E {
           return (d >= 0 && d < Vd) ? Elem<DT>::of_value(Logit<DT>::load1(row, d)) : ninf;

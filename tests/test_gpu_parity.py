@@ -1323,7 +1323,10 @@ def test_pruned_head_full_size_sampled_rows():
 
 # ------------------------------------------------- target-side filtering
 
-FILTERS = [(1, 1.0), (5, 1.0), (0, 0.9), (20, 0.8), (0, 0.0), (3, 0.5), (0, 0.3)]
+# top_k up to 512 takes the kernel's sorted-candidates path (unless ties
+# overflow it), up to 4096 the radix top-k with sorted top-p, beyond that
+# the radix top-k and top-p
+FILTERS = [(1, 1.0), (5, 1.0), (0, 0.9), (20, 0.8), (0, 0.0), (3, 0.5), (0, 0.3), (600, 0.95), (5000, 0.9)]
 
 
 @pytest.mark.parametrize("V,dtype", [(257, torch.float32), (4097, torch.bfloat16), (32000, torch.bfloat16),
