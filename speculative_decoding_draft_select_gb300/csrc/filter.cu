@@ -467,13 +467,24 @@ __global__ void __launch_bounds__(kFT, 2) filter_kernel(void* __restrict__ logit
       // a lower bound of the top-k cut: the top_k-th largest of the
       // threads' maxima (top_k threads each hold an element at least as
       // large); every element at or above it is a candidate, sorted exactly
-      int rk = 0;
-      for (int u = 0; u < kFT; ++u) {
-        const float o = sh.tmax[u];
-        rk += (o > mv.m || (o == mv.m && u < tid)) ? 1 : 0;
+      // (the maxima sorted in descending order by a bitonic network)
+      for (int size = 2; size <= kFT; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const int j = tid ^ stride;
+          if (j > tid) {
+            const float a = sh.tmax[tid], b = sh.tmax[j];
+            if ((b > a) == ((tid & size) == 0)) {
+              sh.tmax[tid] = b;
+              sh.tmax[j] = a;
+            }
+          }
+          __syncthreads();
+        }
       }
-      if (rk == top_k - 1) s_tau = FKey<DT>::of(mv.m);
-      if (tid == 0) s_nc = 0;
+      if (tid == 0) {
+        s_tau = FKey<DT>::of(sh.tmax[top_k - 1]);
+        s_nc = 0;
+      }
       __syncthreads();
       GatherV<DT, true> gv{&sh, &s_nc, s_tau, 0, c, mc};
       for_row_fast<DT, 4>(row, V, gv, tid, kFT);

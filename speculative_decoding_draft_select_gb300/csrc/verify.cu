@@ -789,7 +789,7 @@ int launch_sample_verify_t(int B, int N, int64_t V, const void* target, float c,
     launch_verify<DT, QSrc, 4, WOR>(cap4, smem4, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
                                budget, eos, committed, num_committed, accept_length, accept_path, next_root,
                                walk_info, stats, w);
-  else if (cap2 >= B)
+  else if (cap2 >= 1)  // pairs also when they take several requests each (B=1024 x 16: 708 vs 730 us alone)
     launch_verify<DT, QSrc, 2, WOR>(cap2, smem2, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
                                budget, eos, committed, num_committed, accept_length, accept_path, next_root,
                                walk_info, stats, w);
