@@ -259,8 +259,8 @@ int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_t* stats_or
 int spec_debug_bounds(int64_t* count, int reset);
 
 /* Scratch bytes for spec_verify_greedy / spec_verify_sample (per-row
- * max, normaliser and argmax of the target logits, and the chain verify's
- * per-request state). */
+ * max, normaliser, argmax or ready flag and claim of the target logits, and
+ * the chain verify's per-request state). */
 size_t spec_verify_ws_size(int B, int N);
 
 /* Greedy verify ([ZS] 4.1 greedy_commit, generalised to trees).  One pass

@@ -191,18 +191,18 @@ struct FrozenWeights {
 // in node-major order (every request's root first, then node 1, ...; a
 // child always has a larger node index than its parent, so the rows a walk
 // reaches come in the order it reaches them) and requests.  A cluster walks
-// one request at a time; on entering a node whose row is not done yet,
-// each CTA of the cluster computes queued rows itself until it is (a
-// waiting CTA always has work or waits on a row another running CTA is
-// computing, which never waits, so the launch cannot deadlock; the wait is
-// bounded all the same).  Clusters without a request left compute the
+// one request at a time; on entering a node whose row is not done yet, one
+// CTA of the cluster claims and computes that row itself if no CTA has, and
+// the others compute queued rows until it is done (a waiting CTA always has
+// work or waits on a row another running CTA is computing, which never
+// waits, so the launch cannot deadlock; the wait is bounded all the same).  Clusters without a request left compute the
 // remaining rows.  A row's statistics are published with a release store
 // of its flag and read after an acquire load of it.
 template <int DT, class QSrc, int C, bool WOR>
 __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     sample_verify_kernel(int B, int N, int64_t V, float c, const void* __restrict__ target,
                        float* __restrict__ m_row, float* __restrict__ z_row, int32_t* __restrict__ ready,
-                       int32_t* __restrict__ queues, QSrc qsrc,
+                       int32_t* __restrict__ queues, int32_t* __restrict__ claim, QSrc qsrc,
                        const int32_t* __restrict__ q_row, const int32_t* __restrict__ dtok,
                        const int32_t* __restrict__ ntok, const int32_t* __restrict__ nsib,
                        const float* __restrict__ coins, const float* __restrict__ u_final,
@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
     return s_wsum;
   };
   // queued row i (node-major): its max and normaliser, then its flag
-  auto stats_row = [&](int64_t i) {
-    const int64_t r = (i % B) * N + i / B;
+  // row r: its max and normaliser, then its flag (the caller holds its claim)
+  auto stats_row = [&](int64_t r) {
     const void* row = static_cast<const char*>(target) + r * V * esz;
     RowStatVisitor<DT, true> v{c, neg_inf(), 0.0f, 0.0f, INT_MAX, 0.0f};
     {
@@ -342,18 +342,32 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
   // empty, waits for the CTA computing it).  Taking other rows while row r
   // is in flight keeps the HBM stream going; measured at the c3 sizes it
   // beats waiting idle for r.
+  // Rows are claimed (an exchange on claim[r]) by the CTA that computes
+  // them: queued rows in node-major order, or a row a walk needs, claimed
+  // by one of the walking CTAs out of order so that the walk does not wait
+  // for the queue to reach it (the others take queued rows meanwhile).
+  // A claimed row is always being computed, so a wait on it ends.
   auto wait_row = [&](int64_t r) {
     for (;;) {
       if (tid == 0) {
         s_flag = ld_acquire_gpu(ready + r);
-        s_item = s_flag ? 0 : atomicAdd(next_row, 1);
+        if (s_flag) {
+          s_item = 0;
+        } else if (atomicExch(claim + r, 1) == 0) {
+          s_item = -1;  // this CTA computes row r now
+        } else {
+          const int64_t i = atomicAdd(next_row, 1);
+          const int64_t ri = (i % B) * N + i / B;
+          s_item = i >= rows ? rows : (atomicExch(claim + ri, 1) == 0 ? ri : -2);
+        }
       }
       __syncthreads();
       if (s_flag) break;
       const int64_t item = s_item;
       __syncthreads();
+      if (item == -2) continue;  // that queued row was claimed by a walk
       if (item < rows) {
-        stats_row(item);
+        stats_row(item < 0 ? r : item);
         continue;
       }
       // every row is taken: row r is in flight on a running CTA
@@ -582,12 +596,16 @@ __global__ void __launch_bounds__(kWalkThreads, 512 / kWalkThreads)
   }
   // no request left: the remaining rows
   for (;;) {
-    if (tid == 0) s_item = atomicAdd(next_row, 1);
+    if (tid == 0) {
+      const int64_t i = atomicAdd(next_row, 1);
+      const int64_t ri = (i % B) * N + i / B;
+      s_item = i >= rows ? rows : (atomicExch(claim + ri, 1) == 0 ? ri : -2);
+    }
     __syncthreads();
     const int64_t item = s_item;
     __syncthreads();
     if (item >= rows) break;
-    stats_row(item);
+    if (item >= 0) stats_row(item);
   }
   if (C > 1) cluster_barrier();  // no CTA leaves while another may store into it
 }
@@ -608,7 +626,7 @@ VerifyWs carve(void* ws, int B, int N) {
   VerifyWs w;
   w.amax = reinterpret_cast<int32_t*>(p);
   w.ready = w.amax;
-  p += align256((rows + 2) * sizeof(int32_t));
+  p += align256((2 * rows + 2) * sizeof(int32_t));  // flags, the two queue counters, row claims
   w.m = reinterpret_cast<float*>(p);
   p += align256(rows * sizeof(float));
   w.z = reinterpret_cast<float*>(p);
@@ -679,7 +697,7 @@ extern "C" int spec_wait_probe(const int32_t* flag, int64_t limit_cycles, int32_
 extern "C" size_t spec_verify_ws_size(int B, int N) {
   if (B < 0 || N < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * N;
-  return align256((rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float)) + chain_ws_bytes(B, N);
+  return align256((2 * rows + 2) * sizeof(int32_t)) + 2 * align256(rows * sizeof(float)) + chain_ws_bytes(B, N);
 }
 
 extern "C" int spec_verify_greedy(int B, int N, int64_t V, int dtype, const void* target_logits,
@@ -762,7 +780,7 @@ void launch_verify(int64_t clusters, size_t smem, cudaStream_t s, int B, int N, 
                    int32_t* next_root, int32_t* walk_info, int32_t* stats, const VerifyWs& w) {
   const int64_t rows = static_cast<int64_t>(B) * N;
   launch_kc(sample_verify_kernel<DT, QSrc, C, WOR>, static_cast<unsigned>(clusters * C), kWalkThreads, smem, s, C, B,
-            N, V, c, target, w.m, w.z, w.ready, w.ready + rows, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
+            N, V, c, target, w.m, w.z, w.ready, w.ready + rows, w.ready + rows + 2, qsrc, q_row, dtok, ntok, nsib, coins, u_final, budget,
             eos, committed, num_committed, accept_length, accept_path, next_root, walk_info, stats);
 }
 
@@ -783,7 +801,7 @@ int launch_sample_verify_t(int B, int N, int64_t V, const void* target, float c,
   const int64_t cap4 = walk_capacity<DT, QSrc, 4, WOR>(smem4), cap2 = walk_capacity<DT, QSrc, 2, WOR>(smem2),
                 cap1 = walk_capacity<DT, QSrc, 1, WOR>(smem1);
   if (cap1 < 1) return SPEC_ERR_CUDA;
-  if (cudaMemsetAsync(w.ready, 0, sizeof(int32_t) * static_cast<size_t>(rows + 2), s) != cudaSuccess)
+  if (cudaMemsetAsync(w.ready, 0, sizeof(int32_t) * static_cast<size_t>(2 * rows + 2), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (cap4 >= B)
     launch_verify<DT, QSrc, 4, WOR>(cap4, smem4, s, B, N, V, target, c, qsrc, q_row, dtok, ntok, nsib, coins, u_final,
