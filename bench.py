@@ -97,12 +97,30 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+# The sources each profiled kernel is built from (its file and the headers
+# it includes); a committed ncu summary counts only while their hash matches.
+KERNEL_SOURCES = {
+    "softmax_topk_kernel": ["draft.cu", "common.cuh", "cdf.cuh", "expand.cuh"],
+    "softmax_sample_kernel": ["draft.cu", "common.cuh", "cdf.cuh", "expand.cuh"],
+    "sample_verify_kernel": ["verify.cu", "walk.cuh", "cdf.cuh", "common.cuh", "chain.h"],
+    "row_argmax_kernel": ["verify.cu", "walk.cuh", "cdf.cuh", "common.cuh", "chain.h"],
+    "tli_planned_kernel": ["tli.cu", "common.cuh", "expand.cuh"],
+    "pruned_head_kernel": ["head.cu", "common.cuh"],
+    "filter_kernel": ["filter.cu", "common.cuh"],
+}
+
+
+def kernel_source_hash(kernel=None):
+    """Hash of the sources of `kernel` (every source without one) and of the
+    C ABI header."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_draft_select_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    files = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(d))
+    for f in sorted(files):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
+    with open(os.path.join(ROOT, "include", "specdec.h"), "rb") as fh:
+        h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -117,7 +135,7 @@ def ncu_traffic(kernel, workload):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("source_sha256") != kernel_source_hash():
+    if vals.get("source_sha256") != kernel_source_hash(kernel):
         return None
     try:
         return float(vals["traffic_bytes_per_launch"])
@@ -686,7 +704,8 @@ def pruned_head_leg(M=256, H=896, K=60000, Vd=151936, Vt=128256, launches=20):
     res.update({"workload": f"pruned draft LM head M={M} H={H} K={K} bf16, tcgen05 GEMM + fused top-1 and softmax "
                             f"statistics (2 launches: GEMM with epilogue, partial merge)",
                 "flops_per_launch": 2 * M * K * H, "bytes_per_launch": (K * H + M * H) * 2,
-                "tensor_peak_tflops": tensor_peak()[0], "tensor_peak_source": tensor_peak()[1]})
+                "tensor_peak_tflops": tensor_peak()[0], "tensor_peak_source": tensor_peak()[1],
+                "traffic": ncu_traffic("pruned_head_kernel", "c4")})
     return res
 
 
@@ -723,7 +742,8 @@ def filter_leg(B=128, N=64, V=128256, T=0.7, top_k=50, top_p=0.9, launches=10):
     return {"workload": f"target-side filtering of the c3 target logits: {B * N} rows x V={V} bf16 in place, "
                         f"T={T}, top_k={top_k}, top_p={top_p}",
             "us": round(us, 2), "bytes_per_launch": byts, "dropped_per_row": round(dropped / (B * N), 1),
-            "gbs": round(gbs, 1), "hbm_frac": round(gbs / hpk, 4), "peak_source": hsrc}
+            "gbs": round(gbs, 1), "hbm_frac": round(gbs / hpk, 4), "peak_source": hsrc,
+            "traffic": ncu_traffic("filter_kernel", "c3") if B * N == 8192 else None}
 
 
 def other_configs(args):
