@@ -23,6 +23,7 @@ import subprocess
 import sys
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -379,6 +380,21 @@ def run_ours(args, cfg, mode, rank, world, steps=None, warmup=None, flush=False,
         v_gbs = v_bytes / (v_ms * 1e-3) / 1e9
         verify = {"us_per_step": round(v_ms * 1e3, 2), "logit_bytes": int(v_bytes), "achieved": round(v_gbs, 1),
                   "peak": peak, "unit": "GB/s", "frac": round(v_gbs / peak, 4)}
+        if mode == "sample":
+            # the walks' own bytes, from the walk records of the last step (every
+            # step walks the same trees): one residual pass over a target row and
+            # a q row per rejected child, one pass over the target row per bonus
+            # draw at a leaf (a correction reuses its last pass)
+            wi = buf.verify_out["walk_info"].cpu().numpy()
+            s_t = 2 if cfg.dtype == torch.bfloat16 else 4
+            s_q = 4 if q_mode == "probs" else s_t
+            Vt = cfg.V_t or cfg.V
+            rej = int(wi[:, 1].astype(np.int64).sum())
+            bonus = int((wi[:, 2] == 2).sum())
+            walk_bytes = rej * Vt * (s_t + s_q) + bonus * Vt * s_t
+            w_gbs = (v_bytes + walk_bytes) / (v_ms * 1e-3) / 1e9
+            verify.update({"residual_passes": rej, "bonus_draws": bonus, "walk_bytes": int(walk_bytes),
+                           "achieved_with_walks": round(w_gbs, 1), "frac_with_walks": round(w_gbs / peak, 4)})
         vname = "sample_verify_kernel" if mode == "sample" else "row_argmax_kernel"
         verify_roof = {"bound": "hbm", "kernel": vname if mode == "sample" else vname + " (+ greedy_walk_kernel)",
                        "achieved": round(v_gbs, 1), "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
@@ -643,8 +659,9 @@ def summarize(line):
     v, d = line["verify"], line["rooflines"]["draft"]
     out = {"workload": line["config"]["workload"], "tokens_per_s": line["value"], "ms_per_step": line["ms_per_step"],
            "steps": line["steps"], "mean_accept_length": line["mean_accept_length"],
-           "verify": None if v is None else {"us": v["us_per_step"], "gbs": v["achieved"], "frac": v["frac"],
-                                              "logit_bytes": v["logit_bytes"]},
+           "verify": None if v is None else dict({"us": v["us_per_step"], "gbs": v["achieved"], "frac": v["frac"],
+                                                   "logit_bytes": v["logit_bytes"]},
+                                                  **{k: v[k] for k in ("walk_bytes", "frac_with_walks") if k in v}),
            "draft": None if d is None else {"kernel": d["kernel"], "avg_launch_us": d["avg_launch_us"],
                                              "launches_per_step": d["launches_per_step"], "gbs": d["achieved"],
                                              "frac": d["frac"]},
