@@ -112,16 +112,13 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel=None):
-    """Hash of the sources of `kernel` (every source without one) and of the
-    C ABI header."""
+    """Hash of the sources of `kernel` (every source without one)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_draft_select_gb300", "csrc")
     files = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(d))
     for f in sorted(files):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
-    with open(os.path.join(ROOT, "include", "specdec.h"), "rb") as fh:
-        h.update(fh.read())
     return h.hexdigest()[:16]
 
 

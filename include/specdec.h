@@ -224,7 +224,11 @@ int spec_softmax_sample_expand(const void* logits, int dtype, int64_t R, int64_t
  *   retrieve_next_token   first child of n, -1 if none
  *   retrieve_next_sibling next node with the same parent, -1 if none
  *   q_row                 draft-row table row of n's draft distribution, -1
- * 1 <= N <= min(P, SPEC_MAX_NODES), P <= SPEC_MAX_POOL. */
+ * 1 <= N <= min(P, SPEC_MAX_NODES), P <= SPEC_MAX_POOL.
+ * A selected candidate whose pool parent is out of range, not a selected
+ * candidate, or not an earlier node (a pool that is not a tree) is detached:
+ * parent -1, its mask row and depth from its own chain, and no link from the
+ * root reaches it or its subtree, so the verify never visits them. */
 int spec_build_tree(int B, int k, int num_steps, int N, const float* pool_score,
                     const int32_t* pool_token, const int32_t* pool_parent,
                     const int32_t* pool_qrow, const int32_t* root_token, const int32_t* seq_lens,

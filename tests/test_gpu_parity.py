@@ -289,6 +289,90 @@ def test_tree_parity(B, k, steps, N, ties):
         np.testing.assert_array_equal(gt[name].cpu().numpy(), ot[name], err_msg=name)
 
 
+def test_tree_build_detaches_invalid_parents():
+    """Pool parents that are not a tree (out of range, negative, a candidate
+    outside the selection, the node itself, a later node) must not derail
+    the build: the selection (tokens, draft rows) is the oracle's, every
+    valid parent is the oracle's, and a node with an invalid parent is
+    detached (parent -1, a mask row and depth of its own chain), so that no
+    link from the root reaches it."""
+    B, k, steps, N = 6, 4, 4, 16
+    rng = np.random.default_rng(777)
+    inputs = oracle_topk_inputs(rng, B, k, steps, False)
+    opool = oracle.Pool(B, k, steps)
+    for s, (p, idx) in enumerate(inputs):
+        oracle.tree_expand(opool, s, p, idx)
+    root = rng.integers(0, 1000, B).astype(np.int32)
+    seq = rng.integers(16, 2048, B).astype(np.int32)
+    ot = oracle.build_tree(opool, N, root, seq)
+    P = opool.score.shape[1]
+    # the pool ids of the selected nodes (node n >= 1), from the oracle's tree
+    bad = opool.parent.copy()
+    planted = {}
+    for b in range(B):
+        # selected candidates: nodes 1..N-1 in ascending pool-id order
+        order = np.argsort(-opool.score[b, 1:], kind="stable")[: N - 1] + 1
+        sel = np.sort(order)
+        unselected = np.setdiff1d(np.arange(1, P), sel)
+        picks = rng.choice(np.arange(1, N - 1), size=5, replace=False)  # node N-1 is "later" than each
+        for n, kind in zip(picks, ("range", "negative", "unselected", "self", "later")):
+            pid = sel[n - 1]
+            if kind == "range":
+                bad[b, pid] = P + 3
+            elif kind == "negative":
+                bad[b, pid] = -5
+            elif kind == "unselected":
+                bad[b, pid] = unselected[0]
+            elif kind == "self":
+                bad[b, pid] = pid
+            else:
+                bad[b, pid] = sel[-1]
+            planted[(b, int(n))] = kind
+    gpool = sd.new_pool(B, k, steps)
+    for name, arr in (("score", opool.score), ("token", opool.token), ("parent", bad), ("qrow", opool.qrow)):
+        gpool[name].copy_(torch.from_numpy(np.ascontiguousarray(arr)))
+    gt = sd.spec_build_tree(gpool, N, dev(root), dev(seq))
+    torch.cuda.synchronize()
+    g = {name: t.cpu().numpy() for name, t in gt.items()}
+    for name in ("draft_token", "q_row", "retrieve_index"):
+        np.testing.assert_array_equal(g[name], ot[name], err_msg=name)
+    for b in range(B):
+        par = g["parent"][b]
+        assert par[0] == -1
+        for n in range(1, N):
+            if (b, n) in planted:
+                assert par[n] == -1, (b, n, planted[(b, n)])
+            else:
+                assert par[n] == ot["parent"][b, n], (b, n)
+            # the node's chain, depth and mask row from the kernel's own parents
+            chain, a = [], n
+            while a >= 0:
+                chain.append(a)
+                a = par[a]
+            assert g["positions"][b, n] == seq[b] + (len(chain) - 1 if chain[-1] == 0 else len(chain))
+            row = np.zeros(N, np.uint8)
+            row[chain] = 1
+            np.testing.assert_array_equal(g["tree_mask"][b, n], row)
+        # the nodes the root's links reach: exactly those whose chain ends at the root
+        seen, stack = set(), [0]
+        while stack:
+            a = stack.pop()
+            seen.add(a)
+            c = g["retrieve_next_token"][b, a]
+            while c > 0:
+                stack.append(c)
+                c = g["retrieve_next_sibling"][b, c]
+        reach = set()
+        for n in range(N):
+            a = n
+            while a > 0:
+                a = par[a]
+            if a == 0:
+                reach.add(n)
+        assert seen == reach
+        assert not any((b, n) in planted for n in seen)
+
+
 # ------------------------------------------------------------------ verify
 
 def verify_compare(g, o, b_g, b_o=0, mode="greedy"):
