@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kCT, 4) chain_verify_kernel(const ChainParams 
   __shared__ float tile_sh[kMaxChunkTiles];  // tile sums of one chunk
   __shared__ float ctot_sh[kMaxChunks];
   __shared__ float scan_sh[33];
-  __shared__ float s_tot, s_A;
+  __shared__ float s_A;
   __shared__ int s_what, s_item, s_last, s_tok, s_b, s_n, s_here;
   const ChainIO& io = p.io;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
