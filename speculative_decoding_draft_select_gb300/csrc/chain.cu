@@ -36,6 +36,11 @@ namespace {
 constexpr int kCT = kWalkThreads;  // threads of a CTA
 constexpr int kCE = kWalkElems;    // consecutive elements per thread in a tile
 constexpr int kTile = kCT * kCE;
+// Tuning knobs (compile-time; the defaults are the fastest of the settings
+// measured at B=256 x 5 and B=1024 x 16 nodes): copy-ring depth, pieces per
+// row, CTAs per SM, and draws started in place by the CTA that finishes a
+// request's rows (1: 833 against 798 us at B=1024 x 16, 134 against 128 us
+// at B=256 x 5).
 #ifndef SPEC_CHAIN_RING
 #define SPEC_CHAIN_RING 16
 #endif
@@ -46,7 +51,7 @@ constexpr int kTile = kCT * kCE;
 #define SPEC_CHAIN_CTAS_PER_SM 5
 #endif
 #ifndef SPEC_CHAIN_HERE
-#define SPEC_CHAIN_HERE 0  // draws in place measured slower at B=1024 x 16 (798 vs 833 us) and at B=256 x 5
+#define SPEC_CHAIN_HERE 0
 #endif
 constexpr int kRingItems = SPEC_CHAIN_RING;  // 16-byte copies in flight per thread (row statistics)
 // pieces a row's statistics are cut into (each a work item; the CTA that
