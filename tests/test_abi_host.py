@@ -80,6 +80,27 @@ def test_host_side_argument_checks_null_pointers(lib):
                                          null) == 0
     assert lib.tli_constrain_map_qlogits(0, 10, 10, null, 1, null, null, null, 1.0, null, null, null, null, null,
                                          null, null, null) == 0
+    # filtering: negative rows, V < 1, T <= 0, NaN top_p, bad dtype; nothing to filter; null logits
+    assert lib.spec_filter_logits(null, 1, -1, 8, 1.0, 2, 0.5, null, null) == -1
+    assert lib.spec_filter_logits(null, 1, 4, 0, 1.0, 2, 0.5, null, null) == -1
+    assert lib.spec_filter_logits(null, 1, 4, 8, 0.0, 2, 0.5, null, null) == -1
+    assert lib.spec_filter_logits(null, 1, 4, 8, 1.0, 2, float("nan"), null, null) == -1
+    assert lib.spec_filter_logits(null, 7, 4, 8, 1.0, 2, 0.5, null, null) == -2
+    assert lib.spec_filter_logits(null, 1, 4, 8, 1.0, 0, 1.0, null, null) == 0   # top_k off, top_p 1: no work
+    assert lib.spec_filter_logits(null, 1, 4, 8, 1.0, 8, 1.0, null, null) == 0   # top_k >= V: no work
+    assert lib.spec_filter_logits(null, 1, 4, 8, 1.0, 2, 1.0, null, null) == -1  # work, but no logits
+    # pruned head: bad sizes and temperature, empty batch, null pointers
+    ph = lambda M, H, K, Vd, T: lib.tli_pruned_head(M, H, K, null, null, null, null, Vd, T, *([null] * 8), 0, null)
+    assert ph(-1, 64, 8, 16, 1.0) == -1
+    assert ph(4, 0, 8, 16, 1.0) == -1
+    assert ph(4, 64, 0, 16, 1.0) == -1
+    assert ph(4, 64, 8, 0, 1.0) == -1
+    assert ph(4, 64, 8, 16, 0.0) == -1
+    assert ph(0, 64, 8, 16, 1.0) == 0
+    assert ph(4, 64, 8, 16, 1.0) == -1
+    # the mapped stochastic verify needs its map
+    assert lib.spec_verify_sample_qlogits_mapped(2, 4, 10, 1, null, 1.0, null, 1, null, 1.0, *([null] * 7), -1,
+                                                 *([null] * 8), 0, 0, null, null) == -1
 
 
 def _cuda_present():
